@@ -1,0 +1,244 @@
+"""Pins of the oracle's format codecs against things other than the oracle:
+torch's float8 / bfloat16 decoders, exact rational arithmetic, hand-worked
+golden blocks and brute force over Python ints."""
+import json
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import formats as F
+
+
+# ---------------------------------------------------------------- float codecs
+
+def test_ue4m3_matches_torch_e4m3fn_for_every_finite_code():
+    codes = np.arange(0x7F, dtype=np.uint8)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert np.array_equal(F.ue4m3_value(codes), ref)
+    assert np.isnan(F.ue4m3_value(0x7F))
+    assert np.isnan(F.ue4m3_value(0x80))          # sign bit is not part of UE4M3
+    assert F.ue4m3_value(0x7E) == 448.0
+
+
+def _e2m1_as_e4m3_bits(code: int) -> int:
+    """E2M1 (1 sign, 2 exponent bits with bias 1, 1 mantissa bit) embedded
+    in E4M3 (bias 7): a normal E2M1 exponent e maps to field e + 6 and the
+    mantissa bit to the top mantissa bit; subnormal 0.5 is 2^-1 (field 6)."""
+    s, e, m = code >> 3, (code >> 1) & 3, code & 1
+    if e == 0:
+        bits = 0 if m == 0 else (6 << 3)
+    else:
+        bits = ((e + 6) << 3) | (m << 2)
+    return (s << 7) | bits
+
+
+def test_e2m1_matches_torch_through_e4m3_embedding():
+    bits = np.array([_e2m1_as_e4m3_bits(c) for c in range(16)], dtype=np.uint8)
+    ref = torch.from_numpy(bits).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = F.e2m1_value(np.arange(16))
+    assert np.array_equal(got, ref)
+    assert list(np.abs(got[:8])) == [0, 0.5, 1, 1.5, 2, 3, 4, 6]
+
+
+def test_bf16_decode_matches_torch_all_codes():
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ref = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    got = F.bf16_bits_to_f64(bits)
+    both_nan = np.isnan(ref) & np.isnan(got)
+    assert np.array_equal(got[~both_nan], ref[~both_nan])
+
+
+def test_round_to_bf16_matches_torch_on_fp32_inputs():
+    r = np.random.default_rng(0)
+    x = (r.standard_normal(200000) * np.exp2(r.integers(-30, 30, 200000))).astype(np.float32)
+    ref = torch.from_numpy(x).to(torch.bfloat16).to(torch.float64).numpy()
+    assert np.array_equal(F.round_to_bf16(x.astype(np.float64)), ref)
+    # exact midpoints between bf16 neighbours go to the even mantissa
+    assert F.round_to_bf16(np.array([1.0 + 2.0 ** -8]))[0] == 1.0
+    assert F.round_to_bf16(np.array([1.0 + 3 * 2.0 ** -8]))[0] == 1.0 + 2.0 ** -6
+
+
+def test_ue4m3_encoder_matches_torch_rounding_including_ties():
+    fin = F.ue4m3_value(np.arange(0x7F))
+    mids = (fin[:-1] + fin[1:]) / 2.0                        # exact ties
+    r = np.random.default_rng(1)
+    vals = np.concatenate([mids, r.uniform(0, 448, 5000), r.uniform(0, 0.02, 5000), fin])
+    vals = vals.astype(np.float32)
+    ref = torch.from_numpy(vals).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(F.ue4m3_encode_rne_sat(vals), ref)
+    assert F.ue4m3_encode_rne_sat(np.float32(1000.0)) == 0x7E
+
+
+def test_e2m1_encoder_hand_table_and_brute_force():
+    # hand-derived: ties go to the even code
+    cases = {0.25: 0, 0.26: 1, 0.75: 2, 1.25: 2, 1.75: 4, 2.5: 4, 3.5: 6, 5.0: 6,
+             5.01: 7, 7.0: 7, 100.0: 7, -0.1: 8, -5.0: 14, -6.0: 15, 0.0: 0}
+    for v, c in cases.items():
+        assert F.e2m1_encode_rne_sat(np.float32(v)) == c, v
+    table = [0, 0.5, 1, 1.5, 2, 3, 4, 6]
+    r = np.random.default_rng(2)
+    for v in r.uniform(-8, 8, 3000).astype(np.float32):
+        a = abs(float(v))
+        best = min(range(8), key=lambda i: (abs(table[i] - a), i % 2))
+        assert F.e2m1_encode_rne_sat(v) == best | (8 if v < 0 else 0)
+
+
+# ---------------------------------------------------------------- Q4_K
+
+def test_q4k_scale_unpack_golden(golden_dir):
+    g = json.load(open(os.path.join(golden_dir, "q4k_scales.json")))
+    sc, mn = F.q4k_scale_min(np.array(g["scales12"], dtype=np.uint8))
+    assert list(sc) == g["sc"] and list(mn) == g["m"]
+
+
+def test_q4k_scale_unpack_single_bit_bijection():
+    """Each of the 96 bits lands in exactly one 6-bit field as a single bit,
+    and all 16*6 (field, bit) slots are hit once."""
+    hits = set()
+    for byte in range(12):
+        for bit in range(8):
+            s = np.zeros(12, dtype=np.uint8)
+            s[byte] = 1 << bit
+            sc, mn = F.q4k_scale_min(s)
+            fields = list(sc) + list(mn)
+            nz = [(i, v) for i, v in enumerate(fields) if v]
+            assert len(nz) == 1 and (nz[0][1] & (nz[0][1] - 1)) == 0
+            hits.add((nz[0][0], int(nz[0][1]).bit_length() - 1))
+    assert len(hits) == 96
+
+
+def test_q4k_superblock_golden_values(golden_dir):
+    g = json.load(open(os.path.join(golden_dir, "q4k_scales.json")))["superblock"]
+    sb = np.zeros(144, dtype=np.uint8)
+    sb[0:2] = np.array([g["d_bits"]], dtype=np.uint16).view(np.uint8)
+    sb[2:4] = np.array([g["dmin_bits"]], dtype=np.uint16).view(np.uint8)
+    sb[4:16] = json.load(open(os.path.join(golden_dir, "q4k_scales.json")))["scales12"]
+    for c in range(4):
+        for l in range(32):
+            sb[16 + 32 * c + l] = (l % 16) | (((l + c) % 16) << 4)
+    v = F.dequantize_rows(F.TYPE_Q4_K, sb[None, :], 256)[0]
+    for idx, val in g["values"].items():
+        assert v[int(idx)] == val, idx
+
+
+# ---------------------------------------------------------------- q8_1
+
+def _fp32_round(fr: Fraction) -> Fraction:
+    """Round an exact rational to the nearest fp32 (ties to even), normal range."""
+    if fr == 0:
+        return Fraction(0)
+    sign = -1 if fr < 0 else 1
+    a = abs(fr)
+    e = a.numerator.bit_length() - a.denominator.bit_length()
+    if Fraction(2) ** e > a:
+        e -= 1
+    q = Fraction(2) ** (e - 23)                    # 24 significant bits
+    n = a / q
+    fl = n.numerator // n.denominator
+    rem = n - fl
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and fl % 2 == 1):
+        fl += 1
+    return sign * fl * q
+
+
+def _round_half_even(fr: Fraction) -> int:
+    fl = fr.numerator // fr.denominator
+    rem = fr - fl
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and fl % 2 == 1):
+        fl += 1
+    return fl
+
+
+def test_q8_1_codes_match_exact_rational_reference():
+    r = np.random.default_rng(3)
+    x = (r.standard_normal((40, 32)) * np.exp2(r.integers(-8, 8, (40, 1)))).astype(np.float32)
+    x[0, :] = 0
+    x[1, :] = np.arange(32) - 16                                    # ramp
+    qs, d_bits, s_bits, sumq = F.quantize_q8_1(x)
+    for b in range(40):
+        amax = max(abs(Fraction(float(v))) for v in x[b])
+        d = _fp32_round(amax / 127)
+        for i in range(32):
+            want = 0 if d == 0 else _round_half_even(_fp32_round(Fraction(float(x[b, i])) / d))
+            assert qs[b, 0, i] == want, (b, i)
+        assert float(np.uint16(d_bits[b, 0]).view(np.float16)) == float(np.float16(float(d)))
+        assert sumq[b, 0] == sum(int(v) for v in qs[b, 0])
+
+
+def test_q8_1_golden_blocks(golden_dir):
+    g = json.load(open(os.path.join(golden_dir, "q8_1_blocks.json")))
+    qs, d, s, _ = F.quantize_q8_1(np.zeros(32, np.float32))
+    assert not qs.any() and d[0] == 0 and s[0] == 0
+    x = np.zeros(32, np.float32)
+    x[5] = 3.0
+    qs, d, s, _ = F.quantize_q8_1(x)
+    spike = g["cases"][1]
+    assert qs[0, 5] == spike["qs_at_5"] and np.count_nonzero(qs) == 1
+    assert d[0] == spike["d_bits"] and s[0] == spike["s_bits"]
+
+
+def test_q8_1_round_trip_bound():
+    r = np.random.default_rng(4)
+    x = r.standard_normal((500, 64)).astype(np.float32)
+    qs, d_bits, _, _ = F.quantize_q8_1(x)
+    back = F.dequantize_q8_1(qs, d_bits)
+    xb = x.astype(np.float64).reshape(500, 2, 32)
+    d32 = np.abs(xb).max(axis=-1) / 127.0
+    dh = F.fp16_bits_to_f64(d_bits)
+    bound = d32 / 2 * (1 + 1e-6) + 127 * np.abs(d32 - dh)
+    err = np.abs(back.reshape(500, 2, 32) - xb).max(axis=-1)
+    assert (err <= bound + 1e-12).all()
+
+
+# ---------------------------------------------------------------- block dots
+
+_E2M1_X2 = {0: 0, 1: 1, 2: 2, 3: 3, 4: 4, 5: 6, 6: 8, 7: 12}
+
+
+@pytest.mark.parametrize("wtype,k", [(F.TYPE_Q8_0, 96), (F.TYPE_NVFP4, 128), (F.TYPE_Q4_K, 512)])
+def test_block_dots_brute_force(wtype, k):
+    r = np.random.default_rng(5 + wtype)
+    rb = F.row_bytes(wtype, k)
+    rows = r.integers(0, 256, (3, rb), dtype=np.uint8)
+    a = r.integers(-127, 128, (k // 32, 32)).astype(np.int8)
+    got = F.block_dots(wtype, rows, k, a)
+    af = [int(v) for v in a.reshape(-1)]
+    for ri in range(3):
+        row = [int(b) for b in rows[ri]]
+        if wtype == F.TYPE_Q8_0:
+            want = []
+            for b in range(k // 32):
+                blk = row[b * 34 + 2: b * 34 + 34]
+                want.append(sum((v - 256 if v > 127 else v) * af[b * 32 + i] for i, v in enumerate(blk)))
+        elif wtype == F.TYPE_NVFP4:
+            vals = []
+            for byte in row[: k // 2]:
+                for nib in (byte & 15, byte >> 4):
+                    mag = _E2M1_X2[nib & 7]
+                    vals.append(-mag if nib & 8 else mag)
+            want = [sum(vals[b * 16 + i] * af[b * 16 + i] for i in range(16)) for b in range(k // 16)]
+        else:
+            want = []
+            for sbi in range(k // 256):
+                qs = row[sbi * 144 + 16: sbi * 144 + 144]
+                for j in range(8):
+                    c = j // 2
+                    codes = [(qs[c * 32 + l] >> (4 * (j % 2))) & 15 for l in range(32)]
+                    base = sbi * 256 + j * 32
+                    want.append(sum(codes[l] * af[base + l] for l in range(32)))
+        assert list(got[ri]) == want
+
+
+def test_row_bytes_match_the_pages_geometry():
+    # FreeToken issue #194, Reproduction geometry: Q4_K 3,538,944 B gate/up and
+    # 1,769,472 B down per expert; BF16 12,582,912 B and 6,291,456 B (H=4096, I=768)
+    H, I = 4096, 768
+    assert 2 * I * F.row_bytes(F.TYPE_Q4_K, H) == 3538944
+    assert H * F.row_bytes(F.TYPE_Q4_K, I) == 1769472
+    assert 2 * I * F.row_bytes(F.TYPE_BF16, H) == 12582912
+    assert H * F.row_bytes(F.TYPE_BF16, I) == 6291456
+    assert F.row_bytes(F.TYPE_NVFP4, 2048) == 1152 and F.row_bytes(F.TYPE_Q8_0, 256) == 272
+    assert F.row_bytes(F.TYPE_Q4_K, 100) == 0

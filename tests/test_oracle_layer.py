@@ -1,0 +1,132 @@
+"""Pins of the oracle's layer math: brute force over Python floats on the tiny
+Q8_0 layer, the unit-scale BF16 special case against a numpy matmul
+formula, invariants, and the W4A4 activation quantizer."""
+import math
+
+import numpy as np
+import torch
+
+from oracle import formats as F
+from oracle import layer as L
+from synth import banks as S
+
+
+def _tiny(seed=0, T=1):
+    H, I, E, K = 256, 128, 8, 2
+    geom = L.Geometry(H, I, E, K, F.TYPE_Q8_0, F.TYPE_Q8_0)
+    gu, dn, sb = S.converted_layer(seed, H, I, E, S.Q8_0, S.Q8_0)
+    x = S.hidden_bf16(seed + 1, T, H)
+    ids, w = S.softmax_topk_routing(seed + 2, T, E, K)
+    return geom, gu, dn, sb, x, ids, w
+
+
+def test_tiny_q8_0_layer_brute_force_python_floats():
+    geom, gu, dn, sb, x, ids, w = _tiny()
+    out, _, _ = L.moe_layer(geom, gu, dn, sb, x, ids, w)
+    H, I = geom.H, geom.I
+    xf = [float(v) for v in F.bf16_bits_to_f64(x[0])]
+    qs, d, _, _ = F.quantize_q8_1(np.array(xf, np.float32))
+    xa = [int(qs[b, i]) * float(np.uint16(d[b]).view(np.float16)) for b in range(H // 32) for i in range(32)]
+
+    def q8_0_row(row):
+        row = [int(v) for v in row]
+        vals = []
+        for b in range(len(row) // 34):
+            dd = float(np.frombuffer(bytes(row[b * 34: b * 34 + 2]), np.float16)[0])
+            for v in row[b * 34 + 2: b * 34 + 34]:
+                vals.append(dd * (v - 256 if v > 127 else v))
+        return vals
+
+    want = [0.0] * H
+    for k in range(geom.top_k):
+        e = int(ids[0, k])
+        h = [sum(a * b for a, b in zip(q8_0_row(gu[e, r]), xa)) for r in range(2 * I)]
+        a = []
+        for i in range(I):
+            g, u = h[i] * float(sb[e, 0]), h[I + i] * float(sb[e, 1])
+            a.append(g / (1.0 + math.exp(-g)) * u)
+        aq, ad, _, _ = F.quantize_q8_1(np.array(a, np.float32))
+        av = [int(aq[b, i]) * float(np.uint16(ad[b]).view(np.float16)) for b in range(I // 32) for i in range(32)]
+        for j in range(H):
+            y = sum(p * q for p, q in zip(q8_0_row(dn[e, j]), av))
+            want[j] += y * float(sb[e, 2]) * float(w[0, k])
+    assert np.allclose(out[0], want, rtol=1e-12, atol=1e-15)
+
+
+def test_unit_scale_bf16_layer_equals_matmul_formula():
+    H, I, E = 64, 32, 3
+    r = np.random.default_rng(7)
+    wgu = (r.standard_normal((E, 2 * I, H)) * 0.1).astype(np.float32)
+    wd = (r.standard_normal((E, H, I)) * 0.1).astype(np.float32)
+    gu = np.stack([S.convert_bf16(wgu[e]) for e in range(E)])
+    dn = np.stack([S.convert_bf16(wd[e]) for e in range(E)])
+    x = S.hidden_bf16(8, 2, H)
+    geom = L.Geometry(H, I, E, 1, F.TYPE_BF16, F.TYPE_BF16)
+    ids = np.array([[2], [0]], np.int32)
+    w = np.ones((2, 1), np.float32)
+    out, _, _ = L.moe_layer(geom, gu, dn, None, x, ids, w)
+    # the same layer written with torch's bf16 decode and a numpy matmul
+    xt = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).double().numpy()
+    for t, e in enumerate([2, 0]):
+        Wg = torch.from_numpy(wgu[e][:I]).bfloat16().double().numpy()
+        Wu = torch.from_numpy(wgu[e][I:]).bfloat16().double().numpy()
+        Wd = torch.from_numpy(wd[e]).bfloat16().double().numpy()
+        hg, hu = Wg @ xt[t], Wu @ xt[t]
+        ref = ((hg / (1 + np.exp(-hg))) * hu) @ Wd.T
+        assert np.allclose(out[t], ref, rtol=1e-13, atol=1e-15)
+
+
+def test_layer_invariants():
+    geom, gu, dn, sb, x, ids, w = _tiny(seed=3, T=3)
+    base, _, _ = L.moe_layer(geom, gu, dn, sb, x, ids, w)
+    # linear in the routing weight
+    out2, _, _ = L.moe_layer(geom, gu, dn, sb, x, ids, w * 2)
+    assert np.allclose(out2, 2 * base, rtol=1e-14)
+    # linear in s_down
+    sb2 = sb.copy()
+    sb2[:, 2] *= 4
+    out4, _, _ = L.moe_layer(geom, gu, dn, sb2, x, ids, w)
+    assert np.allclose(out4, 4 * base, rtol=1e-14)
+    # route order does not matter
+    outp, _, _ = L.moe_layer(geom, gu, dn, sb, x, ids[:, ::-1].copy(), w[:, ::-1].copy())
+    assert np.allclose(outp, base, rtol=1e-13, atol=1e-16)
+    # a route with an out-of-range id contributes nothing
+    ids_bad = ids.copy()
+    ids_bad[:, 1] = 99
+    outb, _, _ = L.moe_layer(geom, gu, dn, sb, x, ids_bad, w)
+    g1 = L.Geometry(geom.H, geom.I, geom.E, 1, geom.gate_up_type, geom.down_type)
+    out1, _, _ = L.moe_layer(g1, gu, dn, sb, x, ids[:, :1].copy(), w[:, :1].copy())
+    assert np.allclose(outb, out1, rtol=1e-14)
+    # scaling s_gate and s_up together by c with unit silu slope is not linear:
+    # the GLU must see the scaled values (scales are applied before the GLU)
+    sb3 = sb.copy()
+    sb3[:, 0] *= 3
+    out3, _, _ = L.moe_layer(geom, gu, dn, sb3, x, ids, w)
+    assert not np.allclose(out3, 3 * base, rtol=1e-3)
+
+
+def test_bf16_output_rounding_is_single_rne():
+    geom, gu, dn, sb, x, ids, w = _tiny(seed=5)
+    out, bits, _ = L.moe_layer(geom, gu, dn, sb, x, ids, w)
+    ref = torch.from_numpy(out.astype(np.float32)).bfloat16().view(torch.int16).numpy().view(np.uint16)
+    # fp64 -> bf16 once may differ from fp64 -> fp32 -> bf16 only in rare double-rounding cases
+    assert (bits != ref).mean() < 1e-3
+
+
+def test_nvfp4_activation_quantizer_pins():
+    # a block whose amax is 6 has scale UE4M3(1.0) = 0x38 and grid values map exactly
+    x = np.array([6, -4, 3, 2, 1.5, 1, 0.5, 0, -0.5, -1, -1.5, -2, -3, -6, 4, 0], np.float32)
+    codes, sc = L.quantize_nvfp4_act(x)
+    assert sc[0] == 0x38
+    assert np.array_equal(F.e2m1_value(codes), x.astype(np.float64))
+    # zero block -> scale 0, codes 0
+    codes, sc = L.quantize_nvfp4_act(np.zeros(16, np.float32))
+    assert sc[0] == 0 and not codes.any()
+    # random blocks: every value within half an E2M1 step (times the scale) plus scale rounding
+    r = np.random.default_rng(9)
+    xb = r.standard_normal((300, 16)).astype(np.float32)
+    codes, sc = L.quantize_nvfp4_act(xb)
+    back = L.dequantize_nvfp4_act(codes, sc)
+    sv = F.ue4m3_value(sc)          # [300, 1]: one scale per 16-value block
+    step = np.where(np.abs(back) >= 4 * sv, 2 * sv, np.where(np.abs(back) >= 2 * sv, sv, 0.5 * sv))
+    assert (np.abs(back - xb) <= step / 2 + 1e-12 + np.maximum(0, np.abs(xb) - 6 * sv)).all()
