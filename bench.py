@@ -1,0 +1,406 @@
+"""Benchmark: routed-expert MoE decode on one GB300 (or N replicas under torchrun).
+
+Default workload (the headline line): the Qwen3-30B-A3B-shaped NVFP4 decode
+layer -- H=2048, I=768, E=128 experts, top-8, T=1 token -- as a stack of 48
+distinct resident layer banks (48 x 340 MB, far beyond the 129 MB L2), each
+with its own softmax top-8 routing of N(0,1) logits.  One step = one token
+through all 48 layers (48 moe_decode calls = 144 kernels), replayed from one
+CUDA graph.  value = layer-tokens/s (tokens x layers / s).
+
+Also reported in the same line: the 47-layer Laguna-shaped stack (39 Q4_K +
+8 BF16 layers, H=4096, I=768, E=256, top-10, Zipf(1.1) routing, 85.4 GiB
+resident) at T = 1, 4, 16, 64 as stack tokens/s, and the NVFP4 layer at T=8.
+
+Roofline: the timed unit is one moe_decode pass (k_prep + k_gate_up + k_down,
+chained with programmatic dependent launch so they overlap); achieved GB/s =
+the algorithmic bytes of a pass (each routed expert's gate_up and down rows
+once, plus x, ids, weights and out) / the pass's average duration from CUDA
+events on the launching stream.  Peak = MEASURED_PEAKS.json hbm_gbs.
+
+--impl reference times the CPU oracle (numpy, fp64) on a bounded sample of
+the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+NVFP4, Q4_K, BF16 = 3, 2, 0
+CFG1 = dict(H=2048, I=768, E=128, K=8, gu=NVFP4, dn=NVFP4)
+LAGUNA = dict(H=4096, I=768, E=256, K=10)
+
+
+def row_bytes(t, k):
+    return {0: 2 * k, 1: k // 32 * 34, 2: k // 256 * 144, 3: k // 2 + k // 16}[t]
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.rows = []
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except FileNotFoundError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append([c.strip() for c in line.split(",")])
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in self.rows if len(r) > 8 and r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in self.rows if len(r) > 8 and r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in self.rows:
+            if len(r) > 8:
+                for n, v in zip(names, r[5:9]):
+                    if v.strip().lower() == "active":
+                        reasons.add(n)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(self.rows)}
+
+
+# ------------------------------------------------------------------ stacks of layers on the device
+
+class Stack:
+    """NL resident layers with inputs/outputs and a captured CUDA graph of one step."""
+
+    def __init__(self, layer_types, H, I, E, K, T, routing, seed, dev):
+        import torch
+
+        from quantized_routed_expert_route_gb300 import capi
+        from synth import banks as S
+        from synth import counter as C
+        self.torch, self.capi = torch, capi
+        self.H, self.I, self.E, self.K, self.T = H, I, E, K, T
+        self.NL = len(layer_types)
+        self.layers = []
+        self.bytes_per_step = 0
+        self.unique_per_layer = []
+        stream = torch.cuda.current_stream().cuda_stream
+        for l, (gu_t, dn_t) in enumerate(layer_types):
+            rb_gu, rb_dn = row_bytes(gu_t, H), row_bytes(dn_t, I)
+            gu = torch.empty(E * 2 * I * rb_gu + 16, dtype=torch.uint8, device=dev)
+            dn = torch.empty(E * H * rb_dn + 16, dtype=torch.uint8, device=dev)
+            C.fill_bank_torch(gu[: E * 2 * I * rb_gu], seed * 1000 + 2 * l, gu_t, H)
+            C.fill_bank_torch(dn[: E * H * rb_dn], seed * 1000 + 2 * l + 1, dn_t, I)
+            sb = torch.from_numpy(S.counter_scale_bank(seed * 1000 + l, E, gu_t, dn_t)).to(dev)
+            geom = capi.moe_layer_geom(H, I, E, K, gu_t, dn_t)
+            bank = capi.moe_bank_create(geom, gu.data_ptr(), E * 2 * I * rb_gu, dn.data_ptr(), E * H * rb_dn,
+                                        sb.data_ptr(), capi.MOE_SRC_DEVICE_BORROW, stream)
+            if routing == "zipf":
+                ids, w = S.zipf_routing(seed * 7 + l, T, E, K)
+            else:
+                ids, w = S.softmax_topk_routing(seed * 7 + l, T, E, K)
+            uniq = len(np.unique(ids))
+            self.unique_per_layer.append(uniq)
+            self.bytes_per_step += uniq * (2 * I * rb_gu + H * rb_dn) + T * H * 2 * 2 + T * K * 8
+            self.layers.append(dict(gu=gu, dn=dn, sb=sb, bank=bank, ids_np=ids, w_np=w,
+                                    ids=torch.from_numpy(ids).to(dev), w=torch.from_numpy(w).to(dev)))
+        ws_bytes = max(capi.moe_workspace_bytes(L["bank"], T) for L in self.layers)
+        self.ws_bytes = ws_bytes
+        self.ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+        capi.moe_workspace_init(self.ws.data_ptr(), ws_bytes, stream)
+        g = np.random.default_rng(seed)
+        xs = torch.from_numpy(g.standard_normal((self.NL, T, H)).astype(np.float32))
+        self.x = xs.to(torch.bfloat16).to(dev)
+        self.out = torch.empty((self.NL, T, H), dtype=torch.bfloat16, device=dev)
+        self.graph = None
+        self.stream = torch.cuda.Stream(device=dev)
+
+    def launch_all(self, stream_ptr):
+        capi = self.capi
+        for l, L in enumerate(self.layers):
+            capi.moe_decode(L["bank"], self.x[l].data_ptr(), self.T, L["ids"].data_ptr(), L["w"].data_ptr(),
+                            self.out[l].data_ptr(), self.ws.data_ptr(), self.ws_bytes, stream_ptr)
+
+    def capture(self):
+        torch = self.torch
+        s = self.stream
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            self.launch_all(s.cuda_stream)
+            s.synchronize()
+            self.graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(self.graph, stream=s):
+                self.launch_all(s.cuda_stream)
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+
+    def time_replays(self, steps, warmup):
+        torch = self.torch
+        s = self.stream
+        with torch.cuda.stream(s):
+            for _ in range(warmup):
+                self.graph.replay()
+            s.synchronize()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(s)
+            for _ in range(steps):
+                self.graph.replay()
+            e1.record(s)
+            e1.synchronize()
+        return e0.elapsed_time(e1) / steps   # ms per step
+
+    def time_e2e(self, steps, warmup):
+        """Per step: pinned host -> device copies of x, ids and weights, the
+        graph replay, and the device -> host copy of the outputs."""
+        torch = self.torch
+        s = self.stream
+        hx = self.x.cpu().pin_memory()
+        hids = [L["ids"].cpu().pin_memory() for L in self.layers]
+        hw = [L["w"].cpu().pin_memory() for L in self.layers]
+        hout = torch.empty(self.out.shape, dtype=self.out.dtype, pin_memory=True)
+        h2d = hx.numel() * 2 + sum(t.numel() * 4 for t in hids) + sum(t.numel() * 4 for t in hw)
+        d2h = hout.numel() * 2
+
+        def one():
+            self.x.copy_(hx, non_blocking=True)
+            for L, a, b in zip(self.layers, hids, hw):
+                L["ids"].copy_(a, non_blocking=True)
+                L["w"].copy_(b, non_blocking=True)
+            self.graph.replay()
+            hout.copy_(self.out, non_blocking=True)
+
+        with torch.cuda.stream(s):
+            for _ in range(warmup):
+                one()
+            s.synchronize()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(s)
+            for _ in range(steps):
+                one()
+                s.synchronize()
+            e1.record(s)
+            e1.synchronize()
+        return e0.elapsed_time(e1) / steps, h2d, d2h
+
+    def close(self):
+        for L in self.layers:
+            self.capi.moe_bank_destroy(L["bank"])
+        self.layers = []
+
+
+# ------------------------------------------------------------------ CPU oracle timing
+
+def cpu_oracle_worker(seconds: float, seed: int = 0) -> dict:
+    """Time the oracle on tokens of the headline workload (one NVFP4 layer,
+    T=1, top-8) until `seconds` have elapsed; only the routed experts are
+    generated, and their generation is outside the timed part."""
+    from oracle import layer as OL
+    from synth import banks as S
+    c = CFG1
+    geom = OL.Geometry(c["H"], c["I"], c["E"], c["K"], c["gu"], c["dn"])
+    done, spent = 0, 0.0
+    t = 0
+    while spent < seconds and done < 64:
+        ids, w = S.softmax_topk_routing(seed * 7 + t, 1, c["E"], c["K"])
+        x = S.hidden_bf16(seed + t, 1, c["H"])
+        gu, dn, sb = {}, {}, np.ones((c["E"], 4), np.float32)
+        for e in ids.reshape(-1):
+            gu[int(e)], dn[int(e)], sb[int(e)] = S.converted_expert(seed, int(e), c["H"], c["I"], c["gu"], c["dn"])
+        t0 = time.perf_counter()
+        OL.moe_layer(geom, gu, dn, sb, x, ids, w)
+        spent += time.perf_counter() - t0
+        done += 1
+        t += 1
+    return {"value": done / spent, "unit": "layer-tok/s", "cores": 1, "kind": "oracle",
+            "sample": f"{done} tokens x 1 NVFP4 layer (H=2048, I=768, E=128, top-8), numpy fp64, "
+                      f"1 BLAS thread, {spent:.1f} s of oracle time"}
+
+
+def run_cpu_baseline(seconds: float) -> dict:
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    res = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-oracle-worker", str(seconds)],
+                         stdout=subprocess.PIPE, stderr=subprocess.PIPE, text=True, env=env, cwd=ROOT)
+    if res.returncode != 0:
+        return {"value": None, "unit": "layer-tok/s", "cores": 1, "kind": "oracle",
+                "sample": "failed: " + res.stderr.strip()[-300:]}
+    return json.loads(res.stdout.strip().splitlines()[-1])
+
+
+# ------------------------------------------------------------------ main
+
+def dist_setup(n):
+    if int(os.environ.get("WORLD_SIZE", "1")) > 1:
+        import torch
+        import torch.distributed as dist
+        local = int(os.environ.get("LOCAL_RANK", "0"))
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+        return dist.get_rank(), dist.get_world_size(), local
+    return 0, 1, 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--layers", type=int, default=48)
+    ap.add_argument("--no-stack", action="store_true", help="skip the 47-layer Laguna sweep")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--cpu-oracle-worker", type=float, default=None, help=argparse.SUPPRESS)
+    a = ap.parse_args()
+
+    if a.cpu_oracle_worker is not None:
+        print(json.dumps(cpu_oracle_worker(a.cpu_oracle_worker)))
+        return
+
+    workload = (f"qwen3-30b-a3b-shaped nvfp4 routed-expert decode layer (H=2048, I=768, E=128, top-8, T=1), "
+                f"{a.layers} distinct resident layer banks per step")
+    if a.impl == "reference":
+        rank = int(os.environ.get("RANK", "0"))
+        if rank != 0:
+            return
+        vals = []
+        for i in range(a.warmup + a.steps):
+            r = cpu_oracle_worker(max(1.0, a.cpu_seconds / max(1, a.steps)), seed=i)
+            if i >= a.warmup:
+                vals.append(r["value"])
+        v = float(np.mean(vals))
+        print(json.dumps({
+            "impl": "reference", "metric": "routed-expert decode throughput", "value": v, "unit": "layer-tok/s",
+            "n_gpus": a.gpus, "steps": a.steps, "warmup": a.warmup, "higher_is_better": True,
+            "dtype": "f64", "data": "synthetic", "config": {"workload": workload},
+            "cpu_baseline": {"kind": "oracle", "cores": 1, "value": v,
+                             "sample": "per step: tokens of one NVFP4 layer through the numpy oracle"},
+            "e2e": {"value": v, "unit": "layer-tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}))
+        return
+
+    import torch
+    rank, world, local = dist_setup(a.gpus)
+    dev = f"cuda:{local}"
+    torch.cuda.set_device(local)
+    hbm_peak, peak_kind = peaks()
+
+    # headline: NVFP4 layer stack, T=1
+    c = CFG1
+    st = Stack([(c["gu"], c["dn"])] * a.layers, c["H"], c["I"], c["E"], c["K"], 1, "softmax", 1, dev)
+    st.capture()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        ms = st.time_replays(a.steps, a.warmup)
+    t_max = ms
+    if world > 1:
+        tt = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        t_max = float(tt.item())
+    units = a.layers * 1 * world                     # layer-tokens per step, whole job
+    value = units / (t_max / 1e3)
+    per_pass_ms = ms / a.layers
+    achieved = st.bytes_per_step / a.layers / (per_pass_ms / 1e3) / 1e9
+    e2e_ms, h2d, d2h = st.time_e2e(max(10, a.steps // 2), a.warmup)
+    e2e_val = units / (e2e_ms / 1e3)
+    extra = {"per_layer_us": per_pass_ms * 1e3, "bytes_per_layer": st.bytes_per_step / a.layers,
+             "unique_experts_per_layer": float(np.mean(st.unique_per_layer))}
+    st.close()
+    del st
+    torch.cuda.empty_cache()
+
+    # NVFP4 layer stack at T=8
+    st = Stack([(c["gu"], c["dn"])] * a.layers, c["H"], c["I"], c["E"], c["K"], 8, "softmax", 2, dev)
+    st.capture()
+    ms8 = st.time_replays(max(10, a.steps // 2), a.warmup)
+    extra["t8"] = {"layer_tok_per_s": a.layers * 8 / (ms8 / 1e3), "per_layer_us": ms8 / a.layers * 1e3,
+                   "hbm_gbs": st.bytes_per_step / (ms8 / 1e3) / 1e9}
+    st.close()
+    del st
+    torch.cuda.empty_cache()
+
+    if not a.no_stack:
+        L = LAGUNA
+        types = [(BF16, BF16) if l % 6 == 0 else (Q4_K, Q4_K) for l in range(47)]
+        sweep = {}
+        for T in (1, 4, 16, 64):
+            st = Stack(types, L["H"], L["I"], L["E"], L["K"], T, "zipf", 3, dev)
+            st.capture()
+            msT = st.time_replays(max(5, a.steps // 5), a.warmup)
+            sweep[f"T={T}"] = {"stack_tok_per_s": T / (msT / 1e3), "ms_per_stack": msT,
+                               "hbm_gbs": st.bytes_per_step / (msT / 1e3) / 1e9,
+                               "frac": st.bytes_per_step / (msT / 1e3) / 1e9 / hbm_peak,
+                               "gb_per_step": st.bytes_per_step / 1e9}
+            st.close()
+            del st
+            torch.cuda.empty_cache()
+        extra["laguna_47_layer_stack"] = sweep
+
+    cpu = run_cpu_baseline(a.cpu_seconds) if rank == 0 else None
+    if rank == 0:
+        line = {
+            "metric": "routed-expert decode throughput (tokens x layers / s); achieved HBM GB/s vs peak",
+            "value": value, "unit": "layer-tok/s", "n_gpus": world, "steps": a.steps, "warmup": a.warmup,
+            "ms_per_step": t_max, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "nvfp4 weights x q8_1 activations, int32 block dots, fp32 epilogue, bf16 out",
+            "data": "synthetic (counter-based banks, seeded routings)",
+            "config": {"workload": workload, "T": 1, "layers_per_step": a.layers,
+                       "l2": "inputs larger than L2 (1 GB of expert rows per step, 16 GB resident)",
+                       "parallelism": f"replicas x{world}"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                         "frac": achieved / hbm_peak, "traffic": None, "peak_kind": peak_kind,
+                         "kernel": "moe_decode pass (k_prep+k_gate_up+k_down, PDL-overlapped)"},
+            "clocks": clk.summary(),
+            "e2e": {"value": e2e_val, "unit": "layer-tok/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": 3 * a.layers * a.steps,
+            "cpu_baseline": cpu,
+            "extra": extra,
+        }
+        print(json.dumps(line))
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,194 @@
+/*
+ * qre_moe.h -- C ABI of the GB300 routed-expert MoE library.
+ *
+ * One MoE layer's routed experts, resident in HBM as compact per-layer banks,
+ * evaluated for decode tokens by hand-written sm_103a kernels.  The layer
+ * computes (FreeToken PR #732, "apply the weight scales of nvfp4 gguf
+ * tensors", section "Design"):
+ *
+ *     h = x @ W_gate_up^T;   g = h_gate * s_gate,  u = h_up * s_up
+ *     y = (silu(g) * u  @ W_down^T) * s_down * routing_weight,  summed over routes
+ *
+ * with the per-expert scale bank [E,4] fp32 = (s_gate, s_up, s_down, 1), and
+ * the pipeline of FreeToken PR #704 ("serve GGUF experts on the cpu and hybrid
+ * backends through ggml-cpu", section "How it plugs into the CPU executor"):
+ * prep_input (bf16 hidden -> q8_1, or kept float for BF16 rows), gate_up (a dot
+ * over every gate and up row of the routed expert, then the activation),
+ * prep_inter (intermediate -> the down type's input), down (a dot over every
+ * output row per route) and the sum over routes.
+ *
+ * Conventions for every call below:
+ *   - Return value: MOE_OK (0) or a negative moe_status.  No call throws, and
+ *     no call aborts the process.
+ *   - "device pointer" means memory of the current CUDA device; "stream" is a
+ *     cudaStream_t passed as void* (NULL = the legacy default stream).
+ *   - moe_decode and the test hooks are asynchronous on the given stream; they
+ *     allocate nothing, never synchronize, and may be captured into a CUDA
+ *     graph.  Kernels are launched with programmatic dependent launch, so
+ *     consecutive layers overlap their prologues.
+ *   - The caller owns x, ids, weights, out and the workspace.  The library
+ *     owns each bank (unless created with MOE_SRC_DEVICE_BORROW).
+ */
+#ifndef QRE_MOE_H
+#define QRE_MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Bank row types.  Row layouts (row = K values, rows stored back to back):
+ *   MOE_BF16 : K little-endian bf16 (2K bytes).  FreeToken issue #194, "avoid
+ *              max-stride padding ...", Proposed design: BF16 rows run through
+ *              a float kernel, not the block-quantized one.
+ *   MOE_Q8_0 : K/32 blocks of {fp16 d; int8 q[32]} (34 bytes), value d*q.
+ *   MOE_Q4_K : K/256 super-blocks of 144 bytes {fp16 d; fp16 dmin;
+ *              uint8 scales[12] (8 packed 6-bit (sc, m) pairs); uint8 qs[128]},
+ *              value d*sc_j*q - dmin*m_j (GGUF Q4_K bit layout).
+ *   MOE_NVFP4: K/2 code bytes (E2M1; element 2i in the low nibble of byte i)
+ *              then K/16 UE4M3 scale bytes, one per 16 values (Strata PR #292,
+ *              "NVFP4 routed experts ...", Summary/Pipeline: group 16).  The
+ *              per-expert weight_scale_2 lives in the scale bank, not the row. */
+typedef enum { MOE_BF16 = 0, MOE_Q8_0 = 1, MOE_Q4_K = 2, MOE_NVFP4 = 3 } moe_type;
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_EINVAL = -1,        /* bad argument: null pointer, size, geometry, alignment */
+  MOE_EUNSUPPORTED = -2,  /* valid but not built: e.g. a type or shape outside the limits */
+  MOE_ENOMEM = -3,        /* device allocation failed (bank creation only) */
+  MOE_ECUDA = -4,         /* a CUDA runtime call failed; see moe_last_cuda_error() */
+  MOE_EDEVICE = -5        /* moe_get_error found a device-side error bit */
+} moe_status;
+
+/* Device-side error bits (sticky in the workspace, read by moe_get_error). */
+enum {
+  MOE_DEVERR_BAD_ID = 1,   /* a topk id outside [0, E): that route contributed zero */
+  MOE_DEVERR_TIMEOUT = 2   /* a bounded wait on a TMA copy ran out; outputs are invalid */
+};
+
+/* Limits of this build. */
+enum {
+  MOE_MAX_E = 1024,        /* experts per layer */
+  MOE_MAX_TOPK = 32,       /* routes per token */
+  MOE_DECODE_T_CHUNK = 64  /* tokens per internal decode pass (larger T is split) */
+};
+
+typedef struct {
+  int32_t H;             /* hidden size; multiple of 256 for Q4_K gate_up, else of 32 */
+  int32_t I;             /* intermediate size; multiple of 32 (256 for Q4_K down) */
+  int32_t E;             /* experts, 1..MOE_MAX_E */
+  int32_t top_k;         /* routes per token, 1..min(E, MOE_MAX_TOPK) */
+  int32_t gate_up_type;  /* moe_type of the merged gate_up rows [E, 2I, H]: rows [0,I) gate, [I,2I) up */
+  int32_t down_type;     /* moe_type of the down rows [E, H, I] */
+} moe_layer_geom;
+
+/* Where moe_bank_create reads the rows from. */
+enum {
+  MOE_SRC_HOST = 0,          /* host memory: copied to a library-owned device bank */
+  MOE_SRC_DEVICE = 1,        /* device memory: copied (device to device) */
+  MOE_SRC_DEVICE_BORROW = 2  /* device memory used in place: the caller keeps it alive and
+                                unmodified until moe_bank_destroy; base 16-byte aligned and
+                                readable up to the next 16-byte boundary past its end */
+};
+
+typedef struct moe_bank moe_bank;   /* opaque */
+
+/* Bytes of one row of k values of `type` (FreeToken PR #704, "How it plugs
+ * into the CPU executor": a bank holds rows of row_bytes(type, K)).
+ * Returns 0 when k is not a whole number of the type's blocks. */
+size_t moe_row_bytes(int32_t type, int64_t k);
+
+/* Create a layer bank.  gate_up: E*2I rows of row_bytes(gate_up_type, H);
+ * down: E*H rows of row_bytes(down_type, I); both compact at the exact row
+ * stride (FreeToken issue #194, Proposed design: no padding to another layer's
+ * stride).  gate_up_bytes / down_bytes must equal those products exactly.
+ * scale_bank: [E,4] fp32 (s_gate, s_up, s_down, unused) in the same memory
+ * kind as the rows (host for MOE_SRC_HOST, else device), or NULL for all
+ * ones; it is always copied.  Synchronizes `stream` before returning.
+ * Errors: MOE_EINVAL (geometry, sizes, null or misaligned pointer),
+ * MOE_EUNSUPPORTED, MOE_ENOMEM, MOE_ECUDA.  *out is set only on success. */
+int moe_bank_create(const moe_layer_geom* geom,
+                    const void* gate_up, size_t gate_up_bytes,
+                    const void* down, size_t down_bytes,
+                    const float* scale_bank, int32_t src_kind,
+                    void* stream, moe_bank** out);
+
+/* Free a bank (waits for the device to finish with it).  NULL is a no-op. */
+int moe_bank_destroy(moe_bank* bank);
+
+/* Copy the bank's geometry to *out. */
+int moe_bank_geometry(const moe_bank* bank, moe_layer_geom* out);
+
+/* Workspace bytes moe_decode needs for batches of up to max_tokens tokens
+ * (0 on bad arguments).  The workspace holds the quantized activations, the
+ * intermediate, per-block counters and the sticky error word. */
+size_t moe_workspace_bytes(const moe_bank* bank, int32_t max_tokens);
+
+/* Clear a freshly allocated workspace (error word and counters), async on
+ * `stream`.  Call once after allocating; calls never leave it dirty. */
+int moe_workspace_init(void* ws, size_t ws_bytes, void* stream);
+
+/* Decode T tokens through one MoE layer.
+ *   x:        device, bf16 [T, H] row-major.
+ *   topk_ids: device, int32 [T, top_k]; an id outside [0, E) makes its route
+ *             contribute zero and sets MOE_DEVERR_BAD_ID.
+ *   topk_w:   device, fp32 [T, top_k] routing weights.
+ *   out:      device, bf16 [T, H]; out[t] = bf16(sum over k in order k = 0..top_k-1
+ *             of the route's fp32 result), with no atomics.
+ *   ws:       device workspace of at least moe_workspace_bytes(bank, T') bytes
+ *             for T' = min(T, MOE_DECODE_T_CHUNK), 256-byte aligned, initialised
+ *             once by moe_workspace_init.  Calls sharing a workspace must be
+ *             ordered on one stream.
+ * T = 0 is a no-op.  Errors: MOE_EINVAL, MOE_ECUDA (launch failure). */
+int moe_decode(const moe_bank* bank, const void* x, int32_t T,
+               const int32_t* topk_ids, const float* topk_w, void* out,
+               void* ws, size_t ws_bytes, void* stream);
+
+/* Read and clear the workspace's sticky device error bits (synchronizes
+ * `stream`).  *dev_err receives the MOE_DEVERR_* bits; returns MOE_EDEVICE if
+ * any was set, MOE_OK otherwise. */
+int moe_get_error(void* ws, size_t ws_bytes, void* stream, int32_t* dev_err);
+
+/* Text for a moe_status value (static storage). */
+const char* moe_status_string(int status);
+
+/* The last CUDA error text seen by the library on this thread (static storage). */
+const char* moe_last_cuda_error(void);
+
+/* ---------------------------------------------------------------- test hooks
+ * Not on the decode path; they run the same device functions the decode
+ * kernels use, so parity tests can check intermediate results bit for bit. */
+
+/* Quantize n fp32 values (device, n a multiple of 32) to q8_1 blocks of 36
+ * bytes {fp16 d; fp16 s; int8 q[32]} (device, n/32 blocks): d = amax/127,
+ * q = round-half-even(x/d) (0 when d = 0), s = d * sum(q), all in fp32 with
+ * d and s stored as fp16 -- the input quantizer of the decode path. */
+int moe_quantize_q8_1(const float* x, int64_t n, void* out_blocks, void* stream);
+
+/* Integer block dot products of quantized rows (device, nrows rows of
+ * row_bytes(type, k)) against q8_1 activation blocks (device, k/32 blocks of
+ * 36 bytes).  out: device int32 [nrows, nb] with nb = k/16 for MOE_NVFP4 (one
+ * per 16-value block, sum of (2*E2M1 code value) * q), k/32 for MOE_Q8_0 and
+ * MOE_Q4_K (sum of code * q; Q4_K per 32-value sub-block).  MOE_BF16 is
+ * MOE_EINVAL. */
+int moe_debug_block_dots(int32_t type, const void* rows, int32_t nrows, int32_t k,
+                         const void* act_blocks, int32_t* out, void* stream);
+
+/* Run moe_decode, then export workspace stages (any pointer may be NULL):
+ *   x_blocks:     the q8_1 blocks of x, [T, H/32] x 36 bytes (quantized gate_up only);
+ *   inter:        the fp32 intermediate silu(g)*u, [T*top_k, I];
+ *   inter_blocks: its q8_1 blocks, [T*top_k, I/32] x 36 bytes (quantized down only).
+ * Requires T <= MOE_DECODE_T_CHUNK.  Routes with a bad id leave their rows
+ * unspecified. */
+int moe_debug_decode_stages(const moe_bank* bank, const void* x, int32_t T,
+                            const int32_t* topk_ids, const float* topk_w, void* out,
+                            void* ws, size_t ws_bytes, void* stream,
+                            void* x_blocks, float* inter, void* inter_blocks);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QRE_MOE_H */

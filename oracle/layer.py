@@ -63,21 +63,20 @@ class _ExpertCache:
     """Dequantizes an expert's rows once per call."""
 
     def __init__(self, geom: Geometry, gate_up, down):
+        """gate_up / down: anything indexable by expert id that yields that
+        expert's rows as uint8 ([2I, rb] and [H, rb]) -- a [E, rows, rb]
+        array, or a mapping holding just the experts that are routed to."""
         self.g = geom
-        rb_gu = F.row_bytes(geom.gate_up_type, geom.H)
-        rb_d = F.row_bytes(geom.down_type, geom.I)
-        self.gu = np.asarray(gate_up, dtype=np.uint8).reshape(-1)
-        self.dn = np.asarray(down, dtype=np.uint8).reshape(-1)
-        self.rb_gu, self.rb_d = rb_gu, rb_d
+        self.rb_gu = F.row_bytes(geom.gate_up_type, geom.H)
+        self.rb_d = F.row_bytes(geom.down_type, geom.I)
+        self.gu, self.dn = gate_up, down
         self.cache: dict[int, tuple[np.ndarray, np.ndarray]] = {}
 
     def rows(self, e: int):
         if e not in self.cache:
             g = self.g
-            n_gu = 2 * g.I * self.rb_gu
-            n_d = g.H * self.rb_d
-            gu = self.gu[e * n_gu:(e + 1) * n_gu].reshape(2 * g.I, self.rb_gu)
-            dn = self.dn[e * n_d:(e + 1) * n_d].reshape(g.H, self.rb_d)
+            gu = np.asarray(self.gu[e], dtype=np.uint8).reshape(2 * g.I, self.rb_gu)
+            dn = np.asarray(self.dn[e], dtype=np.uint8).reshape(g.H, self.rb_d)
             self.cache[e] = (F.dequantize_rows(g.gate_up_type, gu, g.H),
                              F.dequantize_rows(g.down_type, dn, g.I))
         return self.cache[e]
@@ -129,7 +128,8 @@ def moe_layer(geom: Geometry, gate_up, down, scale_bank, x_bf16_bits, topk_ids, 
 
     x_bf16_bits: uint16 [T, H]; topk_ids: int [T, K]; topk_w: fp32 [T, K];
     scale_bank: fp32 [E, 4] or None (all ones); gate_up / down: the compact
-    banks as uint8 arrays ([E, 2I, row_bytes] and [E, H, row_bytes]).
+    banks as uint8 arrays ([E, 2I, row_bytes] and [E, H, row_bytes]), or
+    mappings from expert id to that expert's rows.
     act_kind: "q8_1" (decode and the W4A8 prompt path) or "nvfp4" (W4A4).
 
     Returns (out_f64 [T, H], out_bf16_bits [T, H], stages dict or None)."""
@@ -144,12 +144,15 @@ def moe_layer(geom: Geometry, gate_up, down, scale_bank, x_bf16_bits, topk_ids, 
         sb = np.asarray(scale_bank, dtype=np.float32).reshape(g.E, 4).astype(np.float64)
     cache = _ExpertCache(g, gate_up, down)
     out = np.zeros((T, g.H), dtype=np.float64)
-    st = {"x_act": [], "inter": np.zeros((T, g.top_k, g.I)), "inter_act": [],
-          "y": np.zeros((T, g.top_k, g.H)), "valid": np.zeros((T, g.top_k), bool)} if stages else None
+    st = {"x_act": [], "x_hat": np.zeros((T, g.H)), "inter": np.zeros((T, g.top_k, g.I)),
+          "inter_act": [], "inter_hat": np.zeros((T, g.top_k, g.I)),
+          "y": np.zeros((T, g.top_k, g.H)), "valid": np.zeros((T, g.top_k), bool),
+          "experts": cache.cache, "scales": sb, "w": w, "ids": ids} if stages else None
     for t in range(T):
         xa, xinfo = _act_in(act_kind, g.gate_up_type, x[t].astype(np.float32))
         if stages:
             st["x_act"].append(xinfo)
+            st["x_hat"][t] = xa
         row_inter = []
         for k in range(g.top_k):
             e = int(ids[t, k])
@@ -169,6 +172,7 @@ def moe_layer(geom: Geometry, gate_up, down, scale_bank, x_bf16_bits, topk_ids, 
             out[t] += y
             if stages:
                 st["inter"][t, k] = a
+                st["inter_hat"][t, k] = aq
                 st["y"][t, k] = y
                 st["valid"][t, k] = True
             row_inter.append(ainfo)

@@ -1,0 +1,151 @@
+"""Thin ctypes binding of the C ABI in include/qre_moe.h (same names, same arguments).
+
+Pointers are passed as Python ints (device or host addresses), streams as
+ints (a cudaStream_t; 0 = the legacy default stream).  Nothing here computes:
+every step of the decode path runs in the library's kernels.  Importing this
+module fails loudly when the library has not been built.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from .build import lib_path
+
+MOE_BF16, MOE_Q8_0, MOE_Q4_K, MOE_NVFP4 = 0, 1, 2, 3
+MOE_OK, MOE_EINVAL, MOE_EUNSUPPORTED, MOE_ENOMEM, MOE_ECUDA, MOE_EDEVICE = 0, -1, -2, -3, -4, -5
+MOE_DEVERR_BAD_ID, MOE_DEVERR_TIMEOUT = 1, 2
+MOE_SRC_HOST, MOE_SRC_DEVICE, MOE_SRC_DEVICE_BORROW = 0, 1, 2
+MOE_MAX_E, MOE_MAX_TOPK, MOE_DECODE_T_CHUNK = 1024, 32, 64
+
+# every symbol include/qre_moe.h declares
+EXPORTS = (
+    "moe_row_bytes", "moe_bank_create", "moe_bank_destroy", "moe_bank_geometry",
+    "moe_workspace_bytes", "moe_workspace_init", "moe_decode", "moe_get_error",
+    "moe_status_string", "moe_last_cuda_error", "moe_quantize_q8_1",
+    "moe_debug_block_dots", "moe_debug_decode_stages",
+)
+
+
+class moe_layer_geom(ctypes.Structure):
+    _fields_ = [("H", ctypes.c_int32), ("I", ctypes.c_int32), ("E", ctypes.c_int32),
+                ("top_k", ctypes.c_int32), ("gate_up_type", ctypes.c_int32), ("down_type", ctypes.c_int32)]
+
+
+class MoeError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        msg = f"{what}: {status_string(status)}"
+        if status == MOE_ECUDA:
+            msg += f" ({_lib.moe_last_cuda_error().decode()})"
+        super().__init__(msg)
+
+
+def _load() -> ctypes.CDLL:
+    path = lib_path()
+    if not os.path.exists(path):
+        raise RuntimeError(
+            f"the CUDA library {path} is not built; run `python -c 'import __graft_entry__ as g; g.build()'`")
+    lib = ctypes.CDLL(path)
+    vp, sz, i32, i64 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int32, ctypes.c_int64
+    sig = {
+        "moe_row_bytes": (sz, [i32, i64]),
+        "moe_bank_create": (ctypes.c_int, [ctypes.POINTER(moe_layer_geom), vp, sz, vp, sz, vp, i32, vp,
+                                           ctypes.POINTER(vp)]),
+        "moe_bank_destroy": (ctypes.c_int, [vp]),
+        "moe_bank_geometry": (ctypes.c_int, [vp, ctypes.POINTER(moe_layer_geom)]),
+        "moe_workspace_bytes": (sz, [vp, i32]),
+        "moe_workspace_init": (ctypes.c_int, [vp, sz, vp]),
+        "moe_decode": (ctypes.c_int, [vp, vp, i32, vp, vp, vp, vp, sz, vp]),
+        "moe_get_error": (ctypes.c_int, [vp, sz, vp, ctypes.POINTER(i32)]),
+        "moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+        "moe_last_cuda_error": (ctypes.c_char_p, []),
+        "moe_quantize_q8_1": (ctypes.c_int, [vp, i64, vp, vp]),
+        "moe_debug_block_dots": (ctypes.c_int, [i32, vp, i32, i32, vp, vp, vp]),
+        "moe_debug_decode_stages": (ctypes.c_int, [vp, vp, i32, vp, vp, vp, vp, sz, vp, vp, vp, vp]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+_lib = _load()
+
+
+def library() -> ctypes.CDLL:
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return _lib.moe_status_string(status).decode()
+
+
+def _check(status: int, what: str) -> int:
+    if status != MOE_OK:
+        raise MoeError(status, what)
+    return status
+
+
+def moe_row_bytes(wtype: int, k: int) -> int:
+    return int(_lib.moe_row_bytes(wtype, k))
+
+
+def moe_bank_create(geom: moe_layer_geom, gate_up: int, gate_up_bytes: int, down: int, down_bytes: int,
+                    scale_bank: int | None, src_kind: int, stream: int = 0) -> int:
+    out = ctypes.c_void_p()
+    _check(_lib.moe_bank_create(ctypes.byref(geom), gate_up, gate_up_bytes, down, down_bytes,
+                                scale_bank or None, src_kind, stream or None, ctypes.byref(out)),
+           "moe_bank_create")
+    return out.value
+
+
+def moe_bank_destroy(bank: int) -> None:
+    _check(_lib.moe_bank_destroy(bank), "moe_bank_destroy")
+
+
+def moe_bank_geometry(bank: int) -> moe_layer_geom:
+    g = moe_layer_geom()
+    _check(_lib.moe_bank_geometry(bank, ctypes.byref(g)), "moe_bank_geometry")
+    return g
+
+
+def moe_workspace_bytes(bank: int, max_tokens: int) -> int:
+    return int(_lib.moe_workspace_bytes(bank, max_tokens))
+
+
+def moe_workspace_init(ws: int, ws_bytes: int, stream: int = 0) -> None:
+    _check(_lib.moe_workspace_init(ws, ws_bytes, stream or None), "moe_workspace_init")
+
+
+def moe_decode(bank: int, x: int, T: int, topk_ids: int, topk_w: int, out: int, ws: int, ws_bytes: int,
+               stream: int = 0) -> None:
+    _check(_lib.moe_decode(bank, x, T, topk_ids, topk_w, out, ws, ws_bytes, stream or None), "moe_decode")
+
+
+def moe_get_error(ws: int, ws_bytes: int, stream: int = 0) -> int:
+    """Returns the device error bits (0 if none) and clears them."""
+    v = ctypes.c_int32(0)
+    st = _lib.moe_get_error(ws, ws_bytes, stream or None, ctypes.byref(v))
+    if st not in (MOE_OK, MOE_EDEVICE):
+        raise MoeError(st, "moe_get_error")
+    return int(v.value)
+
+
+def moe_quantize_q8_1(x: int, n: int, out_blocks: int, stream: int = 0) -> None:
+    _check(_lib.moe_quantize_q8_1(x, n, out_blocks, stream or None), "moe_quantize_q8_1")
+
+
+def moe_debug_block_dots(wtype: int, rows: int, nrows: int, k: int, act_blocks: int, out: int,
+                         stream: int = 0) -> None:
+    _check(_lib.moe_debug_block_dots(wtype, rows, nrows, k, act_blocks, out, stream or None),
+           "moe_debug_block_dots")
+
+
+def moe_debug_decode_stages(bank: int, x: int, T: int, topk_ids: int, topk_w: int, out: int, ws: int,
+                            ws_bytes: int, stream: int = 0, x_blocks: int | None = None,
+                            inter: int | None = None, inter_blocks: int | None = None) -> None:
+    _check(_lib.moe_debug_decode_stages(bank, x, T, topk_ids, topk_w, out, ws, ws_bytes, stream or None,
+                                        x_blocks or None, inter or None, inter_blocks or None),
+           "moe_debug_decode_stages")

@@ -1,0 +1,349 @@
+// C ABI of the routed-expert MoE library (declared in include/qre_moe.h):
+// bank residency, workspace layout, argument checks and kernel dispatch.
+#include <cuda_runtime.h>
+
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "../../include/qre_moe.h"
+#include "formats.cuh"
+#include "internal.h"
+
+using namespace qre;
+
+struct moe_bank {
+  moe_layer_geom geom;
+  int rb_gu, rb_dn;
+  uint8_t* gu;      // [E][2I][rb_gu] (+ slack)
+  uint8_t* dn;      // [E][H][rb_dn]  (+ slack)
+  float* scales;    // [E][4]
+  bool owns_rows;
+  int device;
+};
+
+namespace {
+
+thread_local char g_cuda_err[256] = "no error";
+
+int cuda_fail(cudaError_t e, const char* what) {
+  std::snprintf(g_cuda_err, sizeof(g_cuda_err), "%s: %s", what, cudaGetErrorString(e));
+  return MOE_ECUDA;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+int geom_check(const moe_layer_geom* g) {
+  if (!g) return MOE_EINVAL;
+  if (g->E < 1 || g->E > kMaxE || g->top_k < 1 || g->top_k > kMaxTopK || g->top_k > g->E) return MOE_EINVAL;
+  if (g->H < 32 || g->I < 32 || g->H > (1 << 16) || g->I > (1 << 16)) return MOE_EINVAL;
+  if (g->gate_up_type < MOE_BF16 || g->gate_up_type > MOE_NVFP4) return MOE_EINVAL;
+  if (g->down_type < MOE_BF16 || g->down_type > MOE_NVFP4) return MOE_EINVAL;
+  if (row_bytes_of(g->gate_up_type, g->H) == 0 || row_bytes_of(g->down_type, g->I) == 0) return MOE_EINVAL;
+  if (g->H % 32 != 0 || g->I % 32 != 0) return MOE_EINVAL;
+  return MOE_OK;
+}
+
+// Rows of the bank that one down CTA owns, and the tokens of one decode pass.
+struct Shape {
+  int g_gu, g_dn, rows_max, t_chunk;
+};
+
+Shape decode_shape(const moe_layer_geom& g) {
+  Shape s;
+  s.g_gu = sm_count();
+  s.g_dn = sm_count();
+  if (s.g_dn > g.H) s.g_dn = g.H;
+  s.rows_max = (g.H + s.g_dn - 1) / s.g_dn;
+  // keep the per-route down results (T*K*rows_max fp32) within 96 KiB of shared memory
+  int t = (96 * 1024) / (4 * g.top_k * s.rows_max);
+  if (t > kTChunk) t = kTChunk;
+  if (t < 1) t = 1;
+  s.t_chunk = t;
+  return s;
+}
+
+struct WsLayout {
+  size_t err, xq, xd, xsum, xsh, inter, iq, id, isum, ish, cnt, total;
+  int cnt_len;
+};
+
+WsLayout ws_layout(const moe_layer_geom& g, int T) {
+  WsLayout L;
+  const size_t A = 256;
+  const size_t RT = (size_t)T * g.top_k;
+  size_t o = 0;
+  L.err = o; o = align_up(o + 4, A);
+  L.xq = o; o = align_up(o + (size_t)T * g.H, A);
+  L.xd = o; o = align_up(o + 4 * (size_t)T * (g.H / 32), A);
+  L.xsum = o; o = align_up(o + 4 * (size_t)T * (g.H / 32), A);
+  L.xsh = o; o = align_up(o + 2 * (size_t)T * (g.H / 32), A);
+  L.inter = o; o = align_up(o + 4 * RT * g.I, A);
+  L.iq = o; o = align_up(o + RT * g.I, A);
+  L.id = o; o = align_up(o + 4 * RT * (g.I / 32), A);
+  L.isum = o; o = align_up(o + 4 * RT * (g.I / 32), A);
+  L.ish = o; o = align_up(o + 2 * RT * (g.I / 32), A);
+  const size_t S = (size_t)g.E < RT ? (size_t)g.E : RT;
+  L.cnt_len = (int)(S * (g.I / 32));
+  L.cnt = o; o = align_up(o + 4 * (size_t)L.cnt_len, A);
+  L.total = o;
+  return L;
+}
+
+DecodeParams make_params(const moe_bank* b, const WsLayout& L, uint8_t* ws, const Shape& sh, int T) {
+  const moe_layer_geom& g = b->geom;
+  DecodeParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.H = g.H; p.I = g.I; p.E = g.E; p.K = g.top_k; p.T = T;
+  p.gu_type = g.gate_up_type; p.dn_type = g.down_type;
+  p.rb_gu = b->rb_gu; p.rb_dn = b->rb_dn;
+  p.gu_bank = b->gu; p.dn_bank = b->dn; p.scales = b->scales;
+  p.err = reinterpret_cast<uint32_t*>(ws + L.err);
+  p.xq = reinterpret_cast<int8_t*>(ws + L.xq);
+  p.xd = reinterpret_cast<float*>(ws + L.xd);
+  p.xsum = reinterpret_cast<int*>(ws + L.xsum);
+  p.xsh = reinterpret_cast<uint16_t*>(ws + L.xsh);
+  p.inter = reinterpret_cast<float*>(ws + L.inter);
+  p.iq = reinterpret_cast<int8_t*>(ws + L.iq);
+  p.id = reinterpret_cast<float*>(ws + L.id);
+  p.isum = reinterpret_cast<int*>(ws + L.isum);
+  p.ish = reinterpret_cast<uint16_t*>(ws + L.ish);
+  p.cnt = reinterpret_cast<unsigned*>(ws + L.cnt);
+  p.cnt_len = L.cnt_len;
+  p.g_gu = sh.g_gu;
+  p.g_dn = sh.g_dn;
+  // gate_up stages: ~20 KiB of (gate, up) row pairs, ~112 KiB in flight
+  int ps = (20 * 1024) / (2 * p.rb_gu);
+  if (ps < 1) ps = 1;
+  if (ps > 32) ps = 32;
+  p.ps = ps;
+  p.gu_up_off = (int)align_up((size_t)ps * p.rb_gu + 16, 128);
+  p.gu_stage_bytes = 2 * p.gu_up_off;
+  int ns = (112 * 1024) / p.gu_stage_bytes;
+  p.gu_nstage = ns < 2 ? 2 : (ns > 8 ? 8 : ns);
+  // down stages: pieces of <= 24 KiB rows of one expert, grouped to ~32 KiB
+  p.dn_rows_max = sh.rows_max;
+  int rs = (24 * 1024) / p.rb_dn;
+  if (rs < 1) rs = 1;
+  if (rs > sh.rows_max) rs = sh.rows_max;
+  p.dn_rs = rs;
+  p.dn_piece_bytes = (int)align_up((size_t)rs * p.rb_dn + 16, 128);
+  int sps = (32 * 1024) / p.dn_piece_bytes;
+  p.dn_slots_per_stage = sps < 1 ? 1 : (sps > 16 ? 16 : sps);
+  p.dn_stage_bytes = p.dn_slots_per_stage * p.dn_piece_bytes;
+  int dns = (96 * 1024) / p.dn_stage_bytes;
+  p.dn_nstage = dns < 2 ? 2 : (dns > 8 ? 8 : dns);
+  switch (p.gu_type) {
+    case W_NVFP4: p.w0 = 2; break;
+    case W_Q4_K: p.w0 = 3; break;
+    case W_Q8_0: p.w0 = 2; break;
+    default: p.w0 = 4; break;
+  }
+  return p;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t moe_row_bytes(int32_t type, int64_t k) {
+  if (k <= 0 || k > (1 << 30)) return 0;
+  return (size_t)row_bytes_of(type, (int)k);
+}
+
+const char* moe_status_string(int s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_EINVAL: return "invalid argument";
+    case MOE_EUNSUPPORTED: return "unsupported";
+    case MOE_ENOMEM: return "out of device memory";
+    case MOE_ECUDA: return "CUDA error";
+    case MOE_EDEVICE: return "device-side error flag set";
+  }
+  return "unknown status";
+}
+
+const char* moe_last_cuda_error(void) { return g_cuda_err; }
+
+int moe_bank_create(const moe_layer_geom* geom, const void* gate_up, size_t gate_up_bytes, const void* down,
+                    size_t down_bytes, const float* scale_bank, int32_t src_kind, void* stream, moe_bank** out) {
+  if (!out || !gate_up || !down) return MOE_EINVAL;
+  int st = geom_check(geom);
+  if (st) return st;
+  if (src_kind < MOE_SRC_HOST || src_kind > MOE_SRC_DEVICE_BORROW) return MOE_EINVAL;
+  const moe_layer_geom& g = *geom;
+  const int rb_gu = row_bytes_of(g.gate_up_type, g.H), rb_dn = row_bytes_of(g.down_type, g.I);
+  const size_t want_gu = (size_t)g.E * 2 * g.I * rb_gu, want_dn = (size_t)g.E * g.H * rb_dn;
+  if (gate_up_bytes != want_gu || down_bytes != want_dn) return MOE_EINVAL;
+  if (src_kind == MOE_SRC_DEVICE_BORROW && (!aligned(gate_up, 16) || !aligned(down, 16))) return MOE_EINVAL;
+  if (scale_bank && !aligned(scale_bank, 4)) return MOE_EINVAL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  moe_bank* b = new (std::nothrow) moe_bank;
+  if (!b) return MOE_ENOMEM;
+  std::memset(b, 0, sizeof(*b));
+  b->geom = g;
+  b->rb_gu = rb_gu;
+  b->rb_dn = rb_dn;
+  cudaGetDevice(&b->device);
+  cudaError_t e;
+  if (src_kind == MOE_SRC_DEVICE_BORROW) {
+    b->gu = const_cast<uint8_t*>(static_cast<const uint8_t*>(gate_up));
+    b->dn = const_cast<uint8_t*>(static_cast<const uint8_t*>(down));
+    b->owns_rows = false;
+  } else {
+    b->owns_rows = true;
+    if ((e = cudaMalloc(&b->gu, want_gu + 256)) != cudaSuccess) { delete b; cudaGetLastError(); return MOE_ENOMEM; }
+    if ((e = cudaMalloc(&b->dn, want_dn + 256)) != cudaSuccess) {
+      cudaFree(b->gu); delete b; cudaGetLastError(); return MOE_ENOMEM;
+    }
+    const cudaMemcpyKind kind = (src_kind == MOE_SRC_HOST) ? cudaMemcpyHostToDevice : cudaMemcpyDeviceToDevice;
+    if ((e = cudaMemcpyAsync(b->gu, gate_up, want_gu, kind, s)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(b->dn, down, want_dn, kind, s)) != cudaSuccess) {
+      cudaFree(b->gu); cudaFree(b->dn); delete b; return cuda_fail(e, "bank copy");
+    }
+  }
+  if ((e = cudaMalloc(&b->scales, 16 * (size_t)g.E)) != cudaSuccess) {
+    if (b->owns_rows) { cudaFree(b->gu); cudaFree(b->dn); }
+    delete b; cudaGetLastError(); return MOE_ENOMEM;
+  }
+  if (scale_bank) {
+    const cudaMemcpyKind kind = (src_kind == MOE_SRC_HOST) ? cudaMemcpyHostToDevice : cudaMemcpyDeviceToDevice;
+    e = cudaMemcpyAsync(b->scales, scale_bank, 16 * (size_t)g.E, kind, s);
+  } else {
+    std::vector<float> ones(4 * (size_t)g.E, 1.0f);
+    e = cudaMemcpyAsync(b->scales, ones.data(), 16 * (size_t)g.E, cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  }
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) {
+    if (b->owns_rows) { cudaFree(b->gu); cudaFree(b->dn); }
+    cudaFree(b->scales); delete b; return cuda_fail(e, "bank create");
+  }
+  *out = b;
+  return MOE_OK;
+}
+
+int moe_bank_destroy(moe_bank* b) {
+  if (!b) return MOE_OK;
+  cudaDeviceSynchronize();
+  if (b->owns_rows) { cudaFree(b->gu); cudaFree(b->dn); }
+  cudaFree(b->scales);
+  delete b;
+  return MOE_OK;
+}
+
+int moe_bank_geometry(const moe_bank* b, moe_layer_geom* out) {
+  if (!b || !out) return MOE_EINVAL;
+  *out = b->geom;
+  return MOE_OK;
+}
+
+size_t moe_workspace_bytes(const moe_bank* b, int32_t max_tokens) {
+  if (!b || max_tokens < 1) return 0;
+  const Shape sh = decode_shape(b->geom);
+  const int t = max_tokens < sh.t_chunk ? max_tokens : sh.t_chunk;
+  return ws_layout(b->geom, t).total;
+}
+
+int moe_workspace_init(void* ws, size_t ws_bytes, void* stream) {
+  if (!ws || ws_bytes < 256 || !aligned(ws, 256)) return MOE_EINVAL;
+  cudaError_t e = cudaMemsetAsync(ws, 0, ws_bytes, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MOE_OK : cuda_fail(e, "workspace init");
+}
+
+static int decode_impl(const moe_bank* b, const void* x, int32_t T, const int32_t* ids, const float* w, void* out,
+                       void* ws, size_t ws_bytes, void* stream, int* chunk_T) {
+  if (!b || T < 0) return MOE_EINVAL;
+  if (T == 0) return MOE_OK;
+  if (!x || !ids || !w || !out || !ws) return MOE_EINVAL;
+  if (!aligned(x, 16) || !aligned(out, 4) || !aligned(ids, 4) || !aligned(w, 4) || !aligned(ws, 256))
+    return MOE_EINVAL;
+  const moe_layer_geom& g = b->geom;
+  const Shape sh = decode_shape(g);
+  const int tc = T < sh.t_chunk ? T : sh.t_chunk;
+  if (chunk_T) *chunk_T = tc;
+  if (ws_bytes < ws_layout(g, tc).total) return MOE_EINVAL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  for (int t0 = 0; t0 < T; t0 += tc) {
+    const int tn = (T - t0) < tc ? (T - t0) : tc;
+    const WsLayout L = ws_layout(g, tn);
+    DecodeParams p = make_params(b, L, static_cast<uint8_t*>(ws), sh, tn);
+    p.x = static_cast<const uint16_t*>(x) + (size_t)t0 * g.H;
+    p.ids = ids + (size_t)t0 * g.top_k;
+    p.w = w + (size_t)t0 * g.top_k;
+    p.out = static_cast<uint16_t*>(out) + (size_t)t0 * g.H;
+    cudaError_t e;
+    if ((e = launch_prep(p, s)) != cudaSuccess) return cuda_fail(e, "prep launch");
+    if ((e = launch_gate_up(p, s)) != cudaSuccess) return cuda_fail(e, "gate_up launch");
+    if ((e = launch_down(p, s)) != cudaSuccess) return cuda_fail(e, "down launch");
+  }
+  return MOE_OK;
+}
+
+int moe_decode(const moe_bank* b, const void* x, int32_t T, const int32_t* ids, const float* w, void* out, void* ws,
+               size_t ws_bytes, void* stream) {
+  return decode_impl(b, x, T, ids, w, out, ws, ws_bytes, stream, nullptr);
+}
+
+int moe_get_error(void* ws, size_t ws_bytes, void* stream, int32_t* dev_err) {
+  if (!ws || ws_bytes < 4 || !dev_err) return MOE_EINVAL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint32_t v = 0;
+  cudaError_t e = cudaMemcpyAsync(&v, ws, 4, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e == cudaSuccess && v) e = cudaMemsetAsync(ws, 0, 4, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "get_error");
+  *dev_err = (int32_t)v;
+  return v ? MOE_EDEVICE : MOE_OK;
+}
+
+int moe_quantize_q8_1(const float* x, int64_t n, void* out_blocks, void* stream) {
+  if (!x || !out_blocks || n < 0 || n % 32 != 0 || !aligned(x, 4) || !aligned(out_blocks, 4)) return MOE_EINVAL;
+  cudaError_t e = launch_quantize_q8_1_blocks(x, n, static_cast<uint8_t*>(out_blocks),
+                                              static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MOE_OK : cuda_fail(e, "quantize_q8_1");
+}
+
+int moe_debug_block_dots(int32_t type, const void* rows, int32_t nrows, int32_t k, const void* act, int32_t* out,
+                         void* stream) {
+  if (!rows || !act || !out || nrows < 0 || k <= 0) return MOE_EINVAL;
+  if (type != MOE_Q8_0 && type != MOE_Q4_K && type != MOE_NVFP4) return MOE_EINVAL;
+  if (row_bytes_of(type, k) == 0 || !aligned(rows, 16) || !aligned(act, 4) || !aligned(out, 4)) return MOE_EINVAL;
+  cudaError_t e = launch_block_dots(type, static_cast<const uint8_t*>(rows), nrows, k,
+                                    static_cast<const uint8_t*>(act), out, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MOE_OK : cuda_fail(e, "block_dots");
+}
+
+int moe_debug_decode_stages(const moe_bank* b, const void* x, int32_t T, const int32_t* ids, const float* w,
+                            void* out, void* ws, size_t ws_bytes, void* stream, void* x_blocks, float* inter,
+                            void* inter_blocks) {
+  if (!b) return MOE_EINVAL;
+  const Shape sh = decode_shape(b->geom);
+  if (T > sh.t_chunk) return MOE_EINVAL;
+  int st = decode_impl(b, x, T, ids, w, out, ws, ws_bytes, stream, nullptr);
+  if (st || T == 0) return st;
+  const moe_layer_geom& g = b->geom;
+  const WsLayout L = ws_layout(g, T);
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaSuccess;
+  const int64_t RT = (int64_t)T * g.top_k;
+  if (x_blocks && g.gate_up_type != MOE_BF16)
+    e = launch_export_q8(reinterpret_cast<int8_t*>(base + L.xq), reinterpret_cast<float*>(base + L.xd),
+                         reinterpret_cast<uint16_t*>(base + L.xsh), (int64_t)T * (g.H / 32),
+                         static_cast<uint8_t*>(x_blocks), s);
+  if (e == cudaSuccess && inter)
+    e = cudaMemcpyAsync(inter, base + L.inter, 4 * (size_t)RT * g.I, cudaMemcpyDeviceToDevice, s);
+  if (e == cudaSuccess && inter_blocks && g.down_type != MOE_BF16)
+    e = launch_export_q8(reinterpret_cast<int8_t*>(base + L.iq), reinterpret_cast<float*>(base + L.id),
+                         reinterpret_cast<uint16_t*>(base + L.ish), RT * (g.I / 32),
+                         static_cast<uint8_t*>(inter_blocks), s);
+  return e == cudaSuccess ? MOE_OK : cuda_fail(e, "debug export");
+}
+
+}  // extern "C"

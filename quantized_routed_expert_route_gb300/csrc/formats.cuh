@@ -1,0 +1,187 @@
+// Block formats of the expert banks and activations, as device functions.
+//
+// One "block" is 32 consecutive values of a row (8 for BF16 rows).  Each
+// quantized type decodes a block into int8x4 words that line up with the
+// q8_1 activation words, so the integer part of a block dot is a run of
+// dp4a instructions; the float part applies the block scales.  These are the
+// only definitions of the formats on the GPU side: the decode kernels and the
+// block-dot test hook both call them.
+//
+// Formats (FreeToken PR #704, "How it plugs into the CPU executor";
+// FreeToken issue #194, "Reproduction geometry"; Strata PR #292,
+// "Summary/Pipeline"):
+//   q8_1  : 32 int8 q, fp16 d, fp16 s; value q*d.
+//   Q8_0  : fp16 d then 32 int8 (34 bytes); value d*q.
+//   Q4_K  : 144-byte super-block of 256: fp16 d, fp16 dmin, 12 packed 6-bit
+//           (sc, m) bytes, 128 code bytes; value d*sc_j*q - dmin*m_j.
+//   NVFP4 : row = K/2 E2M1 code bytes (element 2i low nibble of byte i) then
+//           K/16 UE4M3 scale bytes; value E2M1(code)*UE4M3(scale).
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "ptx.cuh"
+
+namespace qre {
+
+enum WType : int { W_BF16 = 0, W_Q8_0 = 1, W_Q4_K = 2, W_NVFP4 = 3 };
+
+__host__ __device__ inline int row_bytes_of(int t, int k) {
+  switch (t) {
+    case W_BF16: return (k % 32 == 0) ? 2 * k : 0;
+    case W_Q8_0: return (k % 32 == 0) ? (k / 32) * 34 : 0;
+    case W_Q4_K: return (k % 256 == 0) ? (k / 256) * 144 : 0;
+    case W_NVFP4: return (k % 32 == 0) ? k / 2 + k / 16 : 0;
+  }
+  return 0;
+}
+
+// ------------------------------------------------------------------ q8_1
+
+// A q8_1 activation block as the dot loops hold it: the 32 codes as eight
+// int8x4 words in value order, d decoded from its fp16 copy, and the exact
+// integer sum of the codes (for the Q4_K min term).
+struct ActQ8 {
+  int q[8];
+  float d;
+  int sum;
+};
+
+// Quantize one 32-value block held one value per lane of a full warp:
+// d = amax/127 (IEEE fp32 division), q = round-half-even(v/d), 0 when d = 0.
+__device__ __forceinline__ void q8_1_quantize_warp(float v, int& q, float& d, int& sum) {
+  float amax = fabsf(v);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  d = __fdiv_rn(amax, 127.0f);
+  q = (d == 0.0f) ? 0 : __float2int_rn(__fdiv_rn(v, d));
+  sum = __reduce_add_sync(0xffffffffu, q);
+}
+
+// Internal q8_1 storage is planar: codes [rows][n] int8, d [rows][n/32] fp32
+// (an fp16 value), exact code sum [rows][n/32] int32, s [rows][n/32] fp16 bits.
+__device__ __forceinline__ ActQ8 load_act_q8(const int8_t* q, const float* d, const int* sum, size_t row_vals,
+                                             size_t row_blocks, int blk) {
+  ActQ8 a;
+  const int4* p = reinterpret_cast<const int4*>(q + row_vals + 32 * (size_t)blk);
+  const int4 lo = __ldg(p), hi = __ldg(p + 1);
+  a.q[0] = lo.x; a.q[1] = lo.y; a.q[2] = lo.z; a.q[3] = lo.w;
+  a.q[4] = hi.x; a.q[5] = hi.y; a.q[6] = hi.z; a.q[7] = hi.w;
+  a.d = __ldg(d + row_blocks + blk);
+  a.sum = __ldg(sum + row_blocks + blk);
+  return a;
+}
+
+// ------------------------------------------------------------------ NVFP4
+
+// |2*E2M1| for codes 0..7 as bytes: {0,1,2,3,4,6,8,12}.
+constexpr uint32_t kE2M1x2Lo = 0x03020100u;
+constexpr uint32_t kE2M1x2Hi = 0x0C080604u;
+
+// Decode the 32 codes of block b (16 bytes) into magnitude words split by
+// sign: pos[w] holds |2*value| of the non-negative codes of elements
+// 4w..4w+3 (0 for negative codes), neg[w] those of the negative codes.  The
+// split comes free from prmt: a selector nibble with its top bit set yields
+// the replicated sign of a non-negative table byte, i.e. 0.
+__device__ __forceinline__ void nvfp4_decode(const uint8_t* row, int k, int b, uint32_t (&pos)[8],
+                                             uint32_t (&neg)[8], float2& scales) {
+  // A row is 9k/16 bytes: 16-byte aligned when k is a multiple of 256, else
+  // only 2-byte aligned, and then the codes are gathered 2 bytes at a time.
+  const uint8_t* cp = row + 16 * b;
+  uint4 c;
+  if ((reinterpret_cast<uintptr_t>(cp) & 15u) == 0) {
+    c = lds128(cp);
+  } else {
+    c.x = lds16(cp) | ((uint32_t)lds16(cp + 2) << 16);
+    c.y = lds16(cp + 4) | ((uint32_t)lds16(cp + 6) << 16);
+    c.z = lds16(cp + 8) | ((uint32_t)lds16(cp + 10) << 16);
+    c.w = lds16(cp + 12) | ((uint32_t)lds16(cp + 14) << 16);
+  }
+  const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    const uint32_t qv = cw[w], qx = qv ^ 0x88888888u;
+    pos[2 * w] = prmt(kE2M1x2Lo, kE2M1x2Hi, qv);
+    neg[2 * w] = prmt(kE2M1x2Lo, kE2M1x2Hi, qx);
+    pos[2 * w + 1] = prmt(kE2M1x2Lo, kE2M1x2Hi, qv >> 16);
+    neg[2 * w + 1] = prmt(kE2M1x2Lo, kE2M1x2Hi, qx >> 16);
+  }
+  scales = ue4m3x2_to_float2(lds16(row + (k >> 1) + 2 * b));
+}
+
+// Integer dots of the two 16-value halves: sum((2*E2M1) * q).
+__device__ __forceinline__ void nvfp4_int_dots(const uint32_t (&pos)[8], const uint32_t (&neg)[8], const int (&q)[8],
+                                               int& d0, int& d1) {
+  int p0 = 0, n0 = 0, p1 = 0, n1 = 0;
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    p0 = __dp4a((int)pos[w], q[w], p0);
+    n0 = __dp4a((int)neg[w], q[w], n0);
+    p1 = __dp4a((int)pos[w + 4], q[w + 4], p1);
+    n1 = __dp4a((int)neg[w + 4], q[w + 4], n1);
+  }
+  d0 = p0 - n0;
+  d1 = p1 - n1;
+}
+
+// ------------------------------------------------------------------ Q4_K
+
+// Decode sub-block b (32 values) of a Q4_K row: the codes as int8x4 words in
+// value order, and the fp32 factors d*sc_j and dmin*m_j (both exact).
+__device__ __forceinline__ void q4k_decode(const uint8_t* row, int b, int (&nib)[8], float& dsc, float& dmm) {
+  const uint8_t* sb = row + (b >> 3) * 144;
+  const int j = b & 7;
+  const uint4 hdr = lds128(sb);  // x: d | dmin << 16, y: scales[0..3], z: scales[4..7], w: scales[8..11]
+  const float d = f16_bits_to_f32(hdr.x & 0xFFFFu);
+  const float dmin = f16_bits_to_f32(hdr.x >> 16);
+  uint32_t sc, m;
+  if (j < 4) {
+    sc = (hdr.y >> (8 * j)) & 63u;
+    m = (hdr.z >> (8 * j)) & 63u;
+  } else {
+    const int jj = j - 4;
+    const uint32_t s8 = (hdr.w >> (8 * jj)) & 0xFFu;
+    sc = (s8 & 15u) | (((hdr.y >> (8 * jj + 6)) & 3u) << 4);
+    m = (s8 >> 4) | (((hdr.z >> (8 * jj + 6)) & 3u) << 4);
+  }
+  const uint8_t* qs = sb + 16 + (j >> 1) * 32;
+  const uint4 q0 = lds128(qs), q1 = lds128(qs + 16);
+  const int sh = (j & 1) * 4;
+  const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+#pragma unroll
+  for (int i = 0; i < 8; ++i) nib[i] = (int)((w[i] >> sh) & 0x0F0F0F0Fu);
+  dsc = d * (float)sc;
+  dmm = dmin * (float)m;
+}
+
+__device__ __forceinline__ int int_dot8(const int (&w)[8], const int (&q)[8]) {
+  int s = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) s = __dp4a(w[i], q[i], s);
+  return s;
+}
+
+// ------------------------------------------------------------------ Q8_0
+
+// Block b of a Q8_0 row (34-byte blocks, 2-byte aligned in shared memory).
+__device__ __forceinline__ void q8_0_decode(const uint8_t* row, int b, int (&w)[8], float& d) {
+  const uint8_t* blk = row + 34 * b;
+  d = f16_bits_to_f32(lds16(blk));
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint32_t lo = lds16(blk + 2 + 4 * i), hi = lds16(blk + 4 + 4 * i);
+    w[i] = (int)(lo | (hi << 16));
+  }
+}
+
+// ------------------------------------------------------------------ BF16
+
+// 8 bf16 values (16 bytes) -> fp32 (exact).
+__device__ __forceinline__ void bf16x8_to_f32(const uint4 v, float (&f)[8]) {
+  f[0] = __uint_as_float(v.x << 16); f[1] = __uint_as_float(v.x & 0xFFFF0000u);
+  f[2] = __uint_as_float(v.y << 16); f[3] = __uint_as_float(v.y & 0xFFFF0000u);
+  f[4] = __uint_as_float(v.z << 16); f[5] = __uint_as_float(v.z & 0xFFFF0000u);
+  f[6] = __uint_as_float(v.w << 16); f[7] = __uint_as_float(v.w & 0xFFFF0000u);
+}
+
+}  // namespace qre

@@ -1,0 +1,65 @@
+// Internal declarations shared by the C-ABI layer and the kernels.
+#pragma once
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+namespace qre {
+
+constexpr int kMaxE = 1024;
+constexpr int kMaxTopK = 32;
+constexpr int kTChunk = 64;
+
+// Everything one decode pass (at most kTChunk tokens) needs, by value in
+// kernel parameter space.
+struct DecodeParams {
+  int H, I, E, K, T;
+  int gu_type, dn_type;
+  int rb_gu, rb_dn;
+  const uint8_t* gu_bank;  // [E][2I][rb_gu]
+  const uint8_t* dn_bank;  // [E][H][rb_dn]
+  const float* scales;     // [E][4]
+  const uint16_t* x;       // bf16 [T][H]
+  const int32_t* ids;      // [T][K]
+  const float* w;          // [T][K]
+  uint16_t* out;           // bf16 [T][H]
+  // workspace
+  uint32_t* err;
+  int8_t* xq; float* xd; int* xsum; uint16_t* xsh;   // q8_1 of x: [T][H], [T][H/32]
+  float* inter;                                         // [T*K][I]
+  int8_t* iq; float* id; int* isum; uint16_t* ish;   // q8_1 of inter: [T*K][I], [T*K][I/32]
+  unsigned* cnt;                                        // [min(E, T*K)][I/32]
+  int cnt_len;
+  // launch shape
+  int g_gu, g_dn;          // grid sizes
+  int ps;                  // gate_up pairs per stage
+  int gu_up_off;           // byte offset of the up rows inside a gate_up stage buffer
+  int gu_stage_bytes, gu_nstage;
+  int dn_rows_max;         // max rows per down CTA
+  int dn_rs;               // rows per down stage piece
+  int dn_slots_per_stage;
+  int dn_piece_bytes;      // bytes reserved per (slot, row piece) inside a down stage
+  int dn_stage_bytes, dn_nstage;
+  int w0;                  // gate_up cost model: cost per pair = w0 + tokens of the expert
+};
+
+// Sizes of the dynamic shared memory of each kernel for these params.
+size_t gate_up_smem_bytes(const DecodeParams& p);
+size_t down_smem_bytes(const DecodeParams& p);
+
+// Launches (all with programmatic dependent launch on `stream`).
+cudaError_t launch_prep(const DecodeParams& p, cudaStream_t stream);
+cudaError_t launch_gate_up(const DecodeParams& p, cudaStream_t stream);
+cudaError_t launch_down(const DecodeParams& p, cudaStream_t stream);
+
+// Test hooks.
+cudaError_t launch_quantize_q8_1_blocks(const float* x, int64_t n, uint8_t* out, cudaStream_t stream);
+cudaError_t launch_block_dots(int type, const uint8_t* rows, int nrows, int k, const uint8_t* act,
+                              int32_t* out, cudaStream_t stream);
+cudaError_t launch_export_q8(const int8_t* q, const float* d, const uint16_t* s, int64_t nblocks,
+                             uint8_t* out, cudaStream_t stream);
+
+int sm_count();
+
+}  // namespace qre

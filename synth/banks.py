@@ -160,6 +160,42 @@ def q8_0_codes_bank(seed: int, rows: int, k: int) -> np.ndarray:
     return out.reshape(rows, nb * 34)
 
 
+def converted_expert(seed: int, e: int, H: int, I: int, gate_up_type: int, down_type: int):
+    """One converted expert: (gate_up uint8 [2I, rb_gu], down uint8 [H, rb_d],
+    scales fp32 [4]).  Weights ~ N(0, 0.02) (Q8_0: the direct code recipe);
+    NVFP4 projections get s2 = amax / (6 * 448) each (gate, up, down)."""
+    r = rng(seed * 100003 + e)
+    sc = np.ones(4, dtype=np.float32)
+    if gate_up_type == Q8_0:
+        gu = q8_0_codes_bank(seed * 100003 + e, 2 * I, H)
+    else:
+        wg = (r.standard_normal((2 * I, H)) * 0.02).astype(np.float32)
+        if gate_up_type == NVFP4:
+            parts = []
+            for p, (a, b) in enumerate(((0, I), (I, 2 * I))):
+                s2 = np.float32(np.abs(wg[a:b]).max() / np.float32(6.0 * 448.0))
+                sc[p] = s2
+                parts.append(convert_nvfp4(wg[a:b], s2))
+            gu = np.concatenate(parts, axis=0)
+        elif gate_up_type == Q4_K:
+            gu = convert_q4k(wg)
+        else:
+            gu = convert_bf16(wg)
+    if down_type == Q8_0:
+        dn = q8_0_codes_bank(seed * 100003 + e + 50000, H, I)
+    else:
+        wd = (r.standard_normal((H, I)) * 0.02).astype(np.float32)
+        if down_type == NVFP4:
+            s2 = np.float32(np.abs(wd).max() / np.float32(6.0 * 448.0))
+            sc[2] = s2
+            dn = convert_nvfp4(wd, s2)
+        elif down_type == Q4_K:
+            dn = convert_q4k(wd)
+        else:
+            dn = convert_bf16(wd)
+    return gu, dn, sc
+
+
 def converted_layer(seed: int, H: int, I: int, E: int, gate_up_type: int, down_type: int,
                     experts=None, filler_seed: int | None = None):
     """A converted layer: (gate_up uint8 [E, 2I, rb_gu], down uint8 [E, H, rb_d],
@@ -184,32 +220,7 @@ def converted_layer(seed: int, H: int, I: int, E: int, gate_up_type: int, down_t
         gu[:] = counter.bank_bytes_np(fs, gate_up_type, H, 0, E * 2 * I).reshape(E, 2 * I, rb_gu)
         dn[:] = counter.bank_bytes_np(fs + 1, down_type, I, 0, E * H).reshape(E, H, rb_d)
     for e in todo:
-        r = rng(seed * 100003 + e)
-        if gate_up_type == Q8_0:
-            gu[e] = q8_0_codes_bank(seed * 100003 + e, 2 * I, H)
-        else:
-            wg = (r.standard_normal((2 * I, H)) * 0.02).astype(np.float32)
-            if gate_up_type == NVFP4:
-                for p, (a, b) in enumerate(((0, I), (I, 2 * I))):
-                    s2 = np.float32(np.abs(wg[a:b]).max() / np.float32(6.0 * 448.0))
-                    sb[e, p] = s2
-                    gu[e, a:b] = convert_nvfp4(wg[a:b], s2)
-            elif gate_up_type == Q4_K:
-                gu[e] = convert_q4k(wg)
-            else:
-                gu[e] = convert_bf16(wg)
-        if down_type == Q8_0:
-            dn[e] = q8_0_codes_bank(seed * 100003 + e + 50000, H, I)
-        else:
-            wd = (r.standard_normal((H, I)) * 0.02).astype(np.float32)
-            if down_type == NVFP4:
-                s2 = np.float32(np.abs(wd).max() / np.float32(6.0 * 448.0))
-                sb[e, 2] = s2
-                dn[e] = convert_nvfp4(wd, s2)
-            elif down_type == Q4_K:
-                dn[e] = convert_q4k(wd)
-            else:
-                dn[e] = convert_bf16(wd)
+        gu[e], dn[e], sb[e] = converted_expert(seed, e, H, I, gate_up_type, down_type)
     return gu, dn, sb
 
 

@@ -1,0 +1,64 @@
+"""The C-ABI library without a GPU: it builds, loads, exports every function
+include/qre_moe.h declares, and its host-side checks answer as documented
+(no call here launches a kernel)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from oracle import formats as F
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def capi():
+    from quantized_routed_expert_route_gb300 import build
+    if not os.path.exists(build.lib_path()):
+        build.build()
+    from quantized_routed_expert_route_gb300 import capi as c
+    return c
+
+
+def _declared_functions():
+    txt = open(os.path.join(ROOT, "include", "qre_moe.h")).read()
+    txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z0-9_]+)\s*\(", txt)))
+
+
+def test_every_declared_symbol_is_exported(capi):
+    decl = _declared_functions()
+    assert len(decl) >= 13
+    lib = capi.library()
+    for name in decl:
+        assert hasattr(lib, name), name
+    assert sorted(capi.EXPORTS) == decl
+
+
+def test_row_bytes_agree_with_the_oracle(capi):
+    for t in (F.TYPE_BF16, F.TYPE_Q8_0, F.TYPE_Q4_K, F.TYPE_NVFP4):
+        for k in (32, 96, 256, 768, 2048, 4096, 100):
+            assert capi.moe_row_bytes(t, k) == F.row_bytes(t, k), (t, k)
+    assert capi.moe_row_bytes(7, 256) == 0
+
+
+def test_host_argument_checks(capi):
+    lib = capi.library()
+    g = capi.moe_layer_geom(256, 128, 8, 2, capi.MOE_Q8_0, capi.MOE_Q8_0)
+    out = ctypes.c_void_p()
+    # null rows, wrong byte counts, bad geometry: refused before any CUDA call
+    assert lib.moe_bank_create(ctypes.byref(g), None, 0, None, 0, None, 0, None, ctypes.byref(out)) == capi.MOE_EINVAL
+    buf = (ctypes.c_uint8 * 16)()
+    assert lib.moe_bank_create(ctypes.byref(g), buf, 16, buf, 16, None, 0, None, ctypes.byref(out)) == capi.MOE_EINVAL
+    bad = capi.moe_layer_geom(256, 128, 8, 9, capi.MOE_Q8_0, capi.MOE_Q8_0)     # top_k > E
+    assert lib.moe_bank_create(ctypes.byref(bad), buf, 16, buf, 16, None, 0, None, ctypes.byref(out)) == capi.MOE_EINVAL
+    bad = capi.moe_layer_geom(300, 128, 8, 2, capi.MOE_Q4_K, capi.MOE_Q8_0)     # H not a whole super-block
+    assert lib.moe_bank_create(ctypes.byref(bad), buf, 16, buf, 16, None, 0, None, ctypes.byref(out)) == capi.MOE_EINVAL
+    assert out.value is None
+    assert lib.moe_decode(None, None, 1, None, None, None, None, 0, None) == capi.MOE_EINVAL
+    assert lib.moe_quantize_q8_1(None, 32, None, None) == capi.MOE_EINVAL
+    assert lib.moe_debug_block_dots(capi.MOE_BF16, buf, 1, 32, buf, buf, None) == capi.MOE_EINVAL
+    assert lib.moe_workspace_bytes(None, 4) == 0
+    assert lib.moe_bank_destroy(None) == capi.MOE_OK
+    assert capi.status_string(capi.MOE_EDEVICE) == "device-side error flag set"

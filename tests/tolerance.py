@@ -1,0 +1,135 @@
+"""Which GPU results count as correct, derived from the arithmetic.
+
+The GPU computes in fp32 (block contributions accumulated in fp32, SiLU in
+fp32, one bf16 rounding at the end); the oracle computes the same method in
+fp64.  So a GPU output differs from the oracle's fp64 value by at most
+
+  * the fp32 accumulation error of the down dot and the route sum,
+  * for a BF16 down type, the fp32 error of the intermediate carried through
+    the down dot,
+  * for a quantized down type, the q8_1 codes of the intermediate that the
+    fp32 and fp64 intermediates may legitimately round differently: a code
+    whose pre-rounding value lies within the intermediate's fp32 error of a
+    rounding boundary may go either way (and a block scale d whose fp16
+    rounding is equally ambiguous may shift the whole block),
+  * and the final bf16 rounding.
+
+``output_bounds`` turns those into a per-element bound beta (before the bf16
+rounding).  ``check_output`` then asserts: every GPU value is within beta plus
+half a bf16 spacing of the oracle's fp64 value; wherever every value within
+beta of the oracle's value rounds to the same bf16 number, the GPU value is
+that number bit for bit; and the aggregate errors against the oracle's bf16
+output meet the stated tolerances (max |err| / max |ref| <= 2e-3 over the
+elements whose rounding is unambiguous, relative L2 <= 5e-4 over all).
+
+All quantities are computed from the oracle's own stages: no GPU value feeds
+the bounds.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from oracle import formats as F
+
+U32 = 2.0 ** -24
+
+
+def half_ulp_bf16(v):
+    _, ex = np.frexp(np.abs(v))
+    return np.exp2(np.maximum(ex.astype(np.float64) - 9.0, -134.0))
+
+
+def ulp_fp16(v):
+    _, ex = np.frexp(np.abs(v))
+    return np.exp2(np.maximum(ex.astype(np.float64) - 11.0, -24.0))
+
+
+def _inter_error(geom, st, t, k, xh, wgu):
+    """fp32 error bound of the intermediate silu(g)*u of route (t, k)."""
+    I = geom.I
+    e = int(st["ids"][t, k])
+    sg, su = abs(st["scales"][e, 0]), abs(st["scales"][e, 1])
+    hg, hu = wgu[:I] @ xh, wgu[I:] @ xh
+    g, u = hg * st["scales"][e, 0], hu * st["scales"][e, 1]
+    Sg = sg * (np.abs(wgu[:I]) @ np.abs(xh))
+    Su = su * (np.abs(wgu[I:]) @ np.abs(xh))
+    nblk = geom.H // 32
+    eps_h = 2.0 * (nblk + 40) * U32             # per-lane sequential sums, warp tree, scale products
+    with np.errstate(over="ignore"):
+        sig = 1.0 / (1.0 + np.exp(-g))
+    silu = g * sig
+    dsilu = np.abs(sig * (1.0 + g * (1.0 - sig)))
+    a = silu * u
+    return dsilu * np.abs(u) * eps_h * Sg + np.abs(silu) * eps_h * Su + 16 * U32 * np.abs(a) + 1e-30
+
+
+def output_bounds(geom, st):
+    """beta [T, H]: bound on |gpu_fp32_out - oracle_fp64_out| before bf16 rounding,
+    plus per-route data for the intermediate checks."""
+    T, K, H, I = st["ids"].shape[0], geom.top_k, geom.H, geom.I
+    quant_down = geom.down_type != F.TYPE_BF16
+    beta = np.zeros((T, H))
+    inter_err = np.zeros((T, K, I))
+    amb = np.zeros((T, K, I), dtype=bool)
+    nbd = I // 32
+    for t in range(T):
+        xh = st["x_hat"][t]
+        for k in range(K):
+            if not st["valid"][t, k]:
+                continue
+            e = int(st["ids"][t, k])
+            wgu, wd = st["experts"][e]
+            sws = abs(st["scales"][e, 2] * st["w"][t, k])
+            da = _inter_error(geom, st, t, k, xh, wgu)
+            inter_err[t, k] = da
+            a = st["inter"][t, k]
+            c_dn = 2.0 * (nbd + 40) * U32
+            absW = np.abs(wd)
+            if quant_down:
+                a32 = a.astype(np.float32).astype(np.float64).reshape(nbd, 32)
+                amax = np.abs(a32).max(axis=1)
+                d = amax / 127.0
+                dblk = (da.reshape(nbd, 32).max(axis=1) + U32 * amax) / 127.0 + 2 * U32 * d
+                qinfo = st["inter_act"][t][k]
+                q = qinfo["qs"].astype(np.float64)                      # [nbd, 32]
+                dh = F.fp16_bits_to_f64(qinfo["d"])                     # [nbd]
+                with np.errstate(divide="ignore", invalid="ignore"):
+                    ratio = np.where(d[:, None] > 0, a32 / d[:, None], 0.0)
+                    eta = np.where(d[:, None] > 0, (da.reshape(nbd, 32) + np.abs(q) * dblk[:, None]) / d[:, None], 0.0)
+                frac = np.abs(ratio - np.floor(ratio) - 0.5)
+                amb_code = frac <= eta + 8 * U32 * np.abs(ratio)
+                u16 = ulp_fp16(d)
+                mid_dist = np.abs(d - (np.floor(d / u16) + 0.5) * u16)
+                amb_d = mid_dist <= dblk
+                flip = (amb_code * dh[:, None]
+                        + amb_d[:, None] * (np.abs(q) + 1.0) * u16[:, None]).reshape(I)
+                amb[t, k] = (amb_code | amb_d[:, None]).reshape(I)
+                ahat = st["inter_hat"][t, k]
+                beta[t] += sws * (absW @ flip + c_dn * (absW @ np.abs(ahat)))
+            else:
+                beta[t] += sws * (absW @ da + c_dn * (absW @ np.abs(a)))
+            beta[t] += (K + 8) * U32 * np.abs(st["y"][t, k])
+    return beta, inter_err, amb
+
+
+def check_output(out_bits, ref, beta, max_rel_tol=2e-3, l2_tol=5e-4):
+    """Assert the GPU bf16 output against the oracle; returns the figures."""
+    gpu = F.bf16_bits_to_f64(np.asarray(out_bits, dtype=np.uint16)).reshape(ref.shape)
+    ref16 = F.round_to_bf16(ref)
+    bound = beta + half_ulp_bf16(np.abs(ref) + beta) * (1 + 1e-9) + 1e-30
+    err = np.abs(gpu - ref)
+    bad = err > bound
+    assert not bad.any(), (
+        f"{int(bad.sum())} outputs outside the derived bound; worst excess "
+        f"{float((err - bound)[bad].max()):.3e} at {np.argwhere(bad)[:5].tolist()}")
+    unique = F.round_to_bf16(ref - beta) == F.round_to_bf16(ref + beta)
+    mism = unique & (gpu != ref16)
+    assert not mism.any(), f"{int(mism.sum())} outputs differ from an unambiguous bf16 rounding"
+    scale = max(np.abs(ref).max(), 1e-30)
+    max_rel_all = float(np.abs(gpu - ref16).max() / scale)
+    max_rel_unique = float((np.abs(gpu - ref16) * unique).max() / scale)
+    rel_l2 = float(np.linalg.norm(gpu - ref16) / max(np.linalg.norm(ref16), 1e-30))
+    assert max_rel_unique <= max_rel_tol, max_rel_unique
+    assert rel_l2 <= l2_tol, rel_l2
+    return {"max_rel_unique": max_rel_unique, "max_rel_all": max_rel_all, "rel_l2": rel_l2,
+            "ambiguous_frac": float(1 - unique.mean())}
