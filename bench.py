@@ -108,20 +108,19 @@ class ClockSampler:
 # ------------------------------------------------------------------ stacks of layers on the device
 
 class Stack:
-    """NL resident layers with inputs/outputs and a captured CUDA graph of one step."""
+    """NL resident layers (banks on the device) plus, after ``prepare``, the
+    inputs/outputs of one batch size and a captured CUDA graph of one step."""
 
-    def __init__(self, layer_types, H, I, E, K, T, routing, seed, dev):
+    def __init__(self, layer_types, H, I, E, K, seed, dev):
         import torch
 
         from quantized_routed_expert_route_gb300 import capi
         from synth import banks as S
         from synth import counter as C
-        self.torch, self.capi = torch, capi
-        self.H, self.I, self.E, self.K, self.T = H, I, E, K, T
+        self.torch, self.capi, self.S, self.dev = torch, capi, S, dev
+        self.H, self.I, self.E, self.K = H, I, E, K
         self.NL = len(layer_types)
         self.layers = []
-        self.bytes_per_step = 0
-        self.unique_per_layer = []
         stream = torch.cuda.current_stream().cuda_stream
         for l, (gu_t, dn_t) in enumerate(layer_types):
             rb_gu, rb_dn = row_bytes(gu_t, H), row_bytes(dn_t, I)
@@ -133,25 +132,34 @@ class Stack:
             geom = capi.moe_layer_geom(H, I, E, K, gu_t, dn_t)
             bank = capi.moe_bank_create(geom, gu.data_ptr(), E * 2 * I * rb_gu, dn.data_ptr(), E * H * rb_dn,
                                         sb.data_ptr(), capi.MOE_SRC_DEVICE_BORROW, stream)
-            if routing == "zipf":
-                ids, w = S.zipf_routing(seed * 7 + l, T, E, K)
-            else:
-                ids, w = S.softmax_topk_routing(seed * 7 + l, T, E, K)
-            uniq = len(np.unique(ids))
-            self.unique_per_layer.append(uniq)
-            self.bytes_per_step += uniq * (2 * I * rb_gu + H * rb_dn) + T * H * 2 * 2 + T * K * 8
-            self.layers.append(dict(gu=gu, dn=dn, sb=sb, bank=bank, ids_np=ids, w_np=w,
-                                    ids=torch.from_numpy(ids).to(dev), w=torch.from_numpy(w).to(dev)))
-        ws_bytes = max(capi.moe_workspace_bytes(L["bank"], T) for L in self.layers)
-        self.ws_bytes = ws_bytes
-        self.ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
-        capi.moe_workspace_init(self.ws.data_ptr(), ws_bytes, stream)
-        g = np.random.default_rng(seed)
-        xs = torch.from_numpy(g.standard_normal((self.NL, T, H)).astype(np.float32))
-        self.x = xs.to(torch.bfloat16).to(dev)
-        self.out = torch.empty((self.NL, T, H), dtype=torch.bfloat16, device=dev)
+            self.layers.append(dict(gu=gu, dn=dn, sb=sb, bank=bank, expert_bytes=2 * I * rb_gu + H * rb_dn))
         self.graph = None
         self.stream = torch.cuda.Stream(device=dev)
+
+    def prepare(self, T, routing, seed):
+        torch, capi, S = self.torch, self.capi, self.S
+        self.T = T
+        self.bytes_per_step = 0
+        self.unique_per_layer = []
+        for l, L in enumerate(self.layers):
+            if routing == "zipf":
+                ids, w = S.zipf_routing(seed * 7 + l, T, self.E, self.K)
+            else:
+                ids, w = S.softmax_topk_routing(seed * 7 + l, T, self.E, self.K)
+            uniq = len(np.unique(ids))
+            self.unique_per_layer.append(uniq)
+            self.bytes_per_step += uniq * L["expert_bytes"] + T * self.H * 2 * 2 + T * self.K * 8
+            L["ids"] = torch.from_numpy(ids).to(self.dev)
+            L["w"] = torch.from_numpy(w).to(self.dev)
+        self.ws_bytes = max(capi.moe_workspace_bytes(L["bank"], T) for L in self.layers)
+        self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=self.dev)
+        capi.moe_workspace_init(self.ws.data_ptr(), self.ws_bytes, torch.cuda.current_stream().cuda_stream)
+        g = np.random.default_rng(seed)
+        xs = torch.from_numpy(g.standard_normal((self.NL, T, self.H)).astype(np.float32))
+        self.x = xs.to(torch.bfloat16).to(self.dev)
+        self.out = torch.empty((self.NL, T, self.H), dtype=torch.bfloat16, device=self.dev)
+        self.graph = None
+        self.capture()
 
     def launch_all(self, stream_ptr):
         capi = self.capi
@@ -232,20 +240,23 @@ class Stack:
 
 def cpu_oracle_worker(seconds: float, seed: int = 0) -> dict:
     """Time the oracle on tokens of the headline workload (one NVFP4 layer,
-    T=1, top-8) until `seconds` have elapsed; only the routed experts are
-    generated, and their generation is outside the timed part."""
+    T=1, top-8, the same counter-based bank bytes the GPU bench uses) until
+    `seconds` have elapsed; only the routed experts' rows are generated, and
+    generating them is outside the timed part."""
     from oracle import layer as OL
     from synth import banks as S
+    from synth import counter as C
     c = CFG1
     geom = OL.Geometry(c["H"], c["I"], c["E"], c["K"], c["gu"], c["dn"])
-    done, spent = 0, 0.0
-    t = 0
+    sb = S.counter_scale_bank(seed * 1000, c["E"], c["gu"], c["dn"])
+    done, spent, t = 0, 0.0, 0
     while spent < seconds and done < 64:
         ids, w = S.softmax_topk_routing(seed * 7 + t, 1, c["E"], c["K"])
         x = S.hidden_bf16(seed + t, 1, c["H"])
-        gu, dn, sb = {}, {}, np.ones((c["E"], 4), np.float32)
-        for e in ids.reshape(-1):
-            gu[int(e)], dn[int(e)], sb[int(e)] = S.converted_expert(seed, int(e), c["H"], c["I"], c["gu"], c["dn"])
+        gu, dn = {}, {}
+        for e in (int(v) for v in ids.reshape(-1)):
+            gu[e] = C.bank_bytes_np(seed * 1000, c["gu"], c["H"], e * 2 * c["I"], 2 * c["I"])
+            dn[e] = C.bank_bytes_np(seed * 1000 + 1, c["dn"], c["I"], e * c["H"], c["H"])
         t0 = time.perf_counter()
         OL.moe_layer(geom, gu, dn, sb, x, ids, w)
         spent += time.perf_counter() - t0
@@ -265,6 +276,32 @@ def run_cpu_baseline(seconds: float) -> dict:
         return {"value": None, "unit": "layer-tok/s", "cores": 1, "kind": "oracle",
                 "sample": "failed: " + res.stderr.strip()[-300:]}
     return json.loads(res.stdout.strip().splitlines()[-1])
+
+
+# ------------------------------------------------------------------ profiling driver
+
+def profile_layer(a):
+    """Eager decode passes of one layer for a profiler: the NVFP4 layer
+    (H=2048, I=768, E=128, top-8) or a Laguna-shaped Q4_K / BF16 layer
+    (H=4096, I=768, E=256, top-10, Zipf routing), a stack of --layers banks."""
+    import torch
+    dev = "cuda:0"
+    if a.profile_layer == "nvfp4":
+        c = CFG1
+        st = Stack([(c["gu"], c["dn"])] * a.layers, c["H"], c["I"], c["E"], c["K"], 1, dev)
+        st.prepare(a.T, "softmax", 1)
+    else:
+        t = Q4_K if a.profile_layer == "q4_k" else BF16
+        L = LAGUNA
+        st = Stack([(t, t)] * a.layers, L["H"], L["I"], L["E"], L["K"], 3, dev)
+        st.prepare(a.T, "zipf", 3 + a.T)
+    torch.cuda.synchronize()
+    s = torch.cuda.current_stream().cuda_stream
+    for _ in range(a.steps):
+        st.launch_all(s)
+    torch.cuda.synchronize()
+    st.close()
+    print(json.dumps({"profile_layer": a.profile_layer, "T": a.T, "layers": a.layers, "steps": a.steps}))
 
 
 # ------------------------------------------------------------------ main
@@ -290,7 +327,14 @@ def main():
     ap.add_argument("--no-stack", action="store_true", help="skip the 47-layer Laguna sweep")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--cpu-oracle-worker", type=float, default=None, help=argparse.SUPPRESS)
+    ap.add_argument("--profile-layer", choices=["nvfp4", "q4_k", "bf16"], default=None,
+                    help="run --steps eager decode passes of one layer type (for ncu), print nothing else")
+    ap.add_argument("--T", type=int, default=1)
     a = ap.parse_args()
+
+    if a.profile_layer:
+        profile_layer(a)
+        return
 
     if a.cpu_oracle_worker is not None:
         print(json.dumps(cpu_oracle_worker(a.cpu_oracle_worker)))
@@ -325,8 +369,8 @@ def main():
 
     # headline: NVFP4 layer stack, T=1
     c = CFG1
-    st = Stack([(c["gu"], c["dn"])] * a.layers, c["H"], c["I"], c["E"], c["K"], 1, "softmax", 1, dev)
-    st.capture()
+    st = Stack([(c["gu"], c["dn"])] * a.layers, c["H"], c["I"], c["E"], c["K"], 1, dev)
+    st.prepare(1, "softmax", 1)
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
@@ -345,13 +389,9 @@ def main():
     e2e_val = units / (e2e_ms / 1e3)
     extra = {"per_layer_us": per_pass_ms * 1e3, "bytes_per_layer": st.bytes_per_step / a.layers,
              "unique_experts_per_layer": float(np.mean(st.unique_per_layer))}
-    st.close()
-    del st
-    torch.cuda.empty_cache()
 
-    # NVFP4 layer stack at T=8
-    st = Stack([(c["gu"], c["dn"])] * a.layers, c["H"], c["I"], c["E"], c["K"], 8, "softmax", 2, dev)
-    st.capture()
+    # the same NVFP4 layer stack at T=8
+    st.prepare(8, "softmax", 2)
     ms8 = st.time_replays(max(10, a.steps // 2), a.warmup)
     extra["t8"] = {"layer_tok_per_s": a.layers * 8 / (ms8 / 1e3), "per_layer_us": ms8 / a.layers * 1e3,
                    "hbm_gbs": st.bytes_per_step / (ms8 / 1e3) / 1e9}
@@ -363,20 +403,20 @@ def main():
         L = LAGUNA
         types = [(BF16, BF16) if l % 6 == 0 else (Q4_K, Q4_K) for l in range(47)]
         sweep = {}
+        st = Stack(types, L["H"], L["I"], L["E"], L["K"], 3, dev)
         for T in (1, 4, 16, 64):
-            st = Stack(types, L["H"], L["I"], L["E"], L["K"], T, "zipf", 3, dev)
-            st.capture()
+            st.prepare(T, "zipf", 3 + T)
             msT = st.time_replays(max(5, a.steps // 5), a.warmup)
             sweep[f"T={T}"] = {"stack_tok_per_s": T / (msT / 1e3), "ms_per_stack": msT,
                                "hbm_gbs": st.bytes_per_step / (msT / 1e3) / 1e9,
                                "frac": st.bytes_per_step / (msT / 1e3) / 1e9 / hbm_peak,
                                "gb_per_step": st.bytes_per_step / 1e9}
-            st.close()
-            del st
-            torch.cuda.empty_cache()
+        st.close()
+        del st
+        torch.cuda.empty_cache()
         extra["laguna_47_layer_stack"] = sweep
 
-    cpu = run_cpu_baseline(a.cpu_seconds) if rank == 0 else None
+    cpu = run_cpu_baseline(a.cpu_seconds) if (rank == 0 and a.cpu_seconds > 0) else None
     if rank == 0:
         line = {
             "metric": "routed-expert decode throughput (tokens x layers / s); achieved HBM GB/s vs peak",

@@ -54,6 +54,8 @@ struct Shape {
 
 Shape decode_shape(const moe_layer_geom& g) {
   Shape s;
+  // sized for one CTA per SM (the most rows per down CTA); batches of up to
+  // two tokens run two CTAs per SM (make_params)
   s.g_gu = sm_count();
   s.g_dn = sm_count();
   if (s.g_dn > g.H) s.g_dn = g.H;
@@ -113,8 +115,20 @@ DecodeParams make_params(const moe_bank* b, const WsLayout& L, uint8_t* ws, cons
   p.ish = reinterpret_cast<uint16_t*>(ws + L.ish);
   p.cnt = reinterpret_cast<unsigned*>(ws + L.cnt);
   p.cnt_len = L.cnt_len;
+  // Batches of up to two tokens take the two-kernel path (x quantized inside
+  // k_gate_up, the intermediate requantized inside k_down) when the
+  // activations fit in shared memory; larger batches take k_prep + k_gate_up
+  // + k_down.
+  {
+    const size_t RT0 = (size_t)T * g.top_k;
+    const size_t gu_need = (g.gate_up_type == MOE_BF16) ? 2 * (size_t)T * g.H : (size_t)T * g.H * 5 / 4;
+    const size_t dn_need = (g.down_type == MOE_BF16) ? 0 : RT0 * g.I * 5 / 4;
+    p.maxnt = (T <= 2 && gu_need <= 48 * 1024 && dn_need <= 64 * 1024) ? 1 : 4;
+  }
   p.g_gu = sh.g_gu;
   p.g_dn = sh.g_dn;
+  if (p.g_dn > g.H) p.g_dn = g.H;
+  const int rows_max = (g.H + p.g_dn - 1) / p.g_dn;
   // gate_up stages: ~20 KiB of (gate, up) row pairs, ~112 KiB in flight
   int ps = (20 * 1024) / (2 * p.rb_gu);
   if (ps < 1) ps = 1;
@@ -122,20 +136,38 @@ DecodeParams make_params(const moe_bank* b, const WsLayout& L, uint8_t* ws, cons
   p.ps = ps;
   p.gu_up_off = (int)align_up((size_t)ps * p.rb_gu + 16, 128);
   p.gu_stage_bytes = 2 * p.gu_up_off;
-  int ns = (112 * 1024) / p.gu_stage_bytes;
+  int ns = (96 * 1024) / p.gu_stage_bytes;
   p.gu_nstage = ns < 2 ? 2 : (ns > 8 ? 8 : ns);
   // down stages: pieces of <= 24 KiB rows of one expert, grouped to ~32 KiB
-  p.dn_rows_max = sh.rows_max;
+  p.dn_rows_max = rows_max;
   int rs = (24 * 1024) / p.rb_dn;
   if (rs < 1) rs = 1;
-  if (rs > sh.rows_max) rs = sh.rows_max;
+  if (rs > rows_max) rs = rows_max;
   p.dn_rs = rs;
   p.dn_piece_bytes = (int)align_up((size_t)rs * p.rb_dn + 16, 128);
   int sps = (32 * 1024) / p.dn_piece_bytes;
   p.dn_slots_per_stage = sps < 1 ? 1 : (sps > 16 ? 16 : sps);
   p.dn_stage_bytes = p.dn_slots_per_stage * p.dn_piece_bytes;
-  int dns = (96 * 1024) / p.dn_stage_bytes;
+  int dns = (64 * 1024) / p.dn_stage_bytes;
   p.dn_nstage = dns < 2 ? 2 : (dns > 8 ? 8 : dns);
+  // activations staged in shared memory when they fit (always on the two-kernel path)
+  const size_t RT = (size_t)T * g.top_k;
+  const size_t gu_act = (g.gate_up_type == MOE_BF16) ? 2 * (size_t)T * g.H
+                                                     : (size_t)T * g.H + 8 * (size_t)T * (g.H / 32);
+  p.gu_act_smem = (p.maxnt == 1 || gu_act <= 24 * 1024) ? 1 : 0;
+  p.gu_act_bytes = p.gu_act_smem ? (int)align_up(gu_act, 16) : 0;
+  const size_t dn_act = (g.down_type == MOE_BF16) ? 4 * RT * g.I : RT * g.I + 8 * RT * (g.I / 32);
+  p.dn_act_smem = ((p.maxnt == 1 && g.down_type != MOE_BF16) || dn_act <= 24 * 1024) ? 1 : 0;
+  p.dn_act_bytes = p.dn_act_smem ? (int)align_up(dn_act, 16) : 0;
+  // ring depths: no deeper than the stages a CTA is expected to have, and
+  // small enough at low token counts for a down CTA to sit beside a gate_up CTA
+  const size_t U = (size_t)g.E < RT ? (size_t)g.E : RT;
+  const size_t pairs = (U * g.I + p.g_gu - 1) / p.g_gu;
+  int gst = (int)((pairs + ps - 1) / ps) + 2;
+  p.gu_nstage = gst < 2 ? 2 : (gst < p.gu_nstage ? gst : p.gu_nstage);
+  const int dpieces = (rows_max + rs - 1) / rs;
+  int dst = dpieces * (int)((U + p.dn_slots_per_stage - 1) / p.dn_slots_per_stage);
+  p.dn_nstage = dst < 2 ? 2 : (dst < p.dn_nstage ? dst : p.dn_nstage);
   switch (p.gu_type) {
     case W_NVFP4: p.w0 = 2; break;
     case W_Q4_K: p.w0 = 3; break;
@@ -277,7 +309,7 @@ static int decode_impl(const moe_bank* b, const void* x, int32_t T, const int32_
     p.w = w + (size_t)t0 * g.top_k;
     p.out = static_cast<uint16_t*>(out) + (size_t)t0 * g.H;
     cudaError_t e;
-    if ((e = launch_prep(p, s)) != cudaSuccess) return cuda_fail(e, "prep launch");
+    if (p.maxnt != 1 && (e = launch_prep(p, s)) != cudaSuccess) return cuda_fail(e, "prep launch");
     if ((e = launch_gate_up(p, s)) != cudaSuccess) return cuda_fail(e, "gate_up launch");
     if ((e = launch_down(p, s)) != cudaSuccess) return cuda_fail(e, "down launch");
   }

@@ -25,6 +25,8 @@
 namespace qre {
 
 enum WType : int { W_BF16 = 0, W_Q8_0 = 1, W_Q4_K = 2, W_NVFP4 = 3 };
+// Kernel-side variant of W_NVFP4 whose rows (9k/16 bytes) are not 16-byte aligned.
+constexpr int W_NVFP4_U = 4;
 
 __host__ __device__ inline int row_bytes_of(int t, int k) {
   switch (t) {
@@ -47,15 +49,28 @@ struct ActQ8 {
   int sum;
 };
 
-// Quantize one 32-value block held one value per lane of a full warp:
-// d = amax/127 (IEEE fp32 division), q = round-half-even(v/d), 0 when d = 0.
-__device__ __forceinline__ void q8_1_quantize_warp(float v, int& q, float& d, int& sum) {
-  float amax = fabsf(v);
+// Quantize one 32-value block held by one thread: d = amax/127 (IEEE fp32
+// division), q_i = round-half-even(v_i/d) (IEEE fp32 division), 0 when d = 0;
+// returns the 32 codes packed as eight int8x4 words, d, and the exact code
+// sum.  Every q8_1 quantization on the GPU (activations, the intermediate and
+// the test hook) goes through this function.
+__device__ __forceinline__ void q8_1_quantize_block(const float (&v)[32], uint32_t (&qw)[8], float& d, int& sum) {
+  float amax = 0.f;
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
   d = __fdiv_rn(amax, 127.0f);
-  q = (d == 0.0f) ? 0 : __float2int_rn(__fdiv_rn(v, d));
-  sum = __reduce_add_sync(0xffffffffu, q);
+  sum = 0;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) {
+    uint32_t word = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int q = (d == 0.0f) ? 0 : __float2int_rn(__fdiv_rn(v[4 * w + j], d));
+      sum += q;
+      word |= ((uint32_t)(q & 0xFF)) << (8 * j);
+    }
+    qw[w] = word;
+  }
 }
 
 // Internal q8_1 storage is planar: codes [rows][n] int8, d [rows][n/32] fp32
@@ -83,13 +98,15 @@ constexpr uint32_t kE2M1x2Hi = 0x0C080604u;
 // 4w..4w+3 (0 for negative codes), neg[w] those of the negative codes.  The
 // split comes free from prmt: a selector nibble with its top bit set yields
 // the replicated sign of a non-negative table byte, i.e. 0.
+// A row is 9k/16 bytes: 16-byte aligned when k is a multiple of 256, else
+// only 2-byte aligned, and then (kAligned false) the codes are gathered 2
+// bytes at a time.
+template <bool kAligned = true>
 __device__ __forceinline__ void nvfp4_decode(const uint8_t* row, int k, int b, uint32_t (&pos)[8],
                                              uint32_t (&neg)[8], float2& scales) {
-  // A row is 9k/16 bytes: 16-byte aligned when k is a multiple of 256, else
-  // only 2-byte aligned, and then the codes are gathered 2 bytes at a time.
   const uint8_t* cp = row + 16 * b;
   uint4 c;
-  if ((reinterpret_cast<uintptr_t>(cp) & 15u) == 0) {
+  if constexpr (kAligned) {
     c = lds128(cp);
   } else {
     c.x = lds16(cp) | ((uint32_t)lds16(cp + 2) << 16);

@@ -42,6 +42,9 @@ struct DecodeParams {
   int dn_piece_bytes;      // bytes reserved per (slot, row piece) inside a down stage
   int dn_stage_bytes, dn_nstage;
   int w0;                  // gate_up cost model: cost per pair = w0 + tokens of the expert
+  int gu_act_smem, gu_act_bytes;  // stage x's activations in shared memory (bytes reserved)
+  int dn_act_smem, dn_act_bytes;  // stage the intermediate's activations in shared memory
+  int maxnt;               // routes per register-held work item: 1 (small batches) or 4
 };
 
 // Sizes of the dynamic shared memory of each kernel for these params.
