@@ -146,6 +146,29 @@ int moe_decode(const moe_bank* bank, const void* x, int32_t T,
                const int32_t* topk_ids, const float* topk_w, void* out,
                void* ws, size_t ws_bytes, void* stream);
 
+/* moe_decode without a caller-provided workspace, for callers that cannot
+ * allocate device memory: plugins whose host framework owns every device
+ * allocation and hands the library only its own tensors, and latency-critical
+ * serving paths where a cudaMalloc may synchronize the device.  The paper has
+ * no counterpart to this entry point; it exists for those callers.
+ *
+ * The workspace is a fixed MOE_NOALLOC_WS_BYTES array in device memory that
+ * every GPU loading this library holds until the process exits.  The first
+ * call on a device looks up that array's device address (with that device
+ * current); make that first call before any stream capture.  Every call
+ * shares the array and starts by clearing its error word; the array keeps the
+ * last call's contents otherwise.  Calls that overlap on the GPU (on different
+ * streams, or from different threads) race on it, so order them.  Device-side
+ * error bits of these calls are not reported (a bad id still contributes
+ * zero).  Arguments as for moe_decode.  Returns MOE_EINVAL, without launching
+ * anything, when one pass of this call would need more workspace than
+ * MOE_NOALLOC_WS_BYTES (moe_workspace_bytes(bank, T) tells), and never calls
+ * cudaMalloc or cudaFree. */
+enum { MOE_NOALLOC_WS_BYTES = 4 << 20 };
+int moe_decode_noalloc(const moe_bank* bank, const void* x, int32_t T,
+                       const int32_t* topk_ids, const float* topk_w, void* out,
+                       void* stream);
+
 /* Read and clear the workspace's sticky device error bits (synchronizes
  * `stream`).  *dev_err receives the MOE_DEVERR_* bits; returns MOE_EDEVICE if
  * any was set, MOE_OK otherwise. */

@@ -17,13 +17,14 @@ MOE_OK, MOE_EINVAL, MOE_EUNSUPPORTED, MOE_ENOMEM, MOE_ECUDA, MOE_EDEVICE = 0, -1
 MOE_DEVERR_BAD_ID, MOE_DEVERR_TIMEOUT = 1, 2
 MOE_SRC_HOST, MOE_SRC_DEVICE, MOE_SRC_DEVICE_BORROW = 0, 1, 2
 MOE_MAX_E, MOE_MAX_TOPK, MOE_DECODE_T_CHUNK = 1024, 32, 64
+MOE_NOALLOC_WS_BYTES = 4 << 20
 
 # every symbol include/qre_moe.h declares
 EXPORTS = (
     "moe_row_bytes", "moe_bank_create", "moe_bank_destroy", "moe_bank_geometry",
     "moe_workspace_bytes", "moe_workspace_init", "moe_decode", "moe_get_error",
     "moe_status_string", "moe_last_cuda_error", "moe_quantize_q8_1",
-    "moe_debug_block_dots", "moe_debug_decode_stages",
+    "moe_debug_block_dots", "moe_debug_decode_stages", "moe_decode_noalloc",
 )
 
 
@@ -63,6 +64,7 @@ def _load() -> ctypes.CDLL:
         "moe_quantize_q8_1": (ctypes.c_int, [vp, i64, vp, vp]),
         "moe_debug_block_dots": (ctypes.c_int, [i32, vp, i32, i32, vp, vp, vp]),
         "moe_debug_decode_stages": (ctypes.c_int, [vp, vp, i32, vp, vp, vp, vp, sz, vp, vp, vp, vp]),
+        "moe_decode_noalloc": (ctypes.c_int, [vp, vp, i32, vp, vp, vp, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -122,6 +124,11 @@ def moe_workspace_init(ws: int, ws_bytes: int, stream: int = 0) -> None:
 def moe_decode(bank: int, x: int, T: int, topk_ids: int, topk_w: int, out: int, ws: int, ws_bytes: int,
                stream: int = 0) -> None:
     _check(_lib.moe_decode(bank, x, T, topk_ids, topk_w, out, ws, ws_bytes, stream or None), "moe_decode")
+
+
+def moe_decode_noalloc(bank: int, x: int, T: int, topk_ids: int, topk_w: int, out: int, stream: int = 0) -> None:
+    """moe_decode on the library's fixed device workspace (allocates nothing)."""
+    _check(_lib.moe_decode_noalloc(bank, x, T, topk_ids, topk_w, out, stream or None), "moe_decode_noalloc")
 
 
 def moe_get_error(ws: int, ws_bytes: int, stream: int = 0) -> int:

@@ -4,6 +4,7 @@
 
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <new>
 #include <vector>
 
@@ -319,6 +320,57 @@ static int decode_impl(const moe_bank* b, const void* x, int32_t T, const int32_
 int moe_decode(const moe_bank* b, const void* x, int32_t T, const int32_t* ids, const float* w, void* out, void* ws,
                size_t ws_bytes, void* stream) {
   return decode_impl(b, x, T, ids, w, out, ws, ws_bytes, stream, nullptr);
+}
+
+// ------------------------------------------------------------------ decode without allocation
+//
+// The workspace of moe_decode_noalloc: a file-scope device array, so the call
+// itself never allocates.  Host code cannot use `g_noalloc_ws` as a device
+// address (on the host it names a stand-in); the device address is looked up
+// once per device with cudaGetSymbolAddress.
+static __device__ __align__(256) uint8_t g_noalloc_ws[MOE_NOALLOC_WS_BYTES];
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kMaxDevices] = {};
+
+int noalloc_workspace(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "noalloc: cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return MOE_EUNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_noalloc_ws);
+    if (e != cudaSuccess || !ptr) return cuda_fail(e, "noalloc: cudaGetSymbolAddress");
+    g_noalloc_ptr[dev] = ptr;
+  }
+  *out = g_noalloc_ptr[dev];
+  return MOE_OK;
+}
+}  // namespace
+
+int moe_decode_noalloc(const moe_bank* b, const void* x, int32_t T, const int32_t* ids, const float* w, void* out,
+                       void* stream) {
+  if (!b || T < 0) return MOE_EINVAL;
+  if (T == 0) return MOE_OK;
+  const Shape sh = decode_shape(b->geom);
+  const int tc = T < sh.t_chunk ? T : sh.t_chunk;
+  if (ws_layout(b->geom, tc).total > (size_t)MOE_NOALLOC_WS_BYTES) {
+    std::snprintf(g_cuda_err, sizeof(g_cuda_err),
+                  "moe_decode_noalloc: %zu workspace bytes needed, the static workspace holds %d",
+                  ws_layout(b->geom, tc).total, (int)MOE_NOALLOC_WS_BYTES);
+    return MOE_EINVAL;
+  }
+  void* ws = nullptr;
+  int st = noalloc_workspace(&ws);
+  if (st) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemsetAsync(ws, 0, 256, s);   // the error word starts each call at zero
+  if (e != cudaSuccess) return cuda_fail(e, "noalloc: clear error word");
+  return decode_impl(b, x, T, ids, w, out, ws, (size_t)MOE_NOALLOC_WS_BYTES, stream, nullptr);
 }
 
 int moe_get_error(void* ws, size_t ws_bytes, void* stream, int32_t* dev_err) {
