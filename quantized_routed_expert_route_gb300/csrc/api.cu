@@ -70,7 +70,7 @@ Shape decode_shape(const moe_layer_geom& g) {
 }
 
 struct WsLayout {
-  size_t err, xq, xd, xsum, xsh, inter, iq, id, isum, ish, cnt, total;
+  size_t err, bar, xq, xd, xsum, xsh, inter, iq, id, isum, ish, cnt, total;
   int cnt_len;
 };
 
@@ -80,6 +80,7 @@ WsLayout ws_layout(const moe_layer_geom& g, int T) {
   const size_t RT = (size_t)T * g.top_k;
   size_t o = 0;
   L.err = o; o = align_up(o + 4, A);
+  L.bar = o; o = align_up(o + 8, A);
   L.xq = o; o = align_up(o + (size_t)T * g.H, A);
   L.xd = o; o = align_up(o + 4 * (size_t)T * (g.H / 32), A);
   L.xsum = o; o = align_up(o + 4 * (size_t)T * (g.H / 32), A);
@@ -96,6 +97,50 @@ WsLayout ws_layout(const moe_layer_geom& g, int T) {
   return L;
 }
 
+// Shape of the fused small-batch kernel: one CTA per SM, a ring of ~32 KiB
+// slots shared by gate_up and down stages, activations in shared memory.
+// Leaves p.use_ls = 0 when it does not fit (the two-kernel path then runs).
+void plan_layer_small(const moe_layer_geom& g, int T, DecodeParams& p) {
+  DecodeParams q = p;
+  q.g_ls = sm_count();
+  if (q.g_ls > g.H) q.g_ls = g.H;
+  const int rows_max = (g.H + q.g_ls - 1) / q.g_ls;
+  q.dn_rows_max = rows_max;
+  int rs = (24 * 1024) / q.rb_dn;
+  rs = rs < 1 ? 1 : (rs > rows_max ? rows_max : rs);
+  q.dn_rs = rs;
+  q.dn_piece_bytes = (int)align_up((size_t)rs * q.rb_dn + 16, 128);
+  int sps = (32 * 1024) / q.dn_piece_bytes;
+  q.dn_slots_per_stage = sps < 1 ? 1 : (sps > 16 ? 16 : sps);
+  int ps = (32 * 1024) / (2 * q.rb_gu);
+  ps = ps < 1 ? 1 : (ps > 32 ? 32 : ps);
+  q.ps = ps;
+  q.gu_up_off = (int)align_up((size_t)ps * q.rb_gu + 16, 128);
+  const int gu_stage = 2 * q.gu_up_off, dn_stage = q.dn_slots_per_stage * q.dn_piece_bytes;
+  q.ls_sb = gu_stage > dn_stage ? gu_stage : dn_stage;
+  const size_t RT = (size_t)T * g.top_k;
+  const size_t xa = (g.gate_up_type == MOE_BF16) ? 2 * (size_t)T * g.H : (size_t)T * g.H + 8 * (size_t)T * (g.H / 32);
+  q.gu_act_smem = 1;
+  q.gu_act_bytes = (int)align_up(xa, 16);
+  if (g.down_type == MOE_BF16) {
+    const size_t ia = 4 * RT * g.I;
+    q.dn_act_smem = ia <= 48 * 1024 ? 1 : 0;
+    q.dn_act_bytes = q.dn_act_smem ? (int)align_up(ia, 16) : 0;
+  } else {
+    q.dn_act_smem = 1;
+    q.dn_act_bytes = (int)align_up(RT * g.I + 8 * RT * (g.I / 32), 16);
+  }
+  q.ls_ns = 0;
+  const size_t fixed = layer_small_smem_bytes(q);
+  const size_t budget = 210 * 1024;
+  if (fixed + 2 * (size_t)(q.ls_sb + 16) > budget) return;
+  int ns = (int)((budget - fixed) / (q.ls_sb + 16));
+  q.ls_ns = ns > 8 ? 8 : ns;
+  q.use_ls = 1;
+  if (!layer_small_fits(q)) return;
+  p = q;
+}
+
 DecodeParams make_params(const moe_bank* b, const WsLayout& L, uint8_t* ws, const Shape& sh, int T) {
   const moe_layer_geom& g = b->geom;
   DecodeParams p;
@@ -105,6 +150,7 @@ DecodeParams make_params(const moe_bank* b, const WsLayout& L, uint8_t* ws, cons
   p.rb_gu = b->rb_gu; p.rb_dn = b->rb_dn;
   p.gu_bank = b->gu; p.dn_bank = b->dn; p.scales = b->scales;
   p.err = reinterpret_cast<uint32_t*>(ws + L.err);
+  p.bar = reinterpret_cast<unsigned*>(ws + L.bar);
   p.xq = reinterpret_cast<int8_t*>(ws + L.xq);
   p.xd = reinterpret_cast<float*>(ws + L.xd);
   p.xsum = reinterpret_cast<int*>(ws + L.xsum);
@@ -130,8 +176,8 @@ DecodeParams make_params(const moe_bank* b, const WsLayout& L, uint8_t* ws, cons
   p.g_dn = sh.g_dn;
   if (p.g_dn > g.H) p.g_dn = g.H;
   const int rows_max = (g.H + p.g_dn - 1) / p.g_dn;
-  // gate_up stages: ~20 KiB of (gate, up) row pairs, ~112 KiB in flight
-  int ps = (20 * 1024) / (2 * p.rb_gu);
+  // gate_up stages: ~32 KiB of (gate, up) row pairs, ~96 KiB in flight
+  int ps = (32 * 1024) / (2 * p.rb_gu);
   if (ps < 1) ps = 1;
   if (ps > 32) ps = 32;
   p.ps = ps;
@@ -169,6 +215,7 @@ DecodeParams make_params(const moe_bank* b, const WsLayout& L, uint8_t* ws, cons
   const int dpieces = (rows_max + rs - 1) / rs;
   int dst = dpieces * (int)((U + p.dn_slots_per_stage - 1) / p.dn_slots_per_stage);
   p.dn_nstage = dst < 2 ? 2 : (dst < p.dn_nstage ? dst : p.dn_nstage);
+  if (p.maxnt == 1) plan_layer_small(g, T, p);
   switch (p.gu_type) {
     case W_NVFP4: p.w0 = 2; break;
     case W_Q4_K: p.w0 = 3; break;
@@ -310,6 +357,10 @@ static int decode_impl(const moe_bank* b, const void* x, int32_t T, const int32_
     p.w = w + (size_t)t0 * g.top_k;
     p.out = static_cast<uint16_t*>(out) + (size_t)t0 * g.H;
     cudaError_t e;
+    if (p.use_ls) {
+      if ((e = launch_layer_small(p, s)) != cudaSuccess) return cuda_fail(e, "layer launch");
+      continue;
+    }
     if (p.maxnt != 1 && (e = launch_prep(p, s)) != cudaSuccess) return cuda_fail(e, "prep launch");
     if ((e = launch_gate_up(p, s)) != cudaSuccess) return cuda_fail(e, "gate_up launch");
     if ((e = launch_down(p, s)) != cudaSuccess) return cuda_fail(e, "down launch");

@@ -54,23 +54,69 @@ struct ActQ8 {
 // returns the 32 codes packed as eight int8x4 words, d, and the exact code
 // sum.  Every q8_1 quantization on the GPU (activations, the intermediate and
 // the test hook) goes through this function.
+//
+// The codes are computed as rint(v * r) with r = 1/d rounded to nearest.
+// |v*r - v/d| <= 2^-23 * |v/d| + ulp <= 2^-16 here (|v/d| <= 127), so the
+// rounding to an integer can only differ from rint(v/d) when v*r lies within
+// 2^-12 of a half-integer; such elements (and blocks whose d is not a normal
+// number) take the IEEE division itself.
 __device__ __forceinline__ void q8_1_quantize_block(const float (&v)[32], uint32_t (&qw)[8], float& d, int& sum) {
   float amax = 0.f;
 #pragma unroll
   for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
   d = __fdiv_rn(amax, 127.0f);
+  const bool fast = d >= 1.1754944e-38f;   // normal d: r is finite and accurate
+  const float r = fast ? __frcp_rn(d) : 0.0f;
   sum = 0;
 #pragma unroll
   for (int w = 0; w < 8; ++w) {
     uint32_t word = 0;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const int q = (d == 0.0f) ? 0 : __float2int_rn(__fdiv_rn(v[4 * w + j], d));
+      const float x = v[4 * w + j];
+      const float t = x * r;
+      const float near = fabsf(t - floorf(t) - 0.5f);
+      int q;
+      if (fast && near > 0.000244140625f) q = __float2int_rn(t);
+      else q = (d == 0.0f) ? 0 : __float2int_rn(__fdiv_rn(x, d));
       sum += q;
       word |= ((uint32_t)(q & 0xFF)) << (8 * j);
     }
     qw[w] = word;
   }
+}
+
+// The same q8_1 rule with a block spread over a lane quad (lanes 4k..4k+3 of
+// a full warp), each lane holding 8 consecutive values (v[i] is value
+// 8*(lane&3)+i of the block): amax and the code sum are combined with
+// shuffles; w0/w1 receive this lane's 8 codes as two int8x4 words.
+__device__ __forceinline__ void q8_1_quantize_quad(const float (&v)[8], uint32_t& w0, uint32_t& w1, float& d,
+                                                   int& sum) {
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+  d = __fdiv_rn(amax, 127.0f);
+  const bool fast = d >= 1.1754944e-38f;
+  const float r = fast ? __frcp_rn(d) : 0.0f;
+  int s = 0;
+  uint32_t w[2] = {0u, 0u};
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float t = v[i] * r;
+    const float near = fabsf(t - floorf(t) - 0.5f);
+    int q;
+    if (fast && near > 0.000244140625f) q = __float2int_rn(t);
+    else q = (d == 0.0f) ? 0 : __float2int_rn(__fdiv_rn(v[i], d));
+    s += q;
+    w[i >> 2] |= ((uint32_t)(q & 0xFF)) << (8 * (i & 3));
+  }
+  s += __shfl_xor_sync(0xffffffffu, s, 1);
+  s += __shfl_xor_sync(0xffffffffu, s, 2);
+  w0 = w[0];
+  w1 = w[1];
+  sum = s;
 }
 
 // Internal q8_1 storage is planar: codes [rows][n] int8, d [rows][n/32] fp32

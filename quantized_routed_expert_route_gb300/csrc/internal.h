@@ -45,6 +45,11 @@ struct DecodeParams {
   int gu_act_smem, gu_act_bytes;  // stage x's activations in shared memory (bytes reserved)
   int dn_act_smem, dn_act_bytes;  // stage the intermediate's activations in shared memory
   int maxnt;               // routes per register-held work item: 1 (small batches) or 4
+  // fused small-batch layer kernel (layer_small.cu)
+  int use_ls;              // 1: one k_layer_small launch replaces k_gate_up + k_down
+  int g_ls;                // its grid (one CTA per SM)
+  int ls_ns, ls_sb;        // ring depth and bytes per ring slot
+  unsigned* bar;           // grid-barrier words in the workspace (count, generation)
 };
 
 // Sizes of the dynamic shared memory of each kernel for these params.
@@ -55,6 +60,11 @@ size_t down_smem_bytes(const DecodeParams& p);
 cudaError_t launch_prep(const DecodeParams& p, cudaStream_t stream);
 cudaError_t launch_gate_up(const DecodeParams& p, cudaStream_t stream);
 cudaError_t launch_down(const DecodeParams& p, cudaStream_t stream);
+
+// Fused small-batch layer kernel.
+size_t layer_small_smem_bytes(const DecodeParams& p);
+bool layer_small_fits(const DecodeParams& p);
+cudaError_t launch_layer_small(const DecodeParams& p, cudaStream_t stream);
 
 // Test hooks.
 cudaError_t launch_quantize_q8_1_blocks(const float* x, int64_t n, uint8_t* out, cudaStream_t stream);

@@ -1,0 +1,441 @@
+// Fused routed-expert layer for batches of one or two decode tokens.
+//
+// One kernel per decode pass instead of k_gate_up + k_down: with so few
+// tokens each phase has little work per SM, and a kernel boundary, a second
+// route grouping and a second weight-fetch latency cost more than the work.
+// Every CTA (one per SM, 16 consumer warps + 1 TMA producer warp):
+//   1. waits for the previous grid, groups the routes by expert, takes an even
+//      share of the (expert, i) gate/up pairs and H/#CTAs output rows;
+//   2. the producer streams that CTA's gate/up rows and then its down rows of
+//      every routed expert through one ring of TMA stages, so the down rows
+//      are prefetched while gate_up computes;
+//   3. consumers quantize x to q8_1 in shared memory (prep_input), dot every
+//      gate and up row with it, apply s_gate / s_up and SiLU-GLU in fp32 and
+//      write the fp32 intermediate (FreeToken PR #732, "Design"; Strata PR
+//      #292, "Summary/Pipeline");
+//   4. a grid barrier (bounded spin) makes every CTA's intermediate visible;
+//   5. each CTA requantizes the whole intermediate to q8_1 in shared memory
+//      (prep_inter), dots its down rows with every route, and sums the routes
+//      of a token in route order with w * s_down, writing bf16 with no atomics
+//      (FreeToken PR #704, "How it plugs into the CPU executor").
+// All CTAs must be resident at once; the launcher checks that one CTA fits on
+// every SM and uses this kernel only then.
+#include "decode_common.cuh"
+
+namespace qre {
+
+constexpr int kLsWarps = 16;
+constexpr int kLsConsumers = 32 * kLsWarps;
+constexpr int kLsThreads = kLsConsumers + 32;
+constexpr unsigned kGridSpinLimit = 1u << 25;   // polls with ~128 ns sleeps (~4 s) before giving up
+
+// Sense-reversing barrier over all CTAs of the grid.  bar[0] counts arrivals,
+// bar[1] is the generation; the last CTA to arrive resets the count and bumps
+// the generation.  The wait is bounded: on timeout the error word is flagged
+// and the CTA goes on (its results are then invalid, but nothing hangs).
+__device__ void ls_grid_barrier(unsigned* bar, uint32_t* err) {
+  consumer_sync<kLsConsumers>();
+  if (threadIdx.x == 0) {
+    const unsigned gen = atomicAdd(bar + 1, 0u);
+    __threadfence();
+    const unsigned arrived = atomicAdd(bar, 1u) + 1u;
+    if (arrived == gridDim.x) {
+      atomicExch(bar, 0u);
+      __threadfence();
+      atomicAdd(bar + 1, 1u);
+    } else {
+      unsigned spins = 0;
+      while (atomicAdd(bar + 1, 0u) == gen) {
+        if (++spins > kGridSpinLimit) {
+          atomicOr(err, kErrTimeout);
+          break;
+        }
+        __nanosleep(128);
+      }
+    }
+    __threadfence();
+  }
+  consumer_sync<kLsConsumers>();
+}
+
+// q8_1 quantization of `nblk` 32-value blocks (bf16 or fp32 values, row-major)
+// into shared-memory planes, one lane quad per block.  Blocks of rows whose
+// route is invalid (rvalid[row] == 0) are skipped.  CTA 0 mirrors the blocks
+// to the workspace planes for inspection.
+template <bool kBf16In>
+__device__ void ls_quantize(const void* src, int nblk, const uint8_t* rvalid, int blocks_per_row, int8_t* q, float* d,
+                            int* sm, bool mirror, int8_t* wq, float* wd, int* wsum, uint16_t* wsh) {
+  const int quad = threadIdx.x >> 2, ql = threadIdx.x & 3;
+  constexpr int kQuads = kLsConsumers / 4;
+  for (int b0 = 0; b0 < nblk; b0 += kQuads) {
+    const int b = b0 + quad;
+    const bool on = b < nblk && (!rvalid || rvalid[b / blocks_per_row]);
+    float v[8];
+    if (on) {
+      const size_t off = (size_t)b * 32 + 8 * ql;
+      if constexpr (kBf16In) {
+        bf16x8_to_f32(__ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(src) + off)), v);
+      } else {
+        const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(src) + off);
+        const float4 a = __ldcg(p), c = __ldcg(p + 1);
+        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = c.x; v[5] = c.y; v[6] = c.z; v[7] = c.w;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] = 0.f;
+    }
+    uint32_t w0, w1;
+    float dd;
+    int sum;
+    q8_1_quantize_quad(v, w0, w1, dd, sum);
+    if (on) {
+      const size_t off = (size_t)b * 32 + 8 * ql;
+      *reinterpret_cast<uint2*>(q + off) = make_uint2(w0, w1);
+      const float dh = f16_bits_to_f32(f32_to_f16_bits_rn(dd));
+      if (ql == 0) {
+        d[b] = dh;
+        sm[b] = sum;
+      }
+      if (mirror) {
+        *reinterpret_cast<uint2*>(wq + off) = make_uint2(w0, w1);
+        if (ql == 0) {
+          wd[b] = dh;
+          wsum[b] = sum;
+          wsh[b] = (uint16_t)f32_to_f16_bits_rn(dd * (float)sum);
+        }
+      }
+    }
+  }
+}
+
+template <int WG, int WD, int LPR>
+__global__ void __launch_bounds__(kLsThreads, 1) k_layer_small(const __grid_constant__ DecodeParams p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int RT = p.T * p.K;
+  const int NS = p.ls_ns;
+  const int SB = p.ls_sb;
+  constexpr int RPI = 32 / LPR;
+
+  uint8_t* ring = smem;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)NS * SB);
+  uint64_t* empty = full + NS;
+  uint8_t* xact = reinterpret_cast<uint8_t*>(empty + NS);
+  xact += (16 - (reinterpret_cast<uintptr_t>(xact) & 15)) & 15;
+  uint8_t* iact = xact + p.gu_act_bytes;
+  float* ysm = reinterpret_cast<float*>(iact + p.dn_act_bytes);
+  uint8_t* rvalid = reinterpret_cast<uint8_t*>(ysm + (size_t)RT * p.dn_rows_max);
+  uint8_t* gbase_smem = rvalid + RT;
+  gbase_smem += (16 - (reinterpret_cast<uintptr_t>(gbase_smem) & 15)) & 15;
+  GroupSmem g = carve_group(gbase_smem, p.E, RT);
+
+  if (tid == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kLsWarps);
+    }
+    fence_mbar_init();
+  }
+  pdl_wait();   // x and ids may come from the previous grid
+  pdl_launch_dependents();
+  group_routes(p.ids, RT, p.E, p.K, g);
+  const int S = g.misc[0];
+  if (tid == 0) {
+    // even split of the S*I (gate, up) pairs (32-bit)
+    const unsigned P = (unsigned)S * (unsigned)p.I;
+    const unsigned lo = (unsigned)((unsigned long long)P * blockIdx.x / gridDim.x);
+    const unsigned hi = (unsigned)((unsigned long long)P * (blockIdx.x + 1) / gridDim.x);
+    g.misc[2] = lo / p.I;
+    g.misc[3] = lo - (lo / p.I) * p.I;
+    g.misc[4] = hi / p.I;
+    g.misc[5] = hi - (hi / p.I) * p.I;
+    g.misc[6] = 0;
+    g.misc[7] = 0;
+    if (blockIdx.x == 0 && g.misc[1]) atomicOr(p.err, kErrBadId);
+  }
+  for (int r = tid; r < RT; r += kLsThreads) {
+    const int e = p.ids[r];
+    rvalid[r] = (e >= 0 && e < p.E) ? 1 : 0;
+  }
+  __syncthreads();
+  const int ub = g.misc[2], ib = g.misc[3], ue = g.misc[4], ie = g.misc[5];
+  const int j0 = (int)((long long)p.H * blockIdx.x / gridDim.x);
+  const int j1 = (int)((long long)p.H * (blockIdx.x + 1) / gridDim.x);
+  const int nj = j1 - j0;
+  const int sps = p.dn_slots_per_stage, rs = p.dn_rs;
+  const int ngrp = (S + sps - 1) / sps;
+  const int nst_dn = (S > 0 && nj > 0) ? ((nj + rs - 1) / rs) * ngrp : 0;
+
+  if (warp == kLsWarps) {
+    // TMA producer: this CTA's gate/up stages, then its down stages, through one ring.
+    if (lane == 0) {
+      const uint64_t pol = l2_policy_evict_first();
+      PairCursor pc{ub, ib};
+      int buf = 0;
+      uint32_t eph = 0;
+      bool wrapped = false, ok = true;
+      int k = 0;
+      for (;;) {
+        int su = 0, si = 0, sn = 0;
+        const bool gu = next_gu_stage(pc, ue, ie, p.I, p.ps, su, si, sn);
+        if (!gu && k >= nst_dn) break;
+        if (wrapped) {
+          if (!mbar_wait_bounded(&empty[buf], eph, kWaitLimit)) {
+            ok = false;
+            break;
+          }
+          fence_proxy_async_smem();
+        }
+        uint8_t* dst = ring + (size_t)buf * SB;
+        if (gu) issue_gu_stage(p, dst, &full[buf], g.slot_e[su], si, sn, pol);
+        else issue_dn_stage(p, dst, &full[buf], g, down_stage(k++, S, nj, rs, sps), j0, pol);
+        atomicAdd(&g.misc[7], 1);
+        if (++buf == NS) {
+          buf = 0;
+          if (wrapped) eph ^= 1u;
+          wrapped = true;
+        }
+      }
+      if (!ok) g.misc[6] = 1;
+    }
+    return;
+  }
+
+  // ---------------- consumers
+  const int cw = warp;
+  for (int sl = tid; sl < S; sl += kLsConsumers) {
+    const int e = g.slot_e[sl];
+    g.sscale[3 * sl + 0] = __ldg(p.scales + 4 * e + 0);
+    g.sscale[3 * sl + 1] = __ldg(p.scales + 4 * e + 1);
+  }
+  const int nbh = p.H / 32, nbi = p.I / 32;
+  int8_t* xq = reinterpret_cast<int8_t*>(xact);
+  float* xd = reinterpret_cast<float*>(xact + (size_t)p.T * p.H);
+  int* xs = reinterpret_cast<int*>(xd + (size_t)p.T * nbh);
+  if constexpr (WG == W_BF16) {
+    copy_to_smem<kLsConsumers>(xact, p.x, 2 * (size_t)p.T * p.H);
+  } else {
+    ls_quantize<true>(p.x, p.T * nbh, nullptr, nbh, xq, xd, xs, blockIdx.x == 0, p.xq, p.xd, p.xsum, p.xsh);
+  }
+  consumer_sync<kLsConsumers>();
+
+  // gate_up: pairs round-robin over the warps, routes of the expert inside
+  const size_t rbg = (size_t)p.rb_gu;
+  PairCursor cc{ub, ib};
+  int rot = 0, buf = 0, consumed = 0;
+  uint32_t fph = 0;
+  for (;;) {
+    int su, si, sn;
+    if (!next_gu_stage(cc, ue, ie, p.I, p.ps, su, si, sn)) break;
+    const uint8_t* sbuf = ring + (size_t)buf * SB;
+    const int e = g.slot_e[su];
+    const uint8_t* gsrc = p.gu_bank + ((size_t)e * 2 * p.I + si) * rbg;
+    const uint8_t* usrc = gsrc + (size_t)p.I * rbg;
+    const uint8_t* gbase = sbuf + (gsrc - align16_down(gsrc));
+    const uint8_t* ubase = sbuf + p.gu_up_off + (usrc - align16_down(usrc));
+    const int roff = g.slot_off[su];
+    const int Tu = g.slot_off[su + 1] - roff;
+    const float sg = g.sscale[3 * su + 0], su_ = g.sscale[3 * su + 1];
+    if (!mbar_wait_bounded(&full[buf], fph, kWaitLimit)) {
+      g.misc[6] = 1;
+      break;
+    }
+    for (int pi = (cw - rot) & (kLsWarps - 1); pi < sn; pi += kLsWarps) {
+      const uint8_t* grow = gbase + (size_t)pi * rbg;
+      const uint8_t* urow = ubase + (size_t)pi * rbg;
+      for (int ri = 0; ri < Tu; ++ri) {
+        const int t = g.rtok[roff + ri];
+        float2 h;
+        if constexpr (WG == W_BF16) {
+          ActSrc act;
+          act.xb = reinterpret_cast<const uint16_t*>(xact);
+          act.n = p.H;
+          int tok[NT] = {t, 0, 0, 0};
+          float ag[NT], au[NT];
+          gu_item<W_BF16, 1>(grow, urow, p.H, 0, p.H / 8, lane, act, tok, 1, ag, au);
+          h = make_float2(ag[0], au[0]);
+        } else {
+          h = gu_pair_q8<WG>(grow, urow, p.H, lane, xq + (size_t)t * p.H, xd + t * nbh, xs + t * nbh);
+        }
+        if (lane == 0) {
+          const int r = g.routes[roff + ri];
+          p.inter[(size_t)r * p.I + si + pi] = silu_glu(h.x * sg, h.y * su_);
+        }
+      }
+    }
+    rot = (rot + sn) & (kLsWarps - 1);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[buf]);
+    ++consumed;
+    if (++buf == NS) {
+      buf = 0;
+      fph ^= 1u;
+    }
+  }
+
+  // every CTA's intermediate is written before any CTA reads it
+  ls_grid_barrier(p.bar, p.err);
+
+  // prep_inter
+  int8_t* iq = reinterpret_cast<int8_t*>(iact);
+  float* idd = reinterpret_cast<float*>(iact + (size_t)RT * p.I);
+  int* is = reinterpret_cast<int*>(idd + (size_t)RT * nbi);
+  ActSrc dact;
+  dact.n = p.I;
+  dact.xf = p.inter;
+  if constexpr (WD == W_BF16) {
+    if (p.dn_act_smem) {
+      copy_to_smem<kLsConsumers>(iact, p.inter, 4 * (size_t)RT * p.I);
+      dact.xf = reinterpret_cast<const float*>(iact);
+    }
+  } else {
+    ls_quantize<false>(p.inter, RT * nbi, rvalid, nbi, iq, idd, is, blockIdx.x == 0, p.iq, p.id, p.isum, p.ish);
+  }
+  consumer_sync<kLsConsumers>();
+
+  // down: (slot, row group) items round-robin over the warps, routes inside
+  const size_t rbd = (size_t)p.rb_dn;
+  const int grp = lane / LPR, sl = lane % LPR;
+  rot = 0;
+  int k = 0;
+  for (; k < nst_dn && !g.misc[6]; ++k) {
+    const uint8_t* sbuf = ring + (size_t)buf * SB;
+    const DownStage st = down_stage(k, S, nj, rs, sps);
+    const int nq = (st.nr + RPI - 1) / RPI;
+    if (!mbar_wait_bounded(&full[buf], fph, kWaitLimit)) {
+      g.misc[6] = 1;
+      break;
+    }
+    for (int i = 0; i < st.ns; ++i) {
+      const int u = st.u0 + i;
+      const int roff = g.slot_off[u];
+      const int Tu = g.slot_off[u + 1] - roff;
+      const int e = g.slot_e[u];
+      const uint8_t* src = p.dn_bank + ((size_t)e * p.H + j0 + st.js) * rbd;
+      const uint8_t* piece = sbuf + (size_t)i * p.dn_piece_bytes + (src - align16_down(src));
+      for (int q = (cw - rot) & (kLsWarps - 1); q < nq; q += kLsWarps) {
+        const int row = q * RPI + grp;
+        const bool vrow = row < st.nr;
+        const uint8_t* rowp = piece + (size_t)(vrow ? row : 0) * rbd;
+        for (int ri = 0; ri < Tu; ++ri) {
+          const int r = g.routes[roff + ri];
+          float v;
+          if constexpr (WD == W_BF16) {
+            int rt[NT] = {r, 0, 0, 0};
+            float res[NT];
+            dn_item<W_BF16, LPR, 1>(rowp, vrow, p.I, sl, dact, rt, 1, res);
+            v = res[0];
+          } else {
+            v = dn_row_q8<WD, LPR>(rowp, vrow, p.I, sl, iq + (size_t)r * p.I, idd + r * nbi, is + r * nbi);
+          }
+          if (vrow && sl == 0) ysm[(size_t)r * p.dn_rows_max + st.js + row] = v;
+        }
+      }
+      rot = (rot + nq) & (kLsWarps - 1);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[buf]);
+    ++consumed;
+    if (++buf == NS) {
+      buf = 0;
+      fph ^= 1u;
+    }
+  }
+  consumer_sync<kLsConsumers>();
+  if (g.misc[6]) {  // a bounded wait ran out: drain what is in flight (bounded), flag, leave
+    if (tid == 0) {
+      const int issued = g.misc[7];
+      for (int qn = consumed; qn < issued; ++qn)
+        mbar_wait_bounded(&full[qn % NS], (uint32_t)((qn / NS) & 1), kWaitLimit);
+      atomicOr(p.err, kErrTimeout);
+    }
+    return;
+  }
+  // route sum in route order k = 0..K-1, then one rounding to bf16
+  for (int idx = tid; idx < p.T * nj; idx += kLsConsumers) {
+    const int t = idx / nj, jj = idx - t * nj;
+    float acc = 0.f;
+    for (int kk = 0; kk < p.K; ++kk) {
+      const int r = t * p.K + kk;
+      if (!rvalid[r]) continue;
+      const int e = p.ids[r];
+      acc += ysm[(size_t)r * p.dn_rows_max + jj] * (__ldg(p.scales + 4 * e + 2) * __ldg(p.w + r));
+    }
+    p.out[(size_t)t * p.H + j0 + jj] = (uint16_t)f32_to_bf16_bits_rn(acc);
+  }
+}
+
+// ------------------------------------------------------------------ launch
+
+size_t layer_small_smem_bytes(const DecodeParams& p) {
+  const int RT = p.T * p.K;
+  return (size_t)p.ls_ns * p.ls_sb + 16 * (size_t)p.ls_ns + 16 + (size_t)p.gu_act_bytes + (size_t)p.dn_act_bytes +
+         sizeof(float) * (size_t)RT * p.dn_rows_max + (size_t)RT + 16 + group_smem_bytes(p.E, RT);
+}
+
+template <int WG, int WD, int LPR>
+static cudaError_t launch_ls_t(const DecodeParams& p, cudaStream_t stream, bool probe_only, bool* fits) {
+  const size_t smem = layer_small_smem_bytes(p);
+  cudaError_t e = cudaFuncSetAttribute(k_layer_small<WG, WD, LPR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    if (fits) *fits = false;
+    return probe_only ? cudaSuccess : e;
+  }
+  if (probe_only) {
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_layer_small<WG, WD, LPR>, kLsThreads, smem);
+    if (fits) *fits = (e == cudaSuccess && per_sm >= 1);
+    cudaGetLastError();
+    return cudaSuccess;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.g_ls);
+  cfg.blockDim = dim3(kLsThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  // Cooperative: the driver keeps every CTA resident at once, which the grid
+  // barrier needs; programmatic serialization: the next layer's grid may be
+  // scheduled early (it waits before touching anything this one writes).
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, k_layer_small<WG, WD, LPR>, p);
+}
+
+// Same-type layers of the four formats (aligned NVFP4 rows); other pairs use
+// the two-kernel path.
+static cudaError_t dispatch_ls(const DecodeParams& p, cudaStream_t stream, bool probe_only, bool* fits) {
+  if (p.gu_type != p.dn_type) {
+    if (fits) *fits = false;
+    return cudaSuccess;
+  }
+  switch (p.gu_type) {
+    case W_NVFP4:
+      if (p.rb_gu % 16 != 0 || p.rb_dn % 16 != 0) {
+        if (fits) *fits = false;
+        return cudaSuccess;
+      }
+      return launch_ls_t<W_NVFP4, W_NVFP4, 8>(p, stream, probe_only, fits);
+    case W_Q4_K: return launch_ls_t<W_Q4_K, W_Q4_K, 8>(p, stream, probe_only, fits);
+    case W_Q8_0: return launch_ls_t<W_Q8_0, W_Q8_0, 8>(p, stream, probe_only, fits);
+    default: return launch_ls_t<W_BF16, W_BF16, 16>(p, stream, probe_only, fits);
+  }
+}
+
+bool layer_small_fits(const DecodeParams& p) {
+  bool fits = false;
+  dispatch_ls(p, nullptr, true, &fits);
+  return fits;
+}
+
+cudaError_t launch_layer_small(const DecodeParams& p, cudaStream_t stream) {
+  return dispatch_ls(p, stream, false, nullptr);
+}
+
+}  // namespace qre

@@ -37,7 +37,13 @@ def test_q8_1_quantizer_bit_exact():
              np.zeros(32 * 10, np.float32),
              # ramps whose x/d land on exact .5 ties
              np.tile((np.arange(32) - 16).astype(np.float32) * 0.25, 50),
-             (r.integers(-127, 128, 32 * 500) * np.float32(0.5)).astype(np.float32)]
+             (r.integers(-127, 128, 32 * 500) * np.float32(0.5)).astype(np.float32),
+             # values one ulp either side of exact .5 ties of x/d
+             np.nextafter(np.tile((np.arange(32) - 16).astype(np.float32) * 0.25, 20), np.float32(np.inf)),
+             np.nextafter(np.tile((np.arange(32) - 16).astype(np.float32) * 0.25, 20), np.float32(-np.inf)),
+             # blocks whose d is tiny or subnormal
+             (r.standard_normal(32 * 200) * 1e-38).astype(np.float32),
+             (r.standard_normal(32 * 200) * 1e-44).astype(np.float32)]
     x = np.concatenate(parts)
     xd = torch.from_numpy(x).to(DEV)
     out = torch.empty(x.size // 32 * 36, dtype=torch.uint8, device=DEV)
