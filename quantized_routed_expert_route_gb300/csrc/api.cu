@@ -80,7 +80,7 @@ WsLayout ws_layout(const moe_layer_geom& g, int T) {
   const size_t RT = (size_t)T * g.top_k;
   size_t o = 0;
   L.err = o; o = align_up(o + 4, A);
-  L.bar = o; o = align_up(o + 8, A);
+  L.bar = o; o = align_up(o + 128 * (1 + (size_t)kMaxGridCtas), A);   // arrival count + one line per CTA
   L.xq = o; o = align_up(o + (size_t)T * g.H, A);
   L.xd = o; o = align_up(o + 4 * (size_t)T * (g.H / 32), A);
   L.xsum = o; o = align_up(o + 4 * (size_t)T * (g.H / 32), A);
@@ -104,6 +104,7 @@ void plan_layer_small(const moe_layer_geom& g, int T, DecodeParams& p) {
   DecodeParams q = p;
   q.g_ls = sm_count();
   if (q.g_ls > g.H) q.g_ls = g.H;
+  if (q.g_ls > kMaxGridCtas) return;
   const int rows_max = (g.H + q.g_ls - 1) / q.g_ls;
   q.dn_rows_max = rows_max;
   int rs = (24 * 1024) / q.rb_dn;

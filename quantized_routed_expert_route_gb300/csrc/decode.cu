@@ -408,8 +408,8 @@ __global__ void __launch_bounds__(kDecodeThreads, MAXNT == 1 ? 2 : 1) k_down(con
   // read before this kernel waits.
   group_routes(p.ids, RT, p.E, p.K, g);
   const int S = g.misc[0];
-  const int j0 = (int)((long long)p.H * blockIdx.x / gridDim.x);
-  const int j1 = (int)((long long)p.H * (blockIdx.x + 1) / gridDim.x);
+  const int j0 = (int)((unsigned)p.H * blockIdx.x / gridDim.x);
+  const int j1 = (int)((unsigned)p.H * (blockIdx.x + 1) / gridDim.x);
   const int nj = j1 - j0;
   const int sps = p.dn_slots_per_stage, rs = p.dn_rs;
   const int ngrp = (S + sps - 1) / sps;

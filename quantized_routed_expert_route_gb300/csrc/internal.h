@@ -10,6 +10,7 @@ namespace qre {
 constexpr int kMaxE = 1024;
 constexpr int kMaxTopK = 32;
 constexpr int kTChunk = 64;
+constexpr int kMaxGridCtas = 256;   // CTAs of the fused kernel's grid barrier
 
 // Everything one decode pass (at most kTChunk tokens) needs, by value in
 // kernel parameter space.
@@ -49,7 +50,7 @@ struct DecodeParams {
   int use_ls;              // 1: one k_layer_small launch replaces k_gate_up + k_down
   int g_ls;                // its grid (one CTA per SM)
   int ls_ns, ls_sb;        // ring depth and bytes per ring slot
-  unsigned* bar;           // grid-barrier words in the workspace (count, generation)
+  unsigned* bar;           // grid-barrier words in the workspace (count, then one line per CTA)
 };
 
 // Sizes of the dynamic shared memory of each kernel for these params.

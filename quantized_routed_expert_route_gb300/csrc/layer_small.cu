@@ -27,33 +27,53 @@ namespace qre {
 constexpr int kLsWarps = 16;
 constexpr int kLsConsumers = 32 * kLsWarps;
 constexpr int kLsThreads = kLsConsumers + 32;
-constexpr unsigned kGridSpinLimit = 1u << 25;   // polls with ~128 ns sleeps (~4 s) before giving up
+constexpr unsigned kGridSpinLimit = 1u << 23;   // acquire polls of the generation word (~3 s) before giving up
 
-// Sense-reversing barrier over all CTAs of the grid.  bar[0] counts arrivals,
-// bar[1] is the generation; the last CTA to arrive resets the count and bumps
-// the generation.  The wait is bounded: on timeout the error word is flagged
-// and the CTA goes on (its results are then invalid, but nothing hangs).
-__device__ void ls_grid_barrier(unsigned* bar, uint32_t* err) {
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ unsigned atom_add_acq_rel_gpu(unsigned* p, unsigned v) {
+  unsigned old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+__device__ __forceinline__ void red_release_gpu_add(unsigned* p, unsigned v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ void st_relaxed_gpu(unsigned* p, unsigned v) {
+  asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Barrier over all CTAs of the grid.  bar[0] is an epoch that only changes
+// between launches; CTA c owns the word bar[32 * (1 + c)] (its own 128-byte
+// line).  Arriving, a CTA fences (publishing its earlier writes) and stores
+// epoch + 1 into its word; one warp then polls every CTA's word with acquire
+// loads until all hold epoch + 1.  After the barrier CTA 0 advances the epoch
+// for the next launch (every CTA read it at its start, before arriving).  The
+// wait is bounded: on timeout the error word is flagged and the CTA goes on
+// (its results are then invalid, but nothing hangs).
+__device__ void ls_grid_barrier(unsigned* bar, unsigned epoch, uint32_t* err) {
   consumer_sync<kLsConsumers>();
-  if (threadIdx.x == 0) {
-    const unsigned gen = atomicAdd(bar + 1, 0u);
-    __threadfence();
-    const unsigned arrived = atomicAdd(bar, 1u) + 1u;
-    if (arrived == gridDim.x) {
-      atomicExch(bar, 0u);
-      __threadfence();
-      atomicAdd(bar + 1, 1u);
-    } else {
+  if (threadIdx.x < 32) {
+    const unsigned lane = threadIdx.x;
+    const unsigned target = __shfl_sync(0xffffffffu, epoch + 1u, 0);   // thread 0 read the epoch
+    if (lane == 0) {
+      asm volatile("fence.acq_rel.gpu;" ::: "memory");
+      st_relaxed_gpu(bar + 32 * (1 + blockIdx.x), target);
+    }
+    for (unsigned c = lane; c < gridDim.x; c += 32) {
       unsigned spins = 0;
-      while (atomicAdd(bar + 1, 0u) == gen) {
+      while (ld_acquire_gpu(bar + 32 * (1 + c)) != target) {
         if (++spins > kGridSpinLimit) {
           atomicOr(err, kErrTimeout);
           break;
         }
-        __nanosleep(128);
       }
     }
-    __threadfence();
+    __syncwarp();
+    if (lane == 0 && blockIdx.x == 0) st_relaxed_gpu(bar, target);
   }
   consumer_sync<kLsConsumers>();
 }
@@ -67,41 +87,52 @@ __device__ void ls_quantize(const void* src, int nblk, const uint8_t* rvalid, in
                             int* sm, bool mirror, int8_t* wq, float* wd, int* wsum, uint16_t* wsh) {
   const int quad = threadIdx.x >> 2, ql = threadIdx.x & 3;
   constexpr int kQuads = kLsConsumers / 4;
-  for (int b0 = 0; b0 < nblk; b0 += kQuads) {
-    const int b = b0 + quad;
-    const bool on = b < nblk && (!rvalid || rvalid[b / blocks_per_row]);
-    float v[8];
-    if (on) {
-      const size_t off = (size_t)b * 32 + 8 * ql;
-      if constexpr (kBf16In) {
-        bf16x8_to_f32(__ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(src) + off)), v);
-      } else {
-        const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(src) + off);
-        const float4 a = __ldcg(p), c = __ldcg(p + 1);
-        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = c.x; v[5] = c.y; v[6] = c.z; v[7] = c.w;
-      }
-    } else {
+  constexpr int kR = 2;   // blocks per quad per round, all loads issued first
+  for (int b0 = 0; b0 < nblk; b0 += kR * kQuads) {
+    float v[kR][8];
+    bool on[kR];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) v[i] = 0.f;
-    }
-    uint32_t w0, w1;
-    float dd;
-    int sum;
-    q8_1_quantize_quad(v, w0, w1, dd, sum);
-    if (on) {
-      const size_t off = (size_t)b * 32 + 8 * ql;
-      *reinterpret_cast<uint2*>(q + off) = make_uint2(w0, w1);
-      const float dh = f16_bits_to_f32(f32_to_f16_bits_rn(dd));
-      if (ql == 0) {
-        d[b] = dh;
-        sm[b] = sum;
+    for (int h = 0; h < kR; ++h) {
+      const int b = b0 + h * kQuads + quad;
+      on[h] = b < nblk && (!rvalid || rvalid[b / blocks_per_row]);
+      if (on[h]) {
+        const size_t off = (size_t)b * 32 + 8 * ql;
+        if constexpr (kBf16In) {
+          bf16x8_to_f32(__ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(src) + off)), v[h]);
+        } else {
+          const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(src) + off);
+          const float4 a = __ldcg(p), c = __ldcg(p + 1);
+          v[h][0] = a.x; v[h][1] = a.y; v[h][2] = a.z; v[h][3] = a.w;
+          v[h][4] = c.x; v[h][5] = c.y; v[h][6] = c.z; v[h][7] = c.w;
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[h][i] = 0.f;
       }
-      if (mirror) {
-        *reinterpret_cast<uint2*>(wq + off) = make_uint2(w0, w1);
+    }
+#pragma unroll
+    for (int h = 0; h < kR; ++h) {
+      if (b0 + h * kQuads >= nblk) break;   // the same in every lane
+      uint32_t w0, w1;
+      float dd;
+      int sum;
+      q8_1_quantize_quad(v[h], w0, w1, dd, sum);
+      if (on[h]) {
+        const int b = b0 + h * kQuads + quad;
+        const size_t off = (size_t)b * 32 + 8 * ql;
+        *reinterpret_cast<uint2*>(q + off) = make_uint2(w0, w1);
+        const float dh = f16_bits_to_f32(f32_to_f16_bits_rn(dd));
         if (ql == 0) {
-          wd[b] = dh;
-          wsum[b] = sum;
-          wsh[b] = (uint16_t)f32_to_f16_bits_rn(dd * (float)sum);
+          d[b] = dh;
+          sm[b] = sum;
+        }
+        if (mirror) {
+          *reinterpret_cast<uint2*>(wq + off) = make_uint2(w0, w1);
+          if (ql == 0) {
+            wd[b] = dh;
+            wsum[b] = sum;
+            wsh[b] = (uint16_t)f32_to_f16_bits_rn(dd * (float)sum);
+          }
         }
       }
     }
@@ -124,7 +155,8 @@ __global__ void __launch_bounds__(kLsThreads, 1) k_layer_small(const __grid_cons
   xact += (16 - (reinterpret_cast<uintptr_t>(xact) & 15)) & 15;
   uint8_t* iact = xact + p.gu_act_bytes;
   float* ysm = reinterpret_cast<float*>(iact + p.dn_act_bytes);
-  uint8_t* rvalid = reinterpret_cast<uint8_t*>(ysm + (size_t)RT * p.dn_rows_max);
+  float* swd = ysm + (size_t)RT * p.dn_rows_max;                       // [RT] s_down * w (0: bad route)
+  uint8_t* rvalid = reinterpret_cast<uint8_t*>(swd + RT);
   uint8_t* gbase_smem = rvalid + RT;
   gbase_smem += (16 - (reinterpret_cast<uintptr_t>(gbase_smem) & 15)) & 15;
   GroupSmem g = carve_group(gbase_smem, p.E, RT);
@@ -138,13 +170,20 @@ __global__ void __launch_bounds__(kLsThreads, 1) k_layer_small(const __grid_cons
   }
   pdl_wait();   // x and ids may come from the previous grid
   pdl_launch_dependents();
+  const unsigned epoch = (tid == 0) ? ld_acquire_gpu(p.bar) : 0u;
   group_routes(p.ids, RT, p.E, p.K, g);
   const int S = g.misc[0];
   if (tid == 0) {
     // even split of the S*I (gate, up) pairs (32-bit)
     const unsigned P = (unsigned)S * (unsigned)p.I;
-    const unsigned lo = (unsigned)((unsigned long long)P * blockIdx.x / gridDim.x);
-    const unsigned hi = (unsigned)((unsigned long long)P * (blockIdx.x + 1) / gridDim.x);
+    unsigned lo, hi;
+    if (P <= 0xFFFFFFFFu / gridDim.x) {   // 32-bit division when the products fit
+      lo = P * blockIdx.x / gridDim.x;
+      hi = P * (blockIdx.x + 1) / gridDim.x;
+    } else {
+      lo = (unsigned)((unsigned long long)P * blockIdx.x / gridDim.x);
+      hi = (unsigned)((unsigned long long)P * (blockIdx.x + 1) / gridDim.x);
+    }
     g.misc[2] = lo / p.I;
     g.misc[3] = lo - (lo / p.I) * p.I;
     g.misc[4] = hi / p.I;
@@ -153,14 +192,10 @@ __global__ void __launch_bounds__(kLsThreads, 1) k_layer_small(const __grid_cons
     g.misc[7] = 0;
     if (blockIdx.x == 0 && g.misc[1]) atomicOr(p.err, kErrBadId);
   }
-  for (int r = tid; r < RT; r += kLsThreads) {
-    const int e = p.ids[r];
-    rvalid[r] = (e >= 0 && e < p.E) ? 1 : 0;
-  }
   __syncthreads();
   const int ub = g.misc[2], ib = g.misc[3], ue = g.misc[4], ie = g.misc[5];
-  const int j0 = (int)((long long)p.H * blockIdx.x / gridDim.x);
-  const int j1 = (int)((long long)p.H * (blockIdx.x + 1) / gridDim.x);
+  const int j0 = (int)((unsigned)p.H * blockIdx.x / gridDim.x);
+  const int j1 = (int)((unsigned)p.H * (blockIdx.x + 1) / gridDim.x);
   const int nj = j1 - j0;
   const int sps = p.dn_slots_per_stage, rs = p.dn_rs;
   const int ngrp = (S + sps - 1) / sps;
@@ -203,6 +238,22 @@ __global__ void __launch_bounds__(kLsThreads, 1) k_layer_small(const __grid_cons
 
   // ---------------- consumers
   const int cw = warp;
+  // route validity and s_down * w of every route, from the grouping (off the
+  // producer's path: the producer is already streaming)
+  for (int r = tid; r < RT; r += kLsConsumers) {
+    rvalid[r] = 0;
+    swd[r] = 0.f;
+  }
+  consumer_sync<kLsConsumers>();
+  for (int sl = tid; sl < S; sl += kLsConsumers) {
+    const int e = g.slot_e[sl];
+    const float sd = __ldg(p.scales + 4 * e + 2);
+    for (int i = g.slot_off[sl]; i < g.slot_off[sl + 1]; ++i) {
+      const int r = g.routes[i];
+      rvalid[r] = 1;
+      swd[r] = sd * __ldg(p.w + r);
+    }
+  }
   for (int sl = tid; sl < S; sl += kLsConsumers) {
     const int e = g.slot_e[sl];
     g.sscale[3 * sl + 0] = __ldg(p.scales + 4 * e + 0);
@@ -274,7 +325,7 @@ __global__ void __launch_bounds__(kLsThreads, 1) k_layer_small(const __grid_cons
   }
 
   // every CTA's intermediate is written before any CTA reads it
-  ls_grid_barrier(p.bar, p.err);
+  ls_grid_barrier(p.bar, epoch, p.err);
 
   // prep_inter
   int8_t* iq = reinterpret_cast<int8_t*>(iact);
@@ -358,8 +409,7 @@ __global__ void __launch_bounds__(kLsThreads, 1) k_layer_small(const __grid_cons
     for (int kk = 0; kk < p.K; ++kk) {
       const int r = t * p.K + kk;
       if (!rvalid[r]) continue;
-      const int e = p.ids[r];
-      acc += ysm[(size_t)r * p.dn_rows_max + jj] * (__ldg(p.scales + 4 * e + 2) * __ldg(p.w + r));
+      acc += ysm[(size_t)r * p.dn_rows_max + jj] * swd[r];
     }
     p.out[(size_t)t * p.H + j0 + jj] = (uint16_t)f32_to_bf16_bits_rn(acc);
   }
@@ -370,7 +420,7 @@ __global__ void __launch_bounds__(kLsThreads, 1) k_layer_small(const __grid_cons
 size_t layer_small_smem_bytes(const DecodeParams& p) {
   const int RT = p.T * p.K;
   return (size_t)p.ls_ns * p.ls_sb + 16 * (size_t)p.ls_ns + 16 + (size_t)p.gu_act_bytes + (size_t)p.dn_act_bytes +
-         sizeof(float) * (size_t)RT * p.dn_rows_max + (size_t)RT + 16 + group_smem_bytes(p.E, RT);
+         sizeof(float) * (size_t)RT * (p.dn_rows_max + 1) + (size_t)RT + 16 + group_smem_bytes(p.E, RT);
 }
 
 template <int WG, int WD, int LPR>
