@@ -210,6 +210,15 @@ int moe_debug_decode_stages(const moe_bank* bank, const void* x, int32_t T,
                             void* ws, size_t ws_bytes, void* stream,
                             void* x_blocks, float* inter, void* inter_blocks);
 
+/* Tensor-core check: D[128, N] = A[128, K] * B[N, K]^T with fp16 A and B
+ * (device, row-major), fp32 D (device, row-major), computed with the tcgen05
+ * kind::f16 MMA on swizzled shared-memory tiles that the prompt-path GEMMs
+ * use.  K a positive multiple of 64, N a multiple of 16 in [16, 256], A and B
+ * 16-byte aligned.  *dev_err (device int32, caller-zeroed) gets bit 0 if a
+ * bounded wait for the MMA ran out. */
+int moe_debug_tc_gemm(const void* A, const void* B, int32_t K, int32_t N, float* D,
+                      int32_t* dev_err, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -24,7 +24,7 @@ EXPORTS = (
     "moe_row_bytes", "moe_bank_create", "moe_bank_destroy", "moe_bank_geometry",
     "moe_workspace_bytes", "moe_workspace_init", "moe_decode", "moe_get_error",
     "moe_status_string", "moe_last_cuda_error", "moe_quantize_q8_1",
-    "moe_debug_block_dots", "moe_debug_decode_stages", "moe_decode_noalloc",
+    "moe_debug_block_dots", "moe_debug_decode_stages", "moe_decode_noalloc", "moe_debug_tc_gemm",
 )
 
 
@@ -65,6 +65,7 @@ def _load() -> ctypes.CDLL:
         "moe_debug_block_dots": (ctypes.c_int, [i32, vp, i32, i32, vp, vp, vp]),
         "moe_debug_decode_stages": (ctypes.c_int, [vp, vp, i32, vp, vp, vp, vp, sz, vp, vp, vp, vp]),
         "moe_decode_noalloc": (ctypes.c_int, [vp, vp, i32, vp, vp, vp, vp]),
+        "moe_debug_tc_gemm": (ctypes.c_int, [vp, vp, i32, i32, vp, vp, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -156,3 +157,8 @@ def moe_debug_decode_stages(bank: int, x: int, T: int, topk_ids: int, topk_w: in
     _check(_lib.moe_debug_decode_stages(bank, x, T, topk_ids, topk_w, out, ws, ws_bytes, stream or None,
                                         x_blocks or None, inter or None, inter_blocks or None),
            "moe_debug_decode_stages")
+
+
+def moe_debug_tc_gemm(A: int, B: int, K: int, N: int, D: int, dev_err: int, stream: int = 0) -> None:
+    """D[128, N] = A[128, K] @ B[N, K]^T (fp16 in, fp32 out) on the tcgen05 tensor cores."""
+    _check(_lib.moe_debug_tc_gemm(A, B, K, N, D, dev_err, stream or None), "moe_debug_tc_gemm")

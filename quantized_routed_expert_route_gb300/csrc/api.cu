@@ -455,6 +455,15 @@ int moe_debug_block_dots(int32_t type, const void* rows, int32_t nrows, int32_t 
   return e == cudaSuccess ? MOE_OK : cuda_fail(e, "block_dots");
 }
 
+int moe_debug_tc_gemm(const void* A, const void* B, int32_t K, int32_t N, float* D, int32_t* dev_err,
+                      void* stream) {
+  if (!A || !B || !D || !dev_err || K <= 0 || K % 64 != 0 || N < 16 || N > 256 || N % 16 != 0) return MOE_EINVAL;
+  if (!aligned(A, 16) || !aligned(B, 16) || !aligned(D, 4) || !aligned(dev_err, 4)) return MOE_EINVAL;
+  cudaError_t e = launch_tc_gemm_check(static_cast<const uint16_t*>(A), static_cast<const uint16_t*>(B), K, N, D,
+                                       dev_err, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MOE_OK : cuda_fail(e, "tc_gemm");
+}
+
 int moe_debug_decode_stages(const moe_bank* b, const void* x, int32_t T, const int32_t* ids, const float* w,
                             void* out, void* ws, size_t ws_bytes, void* stream, void* x_blocks, float* inter,
                             void* inter_blocks) {

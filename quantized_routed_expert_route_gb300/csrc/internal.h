@@ -71,6 +71,8 @@ cudaError_t launch_layer_small(const DecodeParams& p, cudaStream_t stream);
 cudaError_t launch_quantize_q8_1_blocks(const float* x, int64_t n, uint8_t* out, cudaStream_t stream);
 cudaError_t launch_block_dots(int type, const uint8_t* rows, int nrows, int k, const uint8_t* act,
                               int32_t* out, cudaStream_t stream);
+cudaError_t launch_tc_gemm_check(const uint16_t* A, const uint16_t* B, int K, int N, float* D, int* err,
+                                 cudaStream_t stream);
 cudaError_t launch_export_q8(const int8_t* q, const float* d, const uint16_t* s, int64_t nblocks,
                              uint8_t* out, cudaStream_t stream);
 

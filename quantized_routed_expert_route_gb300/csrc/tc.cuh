@@ -1,0 +1,130 @@
+// Inline-PTX wrappers for the sm_103a tensor cores (tcgen05): tensor-memory
+// allocation, shared-memory matrix descriptors, the kind::f16 MMA with fp32
+// accumulation in tensor memory, its commit to an mbarrier, and tensor-memory
+// loads for the epilogue.
+//
+// Operand layout used throughout: K-major tiles with the 128-byte swizzle.  A
+// tile of R rows x 64 fp16 values occupies R * 128 bytes, rows 128 bytes apart,
+// 8-row groups 1024 bytes apart, and inside each 1024-byte group the 16-byte
+// chunk c of row r is stored at chunk position c ^ (r % 8).  Tile bases are
+// 1024-byte aligned.  One MMA consumes K = 16 (32 bytes of each row); the k-th
+// 16-wide step inside a 64-wide tile starts 32*k bytes into the tile.
+#pragma once
+#include <cstdint>
+
+#include "ptx.cuh"
+
+namespace qre {
+namespace tc {
+
+// Byte offset of fp16 element (r, k) (k < 64) inside a swizzled tile.
+__host__ __device__ __forceinline__ uint32_t sw128_offset(uint32_t r, uint32_t k) {
+  const uint32_t lin = r * 128u + k * 2u;
+  return lin ^ (((lin >> 7) & 7u) << 4);
+}
+
+// Byte offset of the 16-byte chunk c (elements 8c..8c+7) of row r.
+__host__ __device__ __forceinline__ uint32_t sw128_chunk(uint32_t r, uint32_t c) {
+  return r * 128u + ((c ^ (r & 7u)) << 4);
+}
+
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups
+// 1024 bytes apart (stride byte offset), descriptor version 1.
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)1u << 16;                     // leading byte offset (unused with this swizzle)
+  d |= (uint64_t)(1024u >> 4) << 32;           // stride byte offset
+  d |= (uint64_t)1u << 46;                     // version
+  d |= (uint64_t)2u << 61;                     // SWIZZLE_128B
+  return d;
+}
+
+// Instruction descriptor of kind::f16: fp32 accumulator, fp16 (or bf16) A
+// and B, both K-major, M x N.
+__host__ __device__ __forceinline__ uint32_t idesc_f16(uint32_t M, uint32_t N, bool bf16) {
+  uint32_t d = 0;
+  d |= 1u << 4;                       // D format: F32
+  d |= (bf16 ? 1u : 0u) << 7;         // A format
+  d |= (bf16 ? 1u : 0u) << 10;        // B format
+  d |= (N >> 3) << 17;
+  d |= (M >> 4) << 24;
+  return d;
+}
+
+// Tensor memory: allocate `ncols` columns (a power of two >= 32) for the CTA;
+// the whole warp executes it and the address lands in *dst (shared memory).
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(dst)),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+__device__ __forceinline__ void fence_before_sync() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void fence_after_sync() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T, issued by one thread.
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                       uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive once on `bar` when every MMA this thread issued before has completed.
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_addr(bar))
+               : "memory");
+}
+
+// 32 consecutive fp32 columns of this thread's tensor-memory lane (the warp
+// reads lanes 32*(warp%4) .. +31; taddr carries the lane base in bits 16+).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Eight E2M1 codes (one 32-bit word, element 2i in the low nibble of byte i)
+// -> eight fp16 values as four f16x2 words (exact).
+__device__ __forceinline__ void e2m1x8_to_f16x8(uint32_t codes, uint32_t (&h)[4]) {
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\tcvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\tcvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+      : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+      : "r"(codes));
+}
+
+// Two UE4M3 bytes -> f16x2 (exact; bit 7 of each byte clear).
+__device__ __forceinline__ uint32_t ue4m3x2_to_f16x2(uint16_t v) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(v));
+  return h2;
+}
+
+__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+}  // namespace tc
+}  // namespace qre
