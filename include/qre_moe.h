@@ -169,6 +169,38 @@ int moe_decode_noalloc(const moe_bank* bank, const void* x, int32_t T,
                        const int32_t* topk_ids, const float* topk_w, void* out,
                        void* stream);
 
+/* ---------------------------------------------------------------- prompt path
+ * Grouped expert GEMMs for a prompt chunk (Strata PR #292, "Summary/Pipeline":
+ * the prompt path, W4A4 with activations quantized to NVFP4 on the fly, or
+ * W4A8 with q8_1 activations).  NVFP4 gate_up and down banks only, H and I
+ * multiples of 256; other banks return MOE_EUNSUPPORTED. */
+enum { MOE_PREFILL_W4A4 = 0, MOE_PREFILL_W4A8 = 1 };
+
+/* Workspace bytes moe_prefill_grouped needs for T tokens in `mode`; 0 if the
+ * bank or mode is unsupported or T < 1. */
+size_t moe_prefill_workspace_bytes(const moe_bank* bank, int32_t T, int32_t mode);
+
+/* Prompt-path layer: out[t] = bf16(sum over k of the routed expert's output
+ * times s_down * topk_w[t, k]), the same layer as moe_decode with the prompt
+ * path's activation quantization.  Steps: routes sorted by expert (stable);
+ * x quantized per token (W4A4: per 16 values a UE4M3 scale = amax/6 and E2M1
+ * codes, both rounded to nearest even with saturation, global scale 1; W4A8:
+ * the q8_1 rule of the decode path); a grouped gate_up GEMM on the tensor
+ * cores over the exactly dequantized operands (fp16 values, fp32
+ * accumulation) with s_gate, s_up and SiLU-GLU in an fp32 epilogue that
+ * requantizes the intermediate the same way as x; a grouped down GEMM whose
+ * epilogue scales by s_down * routing weight; a sum over k = 0..K-1 in order.
+ * x: bf16 [T, H] (device, 16-byte aligned); topk_ids int32 and topk_w fp32
+ * [T, K] (device); out bf16 [T, H] (device, 8-byte aligned); ws: device,
+ * 256-byte aligned, >= moe_prefill_workspace_bytes(bank, T, mode) bytes (no
+ * initialization needed; each call starts by clearing its error word).
+ * Asynchronous on `stream`; a route whose id is outside [0, E) contributes
+ * zero and sets MOE_DEVERR_BAD_ID (read with moe_get_error on the same
+ * workspace). */
+int moe_prefill_grouped(const moe_bank* bank, const void* x, int32_t T,
+                        const int32_t* topk_ids, const float* topk_w, int32_t mode,
+                        void* out, void* ws, size_t ws_bytes, void* stream);
+
 /* Read and clear the workspace's sticky device error bits (synchronizes
  * `stream`).  *dev_err receives the MOE_DEVERR_* bits; returns MOE_EDEVICE if
  * any was set, MOE_OK otherwise. */
@@ -209,6 +241,19 @@ int moe_debug_decode_stages(const moe_bank* bank, const void* x, int32_t T,
                             const int32_t* topk_ids, const float* topk_w, void* out,
                             void* ws, size_t ws_bytes, void* stream,
                             void* x_blocks, float* inter, void* inter_blocks);
+
+/* Run moe_prefill_grouped, then export its stages (any pointer may be NULL):
+ *   xq:   the quantized x, W4A4: [T] rows of H/2 E2M1 code bytes (element 2i
+ *         in the low nibble of byte i) then H/16 UE4M3 scale bytes; W4A8:
+ *         [T, H/32] q8_1 blocks of 36 bytes {fp16 d; fp16 s; int8 q[32]};
+ *   off:  int32 [E+1], the first sorted row of each expert (off[E] = valid routes);
+ *   perm: int32 [T*K], the route index t*K+k of each sorted row;
+ *   i16:  fp16 [T*K, I], the dequantized requantized intermediate of each
+ *         sorted row. */
+int moe_debug_prefill_stages(const moe_bank* bank, const void* x, int32_t T,
+                             const int32_t* topk_ids, const float* topk_w, int32_t mode,
+                             void* out, void* ws, size_t ws_bytes, void* stream,
+                             void* xq, int32_t* off, int32_t* perm, void* i16);
 
 /* Tensor-core check: D[128, N] = A[128, K] * B[N, K]^T with fp16 A and B
  * (device, row-major), fp32 D (device, row-major), computed with the tcgen05

@@ -17,6 +17,7 @@ MOE_OK, MOE_EINVAL, MOE_EUNSUPPORTED, MOE_ENOMEM, MOE_ECUDA, MOE_EDEVICE = 0, -1
 MOE_DEVERR_BAD_ID, MOE_DEVERR_TIMEOUT = 1, 2
 MOE_SRC_HOST, MOE_SRC_DEVICE, MOE_SRC_DEVICE_BORROW = 0, 1, 2
 MOE_MAX_E, MOE_MAX_TOPK, MOE_DECODE_T_CHUNK = 1024, 32, 64
+MOE_PREFILL_W4A4, MOE_PREFILL_W4A8 = 0, 1
 MOE_NOALLOC_WS_BYTES = 4 << 20
 
 # every symbol include/qre_moe.h declares
@@ -25,6 +26,7 @@ EXPORTS = (
     "moe_workspace_bytes", "moe_workspace_init", "moe_decode", "moe_get_error",
     "moe_status_string", "moe_last_cuda_error", "moe_quantize_q8_1",
     "moe_debug_block_dots", "moe_debug_decode_stages", "moe_decode_noalloc", "moe_debug_tc_gemm",
+    "moe_prefill_workspace_bytes", "moe_prefill_grouped", "moe_debug_prefill_stages",
 )
 
 
@@ -66,6 +68,9 @@ def _load() -> ctypes.CDLL:
         "moe_debug_decode_stages": (ctypes.c_int, [vp, vp, i32, vp, vp, vp, vp, sz, vp, vp, vp, vp]),
         "moe_decode_noalloc": (ctypes.c_int, [vp, vp, i32, vp, vp, vp, vp]),
         "moe_debug_tc_gemm": (ctypes.c_int, [vp, vp, i32, i32, vp, vp, vp]),
+        "moe_prefill_workspace_bytes": (sz, [vp, i32, i32]),
+        "moe_prefill_grouped": (ctypes.c_int, [vp, vp, i32, vp, vp, i32, vp, vp, sz, vp]),
+        "moe_debug_prefill_stages": (ctypes.c_int, [vp, vp, i32, vp, vp, i32, vp, vp, sz, vp, vp, vp, vp, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -162,3 +167,21 @@ def moe_debug_decode_stages(bank: int, x: int, T: int, topk_ids: int, topk_w: in
 def moe_debug_tc_gemm(A: int, B: int, K: int, N: int, D: int, dev_err: int, stream: int = 0) -> None:
     """D[128, N] = A[128, K] @ B[N, K]^T (fp16 in, fp32 out) on the tcgen05 tensor cores."""
     _check(_lib.moe_debug_tc_gemm(A, B, K, N, D, dev_err, stream or None), "moe_debug_tc_gemm")
+
+
+def moe_prefill_workspace_bytes(bank: int, T: int, mode: int) -> int:
+    return int(_lib.moe_prefill_workspace_bytes(bank, T, mode))
+
+
+def moe_prefill_grouped(bank: int, x: int, T: int, topk_ids: int, topk_w: int, mode: int, out: int, ws: int,
+                        ws_bytes: int, stream: int = 0) -> None:
+    _check(_lib.moe_prefill_grouped(bank, x, T, topk_ids, topk_w, mode, out, ws, ws_bytes, stream or None),
+           "moe_prefill_grouped")
+
+
+def moe_debug_prefill_stages(bank: int, x: int, T: int, topk_ids: int, topk_w: int, mode: int, out: int, ws: int,
+                             ws_bytes: int, stream: int = 0, xq: int | None = None, off: int | None = None,
+                             perm: int | None = None, i16: int | None = None) -> None:
+    _check(_lib.moe_debug_prefill_stages(bank, x, T, topk_ids, topk_w, mode, out, ws, ws_bytes, stream or None,
+                                         xq or None, off or None, perm or None, i16 or None),
+           "moe_debug_prefill_stages")

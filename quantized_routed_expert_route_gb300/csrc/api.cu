@@ -455,6 +455,103 @@ int moe_debug_block_dots(int32_t type, const void* rows, int32_t nrows, int32_t 
   return e == cudaSuccess ? MOE_OK : cuda_fail(e, "block_dots");
 }
 
+// ------------------------------------------------------------------ prompt path
+
+namespace {
+
+struct PfLayout {
+  size_t err, off, perm, xq, x16, x16lo, i16, y, total;
+};
+
+PfLayout pf_layout(const moe_layer_geom& g, int64_t T, int mode) {
+  PfLayout L;
+  const size_t A = 256;
+  const size_t RT = (size_t)T * g.top_k;
+  size_t o = 0;
+  L.err = o; o = align_up(o + 4, A);
+  L.off = o; o = align_up(o + 4 * ((size_t)g.E + 1), A);
+  L.perm = o; o = align_up(o + 4 * RT, A);
+  L.xq = o;
+  o = align_up(o + (mode == PF_W4A4 ? (size_t)T * (g.H / 2 + g.H / 16) : (size_t)T * (g.H / 32) * 36), A);
+  L.x16 = o; o = align_up(o + 2 * (size_t)T * g.H, A);
+  L.x16lo = o; o = align_up(o + (mode == PF_W4A8 ? 2 * (size_t)T * g.H : 0), A);
+  L.i16 = o; o = align_up(o + 2 * RT * g.I, A);
+  L.y = o; o = align_up(o + 4 * RT * g.H, A);
+  L.total = o;
+  return L;
+}
+
+int pf_check(const moe_bank* b, int32_t mode) {
+  if (!b || (mode != PF_W4A4 && mode != PF_W4A8)) return MOE_EINVAL;
+  const moe_layer_geom& g = b->geom;
+  if (g.gate_up_type != MOE_NVFP4 || g.down_type != MOE_NVFP4) return MOE_EUNSUPPORTED;
+  if (g.H % 256 != 0 || g.I % 256 != 0) return MOE_EUNSUPPORTED;
+  return MOE_OK;
+}
+
+}  // namespace
+
+size_t moe_prefill_workspace_bytes(const moe_bank* b, int32_t T, int32_t mode) {
+  if (pf_check(b, mode) != MOE_OK || T < 1) return 0;
+  if ((int64_t)T * b->geom.top_k > (int64_t)(1 << 30)) return 0;
+  return pf_layout(b->geom, T, mode).total;
+}
+
+int moe_prefill_grouped(const moe_bank* b, const void* x, int32_t T, const int32_t* ids, const float* w,
+                        int32_t mode, void* out, void* ws, size_t ws_bytes, void* stream) {
+  int st = pf_check(b, mode);
+  if (st) return st;
+  if (T < 0) return MOE_EINVAL;
+  if (T == 0) return MOE_OK;
+  if (!x || !ids || !w || !out || !ws) return MOE_EINVAL;
+  if (!aligned(x, 16) || !aligned(out, 8) || !aligned(ids, 4) || !aligned(w, 4) || !aligned(ws, 256))
+    return MOE_EINVAL;
+  const moe_layer_geom& g = b->geom;
+  if ((int64_t)T * g.top_k > (int64_t)(1 << 30)) return MOE_EINVAL;
+  const PfLayout L = pf_layout(g, T, mode);
+  if (ws_bytes < L.total) return MOE_EINVAL;
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  PfParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.H = g.H; p.I = g.I; p.E = g.E; p.K = g.top_k; p.T = T; p.RT = T * g.top_k;
+  p.mode = mode;
+  p.rb_gu = b->rb_gu; p.rb_dn = b->rb_dn;
+  p.gu_bank = b->gu; p.dn_bank = b->dn; p.scales = b->scales;
+  p.x = static_cast<const uint16_t*>(x);
+  p.ids = ids;
+  p.w = w;
+  p.out = static_cast<uint16_t*>(out);
+  p.err = reinterpret_cast<uint32_t*>(base + L.err);
+  p.off = reinterpret_cast<int*>(base + L.off);
+  p.perm = reinterpret_cast<int*>(base + L.perm);
+  p.xq = base + L.xq;
+  p.x16 = reinterpret_cast<uint16_t*>(base + L.x16);
+  p.x16lo = reinterpret_cast<uint16_t*>(base + L.x16lo);
+  p.i16 = reinterpret_cast<uint16_t*>(base + L.i16);
+  p.y = reinterpret_cast<float*>(base + L.y);
+  cudaError_t e = launch_prefill(p, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MOE_OK : cuda_fail(e, "prefill launch");
+}
+
+int moe_debug_prefill_stages(const moe_bank* b, const void* x, int32_t T, const int32_t* ids, const float* w,
+                             int32_t mode, void* out, void* ws, size_t ws_bytes, void* stream, void* xq,
+                             int32_t* off, int32_t* perm, void* i16) {
+  int st = moe_prefill_grouped(b, x, T, ids, w, mode, out, ws, ws_bytes, stream);
+  if (st || T == 0) return st;
+  const moe_layer_geom& g = b->geom;
+  const PfLayout L = pf_layout(g, T, mode);
+  const uint8_t* base = static_cast<const uint8_t*>(ws);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t RT = (size_t)T * g.top_k;
+  cudaError_t e = cudaSuccess;
+  const size_t xq_bytes = (mode == PF_W4A4) ? (size_t)T * (g.H / 2 + g.H / 16) : (size_t)T * (g.H / 32) * 36;
+  if (xq) e = cudaMemcpyAsync(xq, base + L.xq, xq_bytes, cudaMemcpyDeviceToDevice, s);
+  if (e == cudaSuccess && off) e = cudaMemcpyAsync(off, base + L.off, 4 * ((size_t)g.E + 1), cudaMemcpyDeviceToDevice, s);
+  if (e == cudaSuccess && perm) e = cudaMemcpyAsync(perm, base + L.perm, 4 * RT, cudaMemcpyDeviceToDevice, s);
+  if (e == cudaSuccess && i16) e = cudaMemcpyAsync(i16, base + L.i16, 2 * RT * g.I, cudaMemcpyDeviceToDevice, s);
+  return e == cudaSuccess ? MOE_OK : cuda_fail(e, "prefill debug export");
+}
+
 int moe_debug_tc_gemm(const void* A, const void* B, int32_t K, int32_t N, float* D, int32_t* dev_err,
                       void* stream) {
   if (!A || !B || !D || !dev_err || K <= 0 || K % 64 != 0 || N < 16 || N > 256 || N % 16 != 0) return MOE_EINVAL;

@@ -53,6 +53,31 @@ struct DecodeParams {
   unsigned* bar;           // grid-barrier words in the workspace (count, then one line per CTA)
 };
 
+// The prompt path (prefill.cu): routes sorted by expert, then two grouped
+// GEMMs on the tensor cores (gate_up, down) and a fixed-order combine.
+enum PfMode : int { PF_W4A4 = 0, PF_W4A8 = 1 };
+struct PfParams {
+  int H, I, E, K, T, RT;
+  int mode;
+  int rb_gu, rb_dn;
+  const uint8_t* gu_bank;   // NVFP4 rows [E][2I][rb_gu]
+  const uint8_t* dn_bank;   // NVFP4 rows [E][H][rb_dn]
+  const float* scales;      // [E][4]
+  const uint16_t* x;        // bf16 [T][H]
+  const int32_t* ids;       // [T][K]
+  const float* w;           // [T][K]
+  uint16_t* out;            // bf16 [T][H]
+  // workspace
+  uint32_t* err;
+  int* off;                 // [E+1] first sorted row of each expert; off[E] = valid routes
+  int* perm;                // [RT]  route index of each sorted row
+  uint8_t* xq;              // quantized x: NVFP4 rows [T][H/2 + H/16] (W4A4) or q8_1 blocks [T][H/32][36] (W4A8)
+  uint16_t* x16;            // fp16 [T][H]: the dequantized quantized x (the gate_up A operand)
+  uint16_t* x16lo;          // fp16 [T][H], W4A8 only: q*d - x16 (x16 + x16lo carries q*d to ~2^-22)
+  uint16_t* i16;            // fp16 [RT][I]: the dequantized requantized intermediate, sorted rows
+  float* y;                 // fp32 [RT][H]: down output of each route times s_down * w, by route index
+};
+
 // Sizes of the dynamic shared memory of each kernel for these params.
 size_t gate_up_smem_bytes(const DecodeParams& p);
 size_t down_smem_bytes(const DecodeParams& p);
@@ -71,6 +96,7 @@ cudaError_t launch_layer_small(const DecodeParams& p, cudaStream_t stream);
 cudaError_t launch_quantize_q8_1_blocks(const float* x, int64_t n, uint8_t* out, cudaStream_t stream);
 cudaError_t launch_block_dots(int type, const uint8_t* rows, int nrows, int k, const uint8_t* act,
                               int32_t* out, cudaStream_t stream);
+cudaError_t launch_prefill(const PfParams& p, cudaStream_t stream);
 cudaError_t launch_tc_gemm_check(const uint16_t* A, const uint16_t* B, int K, int N, float* D, int* err,
                                  cudaStream_t stream);
 cudaError_t launch_export_q8(const int8_t* q, const float* d, const uint16_t* s, int64_t nblocks,

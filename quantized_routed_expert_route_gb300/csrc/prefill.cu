@@ -1,4 +1,36 @@
 // Prompt-path (prefill) kernels on the sm_103a tensor cores.
+//
+// One prompt chunk of T tokens through one routed-expert layer (Strata PR
+// #292, "Summary/Pipeline": the prompt path runs the routed experts as
+// grouped GEMMs, W4A4 with activations quantized to NVFP4 on the fly or W4A8
+// with q8_1 activations; FreeToken PR #732, "Design", for the layer formula
+// and the per-expert weight_scale_2 applied to each projection's fp32 output):
+//
+//   k_pf_sort     P1: the T*K routes sorted by expert (stable: route order
+//                 t*K+k inside an expert), per-expert row offsets.
+//   k_pf_quant    P2: every token's hidden state quantized once -- NVFP4 (per
+//                 16 values: UE4M3 scale = amax/6 nearest-even, E2M1 codes
+//                 nearest-even, global scale 1) or q8_1 -- and stored both as
+//                 codes and as fp16 operands: the exact dequantized NVFP4
+//                 values, or each q8_1 value q*d as an fp16 pair hi + lo.
+//   k_pf_gemm<0>  P3: grouped gate_up GEMM.  A tile is (expert, 256 sorted
+//                 rows, 128 intermediate columns): 128 gate rows and 128 up
+//                 rows of the expert's NVFP4 bank are expanded to fp16
+//                 (code * UE4M3 scale, exact) into swizzled shared-memory
+//                 tiles, the rows' activations are gathered beside them, and
+//                 one thread issues tcgen05 kind::f16 MMAs into two 128x256
+//                 fp32 accumulators in tensor memory.  The epilogue applies
+//                 s_gate / s_up and SiLU-GLU in fp32, requantizes each 16 (or
+//                 32) intermediate values to NVFP4 (or q8_1), and stores the
+//                 exact fp16 dequantized values.
+//   k_pf_gemm<1>  P4: grouped down GEMM, (expert, 256 rows, 256 outputs)
+//                 tiles over the requantized intermediate; the epilogue scales
+//                 by s_down * routing weight and stores fp32 per route.
+//   k_pf_combine  P6: out[t] = bf16(sum over k = 0..K-1 of the route rows),
+//                 in route order, no atomics.
+//
+// Every product in the MMAs is of two exact fp16 values (NVFP4 code * scale,
+// or a q8_1 value rounded to fp16 once), accumulated in fp32.
 #include <cuda_fp16.h>
 
 #include "decode_common.cuh"
@@ -81,6 +113,449 @@ cudaError_t launch_tc_gemm_check(const uint16_t* A, const uint16_t* B, int K, in
   cudaError_t e = cudaFuncSetAttribute(k_tc_gemm_check, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   k_tc_gemm_check<<<1, 128, smem, stream>>>(A, B, K, N, D, err);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ P1: routes sorted by expert
+
+constexpr int kSortThreads = 1024;
+
+// One CTA: per-warp expert counts over contiguous route ranges, an exclusive
+// scan over experts, then each warp places its routes (match/rank inside each
+// group of 32), so rows of an expert keep route order.  Routes whose id is
+// outside [0, E) are left out and flag the error word.
+__global__ void __launch_bounds__(kSortThreads) k_pf_sort(const __grid_constant__ PfParams p) {
+  extern __shared__ int ssm[];
+  constexpr int NW = kSortThreads / 32;
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const int E = p.E, RT = p.RT;
+  int* cnt = ssm;             // [NW][E]
+  int* base = cnt + NW * E;   // [E]
+  int* wsum = base + E;       // [33]
+  if (tid == 0) *p.err = 0u;  // each prompt-path call starts with a clear error word
+  for (int i = tid; i < NW * E; i += kSortThreads) cnt[i] = 0;
+  __syncthreads();
+  const int per = (RT + NW - 1) / NW;
+  const int r0 = min(RT, w * per), r1 = min(RT, r0 + per);
+  bool bad = false;
+  for (int r = r0 + lane; r < r1; r += 32) {
+    const int e = p.ids[r];
+    if (e >= 0 && e < E) atomicAdd(&cnt[w * E + e], 1);
+    else bad = true;
+  }
+  __syncthreads();
+  for (int e = tid; e < E; e += kSortThreads) {
+    int acc = 0;
+    for (int ww = 0; ww < NW; ++ww) {
+      const int c = cnt[ww * E + e];
+      cnt[ww * E + e] = acc;
+      acc += c;
+    }
+    base[e] = acc;
+  }
+  __syncthreads();
+  const int total = block_exclusive_scan(base, E, wsum);
+  for (int e = tid; e < E; e += kSortThreads) p.off[e] = base[e];
+  if (tid == 0) p.off[E] = total;
+  for (int rb = r0; rb < r1; rb += 32) {
+    const int r = rb + lane;
+    const int e = (r < r1) ? p.ids[r] : -1;
+    const bool v = r < r1 && e >= 0 && e < E;
+    const unsigned peers = __match_any_sync(0xffffffffu, v ? e : -1 - lane);
+    const int rank = __popc(peers & ((1u << lane) - 1u));
+    if (v) p.perm[base[e] + cnt[w * E + e] + rank] = r;
+    __syncwarp();
+    if (v && rank == 0) cnt[w * E + e] += __popc(peers);
+    __syncwarp();
+  }
+  const bool any_bad = __any_sync(0xffffffffu, bad);
+  if (any_bad && lane == 0) atomicOr(p.err, kErrBadId);
+}
+
+size_t pf_sort_smem(int E) { return sizeof(int) * ((size_t)(kSortThreads / 32) * E + E + 33); }
+
+// ------------------------------------------------------------------ P2: activation quantizers
+
+// NVFP4 quantization of 16 values (W4A4 activations and intermediate): the
+// UE4M3 scale byte, the eight code bytes as two words, and the exact fp16
+// dequantized values (code * scale) as eight f16x2 words.
+__device__ __forceinline__ void nvfp4_quant16(const float* v, uint32_t& sbyte, uint32_t& c0, uint32_t& c1,
+                                              uint32_t (&h)[8]) {
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  sbyte = tc::e4m3_rne_sat(__fdiv_rn(amax, 6.0f));
+  const uint32_t s2 = tc::ue4m3x2_to_f16x2((uint16_t)(sbyte | (sbyte << 8)));   // (scale, scale)
+  const float sv = f16_bits_to_f32(s2 & 0xFFFFu);
+  if (sv > 0.f) {
+    float q[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) q[i] = __fdiv_rn(v[i], sv);
+    c0 = tc::e2m1x8_rne_sat(q);
+    c1 = tc::e2m1x8_rne_sat(q + 8);
+  } else {
+    c0 = c1 = 0u;
+  }
+  uint32_t a[4], b[4];
+  tc::e2m1x8_to_f16x8(c0, a);
+  tc::e2m1x8_to_f16x8(c1, b);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    h[i] = tc::hmul2(a[i], s2);
+    h[4 + i] = tc::hmul2(b[i], s2);
+  }
+}
+
+// q8_1 quantization of 32 values (W4A8 activations and intermediate, the same
+// device function as the decode path): codes, d (fp16 value as fp32), and
+// the fp16 values round(q * d) as sixteen f16x2 words.
+__device__ __forceinline__ void q8_1_quant32_f16(const float (&v)[32], uint32_t (&qw)[8], float& dh, int& sum,
+                                                 float& dfull, uint32_t (&h)[16]) {
+  q8_1_quantize_block(v, qw, dfull, sum);
+  dh = f16_bits_to_f32(f32_to_f16_bits_rn(dfull));
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const int q0 = (int)(int8_t)((qw[i >> 1] >> (16 * (i & 1))) & 0xFFu);
+    const int q1 = (int)(int8_t)((qw[i >> 1] >> (16 * (i & 1) + 8)) & 0xFFu);
+    const uint32_t lo = f32_to_f16_bits_rn((float)q0 * dh), hi = f32_to_f16_bits_rn((float)q1 * dh);
+    h[i] = lo | (hi << 16);
+  }
+}
+
+// One thread per 16 (W4A4) or 32 (W4A8) values of x.
+__global__ void k_pf_quant(const __grid_constant__ PfParams p) {
+  const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (p.mode == PF_W4A4) {
+    const int nb = p.H / 16;
+    if (idx >= (long long)p.T * nb) return;
+    const int t = (int)(idx / nb), b = (int)(idx - (long long)t * nb);
+    const uint4* src = reinterpret_cast<const uint4*>(p.x + (size_t)t * p.H + 16 * b);
+    float v[16];
+    {
+      float f[8];
+      bf16x8_to_f32(__ldg(src), f);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] = f[i];
+      bf16x8_to_f32(__ldg(src + 1), f);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[8 + i] = f[i];
+    }
+    uint32_t sbyte, c0, c1, h[8];
+    nvfp4_quant16(v, sbyte, c0, c1, h);
+    const size_t rbx = (size_t)p.H / 2 + p.H / 16;
+    *reinterpret_cast<uint2*>(p.xq + (size_t)t * rbx + 8 * b) = make_uint2(c0, c1);
+    p.xq[(size_t)t * rbx + p.H / 2 + b] = (uint8_t)sbyte;
+    uint4* dst = reinterpret_cast<uint4*>(p.x16 + (size_t)t * p.H + 16 * b);
+    dst[0] = make_uint4(h[0], h[1], h[2], h[3]);
+    dst[1] = make_uint4(h[4], h[5], h[6], h[7]);
+  } else {
+    const int nb = p.H / 32;
+    if (idx >= (long long)p.T * nb) return;
+    const int t = (int)(idx / nb), b = (int)(idx - (long long)t * nb);
+    float v[32];
+    load_block32<true>(p.x + (size_t)t * p.H, b, v);
+    uint32_t qw[8], h[16];
+    float dh, dfull;
+    int sum;
+    q8_1_quant32_f16(v, qw, dh, sum, dfull, h);
+    uint32_t* blk = reinterpret_cast<uint32_t*>(p.xq + ((size_t)t * nb + b) * 36);
+    blk[0] = f32_to_f16_bits_rn(dfull) | (f32_to_f16_bits_rn(dfull * (float)sum) << 16);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) blk[1 + i] = qw[i];
+    uint4* dst = reinterpret_cast<uint4*>(p.x16 + (size_t)t * p.H + 32 * b);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) dst[i] = make_uint4(h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]);
+    // the remainder q*d - fp16(q*d), also in fp16: hi + lo carries q*d to
+    // about 2^-22, so the gate_up products see the q8_1 values themselves
+    uint32_t l[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int q0 = (int)(int8_t)((qw[i >> 1] >> (16 * (i & 1))) & 0xFFu);
+      const int q1 = (int)(int8_t)((qw[i >> 1] >> (16 * (i & 1) + 8)) & 0xFFu);
+      const float p0 = (float)q0 * dh, p1 = (float)q1 * dh;   // exact
+      const float r0 = p0 - f16_bits_to_f32(h[i] & 0xFFFFu), r1 = p1 - f16_bits_to_f32(h[i] >> 16);
+      l[i] = f32_to_f16_bits_rn(r0) | (f32_to_f16_bits_rn(r1) << 16);
+    }
+    uint4* dlo = reinterpret_cast<uint4*>(p.x16lo + (size_t)t * p.H + 32 * b);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) dlo[i] = make_uint4(l[4 * i], l[4 * i + 1], l[4 * i + 2], l[4 * i + 3]);
+  }
+}
+
+// ------------------------------------------------------------------ P3 / P4: grouped GEMMs
+
+constexpr int kPfThreads = 512;     // 16 warps: all expand operands, one thread issues MMAs, all run the epilogue
+constexpr int kPfTileRows = 256;
+constexpr int kPfMaxStages = 3;
+// Stage layout: A rows 0..127 (16 KB), A rows 128..255 (16 KB), B 256 rows
+// (32 KB), and with SPLIT the low parts of A rows 0..127 and 128..255.
+template <bool SPLIT>
+struct PfStage {
+  static constexpr int kStages = SPLIT ? 2 : 3;
+  static constexpr int kBytes = SPLIT ? 98304 : 65536;
+};
+
+// PHASE 0: gate_up (K = H; B rows = 128 gate + 128 up rows; epilogue GLU +
+// requant); PHASE 1: down (K = I; B rows = 256 output rows; epilogue scales).
+// SPLIT (W4A8 gate_up): the activations are the fp16 pair hi + lo and each
+// product is formed as hi*B + lo*B into the same accumulator.
+template <int PHASE, bool SPLIT>
+__global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(const __grid_constant__ PfParams p) {
+  constexpr int kPfStages = PfStage<SPLIT>::kStages;
+  constexpr int kPfStageBytes = PfStage<SPLIT>::kBytes;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint64_t mma_bar[kPfMaxStages];
+  __shared__ uint32_t tmem_base;
+  __shared__ int tile_pre[kMaxE + 1];
+  __shared__ int wsum[33];
+  __shared__ int arow[kPfTileRows];
+  uint8_t* stages = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int E = p.E;
+  const int NT = PHASE == 0 ? p.I / 128 : p.H / 256;   // column tiles per expert
+  const int Kd = PHASE == 0 ? p.H : p.I;               // reduction length
+  const int nK = Kd / 64;
+  for (int e = tid; e < E; e += kPfThreads) {
+    const int M = p.off[e + 1] - p.off[e];
+    tile_pre[e] = ((M + kPfTileRows - 1) / kPfTileRows) * NT;
+  }
+  __syncthreads();
+  const int total = block_exclusive_scan(tile_pre, E, wsum);
+  if (warp == 0) {
+    tc::tmem_alloc(&tmem_base, 512);
+    tc::tmem_relinquish();
+  }
+  if (tid == 0) {
+    for (int s = 0; s < kPfStages; ++s) mbar_init(&mma_bar[s], 1);
+    fence_mbar_init();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = tmem_base;
+  const uint32_t idesc = tc::idesc_f16(128, 256, false);
+  const uint16_t* asrc = PHASE == 0 ? p.x16 : p.i16;
+  uint32_t chunk = 0;
+  bool ok = true;
+  for (int t = blockIdx.x; t < total; t += gridDim.x) {
+    // the expert of tile t: the largest e with tile_pre[e] <= t (never an empty one)
+    int lo = 0, hi = E;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (tile_pre[mid] <= t) lo = mid;
+      else hi = mid;
+    }
+    const int e = lo;
+    const int tl = t - tile_pre[e];
+    const int Me = p.off[e + 1] - p.off[e];
+    const int mtiles = (Me + kPfTileRows - 1) / kPfTileRows;
+    const int mt = tl % mtiles, nt = tl / mtiles;
+    const int rows = min(kPfTileRows, Me - mt * kPfTileRows);
+    const int srow0 = p.off[e] + mt * kPfTileRows;
+    for (int m = tid; m < kPfTileRows; m += kPfThreads)
+      arow[m] = (m < rows) ? (PHASE == 0 ? p.perm[srow0 + m] / p.K : srow0 + m) : -1;
+    __syncthreads();   // arow visible; the previous tile's epilogue is done with tensor memory
+    tc::fence_after_sync();
+    const int rb = PHASE == 0 ? p.rb_gu : p.rb_dn;
+    const int brow = tid >> 1, bh = tid & 1;
+    const size_t bsrc_row = PHASE == 0 ? ((size_t)e * 2 * p.I + (brow < 128 ? nt * 128 + brow : p.I + nt * 128 + brow - 128))
+                                       : ((size_t)e * p.H + (size_t)nt * 256 + brow);
+    const uint8_t* brp = (PHASE == 0 ? p.gu_bank : p.dn_bank) + bsrc_row * rb;
+    for (int kc = 0; kc < nK; ++kc, ++chunk) {
+      const uint32_t s = chunk % kPfStages;
+      uint8_t* st = stages + (size_t)s * kPfStageBytes;
+      const int k0 = kc * 64;
+      // operand loads first (A: four 16-byte chunks; B: 32 NVFP4 values)
+      constexpr int NA = SPLIT ? 8 : 4;
+      uint4 av[NA];
+#pragma unroll
+      for (int j = 0; j < NA; ++j) {
+        const int i = tid + (j & 3) * kPfThreads;
+        const int src = arow[i >> 3];
+        const uint16_t* as = (j < 4) ? asrc : p.x16lo;
+        av[j] = (src >= 0) ? __ldcg(reinterpret_cast<const uint4*>(as + (size_t)src * Kd + k0 + 8 * (i & 7)))
+                           : make_uint4(0u, 0u, 0u, 0u);
+      }
+      const int kabs = k0 + 32 * bh;
+      const uint4 cw = __ldg(reinterpret_cast<const uint4*>(brp + kabs / 2));
+      const uint16_t sw = __ldg(reinterpret_cast<const uint16_t*>(brp + Kd / 2 + kabs / 16));
+      if (chunk >= (uint32_t)kPfStages) {
+        // the MMAs that last read this stage are done
+        if (!mbar_wait_bounded(&mma_bar[s], ((chunk - kPfStages) / kPfStages) & 1u, kWaitLimit)) ok = false;
+      }
+#pragma unroll
+      for (int j = 0; j < NA; ++j) {
+        const int i = tid + (j & 3) * kPfThreads;
+        const int m = i >> 3, c = i & 7;
+        *reinterpret_cast<uint4*>(st + (j < 4 ? 0 : 65536) + (m < 128 ? 0 : 16384) + tc::sw128_chunk(m & 127, c)) =
+            av[j];
+      }
+      {
+        const uint32_t s2 = tc::ue4m3x2_to_f16x2(sw);
+        const uint32_t s0 = prmt(s2, 0u, 0x1010u), s1 = prmt(s2, 0u, 0x3232u);
+        const uint32_t cws[4] = {cw.x, cw.y, cw.z, cw.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint32_t h[4];
+          tc::e2m1x8_to_f16x8(cws[q], h);
+          const uint32_t sc = q < 2 ? s0 : s1;
+          *reinterpret_cast<uint4*>(st + 32768 + tc::sw128_chunk(brow, 4 * bh + q)) =
+              make_uint4(tc::hmul2(h[0], sc), tc::hmul2(h[1], sc), tc::hmul2(h[2], sc), tc::hmul2(h[3], sc));
+        }
+      }
+      fence_proxy_async_smem();
+      __syncthreads();
+      if (tid == 0) {
+        tc::fence_after_sync();
+        const uint32_t a0 = smem_addr(st), a1 = a0 + 16384, b0 = a0 + 32768;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint32_t acc = (kc > 0 || kk > 0) ? 1u : 0u;
+          const uint64_t bd = tc::desc_sw128(b0 + 32 * kk);
+          tc::mma_f16(tmem, tc::desc_sw128(a0 + 32 * kk), bd, idesc, acc);
+          if (SPLIT) tc::mma_f16(tmem, tc::desc_sw128(a0 + 65536 + 32 * kk), bd, idesc, 1u);
+          if (rows > 128) {
+            tc::mma_f16(tmem + 256, tc::desc_sw128(a1 + 32 * kk), bd, idesc, acc);
+            if (SPLIT) tc::mma_f16(tmem + 256, tc::desc_sw128(a1 + 65536 + 32 * kk), bd, idesc, 1u);
+          }
+        }
+        tc::mma_commit(&mma_bar[s]);
+      }
+    }
+    {
+      const uint32_t last = chunk - 1;
+      if (!mbar_wait_bounded(&mma_bar[last % kPfStages], (last / kPfStages) & 1u, kWaitLimit)) ok = false;
+    }
+    tc::fence_after_sync();
+    // epilogue: warp w reads lanes 32*(w%4).. of each accumulator, column group w/4
+    const int q = warp & 3, cg = warp >> 2;
+    const uint32_t tq = tmem + ((uint32_t)(32 * q) << 16);
+    for (int h = 0; h < 2; ++h) {
+      if (h == 1 && rows <= 128) break;
+      const int m = h * 128 + 32 * q + lane;
+      const bool valid = m < rows;
+      if (PHASE == 0) {
+        const float sg = __ldg(p.scales + 4 * e + 0), su = __ldg(p.scales + 4 * e + 1);
+        float a[32];
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          uint32_t g16[16], u16[16];
+          tc::tmem_ld16(tq + h * 256 + 32 * cg + 16 * half, g16);
+          tc::tmem_ld16(tq + h * 256 + 128 + 32 * cg + 16 * half, u16);
+          tc::tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            a[16 * half + j] = silu_glu(__uint_as_float(g16[j]) * sg, __uint_as_float(u16[j]) * su);
+        }
+        if (valid) {
+          uint4* dst = reinterpret_cast<uint4*>(p.i16 + (size_t)(srow0 + m) * p.I + nt * 128 + 32 * cg);
+          if (p.mode == PF_W4A4) {
+#pragma unroll
+            for (int b = 0; b < 2; ++b) {
+              uint32_t sbyte, c0, c1, hw[8];
+              nvfp4_quant16(a + 16 * b, sbyte, c0, c1, hw);
+              dst[2 * b] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+              dst[2 * b + 1] = make_uint4(hw[4], hw[5], hw[6], hw[7]);
+            }
+          } else {
+            uint32_t qw[8], hw[16];
+            float dh, dfull;
+            int sum;
+            q8_1_quant32_f16(a, qw, dh, sum, dfull, hw);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) dst[i] = make_uint4(hw[4 * i], hw[4 * i + 1], hw[4 * i + 2], hw[4 * i + 3]);
+          }
+        }
+      } else {
+        const float sd = __ldg(p.scales + 4 * e + 2);
+        const int r = valid ? p.perm[srow0 + m] : 0;
+        const float f = valid ? sd * __ldg(p.w + r) : 0.f;
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          uint32_t v[32];
+          tc::tmem_ld32(tq + h * 256 + 64 * cg + 32 * cc, v);
+          tc::tmem_ld_wait();
+          if (valid) {
+            float4* dst = reinterpret_cast<float4*>(p.y + (size_t)r * p.H + nt * 256 + 64 * cg + 32 * cc);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              dst[i] = make_float4(__uint_as_float(v[4 * i]) * f, __uint_as_float(v[4 * i + 1]) * f,
+                                   __uint_as_float(v[4 * i + 2]) * f, __uint_as_float(v[4 * i + 3]) * f);
+          }
+        }
+      }
+    }
+    tc::fence_before_sync();
+  }
+  if (!ok) atomicOr(p.err, kErrTimeout);
+  __syncthreads();
+  tc::fence_after_sync();
+  if (warp == 0) tc::tmem_dealloc(tmem, 512);
+}
+
+size_t pf_gemm_smem() { return 1024 + (size_t)3 * 65536; }   // = 1024 + 2 * 98304
+
+// ------------------------------------------------------------------ P6: fixed-order combine
+
+// out[t][n] = bf16(sum over k = 0..K-1 of y[t*K+k][n]), valid routes only.
+__global__ void k_pf_combine(const __grid_constant__ PfParams p) {
+  const int nq = p.H / 4;
+  const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= (long long)p.T * nq) return;
+  const int t = (int)(idx / nq), n = 4 * (int)(idx - (long long)t * nq);
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int k = 0; k < p.K; ++k) {
+    const int r = t * p.K + k;
+    const int e = __ldg(p.ids + r);
+    if (e < 0 || e >= p.E) continue;
+    const float4 v = __ldcg(reinterpret_cast<const float4*>(p.y + (size_t)r * p.H + n));
+    acc.x += v.x;
+    acc.y += v.y;
+    acc.z += v.z;
+    acc.w += v.w;
+  }
+  uint2 o;
+  o.x = f32_to_bf16_bits_rn(acc.x) | (f32_to_bf16_bits_rn(acc.y) << 16);
+  o.y = f32_to_bf16_bits_rn(acc.z) | (f32_to_bf16_bits_rn(acc.w) << 16);
+  *reinterpret_cast<uint2*>(p.out + (size_t)t * p.H + n) = o;
+}
+
+// ------------------------------------------------------------------ launch
+
+cudaError_t launch_prefill(const PfParams& p, cudaStream_t stream) {
+  cudaError_t e;
+  const size_t ssort = pf_sort_smem(p.E);
+  if ((e = cudaFuncSetAttribute(k_pf_sort, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ssort)) != cudaSuccess)
+    return e;
+  k_pf_sort<<<1, kSortThreads, ssort, stream>>>(p);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  {
+    const long long n = (long long)p.T * (p.mode == PF_W4A4 ? p.H / 16 : p.H / 32);
+    k_pf_quant<<<(unsigned)((n + 255) / 256), 256, 0, stream>>>(p);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  const size_t sg = pf_gemm_smem();
+  if (p.mode == PF_W4A8) {
+    if ((e = cudaFuncSetAttribute(k_pf_gemm<0, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sg)) !=
+        cudaSuccess)
+      return e;
+    k_pf_gemm<0, true><<<sm_count(), kPfThreads, sg, stream>>>(p);
+  } else {
+    if ((e = cudaFuncSetAttribute(k_pf_gemm<0, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sg)) !=
+        cudaSuccess)
+      return e;
+    k_pf_gemm<0, false><<<sm_count(), kPfThreads, sg, stream>>>(p);
+  }
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if ((e = cudaFuncSetAttribute(k_pf_gemm<1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sg)) !=
+      cudaSuccess)
+    return e;
+  k_pf_gemm<1, false><<<sm_count(), kPfThreads, sg, stream>>>(p);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  {
+    const long long n = (long long)p.T * (p.H / 4);
+    k_pf_combine<<<(unsigned)((n + 255) / 256), 256, 0, stream>>>(p);
+  }
   return cudaGetLastError();
 }
 

@@ -37,3 +37,101 @@ def test_tc_gemm_matches_f64(K, N):
     bound = K * 2.0 ** -24 * (np.abs(a64) @ np.abs(b64).T) + 1e-30
     assert np.isfinite(got).all()
     assert (np.abs(got - want) <= bound).all(), float(np.max(np.abs(got - want) / bound))
+
+
+# ------------------------------------------------------------------ prompt path (grouped GEMMs)
+
+from oracle import formats as F  # noqa: E402
+from oracle import layer as OL  # noqa: E402
+from tests import cases  # noqa: E402
+
+# The prompt configuration's tolerances (relative L2 of the bf16 output against
+# the oracle's bf16 output): 1e-2 for W4A4, 2e-3 for W4A8.
+TOL_L2 = {0: 1e-2, 1: 2e-3}
+
+
+def _stable_sort(ids, E):
+    r = ids.reshape(-1).astype(np.int64)
+    valid = (r >= 0) & (r < E)
+    order = np.argsort(np.where(valid, r, E), kind="stable")
+    order = order[valid[order]]
+    off = np.zeros(E + 1, dtype=np.int64)
+    off[1:] = np.cumsum(np.bincount(r[valid], minlength=E))
+    return order, off
+
+
+def _x_quantized(case, mode):
+    x32 = F.bf16_bits_to_f64(case.x).astype(np.float32)
+    if mode == 0:
+        codes, sc = OL.quantize_nvfp4_act(x32)
+        packed = (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
+        return np.concatenate([packed, sc], axis=1).reshape(-1)
+    qs, d, s, _ = F.quantize_q8_1(x32)
+    return F.q8_1_pack_blocks(qs, d, s).reshape(-1)
+
+
+def _check_prefill(case, mode, tokens=None):
+    res = cases.run_prefill_gpu(case, mode)
+    g = case.geom
+    T = case.x.shape[0]
+    order, off = _stable_sort(case.ids, g.E)
+    assert np.array_equal(res["off"], off), "expert row offsets differ"
+    assert np.array_equal(res["perm"][: off[-1]], order), "sorted route order differs"
+    assert np.array_equal(res["xq"], _x_quantized(case, mode)), "quantized activations differ"
+    ref, ref_bits, st = cases.prefill_oracle(case, mode, tokens)
+    sel = np.arange(T) if tokens is None else np.asarray(tokens)
+    got = F.bf16_bits_to_f64(res["out"][sel])
+    refb = F.bf16_bits_to_f64(ref_bits)
+    assert np.isfinite(got).all()
+    rel_l2 = np.linalg.norm(got - refb) / max(np.linalg.norm(refb), 1e-30)
+    rel_l2_f64 = np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-30)
+    assert rel_l2 <= TOL_L2[mode], (rel_l2, rel_l2_f64)
+    # the requantized intermediate of the checked routes: most values equal
+    # the oracle's exactly (a value may differ where the fp32 and fp64
+    # intermediates round to different codes; W4A4 values are exact in fp16)
+    pos = np.full(case.ids.size, -1, dtype=np.int64)
+    pos[order] = np.arange(order.size)
+    eq = tot = 0
+    for i, t in enumerate(sel):
+        for k in range(g.top_k):
+            if not st["valid"][i, k]:
+                continue
+            row = res["i16"][pos[t * g.top_k + k]].astype(np.float64)
+            want = st["inter_hat"][i, k]
+            if mode == 1:   # the exported W4A8 operand is q*d rounded once to fp16
+                want = want.astype(np.float16).astype(np.float64)
+            eq += int(np.sum(row == want))
+            tot += row.size
+    assert eq >= 0.99 * tot, (eq, tot)
+    return res, rel_l2
+
+
+def _ragged_ids(T, E, K, seed):
+    """Expert 0 gets every token's first route (more than two 128-row tiles),
+    the rest spread unevenly, one expert gets none, one route is invalid."""
+    r = np.random.default_rng(seed)
+    ids = np.zeros((T, K), dtype=np.int32)
+    for t in range(T):
+        others = r.choice(np.arange(1, E - 1), size=K - 1, replace=False, p=None)
+        ids[t, 1:] = others
+    ids[T // 2, K - 1] = E + 3
+    return ids
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_prefill_ragged_small(mode):
+    """H=256 I=256 E=8 top-3, T=300: one expert with 300 rows (two tiles, the
+    second partly filled), uneven others, an empty expert, a bad id."""
+    T, E, K = 300, 8, 3
+    case = cases.make_prefill_case(256, 256, E, K, T, seed=200 + mode, ids=_ragged_ids(T, E, K, 7))
+    res, _ = _check_prefill(case, mode)
+    assert res["err"] & capi.MOE_DEVERR_BAD_ID
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_prefill_qwen3_30b_a3b_shaped_chunk(mode):
+    """H=2048 I=768 E=128 top-8, a 4096-token chunk (32768 routed rows); the
+    oracle checks a sample of tokens, the sort and the quantized x in full."""
+    case = cases.make_prefill_case(2048, 768, 128, 8, 4096, seed=300 + mode)
+    res, rel = _check_prefill(case, mode, tokens=[0, 1, 2047, 4095])
+    assert res["err"] == 0
