@@ -4,15 +4,18 @@ Default workload (the headline line): the Qwen3-30B-A3B-shaped NVFP4 decode
 layer -- H=2048, I=768, E=128 experts, top-8, T=1 token -- as a stack of 48
 distinct resident layer banks (48 x 340 MB, far beyond the 129 MB L2), each
 with its own softmax top-8 routing of N(0,1) logits.  One step = one token
-through all 48 layers (48 moe_decode calls = 144 kernels), replayed from one
-CUDA graph.  value = layer-tokens/s (tokens x layers / s).
+through all 48 layers (48 moe_decode calls, one fused kernel each at T=1),
+replayed from one CUDA graph.  value = layer-tokens/s (tokens x layers / s).
 
 Also reported in the same line: the 47-layer Laguna-shaped stack (39 Q4_K +
 8 BF16 layers, H=4096, I=768, E=256, top-10, Zipf(1.1) routing, 85.4 GiB
 resident) at T = 1, 4, 16, 64 as stack tokens/s, and the NVFP4 layer at T=8.
 
-Roofline: the timed unit is one moe_decode pass (k_prep + k_gate_up + k_down,
-chained with programmatic dependent launch so they overlap); achieved GB/s =
+Also reported: the prompt path (moe_prefill_grouped) on a 4096-token chunk of
+the same NVFP4 layer, W4A4 and W4A8, as tokens/s and tensor TFLOP/s.
+
+Roofline: the timed unit is one moe_decode pass (at T=1 one k_layer_small
+launch); achieved GB/s =
 the algorithmic bytes of a pass (each routed expert's gate_up and down rows
 once, plus x, ids, weights and out) / the pass's average duration from CUDA
 events on the launching stream.  Peak = MEASURED_PEAKS.json hbm_gbs.
@@ -52,6 +55,13 @@ def peaks():
     return 6800.0, "fallback"
 
 
+def bf16_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        return float(json.load(open(p))["bf16_tflops"]), "measured"
+    return 1900.0, "fallback"
+
+
 # ------------------------------------------------------------------ clocks
 
 class ClockSampler:
@@ -70,7 +80,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "20"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
         except FileNotFoundError:
@@ -152,6 +162,7 @@ class Stack:
             L["ids"] = torch.from_numpy(ids).to(self.dev)
             L["w"] = torch.from_numpy(w).to(self.dev)
         self.ws_bytes = max(capi.moe_workspace_bytes(L["bank"], T) for L in self.layers)
+        self.launches_per_step = sum(capi.moe_decode_kernel_count(L["bank"], T) for L in self.layers)
         self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=self.dev)
         capi.moe_workspace_init(self.ws.data_ptr(), self.ws_bytes, torch.cuda.current_stream().cuda_stream)
         g = np.random.default_rng(seed)
@@ -197,34 +208,43 @@ class Stack:
         return e0.elapsed_time(e1) / steps   # ms per step
 
     def time_e2e(self, steps, warmup):
-        """Per step: pinned host -> device copies of x, ids and weights, the
-        graph replay, and the device -> host copy of the outputs."""
-        torch = self.torch
+        """End to end through the C ABI's host-buffer entry point: per step,
+        every layer's moe_decode_host copies its x, ids and weights from
+        pinned host memory, decodes and copies its output back to pinned host
+        memory (48 calls captured in one CUDA graph); the step ends when the
+        host has the outputs."""
+        torch, capi = self.torch, self.capi
         s = self.stream
-        hx = self.x.cpu().pin_memory()
+        T = self.T
+        hx = [self.x[l].cpu().view(torch.int16).pin_memory() for l in range(self.NL)]
         hids = [L["ids"].cpu().pin_memory() for L in self.layers]
         hw = [L["w"].cpu().pin_memory() for L in self.layers]
-        hout = torch.empty(self.out.shape, dtype=self.out.dtype, pin_memory=True)
-        h2d = hx.numel() * 2 + sum(t.numel() * 4 for t in hids) + sum(t.numel() * 4 for t in hw)
-        d2h = hout.numel() * 2
+        hout = [torch.empty((T, self.H), dtype=torch.int16).pin_memory() for _ in range(self.NL)]
+        iob = max(capi.moe_decode_io_bytes(L["bank"], T) for L in self.layers)
+        io = torch.empty((self.NL, iob), dtype=torch.uint8, device=self.dev)
+        h2d = sum(t.numel() * 2 for t in hx) + sum(t.numel() * 4 for t in hids) + sum(t.numel() * 4 for t in hw)
+        d2h = sum(t.numel() * 2 for t in hout)
 
-        def one():
-            self.x.copy_(hx, non_blocking=True)
-            for L, a, b in zip(self.layers, hids, hw):
-                L["ids"].copy_(a, non_blocking=True)
-                L["w"].copy_(b, non_blocking=True)
-            self.graph.replay()
-            hout.copy_(self.out, non_blocking=True)
+        def launch(sp):
+            for l, L in enumerate(self.layers):
+                capi.moe_decode_host(L["bank"], hx[l].data_ptr(), T, hids[l].data_ptr(), hw[l].data_ptr(),
+                                     hout[l].data_ptr(), io[l].data_ptr(), iob, self.ws.data_ptr(), self.ws_bytes, sp)
 
+        s.wait_stream(torch.cuda.current_stream())
         with torch.cuda.stream(s):
+            launch(s.cuda_stream)
+            s.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=s):
+                launch(s.cuda_stream)
             for _ in range(warmup):
-                one()
+                g.replay()
             s.synchronize()
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
             e0.record(s)
             for _ in range(steps):
-                one()
+                g.replay()
                 s.synchronize()
             e1.record(s)
             e1.synchronize()
@@ -234,6 +254,69 @@ class Stack:
         for L in self.layers:
             self.capi.moe_bank_destroy(L["bank"])
         self.layers = []
+
+
+# ------------------------------------------------------------------ prompt path
+
+PREFILL = dict(H=2048, I=768, E=128, K=8, T=4096)
+
+
+def prefill_flops(c):
+    """Algorithmic FLOPs of one chunk: 2 per multiply-add of gate_up (2I x H)
+    and down (H x I) for every routed row."""
+    return 2.0 * c["T"] * c["K"] * (2 * c["I"] * c["H"] + c["H"] * c["I"])
+
+
+def bench_prefill(dev, steps, warmup, mode, bf16_peak):
+    """One NVFP4 layer (H=2048, I=768, E=128, top-8), a 4096-token chunk
+    (32,768 routed rows) through moe_prefill_grouped; CUDA events around
+    `steps` calls on one stream (weights 340 MB, beyond L2)."""
+    import torch
+
+    from quantized_routed_expert_route_gb300 import capi
+    from synth import banks as S
+    from synth import counter as C
+    c = PREFILL
+    H, I, E, K, T = c["H"], c["I"], c["E"], c["K"], c["T"]
+    rb_gu, rb_dn = row_bytes(NVFP4, H), row_bytes(NVFP4, I)
+    gu = torch.empty(E * 2 * I * rb_gu + 16, dtype=torch.uint8, device=dev)
+    dn = torch.empty(E * H * rb_dn + 16, dtype=torch.uint8, device=dev)
+    C.fill_bank_torch(gu[: E * 2 * I * rb_gu], 4001, NVFP4, H)
+    C.fill_bank_torch(dn[: E * H * rb_dn], 4002, NVFP4, I)
+    sb = torch.from_numpy(S.counter_scale_bank(4003, E, NVFP4, NVFP4)).to(dev)
+    stream = torch.cuda.current_stream().cuda_stream
+    geom = capi.moe_layer_geom(H, I, E, K, NVFP4, NVFP4)
+    bank = capi.moe_bank_create(geom, gu.data_ptr(), E * 2 * I * rb_gu, dn.data_ptr(), E * H * rb_dn, sb.data_ptr(),
+                                capi.MOE_SRC_DEVICE_BORROW, stream)
+    ids, w = S.softmax_topk_routing(4004, T, E, K)
+    x = torch.from_numpy(S.hidden_bf16(4005, T, H).view(np.int16)).to(dev)
+    idsd, wd = torch.from_numpy(ids).to(dev), torch.from_numpy(w).to(dev)
+    out = torch.empty((T, H), dtype=torch.int16, device=dev)
+    wsb = capi.moe_prefill_workspace_bytes(bank, T, mode)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
+
+    def call():
+        capi.moe_prefill_grouped(bank, x.data_ptr(), T, idsd.data_ptr(), wd.data_ptr(), mode, out.data_ptr(),
+                                 ws.data_ptr(), wsb, stream)
+
+    for _ in range(warmup):
+        call()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        call()
+    e1.record()
+    e1.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    err = capi.moe_get_error(ws.data_ptr(), wsb, stream)
+    capi.moe_bank_destroy(bank)
+    tflops = prefill_flops(c) / (ms / 1e3) / 1e12
+    return {"mode": "W4A4" if mode == 0 else "W4A8", "ms_per_chunk": ms, "tok_per_s": T / (ms / 1e3),
+            "tflops": tflops, "mma": "tcgen05 kind::f16 (exact fp16 operands, fp32 accumulation)",
+            "frac_of_measured_bf16_peak": tflops / bf16_peak,
+            "frac_of_nominal_fp4_peak": tflops / 13500.0, "device_error_bits": err,
+            "launches_per_chunk": 5}
 
 
 # ------------------------------------------------------------------ CPU oracle timing
@@ -320,20 +403,28 @@ def dist_setup(n):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=400)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--layers", type=int, default=48)
     ap.add_argument("--no-stack", action="store_true", help="skip the 47-layer Laguna sweep")
+    ap.add_argument("--no-prefill", action="store_true", help="skip the prompt-path chunk")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--cpu-oracle-worker", type=float, default=None, help=argparse.SUPPRESS)
     ap.add_argument("--profile-layer", choices=["nvfp4", "q4_k", "bf16"], default=None,
                     help="run --steps eager decode passes of one layer type (for ncu), print nothing else")
     ap.add_argument("--T", type=int, default=1)
+    ap.add_argument("--profile-prefill", choices=["w4a4", "w4a8"], default=None,
+                    help="run --steps prompt-path chunks (for ncu), print nothing else")
     a = ap.parse_args()
 
     if a.profile_layer:
         profile_layer(a)
+        return
+    if a.profile_prefill:
+        import torch
+        r = bench_prefill("cuda:0", a.steps, 1, 0 if a.profile_prefill == "w4a4" else 1, bf16_peak()[0])
+        print(json.dumps(r))
         return
 
     if a.cpu_oracle_worker is not None:
@@ -385,7 +476,8 @@ def main():
     value = units / (t_max / 1e3)
     per_pass_ms = ms / a.layers
     achieved = st.bytes_per_step / a.layers / (per_pass_ms / 1e3) / 1e9
-    e2e_ms, h2d, d2h = st.time_e2e(max(10, a.steps // 2), a.warmup)
+    launches = st.launches_per_step * a.steps
+    e2e_ms, h2d, d2h = st.time_e2e(max(10, a.steps // 4), a.warmup)
     e2e_val = units / (e2e_ms / 1e3)
     extra = {"per_layer_us": per_pass_ms * 1e3, "bytes_per_layer": st.bytes_per_step / a.layers,
              "unique_experts_per_layer": float(np.mean(st.unique_per_layer))}
@@ -406,7 +498,7 @@ def main():
         st = Stack(types, L["H"], L["I"], L["E"], L["K"], 3, dev)
         for T in (1, 4, 16, 64):
             st.prepare(T, "zipf", 3 + T)
-            msT = st.time_replays(max(5, a.steps // 5), a.warmup)
+            msT = st.time_replays(max(5, min(20, a.steps // 5)), a.warmup)
             sweep[f"T={T}"] = {"stack_tok_per_s": T / (msT / 1e3), "ms_per_stack": msT,
                                "hbm_gbs": st.bytes_per_step / (msT / 1e3) / 1e9,
                                "frac": st.bytes_per_step / (msT / 1e3) / 1e9 / hbm_peak,
@@ -415,6 +507,15 @@ def main():
         del st
         torch.cuda.empty_cache()
         extra["laguna_47_layer_stack"] = sweep
+
+    if not a.no_prefill:
+        pk, pk_kind = bf16_peak()
+        extra["prefill_4096_token_chunk"] = {
+            "workload": "nvfp4 layer H=2048 I=768 E=128 top-8, 4096 tokens (32768 routed rows)",
+            "peak_tflops": pk, "peak_kind": pk_kind, "gflop_per_chunk": prefill_flops(PREFILL) / 1e9,
+            "w4a4": bench_prefill(dev, max(3, min(20, a.steps // 20)), a.warmup, 0, pk),
+            "w4a8": bench_prefill(dev, max(3, min(20, a.steps // 20)), a.warmup, 1, pk)}
+        torch.cuda.empty_cache()
 
     cpu = run_cpu_baseline(a.cpu_seconds) if (rank == 0 and a.cpu_seconds > 0) else None
     if rank == 0:
@@ -429,10 +530,10 @@ def main():
                        "parallelism": f"replicas x{world}"},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                          "frac": achieved / hbm_peak, "traffic": None, "peak_kind": peak_kind,
-                         "kernel": "moe_decode pass (k_prep+k_gate_up+k_down, PDL-overlapped)"},
+                         "kernel": "k_layer_small (one fused launch per moe_decode pass at T=1)"},
             "clocks": clk.summary(),
             "e2e": {"value": e2e_val, "unit": "layer-tok/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-            "gpu_launches": 3 * a.layers * a.steps,
+            "gpu_launches": launches,
             "cpu_baseline": cpu,
             "extra": extra,
         }

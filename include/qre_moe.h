@@ -201,6 +201,24 @@ int moe_prefill_grouped(const moe_bank* bank, const void* x, int32_t T,
                         const int32_t* topk_ids, const float* topk_w, int32_t mode,
                         void* out, void* ws, size_t ws_bytes, void* stream);
 
+/* Number of kernels one moe_decode call of T tokens launches on this bank
+ * (for graph builders and launch accounting), or a negative status. */
+int moe_decode_kernel_count(const moe_bank* bank, int32_t T);
+
+/* Device staging bytes moe_decode_host needs for T tokens (0 on bad arguments). */
+size_t moe_decode_io_bytes(const moe_bank* bank, int32_t T);
+
+/* moe_decode on host buffers: copies x (bf16 [T, H]), topk_ids (int32 [T, K])
+ * and topk_w (fp32 [T, K]) from the host into `io` (device, 256-byte aligned,
+ * >= moe_decode_io_bytes(bank, T) bytes), decodes, and copies the bf16
+ * [T, H] result back to `out` on the host, all asynchronous on `stream`
+ * (host buffers must be pinned for the copies to overlap and to be
+ * capturable in a CUDA graph; the result is in `out` once the stream has
+ * reached this point).  Workspace as for moe_decode. */
+int moe_decode_host(const moe_bank* bank, const void* x, int32_t T,
+                    const int32_t* topk_ids, const float* topk_w, void* out,
+                    void* io, size_t io_bytes, void* ws, size_t ws_bytes, void* stream);
+
 /* Read and clear the workspace's sticky device error bits (synchronizes
  * `stream`).  *dev_err receives the MOE_DEVERR_* bits; returns MOE_EDEVICE if
  * any was set, MOE_OK otherwise. */

@@ -27,6 +27,7 @@ EXPORTS = (
     "moe_status_string", "moe_last_cuda_error", "moe_quantize_q8_1",
     "moe_debug_block_dots", "moe_debug_decode_stages", "moe_decode_noalloc", "moe_debug_tc_gemm",
     "moe_prefill_workspace_bytes", "moe_prefill_grouped", "moe_debug_prefill_stages",
+    "moe_decode_kernel_count", "moe_decode_io_bytes", "moe_decode_host",
 )
 
 
@@ -69,6 +70,9 @@ def _load() -> ctypes.CDLL:
         "moe_decode_noalloc": (ctypes.c_int, [vp, vp, i32, vp, vp, vp, vp]),
         "moe_debug_tc_gemm": (ctypes.c_int, [vp, vp, i32, i32, vp, vp, vp]),
         "moe_prefill_workspace_bytes": (sz, [vp, i32, i32]),
+        "moe_decode_kernel_count": (ctypes.c_int, [vp, i32]),
+        "moe_decode_io_bytes": (sz, [vp, i32]),
+        "moe_decode_host": (ctypes.c_int, [vp, vp, i32, vp, vp, vp, vp, sz, vp, sz, vp]),
         "moe_prefill_grouped": (ctypes.c_int, [vp, vp, i32, vp, vp, i32, vp, vp, sz, vp]),
         "moe_debug_prefill_stages": (ctypes.c_int, [vp, vp, i32, vp, vp, i32, vp, vp, sz, vp, vp, vp, vp, vp]),
     }
@@ -185,3 +189,21 @@ def moe_debug_prefill_stages(bank: int, x: int, T: int, topk_ids: int, topk_w: i
     _check(_lib.moe_debug_prefill_stages(bank, x, T, topk_ids, topk_w, mode, out, ws, ws_bytes, stream or None,
                                          xq or None, off or None, perm or None, i16 or None),
            "moe_debug_prefill_stages")
+
+
+def moe_decode_kernel_count(bank: int, T: int) -> int:
+    n = int(_lib.moe_decode_kernel_count(bank, T))
+    if n < 0:
+        raise MoeError(n, "moe_decode_kernel_count")
+    return n
+
+
+def moe_decode_io_bytes(bank: int, T: int) -> int:
+    return int(_lib.moe_decode_io_bytes(bank, T))
+
+
+def moe_decode_host(bank: int, x: int, T: int, topk_ids: int, topk_w: int, out: int, io: int, io_bytes: int, ws: int,
+                    ws_bytes: int, stream: int = 0) -> None:
+    """moe_decode with x, ids, weights and out in (pinned) host memory; io is device staging."""
+    _check(_lib.moe_decode_host(bank, x, T, topk_ids, topk_w, out, io, io_bytes, ws, ws_bytes, stream or None),
+           "moe_decode_host")

@@ -374,6 +374,65 @@ int moe_decode(const moe_bank* b, const void* x, int32_t T, const int32_t* ids, 
   return decode_impl(b, x, T, ids, w, out, ws, ws_bytes, stream, nullptr);
 }
 
+int moe_decode_kernel_count(const moe_bank* b, int32_t T) {
+  if (!b || T < 0) return MOE_EINVAL;
+  const moe_layer_geom& g = b->geom;
+  const Shape sh = decode_shape(g);
+  const int tc = T < sh.t_chunk ? T : sh.t_chunk;
+  int n = 0;
+  for (int t0 = 0; t0 < T; t0 += tc) {
+    const int tn = (T - t0) < tc ? (T - t0) : tc;
+    const WsLayout L = ws_layout(g, tn);
+    const DecodeParams p = make_params(b, L, nullptr, sh, tn);
+    n += p.use_ls ? 1 : (p.maxnt != 1 ? 3 : 2);
+  }
+  return n;
+}
+
+namespace {
+struct IoLayout {
+  size_t x, ids, w, out, total;
+};
+IoLayout io_layout(const moe_layer_geom& g, int T) {
+  IoLayout L;
+  size_t o = 0;
+  L.x = o; o = align_up(o + 2 * (size_t)T * g.H, 256);
+  L.ids = o; o = align_up(o + 4 * (size_t)T * g.top_k, 256);
+  L.w = o; o = align_up(o + 4 * (size_t)T * g.top_k, 256);
+  L.out = o; o = align_up(o + 2 * (size_t)T * g.H, 256);
+  L.total = o;
+  return L;
+}
+}  // namespace
+
+size_t moe_decode_io_bytes(const moe_bank* b, int32_t T) {
+  if (!b || T < 1) return 0;
+  return io_layout(b->geom, T).total;
+}
+
+int moe_decode_host(const moe_bank* b, const void* x, int32_t T, const int32_t* ids, const float* w, void* out,
+                    void* io, size_t io_bytes, void* ws, size_t ws_bytes, void* stream) {
+  if (!b || T < 0) return MOE_EINVAL;
+  if (T == 0) return MOE_OK;
+  if (!x || !ids || !w || !out || !io || !aligned(io, 256)) return MOE_EINVAL;
+  const moe_layer_geom& g = b->geom;
+  const IoLayout L = io_layout(g, T);
+  if (io_bytes < L.total) return MOE_EINVAL;
+  uint8_t* d = static_cast<uint8_t*>(io);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if ((e = cudaMemcpyAsync(d + L.x, x, 2 * (size_t)T * g.H, cudaMemcpyHostToDevice, s)) != cudaSuccess ||
+      (e = cudaMemcpyAsync(d + L.ids, ids, 4 * (size_t)T * g.top_k, cudaMemcpyHostToDevice, s)) != cudaSuccess ||
+      (e = cudaMemcpyAsync(d + L.w, w, 4 * (size_t)T * g.top_k, cudaMemcpyHostToDevice, s)) != cudaSuccess)
+    return cuda_fail(e, "decode_host: inputs to device");
+  const int st = decode_impl(b, d + L.x, T, reinterpret_cast<const int32_t*>(d + L.ids),
+                             reinterpret_cast<const float*>(d + L.w), d + L.out, ws, ws_bytes, stream, nullptr);
+  if (st) return st;
+  if ((e = cudaMemcpyAsync(out, d + L.out, 2 * (size_t)T * g.H, cudaMemcpyDeviceToHost, s)) != cudaSuccess)
+    return cuda_fail(e, "decode_host: output to host");
+  return MOE_OK;
+}
+
 // ------------------------------------------------------------------ decode without allocation
 //
 // The workspace of moe_decode_noalloc: a file-scope device array, so the call

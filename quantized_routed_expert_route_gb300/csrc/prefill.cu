@@ -284,16 +284,60 @@ __global__ void k_pf_quant(const __grid_constant__ PfParams p) {
 
 // ------------------------------------------------------------------ P3 / P4: grouped GEMMs
 
-constexpr int kPfThreads = 512;     // 16 warps: all expand operands, one thread issues MMAs, all run the epilogue
+constexpr int kPfThreads = 512;     // 16 warps: all stage operands, one thread issues MMAs, all run the epilogue
 constexpr int kPfTileRows = 256;
 constexpr int kPfMaxStages = 3;
-// Stage layout: A rows 0..127 (16 KB), A rows 128..255 (16 KB), B 256 rows
-// (32 KB), and with SPLIT the low parts of A rows 0..127 and 128..255.
+constexpr uint32_t kSpinLimit = 1u << 24;   // polls of an MMA barrier (each returns within ~1 us) before giving up
+constexpr int kPfBRawBytes = 9216;  // raw NVFP4 of 256 weight rows x 64 values: 32 code bytes + 4 scale bytes each
+
+// Shared-memory plan of the GEMM (1024-byte aligned base):
+//   A stages  [NS][A rows 0..127 | A rows 128..255 (| low parts, SPLIT)]
+//   B16       [2][256 rows x 64 fp16, swizzled]         (the MMA's B operand)
+//   Braw      [NS][256 x 32 code bytes | 256 x 4 scale bytes]
+// A and Braw of chunk c + NS - 1 are copied (cp.async) while chunk c is
+// expanded and multiplied.
 template <bool SPLIT>
-struct PfStage {
+struct PfPlan {
   static constexpr int kStages = SPLIT ? 2 : 3;
-  static constexpr int kBytes = SPLIT ? 98304 : 65536;
+  static constexpr int kABytes = SPLIT ? 65536 : 32768;
+  static constexpr int kB16Off = kStages * kABytes;
+  static constexpr int kBRawOff = kB16Off + 2 * 32768;
+  static constexpr int kBytes = kBRawOff + kStages * kPfBRawBytes;
 };
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(valid ? 16 : 0) : "memory");
+}
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Issue the copies of K chunk kc of the current tile into A stage / Braw stage.
+template <int PHASE, bool SPLIT>
+__device__ __forceinline__ void pf_prefetch(const PfParams& p, const int* arow, const uint8_t* brp, int kc, int Kd,
+                                            uint8_t* astage, uint8_t* braw, int tid) {
+  const uint16_t* asrc = PHASE == 0 ? p.x16 : p.i16;
+  const int k0 = kc * 64;
+  constexpr int NA = SPLIT ? 8 : 4;
+#pragma unroll
+  for (int j = 0; j < NA; ++j) {
+    const int i = tid + (j & 3) * kPfThreads;
+    const int m = i >> 3, c = i & 7;
+    const int src = arow[m];
+    const uint16_t* as = (j < 4) ? asrc : p.x16lo;
+    const uint16_t* g = as + (size_t)(src >= 0 ? src : 0) * Kd + k0 + 8 * c;
+    cp_async16(smem_addr(astage + (j < 4 ? 0 : 32768) + (m < 128 ? 0 : 16384) + tc::sw128_chunk(m & 127, c)), g,
+               src >= 0);
+  }
+  const int brow = tid >> 1, bh = tid & 1;
+  cp_async16(smem_addr(braw + brow * 32 + 16 * bh), brp + (k0 + 32 * bh) / 2, true);
+  if (bh == 0) cp_async4(smem_addr(braw + 8192 + brow * 4), brp + Kd / 2 + k0 / 16);
+}
 
 // PHASE 0: gate_up (K = H; B rows = 128 gate + 128 up rows; epilogue GLU +
 // requant); PHASE 1: down (K = I; B rows = 256 output rows; epilogue scales).
@@ -301,15 +345,15 @@ struct PfStage {
 // product is formed as hi*B + lo*B into the same accumulator.
 template <int PHASE, bool SPLIT>
 __global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(const __grid_constant__ PfParams p) {
-  constexpr int kPfStages = PfStage<SPLIT>::kStages;
-  constexpr int kPfStageBytes = PfStage<SPLIT>::kBytes;
+  using Plan = PfPlan<SPLIT>;
+  constexpr int NS = Plan::kStages;
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t mma_bar[kPfMaxStages];
   __shared__ uint32_t tmem_base;
   __shared__ int tile_pre[kMaxE + 1];
   __shared__ int wsum[33];
   __shared__ int arow[kPfTileRows];
-  uint8_t* stages = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+  uint8_t* base = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int E = p.E;
   const int NT = PHASE == 0 ? p.I / 128 : p.H / 256;   // column tiles per expert
@@ -326,7 +370,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(const __grid_constant
     tc::tmem_relinquish();
   }
   if (tid == 0) {
-    for (int s = 0; s < kPfStages; ++s) mbar_init(&mma_bar[s], 1);
+    for (int s = 0; s < NS; ++s) mbar_init(&mma_bar[s], 1);
     fence_mbar_init();
   }
   tc::fence_before_sync();
@@ -334,8 +378,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(const __grid_constant
   tc::fence_after_sync();
   const uint32_t tmem = tmem_base;
   const uint32_t idesc = tc::idesc_f16(128, 256, false);
-  const uint16_t* asrc = PHASE == 0 ? p.x16 : p.i16;
-  uint32_t chunk = 0;
+  uint32_t chunk = 0;   // chunks multiplied so far (all tiles): picks the stage and barrier phase
   bool ok = true;
   for (int t = blockIdx.x; t < total; t += gridDim.x) {
     // the expert of tile t: the largest e with tile_pre[e] <= t (never an empty one)
@@ -361,36 +404,29 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(const __grid_constant
     const size_t bsrc_row = PHASE == 0 ? ((size_t)e * 2 * p.I + (brow < 128 ? nt * 128 + brow : p.I + nt * 128 + brow - 128))
                                        : ((size_t)e * p.H + (size_t)nt * 256 + brow);
     const uint8_t* brp = (PHASE == 0 ? p.gu_bank : p.dn_bank) + bsrc_row * rb;
+    // prologue: chunks 0 .. NS-2 in flight (their stages were last read by
+    // MMAs this thread already waited for at the end of the previous tile)
+#pragma unroll
+    for (int j = 0; j < NS - 1; ++j) {
+      if (j < nK) {
+        const uint32_t s = (chunk + j) % NS;
+        pf_prefetch<PHASE, SPLIT>(p, arow, brp, j, Kd, base + s * Plan::kABytes,
+                                  base + Plan::kBRawOff + s * kPfBRawBytes, tid);
+      }
+      cp_async_commit();
+    }
     for (int kc = 0; kc < nK; ++kc, ++chunk) {
-      const uint32_t s = chunk % kPfStages;
-      uint8_t* st = stages + (size_t)s * kPfStageBytes;
-      const int k0 = kc * 64;
-      // operand loads first (A: four 16-byte chunks; B: 32 NVFP4 values)
-      constexpr int NA = SPLIT ? 8 : 4;
-      uint4 av[NA];
-#pragma unroll
-      for (int j = 0; j < NA; ++j) {
-        const int i = tid + (j & 3) * kPfThreads;
-        const int src = arow[i >> 3];
-        const uint16_t* as = (j < 4) ? asrc : p.x16lo;
-        av[j] = (src >= 0) ? __ldcg(reinterpret_cast<const uint4*>(as + (size_t)src * Kd + k0 + 8 * (i & 7)))
-                           : make_uint4(0u, 0u, 0u, 0u);
-      }
-      const int kabs = k0 + 32 * bh;
-      const uint4 cw = __ldg(reinterpret_cast<const uint4*>(brp + kabs / 2));
-      const uint16_t sw = __ldg(reinterpret_cast<const uint16_t*>(brp + Kd / 2 + kabs / 16));
-      if (chunk >= (uint32_t)kPfStages) {
-        // the MMAs that last read this stage are done
-        if (!mbar_wait_bounded(&mma_bar[s], ((chunk - kPfStages) / kPfStages) & 1u, kWaitLimit)) ok = false;
-      }
-#pragma unroll
-      for (int j = 0; j < NA; ++j) {
-        const int i = tid + (j & 3) * kPfThreads;
-        const int m = i >> 3, c = i & 7;
-        *reinterpret_cast<uint4*>(st + (j < 4 ? 0 : 65536) + (m < 128 ? 0 : 16384) + tc::sw128_chunk(m & 127, c)) =
-            av[j];
-      }
+      const uint32_t s = chunk % NS;
+      uint8_t* ast = base + s * Plan::kABytes;
+      const uint8_t* braw = base + Plan::kBRawOff + s * kPfBRawBytes;
+      uint8_t* b16 = base + Plan::kB16Off + (chunk & 1u) * 32768;
+      cp_async_wait<NS - 2>();   // this thread's copies of chunk kc have landed
+      fence_proxy_async_smem();
+      __syncthreads();           // everyone's copies of chunk kc are visible; MMA(chunk - 2) is done (see below)
       {
+        // expand this thread's 32 NVFP4 weight values to fp16 (code * scale, exact)
+        const uint4 cw = *reinterpret_cast<const uint4*>(braw + brow * 32 + 16 * bh);
+        const uint16_t sw = *reinterpret_cast<const uint16_t*>(braw + 8192 + brow * 4 + 2 * bh);
         const uint32_t s2 = tc::ue4m3x2_to_f16x2(sw);
         const uint32_t s0 = prmt(s2, 0u, 0x1010u), s1 = prmt(s2, 0u, 0x3232u);
         const uint32_t cws[4] = {cw.x, cw.y, cw.z, cw.w};
@@ -399,7 +435,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(const __grid_constant
           uint32_t h[4];
           tc::e2m1x8_to_f16x8(cws[q], h);
           const uint32_t sc = q < 2 ? s0 : s1;
-          *reinterpret_cast<uint4*>(st + 32768 + tc::sw128_chunk(brow, 4 * bh + q)) =
+          *reinterpret_cast<uint4*>(b16 + tc::sw128_chunk(brow, 4 * bh + q)) =
               make_uint4(tc::hmul2(h[0], sc), tc::hmul2(h[1], sc), tc::hmul2(h[2], sc), tc::hmul2(h[3], sc));
         }
       }
@@ -407,24 +443,36 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(const __grid_constant
       __syncthreads();
       if (tid == 0) {
         tc::fence_after_sync();
-        const uint32_t a0 = smem_addr(st), a1 = a0 + 16384, b0 = a0 + 32768;
+        const uint32_t a0 = smem_addr(ast), a1 = a0 + 16384, b0 = smem_addr(b16);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
           const uint32_t acc = (kc > 0 || kk > 0) ? 1u : 0u;
           const uint64_t bd = tc::desc_sw128(b0 + 32 * kk);
           tc::mma_f16(tmem, tc::desc_sw128(a0 + 32 * kk), bd, idesc, acc);
-          if (SPLIT) tc::mma_f16(tmem, tc::desc_sw128(a0 + 65536 + 32 * kk), bd, idesc, 1u);
+          if (SPLIT) tc::mma_f16(tmem, tc::desc_sw128(a0 + 32768 + 32 * kk), bd, idesc, 1u);
           if (rows > 128) {
             tc::mma_f16(tmem + 256, tc::desc_sw128(a1 + 32 * kk), bd, idesc, acc);
-            if (SPLIT) tc::mma_f16(tmem + 256, tc::desc_sw128(a1 + 65536 + 32 * kk), bd, idesc, 1u);
+            if (SPLIT) tc::mma_f16(tmem + 256, tc::desc_sw128(a1 + 32768 + 32 * kk), bd, idesc, 1u);
           }
         }
         tc::mma_commit(&mma_bar[s]);
       }
+      // Chunk kc + NS - 1 goes to the stage that MMA(chunk - 1) read: wait for
+      // it (this also covers the B16 buffer that chunk + 1 will overwrite).
+      if (chunk >= 1) {
+        const uint32_t pc = chunk - 1;
+        if (!mbar_wait_spin(&mma_bar[pc % NS], (pc / NS) & 1u, kSpinLimit)) ok = false;
+      }
+      if (kc + NS - 1 < nK) {
+        const uint32_t s2 = (chunk + NS - 1) % NS;
+        pf_prefetch<PHASE, SPLIT>(p, arow, brp, kc + NS - 1, Kd, base + s2 * Plan::kABytes,
+                                  base + Plan::kBRawOff + s2 * kPfBRawBytes, tid);
+      }
+      cp_async_commit();
     }
     {
       const uint32_t last = chunk - 1;
-      if (!mbar_wait_bounded(&mma_bar[last % kPfStages], (last / kPfStages) & 1u, kWaitLimit)) ok = false;
+      if (!mbar_wait_spin(&mma_bar[last % NS], (last / NS) & 1u, kSpinLimit)) ok = false;
     }
     tc::fence_after_sync();
     // epilogue: warp w reads lanes 32*(w%4).. of each accumulator, column group w/4
@@ -493,7 +541,10 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(const __grid_constant
   if (warp == 0) tc::tmem_dealloc(tmem, 512);
 }
 
-size_t pf_gemm_smem() { return 1024 + (size_t)3 * 65536; }   // = 1024 + 2 * 98304
+size_t pf_gemm_smem() {
+  constexpr int a = PfPlan<false>::kBytes, b = PfPlan<true>::kBytes;
+  return 1024 + (size_t)(a > b ? a : b);
+}
 
 // ------------------------------------------------------------------ P6: fixed-order combine
 

@@ -210,3 +210,33 @@ def test_graph_replay_equals_eager_and_runs_are_deterministic():
     assert torch.equal(eager1.view(torch.int16), eager2.view(torch.int16))
     assert torch.equal(out.view(torch.int16), eager1.view(torch.int16))
     layer.close()
+
+
+def test_decode_host_buffers_equal_device_decode_and_kernel_count():
+    """moe_decode_host (pinned host x / ids / weights / out) gives the same bits
+    as moe_decode on device buffers; moe_decode_kernel_count is 1 for a fused
+    small batch and more for larger batches."""
+    case = cases.make_case(2048, 768, 128, 8, F.TYPE_NVFP4, F.TYPE_NVFP4, 2, seed=110)
+    from quantized_routed_expert_route_gb300.layer import MoeLayer
+    g = case.geom
+    layer = MoeLayer(g.H, g.I, g.E, g.top_k, g.gate_up_type, g.down_type, case.gu_dev, case.dn_dev,
+                     torch.from_numpy(case.sb).to(DEV), borrow=True)
+    x = torch.from_numpy(case.x.view(np.int16)).to(DEV).view(torch.bfloat16)
+    ids = torch.from_numpy(case.ids).to(DEV)
+    w = torch.from_numpy(case.w).to(DEV)
+    want = layer.decode(x, ids, w).clone()
+    T = case.x.shape[0]
+    hx = torch.from_numpy(case.x.view(np.int16)).pin_memory()
+    hids = torch.from_numpy(case.ids).pin_memory()
+    hw = torch.from_numpy(case.w).pin_memory()
+    hout = torch.zeros((T, g.H), dtype=torch.int16).pin_memory()
+    iob = capi.moe_decode_io_bytes(layer.bank, T)
+    io = torch.empty(iob, dtype=torch.uint8, device=DEV)
+    capi.moe_decode_host(layer.bank, hx.data_ptr(), T, hids.data_ptr(), hw.data_ptr(), hout.data_ptr(),
+                         io.data_ptr(), iob, layer.ws.data_ptr(), layer.ws_bytes, _stream())
+    torch.cuda.synchronize()
+    assert torch.equal(hout, want.view(torch.int16).cpu())
+    assert capi.moe_decode_kernel_count(layer.bank, 1) >= 1
+    assert capi.moe_decode_kernel_count(layer.bank, 0) == 0
+    assert capi.moe_decode_kernel_count(layer.bank, 64) >= capi.moe_decode_kernel_count(layer.bank, 1)
+    layer.close()
