@@ -258,6 +258,21 @@ class Stack:
 
 # ------------------------------------------------------------------ prompt path
 
+# DRAM bytes of one k_layer_small launch (NVFP4 layer, T=1) from an ncu capture
+# (dram__bytes_read.sum + dram__bytes_write.sum); valid only for the kernel
+# source it was taken on.
+TRAFFIC = {"file": "quantized_routed_expert_route_gb300/csrc/layer_small.cu",
+           "sha1": "7cd91119e57f8d09914185c61cba034eb1bf622a", "bytes": 21361152}
+
+
+def traffic_bytes():
+    import hashlib
+    p = os.path.join(ROOT, TRAFFIC["file"])
+    if not os.path.exists(p):
+        return None
+    return TRAFFIC["bytes"] if hashlib.sha1(open(p, "rb").read()).hexdigest() == TRAFFIC["sha1"] else None
+
+
 PREFILL = dict(H=2048, I=768, E=128, K=8, T=4096)
 
 
@@ -529,7 +544,7 @@ def main():
                        "l2": "inputs larger than L2 (1 GB of expert rows per step, 16 GB resident)",
                        "parallelism": f"replicas x{world}"},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                         "frac": achieved / hbm_peak, "traffic": None, "peak_kind": peak_kind,
+                         "frac": achieved / hbm_peak, "traffic": traffic_bytes(), "peak_kind": peak_kind,
                          "kernel": "k_layer_small (one fused launch per moe_decode pass at T=1)"},
             "clocks": clk.summary(),
             "e2e": {"value": e2e_val, "unit": "layer-tok/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
