@@ -287,7 +287,7 @@ __global__ void k_pf_quant(const __grid_constant__ PfParams p) {
 constexpr int kPfThreads = 512;     // 16 warps: all stage operands, one thread issues MMAs, all run the epilogue
 constexpr int kPfTileRows = 256;
 constexpr int kPfMaxStages = 3;
-constexpr uint32_t kSpinLimit = 1u << 24;   // polls of an MMA barrier (each returns within ~1 us) before giving up
+constexpr uint64_t kSpinLimit = 2000000000ull;   // an MMA-barrier wait gives up after 2 s of device time
 constexpr int kPfBRawBytes = 9216;  // raw NVFP4 of 256 weight rows x 64 values: 32 code bytes + 4 scale bytes each
 
 // Shared-memory plan of the GEMM (1024-byte aligned base):
