@@ -27,20 +27,17 @@ namespace qre {
 constexpr int kLsWarps = 16;
 constexpr int kLsConsumers = 32 * kLsWarps;
 constexpr int kLsThreads = kLsConsumers + 32;
-constexpr unsigned kGridSpinLimit = 1u << 23;   // acquire polls of the generation word (~3 s) before giving up
+constexpr unsigned kGridSpinLimit = 1u << 21;   // polling rounds of the barrier words (~2 s) before giving up
 
 __device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
   unsigned v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
-__device__ __forceinline__ unsigned atom_add_acq_rel_gpu(unsigned* p, unsigned v) {
-  unsigned old;
-  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
-  return old;
-}
-__device__ __forceinline__ void red_release_gpu_add(unsigned* p, unsigned v) {
-  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+__device__ __forceinline__ unsigned ld_relaxed_gpu(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
 }
 __device__ __forceinline__ void st_relaxed_gpu(unsigned* p, unsigned v) {
   asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
@@ -49,8 +46,9 @@ __device__ __forceinline__ void st_relaxed_gpu(unsigned* p, unsigned v) {
 // Barrier over all CTAs of the grid.  bar[0] is an epoch that only changes
 // between launches; CTA c owns the word bar[32 * (1 + c)] (its own 128-byte
 // line).  Arriving, a CTA fences (publishing its earlier writes) and stores
-// epoch + 1 into its word; one warp then polls every CTA's word with acquire
-// loads until all hold epoch + 1.  After the barrier CTA 0 advances the epoch
+// epoch + 1 into its word; one warp then reads every CTA's word in rounds of
+// independent relaxed loads until all hold epoch + 1, and fences (acquire).
+// After the barrier CTA 0 advances the epoch
 // for the next launch (every CTA read it at its start, before arriving).  The
 // wait is bounded: on timeout the error word is flagged and the CTA goes on
 // (its results are then invalid, but nothing hangs).
@@ -63,15 +61,19 @@ __device__ void ls_grid_barrier(unsigned* bar, unsigned epoch, uint32_t* err) {
       asm volatile("fence.acq_rel.gpu;" ::: "memory");
       st_relaxed_gpu(bar + 32 * (1 + blockIdx.x), target);
     }
-    for (unsigned c = lane; c < gridDim.x; c += 32) {
-      unsigned spins = 0;
-      while (ld_acquire_gpu(bar + 32 * (1 + c)) != target) {
-        if (++spins > kGridSpinLimit) {
-          atomicOr(err, kErrTimeout);
-          break;
-        }
+    // each round reads every CTA's word once (independent relaxed loads,
+    // one L2 round trip), then an acquire fence once all hold the target
+    unsigned spins = 0;
+    for (;;) {
+      bool mine = true;
+      for (unsigned c = lane; c < gridDim.x; c += 32) mine &= (ld_relaxed_gpu(bar + 32 * (1 + c)) == target);
+      if (__all_sync(0xffffffffu, mine)) break;
+      if (++spins > kGridSpinLimit) {
+        if (lane == 0) atomicOr(err, kErrTimeout);
+        break;
       }
     }
+    asm volatile("fence.acq_rel.gpu;" ::: "memory");
     __syncwarp();
     if (lane == 0 && blockIdx.x == 0) st_relaxed_gpu(bar, target);
   }
