@@ -216,7 +216,7 @@ DecodeParams make_params(const moe_bank* b, const WsLayout& L, uint8_t* ws, cons
   const int dpieces = (rows_max + rs - 1) / rs;
   int dst = dpieces * (int)((U + p.dn_slots_per_stage - 1) / p.dn_slots_per_stage);
   p.dn_nstage = dst < 2 ? 2 : (dst < p.dn_nstage ? dst : p.dn_nstage);
-  if (p.maxnt == 1) plan_layer_small(g, T, p);
+  plan_layer_small(g, T, p);
   switch (p.gu_type) {
     case W_NVFP4: p.w0 = 2; break;
     case W_Q4_K: p.w0 = 3; break;

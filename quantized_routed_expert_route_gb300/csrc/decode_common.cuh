@@ -106,10 +106,95 @@ __device__ inline int block_exclusive_scan(int* a, int n, int* wsum) {
   return total;
 }
 
+constexpr int kGroupWarpRoutes = 128;   // routes one warp groups (four per lane)
+
+// Group up to kGroupWarpRoutes routes with one warp: an expert histogram in
+// slot_of, a warp scan over the experts in ascending order gives each routed
+// expert its slot and the start of its routes, then match/rank places every
+// route after the earlier routes of the same expert.
+__device__ inline void group_routes_warp(const int32_t* ids, int RT, int E, int K, const GroupSmem& g, int lane) {
+  for (int e = lane; e < E; e += 32) g.slot_of[e] = 0;
+  __syncwarp();
+  int ev[4];
+  bool bad = false;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const int r = 32 * c + lane;
+    ev[c] = (r < RT) ? ids[r] : -1;
+  }
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const int r = 32 * c + lane;
+    const bool v = r < RT && ev[c] >= 0 && ev[c] < E;
+    bad |= (r < RT && !v);
+    if (v) atomicAdd(&g.slot_of[ev[c]], 1);
+  }
+  __syncwarp();
+  const int per = (E + 31) >> 5, e0 = lane * per;
+  int cnt = 0, pres = 0;
+  for (int i = 0; i < per; ++i) {
+    const int e = e0 + i;
+    if (e < E) {
+      const int h = g.slot_of[e];
+      cnt += h;
+      pres += (h > 0) ? 1 : 0;
+    }
+  }
+  int ci = cnt, pi = pres;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int x = __shfl_up_sync(0xffffffffu, ci, o), y = __shfl_up_sync(0xffffffffu, pi, o);
+    if (lane >= o) {
+      ci += x;
+      pi += y;
+    }
+  }
+  const int S = __shfl_sync(0xffffffffu, pi, 31), NV = __shfl_sync(0xffffffffu, ci, 31);
+  int co = ci - cnt, po = pi - pres;
+  for (int i = 0; i < per; ++i) {
+    const int e = e0 + i;
+    if (e < E) {
+      const int h = g.slot_of[e];
+      if (h > 0) {
+        g.slot_of[e] = po;
+        g.slot_e[po] = e;
+        g.slot_off[po] = co;
+        g.cursor[po] = co;
+        ++po;
+        co += h;
+      }
+    }
+  }
+  if (lane == 0) {
+    g.slot_off[S] = NV;
+    g.misc[0] = S;
+  }
+  __syncwarp();
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    if (32 * c >= RT) break;
+    const int r = 32 * c + lane;
+    const bool v = r < RT && ev[c] >= 0 && ev[c] < E;
+    const unsigned peers = __match_any_sync(0xffffffffu, v ? ev[c] : -1 - lane);
+    const int rank = __popc(peers & ((1u << lane) - 1u));
+    if (v) {
+      const int pos = g.cursor[g.slot_of[ev[c]]] + rank;
+      g.routes[pos] = (int16_t)r;
+      g.rtok[pos] = (int16_t)(r / K);
+    }
+    __syncwarp();
+    if (v && rank == 0) g.cursor[g.slot_of[ev[c]]] += __popc(peers);
+    __syncwarp();
+  }
+  bad = __any_sync(0xffffffffu, bad);
+  if (lane == 0) g.misc[1] = bad ? 1 : 0;
+}
+
 // Group the T*K routes by expert: the distinct valid experts in ascending id
 // order become slots; each slot lists its routes in route order.  Reads only
 // `ids`.  Every CTA of a kernel computes the same grouping.  Up to 32 routes
-// one warp does it with match/shuffle; beyond that the whole block scans.
+// one warp does it with match/shuffle, up to 128 one warp with a histogram;
+// beyond that the whole block scans.
 __device__ inline void group_routes(const int32_t* ids, int RT, int E, int K, const GroupSmem& g) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nthr = blockDim.x;
@@ -149,6 +234,11 @@ __device__ inline void group_routes(const int32_t* ids, int RT, int E, int K, co
         g.misc[1] = bads ? 1 : 0;
       }
     }
+    __syncthreads();
+    return;
+  }
+  if (RT <= kGroupWarpRoutes) {
+    if (warp == 0) group_routes_warp(ids, RT, E, K, g, lane);
     __syncthreads();
     return;
   }
@@ -266,6 +356,42 @@ __device__ inline void pair_at_cost(long long target, const int* slot_off, int S
       return;
     }
     c += span;
+  }
+  u = S;
+  i = 0;
+}
+
+// pair_at_cost computed by one warp (all 32 lanes call it with the same
+// arguments; the result is valid in every lane): slot costs 1 + routes, in
+// chunks of 32 slots with a warp scan instead of a serial walk.
+__device__ inline void pair_at_cost_warp(long long target, const int* slot_off, int S, int I, int w0, int lane,
+                                         int& u, int& i) {
+  long long run = 0;
+  for (int base = 0; base < S; base += 32) {
+    const int sl = base + lane;
+    const int c = (sl < S) ? w0 + (slot_off[sl + 1] - slot_off[sl]) : 0;
+    int incl = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int x = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += x;
+    }
+    const long long start = (run + (incl - c)) * I, end = (run + incl) * I;
+    const unsigned hit = __ballot_sync(0xffffffffu, sl < S && start <= target && target < end);
+    if (hit) {
+      const int l = __ffs(hit) - 1;
+      const long long st = __shfl_sync(0xffffffffu, start, l);
+      const int cs = __shfl_sync(0xffffffffu, c, l);
+      const long long rem = target - st;
+      u = base + l;
+      i = rem <= 0 ? 0 : (int)(((unsigned)rem + (unsigned)cs - 1u) / (unsigned)cs);
+      if (i >= I) {
+        u += 1;
+        i = 0;
+      }
+      return;
+    }
+    run += __shfl_sync(0xffffffffu, incl, 31);
   }
   u = S;
   i = 0;

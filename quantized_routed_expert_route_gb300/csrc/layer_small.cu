@@ -29,11 +29,6 @@ constexpr int kLsConsumers = 32 * kLsWarps;
 constexpr int kLsThreads = kLsConsumers + 32;
 constexpr unsigned kGridSpinLimit = 1u << 21;   // polling rounds of the barrier words (~2 s) before giving up
 
-__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
-  unsigned v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
 __device__ __forceinline__ unsigned ld_relaxed_gpu(const unsigned* p) {
   unsigned v;
   asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -48,8 +43,8 @@ __device__ __forceinline__ void st_relaxed_gpu(unsigned* p, unsigned v) {
 // line).  Arriving, a CTA fences (publishing its earlier writes) and stores
 // epoch + 1 into its word; one warp then reads every CTA's word in rounds of
 // independent relaxed loads until all hold epoch + 1, and fences (acquire).
-// After the barrier CTA 0 advances the epoch
-// for the next launch (every CTA read it at its start, before arriving).  The
+// After the barrier CTA 0 advances the epoch for the next launch (every CTA
+// read it before publishing its own word, so before CTA 0 could pass).  The
 // wait is bounded: on timeout the error word is flagged and the CTA goes on
 // (its results are then invalid, but nothing hangs).
 __device__ void ls_grid_barrier(unsigned* bar, unsigned epoch, uint32_t* err) {
@@ -89,7 +84,7 @@ __device__ void ls_quantize(const void* src, int nblk, const uint8_t* rvalid, in
                             int* sm, bool mirror, int8_t* wq, float* wd, int* wsum, uint16_t* wsh) {
   const int quad = threadIdx.x >> 2, ql = threadIdx.x & 3;
   constexpr int kQuads = kLsConsumers / 4;
-  constexpr int kR = 2;   // blocks per quad per round, all loads issued first
+  constexpr int kR = 4;   // blocks per quad per round, all loads issued first
   for (int b0 = 0; b0 < nblk; b0 += kR * kQuads) {
     float v[kR][8];
     bool on[kR];
@@ -172,14 +167,17 @@ __global__ void __launch_bounds__(kLsThreads, 1) k_layer_small(const __grid_cons
   }
   pdl_wait();   // x and ids may come from the previous grid
   pdl_launch_dependents();
-  const unsigned epoch = (tid == 0) ? ld_acquire_gpu(p.bar) : 0u;
+  // the barrier epoch (written by the previous launch); a relaxed load, so
+  // it does not hold up this thread's later work
+  const unsigned epoch = (tid == 0) ? ld_relaxed_gpu(p.bar) : 0u;
   group_routes(p.ids, RT, p.E, p.K, g);
   const int S = g.misc[0];
-  if (tid == 0) {
-    // even split of the S*I (gate, up) pairs (32-bit)
+  if (RT <= 32 && tid == 0) {
+    // small batch: every expert has about one route, so split the pairs
+    // evenly (32-bit arithmetic when the products fit)
     const unsigned P = (unsigned)S * (unsigned)p.I;
     unsigned lo, hi;
-    if (P <= 0xFFFFFFFFu / gridDim.x) {   // 32-bit division when the products fit
+    if (P <= 0xFFFFFFFFu / gridDim.x) {
       lo = P * blockIdx.x / gridDim.x;
       hi = P * (blockIdx.x + 1) / gridDim.x;
     } else {
@@ -193,6 +191,27 @@ __global__ void __launch_bounds__(kLsThreads, 1) k_layer_small(const __grid_cons
     g.misc[6] = 0;
     g.misc[7] = 0;
     if (blockIdx.x == 0 && g.misc[1]) atomicOr(p.err, kErrBadId);
+  } else if (RT > 32 && warp == 0) {
+    // Split of the S*I (gate, up) pairs, balanced by cost: a pair costs its
+    // row bytes plus one decode-and-dot per route of its expert, so cost =
+    // 1 + routes of the slot.
+    long long W = 0;
+    for (int sl = lane; sl < S; sl += 32) W += 1 + g.slot_off[sl + 1] - g.slot_off[sl];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) W += __shfl_xor_sync(0xffffffffu, W, o);
+    W *= p.I;
+    int ub, ib, ue, ie;
+    pair_at_cost_warp(cost_cut(W, blockIdx.x, gridDim.x), g.slot_off, S, p.I, 1, lane, ub, ib);
+    pair_at_cost_warp(cost_cut(W, blockIdx.x + 1, gridDim.x), g.slot_off, S, p.I, 1, lane, ue, ie);
+    if (lane == 0) {
+      g.misc[2] = ub;
+      g.misc[3] = ib;
+      g.misc[4] = ue;
+      g.misc[5] = ie;
+      g.misc[6] = 0;
+      g.misc[7] = 0;
+      if (blockIdx.x == 0 && g.misc[1]) atomicOr(p.err, kErrBadId);
+    }
   }
   __syncthreads();
   const int ub = g.misc[2], ib = g.misc[3], ue = g.misc[4], ie = g.misc[5];
