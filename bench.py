@@ -262,7 +262,7 @@ class Stack:
 # (dram__bytes_read.sum + dram__bytes_write.sum); valid only for the kernel
 # source it was taken on.
 TRAFFIC = {"file": "quantized_routed_expert_route_gb300/csrc/layer_small.cu",
-           "sha1": "7cd91119e57f8d09914185c61cba034eb1bf622a", "bytes": 21361152}
+           "sha1": "178bc0a816245293ca5905a693df15852c714cc8", "bytes": 21380096}
 
 
 def traffic_bytes():

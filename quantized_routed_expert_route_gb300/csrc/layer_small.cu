@@ -493,7 +493,7 @@ static cudaError_t dispatch_ls(const DecodeParams& p, cudaStream_t stream, bool 
         return cudaSuccess;
       }
       return launch_ls_t<W_NVFP4, W_NVFP4, 8>(p, stream, probe_only, fits);
-    case W_Q4_K: return launch_ls_t<W_Q4_K, W_Q4_K, 8>(p, stream, probe_only, fits);
+    case W_Q4_K: return launch_ls_t<W_Q4_K, W_Q4_K, 4>(p, stream, probe_only, fits);
     case W_Q8_0: return launch_ls_t<W_Q8_0, W_Q8_0, 8>(p, stream, probe_only, fits);
     default: return launch_ls_t<W_BF16, W_BF16, 16>(p, stream, probe_only, fits);
   }
