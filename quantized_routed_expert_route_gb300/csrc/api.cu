@@ -22,6 +22,9 @@ struct moe_bank {
   float* scales;    // [E][4]
   bool owns_rows;
   int device;
+  bool dense;               // BF16 gate_up and down with H, I multiples of 64: the dense path is available
+  CUtensorMap map_gu;       // the gate_up rows as a 2-D bf16 tensor [E*2I][H] (dense only)
+  CUtensorMap map_dn;       // the down rows as [E*H][I]
 };
 
 namespace {
@@ -36,6 +39,46 @@ int cuda_fail(cudaError_t e, const char* what) {
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// cuTensorMapEncodeTiled, looked up once through the runtime (the library
+// does not link the driver library).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled() {
+  static std::once_flag once;
+  static EncodeTiledFn fn = nullptr;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess && f)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+    else
+      cudaGetLastError();
+  });
+  return fn;
+}
+
+// A row-major bf16 matrix [rows][cols] as a 2-D tensor map: boxes of 64
+// columns (128 bytes) x box_rows rows, written to shared memory with the
+// 128-byte swizzle; reads outside the matrix fill zeros.
+bool map_bf16_rows(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  const EncodeTiledFn fn = encode_tiled();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint32_t box[2] = {64, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool dense_geometry(const moe_layer_geom& g) {
+  return g.gate_up_type == MOE_BF16 && g.down_type == MOE_BF16 && g.H % 64 == 0 && g.I % 64 == 0;
+}
 
 int geom_check(const moe_layer_geom* g) {
   if (!g) return MOE_EINVAL;
@@ -72,6 +115,8 @@ Shape decode_shape(const moe_layer_geom& g) {
 struct WsLayout {
   size_t err, bar, xq, xd, xsum, xsh, inter, iq, id, isum, ish, cnt, total;
   int cnt_len;
+  size_t d_off, d_perm, d_xs, d_ih, d_y;   // dense path (BF16 banks) only
+  int RTp;
 };
 
 WsLayout ws_layout(const moe_layer_geom& g, int T) {
@@ -93,6 +138,15 @@ WsLayout ws_layout(const moe_layer_geom& g, int T) {
   const size_t S = (size_t)g.E < RT ? (size_t)g.E : RT;
   L.cnt_len = (int)(S * (g.I / 32));
   L.cnt = o; o = align_up(o + 4 * (size_t)L.cnt_len, A);
+  L.RTp = (int)((RT + 15) / 16 * 16);
+  L.d_off = L.d_perm = L.d_xs = L.d_ih = L.d_y = 0;
+  if (dense_geometry(g)) {
+    L.d_off = o; o = align_up(o + 4 * ((size_t)g.E + 1), A);
+    L.d_perm = o; o = align_up(o + 4 * (size_t)L.RTp, A);
+    L.d_xs = o; o = align_up(o + 2 * (size_t)L.RTp * g.H, A);
+    L.d_ih = o; o = align_up(o + 2 * 2 * (size_t)L.RTp * g.I, A);
+    L.d_y = o; o = align_up(o + 4 * RT * g.H, A);
+  }
   L.total = o;
   return L;
 }
@@ -304,6 +358,10 @@ int moe_bank_create(const moe_layer_geom* geom, const void* gate_up, size_t gate
     if (b->owns_rows) { cudaFree(b->gu); cudaFree(b->dn); }
     cudaFree(b->scales); delete b; return cuda_fail(e, "bank create");
   }
+  // the dense path streams BF16 rows with 2-D TMA: one tensor map per projection
+  b->dense = dense_geometry(g) &&
+             map_bf16_rows(&b->map_gu, b->gu, (uint64_t)g.E * 2 * g.I, (uint64_t)g.H, 128) &&
+             map_bf16_rows(&b->map_dn, b->dn, (uint64_t)g.E * g.H, (uint64_t)g.I, 128);
   *out = b;
   return MOE_OK;
 }
@@ -336,6 +394,33 @@ int moe_workspace_init(void* ws, size_t ws_bytes, void* stream) {
   return e == cudaSuccess ? MOE_OK : cuda_fail(e, "workspace init");
 }
 
+// Parameters of the dense path for one pass: the bank's tensor maps, two
+// maps over this pass's workspace buffers, and the buffers themselves.
+static bool dense_params(const moe_bank* b, const WsLayout& L, uint8_t* ws, const DecodeParams& p, DtParams& d) {
+  const moe_layer_geom& g = b->geom;
+  std::memset(&d, 0, sizeof(d));
+  d.map_gu = b->map_gu;
+  d.map_dn = b->map_dn;
+  d.H = g.H; d.I = g.I; d.E = g.E; d.K = g.top_k; d.T = p.T;
+  d.RT = p.T * g.top_k;
+  d.RTp = L.RTp;
+  d.scales = b->scales;
+  d.x = p.x; d.ids = p.ids; d.w = p.w; d.out = p.out;
+  d.err = p.err;
+  d.off = reinterpret_cast<int*>(ws + L.d_off);
+  d.perm = reinterpret_cast<int*>(ws + L.d_perm);
+  d.xs = reinterpret_cast<uint16_t*>(ws + L.d_xs);
+  d.ih = reinterpret_cast<uint16_t*>(ws + L.d_ih);
+  d.inter = p.inter;
+  d.y = reinterpret_cast<float*>(ws + L.d_y);
+  if (!map_bf16_rows(&d.map_xs, d.xs, (uint64_t)L.RTp, (uint64_t)g.H, 16) ||
+      !map_bf16_rows(&d.map_ih, d.ih, 2 * (uint64_t)L.RTp, (uint64_t)g.I, 16)) {
+    std::snprintf(g_cuda_err, sizeof(g_cuda_err), "dense path: tensor map encode failed");
+    return false;
+  }
+  return true;
+}
+
 static int decode_impl(const moe_bank* b, const void* x, int32_t T, const int32_t* ids, const float* w, void* out,
                        void* ws, size_t ws_bytes, void* stream, int* chunk_T) {
   if (!b || T < 0) return MOE_EINVAL;
@@ -362,6 +447,12 @@ static int decode_impl(const moe_bank* b, const void* x, int32_t T, const int32_
       if ((e = launch_layer_small(p, s)) != cudaSuccess) return cuda_fail(e, "layer launch");
       continue;
     }
+    if (b->dense) {
+      DtParams d;
+      if (!dense_params(b, L, static_cast<uint8_t*>(ws), p, d)) return MOE_ECUDA;
+      if ((e = launch_dense(d, s)) != cudaSuccess) return cuda_fail(e, "dense launch");
+      continue;
+    }
     if (p.maxnt != 1 && (e = launch_prep(p, s)) != cudaSuccess) return cuda_fail(e, "prep launch");
     if ((e = launch_gate_up(p, s)) != cudaSuccess) return cuda_fail(e, "gate_up launch");
     if ((e = launch_down(p, s)) != cudaSuccess) return cuda_fail(e, "down launch");
@@ -384,7 +475,7 @@ int moe_decode_kernel_count(const moe_bank* b, int32_t T) {
     const int tn = (T - t0) < tc ? (T - t0) : tc;
     const WsLayout L = ws_layout(g, tn);
     const DecodeParams p = make_params(b, L, nullptr, sh, tn);
-    n += p.use_ls ? 1 : (p.maxnt != 1 ? 3 : 2);
+    n += p.use_ls ? 1 : (b->dense ? kDtLaunches : (p.maxnt != 1 ? 3 : 2));
   }
   return n;
 }

@@ -106,6 +106,58 @@ __device__ inline int block_exclusive_scan(int* a, int n, int* wsum) {
   return total;
 }
 
+// Stable sort of routes 0..RT-1 by expert id, by the whole block: per-warp
+// expert counts over contiguous route ranges, an exclusive scan over experts,
+// then each warp places its routes (match/rank inside each group of 32), so
+// the rows of an expert keep route order.  Routes whose id is outside [0, E)
+// are left out.  Scratch in shared memory: cnt [warps][E], base [E], wsum
+// [33].  Results: off[e] = first sorted row of expert e, off[E] = valid
+// routes, perm[row] = route index (shared or global memory), complete for the
+// whole block on return.  Returns, in every lane of a warp, whether that warp
+// saw an invalid id.
+__device__ inline bool sort_routes_block(const int32_t* ids, int RT, int E, int* cnt, int* base, int* wsum, int* off,
+                                         int* perm) {
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const int nthr = blockDim.x, NW = nthr >> 5;
+  for (int i = tid; i < NW * E; i += nthr) cnt[i] = 0;
+  __syncthreads();
+  const int per = (RT + NW - 1) / NW;
+  const int r0 = min(RT, w * per), r1 = min(RT, r0 + per);
+  bool bad = false;
+  for (int r = r0 + lane; r < r1; r += 32) {
+    const int e = ids[r];
+    if (e >= 0 && e < E) atomicAdd(&cnt[w * E + e], 1);
+    else bad = true;
+  }
+  __syncthreads();
+  for (int e = tid; e < E; e += nthr) {
+    int acc = 0;
+    for (int ww = 0; ww < NW; ++ww) {
+      const int c = cnt[ww * E + e];
+      cnt[ww * E + e] = acc;
+      acc += c;
+    }
+    base[e] = acc;
+  }
+  __syncthreads();
+  const int total = block_exclusive_scan(base, E, wsum);
+  for (int e = tid; e < E; e += nthr) off[e] = base[e];
+  if (tid == 0) off[E] = total;
+  for (int rb = r0; rb < r1; rb += 32) {
+    const int r = rb + lane;
+    const int e = (r < r1) ? ids[r] : -1;
+    const bool v = r < r1 && e >= 0 && e < E;
+    const unsigned peers = __match_any_sync(0xffffffffu, v ? e : -1 - lane);
+    const int rank = __popc(peers & ((1u << lane) - 1u));
+    if (v) perm[base[e] + cnt[w * E + e] + rank] = r;
+    __syncwarp();
+    if (v && rank == 0) cnt[w * E + e] += __popc(peers);
+    __syncwarp();
+  }
+  __syncthreads();
+  return __any_sync(0xffffffffu, bad);
+}
+
 constexpr int kGroupWarpRoutes = 128;   // routes one warp groups (four per lane)
 
 // Group up to kGroupWarpRoutes routes with one warp: an expert histogram in

@@ -1,5 +1,6 @@
 // Internal declarations shared by the C-ABI layer and the kernels.
 #pragma once
+#include <cuda.h>   // CUtensorMap (the type only; the library links the runtime alone)
 #include <cuda_runtime.h>
 
 #include <cstddef>
@@ -78,6 +79,32 @@ struct PfParams {
   float* y;                 // fp32 [RT][H]: down output of each route times s_down * w, by route index
 };
 
+// The dense path (decode_tc.cu): BF16 gate_up and down banks at batches the
+// fused kernel cannot hold.  Routes sorted by expert, the routed tokens'
+// hidden states gathered in that order, then two grouped GEMMs on the tensor
+// cores (weights streamed by 2-D TMA into swizzled tiles) and a fixed-order
+// route sum.  H and I are multiples of 64.
+struct DtParams {
+  CUtensorMap map_gu;       // gate_up bank as bf16 [E*2I][H], box 64 x 128 rows, 128-byte swizzle
+  CUtensorMap map_dn;       // down bank as bf16 [E*H][I], box 64 x 128 rows
+  CUtensorMap map_xs;       // xs: bf16 [RTp][H], box 64 x 16 rows
+  CUtensorMap map_ih;       // ih: bf16 [2*RTp][I] (hi rows, then lo rows), box 64 x 16 rows
+  int H, I, E, K, T, RT, RTp;
+  const float* scales;      // [E][4]
+  const uint16_t* x;        // bf16 [T][H]
+  const int32_t* ids;       // [T][K]
+  const float* w;           // [T][K]
+  uint16_t* out;            // bf16 [T][H]
+  // workspace
+  uint32_t* err;
+  int* off;                 // [E+1] first sorted row of each expert; off[E] = valid routes
+  int* perm;                // [RTp] route index of each sorted row
+  uint16_t* xs;             // bf16 [RTp][H]: x of the token of each sorted row
+  uint16_t* ih;             // bf16 [2*RTp][I]: intermediate of each sorted row as hi + lo (a = hi + lo to ~2^-16)
+  float* inter;             // fp32 [RT][I]: the intermediate by route index (as the other paths leave it)
+  float* y;                 // fp32 [RT][H]: down output of each route times s_down * w, by route index
+};
+
 // Sizes of the dynamic shared memory of each kernel for these params.
 size_t gate_up_smem_bytes(const DecodeParams& p);
 size_t down_smem_bytes(const DecodeParams& p);
@@ -91,6 +118,10 @@ cudaError_t launch_down(const DecodeParams& p, cudaStream_t stream);
 size_t layer_small_smem_bytes(const DecodeParams& p);
 bool layer_small_fits(const DecodeParams& p);
 cudaError_t launch_layer_small(const DecodeParams& p, cudaStream_t stream);
+
+// Dense path for BF16 banks (four launches: route + gather, gate_up, down, route sum).
+constexpr int kDtLaunches = 4;
+cudaError_t launch_dense(const DtParams& p, cudaStream_t stream);
 
 // Test hooks.
 cudaError_t launch_quantize_q8_1_blocks(const float* x, int64_t n, uint8_t* out, cudaStream_t stream);

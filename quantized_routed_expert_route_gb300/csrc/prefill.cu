@@ -120,56 +120,17 @@ cudaError_t launch_tc_gemm_check(const uint16_t* A, const uint16_t* B, int K, in
 
 constexpr int kSortThreads = 1024;
 
-// One CTA: per-warp expert counts over contiguous route ranges, an exclusive
-// scan over experts, then each warp places its routes (match/rank inside each
-// group of 32), so rows of an expert keep route order.  Routes whose id is
-// outside [0, E) are left out and flag the error word.
+// One CTA sorts the routes by expert (stable: route order inside an expert);
+// routes whose id is outside [0, E) are left out and flag the error word.
 __global__ void __launch_bounds__(kSortThreads) k_pf_sort(const __grid_constant__ PfParams p) {
   extern __shared__ int ssm[];
   constexpr int NW = kSortThreads / 32;
-  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-  const int E = p.E, RT = p.RT;
-  int* cnt = ssm;             // [NW][E]
-  int* base = cnt + NW * E;   // [E]
-  int* wsum = base + E;       // [33]
-  if (tid == 0) *p.err = 0u;  // each prompt-path call starts with a clear error word
-  for (int i = tid; i < NW * E; i += kSortThreads) cnt[i] = 0;
-  __syncthreads();
-  const int per = (RT + NW - 1) / NW;
-  const int r0 = min(RT, w * per), r1 = min(RT, r0 + per);
-  bool bad = false;
-  for (int r = r0 + lane; r < r1; r += 32) {
-    const int e = p.ids[r];
-    if (e >= 0 && e < E) atomicAdd(&cnt[w * E + e], 1);
-    else bad = true;
-  }
-  __syncthreads();
-  for (int e = tid; e < E; e += kSortThreads) {
-    int acc = 0;
-    for (int ww = 0; ww < NW; ++ww) {
-      const int c = cnt[ww * E + e];
-      cnt[ww * E + e] = acc;
-      acc += c;
-    }
-    base[e] = acc;
-  }
-  __syncthreads();
-  const int total = block_exclusive_scan(base, E, wsum);
-  for (int e = tid; e < E; e += kSortThreads) p.off[e] = base[e];
-  if (tid == 0) p.off[E] = total;
-  for (int rb = r0; rb < r1; rb += 32) {
-    const int r = rb + lane;
-    const int e = (r < r1) ? p.ids[r] : -1;
-    const bool v = r < r1 && e >= 0 && e < E;
-    const unsigned peers = __match_any_sync(0xffffffffu, v ? e : -1 - lane);
-    const int rank = __popc(peers & ((1u << lane) - 1u));
-    if (v) p.perm[base[e] + cnt[w * E + e] + rank] = r;
-    __syncwarp();
-    if (v && rank == 0) cnt[w * E + e] += __popc(peers);
-    __syncwarp();
-  }
-  const bool any_bad = __any_sync(0xffffffffu, bad);
-  if (any_bad && lane == 0) atomicOr(p.err, kErrBadId);
+  int* cnt = ssm;               // [NW][E]
+  int* base = cnt + NW * p.E;   // [E]
+  int* wsum = base + p.E;       // [33]
+  if (threadIdx.x == 0) *p.err = 0u;  // each prompt-path call starts with a clear error word
+  const bool bad = sort_routes_block(p.ids, p.RT, p.E, cnt, base, wsum, p.off, p.perm);
+  if (bad && (threadIdx.x & 31) == 0) atomicOr(p.err, kErrBadId);
 }
 
 size_t pf_sort_smem(int E) { return sizeof(int) * ((size_t)(kSortThreads / 32) * E + E + 33); }

@@ -101,6 +101,7 @@ def run_gpu(case: Case, stages=True):
         torch.cuda.synchronize()
     res["out"] = out.cpu().numpy().view(np.uint16)
     res["err"] = layer.error_bits()
+    res["launches"] = capi.moe_decode_kernel_count(layer.bank, T)
     layer.close()
     return res
 

@@ -103,6 +103,7 @@ def _check_case(case, tokens=None, check_stages=True):
                     assert (np.abs(gq - oq) <= 1).all()
                     assert not (diff & ~amb[i, k]).any(), f"unambiguous q8_1 code differs (route {t},{k})"
     figs["err_bits"] = res["err"]
+    figs["launches"] = res["launches"]
     return figs
 
 
