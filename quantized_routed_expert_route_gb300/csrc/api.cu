@@ -22,9 +22,12 @@ struct moe_bank {
   float* scales;    // [E][4]
   bool owns_rows;
   int device;
-  bool dense;               // BF16 gate_up and down with H, I multiples of 64: the dense path is available
-  CUtensorMap map_gu;       // the gate_up rows as a 2-D bf16 tensor [E*2I][H] (dense only)
-  CUtensorMap map_dn;       // the down rows as [E*H][I]
+  // Grouped path for batches the fused kernel cannot hold: kGroupedDense
+  // (BF16 gate_up and down, H and I multiples of 64) or kGroupedQ4K (Q4_K
+  // gate_up and down), with the bank's rows as 2-D tensors for TMA.
+  int grouped;
+  CUtensorMap map_gu;       // dense: bf16 [E*2I][H], box 64 x 128; Q4_K: bytes [E*2I][rb_gu], box 144 x 128
+  CUtensorMap map_dn;       // dense: bf16 [E*H][I]; Q4_K: bytes [E*H][rb_dn]
 };
 
 namespace {
@@ -76,8 +79,28 @@ bool map_bf16_rows(CUtensorMap* m, const void* base, uint64_t rows, uint64_t col
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-bool dense_geometry(const moe_layer_geom& g) {
-  return g.gate_up_type == MOE_BF16 && g.down_type == MOE_BF16 && g.H % 64 == 0 && g.I % 64 == 0;
+// A row-major byte matrix [rows][cols] as a 2-D tensor map: boxes of
+// box_cols bytes (a multiple of 16) x box_rows rows, copied to shared memory
+// densely (rows box_cols bytes apart); reads outside the matrix fill zeros.
+bool map_byte_rows(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_cols,
+                   uint32_t box_rows) {
+  const EncodeTiledFn fn = encode_tiled();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols};
+  const cuuint32_t box[2] = {box_cols, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+enum { kGroupedNone = 0, kGroupedDense = 1, kGroupedQ4K = 2 };
+
+int grouped_kind(const moe_layer_geom& g) {
+  if (g.gate_up_type == MOE_BF16 && g.down_type == MOE_BF16 && g.H % 64 == 0 && g.I % 64 == 0) return kGroupedDense;
+  if (g.gate_up_type == MOE_Q4_K && g.down_type == MOE_Q4_K && g.H % 256 == 0 && g.I % 256 == 0) return kGroupedQ4K;
+  return kGroupedNone;
 }
 
 int geom_check(const moe_layer_geom* g) {
@@ -115,7 +138,9 @@ Shape decode_shape(const moe_layer_geom& g) {
 struct WsLayout {
   size_t err, bar, xq, xd, xsum, xsh, inter, iq, id, isum, ish, cnt, total;
   int cnt_len;
-  size_t d_off, d_perm, d_xs, d_ih, d_y;   // dense path (BF16 banks) only
+  size_t d_off, d_perm, d_y;               // grouped paths: routes sorted by expert, per-route down output
+  size_t d_xs, d_ih;                       // dense path: gathered x, intermediate hi + lo
+  size_t q_aq, q_as, q_iq, q_is;           // Q4_K path: sorted q8_1 planes of x and of the intermediate
   int RTp;
 };
 
@@ -138,14 +163,22 @@ WsLayout ws_layout(const moe_layer_geom& g, int T) {
   const size_t S = (size_t)g.E < RT ? (size_t)g.E : RT;
   L.cnt_len = (int)(S * (g.I / 32));
   L.cnt = o; o = align_up(o + 4 * (size_t)L.cnt_len, A);
-  L.RTp = (int)((RT + 15) / 16 * 16);
-  L.d_off = L.d_perm = L.d_xs = L.d_ih = L.d_y = 0;
-  if (dense_geometry(g)) {
+  L.RTp = (int)((RT + 31) / 32 * 32);
+  L.d_off = L.d_perm = L.d_y = L.d_xs = L.d_ih = L.q_aq = L.q_as = L.q_iq = L.q_is = 0;
+  const int gk = grouped_kind(g);
+  if (gk != kGroupedNone) {
     L.d_off = o; o = align_up(o + 4 * ((size_t)g.E + 1), A);
     L.d_perm = o; o = align_up(o + 4 * (size_t)L.RTp, A);
+    L.d_y = o; o = align_up(o + 4 * RT * g.H, A);
+  }
+  if (gk == kGroupedDense) {
     L.d_xs = o; o = align_up(o + 2 * (size_t)L.RTp * g.H, A);
     L.d_ih = o; o = align_up(o + 2 * 2 * (size_t)L.RTp * g.I, A);
-    L.d_y = o; o = align_up(o + 4 * RT * g.H, A);
+  } else if (gk == kGroupedQ4K) {
+    L.q_aq = o; o = align_up(o + (size_t)L.RTp * g.H, A);
+    L.q_as = o; o = align_up(o + (size_t)L.RTp * (g.H / 4), A);
+    L.q_iq = o; o = align_up(o + (size_t)L.RTp * g.I, A);
+    L.q_is = o; o = align_up(o + (size_t)L.RTp * (g.I / 4), A);
   }
   L.total = o;
   return L;
@@ -358,10 +391,17 @@ int moe_bank_create(const moe_layer_geom* geom, const void* gate_up, size_t gate
     if (b->owns_rows) { cudaFree(b->gu); cudaFree(b->dn); }
     cudaFree(b->scales); delete b; return cuda_fail(e, "bank create");
   }
-  // the dense path streams BF16 rows with 2-D TMA: one tensor map per projection
-  b->dense = dense_geometry(g) &&
-             map_bf16_rows(&b->map_gu, b->gu, (uint64_t)g.E * 2 * g.I, (uint64_t)g.H, 128) &&
-             map_bf16_rows(&b->map_dn, b->dn, (uint64_t)g.E * g.H, (uint64_t)g.I, 128);
+  // the grouped paths stream the rows with 2-D TMA: one tensor map per projection
+  b->grouped = kGroupedNone;
+  const int gk = grouped_kind(g);
+  if (gk == kGroupedDense &&
+      map_bf16_rows(&b->map_gu, b->gu, (uint64_t)g.E * 2 * g.I, (uint64_t)g.H, 128) &&
+      map_bf16_rows(&b->map_dn, b->dn, (uint64_t)g.E * g.H, (uint64_t)g.I, 128))
+    b->grouped = kGroupedDense;
+  if (gk == kGroupedQ4K &&
+      map_byte_rows(&b->map_gu, b->gu, (uint64_t)g.E * 2 * g.I, (uint64_t)rb_gu, 144, 128) &&
+      map_byte_rows(&b->map_dn, b->dn, (uint64_t)g.E * g.H, (uint64_t)rb_dn, 144, 128))
+    b->grouped = kGroupedQ4K;
   *out = b;
   return MOE_OK;
 }
@@ -421,6 +461,38 @@ static bool dense_params(const moe_bank* b, const WsLayout& L, uint8_t* ws, cons
   return true;
 }
 
+// Parameters of the batched Q4_K path for one pass.
+static bool qbatch_params(const moe_bank* b, const WsLayout& L, uint8_t* ws, const DecodeParams& p, QbParams& q) {
+  const moe_layer_geom& g = b->geom;
+  std::memset(&q, 0, sizeof(q));
+  q.map_wgu = b->map_gu;
+  q.map_wdn = b->map_dn;
+  q.H = g.H; q.I = g.I; q.E = g.E; q.K = g.top_k; q.T = p.T;
+  q.RT = p.T * g.top_k;
+  q.RTp = L.RTp;
+  q.scales = b->scales;
+  q.x = p.x; q.ids = p.ids; q.w = p.w; q.out = p.out;
+  q.err = p.err;
+  q.off = reinterpret_cast<int*>(ws + L.d_off);
+  q.perm = reinterpret_cast<int*>(ws + L.d_perm);
+  q.aq = reinterpret_cast<int8_t*>(ws + L.q_aq);
+  q.as = ws + L.q_as;
+  q.iqs = reinterpret_cast<int8_t*>(ws + L.q_iq);
+  q.iss = ws + L.q_is;
+  q.xq = p.xq; q.xd = p.xd; q.xsum = p.xsum; q.xsh = p.xsh;
+  q.inter = p.inter;
+  q.iq = p.iq; q.id = p.id; q.isum = p.isum; q.ish = p.ish;
+  q.y = reinterpret_cast<float*>(ws + L.d_y);
+  if (!map_byte_rows(&q.map_aq, q.aq, (uint64_t)L.RTp, (uint64_t)g.H, 256, 32) ||
+      !map_byte_rows(&q.map_as, q.as, (uint64_t)L.RTp, (uint64_t)g.H / 4, 64, 32) ||
+      !map_byte_rows(&q.map_iq, q.iqs, (uint64_t)L.RTp, (uint64_t)g.I, 256, 32) ||
+      !map_byte_rows(&q.map_is, q.iss, (uint64_t)L.RTp, (uint64_t)g.I / 4, 64, 32)) {
+    std::snprintf(g_cuda_err, sizeof(g_cuda_err), "batched path: tensor map encode failed");
+    return false;
+  }
+  return true;
+}
+
 static int decode_impl(const moe_bank* b, const void* x, int32_t T, const int32_t* ids, const float* w, void* out,
                        void* ws, size_t ws_bytes, void* stream, int* chunk_T) {
   if (!b || T < 0) return MOE_EINVAL;
@@ -447,10 +519,16 @@ static int decode_impl(const moe_bank* b, const void* x, int32_t T, const int32_
       if ((e = launch_layer_small(p, s)) != cudaSuccess) return cuda_fail(e, "layer launch");
       continue;
     }
-    if (b->dense) {
+    if (b->grouped == kGroupedDense) {
       DtParams d;
       if (!dense_params(b, L, static_cast<uint8_t*>(ws), p, d)) return MOE_ECUDA;
       if ((e = launch_dense(d, s)) != cudaSuccess) return cuda_fail(e, "dense launch");
+      continue;
+    }
+    if (b->grouped == kGroupedQ4K) {
+      QbParams q;
+      if (!qbatch_params(b, L, static_cast<uint8_t*>(ws), p, q)) return MOE_ECUDA;
+      if ((e = launch_qbatch(q, s)) != cudaSuccess) return cuda_fail(e, "batched launch");
       continue;
     }
     if (p.maxnt != 1 && (e = launch_prep(p, s)) != cudaSuccess) return cuda_fail(e, "prep launch");
@@ -475,7 +553,10 @@ int moe_decode_kernel_count(const moe_bank* b, int32_t T) {
     const int tn = (T - t0) < tc ? (T - t0) : tc;
     const WsLayout L = ws_layout(g, tn);
     const DecodeParams p = make_params(b, L, nullptr, sh, tn);
-    n += p.use_ls ? 1 : (b->dense ? kDtLaunches : (p.maxnt != 1 ? 3 : 2));
+    n += p.use_ls                            ? 1
+         : b->grouped == kGroupedDense       ? kDtLaunches
+         : b->grouped == kGroupedQ4K         ? kQbLaunches
+         : (p.maxnt != 1 ? 3 : 2);
   }
   return n;
 }

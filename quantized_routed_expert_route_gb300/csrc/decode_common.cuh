@@ -158,6 +158,32 @@ __device__ inline bool sort_routes_block(const int32_t* ids, int RT, int E, int*
   return __any_sync(0xffffffffu, bad);
 }
 
+// Route sum of the grouped paths, four outputs per thread: for element
+// idx of [T][H/4], out[t][n..n+3] = bf16(sum over k = 0..K-1, in route order,
+// of y[t*K+k][n..n+3]) over the routes whose expert id is valid; one
+// rounding to bf16, no atomics.
+__device__ __forceinline__ void route_sum4(const int32_t* ids, const float* y, uint16_t* out, int T, int K, int E,
+                                           int H, long long idx) {
+  const int nq = H / 4;
+  if (idx >= (long long)T * nq) return;
+  const int t = (int)(idx / nq), n = 4 * (int)(idx - (long long)t * nq);
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int k = 0; k < K; ++k) {
+    const int r = t * K + k;
+    const int e = __ldg(ids + r);
+    if (e < 0 || e >= E) continue;
+    const float4 v = __ldcg(reinterpret_cast<const float4*>(y + (size_t)r * H + n));
+    acc.x += v.x;
+    acc.y += v.y;
+    acc.z += v.z;
+    acc.w += v.w;
+  }
+  uint2 o;
+  o.x = f32_to_bf16_bits_rn(acc.x) | (f32_to_bf16_bits_rn(acc.y) << 16);
+  o.y = f32_to_bf16_bits_rn(acc.z) | (f32_to_bf16_bits_rn(acc.w) << 16);
+  *reinterpret_cast<uint2*>(out + (size_t)t * H + n) = o;
+}
+
 constexpr int kGroupWarpRoutes = 128;   // routes one warp groups (four per lane)
 
 // Group up to kGroupWarpRoutes routes with one warp: an expert histogram in

@@ -130,25 +130,7 @@ size_t dt_route_smem(int E, int RT) {
 __global__ void k_dt_combine(const __grid_constant__ DtParams p) {
   pdl_wait();   // the down GEMM's y is complete
   pdl_launch_dependents();
-  const int nq = p.H / 4;
-  const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  if (idx >= (long long)p.T * nq) return;
-  const int t = (int)(idx / nq), n = 4 * (int)(idx - (long long)t * nq);
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int k = 0; k < p.K; ++k) {
-    const int r = t * p.K + k;
-    const int e = __ldg(p.ids + r);
-    if (e < 0 || e >= p.E) continue;
-    const float4 v = __ldcg(reinterpret_cast<const float4*>(p.y + (size_t)r * p.H + n));
-    acc.x += v.x;
-    acc.y += v.y;
-    acc.z += v.z;
-    acc.w += v.w;
-  }
-  uint2 o;
-  o.x = f32_to_bf16_bits_rn(acc.x) | (f32_to_bf16_bits_rn(acc.y) << 16);
-  o.y = f32_to_bf16_bits_rn(acc.z) | (f32_to_bf16_bits_rn(acc.w) << 16);
-  *reinterpret_cast<uint2*>(p.out + (size_t)t * p.H + n) = o;
+  route_sum4(p.ids, p.y, p.out, p.T, p.K, p.E, p.H, (long long)blockIdx.x * blockDim.x + threadIdx.x);
 }
 
 // ------------------------------------------------------------------ grouped GEMMs

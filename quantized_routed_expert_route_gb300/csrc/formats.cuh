@@ -119,6 +119,28 @@ __device__ __forceinline__ void q8_1_quantize_quad(const float (&v)[8], uint32_t
   sum = s;
 }
 
+// The same q8_1 rule with a block spread over a full warp, one value per
+// lane (lane i holds value i of the block): amax and the code sum are
+// combined with shuffles; returns this lane's code.
+__device__ __forceinline__ int q8_1_quantize_lane(float v, float& d, int& sum) {
+  float amax = fabsf(v);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  d = __fdiv_rn(amax, 127.0f);
+  const bool fast = d >= 1.1754944e-38f;
+  const float r = fast ? __frcp_rn(d) : 0.0f;
+  const float t = v * r;
+  const float near = fabsf(t - floorf(t) - 0.5f);
+  int q;
+  if (fast && near > 0.000244140625f) q = __float2int_rn(t);
+  else q = (d == 0.0f) ? 0 : __float2int_rn(__fdiv_rn(v, d));
+  int s = q;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  sum = s;
+  return q;
+}
+
 // Internal q8_1 storage is planar: codes [rows][n] int8, d [rows][n/32] fp32
 // (an fp16 value), exact code sum [rows][n/32] int32, s [rows][n/32] fp16 bits.
 __device__ __forceinline__ ActQ8 load_act_q8(const int8_t* q, const float* d, const int* sum, size_t row_vals,

@@ -105,6 +105,41 @@ struct DtParams {
   float* y;                 // fp32 [RT][H]: down output of each route times s_down * w, by route index
 };
 
+// The batched path for Q4_K banks (decode_qb.cu) at batches the fused kernel
+// cannot hold: routes sorted by expert and each sorted route's x quantized
+// to q8_1 in that order, then two grouped CUDA-core kernels that stream one
+// 144-byte super-block column of 256 weight rows per 2-D TMA stage and dot
+// each decoded block with up to 32 routed tokens, and the fixed-order route
+// sum.  A q8_1 block record is 8 bytes: the fp16-rounded scale as fp32, then
+// the int32 code sum.  H and I are multiples of 256.
+struct QbParams {
+  CUtensorMap map_wgu;      // gate_up bank as bytes [E*2I][rb_gu], box 144 x 128 rows
+  CUtensorMap map_wdn;      // down bank as bytes [E*H][rb_dn], box 144 x 128 rows
+  CUtensorMap map_aq;       // aq [RTp][H], box 256 x 32 rows
+  CUtensorMap map_as;       // as [RTp][H/4], box 64 x 32 rows
+  CUtensorMap map_iq;       // iqs [RTp][I], box 256 x 32 rows
+  CUtensorMap map_is;       // iss [RTp][I/4], box 64 x 32 rows
+  int H, I, E, K, T, RT, RTp;
+  const float* scales;      // [E][4]
+  const uint16_t* x;        // bf16 [T][H]
+  const int32_t* ids;       // [T][K]
+  const float* w;           // [T][K]
+  uint16_t* out;            // bf16 [T][H]
+  // workspace
+  uint32_t* err;
+  int* off;                 // [E+1] first sorted row of each expert; off[E] = valid routes
+  int* perm;                // [RTp] route index of each sorted row
+  int8_t* aq;               // q8_1 codes of x for each sorted row [RTp][H]
+  uint8_t* as;              // block records [RTp][H/32][8]
+  int8_t* iqs;              // q8_1 codes of the intermediate for each sorted row [RTp][I]
+  uint8_t* iss;             // block records [RTp][I/32][8]
+  // the per-token / per-route planes the other paths leave (for inspection)
+  int8_t* xq; float* xd; int* xsum; uint16_t* xsh;
+  float* inter;
+  int8_t* iq; float* id; int* isum; uint16_t* ish;
+  float* y;                 // fp32 [RT][H]: down output of each route times s_down * w, by route index
+};
+
 // Sizes of the dynamic shared memory of each kernel for these params.
 size_t gate_up_smem_bytes(const DecodeParams& p);
 size_t down_smem_bytes(const DecodeParams& p);
@@ -122,6 +157,10 @@ cudaError_t launch_layer_small(const DecodeParams& p, cudaStream_t stream);
 // Dense path for BF16 banks (four launches: route + gather, gate_up, down, route sum).
 constexpr int kDtLaunches = 4;
 cudaError_t launch_dense(const DtParams& p, cudaStream_t stream);
+
+// Batched path for Q4_K banks (five launches: route + quantize, gate_up, requantize, down, route sum).
+constexpr int kQbLaunches = 5;
+cudaError_t launch_qbatch(const QbParams& p, cudaStream_t stream);
 
 // Test hooks.
 cudaError_t launch_quantize_q8_1_blocks(const float* x, int64_t n, uint8_t* out, cudaStream_t stream);
