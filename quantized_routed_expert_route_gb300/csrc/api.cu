@@ -140,7 +140,7 @@ struct WsLayout {
   int cnt_len;
   size_t d_off, d_perm, d_y;               // grouped paths: routes sorted by expert, per-route down output
   size_t d_xs, d_ih;                       // dense path: gathered x, intermediate hi + lo
-  size_t q_aq, q_as, q_iq, q_is;           // Q4_K path: sorted q8_1 planes of x and of the intermediate
+  size_t q_sched, q_eord, q_xr, q_iq, q_is; // Q4_K path: tile counters, expert order, x block records, sorted intermediate
   int RTp;
 };
 
@@ -164,7 +164,7 @@ WsLayout ws_layout(const moe_layer_geom& g, int T) {
   L.cnt_len = (int)(S * (g.I / 32));
   L.cnt = o; o = align_up(o + 4 * (size_t)L.cnt_len, A);
   L.RTp = (int)((RT + 31) / 32 * 32);
-  L.d_off = L.d_perm = L.d_y = L.d_xs = L.d_ih = L.q_aq = L.q_as = L.q_iq = L.q_is = 0;
+  L.d_off = L.d_perm = L.d_y = L.d_xs = L.d_ih = L.q_sched = L.q_eord = L.q_xr = L.q_iq = L.q_is = 0;
   const int gk = grouped_kind(g);
   if (gk != kGroupedNone) {
     L.d_off = o; o = align_up(o + 4 * ((size_t)g.E + 1), A);
@@ -175,8 +175,9 @@ WsLayout ws_layout(const moe_layer_geom& g, int T) {
     L.d_xs = o; o = align_up(o + 2 * (size_t)L.RTp * g.H, A);
     L.d_ih = o; o = align_up(o + 2 * 2 * (size_t)L.RTp * g.I, A);
   } else if (gk == kGroupedQ4K) {
-    L.q_aq = o; o = align_up(o + (size_t)L.RTp * g.H, A);
-    L.q_as = o; o = align_up(o + (size_t)L.RTp * (g.H / 4), A);
+    L.q_sched = o; o = align_up(o + 4 * 4, A);
+    L.q_eord = o; o = align_up(o + 4 * (size_t)g.E, A);
+    L.q_xr = o; o = align_up(o + (size_t)T * (g.H / 4), A);
     L.q_iq = o; o = align_up(o + (size_t)L.RTp * g.I, A);
     L.q_is = o; o = align_up(o + (size_t)L.RTp * (g.I / 4), A);
   }
@@ -475,16 +476,17 @@ static bool qbatch_params(const moe_bank* b, const WsLayout& L, uint8_t* ws, con
   q.err = p.err;
   q.off = reinterpret_cast<int*>(ws + L.d_off);
   q.perm = reinterpret_cast<int*>(ws + L.d_perm);
-  q.aq = reinterpret_cast<int8_t*>(ws + L.q_aq);
-  q.as = ws + L.q_as;
+  q.sched = reinterpret_cast<unsigned*>(ws + L.q_sched);
+  q.eorder = reinterpret_cast<int*>(ws + L.q_eord);
+  q.xrec = ws + L.q_xr;
   q.iqs = reinterpret_cast<int8_t*>(ws + L.q_iq);
   q.iss = ws + L.q_is;
   q.xq = p.xq; q.xd = p.xd; q.xsum = p.xsum; q.xsh = p.xsh;
   q.inter = p.inter;
   q.iq = p.iq; q.id = p.id; q.isum = p.isum; q.ish = p.ish;
   q.y = reinterpret_cast<float*>(ws + L.d_y);
-  if (!map_byte_rows(&q.map_aq, q.aq, (uint64_t)L.RTp, (uint64_t)g.H, 256, 32) ||
-      !map_byte_rows(&q.map_as, q.as, (uint64_t)L.RTp, (uint64_t)g.H / 4, 64, 32) ||
+  if (!map_byte_rows(&q.map_xq, q.xq, (uint64_t)p.T, (uint64_t)g.H, 256, 1) ||
+      !map_byte_rows(&q.map_xr, q.xrec, (uint64_t)p.T, (uint64_t)g.H / 4, 64, 1) ||
       !map_byte_rows(&q.map_iq, q.iqs, (uint64_t)L.RTp, (uint64_t)g.I, 256, 32) ||
       !map_byte_rows(&q.map_is, q.iss, (uint64_t)L.RTp, (uint64_t)g.I / 4, 64, 32)) {
     std::snprintf(g_cuda_err, sizeof(g_cuda_err), "batched path: tensor map encode failed");

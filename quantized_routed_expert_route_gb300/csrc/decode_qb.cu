@@ -13,20 +13,24 @@
 // expert.  Five launches chained with programmatic dependent launch:
 //
 //   k_qb_route   every CTA sorts the routes by expert (stable) in shared
-//                memory; CTA 0 publishes the offsets and the permutation; all
-//                CTAs quantize the x row of each sorted route to q8_1 into
-//                sorted planes (codes, 8-byte block records).
+//                memory; CTA 0 publishes the offsets, the permutation and the
+//                routed experts ordered by route count (most first), and
+//                resets the tile counters; every token's x is quantized to
+//                q8_1 once (codes and 8-byte block records).
 //   k_qb_gemm<0> gate_up.  A tile is (expert, 128 intermediate columns, <= 32
-//                routed tokens).  Per 256-value K chunk one stage holds the
-//                chunk's 144-byte super-block of the 128 gate rows and of the
-//                128 up rows (2-D TMA, rows 144 bytes apart: conflict-free
-//                16-byte loads) and the tokens' q8_1 codes and records.  A
-//                thread owns a (gate, up) pair and half of each chunk's eight
-//                blocks; it decodes each block once and accumulates its dot
-//                products with every token (activation loads are
-//                shared-memory broadcasts).  The two halves of a pair meet in
-//                one shuffle; the epilogue applies s_gate / s_up and SiLU-GLU
-//                in fp32 and stores the intermediate by route.
+//                routed tokens); tiles are taken from a global counter,
+//                heaviest experts first.  Per 256-value K chunk one stage
+//                holds the chunk's 144-byte super-block of the 128 gate rows
+//                and of the 128 up rows (2-D TMA, rows 144 bytes apart:
+//                conflict-free 16-byte loads) and each token's q8_1 codes and
+//                records (one TMA row per token).  A thread owns a (gate, up)
+//                pair and half of each chunk's eight blocks: it decodes the
+//                chunk's scales once, each 32-byte nibble run once for its two
+//                blocks, and accumulates the block dots with every token
+//                (activation loads are shared-memory broadcasts).  The two
+//                halves of a pair meet in one shuffle; the epilogue applies
+//                s_gate / s_up and SiLU-GLU in fp32 and stores the
+//                intermediate by route.
 //   k_qb_requant prep_inter: the q8_1 of each sorted route's intermediate.
 //   k_qb_gemm<1> down.  A tile is (expert, 256 output rows, <= 32 tokens), a
 //                thread owns rows j and j+128; the epilogue scales by s_down *
@@ -49,9 +53,14 @@ constexpr int kQbThreads = kQbConsumers + 32;            // + one TMA producer w
 constexpr int kQbTok = 32;                               // routed tokens per tile
 constexpr int kQbStages = 4;
 constexpr int kQbSb = 144;                               // bytes of one Q4_K super-block (256 values) of a row
-constexpr int kQbCodesOff = 256 * kQbSb;                 // 36,864: the 256 rows' super-blocks come first
-constexpr int kQbRecOff = kQbCodesOff + kQbTok * 256;    // tokens' codes, 256 per token
-constexpr int kQbStageBytes = kQbRecOff + kQbTok * 64;   // tokens' block records, 8 blocks x 8 bytes
+// A stage: the 256 rows' super-blocks, then the tokens' codes (256 bytes a
+// token), then their block records (8 blocks x 8 bytes a token).  Every
+// tensor-copy destination is 128-byte aligned: gate_up copies each token's
+// records on its own, so its record slots are 128 bytes apart; down copies
+// the 32 tokens' records in one box, 64 bytes apart.
+constexpr int kQbCodesOff = 256 * kQbSb;                 // 36,864
+constexpr int kQbRecOff = kQbCodesOff + kQbTok * 256;    // 45,056
+constexpr int kQbStageBytes = kQbRecOff + kQbTok * 128;  // 49,152
 constexpr uint64_t kQbWaitNs = 2000000000ull;            // one wait gives up after 2 s of device time
 constexpr int kQbRouteThreads = 512;
 
@@ -118,6 +127,7 @@ __global__ void __launch_bounds__(kQbRouteThreads) k_qb_route(const __grid_const
   int* wsum = base + E;                              // [33]
   int* off = wsum + 33;                              // [E+1]
   int* perm = off + E + 1;                           // [RT]
+  int* cm = perm + RT;                               // [RT+1]: experts per route count, then positions
   pdl_wait();   // x and ids may come from the previous grid
   const bool bad = sort_routes_block(p.ids, RT, E, cnt, base, wsum, off, perm);
   pdl_launch_dependents();
@@ -127,24 +137,28 @@ __global__ void __launch_bounds__(kQbRouteThreads) k_qb_route(const __grid_const
     for (int e = tid; e <= E; e += kQbRouteThreads) p.off[e] = off[e];
     for (int s = tid; s < NV; s += kQbRouteThreads) p.perm[s] = perm[s];
     if (bad && (tid & 31) == 0) atomicOr(p.err, kErrBadId);
-  }
-  const int nbh = p.H / 32;
-  // sorted rows: the q8_1 of x[token of route perm[s]], one block per thread
-  for (int s = blockIdx.x; s < NV; s += gridDim.x) {
-    const uint16_t* xrow = p.x + (size_t)(perm[s] / p.K) * p.H;
-    for (int b = tid; b < nbh; b += kQbRouteThreads) {
-      uint32_t qw[8];
-      float dh;
-      int sum;
-      uint16_t sh;
-      quantize_x_block(xrow, b, qw, dh, sum, sh);
-      uint4* qd = reinterpret_cast<uint4*>(p.aq + (size_t)s * p.H + 32 * b);
-      qd[0] = make_uint4(qw[0], qw[1], qw[2], qw[3]);
-      qd[1] = make_uint4(qw[4], qw[5], qw[6], qw[7]);
-      *reinterpret_cast<uint2*>(p.as + ((size_t)s * nbh + b) * 8) = make_uint2(__float_as_uint(dh), (uint32_t)sum);
+    // the routed experts by route count, most first: cm[i] counts the experts
+    // with RT - i routes, its exclusive scan gives each count's first position
+    for (int i = tid; i <= RT; i += kQbRouteThreads) cm[i] = 0;
+    __syncthreads();
+    for (int e = tid; e < E; e += kQbRouteThreads) {
+      const int M = off[e + 1] - off[e];
+      if (M > 0) atomicAdd(&cm[RT - M], 1);
+    }
+    __syncthreads();
+    const int U = block_exclusive_scan(cm, RT + 1, wsum);
+    for (int e = tid; e < E; e += kQbRouteThreads) {
+      const int M = off[e + 1] - off[e];
+      if (M > 0) p.eorder[atomicAdd(&cm[RT - M], 1)] = e;
+    }
+    if (tid == 0) {
+      p.sched[0] = 0u;
+      p.sched[1] = 0u;
+      p.sched[2] = (unsigned)U;
     }
   }
-  // the per-token planes the other decode paths leave in the workspace
+  // every token's q8_1, once: codes, records, and the planes left for inspection
+  const int nbh = p.H / 32;
   for (int t = blockIdx.x; t < p.T; t += gridDim.x) {
     const uint16_t* xrow = p.x + (size_t)t * p.H;
     for (int b = tid; b < nbh; b += kQbRouteThreads) {
@@ -156,6 +170,7 @@ __global__ void __launch_bounds__(kQbRouteThreads) k_qb_route(const __grid_const
       uint4* qd = reinterpret_cast<uint4*>(p.xq + (size_t)t * p.H + 32 * b);
       qd[0] = make_uint4(qw[0], qw[1], qw[2], qw[3]);
       qd[1] = make_uint4(qw[4], qw[5], qw[6], qw[7]);
+      *reinterpret_cast<uint2*>(p.xrec + ((size_t)t * nbh + b) * 8) = make_uint2(__float_as_uint(dh), (uint32_t)sum);
       p.xd[t * nbh + b] = dh;
       p.xsum[t * nbh + b] = sum;
       p.xsh[t * nbh + b] = sh;
@@ -164,7 +179,7 @@ __global__ void __launch_bounds__(kQbRouteThreads) k_qb_route(const __grid_const
 }
 
 size_t qb_route_smem(int E, int RT) {
-  return sizeof(int) * ((size_t)(kQbRouteThreads / 32) * E + E + 33 + (E + 1) + RT);
+  return sizeof(int) * ((size_t)(kQbRouteThreads / 32) * E + E + 33 + (E + 1) + RT + (RT + 1));
 }
 
 __global__ void k_qb_combine(const __grid_constant__ QbParams p) {
@@ -214,51 +229,77 @@ __global__ void k_qb_requant(const __grid_constant__ QbParams p) {
 
 // ------------------------------------------------------------------ grouped kernels
 
-// Tile t of the persistent schedule: expert e (experts in order, tile_pre[e]
-// = first tile of e), row block rb fastest, then token block.
-struct QbTile {
-  int e, rb, srow0, nv;   // expert, row block, first sorted row, tokens
+// What the producer tells the consumers about a stage: the tile's expert,
+// row block, first sorted row, tokens (nv < 0: no more tiles) and the chunk.
+struct __align__(16) QbMeta {
+  int e, rb, srow0, nv_kc;   // nv_kc = nv | kc << 8
 };
 
-__device__ __forceinline__ QbTile qb_tile(const int* tile_pre, const int* offs, int E, int NB, int t) {
-  int lo = 0, hi = E;
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if (tile_pre[mid] <= t) lo = mid;
-    else hi = mid;
+// d * sc and dmin * m of blocks 4h .. 4h+3 of a Q4_K super-block, from its
+// 16-byte header (d | dmin << 16, then the 12 packed 6-bit scale bytes).
+__device__ __forceinline__ void q4k_scales4(const uint4 hdr, int h, float (&dsc)[4], float (&dmm)[4]) {
+  const float d = f16_bits_to_f32(hdr.x & 0xFFFFu);
+  const float dmin = f16_bits_to_f32(hdr.x >> 16);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint32_t sc, m;
+    if (h == 0) {
+      sc = (hdr.y >> (8 * i)) & 63u;
+      m = (hdr.z >> (8 * i)) & 63u;
+    } else {
+      const uint32_t s8 = (hdr.w >> (8 * i)) & 0xFFu;
+      sc = (s8 & 15u) | (((hdr.y >> (8 * i + 6)) & 3u) << 4);
+      m = (s8 >> 4) | (((hdr.z >> (8 * i + 6)) & 3u) << 4);
+    }
+    dsc[i] = d * (float)sc;
+    dmm[i] = dmin * (float)m;
   }
-  QbTile d;
-  d.e = lo;
-  const int tl = t - tile_pre[lo];
-  d.rb = tl % NB;
-  d.srow0 = offs[lo] + (tl / NB) * kQbTok;
-  d.nv = min(kQbTok, offs[lo + 1] - d.srow0);
-  return d;
 }
 
 // Blocks 4h .. 4h+3 of one K chunk (a 256-value super-block) of the thread's
-// two weight rows against the tile's tokens: each block decoded once, its
-// integer dot with every token's q8_1 block scaled as d_a * (d*sc*dot -
-// dmin*m*sum_a).
+// two weight rows against the tile's tokens.  Each 32-byte nibble run holds
+// blocks 2c (low nibbles) and 2c+1 (high nibbles); each block's integer dot
+// with a token's q8_1 block is scaled as d_a * (d*sc*dot - dmin*m*sum_a).
+template <int REC_PITCH>
 __device__ __forceinline__ void qb_chunk(const uint8_t* rowa, const uint8_t* rowb, const uint8_t* codes,
                                          const uint8_t* recs, int h, int nv, float (&acca)[kQbTok],
                                          float (&accb)[kQbTok]) {
-#pragma unroll 1
-  for (int j = 4 * h; j < 4 * h + 4; ++j) {
-    int na[8], nb[8];
-    float dsa, dma, dsb, dmb;
-    q4k_decode(rowa, j, na, dsa, dma);
-    q4k_decode(rowb, j, nb, dsb, dmb);
+  float dsa[4], dma[4], dsb[4], dmb[4];
+  q4k_scales4(lds128(rowa), h, dsa, dma);
+  q4k_scales4(lds128(rowb), h, dsb, dmb);
+#pragma unroll
+  for (int c = 0; c < 2; ++c) {
+    const int cc = 2 * h + c;
+    int al[8], ah[8], bl[8], bh[8];
+    {
+      const uint4 a0 = lds128(rowa + 16 + 32 * cc), a1 = lds128(rowa + 32 + 32 * cc);
+      const uint4 b0 = lds128(rowb + 16 + 32 * cc), b1 = lds128(rowb + 32 + 32 * cc);
+      const uint32_t wa[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+      const uint32_t wb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        al[i] = (int)(wa[i] & 0x0F0F0F0Fu);
+        ah[i] = (int)((wa[i] >> 4) & 0x0F0F0F0Fu);
+        bl[i] = (int)(wb[i] & 0x0F0F0F0Fu);
+        bh[i] = (int)((wb[i] >> 4) & 0x0F0F0F0Fu);
+      }
+    }
+    const float sa0 = dsa[2 * c], ma0 = dma[2 * c], sa1 = dsa[2 * c + 1], ma1 = dma[2 * c + 1];
+    const float sb0 = dsb[2 * c], mb0 = dmb[2 * c], sb1 = dsb[2 * c + 1], mb1 = dmb[2 * c + 1];
 #pragma unroll
     for (int t = 0; t < kQbTok; ++t) {
       if (t >= nv) break;
-      const uint8_t* c = codes + t * 256 + 32 * j;
-      const uint4 c0 = lds128(c), c1 = lds128(c + 16);
-      const uint2 rc = *reinterpret_cast<const uint2*>(recs + t * 64 + 8 * j);
-      const int q[8] = {(int)c0.x, (int)c0.y, (int)c0.z, (int)c0.w, (int)c1.x, (int)c1.y, (int)c1.z, (int)c1.w};
-      const float ad = __uint_as_float(rc.x), asum = (float)(int)rc.y;
-      acca[t] += ad * (dsa * (float)int_dot8(na, q) - dma * asum);
-      accb[t] += ad * (dsb * (float)int_dot8(nb, q) - dmb * asum);
+      const uint8_t* cp = codes + t * 256 + 64 * cc;
+      const uint4 q0 = lds128(cp), q1 = lds128(cp + 16), q2 = lds128(cp + 32), q3 = lds128(cp + 48);
+      const uint4 rc = lds128(recs + t * REC_PITCH + 16 * cc);   // (d, sum) of blocks 2cc and 2cc+1
+      const int ql[8] = {(int)q0.x, (int)q0.y, (int)q0.z, (int)q0.w, (int)q1.x, (int)q1.y, (int)q1.z, (int)q1.w};
+      const int qh[8] = {(int)q2.x, (int)q2.y, (int)q2.z, (int)q2.w, (int)q3.x, (int)q3.y, (int)q3.z, (int)q3.w};
+      const float d0 = __uint_as_float(rc.x), s0 = (float)(int)rc.y;
+      const float d1 = __uint_as_float(rc.z), s1 = (float)(int)rc.w;
+      acca[t] += d0 * (sa0 * (float)int_dot8(al, ql) - ma0 * s0);
+      accb[t] += d0 * (sb0 * (float)int_dot8(bl, ql) - mb0 * s0);
+      acca[t] += d1 * (sa1 * (float)int_dot8(ah, qh) - ma1 * s1);
+      accb[t] += d1 * (sb1 * (float)int_dot8(bh, qh) - mb1 * s1);
     }
   }
 }
@@ -272,8 +313,10 @@ template <int PHASE>
 __global__ void __launch_bounds__(kQbThreads, 1) k_qb_gemm(const __grid_constant__ QbParams p) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t full_bar[kQbStages], empty_bar[kQbStages];
+  __shared__ QbMeta smeta[kQbStages];
   __shared__ int tile_pre[kMaxE + 1];
   __shared__ int offs[kMaxE + 1];
+  __shared__ int eord[kMaxE];
   __shared__ int wsum[33];
   __shared__ volatile int abort_flag;
   uint8_t* base = smem_raw + ((128u - (smem_addr(smem_raw) & 127u)) & 127u);
@@ -290,51 +333,83 @@ __global__ void __launch_bounds__(kQbThreads, 1) k_qb_gemm(const __grid_constant
     }
     fence_mbar_init();
     prefetch_map(PHASE == 0 ? &p.map_wgu : &p.map_wdn);
-    prefetch_map(PHASE == 0 ? &p.map_aq : &p.map_iq);
-    prefetch_map(PHASE == 0 ? &p.map_as : &p.map_is);
+    prefetch_map(PHASE == 0 ? &p.map_xq : &p.map_iq);
+    prefetch_map(PHASE == 0 ? &p.map_xr : &p.map_is);
   }
   pdl_wait();   // PHASE 0: routes sorted and x quantized; PHASE 1: the intermediate requantized
+  const int U = (int)__ldcg(p.sched + 2);
   for (int e = tid; e <= E; e += kQbThreads) offs[e] = __ldcg(p.off + e);
+  for (int i = tid; i < U; i += kQbThreads) eord[i] = __ldcg(p.eorder + i);
   __syncthreads();
-  for (int e = tid; e < E; e += kQbThreads) {
-    const int M = offs[e + 1] - offs[e];
-    tile_pre[e] = ((M + kQbTok - 1) / kQbTok) * NB;
+  for (int i = tid; i < U; i += kQbThreads) {
+    const int e = eord[i];
+    tile_pre[i] = ((offs[e + 1] - offs[e] + kQbTok - 1) / kQbTok) * NB;
   }
   __syncthreads();
-  const int total = block_exclusive_scan(tile_pre, E, wsum);   // ends with a block barrier
+  const int total = block_exclusive_scan(tile_pre, U, wsum);   // ends with a block barrier
   pdl_launch_dependents();
   volatile int* abort = &abort_flag;
 
   if (warp == kQbConsumers / 32) {
-    // ---------------- TMA producer
+    // ---------------- TMA producer: tiles from the global counter, most routes first
     if (lane == 0) {
       const uint64_t pol = l2_policy_evict_first();   // weight rows: read once
       uint32_t g = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-        const QbTile ti = qb_tile(tile_pre, offs, E, NB, t);
+      int tok[kQbTok];
+      for (;;) {
+        const int t = (int)atomicAdd(p.sched + PHASE, 1u);
+        const uint32_t s0 = g % kQbStages, u0 = g / kQbStages;
+        if (t >= total) {
+          // no tile left: a stage with nv < 0 tells the consumers to stop
+          if (u0 >= 1 && !qb_wait(&empty_bar[s0], (u0 - 1) & 1u, abort)) {
+            ok = false;
+            break;
+          }
+          smeta[s0] = QbMeta{0, 0, 0, -1};
+          mbar_arrive(&full_bar[s0]);
+          break;
+        }
+        int lo = 0, hi = U;
+        while (hi - lo > 1) {
+          const int mid = (lo + hi) >> 1;
+          if (tile_pre[mid] <= t) lo = mid;
+          else hi = mid;
+        }
+        const int e = eord[lo];
+        const int tl = t - tile_pre[lo];
+        const int rb = tl % NB;
+        const int srow0 = offs[e] + (tl / NB) * kQbTok;
+        const int nv = min(kQbTok, offs[e + 1] - srow0);
+        if (PHASE == 0)
+          for (int i = 0; i < nv; ++i) tok[i] = __ldcg(p.perm + srow0 + i) / p.K;
         for (int kc = 0; kc < nK; ++kc, ++g) {
           const uint32_t s = g % kQbStages, u = g / kQbStages;
           if (u >= 1 && !qb_wait(&empty_bar[s], (u - 1) & 1u, abort)) {
             ok = false;
             break;
           }
+          smeta[s] = QbMeta{e, rb, srow0, nv | (kc << 8)};
           uint8_t* st = base + s * kQbStageBytes;
-          mbar_arrive_expect_tx(&full_bar[s], (uint32_t)kQbStageBytes);
           if (PHASE == 0) {
-            const int y0 = ti.e * 2 * p.I + ti.rb * 128;
+            mbar_arrive_expect_tx(&full_bar[s], (uint32_t)(kQbCodesOff + nv * 320));
+            const int y0 = e * 2 * p.I + rb * 128;
             tma_load_2d_hint(st, &p.map_wgu, kc * kQbSb, y0, &full_bar[s], pol);
             tma_load_2d_hint(st + 128 * kQbSb, &p.map_wgu, kc * kQbSb, y0 + p.I, &full_bar[s], pol);
-            tma_load_2d(st + kQbCodesOff, &p.map_aq, kc * 256, ti.srow0, &full_bar[s]);
-            tma_load_2d(st + kQbRecOff, &p.map_as, kc * 64, ti.srow0, &full_bar[s]);
+            for (int i = 0; i < nv; ++i) {
+              tma_load_2d(st + kQbCodesOff + 256 * i, &p.map_xq, kc * 256, tok[i], &full_bar[s]);
+              tma_load_2d(st + kQbRecOff + 128 * i, &p.map_xr, kc * 64, tok[i], &full_bar[s]);
+            }
           } else {
-            const int y0 = ti.e * p.H + ti.rb * 256;
+            mbar_arrive_expect_tx(&full_bar[s], (uint32_t)(kQbRecOff + kQbTok * 64));
+            const int y0 = e * p.H + rb * 256;
             tma_load_2d_hint(st, &p.map_wdn, kc * kQbSb, y0, &full_bar[s], pol);
             tma_load_2d_hint(st + 128 * kQbSb, &p.map_wdn, kc * kQbSb, y0 + 128, &full_bar[s], pol);
-            tma_load_2d(st + kQbCodesOff, &p.map_iq, kc * 256, ti.srow0, &full_bar[s]);
-            tma_load_2d(st + kQbRecOff, &p.map_is, kc * 64, ti.srow0, &full_bar[s]);
+            tma_load_2d(st + kQbCodesOff, &p.map_iq, kc * 256, srow0, &full_bar[s]);
+            tma_load_2d(st + kQbRecOff, &p.map_is, kc * 64, srow0, &full_bar[s]);
           }
         }
+        if (!ok) break;
       }
       if (!ok) {
         atomicOr(p.err, kErrTimeout);
@@ -346,52 +421,55 @@ __global__ void __launch_bounds__(kQbThreads, 1) k_qb_gemm(const __grid_constant
     return;
   }
 
-  // ---------------- consumers
+  // ---------------- consumers: follow the producer's stages
   const int u = 16 * warp + (lane & 15), h = lane >> 4;
-  uint32_t g = 0;
+  float acca[kQbTok], accb[kQbTok];
   bool ok = true;
-  for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-    const QbTile ti = qb_tile(tile_pre, offs, E, NB, t);
-    float acca[kQbTok], accb[kQbTok];
-#pragma unroll
-    for (int i = 0; i < kQbTok; ++i) acca[i] = accb[i] = 0.f;
-    for (int kc = 0; kc < nK; ++kc, ++g) {
-      const uint32_t s = g % kQbStages, ph = (g / kQbStages) & 1u;
-      if (!qb_wait(&full_bar[s], ph, abort)) {
-        ok = false;
-        break;
-      }
-      const uint8_t* st = base + s * kQbStageBytes;
-      qb_chunk(st + u * kQbSb, st + (128 + u) * kQbSb, st + kQbCodesOff, st + kQbRecOff, h, ti.nv, acca, accb);
-      mbar_arrive(&empty_bar[s]);
+  for (uint32_t g = 0;; ++g) {
+    const uint32_t s = g % kQbStages, ph = (g / kQbStages) & 1u;
+    if (!qb_wait(&full_bar[s], ph, abort)) {
+      ok = false;
+      break;
     }
-    if (!ok) break;
+    const QbMeta m = smeta[s];
+    if (m.nv_kc < 0) break;
+    const int nv = m.nv_kc & 0xFF, kc = m.nv_kc >> 8;
+    if (kc == 0) {
+#pragma unroll
+      for (int i = 0; i < kQbTok; ++i) acca[i] = accb[i] = 0.f;
+    }
+    const uint8_t* st = base + s * kQbStageBytes;
+    qb_chunk<PHASE == 0 ? 128 : 64>(st + u * kQbSb, st + (128 + u) * kQbSb, st + kQbCodesOff, st + kQbRecOff, h,
+                                    nv, acca, accb);
+    mbar_arrive(&empty_bar[s]);
+    if (kc != nK - 1) continue;
+    // ---- the tile is complete
 #pragma unroll
     for (int i = 0; i < kQbTok; ++i) {
-      if (i >= ti.nv) break;
+      if (i >= nv) break;
       acca[i] += __shfl_xor_sync(0xffffffffu, acca[i], 16);
       accb[i] += __shfl_xor_sync(0xffffffffu, accb[i], 16);
     }
-    const int e = ti.e;
+    const int e = m.e;
     if (PHASE == 0) {
       // a = silu(h_gate * s_gate) * (h_up * s_up), by route; half h stores tokens of parity h
-      const int i = ti.rb * 128 + u;
+      const int i = m.rb * 128 + u;
       const float sg = __ldg(p.scales + 4 * e + 0), su = __ldg(p.scales + 4 * e + 1);
 #pragma unroll
       for (int k = 0; k < kQbTok; ++k) {
-        if (k >= ti.nv) break;
+        if (k >= nv) break;
         if ((k & 1) != h) continue;
-        const int r = __ldcg(p.perm + ti.srow0 + k);
+        const int r = __ldcg(p.perm + m.srow0 + k);
         p.inter[(size_t)r * p.I + i] = silu_glu(acca[k] * sg, accb[k] * su);
       }
     } else {
-      const int j = ti.rb * 256 + u;
+      const int j = m.rb * 256 + u;
       const float sd = __ldg(p.scales + 4 * e + 2);
 #pragma unroll
       for (int k = 0; k < kQbTok; ++k) {
-        if (k >= ti.nv) break;
+        if (k >= nv) break;
         if ((k & 1) != h) continue;
-        const int r = __ldcg(p.perm + ti.srow0 + k);
+        const int r = __ldcg(p.perm + m.srow0 + k);
         const float f = sd * __ldg(p.w + r);
         p.y[(size_t)r * p.H + j] = acca[k] * f;
         p.y[(size_t)r * p.H + j + 128] = accb[k] * f;

@@ -106,17 +106,17 @@ struct DtParams {
 };
 
 // The batched path for Q4_K banks (decode_qb.cu) at batches the fused kernel
-// cannot hold: routes sorted by expert and each sorted route's x quantized
-// to q8_1 in that order, then two grouped CUDA-core kernels that stream one
-// 144-byte super-block column of 256 weight rows per 2-D TMA stage and dot
-// each decoded block with up to 32 routed tokens, and the fixed-order route
-// sum.  A q8_1 block record is 8 bytes: the fp16-rounded scale as fp32, then
-// the int32 code sum.  H and I are multiples of 256.
+// cannot hold: routes sorted by expert, each token's x quantized to q8_1 once,
+// then two grouped CUDA-core kernels that stream one 144-byte super-block
+// column of 256 weight rows per 2-D TMA stage and dot each decoded block with
+// up to 32 routed tokens (tiles handed out heaviest expert first), and the
+// fixed-order route sum.  A q8_1 block record is 8 bytes: the fp16-rounded
+// scale as fp32, then the int32 code sum.  H and I are multiples of 256.
 struct QbParams {
   CUtensorMap map_wgu;      // gate_up bank as bytes [E*2I][rb_gu], box 144 x 128 rows
   CUtensorMap map_wdn;      // down bank as bytes [E*H][rb_dn], box 144 x 128 rows
-  CUtensorMap map_aq;       // aq [RTp][H], box 256 x 32 rows
-  CUtensorMap map_as;       // as [RTp][H/4], box 64 x 32 rows
+  CUtensorMap map_xq;       // xq [T][H], box 256 x 1 row
+  CUtensorMap map_xr;       // xrec [T][H/4], box 64 x 1 row
   CUtensorMap map_iq;       // iqs [RTp][I], box 256 x 32 rows
   CUtensorMap map_is;       // iss [RTp][I/4], box 64 x 32 rows
   int H, I, E, K, T, RT, RTp;
@@ -129,11 +129,12 @@ struct QbParams {
   uint32_t* err;
   int* off;                 // [E+1] first sorted row of each expert; off[E] = valid routes
   int* perm;                // [RTp] route index of each sorted row
-  int8_t* aq;               // q8_1 codes of x for each sorted row [RTp][H]
-  uint8_t* as;              // block records [RTp][H/32][8]
+  unsigned* sched;          // [0], [1]: next tile of gate_up / down; [2]: routed experts U
+  int* eorder;              // [E]: the routed experts, most routes first
+  uint8_t* xrec;            // q8_1 block records of x [T][H/32][8]
   int8_t* iqs;              // q8_1 codes of the intermediate for each sorted row [RTp][I]
   uint8_t* iss;             // block records [RTp][I/32][8]
-  // the per-token / per-route planes the other paths leave (for inspection)
+  // per-token / per-route planes, also left for inspection
   int8_t* xq; float* xd; int* xsum; uint16_t* xsh;
   float* inter;
   int8_t* iq; float* id; int* isum; uint16_t* ish;
