@@ -305,6 +305,11 @@ DecodeParams make_params(const moe_bank* b, const WsLayout& L, uint8_t* ws, cons
   int dst = dpieces * (int)((U + p.dn_slots_per_stage - 1) / p.dn_slots_per_stage);
   p.dn_nstage = dst < 2 ? 2 : (dst < p.dn_nstage ? dst : p.dn_nstage);
   plan_layer_small(g, T, p);
+  // The grouped paths take over from the fused kernel once they are faster
+  // (measured on the Laguna-shaped layers: BF16 from 2 tokens, Q4_K from
+  // 64 routes per pass).
+  const int RTn = T * g.top_k;
+  if ((b->grouped == kGroupedDense && T >= 2) || (b->grouped == kGroupedQ4K && RTn >= 64)) p.use_ls = 0;
   switch (p.gu_type) {
     case W_NVFP4: p.w0 = 2; break;
     case W_Q4_K: p.w0 = 3; break;
@@ -487,8 +492,8 @@ static bool qbatch_params(const moe_bank* b, const WsLayout& L, uint8_t* ws, con
   q.y = reinterpret_cast<float*>(ws + L.d_y);
   if (!map_byte_rows(&q.map_xq, q.xq, (uint64_t)p.T, (uint64_t)g.H, 256, 1) ||
       !map_byte_rows(&q.map_xr, q.xrec, (uint64_t)p.T, (uint64_t)g.H / 4, 64, 1) ||
-      !map_byte_rows(&q.map_iq, q.iqs, (uint64_t)L.RTp, (uint64_t)g.I, 256, 32) ||
-      !map_byte_rows(&q.map_is, q.iss, (uint64_t)L.RTp, (uint64_t)g.I / 4, 64, 32)) {
+      !map_byte_rows(&q.map_iq, q.iqs, (uint64_t)L.RTp, (uint64_t)g.I, 256, kQbTileTokens) ||
+      !map_byte_rows(&q.map_is, q.iss, (uint64_t)L.RTp, (uint64_t)g.I / 4, 64, kQbTileTokens)) {
     std::snprintf(g_cuda_err, sizeof(g_cuda_err), "batched path: tensor map encode failed");
     return false;
   }

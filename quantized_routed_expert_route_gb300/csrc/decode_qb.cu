@@ -10,15 +10,15 @@
 // "perf(moe): avoid max-stride padding for heterogeneous GGUF expert banks",
 // Reproduction geometry).  What changes is the order: each block of a
 // weight row is decoded once and dotted with every routed token of its
-// expert.  Five launches chained with programmatic dependent launch:
+// expert.  Four launches chained with programmatic dependent launch:
 //
-//   k_qb_route   every CTA sorts the routes by expert (stable) in shared
-//                memory; CTA 0 publishes the offsets, the permutation and the
-//                routed experts ordered by route count (most first), and
-//                resets the tile counters; every token's x is quantized to
-//                q8_1 once (codes and 8-byte block records).
-//   k_qb_gemm<0> gate_up.  A tile is (expert, 128 intermediate columns, <= 32
-//                routed tokens); tiles are taken from a global counter,
+//   k_qb_route   CTA 0 sorts the routes by expert (stable), publishes the
+//                offsets, the permutation and the routed experts ordered by
+//                route count (most first), and resets the tile counters; the
+//                other CTAs quantize every token's x to q8_1 once (codes and
+//                8-byte block records).
+//   k_qb_gemm<0> gate_up + prep_inter.  A tile is (expert, 128 intermediate
+//                columns, <= 16 routed tokens); tiles come from a global counter,
 //                heaviest experts first.  Per 256-value K chunk one stage
 //                holds the chunk's 144-byte super-block of the 128 gate rows
 //                and of the 128 up rows (2-D TMA, rows 144 bytes apart:
@@ -28,19 +28,18 @@
 //                chunk's scales once, each 32-byte nibble run once for its two
 //                blocks, and accumulates the block dots with every token
 //                (activation loads are shared-memory broadcasts).  The two
-//                halves of a pair meet in one shuffle; the epilogue applies
-//                s_gate / s_up and SiLU-GLU in fp32 and stores the
-//                intermediate by route.
-//   k_qb_requant prep_inter: the q8_1 of each sorted route's intermediate.
-//   k_qb_gemm<1> down.  A tile is (expert, 256 output rows, <= 32 tokens), a
+//                halves of a pair meet in shared memory; the epilogue applies
+//                s_gate / s_up and SiLU-GLU in fp32 and requantizes each
+//                warp's 32 intermediate values to q8_1 (sorted rows for the
+//                down kernel, and by route).
+//   k_qb_gemm<1> down.  A tile is (expert, 256 output rows, <= 16 tokens), a
 //                thread owns rows j and j+128; the epilogue scales by s_down *
 //                routing weight and stores fp32 per route.
 //   k_qb_combine out[t] = bf16(sum over k = 0..K-1 of the route rows), in
 //                route order, no atomics.
 //
-// Every selected expert's rows are read from HBM once per pass (twice only
-// for an expert with more than 32 routed tokens, the second time mostly from
-// L2).  Every wait is bounded in device time; on a timeout the CTA raises the
+// Every selected expert's rows are read from HBM once per pass (again, mostly
+// from L2, for each further 16 routed tokens of an expert).  Every wait is bounded in device time; on a timeout the CTA raises the
 // error word, stops issuing and lets its copies in flight land before exiting.
 #include "decode_common.cuh"
 
@@ -50,17 +49,17 @@ namespace {
 
 constexpr int kQbConsumers = 256;                        // two weight rows x half the blocks per thread
 constexpr int kQbThreads = kQbConsumers + 32;            // + one TMA producer warp (warp 8)
-constexpr int kQbTok = 32;                               // routed tokens per tile
+constexpr int kQbTok = kQbTileTokens;                     // routed tokens per tile
 constexpr int kQbStages = 4;
 constexpr int kQbSb = 144;                               // bytes of one Q4_K super-block (256 values) of a row
 // A stage: the 256 rows' super-blocks, then the tokens' codes (256 bytes a
 // token), then their block records (8 blocks x 8 bytes a token).  Every
 // tensor-copy destination is 128-byte aligned: gate_up copies each token's
 // records on its own, so its record slots are 128 bytes apart; down copies
-// the 32 tokens' records in one box, 64 bytes apart.
+// the tile's tokens' records in one box, 64 bytes apart.
 constexpr int kQbCodesOff = 256 * kQbSb;                 // 36,864
-constexpr int kQbRecOff = kQbCodesOff + kQbTok * 256;    // 45,056
-constexpr int kQbStageBytes = kQbRecOff + kQbTok * 128;  // 49,152
+constexpr int kQbRecOff = kQbCodesOff + kQbTok * 256;    // 40,960
+constexpr int kQbStageBytes = kQbRecOff + kQbTok * 128;  // 43,008
 constexpr uint64_t kQbWaitNs = 2000000000ull;            // one wait gives up after 2 s of device time
 constexpr int kQbRouteThreads = 512;
 
@@ -121,24 +120,25 @@ __device__ __forceinline__ void quantize_x_block(const uint16_t* xrow, int b, ui
 
 __global__ void __launch_bounds__(kQbRouteThreads) k_qb_route(const __grid_constant__ QbParams p) {
   extern __shared__ int rsm[];
-  const int E = p.E, RT = p.RT;
-  int* cnt = rsm;                                    // [16][E]
-  int* base = cnt + (kQbRouteThreads / 32) * E;      // [E]
-  int* wsum = base + E;                              // [33]
-  int* off = wsum + 33;                              // [E+1]
-  int* perm = off + E + 1;                           // [RT]
-  int* cm = perm + RT;                               // [RT+1]: experts per route count, then positions
   pdl_wait();   // x and ids may come from the previous grid
-  const bool bad = sort_routes_block(p.ids, RT, E, cnt, base, wsum, off, perm);
   pdl_launch_dependents();
   const int tid = threadIdx.x;
-  const int NV = off[E];
   if (blockIdx.x == 0) {
+    // the routes sorted by expert, and the routed experts by route count
+    const int E = p.E, RT = p.RT;
+    int* cnt = rsm;                                    // [16][E]
+    int* base = cnt + (kQbRouteThreads / 32) * E;      // [E]
+    int* wsum = base + E;                              // [33]
+    int* off = wsum + 33;                              // [E+1]
+    int* perm = off + E + 1;                           // [RT]
+    int* cm = perm + RT;                               // [RT+1]: experts per route count, then positions
+    const bool bad = sort_routes_block(p.ids, RT, E, cnt, base, wsum, off, perm);
+    const int NV = off[E];
     for (int e = tid; e <= E; e += kQbRouteThreads) p.off[e] = off[e];
     for (int s = tid; s < NV; s += kQbRouteThreads) p.perm[s] = perm[s];
     if (bad && (tid & 31) == 0) atomicOr(p.err, kErrBadId);
-    // the routed experts by route count, most first: cm[i] counts the experts
-    // with RT - i routes, its exclusive scan gives each count's first position
+    // most routes first: cm[i] counts the experts with RT - i routes, its
+    // exclusive scan gives each count's first position
     for (int i = tid; i <= RT; i += kQbRouteThreads) cm[i] = 0;
     __syncthreads();
     for (int e = tid; e < E; e += kQbRouteThreads) {
@@ -156,10 +156,13 @@ __global__ void __launch_bounds__(kQbRouteThreads) k_qb_route(const __grid_const
       p.sched[1] = 0u;
       p.sched[2] = (unsigned)U;
     }
+    if (gridDim.x > 1) return;
   }
-  // every token's q8_1, once: codes, records, and the planes left for inspection
+  // every token's q8_1, once (by the other CTAs): codes, records, and the
+  // planes left for inspection
   const int nbh = p.H / 32;
-  for (int t = blockIdx.x; t < p.T; t += gridDim.x) {
+  const int c0 = gridDim.x > 1 ? 1 : 0, nc = gridDim.x > 1 ? gridDim.x - 1 : 1;
+  for (int t = blockIdx.x - c0; t < p.T; t += nc) {
     const uint16_t* xrow = p.x + (size_t)t * p.H;
     for (int b = tid; b < nbh; b += kQbRouteThreads) {
       uint32_t qw[8];
@@ -186,45 +189,6 @@ __global__ void k_qb_combine(const __grid_constant__ QbParams p) {
   pdl_wait();   // the down kernel's y is complete
   pdl_launch_dependents();
   route_sum4(p.ids, p.y, p.out, p.T, p.K, p.E, p.H, (long long)blockIdx.x * blockDim.x + threadIdx.x);
-}
-
-// q8_1 of the intermediate for the down kernel: sorted row s takes the fp32
-// intermediate of route perm[s]; one 32-value block per thread.  The
-// per-route planes the other paths leave are written too.
-__global__ void k_qb_requant(const __grid_constant__ QbParams p) {
-  pdl_wait();   // the gate_up kernel's intermediate is complete
-  pdl_launch_dependents();
-  const int nbi = p.I / 32;
-  const int NV = __ldcg(p.off + p.E);
-  const long long b = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  if (b >= (long long)NV * nbi) return;
-  const int s = (int)(b / nbi), blk = (int)(b - (long long)s * nbi);
-  const int r = __ldcg(p.perm + s);
-  float v[32];
-  const float4* src = reinterpret_cast<const float4*>(p.inter + (size_t)r * p.I + 32 * blk);
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const float4 f = __ldcg(src + i);
-    v[4 * i] = f.x;
-    v[4 * i + 1] = f.y;
-    v[4 * i + 2] = f.z;
-    v[4 * i + 3] = f.w;
-  }
-  uint32_t qw[8];
-  float d;
-  int sum;
-  q8_1_quantize_block(v, qw, d, sum);
-  const float dh = f16_bits_to_f32(f32_to_f16_bits_rn(d));
-  uint4* qs = reinterpret_cast<uint4*>(p.iqs + (size_t)s * p.I + 32 * blk);
-  qs[0] = make_uint4(qw[0], qw[1], qw[2], qw[3]);
-  qs[1] = make_uint4(qw[4], qw[5], qw[6], qw[7]);
-  *reinterpret_cast<uint2*>(p.iss + ((size_t)s * nbi + blk) * 8) = make_uint2(__float_as_uint(dh), (uint32_t)sum);
-  uint4* qr = reinterpret_cast<uint4*>(p.iq + (size_t)r * p.I + 32 * blk);
-  qr[0] = make_uint4(qw[0], qw[1], qw[2], qw[3]);
-  qr[1] = make_uint4(qw[4], qw[5], qw[6], qw[7]);
-  p.id[r * nbi + blk] = dh;
-  p.isum[r * nbi + blk] = sum;
-  p.ish[r * nbi + blk] = (uint16_t)f32_to_f16_bits_rn(d * (float)sum);
 }
 
 // ------------------------------------------------------------------ grouped kernels
@@ -306,13 +270,16 @@ __device__ __forceinline__ void qb_chunk(const uint8_t* rowa, const uint8_t* row
 
 // PHASE 0: gate_up (row a = gate row i, row b = up row I+i of a 128-pair
 // tile, K = H).  PHASE 1: down (rows a, b = output rows j, j+128 of a
-// 256-row tile, K = I).  Consumer thread (warp w, lane l): unit u = 16w +
-// l%16 of the tile, blocks 4h..4h+3 of each chunk with h = l/16; the two
-// halves of a unit are summed with one shuffle at the end of the tile.
+// 256-row tile, K = I).  Consumer warp w takes blocks 4h..4h+3 of each chunk
+// (h = w/4) for the 32 units 32*(w%4) .. +31 of the tile, one per lane, so
+// a warp's activation loads are broadcasts and a warp of half 0 holds 32
+// consecutive intermediate values (one q8_1 block).  At the end of a tile
+// half 1 hands its partial sums to half 0 through shared memory (two
+// mbarriers, bounded waits) and half 0 runs the epilogue.
 template <int PHASE>
 __global__ void __launch_bounds__(kQbThreads, 1) k_qb_gemm(const __grid_constant__ QbParams p) {
   extern __shared__ uint8_t smem_raw[];
-  __shared__ uint64_t full_bar[kQbStages], empty_bar[kQbStages];
+  __shared__ uint64_t full_bar[kQbStages], empty_bar[kQbStages], xfull_bar, xfree_bar;
   __shared__ QbMeta smeta[kQbStages];
   __shared__ int tile_pre[kMaxE + 1];
   __shared__ int offs[kMaxE + 1];
@@ -331,6 +298,8 @@ __global__ void __launch_bounds__(kQbThreads, 1) k_qb_gemm(const __grid_constant
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], kQbConsumers);
     }
+    mbar_init(&xfull_bar, kQbConsumers / 2);
+    mbar_init(&xfree_bar, kQbConsumers / 2);
     fence_mbar_init();
     prefetch_map(PHASE == 0 ? &p.map_wgu : &p.map_wdn);
     prefetch_map(PHASE == 0 ? &p.map_xq : &p.map_iq);
@@ -422,9 +391,11 @@ __global__ void __launch_bounds__(kQbThreads, 1) k_qb_gemm(const __grid_constant
   }
 
   // ---------------- consumers: follow the producer's stages
-  const int u = 16 * warp + (lane & 15), h = lane >> 4;
+  const int u = 32 * (warp & 3) + lane, h = warp >> 2;
+  float2* xch = reinterpret_cast<float2*>(base + (size_t)kQbStages * kQbStageBytes);   // [kQbTok][128]
   float acca[kQbTok], accb[kQbTok];
   bool ok = true;
+  uint32_t ntile = 0;
   for (uint32_t g = 0;; ++g) {
     const uint32_t s = g % kQbStages, ph = (g / kQbStages) & 1u;
     if (!qb_wait(&full_bar[s], ph, abort)) {
@@ -443,24 +414,60 @@ __global__ void __launch_bounds__(kQbThreads, 1) k_qb_gemm(const __grid_constant
                                     nv, acca, accb);
     mbar_arrive(&empty_bar[s]);
     if (kc != nK - 1) continue;
-    // ---- the tile is complete
+    // ---- the tile is complete: half 1 hands over, half 0 finishes
+    const uint32_t n = ntile++;
+    if (h == 1) {
+      if (n >= 1 && !qb_wait(&xfree_bar, (n - 1) & 1u, abort)) {
+        ok = false;
+        break;
+      }
 #pragma unroll
-    for (int i = 0; i < kQbTok; ++i) {
-      if (i >= nv) break;
-      acca[i] += __shfl_xor_sync(0xffffffffu, acca[i], 16);
-      accb[i] += __shfl_xor_sync(0xffffffffu, accb[i], 16);
+      for (int k = 0; k < kQbTok; ++k) {
+        if (k >= nv) break;
+        xch[k * 128 + u] = make_float2(acca[k], accb[k]);
+      }
+      mbar_arrive(&xfull_bar);
+      continue;
     }
+    if (!qb_wait(&xfull_bar, n & 1u, abort)) {
+      ok = false;
+      break;
+    }
+#pragma unroll
+    for (int k = 0; k < kQbTok; ++k) {
+      if (k >= nv) break;
+      const float2 o = xch[k * 128 + u];
+      acca[k] += o.x;
+      accb[k] += o.y;
+    }
+    mbar_arrive(&xfree_bar);
     const int e = m.e;
     if (PHASE == 0) {
-      // a = silu(h_gate * s_gate) * (h_up * s_up), by route; half h stores tokens of parity h
+      // prep_inter: a = silu(h_gate * s_gate) * (h_up * s_up) in fp32, then
+      // the q8_1 of the warp's 32 values for every token, sorted and by route
       const int i = m.rb * 128 + u;
+      const int nbi = p.I / 32, blk = i / 32;
       const float sg = __ldg(p.scales + 4 * e + 0), su = __ldg(p.scales + 4 * e + 1);
 #pragma unroll
       for (int k = 0; k < kQbTok; ++k) {
         if (k >= nv) break;
-        if ((k & 1) != h) continue;
-        const int r = __ldcg(p.perm + m.srow0 + k);
-        p.inter[(size_t)r * p.I + i] = silu_glu(acca[k] * sg, accb[k] * su);
+        const int srow = m.srow0 + k;
+        const int r = __ldcg(p.perm + srow);
+        const float a = silu_glu(acca[k] * sg, accb[k] * su);
+        float d;
+        int sum;
+        const int q = q8_1_quantize_lane(a, d, sum);
+        const float dh = f16_bits_to_f32(f32_to_f16_bits_rn(d));
+        p.inter[(size_t)r * p.I + i] = a;
+        p.iqs[(size_t)srow * p.I + i] = (int8_t)q;
+        p.iq[(size_t)r * p.I + i] = (int8_t)q;
+        if (lane == 0) {
+          *reinterpret_cast<uint2*>(p.iss + ((size_t)srow * nbi + blk) * 8) =
+              make_uint2(__float_as_uint(dh), (uint32_t)sum);
+          p.id[r * nbi + blk] = dh;
+          p.isum[r * nbi + blk] = sum;
+          p.ish[r * nbi + blk] = (uint16_t)f32_to_f16_bits_rn(d * (float)sum);
+        }
       }
     } else {
       const int j = m.rb * 256 + u;
@@ -468,7 +475,6 @@ __global__ void __launch_bounds__(kQbThreads, 1) k_qb_gemm(const __grid_constant
 #pragma unroll
       for (int k = 0; k < kQbTok; ++k) {
         if (k >= nv) break;
-        if ((k & 1) != h) continue;
         const int r = __ldcg(p.perm + m.srow0 + k);
         const float f = sd * __ldg(p.w + r);
         p.y[(size_t)r * p.H + j] = acca[k] * f;
@@ -479,7 +485,7 @@ __global__ void __launch_bounds__(kQbThreads, 1) k_qb_gemm(const __grid_constant
   if (!ok) atomicOr(p.err, kErrTimeout);
 }
 
-size_t qb_gemm_smem() { return 128 + (size_t)kQbStages * kQbStageBytes; }
+size_t qb_gemm_smem() { return 128 + (size_t)kQbStages * kQbStageBytes + (size_t)kQbTok * 128 * sizeof(float2); }
 
 template <typename Kern>
 cudaError_t launch_qb(Kern kernel, int grid, int threads, size_t smem, cudaStream_t stream, const QbParams& p) {
@@ -505,10 +511,6 @@ cudaError_t launch_qbatch(const QbParams& p, cudaStream_t stream) {
   cudaError_t e;
   if ((e = launch_qb(k_qb_route, G, kQbRouteThreads, qb_route_smem(p.E, p.RT), stream, p)) != cudaSuccess) return e;
   if ((e = launch_qb(k_qb_gemm<0>, G, kQbThreads, qb_gemm_smem(), stream, p)) != cudaSuccess) return e;
-  {
-    const long long n = (long long)p.RT * (p.I / 32);   // upper bound of the valid routes' blocks
-    if ((e = launch_qb(k_qb_requant, (int)((n + 255) / 256), 256, 0, stream, p)) != cudaSuccess) return e;
-  }
   if ((e = launch_qb(k_qb_gemm<1>, G, kQbThreads, qb_gemm_smem(), stream, p)) != cudaSuccess) return e;
   const long long n = (long long)p.T * (p.H / 4);
   return launch_qb(k_qb_combine, (int)((n + 255) / 256), 256, 0, stream, p);

@@ -109,16 +109,17 @@ struct DtParams {
 // cannot hold: routes sorted by expert, each token's x quantized to q8_1 once,
 // then two grouped CUDA-core kernels that stream one 144-byte super-block
 // column of 256 weight rows per 2-D TMA stage and dot each decoded block with
-// up to 32 routed tokens (tiles handed out heaviest expert first), and the
+// up to kQbTileTokens routed tokens (tiles handed out heaviest expert first), and the
 // fixed-order route sum.  A q8_1 block record is 8 bytes: the fp16-rounded
 // scale as fp32, then the int32 code sum.  H and I are multiples of 256.
+constexpr int kQbTileTokens = 16;   // routed tokens per tile of the batched Q4_K kernels
 struct QbParams {
   CUtensorMap map_wgu;      // gate_up bank as bytes [E*2I][rb_gu], box 144 x 128 rows
   CUtensorMap map_wdn;      // down bank as bytes [E*H][rb_dn], box 144 x 128 rows
   CUtensorMap map_xq;       // xq [T][H], box 256 x 1 row
   CUtensorMap map_xr;       // xrec [T][H/4], box 64 x 1 row
-  CUtensorMap map_iq;       // iqs [RTp][I], box 256 x 32 rows
-  CUtensorMap map_is;       // iss [RTp][I/4], box 64 x 32 rows
+  CUtensorMap map_iq;       // iqs [RTp][I], box 256 x kQbTileTokens rows
+  CUtensorMap map_is;       // iss [RTp][I/4], box 64 x kQbTileTokens rows
   int H, I, E, K, T, RT, RTp;
   const float* scales;      // [E][4]
   const uint16_t* x;        // bf16 [T][H]
@@ -159,8 +160,8 @@ cudaError_t launch_layer_small(const DecodeParams& p, cudaStream_t stream);
 constexpr int kDtLaunches = 4;
 cudaError_t launch_dense(const DtParams& p, cudaStream_t stream);
 
-// Batched path for Q4_K banks (five launches: route + quantize, gate_up, requantize, down, route sum).
-constexpr int kQbLaunches = 5;
+// Batched path for Q4_K banks (four launches: route + quantize, gate_up + requantize, down, route sum).
+constexpr int kQbLaunches = 4;
 cudaError_t launch_qbatch(const QbParams& p, cudaStream_t stream);
 
 // Test hooks.
