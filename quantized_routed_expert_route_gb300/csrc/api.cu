@@ -23,11 +23,15 @@ struct moe_bank {
   bool owns_rows;
   int device;
   // Grouped path for batches the fused kernel cannot hold: kGroupedDense
-  // (BF16 gate_up and down, H and I multiples of 64) or kGroupedQ4K (Q4_K
-  // gate_up and down), with the bank's rows as 2-D tensors for TMA.
+  // (BF16 gate_up and down, H and I multiples of 64) or kGroupedQuant (Q4_K
+  // or NVFP4 gate_up and down, H and I multiples of 256), with the bank's
+  // rows as 2-D tensors for TMA.
   int grouped;
-  CUtensorMap map_gu;       // dense: bf16 [E*2I][H], box 64 x 128; Q4_K: bytes [E*2I][rb_gu], box 144 x 128
-  CUtensorMap map_dn;       // dense: bf16 [E*H][I]; Q4_K: bytes [E*H][rb_dn]
+  CUtensorMap map_gu;       // dense: bf16 [E*2I][H], box 64 x 128; Q4_K: bytes [E*2I][rb_gu], box 144 x 128;
+                            // NVFP4: the same bytes, box 128 x 128 (code bytes, 128-byte swizzle)
+  CUtensorMap map_dn;       // the same for [E*H] down rows
+  CUtensorMap map_gus;      // NVFP4: the same bytes, box 16 x 128 (scale bytes)
+  CUtensorMap map_dns;
 };
 
 namespace {
@@ -81,9 +85,10 @@ bool map_bf16_rows(CUtensorMap* m, const void* base, uint64_t rows, uint64_t col
 
 // A row-major byte matrix [rows][cols] as a 2-D tensor map: boxes of
 // box_cols bytes (a multiple of 16) x box_rows rows, copied to shared memory
-// densely (rows box_cols bytes apart); reads outside the matrix fill zeros.
+// densely (rows box_cols bytes apart), or with the 128-byte swizzle (box_cols
+// = 128); reads outside the matrix fill zeros.
 bool map_byte_rows(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_cols,
-                   uint32_t box_rows) {
+                   uint32_t box_rows, bool swizzle128 = false) {
   const EncodeTiledFn fn = encode_tiled();
   if (!fn) return false;
   const cuuint64_t dims[2] = {cols, rows};
@@ -91,15 +96,17 @@ bool map_byte_rows(CUtensorMap* m, const void* base, uint64_t rows, uint64_t col
   const cuuint32_t box[2] = {box_cols, box_rows};
   const cuuint32_t estr[2] = {1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+            CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-enum { kGroupedNone = 0, kGroupedDense = 1, kGroupedQ4K = 2 };
+enum { kGroupedNone = 0, kGroupedDense = 1, kGroupedQuant = 2 };
 
 int grouped_kind(const moe_layer_geom& g) {
   if (g.gate_up_type == MOE_BF16 && g.down_type == MOE_BF16 && g.H % 64 == 0 && g.I % 64 == 0) return kGroupedDense;
-  if (g.gate_up_type == MOE_Q4_K && g.down_type == MOE_Q4_K && g.H % 256 == 0 && g.I % 256 == 0) return kGroupedQ4K;
+  if ((g.gate_up_type == MOE_Q4_K || g.gate_up_type == MOE_NVFP4) && g.down_type == g.gate_up_type &&
+      g.H % 256 == 0 && g.I % 256 == 0)
+    return kGroupedQuant;
   return kGroupedNone;
 }
 
@@ -174,7 +181,7 @@ WsLayout ws_layout(const moe_layer_geom& g, int T) {
   if (gk == kGroupedDense) {
     L.d_xs = o; o = align_up(o + 2 * (size_t)L.RTp * g.H, A);
     L.d_ih = o; o = align_up(o + 2 * 2 * (size_t)L.RTp * g.I, A);
-  } else if (gk == kGroupedQ4K) {
+  } else if (gk == kGroupedQuant) {
     L.q_sched = o; o = align_up(o + 4 * 4, A);
     L.q_eord = o; o = align_up(o + 4 * (size_t)g.E, A);
     L.q_xr = o; o = align_up(o + (size_t)T * (g.H / 4), A);
@@ -307,9 +314,9 @@ DecodeParams make_params(const moe_bank* b, const WsLayout& L, uint8_t* ws, cons
   plan_layer_small(g, T, p);
   // The grouped paths take over from the fused kernel once they are faster
   // (measured on the Laguna-shaped layers: BF16 from 2 tokens, Q4_K from
-  // 64 routes per pass).
+  // 64 routes per pass; NVFP4 takes the Q4_K rule).
   const int RTn = T * g.top_k;
-  if ((b->grouped == kGroupedDense && T >= 2) || (b->grouped == kGroupedQ4K && RTn >= 64)) p.use_ls = 0;
+  if ((b->grouped == kGroupedDense && T >= 2) || (b->grouped == kGroupedQuant && RTn >= 64)) p.use_ls = 0;
   switch (p.gu_type) {
     case W_NVFP4: p.w0 = 2; break;
     case W_Q4_K: p.w0 = 3; break;
@@ -404,10 +411,16 @@ int moe_bank_create(const moe_layer_geom* geom, const void* gate_up, size_t gate
       map_bf16_rows(&b->map_gu, b->gu, (uint64_t)g.E * 2 * g.I, (uint64_t)g.H, 128) &&
       map_bf16_rows(&b->map_dn, b->dn, (uint64_t)g.E * g.H, (uint64_t)g.I, 128))
     b->grouped = kGroupedDense;
-  if (gk == kGroupedQ4K &&
+  if (gk == kGroupedQuant && g.gate_up_type == MOE_Q4_K &&
       map_byte_rows(&b->map_gu, b->gu, (uint64_t)g.E * 2 * g.I, (uint64_t)rb_gu, 144, 128) &&
       map_byte_rows(&b->map_dn, b->dn, (uint64_t)g.E * g.H, (uint64_t)rb_dn, 144, 128))
-    b->grouped = kGroupedQ4K;
+    b->grouped = kGroupedQuant;
+  if (gk == kGroupedQuant && g.gate_up_type == MOE_NVFP4 &&
+      map_byte_rows(&b->map_gu, b->gu, (uint64_t)g.E * 2 * g.I, (uint64_t)rb_gu, 128, 128, true) &&
+      map_byte_rows(&b->map_dn, b->dn, (uint64_t)g.E * g.H, (uint64_t)rb_dn, 128, 128, true) &&
+      map_byte_rows(&b->map_gus, b->gu, (uint64_t)g.E * 2 * g.I, (uint64_t)rb_gu, 16, 128) &&
+      map_byte_rows(&b->map_dns, b->dn, (uint64_t)g.E * g.H, (uint64_t)rb_dn, 16, 128))
+    b->grouped = kGroupedQuant;
   *out = b;
   return MOE_OK;
 }
@@ -473,6 +486,9 @@ static bool qbatch_params(const moe_bank* b, const WsLayout& L, uint8_t* ws, con
   std::memset(&q, 0, sizeof(q));
   q.map_wgu = b->map_gu;
   q.map_wdn = b->map_dn;
+  q.map_wgus = b->map_gus;
+  q.map_wdns = b->map_dns;
+  q.wt = g.gate_up_type;
   q.H = g.H; q.I = g.I; q.E = g.E; q.K = g.top_k; q.T = p.T;
   q.RT = p.T * g.top_k;
   q.RTp = L.RTp;
@@ -532,7 +548,7 @@ static int decode_impl(const moe_bank* b, const void* x, int32_t T, const int32_
       if ((e = launch_dense(d, s)) != cudaSuccess) return cuda_fail(e, "dense launch");
       continue;
     }
-    if (b->grouped == kGroupedQ4K) {
+    if (b->grouped == kGroupedQuant) {
       QbParams q;
       if (!qbatch_params(b, L, static_cast<uint8_t*>(ws), p, q)) return MOE_ECUDA;
       if ((e = launch_qbatch(q, s)) != cudaSuccess) return cuda_fail(e, "batched launch");
@@ -562,7 +578,7 @@ int moe_decode_kernel_count(const moe_bank* b, int32_t T) {
     const DecodeParams p = make_params(b, L, nullptr, sh, tn);
     n += p.use_ls                            ? 1
          : b->grouped == kGroupedDense       ? kDtLaunches
-         : b->grouped == kGroupedQ4K         ? kQbLaunches
+         : b->grouped == kGroupedQuant         ? kQbLaunches
          : (p.maxnt != 1 ? 3 : 2);
   }
   return n;

@@ -42,6 +42,7 @@
 // from L2, for each further 16 routed tokens of an expert).  Every wait is bounded in device time; on a timeout the CTA raises the
 // error word, stops issuing and lets its copies in flight land before exiting.
 #include "decode_common.cuh"
+#include "tc.cuh"
 
 namespace qre {
 
@@ -268,6 +269,44 @@ __device__ __forceinline__ void qb_chunk(const uint8_t* rowa, const uint8_t* row
   }
 }
 
+// NVFP4 blocks 4h .. 4h+3 of one K chunk for rows a and b (unit u of the
+// tile): each row's 128 code bytes sit in a 128-byte-swizzled tile (16-byte
+// chunk j of row u at position j ^ (u % 8)), its 16 UE4M3 bytes at scl + 16u.
+// Each 32-value block's two 16-value integer dots with a token's q8_1 block
+// are scaled as d_a * 0.5 * (scale_0 * dot_0 + scale_1 * dot_1).
+template <int REC_PITCH>
+__device__ __forceinline__ void qb_chunk_nvfp4(const uint8_t* ca, const uint8_t* cb, const uint8_t* sla,
+                                               const uint8_t* slb, int u, const uint8_t* codes, const uint8_t* recs,
+                                               int h, int nv, float (&acca)[kQbTok], float (&accb)[kQbTok]) {
+  const uint4 sa4 = lds128(sla + 16 * u), sb4 = lds128(slb + 16 * u);
+  // the scale words of blocks 4h .. 4h+3 (two UE4M3 bytes a block)
+  const uint32_t swa0 = h ? sa4.z : sa4.x, swa1 = h ? sa4.w : sa4.y;
+  const uint32_t swb0 = h ? sb4.z : sb4.x, swb1 = h ? sb4.w : sb4.y;
+#pragma unroll
+  for (int jj = 0; jj < 4; ++jj) {
+    const int j = 4 * h + jj;
+    uint32_t pa[8], na[8], pb[8], nb[8];
+    nvfp4_words(lds128(ca + tc::sw128_chunk(u, j)), pa, na);
+    nvfp4_words(lds128(cb + tc::sw128_chunk(u, j)), pb, nb);
+    const uint32_t wa = jj < 2 ? swa0 : swa1, wb = jj < 2 ? swb0 : swb1;
+    const float2 fa = ue4m3x2_to_float2((uint16_t)(wa >> (16 * (jj & 1))));
+    const float2 fb = ue4m3x2_to_float2((uint16_t)(wb >> (16 * (jj & 1))));
+#pragma unroll
+    for (int t = 0; t < kQbTok; ++t) {
+      if (t >= nv) break;
+      const uint8_t* cp = codes + t * 256 + 32 * j;
+      const uint4 q0 = lds128(cp), q1 = lds128(cp + 16);
+      const int q[8] = {(int)q0.x, (int)q0.y, (int)q0.z, (int)q0.w, (int)q1.x, (int)q1.y, (int)q1.z, (int)q1.w};
+      const float ad = *reinterpret_cast<const float*>(recs + t * REC_PITCH + 8 * j);
+      int a0, a1, b0, b1;
+      nvfp4_int_dots(pa, na, q, a0, a1);
+      nvfp4_int_dots(pb, nb, q, b0, b1);
+      acca[t] += ad * 0.5f * (fa.x * (float)a0 + fa.y * (float)a1);
+      accb[t] += ad * 0.5f * (fb.x * (float)b0 + fb.y * (float)b1);
+    }
+  }
+}
+
 // PHASE 0: gate_up (row a = gate row i, row b = up row I+i of a 128-pair
 // tile, K = H).  PHASE 1: down (rows a, b = output rows j, j+128 of a
 // 256-row tile, K = I).  Consumer warp w takes blocks 4h..4h+3 of each chunk
@@ -276,7 +315,7 @@ __device__ __forceinline__ void qb_chunk(const uint8_t* rowa, const uint8_t* row
 // consecutive intermediate values (one q8_1 block).  At the end of a tile
 // half 1 hands its partial sums to half 0 through shared memory (two
 // mbarriers, bounded waits) and half 0 runs the epilogue.
-template <int PHASE>
+template <int PHASE, int WT>
 __global__ void __launch_bounds__(kQbThreads, 1) k_qb_gemm(const __grid_constant__ QbParams p) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t full_bar[kQbStages], empty_bar[kQbStages], xfull_bar, xfree_bar;
@@ -286,7 +325,7 @@ __global__ void __launch_bounds__(kQbThreads, 1) k_qb_gemm(const __grid_constant
   __shared__ int eord[kMaxE];
   __shared__ int wsum[33];
   __shared__ volatile int abort_flag;
-  uint8_t* base = smem_raw + ((128u - (smem_addr(smem_raw) & 127u)) & 127u);
+  uint8_t* base = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);   // swizzled tiles need 1024
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int E = p.E;
   const int NB = PHASE == 0 ? p.I / 128 : p.H / 256;
@@ -302,6 +341,7 @@ __global__ void __launch_bounds__(kQbThreads, 1) k_qb_gemm(const __grid_constant
     mbar_init(&xfree_bar, kQbConsumers / 2);
     fence_mbar_init();
     prefetch_map(PHASE == 0 ? &p.map_wgu : &p.map_wdn);
+    if (WT == W_NVFP4) prefetch_map(PHASE == 0 ? &p.map_wgus : &p.map_wdns);
     prefetch_map(PHASE == 0 ? &p.map_xq : &p.map_iq);
     prefetch_map(PHASE == 0 ? &p.map_xr : &p.map_is);
   }
@@ -360,20 +400,29 @@ __global__ void __launch_bounds__(kQbThreads, 1) k_qb_gemm(const __grid_constant
           }
           smeta[s] = QbMeta{e, rb, srow0, nv | (kc << 8)};
           uint8_t* st = base + s * kQbStageBytes;
+          // rows a (box at ya) and b (box at yb) of the tile: 36,864 bytes in both formats
+          const int ya = PHASE == 0 ? e * 2 * p.I + rb * 128 : e * p.H + rb * 256;
+          const int yb = PHASE == 0 ? ya + p.I : ya + 128;
+          const CUtensorMap* mw = PHASE == 0 ? &p.map_wgu : &p.map_wdn;
+          mbar_arrive_expect_tx(&full_bar[s], PHASE == 0 ? (uint32_t)(kQbCodesOff + nv * 320)
+                                                         : (uint32_t)(kQbRecOff + kQbTok * 64));
+          if (WT == W_Q4_K) {
+            tma_load_2d_hint(st, mw, kc * kQbSb, ya, &full_bar[s], pol);
+            tma_load_2d_hint(st + 128 * kQbSb, mw, kc * kQbSb, yb, &full_bar[s], pol);
+          } else {
+            const CUtensorMap* ms = PHASE == 0 ? &p.map_wgus : &p.map_wdns;
+            const int xs = (PHASE == 0 ? p.H : p.I) / 2 + kc * 16;
+            tma_load_2d_hint(st, mw, kc * 128, ya, &full_bar[s], pol);
+            tma_load_2d_hint(st + 16384, mw, kc * 128, yb, &full_bar[s], pol);
+            tma_load_2d_hint(st + 32768, ms, xs, ya, &full_bar[s], pol);
+            tma_load_2d_hint(st + 34816, ms, xs, yb, &full_bar[s], pol);
+          }
           if (PHASE == 0) {
-            mbar_arrive_expect_tx(&full_bar[s], (uint32_t)(kQbCodesOff + nv * 320));
-            const int y0 = e * 2 * p.I + rb * 128;
-            tma_load_2d_hint(st, &p.map_wgu, kc * kQbSb, y0, &full_bar[s], pol);
-            tma_load_2d_hint(st + 128 * kQbSb, &p.map_wgu, kc * kQbSb, y0 + p.I, &full_bar[s], pol);
             for (int i = 0; i < nv; ++i) {
               tma_load_2d(st + kQbCodesOff + 256 * i, &p.map_xq, kc * 256, tok[i], &full_bar[s]);
               tma_load_2d(st + kQbRecOff + 128 * i, &p.map_xr, kc * 64, tok[i], &full_bar[s]);
             }
           } else {
-            mbar_arrive_expect_tx(&full_bar[s], (uint32_t)(kQbRecOff + kQbTok * 64));
-            const int y0 = e * p.H + rb * 256;
-            tma_load_2d_hint(st, &p.map_wdn, kc * kQbSb, y0, &full_bar[s], pol);
-            tma_load_2d_hint(st + 128 * kQbSb, &p.map_wdn, kc * kQbSb, y0 + 128, &full_bar[s], pol);
             tma_load_2d(st + kQbCodesOff, &p.map_iq, kc * 256, srow0, &full_bar[s]);
             tma_load_2d(st + kQbRecOff, &p.map_is, kc * 64, srow0, &full_bar[s]);
           }
@@ -410,8 +459,12 @@ __global__ void __launch_bounds__(kQbThreads, 1) k_qb_gemm(const __grid_constant
       for (int i = 0; i < kQbTok; ++i) acca[i] = accb[i] = 0.f;
     }
     const uint8_t* st = base + s * kQbStageBytes;
-    qb_chunk<PHASE == 0 ? 128 : 64>(st + u * kQbSb, st + (128 + u) * kQbSb, st + kQbCodesOff, st + kQbRecOff, h,
-                                    nv, acca, accb);
+    if (WT == W_Q4_K)
+      qb_chunk<PHASE == 0 ? 128 : 64>(st + u * kQbSb, st + (128 + u) * kQbSb, st + kQbCodesOff, st + kQbRecOff, h,
+                                      nv, acca, accb);
+    else
+      qb_chunk_nvfp4<PHASE == 0 ? 128 : 64>(st, st + 16384, st + 32768, st + 34816, u, st + kQbCodesOff,
+                                            st + kQbRecOff, h, nv, acca, accb);
     mbar_arrive(&empty_bar[s]);
     if (kc != nK - 1) continue;
     // ---- the tile is complete: half 1 hands over, half 0 finishes
@@ -485,7 +538,7 @@ __global__ void __launch_bounds__(kQbThreads, 1) k_qb_gemm(const __grid_constant
   if (!ok) atomicOr(p.err, kErrTimeout);
 }
 
-size_t qb_gemm_smem() { return 128 + (size_t)kQbStages * kQbStageBytes + (size_t)kQbTok * 128 * sizeof(float2); }
+size_t qb_gemm_smem() { return 1024 + (size_t)kQbStages * kQbStageBytes + (size_t)kQbTok * 128 * sizeof(float2); }
 
 template <typename Kern>
 cudaError_t launch_qb(Kern kernel, int grid, int threads, size_t smem, cudaStream_t stream, const QbParams& p) {
@@ -510,8 +563,13 @@ cudaError_t launch_qbatch(const QbParams& p, cudaStream_t stream) {
   const int G = sm_count();
   cudaError_t e;
   if ((e = launch_qb(k_qb_route, G, kQbRouteThreads, qb_route_smem(p.E, p.RT), stream, p)) != cudaSuccess) return e;
-  if ((e = launch_qb(k_qb_gemm<0>, G, kQbThreads, qb_gemm_smem(), stream, p)) != cudaSuccess) return e;
-  if ((e = launch_qb(k_qb_gemm<1>, G, kQbThreads, qb_gemm_smem(), stream, p)) != cudaSuccess) return e;
+  if (p.wt == W_NVFP4) {
+    if ((e = launch_qb(k_qb_gemm<0, W_NVFP4>, G, kQbThreads, qb_gemm_smem(), stream, p)) != cudaSuccess) return e;
+    if ((e = launch_qb(k_qb_gemm<1, W_NVFP4>, G, kQbThreads, qb_gemm_smem(), stream, p)) != cudaSuccess) return e;
+  } else {
+    if ((e = launch_qb(k_qb_gemm<0, W_Q4_K>, G, kQbThreads, qb_gemm_smem(), stream, p)) != cudaSuccess) return e;
+    if ((e = launch_qb(k_qb_gemm<1, W_Q4_K>, G, kQbThreads, qb_gemm_smem(), stream, p)) != cudaSuccess) return e;
+  }
   const long long n = (long long)p.T * (p.H / 4);
   return launch_qb(k_qb_combine, (int)((n + 255) / 256), 256, 0, stream, p);
 }

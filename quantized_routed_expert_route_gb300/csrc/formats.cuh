@@ -161,11 +161,26 @@ __device__ __forceinline__ ActQ8 load_act_q8(const int8_t* q, const float* d, co
 constexpr uint32_t kE2M1x2Lo = 0x03020100u;
 constexpr uint32_t kE2M1x2Hi = 0x0C080604u;
 
-// Decode the 32 codes of block b (16 bytes) into magnitude words split by
-// sign: pos[w] holds |2*value| of the non-negative codes of elements
-// 4w..4w+3 (0 for negative codes), neg[w] those of the negative codes.  The
-// split comes free from prmt: a selector nibble with its top bit set yields
-// the replicated sign of a non-negative table byte, i.e. 0.
+// The 32 codes of one block (16 bytes, element 2i in the low nibble of byte
+// i) as magnitude words split by sign: pos[w] holds |2*value| of the
+// non-negative codes of elements 4w..4w+3 (0 for negative codes), neg[w]
+// those of the negative codes.  The split comes free from prmt: a selector
+// nibble with its top bit set yields the replicated sign of a non-negative
+// table byte, i.e. 0.
+__device__ __forceinline__ void nvfp4_words(const uint4 c, uint32_t (&pos)[8], uint32_t (&neg)[8]) {
+  const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    const uint32_t qv = cw[w], qx = qv ^ 0x88888888u;
+    pos[2 * w] = prmt(kE2M1x2Lo, kE2M1x2Hi, qv);
+    neg[2 * w] = prmt(kE2M1x2Lo, kE2M1x2Hi, qx);
+    pos[2 * w + 1] = prmt(kE2M1x2Lo, kE2M1x2Hi, qv >> 16);
+    neg[2 * w + 1] = prmt(kE2M1x2Lo, kE2M1x2Hi, qx >> 16);
+  }
+}
+
+// Decode the 32 codes of block b of a row (see nvfp4_words) and the UE4M3
+// scales of its two 16-value halves.
 // A row is 9k/16 bytes: 16-byte aligned when k is a multiple of 256, else
 // only 2-byte aligned, and then (kAligned false) the codes are gathered 2
 // bytes at a time.
@@ -182,15 +197,7 @@ __device__ __forceinline__ void nvfp4_decode(const uint8_t* row, int k, int b, u
     c.z = lds16(cp + 8) | ((uint32_t)lds16(cp + 10) << 16);
     c.w = lds16(cp + 12) | ((uint32_t)lds16(cp + 14) << 16);
   }
-  const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
-#pragma unroll
-  for (int w = 0; w < 4; ++w) {
-    const uint32_t qv = cw[w], qx = qv ^ 0x88888888u;
-    pos[2 * w] = prmt(kE2M1x2Lo, kE2M1x2Hi, qv);
-    neg[2 * w] = prmt(kE2M1x2Lo, kE2M1x2Hi, qx);
-    pos[2 * w + 1] = prmt(kE2M1x2Lo, kE2M1x2Hi, qv >> 16);
-    neg[2 * w + 1] = prmt(kE2M1x2Lo, kE2M1x2Hi, qx >> 16);
-  }
+  nvfp4_words(c, pos, neg);
   scales = ue4m3x2_to_float2(lds16(row + (k >> 1) + 2 * b));
 }
 

@@ -105,21 +105,25 @@ struct DtParams {
   float* y;                 // fp32 [RT][H]: down output of each route times s_down * w, by route index
 };
 
-// The batched path for Q4_K banks (decode_qb.cu) at batches the fused kernel
-// cannot hold: routes sorted by expert, each token's x quantized to q8_1 once,
-// then two grouped CUDA-core kernels that stream one 144-byte super-block
-// column of 256 weight rows per 2-D TMA stage and dot each decoded block with
-// up to kQbTileTokens routed tokens (tiles handed out heaviest expert first), and the
-// fixed-order route sum.  A q8_1 block record is 8 bytes: the fp16-rounded
-// scale as fp32, then the int32 code sum.  H and I are multiples of 256.
-constexpr int kQbTileTokens = 16;   // routed tokens per tile of the batched Q4_K kernels
+// The batched path for Q4_K and NVFP4 banks (decode_qb.cu) at batches the
+// fused kernel cannot hold: routes sorted by expert, each token's x quantized
+// to q8_1 once, then two grouped CUDA-core kernels that stream one 256-value
+// K chunk of 256 weight rows per 2-D TMA stage (144 bytes a row in both
+// formats) and dot each decoded block with up to kQbTileTokens routed tokens
+// (tiles handed out heaviest expert first), and the fixed-order route sum.
+// A q8_1 block record is 8 bytes: the fp16-rounded scale as fp32, then the
+// int32 code sum.  H and I are multiples of 256.
+constexpr int kQbTileTokens = 16;   // routed tokens per tile of the batched kernels
 struct QbParams {
-  CUtensorMap map_wgu;      // gate_up bank as bytes [E*2I][rb_gu], box 144 x 128 rows
-  CUtensorMap map_wdn;      // down bank as bytes [E*H][rb_dn], box 144 x 128 rows
+  // banks as byte matrices [E*2I][rb_gu] and [E*H][rb_dn], boxes of 128 rows:
+  // Q4_K: map_w* boxes 144 bytes wide (one super-block); NVFP4: map_w* boxes
+  // the 128 code bytes of a chunk (128-byte swizzle), map_w*s its 16 scale bytes
+  CUtensorMap map_wgu, map_wdn, map_wgus, map_wdns;
   CUtensorMap map_xq;       // xq [T][H], box 256 x 1 row
   CUtensorMap map_xr;       // xrec [T][H/4], box 64 x 1 row
   CUtensorMap map_iq;       // iqs [RTp][I], box 256 x kQbTileTokens rows
   CUtensorMap map_is;       // iss [RTp][I/4], box 64 x kQbTileTokens rows
+  int wt;                   // W_Q4_K or W_NVFP4 (both projections)
   int H, I, E, K, T, RT, RTp;
   const float* scales;      // [E][4]
   const uint16_t* x;        // bf16 [T][H]

@@ -1,4 +1,4 @@
-"""GPU parity of the batched path for Q4_K banks: batches the fused
+"""GPU parity of the batched path for Q4_K and NVFP4 banks: batches the fused
 small-batch kernel cannot hold, decoded by the grouped CUDA-core kernels
 (route + quantize, gate_up + requantize, down, route sum: four launches per
 pass).  Same bounds as the other decode tests (tests/tolerance.py),
@@ -21,6 +21,7 @@ from tests.test_decode_gpu import _check_case  # noqa: E402
 
 BATCHED_LAUNCHES = 4
 Q4K = F.TYPE_Q4_K
+NV4 = F.TYPE_NVFP4
 
 
 @pytest.mark.parametrize("T", [16, 64])
@@ -33,34 +34,47 @@ def test_laguna_q4k_zipf_batches(T):
     assert figs["err_bits"] == 0
 
 
-def test_every_token_with_stages():
-    """40 tokens over 24 experts (tiles of 1..32 tokens), every token checked
-    with the stage exports."""
-    case = cases.make_case(2048, 512, 24, 5, Q4K, Q4K, 40, seed=310)
+@pytest.mark.parametrize("T", [8, 16])
+def test_qwen3_30b_a3b_shaped_nvfp4_batches(T):
+    """H=2048 I=768 E=128 top-8 NVFP4 with per-expert weight_scale_2, softmax
+    routing, every token checked with the stage exports."""
+    case = cases.make_case(2048, 768, 128, 8, NV4, NV4, T, seed=350 + T)
     figs = _check_case(case)
     assert figs["launches"] == BATCHED_LAUNCHES
     assert figs["err_bits"] == 0
 
 
-def test_one_expert_over_many_token_blocks():
+@pytest.mark.parametrize("wtype", [Q4K, NV4])
+def test_every_token_with_stages(wtype):
+    """40 tokens over 24 experts (tiles of 1..16 tokens), every token checked
+    with the stage exports."""
+    case = cases.make_case(2048, 512, 24, 5, wtype, wtype, 40, seed=310 + wtype)
+    figs = _check_case(case)
+    assert figs["launches"] == BATCHED_LAUNCHES
+    assert figs["err_bits"] == 0
+
+
+@pytest.mark.parametrize("wtype", [Q4K, NV4])
+def test_one_expert_over_many_token_blocks(wtype):
     """Every route on one expert (duplicates inside each token): 256 routed
-    rows, eight 32-token blocks per weight tile."""
+    rows, sixteen 16-token blocks per weight tile."""
     T, K = 64, 4
     ids = [[3] * K for _ in range(T)]
-    case = cases.make_case(2048, 512, 8, K, Q4K, Q4K, T, seed=320, ids=ids)
+    case = cases.make_case(2048, 512, 8, K, wtype, wtype, T, seed=320 + wtype, ids=ids)
     figs = _check_case(case, tokens=[0, 31, 32, 63])
     assert figs["launches"] == BATCHED_LAUNCHES
     assert figs["err_bits"] == 0
 
 
-def test_bad_ids_flag_and_contribute_zero():
+@pytest.mark.parametrize("wtype", [Q4K, NV4])
+def test_bad_ids_flag_and_contribute_zero(wtype):
     T, K = 48, 3
     r = np.random.default_rng(7)
     ids = r.integers(0, 16, size=(T, K)).astype(np.int32)
     ids[0, 1] = 99
     ids[7, 0] = -1
     ids[47, 2] = 16
-    case = cases.make_case(2048, 512, 16, K, Q4K, Q4K, T, seed=330, ids=ids)
+    case = cases.make_case(2048, 512, 16, K, wtype, wtype, T, seed=330 + wtype, ids=ids)
     figs = _check_case(case, tokens=[0, 7, 20, 47])
     assert figs["launches"] == BATCHED_LAUNCHES
     assert figs["err_bits"] & capi.MOE_DEVERR_BAD_ID
