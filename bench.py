@@ -391,7 +391,7 @@ def profile_layer(a):
     else:
         t = Q4_K if a.profile_layer == "q4_k" else BF16
         L = LAGUNA
-        st = Stack([(t, t)] * a.layers, L["H"], L["I"], L["E"], L["K"], 3, dev)
+        st = Stack([(t, t)] * a.layers, L["H"], L["I"], a.experts or L["E"], L["K"], 3, dev)
         st.prepare(a.T, "zipf", 3 + a.T)
     torch.cuda.synchronize()
     s = torch.cuda.current_stream().cuda_stream
@@ -429,6 +429,8 @@ def main():
     ap.add_argument("--profile-layer", choices=["nvfp4", "q4_k", "bf16"], default=None,
                     help="run --steps eager decode passes of one layer type (for ncu), print nothing else")
     ap.add_argument("--T", type=int, default=1)
+    ap.add_argument("--experts", type=int, default=0,
+                    help="with --profile-layer q4_k/bf16: experts per layer (default 256), to shrink a capture")
     ap.add_argument("--profile-prefill", choices=["w4a4", "w4a8"], default=None,
                     help="run --steps prompt-path chunks (for ncu), print nothing else")
     a = ap.parse_args()

@@ -18,7 +18,7 @@
 //                other CTAs quantize every token's x to q8_1 once (codes and
 //                8-byte block records).
 //   k_qb_gemm<0> gate_up + prep_inter.  A tile is (expert, 128 intermediate
-//                columns, <= 16 routed tokens); tiles come from a global counter,
+//                columns, <= 8 routed tokens); tiles come from a global counter,
 //                heaviest experts first.  Per 256-value K chunk one stage
 //                holds the chunk's 144-byte super-block of the 128 gate rows
 //                and of the 128 up rows (2-D TMA, rows 144 bytes apart:
@@ -32,15 +32,17 @@
 //                s_gate / s_up and SiLU-GLU in fp32 and requantizes each
 //                warp's 32 intermediate values to q8_1 (sorted rows for the
 //                down kernel, and by route).
-//   k_qb_gemm<1> down.  A tile is (expert, 256 output rows, <= 16 tokens), a
+//   k_qb_gemm<1> down.  A tile is (expert, 256 output rows, <= 8 tokens), a
 //                thread owns rows j and j+128; the epilogue scales by s_down *
 //                routing weight and stores fp32 per route.
 //   k_qb_combine out[t] = bf16(sum over k = 0..K-1 of the route rows), in
 //                route order, no atomics.
 //
 // Every selected expert's rows are read from HBM once per pass (again, mostly
-// from L2, for each further 16 routed tokens of an expert).  Every wait is bounded in device time; on a timeout the CTA raises the
-// error word, stops issuing and lets its copies in flight land before exiting.
+// from L2, for each further 8 routed tokens of an expert: small token blocks
+// keep the tiles' costs even).  Every wait is bounded in device time; on a
+// timeout the CTA raises the error word, stops issuing and lets its copies in
+// flight land before exiting.
 #include "decode_common.cuh"
 #include "tc.cuh"
 

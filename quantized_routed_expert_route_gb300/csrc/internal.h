@@ -113,7 +113,7 @@ struct DtParams {
 // (tiles handed out heaviest expert first), and the fixed-order route sum.
 // A q8_1 block record is 8 bytes: the fp16-rounded scale as fp32, then the
 // int32 code sum.  H and I are multiples of 256.
-constexpr int kQbTileTokens = 16;   // routed tokens per tile of the batched kernels
+constexpr int kQbTileTokens = 8;    // routed tokens per tile of the batched kernels
 struct QbParams {
   // banks as byte matrices [E*2I][rb_gu] and [E*H][rb_dn], boxes of 128 rows:
   // Q4_K: map_w* boxes 144 bytes wide (one super-block); NVFP4: map_w* boxes

@@ -46,7 +46,7 @@ def test_qwen3_30b_a3b_shaped_nvfp4_batches(T):
 
 @pytest.mark.parametrize("wtype", [Q4K, NV4])
 def test_every_token_with_stages(wtype):
-    """40 tokens over 24 experts (tiles of 1..16 tokens), every token checked
+    """40 tokens over 24 experts (tiles of 1..8 tokens), every token checked
     with the stage exports."""
     case = cases.make_case(2048, 512, 24, 5, wtype, wtype, 40, seed=310 + wtype)
     figs = _check_case(case)
@@ -57,7 +57,7 @@ def test_every_token_with_stages(wtype):
 @pytest.mark.parametrize("wtype", [Q4K, NV4])
 def test_one_expert_over_many_token_blocks(wtype):
     """Every route on one expert (duplicates inside each token): 256 routed
-    rows, sixteen 16-token blocks per weight tile."""
+    rows, thirty-two 8-token blocks per weight tile."""
     T, K = 64, 4
     ids = [[3] * K for _ in range(T)]
     case = cases.make_case(2048, 512, 8, K, wtype, wtype, T, seed=320 + wtype, ids=ids)
