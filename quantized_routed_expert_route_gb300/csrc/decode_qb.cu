@@ -50,8 +50,8 @@ namespace qre {
 
 namespace {
 
-constexpr int kQbConsumers = 256;                        // two weight rows x half the blocks per thread
-constexpr int kQbThreads = kQbConsumers + 32;            // + one TMA producer warp (warp 8)
+constexpr int kQbConsumers = 512;                        // two weight rows x a quarter of the blocks per thread
+constexpr int kQbThreads = kQbConsumers + 32;            // + one TMA producer warp (warp 16)
 constexpr int kQbTok = kQbTileTokens;                     // routed tokens per tile
 constexpr int kQbStages = 4;
 constexpr int kQbSb = 144;                               // bytes of one Q4_K super-block (256 values) of a row
@@ -202,107 +202,101 @@ struct __align__(16) QbMeta {
   int e, rb, srow0, nv_kc;   // nv_kc = nv | kc << 8
 };
 
-// d * sc and dmin * m of blocks 4h .. 4h+3 of a Q4_K super-block, from its
+// d * sc and dmin * m of blocks 2q and 2q+1 of a Q4_K super-block, from its
 // 16-byte header (d | dmin << 16, then the 12 packed 6-bit scale bytes).
-__device__ __forceinline__ void q4k_scales4(const uint4 hdr, int h, float (&dsc)[4], float (&dmm)[4]) {
+__device__ __forceinline__ void q4k_scales2(const uint4 hdr, int q, float (&dsc)[2], float (&dmm)[2]) {
   const float d = f16_bits_to_f32(hdr.x & 0xFFFFu);
   const float dmin = f16_bits_to_f32(hdr.x >> 16);
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
+  for (int i = 0; i < 2; ++i) {
+    const int j = 2 * q + i;
     uint32_t sc, m;
-    if (h == 0) {
-      sc = (hdr.y >> (8 * i)) & 63u;
-      m = (hdr.z >> (8 * i)) & 63u;
+    if (j < 4) {
+      sc = (hdr.y >> (8 * j)) & 63u;
+      m = (hdr.z >> (8 * j)) & 63u;
     } else {
-      const uint32_t s8 = (hdr.w >> (8 * i)) & 0xFFu;
-      sc = (s8 & 15u) | (((hdr.y >> (8 * i + 6)) & 3u) << 4);
-      m = (s8 >> 4) | (((hdr.z >> (8 * i + 6)) & 3u) << 4);
+      const int jj = j - 4;
+      const uint32_t s8 = (hdr.w >> (8 * jj)) & 0xFFu;
+      sc = (s8 & 15u) | (((hdr.y >> (8 * jj + 6)) & 3u) << 4);
+      m = (s8 >> 4) | (((hdr.z >> (8 * jj + 6)) & 3u) << 4);
     }
     dsc[i] = d * (float)sc;
     dmm[i] = dmin * (float)m;
   }
 }
 
-// Blocks 4h .. 4h+3 of one K chunk (a 256-value super-block) of the thread's
-// two weight rows against the tile's tokens.  Each 32-byte nibble run holds
-// blocks 2c (low nibbles) and 2c+1 (high nibbles); each block's integer dot
-// with a token's q8_1 block is scaled as d_a * (d*sc*dot - dmin*m*sum_a).
+// Blocks 2q and 2q+1 of one K chunk (a 256-value super-block) of the
+// thread's two weight rows against the tile's tokens: the chunk's 32-byte
+// nibble run q holds block 2q (low nibbles) and block 2q+1 (high nibbles);
+// each block's integer dot with a token's q8_1 block is scaled as
+// d_a * (d*sc*dot - dmin*m*sum_a).
 template <int REC_PITCH>
 __device__ __forceinline__ void qb_chunk(const uint8_t* rowa, const uint8_t* rowb, const uint8_t* codes,
-                                         const uint8_t* recs, int h, int nv, float (&acca)[kQbTok],
+                                         const uint8_t* recs, int q, int nv, float (&acca)[kQbTok],
                                          float (&accb)[kQbTok]) {
-  float dsa[4], dma[4], dsb[4], dmb[4];
-  q4k_scales4(lds128(rowa), h, dsa, dma);
-  q4k_scales4(lds128(rowb), h, dsb, dmb);
+  float dsa[2], dma[2], dsb[2], dmb[2];
+  q4k_scales2(lds128(rowa), q, dsa, dma);
+  q4k_scales2(lds128(rowb), q, dsb, dmb);
+  int al[8], ah[8], bl[8], bh[8];
+  {
+    const uint4 a0 = lds128(rowa + 16 + 32 * q), a1 = lds128(rowa + 32 + 32 * q);
+    const uint4 b0 = lds128(rowb + 16 + 32 * q), b1 = lds128(rowb + 32 + 32 * q);
+    const uint32_t wa[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+    const uint32_t wb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll
-  for (int c = 0; c < 2; ++c) {
-    const int cc = 2 * h + c;
-    int al[8], ah[8], bl[8], bh[8];
-    {
-      const uint4 a0 = lds128(rowa + 16 + 32 * cc), a1 = lds128(rowa + 32 + 32 * cc);
-      const uint4 b0 = lds128(rowb + 16 + 32 * cc), b1 = lds128(rowb + 32 + 32 * cc);
-      const uint32_t wa[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-      const uint32_t wb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        al[i] = (int)(wa[i] & 0x0F0F0F0Fu);
-        ah[i] = (int)((wa[i] >> 4) & 0x0F0F0F0Fu);
-        bl[i] = (int)(wb[i] & 0x0F0F0F0Fu);
-        bh[i] = (int)((wb[i] >> 4) & 0x0F0F0F0Fu);
-      }
+    for (int i = 0; i < 8; ++i) {
+      al[i] = (int)(wa[i] & 0x0F0F0F0Fu);
+      ah[i] = (int)((wa[i] >> 4) & 0x0F0F0F0Fu);
+      bl[i] = (int)(wb[i] & 0x0F0F0F0Fu);
+      bh[i] = (int)((wb[i] >> 4) & 0x0F0F0F0Fu);
     }
-    const float sa0 = dsa[2 * c], ma0 = dma[2 * c], sa1 = dsa[2 * c + 1], ma1 = dma[2 * c + 1];
-    const float sb0 = dsb[2 * c], mb0 = dmb[2 * c], sb1 = dsb[2 * c + 1], mb1 = dmb[2 * c + 1];
+  }
 #pragma unroll
-    for (int t = 0; t < kQbTok; ++t) {
-      if (t >= nv) break;
-      const uint8_t* cp = codes + t * 256 + 64 * cc;
-      const uint4 q0 = lds128(cp), q1 = lds128(cp + 16), q2 = lds128(cp + 32), q3 = lds128(cp + 48);
-      const uint4 rc = lds128(recs + t * REC_PITCH + 16 * cc);   // (d, sum) of blocks 2cc and 2cc+1
-      const int ql[8] = {(int)q0.x, (int)q0.y, (int)q0.z, (int)q0.w, (int)q1.x, (int)q1.y, (int)q1.z, (int)q1.w};
-      const int qh[8] = {(int)q2.x, (int)q2.y, (int)q2.z, (int)q2.w, (int)q3.x, (int)q3.y, (int)q3.z, (int)q3.w};
-      const float d0 = __uint_as_float(rc.x), s0 = (float)(int)rc.y;
-      const float d1 = __uint_as_float(rc.z), s1 = (float)(int)rc.w;
-      acca[t] += d0 * (sa0 * (float)int_dot8(al, ql) - ma0 * s0);
-      accb[t] += d0 * (sb0 * (float)int_dot8(bl, ql) - mb0 * s0);
-      acca[t] += d1 * (sa1 * (float)int_dot8(ah, qh) - ma1 * s1);
-      accb[t] += d1 * (sb1 * (float)int_dot8(bh, qh) - mb1 * s1);
-    }
+  for (int t = 0; t < kQbTok; ++t) {
+    if (t >= nv) break;
+    const uint8_t* cp = codes + t * 256 + 64 * q;
+    const uint4 q0 = lds128(cp), q1 = lds128(cp + 16), q2 = lds128(cp + 32), q3 = lds128(cp + 48);
+    const uint4 rc = lds128(recs + t * REC_PITCH + 16 * q);   // (d, sum) of blocks 2q and 2q+1
+    const int ql[8] = {(int)q0.x, (int)q0.y, (int)q0.z, (int)q0.w, (int)q1.x, (int)q1.y, (int)q1.z, (int)q1.w};
+    const int qh[8] = {(int)q2.x, (int)q2.y, (int)q2.z, (int)q2.w, (int)q3.x, (int)q3.y, (int)q3.z, (int)q3.w};
+    const float d0 = __uint_as_float(rc.x), s0 = (float)(int)rc.y;
+    const float d1 = __uint_as_float(rc.z), s1 = (float)(int)rc.w;
+    acca[t] += d0 * (dsa[0] * (float)int_dot8(al, ql) - dma[0] * s0);
+    accb[t] += d0 * (dsb[0] * (float)int_dot8(bl, ql) - dmb[0] * s0);
+    acca[t] += d1 * (dsa[1] * (float)int_dot8(ah, qh) - dma[1] * s1);
+    accb[t] += d1 * (dsb[1] * (float)int_dot8(bh, qh) - dmb[1] * s1);
   }
 }
 
-// NVFP4 blocks 4h .. 4h+3 of one K chunk for rows a and b (unit u of the
+// NVFP4 blocks 2q and 2q+1 of one K chunk for rows a and b (unit u of the
 // tile): each row's 128 code bytes sit in a 128-byte-swizzled tile (16-byte
-// chunk j of row u at position j ^ (u % 8)), its 16 UE4M3 bytes at scl + 16u.
-// Each 32-value block's two 16-value integer dots with a token's q8_1 block
-// are scaled as d_a * 0.5 * (scale_0 * dot_0 + scale_1 * dot_1).
+// chunk j of row u at position j ^ (u % 8)), its 16 UE4M3 bytes at scl + 16u
+// (word q holds the four scales of blocks 2q and 2q+1).  Each 32-value
+// block's two 16-value integer dots with a token's q8_1 block are scaled as
+// d_a * 0.5 * (scale_0 * dot_0 + scale_1 * dot_1).
 template <int REC_PITCH>
 __device__ __forceinline__ void qb_chunk_nvfp4(const uint8_t* ca, const uint8_t* cb, const uint8_t* sla,
                                                const uint8_t* slb, int u, const uint8_t* codes, const uint8_t* recs,
-                                               int h, int nv, float (&acca)[kQbTok], float (&accb)[kQbTok]) {
-  const uint4 sa4 = lds128(sla + 16 * u), sb4 = lds128(slb + 16 * u);
-  // the scale words of blocks 4h .. 4h+3 (two UE4M3 bytes a block)
-  const uint32_t swa0 = h ? sa4.z : sa4.x, swa1 = h ? sa4.w : sa4.y;
-  const uint32_t swb0 = h ? sb4.z : sb4.x, swb1 = h ? sb4.w : sb4.y;
+                                               int q, int nv, float (&acca)[kQbTok], float (&accb)[kQbTok]) {
+  const uint32_t swa = lds32(sla + 16 * u + 4 * q), swb = lds32(slb + 16 * u + 4 * q);
 #pragma unroll
-  for (int jj = 0; jj < 4; ++jj) {
-    const int j = 4 * h + jj;
+  for (int jj = 0; jj < 2; ++jj) {
+    const int j = 2 * q + jj;
     uint32_t pa[8], na[8], pb[8], nb[8];
     nvfp4_words(lds128(ca + tc::sw128_chunk(u, j)), pa, na);
     nvfp4_words(lds128(cb + tc::sw128_chunk(u, j)), pb, nb);
-    const uint32_t wa = jj < 2 ? swa0 : swa1, wb = jj < 2 ? swb0 : swb1;
-    const float2 fa = ue4m3x2_to_float2((uint16_t)(wa >> (16 * (jj & 1))));
-    const float2 fb = ue4m3x2_to_float2((uint16_t)(wb >> (16 * (jj & 1))));
+    const float2 fa = ue4m3x2_to_float2((uint16_t)(swa >> (16 * jj)));
+    const float2 fb = ue4m3x2_to_float2((uint16_t)(swb >> (16 * jj)));
 #pragma unroll
     for (int t = 0; t < kQbTok; ++t) {
       if (t >= nv) break;
       const uint8_t* cp = codes + t * 256 + 32 * j;
       const uint4 q0 = lds128(cp), q1 = lds128(cp + 16);
-      const int q[8] = {(int)q0.x, (int)q0.y, (int)q0.z, (int)q0.w, (int)q1.x, (int)q1.y, (int)q1.z, (int)q1.w};
+      const int qv[8] = {(int)q0.x, (int)q0.y, (int)q0.z, (int)q0.w, (int)q1.x, (int)q1.y, (int)q1.z, (int)q1.w};
       const float ad = *reinterpret_cast<const float*>(recs + t * REC_PITCH + 8 * j);
       int a0, a1, b0, b1;
-      nvfp4_int_dots(pa, na, q, a0, a1);
-      nvfp4_int_dots(pb, nb, q, b0, b1);
+      nvfp4_int_dots(pa, na, qv, a0, a1);
+      nvfp4_int_dots(pb, nb, qv, b0, b1);
       acca[t] += ad * 0.5f * (fa.x * (float)a0 + fa.y * (float)a1);
       accb[t] += ad * 0.5f * (fb.x * (float)b0 + fb.y * (float)b1);
     }
@@ -311,12 +305,13 @@ __device__ __forceinline__ void qb_chunk_nvfp4(const uint8_t* ca, const uint8_t*
 
 // PHASE 0: gate_up (row a = gate row i, row b = up row I+i of a 128-pair
 // tile, K = H).  PHASE 1: down (rows a, b = output rows j, j+128 of a
-// 256-row tile, K = I).  Consumer warp w takes blocks 4h..4h+3 of each chunk
-// (h = w/4) for the 32 units 32*(w%4) .. +31 of the tile, one per lane, so
-// a warp's activation loads are broadcasts and a warp of half 0 holds 32
-// consecutive intermediate values (one q8_1 block).  At the end of a tile
-// half 1 hands its partial sums to half 0 through shared memory (two
-// mbarriers, bounded waits) and half 0 runs the epilogue.
+// 256-row tile, K = I).  Consumer warp w takes blocks 2q and 2q+1 of each
+// chunk (q = w/4, a quarter of the chunk) for the 32 units 32*(w%4) .. +31 of
+// the tile, one per lane, so a warp's activation loads are broadcasts and a
+// warp of quarter 0 holds 32 consecutive intermediate values (one q8_1
+// block).  At the end of a tile quarters 1..3 hand their partial sums to
+// quarter 0 through shared memory (two mbarriers, bounded waits), which adds
+// them in quarter order and runs the epilogue.
 template <int PHASE, int WT>
 __global__ void __launch_bounds__(kQbThreads, 1) k_qb_gemm(const __grid_constant__ QbParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -339,8 +334,8 @@ __global__ void __launch_bounds__(kQbThreads, 1) k_qb_gemm(const __grid_constant
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], kQbConsumers);
     }
-    mbar_init(&xfull_bar, kQbConsumers / 2);
-    mbar_init(&xfree_bar, kQbConsumers / 2);
+    mbar_init(&xfull_bar, kQbConsumers - 128);   // quarters 1..3
+    mbar_init(&xfree_bar, 128);                  // quarter 0
     fence_mbar_init();
     prefetch_map(PHASE == 0 ? &p.map_wgu : &p.map_wdn);
     if (WT == W_NVFP4) prefetch_map(PHASE == 0 ? &p.map_wgus : &p.map_wdns);
@@ -442,8 +437,8 @@ __global__ void __launch_bounds__(kQbThreads, 1) k_qb_gemm(const __grid_constant
   }
 
   // ---------------- consumers: follow the producer's stages
-  const int u = 32 * (warp & 3) + lane, h = warp >> 2;
-  float2* xch = reinterpret_cast<float2*>(base + (size_t)kQbStages * kQbStageBytes);   // [kQbTok][128]
+  const int u = 32 * (warp & 3) + lane, q = warp >> 2;
+  float2* xch = reinterpret_cast<float2*>(base + (size_t)kQbStages * kQbStageBytes);   // [3][kQbTok][128]
   float acca[kQbTok], accb[kQbTok];
   bool ok = true;
   uint32_t ntile = 0;
@@ -462,24 +457,25 @@ __global__ void __launch_bounds__(kQbThreads, 1) k_qb_gemm(const __grid_constant
     }
     const uint8_t* st = base + s * kQbStageBytes;
     if (WT == W_Q4_K)
-      qb_chunk<PHASE == 0 ? 128 : 64>(st + u * kQbSb, st + (128 + u) * kQbSb, st + kQbCodesOff, st + kQbRecOff, h,
+      qb_chunk<PHASE == 0 ? 128 : 64>(st + u * kQbSb, st + (128 + u) * kQbSb, st + kQbCodesOff, st + kQbRecOff, q,
                                       nv, acca, accb);
     else
       qb_chunk_nvfp4<PHASE == 0 ? 128 : 64>(st, st + 16384, st + 32768, st + 34816, u, st + kQbCodesOff,
-                                            st + kQbRecOff, h, nv, acca, accb);
+                                            st + kQbRecOff, q, nv, acca, accb);
     mbar_arrive(&empty_bar[s]);
     if (kc != nK - 1) continue;
-    // ---- the tile is complete: half 1 hands over, half 0 finishes
+    // ---- the tile is complete: quarters 1..3 hand over, quarter 0 finishes
     const uint32_t n = ntile++;
-    if (h == 1) {
+    if (q != 0) {
       if (n >= 1 && !qb_wait(&xfree_bar, (n - 1) & 1u, abort)) {
         ok = false;
         break;
       }
+      float2* xq = xch + (q - 1) * kQbTok * 128;
 #pragma unroll
       for (int k = 0; k < kQbTok; ++k) {
         if (k >= nv) break;
-        xch[k * 128 + u] = make_float2(acca[k], accb[k]);
+        xq[k * 128 + u] = make_float2(acca[k], accb[k]);
       }
       mbar_arrive(&xfull_bar);
       continue;
@@ -491,9 +487,12 @@ __global__ void __launch_bounds__(kQbThreads, 1) k_qb_gemm(const __grid_constant
 #pragma unroll
     for (int k = 0; k < kQbTok; ++k) {
       if (k >= nv) break;
-      const float2 o = xch[k * 128 + u];
-      acca[k] += o.x;
-      accb[k] += o.y;
+#pragma unroll
+      for (int qq = 0; qq < 3; ++qq) {
+        const float2 o = xch[(qq * kQbTok + k) * 128 + u];
+        acca[k] += o.x;
+        accb[k] += o.y;
+      }
     }
     mbar_arrive(&xfree_bar);
     const int e = m.e;
@@ -540,7 +539,7 @@ __global__ void __launch_bounds__(kQbThreads, 1) k_qb_gemm(const __grid_constant
   if (!ok) atomicOr(p.err, kErrTimeout);
 }
 
-size_t qb_gemm_smem() { return 1024 + (size_t)kQbStages * kQbStageBytes + (size_t)kQbTok * 128 * sizeof(float2); }
+size_t qb_gemm_smem() { return 1024 + (size_t)kQbStages * kQbStageBytes + 3 * (size_t)kQbTok * 128 * sizeof(float2); }
 
 template <typename Kern>
 cudaError_t launch_qb(Kern kernel, int grid, int threads, size_t smem, cudaStream_t stream, const QbParams& p) {
