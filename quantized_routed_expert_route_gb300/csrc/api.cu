@@ -147,7 +147,7 @@ struct WsLayout {
   int cnt_len;
   size_t d_off, d_perm, d_y;               // grouped paths: routes sorted by expert, per-route down output
   size_t d_xs, d_ih;                       // dense path: gathered x, intermediate hi + lo
-  size_t q_sched, q_eord, q_xr, q_iq, q_is; // Q4_K path: tile counters, expert order, x block records, sorted intermediate
+  size_t q_sched, q_xr, q_iq, q_is;        // batched path: tile counters, x block records, sorted intermediate
   int RTp;
 };
 
@@ -171,7 +171,7 @@ WsLayout ws_layout(const moe_layer_geom& g, int T) {
   L.cnt_len = (int)(S * (g.I / 32));
   L.cnt = o; o = align_up(o + 4 * (size_t)L.cnt_len, A);
   L.RTp = (int)((RT + 31) / 32 * 32);
-  L.d_off = L.d_perm = L.d_y = L.d_xs = L.d_ih = L.q_sched = L.q_eord = L.q_xr = L.q_iq = L.q_is = 0;
+  L.d_off = L.d_perm = L.d_y = L.d_xs = L.d_ih = L.q_sched = L.q_xr = L.q_iq = L.q_is = 0;
   const int gk = grouped_kind(g);
   if (gk != kGroupedNone) {
     L.d_off = o; o = align_up(o + 4 * ((size_t)g.E + 1), A);
@@ -183,7 +183,6 @@ WsLayout ws_layout(const moe_layer_geom& g, int T) {
     L.d_ih = o; o = align_up(o + 2 * 2 * (size_t)L.RTp * g.I, A);
   } else if (gk == kGroupedQuant) {
     L.q_sched = o; o = align_up(o + 4 * 4, A);
-    L.q_eord = o; o = align_up(o + 4 * (size_t)g.E, A);
     L.q_xr = o; o = align_up(o + (size_t)T * (g.H / 4), A);
     L.q_iq = o; o = align_up(o + (size_t)L.RTp * g.I, A);
     L.q_is = o; o = align_up(o + (size_t)L.RTp * (g.I / 4), A);
@@ -495,10 +494,7 @@ static bool qbatch_params(const moe_bank* b, const WsLayout& L, uint8_t* ws, con
   q.scales = b->scales;
   q.x = p.x; q.ids = p.ids; q.w = p.w; q.out = p.out;
   q.err = p.err;
-  q.off = reinterpret_cast<int*>(ws + L.d_off);
-  q.perm = reinterpret_cast<int*>(ws + L.d_perm);
   q.sched = reinterpret_cast<unsigned*>(ws + L.q_sched);
-  q.eorder = reinterpret_cast<int*>(ws + L.q_eord);
   q.xrec = ws + L.q_xr;
   q.iqs = reinterpret_cast<int8_t*>(ws + L.q_iq);
   q.iss = ws + L.q_is;

@@ -12,29 +12,30 @@
 // weight row is decoded once and dotted with every routed token of its
 // expert.  Four launches chained with programmatic dependent launch:
 //
-//   k_qb_route   CTA 0 sorts the routes by expert (stable), publishes the
-//                offsets, the permutation and the routed experts ordered by
-//                route count (most first), and resets the tile counters; the
-//                other CTAs quantize every token's x to q8_1 once (codes and
-//                8-byte block records).
-//   k_qb_gemm<0> gate_up + prep_inter.  A tile is (expert, 128 intermediate
-//                columns, <= 8 routed tokens); tiles come from a global counter,
-//                heaviest experts first.  Per 256-value K chunk one stage
-//                holds the chunk's 144-byte super-block of the 128 gate rows
-//                and of the 128 up rows (2-D TMA, rows 144 bytes apart:
-//                conflict-free 16-byte loads) and each token's q8_1 codes and
-//                records (one TMA row per token).  A thread owns a (gate, up)
-//                pair and half of each chunk's eight blocks: it decodes the
-//                chunk's scales once, each 32-byte nibble run once for its two
-//                blocks, and accumulates the block dots with every token
-//                (activation loads are shared-memory broadcasts).  The two
-//                halves of a pair meet in shared memory; the epilogue applies
-//                s_gate / s_up and SiLU-GLU in fp32 and requantizes each
-//                warp's 32 intermediate values to q8_1 (sorted rows for the
-//                down kernel, and by route).
-//   k_qb_gemm<1> down.  A tile is (expert, 256 output rows, <= 8 tokens), a
-//                thread owns rows j and j+128; the epilogue scales by s_down *
-//                routing weight and stores fp32 per route.
+//   k_qb_route   quantizes every token's x to q8_1 once (codes and 8-byte
+//                block records) and resets the tile counters.
+//   k_qb_gemm<0> gate_up + prep_inter.  Every CTA first sorts the routes by
+//                expert (stable) and orders the routed experts by route count
+//                in shared memory, from the ids, before it waits on the route
+//                kernel.  A tile is (expert, 128 intermediate columns, <= 8
+//                routed tokens); tiles come from a global counter, heaviest
+//                experts first.  Per 256-value K chunk one stage holds the
+//                chunk's 144-byte super-block of the 128 gate rows and of the
+//                128 up rows (2-D TMA, rows 144 bytes apart: conflict-free
+//                16-byte loads) and each token's q8_1 codes and records (one
+//                TMA row per token).  A thread owns a (gate, up) pair and a
+//                quarter of each chunk's eight blocks: it decodes the chunk's
+//                scales once, the 32-byte nibble run of its two blocks once,
+//                and accumulates the block dots with every token (activation
+//                loads are shared-memory broadcasts).  The quarters of a pair
+//                meet in shared memory; the epilogue applies s_gate / s_up and
+//                SiLU-GLU in fp32 and requantizes each warp's 32 intermediate
+//                values to q8_1 (sorted rows for the down kernel, and by
+//                route).
+//   k_qb_gemm<1> down (the same prologue).  A tile is (expert, 256 output
+//                rows, <= 8 tokens), a thread owns rows j and j+128; the
+//                epilogue scales by s_down * routing weight and stores fp32
+//                per route.
 //   k_qb_combine out[t] = bf16(sum over k = 0..K-1 of the route rows), in
 //                route order, no atomics.
 //
@@ -122,50 +123,16 @@ __device__ __forceinline__ void quantize_x_block(const uint16_t* xrow, int b, ui
 // ------------------------------------------------------------------ routes and activations
 
 __global__ void __launch_bounds__(kQbRouteThreads) k_qb_route(const __grid_constant__ QbParams p) {
-  extern __shared__ int rsm[];
   pdl_wait();   // x and ids may come from the previous grid
   pdl_launch_dependents();
   const int tid = threadIdx.x;
-  if (blockIdx.x == 0) {
-    // the routes sorted by expert, and the routed experts by route count
-    const int E = p.E, RT = p.RT;
-    int* cnt = rsm;                                    // [16][E]
-    int* base = cnt + (kQbRouteThreads / 32) * E;      // [E]
-    int* wsum = base + E;                              // [33]
-    int* off = wsum + 33;                              // [E+1]
-    int* perm = off + E + 1;                           // [RT]
-    int* cm = perm + RT;                               // [RT+1]: experts per route count, then positions
-    const bool bad = sort_routes_block(p.ids, RT, E, cnt, base, wsum, off, perm);
-    const int NV = off[E];
-    for (int e = tid; e <= E; e += kQbRouteThreads) p.off[e] = off[e];
-    for (int s = tid; s < NV; s += kQbRouteThreads) p.perm[s] = perm[s];
-    if (bad && (tid & 31) == 0) atomicOr(p.err, kErrBadId);
-    // most routes first: cm[i] counts the experts with RT - i routes, its
-    // exclusive scan gives each count's first position
-    for (int i = tid; i <= RT; i += kQbRouteThreads) cm[i] = 0;
-    __syncthreads();
-    for (int e = tid; e < E; e += kQbRouteThreads) {
-      const int M = off[e + 1] - off[e];
-      if (M > 0) atomicAdd(&cm[RT - M], 1);
-    }
-    __syncthreads();
-    const int U = block_exclusive_scan(cm, RT + 1, wsum);
-    for (int e = tid; e < E; e += kQbRouteThreads) {
-      const int M = off[e + 1] - off[e];
-      if (M > 0) p.eorder[atomicAdd(&cm[RT - M], 1)] = e;
-    }
-    if (tid == 0) {
-      p.sched[0] = 0u;
-      p.sched[1] = 0u;
-      p.sched[2] = (unsigned)U;
-    }
-    if (gridDim.x > 1) return;
+  if (blockIdx.x == 0 && tid == 0) {
+    p.sched[0] = 0u;   // the tile counters of the two grouped kernels
+    p.sched[1] = 0u;
   }
-  // every token's q8_1, once (by the other CTAs): codes, records, and the
-  // planes left for inspection
+  // every token's q8_1, once: codes, records, and the planes left for inspection
   const int nbh = p.H / 32;
-  const int c0 = gridDim.x > 1 ? 1 : 0, nc = gridDim.x > 1 ? gridDim.x - 1 : 1;
-  for (int t = blockIdx.x - c0; t < p.T; t += nc) {
+  for (int t = blockIdx.x; t < p.T; t += gridDim.x) {
     const uint16_t* xrow = p.x + (size_t)t * p.H;
     for (int b = tid; b < nbh; b += kQbRouteThreads) {
       uint32_t qw[8];
@@ -182,10 +149,6 @@ __global__ void __launch_bounds__(kQbRouteThreads) k_qb_route(const __grid_const
       p.xsh[t * nbh + b] = sh;
     }
   }
-}
-
-size_t qb_route_smem(int E, int RT) {
-  return sizeof(int) * ((size_t)(kQbRouteThreads / 32) * E + E + 33 + (E + 1) + RT + (RT + 1));
 }
 
 __global__ void k_qb_combine(const __grid_constant__ QbParams p) {
@@ -320,6 +283,7 @@ __global__ void __launch_bounds__(kQbThreads, 1) k_qb_gemm(const __grid_constant
   __shared__ int tile_pre[kMaxE + 1];
   __shared__ int offs[kMaxE + 1];
   __shared__ int eord[kMaxE];
+  __shared__ int perm_s[kMaxTopK * kTChunk];   // route index of each sorted row
   __shared__ int wsum[33];
   __shared__ volatile int abort_flag;
   uint8_t* base = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);   // swizzled tiles need 1024
@@ -342,23 +306,57 @@ __global__ void __launch_bounds__(kQbThreads, 1) k_qb_gemm(const __grid_constant
     prefetch_map(PHASE == 0 ? &p.map_xq : &p.map_iq);
     prefetch_map(PHASE == 0 ? &p.map_xr : &p.map_is);
   }
-  pdl_wait();   // PHASE 0: routes sorted and x quantized; PHASE 1: the intermediate requantized
-  const int U = (int)__ldcg(p.sched + 2);
-  for (int e = tid; e <= E; e += kQbThreads) offs[e] = __ldcg(p.off + e);
-  for (int i = tid; i < U; i += kQbThreads) eord[i] = __ldcg(p.eorder + i);
-  __syncthreads();
-  for (int i = tid; i < U; i += kQbThreads) {
-    const int e = eord[i];
-    tile_pre[i] = ((offs[e + 1] - offs[e] + kQbTok - 1) / kQbTok) * NB;
+  // The routes sorted by expert (stable) and the routed experts ordered by
+  // route count (most first, then by id), computed by every CTA from the ids
+  // before waiting on the previous grid: the ids were complete before the
+  // route kernel let this grid launch (it waits first, then lets dependents
+  // launch).  The scratch lives in the stage ring, which no copy has touched.
+  int U, total;
+  {
+    const int RT = p.RT;
+    int* cnt = reinterpret_cast<int*>(base);        // [warps][E]
+    int* bse = cnt + (kQbThreads / 32) * E;          // [E]
+    int* cm = bse + E;                               // [RT+1]: experts per route count, then positions
+    const bool bad = sort_routes_block(p.ids, RT, E, cnt, bse, wsum, offs, perm_s);
+    if (PHASE == 0 && blockIdx.x == 0 && bad && lane == 0) atomicOr(p.err, kErrBadId);
+    for (int i = tid; i <= RT; i += kQbThreads) cm[i] = 0;
+    __syncthreads();
+    for (int e = tid; e < E; e += kQbThreads) {
+      const int M = offs[e + 1] - offs[e];
+      if (M > 0) atomicAdd(&cm[RT - M], 1);
+    }
+    __syncthreads();
+    U = block_exclusive_scan(cm, RT + 1, wsum);
+    if (warp == 0) {
+      // experts in id order, each placed after the earlier ones of its count
+      for (int e0 = 0; e0 < E; e0 += 32) {
+        const int e = e0 + lane;
+        const int M = (e < E) ? offs[e + 1] - offs[e] : 0;
+        const bool v = M > 0;
+        const unsigned peers = __match_any_sync(0xffffffffu, v ? M : -1 - lane);
+        const int rank = __popc(peers & ((1u << lane) - 1u));
+        if (v) eord[cm[RT - M] + rank] = e;
+        __syncwarp();
+        if (v && rank == 0) cm[RT - M] += __popc(peers);
+        __syncwarp();
+      }
+    }
+    __syncthreads();
+    for (int i = tid; i < U; i += kQbThreads) {
+      const int e = eord[i];
+      tile_pre[i] = ((offs[e + 1] - offs[e] + kQbTok - 1) / kQbTok) * NB;
+    }
+    __syncthreads();
+    total = block_exclusive_scan(tile_pre, U, wsum);   // ends with a block barrier
   }
-  __syncthreads();
-  const int total = block_exclusive_scan(tile_pre, U, wsum);   // ends with a block barrier
+  pdl_wait();   // PHASE 0: x quantized, counters reset; PHASE 1: the intermediate requantized
   pdl_launch_dependents();
   volatile int* abort = &abort_flag;
 
   if (warp == kQbConsumers / 32) {
     // ---------------- TMA producer: tiles from the global counter, most routes first
     if (lane == 0) {
+      fence_proxy_async_smem();   // the prologue's scratch writes come before the copies into the ring
       const uint64_t pol = l2_policy_evict_first();   // weight rows: read once
       uint32_t g = 0;
       bool ok = true;
@@ -388,7 +386,7 @@ __global__ void __launch_bounds__(kQbThreads, 1) k_qb_gemm(const __grid_constant
         const int srow0 = offs[e] + (tl / NB) * kQbTok;
         const int nv = min(kQbTok, offs[e + 1] - srow0);
         if (PHASE == 0)
-          for (int i = 0; i < nv; ++i) tok[i] = __ldcg(p.perm + srow0 + i) / p.K;
+          for (int i = 0; i < nv; ++i) tok[i] = perm_s[srow0 + i] / p.K;
         for (int kc = 0; kc < nK; ++kc, ++g) {
           const uint32_t s = g % kQbStages, u = g / kQbStages;
           if (u >= 1 && !qb_wait(&empty_bar[s], (u - 1) & 1u, abort)) {
@@ -506,7 +504,7 @@ __global__ void __launch_bounds__(kQbThreads, 1) k_qb_gemm(const __grid_constant
       for (int k = 0; k < kQbTok; ++k) {
         if (k >= nv) break;
         const int srow = m.srow0 + k;
-        const int r = __ldcg(p.perm + srow);
+        const int r = perm_s[srow];
         const float a = silu_glu(acca[k] * sg, accb[k] * su);
         float d;
         int sum;
@@ -529,7 +527,7 @@ __global__ void __launch_bounds__(kQbThreads, 1) k_qb_gemm(const __grid_constant
 #pragma unroll
       for (int k = 0; k < kQbTok; ++k) {
         if (k >= nv) break;
-        const int r = __ldcg(p.perm + m.srow0 + k);
+        const int r = perm_s[m.srow0 + k];
         const float f = sd * __ldg(p.w + r);
         p.y[(size_t)r * p.H + j] = acca[k] * f;
         p.y[(size_t)r * p.H + j + 128] = accb[k] * f;
@@ -563,7 +561,7 @@ cudaError_t launch_qb(Kern kernel, int grid, int threads, size_t smem, cudaStrea
 cudaError_t launch_qbatch(const QbParams& p, cudaStream_t stream) {
   const int G = sm_count();
   cudaError_t e;
-  if ((e = launch_qb(k_qb_route, G, kQbRouteThreads, qb_route_smem(p.E, p.RT), stream, p)) != cudaSuccess) return e;
+  if ((e = launch_qb(k_qb_route, G, kQbRouteThreads, 0, stream, p)) != cudaSuccess) return e;
   if (p.wt == W_NVFP4) {
     if ((e = launch_qb(k_qb_gemm<0, W_NVFP4>, G, kQbThreads, qb_gemm_smem(), stream, p)) != cudaSuccess) return e;
     if ((e = launch_qb(k_qb_gemm<1, W_NVFP4>, G, kQbThreads, qb_gemm_smem(), stream, p)) != cudaSuccess) return e;

@@ -106,8 +106,8 @@ struct DtParams {
 };
 
 // The batched path for Q4_K and NVFP4 banks (decode_qb.cu) at batches the
-// fused kernel cannot hold: routes sorted by expert, each token's x quantized
-// to q8_1 once, then two grouped CUDA-core kernels that stream one 256-value
+// fused kernel cannot hold: each token's x quantized to q8_1 once, then two
+// grouped CUDA-core kernels (each sorts the routes by expert itself) that stream one 256-value
 // K chunk of 256 weight rows per 2-D TMA stage (144 bytes a row in both
 // formats) and dot each decoded block with up to kQbTileTokens routed tokens
 // (tiles handed out heaviest expert first), and the fixed-order route sum.
@@ -132,10 +132,7 @@ struct QbParams {
   uint16_t* out;            // bf16 [T][H]
   // workspace
   uint32_t* err;
-  int* off;                 // [E+1] first sorted row of each expert; off[E] = valid routes
-  int* perm;                // [RTp] route index of each sorted row
-  unsigned* sched;          // [0], [1]: next tile of gate_up / down; [2]: routed experts U
-  int* eorder;              // [E]: the routed experts, most routes first
+  unsigned* sched;          // [0], [1]: next tile of gate_up / down
   uint8_t* xrec;            // q8_1 block records of x [T][H/32][8]
   int8_t* iqs;              // q8_1 codes of the intermediate for each sorted row [RTp][I]
   uint8_t* iss;             // block records [RTp][I/32][8]
