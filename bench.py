@@ -404,6 +404,19 @@ def profile_layer(a):
 
 # ------------------------------------------------------------------ main
 
+def job_throughput(ms_local, units_per_rank, world, device):
+    """Whole-job throughput of independent replicas: the units every rank
+    processed, over the slowest rank's time (max over ranks).  Returns
+    (units per second, max ms)."""
+    t_max = ms_local
+    if world > 1:
+        import torch
+        tt = torch.tensor([float(ms_local)], dtype=torch.float64, device=device)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        t_max = float(tt.item())
+    return units_per_rank * world / (t_max / 1e3), t_max
+
+
 def dist_setup(n):
     if int(os.environ.get("WORLD_SIZE", "1")) > 1:
         import torch
@@ -484,13 +497,8 @@ def main():
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
         ms = st.time_replays(a.steps, a.warmup)
-    t_max = ms
-    if world > 1:
-        tt = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        t_max = float(tt.item())
-    units = a.layers * 1 * world                     # layer-tokens per step, whole job
-    value = units / (t_max / 1e3)
+    value, t_max = job_throughput(ms, a.layers * 1, world, dev)   # layer-tokens per step per rank
+    units = a.layers * 1 * world                                   # whole job
     per_pass_ms = ms / a.layers
     achieved = st.bytes_per_step / a.layers / (per_pass_ms / 1e3) / 1e9
     launches = st.launches_per_step * a.steps
