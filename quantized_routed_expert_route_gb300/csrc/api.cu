@@ -312,10 +312,11 @@ DecodeParams make_params(const moe_bank* b, const WsLayout& L, uint8_t* ws, cons
   p.dn_nstage = dst < 2 ? 2 : (dst < p.dn_nstage ? dst : p.dn_nstage);
   plan_layer_small(g, T, p);
   // The grouped paths take over from the fused kernel once they are faster
-  // (measured on the Laguna-shaped layers: BF16 from 2 tokens, Q4_K from
-  // 64 routes per pass; NVFP4 takes the Q4_K rule).
+  // (measured: BF16 from 2 tokens; Q4_K from 20 routes per pass, the
+  // Laguna-shaped layer at T=2; NVFP4 between 16 and 32 routes, the
+  // Qwen3-30B-A3B-shaped layer at T=2 and T=4).
   const int RTn = T * g.top_k;
-  if ((b->grouped == kGroupedDense && T >= 2) || (b->grouped == kGroupedQuant && RTn >= 64)) p.use_ls = 0;
+  if ((b->grouped == kGroupedDense && T >= 2) || (b->grouped == kGroupedQuant && RTn >= 20)) p.use_ls = 0;
   switch (p.gu_type) {
     case W_NVFP4: p.w0 = 2; break;
     case W_Q4_K: p.w0 = 3; break;

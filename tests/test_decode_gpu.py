@@ -123,6 +123,15 @@ def test_qwen3_30b_a3b_shaped_nvfp4_layer(T):
     assert figs["err_bits"] == 0
 
 
+def test_fused_kernel_many_routes_cost_balanced_split():
+    """Q8_0 banks have no grouped path, so 64 routes per pass still take the
+    fused kernel (one launch) with its cost-balanced split of the pairs."""
+    case = cases.make_case(2048, 768, 128, 8, F.TYPE_Q8_0, F.TYPE_Q8_0, 8, seed=15)
+    figs = _check_case(case)
+    assert figs["launches"] == 1
+    assert figs["err_bits"] == 0
+
+
 @pytest.mark.parametrize("wtype", [F.TYPE_Q4_K, F.TYPE_BF16])
 def test_laguna_shaped_layer(wtype):
     """H=4096 I=768 E=256 top-10 T=1, one Q4_K layer and one BF16 layer."""
