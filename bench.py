@@ -210,25 +210,30 @@ class Stack:
     def time_e2e(self, steps, warmup):
         """End to end through the C ABI's host-buffer entry point: per step,
         every layer's moe_decode_host copies its x, ids and weights from
-        pinned host memory, decodes and copies its output back to pinned host
-        memory (48 calls captured in one CUDA graph); the step ends when the
-        host has the outputs."""
+        pinned host memory (laid out as the library's staging layout, so one
+        copy carries all three), decodes and copies its output back to pinned
+        host memory (48 calls captured in one CUDA graph); the step ends when
+        the host has the outputs."""
         torch, capi = self.torch, self.capi
         s = self.stream
-        T = self.T
-        hx = [self.x[l].cpu().view(torch.int16).pin_memory() for l in range(self.NL)]
-        hids = [L["ids"].cpu().pin_memory() for L in self.layers]
-        hw = [L["w"].cpu().pin_memory() for L in self.layers]
-        hout = [torch.empty((T, self.H), dtype=torch.int16).pin_memory() for _ in range(self.NL)]
+        T, K, H = self.T, self.K, self.H
         iob = max(capi.moe_decode_io_bytes(L["bank"], T) for L in self.layers)
+        o_ids, o_w, _ = capi.moe_decode_io_offsets(self.layers[0]["bank"], T)
+        hin = torch.zeros((self.NL, iob), dtype=torch.uint8).pin_memory()
+        for l, L in enumerate(self.layers):
+            hin[l, : 2 * T * H] = self.x[l].cpu().view(torch.uint8).reshape(-1)
+            hin[l, o_ids: o_ids + 4 * T * K] = L["ids"].cpu().view(torch.uint8).reshape(-1)
+            hin[l, o_w: o_w + 4 * T * K] = L["w"].cpu().view(torch.uint8).reshape(-1)
+        hout = [torch.empty((T, H), dtype=torch.int16).pin_memory() for _ in range(self.NL)]
         io = torch.empty((self.NL, iob), dtype=torch.uint8, device=self.dev)
-        h2d = sum(t.numel() * 2 for t in hx) + sum(t.numel() * 4 for t in hids) + sum(t.numel() * 4 for t in hw)
+        h2d = self.NL * (o_w + 4 * T * K)
         d2h = sum(t.numel() * 2 for t in hout)
 
         def launch(sp):
             for l, L in enumerate(self.layers):
-                capi.moe_decode_host(L["bank"], hx[l].data_ptr(), T, hids[l].data_ptr(), hw[l].data_ptr(),
-                                     hout[l].data_ptr(), io[l].data_ptr(), iob, self.ws.data_ptr(), self.ws_bytes, sp)
+                base = hin[l].data_ptr()
+                capi.moe_decode_host(L["bank"], base, T, base + o_ids, base + o_w, hout[l].data_ptr(), io[l].data_ptr(),
+                                     iob, self.ws.data_ptr(), self.ws_bytes, sp)
 
         s.wait_stream(torch.cuda.current_stream())
         with torch.cuda.stream(s):

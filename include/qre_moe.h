@@ -208,13 +208,20 @@ int moe_decode_kernel_count(const moe_bank* bank, int32_t T);
 /* Device staging bytes moe_decode_host needs for T tokens (0 on bad arguments). */
 size_t moe_decode_io_bytes(const moe_bank* bank, int32_t T);
 
+/* Byte offsets of topk_ids, topk_w and out in the staging layout of
+ * moe_decode_host for T tokens (x is at offset 0): offsets[0..2].  Returns
+ * MOE_EINVAL on bad arguments. */
+int moe_decode_io_offsets(const moe_bank* bank, int32_t T, size_t* offsets);
+
 /* moe_decode on host buffers: copies x (bf16 [T, H]), topk_ids (int32 [T, K])
  * and topk_w (fp32 [T, K]) from the host into `io` (device, 256-byte aligned,
  * >= moe_decode_io_bytes(bank, T) bytes), decodes, and copies the bf16
  * [T, H] result back to `out` on the host, all asynchronous on `stream`
  * (host buffers must be pinned for the copies to overlap and to be
  * capturable in a CUDA graph; the result is in `out` once the stream has
- * reached this point).  Workspace as for moe_decode. */
+ * reached this point).  When topk_ids and topk_w sit at x plus the offsets
+ * of moe_decode_io_offsets, the three inputs move in one copy.  Workspace as
+ * for moe_decode. */
 int moe_decode_host(const moe_bank* bank, const void* x, int32_t T,
                     const int32_t* topk_ids, const float* topk_w, void* out,
                     void* io, size_t io_bytes, void* ws, size_t ws_bytes, void* stream);

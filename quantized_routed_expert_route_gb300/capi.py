@@ -27,7 +27,7 @@ EXPORTS = (
     "moe_status_string", "moe_last_cuda_error", "moe_quantize_q8_1",
     "moe_debug_block_dots", "moe_debug_decode_stages", "moe_decode_noalloc", "moe_debug_tc_gemm",
     "moe_prefill_workspace_bytes", "moe_prefill_grouped", "moe_debug_prefill_stages",
-    "moe_decode_kernel_count", "moe_decode_io_bytes", "moe_decode_host",
+    "moe_decode_kernel_count", "moe_decode_io_bytes", "moe_decode_io_offsets", "moe_decode_host",
 )
 
 
@@ -72,6 +72,7 @@ def _load() -> ctypes.CDLL:
         "moe_prefill_workspace_bytes": (sz, [vp, i32, i32]),
         "moe_decode_kernel_count": (ctypes.c_int, [vp, i32]),
         "moe_decode_io_bytes": (sz, [vp, i32]),
+        "moe_decode_io_offsets": (i32, [vp, i32, vp]),
         "moe_decode_host": (ctypes.c_int, [vp, vp, i32, vp, vp, vp, vp, sz, vp, sz, vp]),
         "moe_prefill_grouped": (ctypes.c_int, [vp, vp, i32, vp, vp, i32, vp, vp, sz, vp]),
         "moe_debug_prefill_stages": (ctypes.c_int, [vp, vp, i32, vp, vp, i32, vp, vp, sz, vp, vp, vp, vp, vp]),
@@ -200,6 +201,13 @@ def moe_decode_kernel_count(bank: int, T: int) -> int:
 
 def moe_decode_io_bytes(bank: int, T: int) -> int:
     return int(_lib.moe_decode_io_bytes(bank, T))
+
+
+def moe_decode_io_offsets(bank: int, T: int) -> tuple:
+    """(ids, weights, out) byte offsets of the host-buffer staging layout; x is at 0."""
+    offs = (ctypes.c_size_t * 3)()
+    _check(_lib.moe_decode_io_offsets(bank, T, ctypes.addressof(offs)), "moe_decode_io_offsets")
+    return int(offs[0]), int(offs[1]), int(offs[2])
 
 
 def moe_decode_host(bank: int, x: int, T: int, topk_ids: int, topk_w: int, out: int, io: int, io_bytes: int, ws: int,

@@ -602,6 +602,15 @@ size_t moe_decode_io_bytes(const moe_bank* b, int32_t T) {
   return io_layout(b->geom, T).total;
 }
 
+int moe_decode_io_offsets(const moe_bank* b, int32_t T, size_t* offsets) {
+  if (!b || T < 1 || !offsets) return MOE_EINVAL;
+  const IoLayout L = io_layout(b->geom, T);
+  offsets[0] = L.ids;
+  offsets[1] = L.w;
+  offsets[2] = L.out;
+  return MOE_OK;
+}
+
 int moe_decode_host(const moe_bank* b, const void* x, int32_t T, const int32_t* ids, const float* w, void* out,
                     void* io, size_t io_bytes, void* ws, size_t ws_bytes, void* stream) {
   if (!b || T < 0) return MOE_EINVAL;
@@ -613,10 +622,16 @@ int moe_decode_host(const moe_bank* b, const void* x, int32_t T, const int32_t* 
   uint8_t* d = static_cast<uint8_t*>(io);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e;
-  if ((e = cudaMemcpyAsync(d + L.x, x, 2 * (size_t)T * g.H, cudaMemcpyHostToDevice, s)) != cudaSuccess ||
-      (e = cudaMemcpyAsync(d + L.ids, ids, 4 * (size_t)T * g.top_k, cudaMemcpyHostToDevice, s)) != cudaSuccess ||
-      (e = cudaMemcpyAsync(d + L.w, w, 4 * (size_t)T * g.top_k, cudaMemcpyHostToDevice, s)) != cudaSuccess)
+  const uint8_t* hx = static_cast<const uint8_t*>(x);
+  if (reinterpret_cast<const uint8_t*>(ids) == hx + L.ids && reinterpret_cast<const uint8_t*>(w) == hx + L.w) {
+    // the host inputs already sit in the staging layout: one copy
+    if ((e = cudaMemcpyAsync(d, x, L.w + 4 * (size_t)T * g.top_k, cudaMemcpyHostToDevice, s)) != cudaSuccess)
+      return cuda_fail(e, "decode_host: inputs to device");
+  } else if ((e = cudaMemcpyAsync(d + L.x, x, 2 * (size_t)T * g.H, cudaMemcpyHostToDevice, s)) != cudaSuccess ||
+             (e = cudaMemcpyAsync(d + L.ids, ids, 4 * (size_t)T * g.top_k, cudaMemcpyHostToDevice, s)) != cudaSuccess ||
+             (e = cudaMemcpyAsync(d + L.w, w, 4 * (size_t)T * g.top_k, cudaMemcpyHostToDevice, s)) != cudaSuccess) {
     return cuda_fail(e, "decode_host: inputs to device");
+  }
   const int st = decode_impl(b, d + L.x, T, reinterpret_cast<const int32_t*>(d + L.ids),
                              reinterpret_cast<const float*>(d + L.w), d + L.out, ws, ws_bytes, stream, nullptr);
   if (st) return st;

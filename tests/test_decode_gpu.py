@@ -250,3 +250,33 @@ def test_decode_host_buffers_equal_device_decode_and_kernel_count():
     assert capi.moe_decode_kernel_count(layer.bank, 0) == 0
     assert capi.moe_decode_kernel_count(layer.bank, 64) >= capi.moe_decode_kernel_count(layer.bank, 1)
     layer.close()
+
+
+def test_decode_host_single_staged_buffer_equals_device_decode():
+    """Host inputs laid out at moe_decode_io_offsets (one pinned buffer, one
+    copy) give the same bits as moe_decode on device buffers."""
+    case = cases.make_case(2048, 768, 128, 8, F.TYPE_NVFP4, F.TYPE_NVFP4, 3, seed=120)
+    from quantized_routed_expert_route_gb300.layer import MoeLayer
+    g = case.geom
+    layer = MoeLayer(g.H, g.I, g.E, g.top_k, g.gate_up_type, g.down_type, case.gu_dev, case.dn_dev,
+                     torch.from_numpy(case.sb).to(DEV), borrow=True)
+    x = torch.from_numpy(case.x.view(np.int16)).to(DEV).view(torch.bfloat16)
+    ids = torch.from_numpy(case.ids).to(DEV)
+    w = torch.from_numpy(case.w).to(DEV)
+    want = layer.decode(x, ids, w).clone()
+    T, K = case.x.shape[0], g.top_k
+    iob = capi.moe_decode_io_bytes(layer.bank, T)
+    o_ids, o_w, o_out = capi.moe_decode_io_offsets(layer.bank, T)
+    assert 2 * T * g.H <= o_ids and o_ids + 4 * T * K <= o_w and o_w + 4 * T * K <= o_out <= iob
+    hin = torch.zeros(iob, dtype=torch.uint8).pin_memory()
+    hin[: 2 * T * g.H] = torch.from_numpy(case.x.view(np.uint8).reshape(-1).copy())
+    hin[o_ids: o_ids + 4 * T * K] = torch.from_numpy(case.ids.view(np.uint8).reshape(-1).copy())
+    hin[o_w: o_w + 4 * T * K] = torch.from_numpy(case.w.view(np.uint8).reshape(-1).copy())
+    hout = torch.zeros((T, g.H), dtype=torch.int16).pin_memory()
+    io = torch.empty(iob, dtype=torch.uint8, device=DEV)
+    base = hin.data_ptr()
+    capi.moe_decode_host(layer.bank, base, T, base + o_ids, base + o_w, hout.data_ptr(), io.data_ptr(), iob,
+                         layer.ws.data_ptr(), layer.ws_bytes, _stream())
+    torch.cuda.synchronize()
+    assert torch.equal(hout, want.view(torch.int16).cpu())
+    layer.close()
