@@ -145,8 +145,8 @@ Shape decode_shape(const moe_layer_geom& g) {
 struct WsLayout {
   size_t err, bar, xq, xd, xsum, xsh, inter, iq, id, isum, ish, cnt, total;
   int cnt_len;
-  size_t d_off, d_perm, d_y;               // grouped paths: routes sorted by expert, per-route down output
-  size_t d_xs, d_ih;                       // dense path: gathered x, intermediate hi + lo
+  size_t d_y;                              // grouped paths: per-route down output
+  size_t d_off, d_perm, d_xs, d_ih;        // dense path: routes sorted by expert, gathered x, intermediate hi + lo
   size_t q_sched, q_xr, q_iq, q_is;        // batched path: tile counters, x block records, sorted intermediate
   int RTp;
 };
@@ -174,11 +174,11 @@ WsLayout ws_layout(const moe_layer_geom& g, int T) {
   L.d_off = L.d_perm = L.d_y = L.d_xs = L.d_ih = L.q_sched = L.q_xr = L.q_iq = L.q_is = 0;
   const int gk = grouped_kind(g);
   if (gk != kGroupedNone) {
-    L.d_off = o; o = align_up(o + 4 * ((size_t)g.E + 1), A);
-    L.d_perm = o; o = align_up(o + 4 * (size_t)L.RTp, A);
     L.d_y = o; o = align_up(o + 4 * RT * g.H, A);
   }
   if (gk == kGroupedDense) {
+    L.d_off = o; o = align_up(o + 4 * ((size_t)g.E + 1), A);
+    L.d_perm = o; o = align_up(o + 4 * (size_t)L.RTp, A);
     L.d_xs = o; o = align_up(o + 2 * (size_t)L.RTp * g.H, A);
     L.d_ih = o; o = align_up(o + 2 * 2 * (size_t)L.RTp * g.I, A);
   } else if (gk == kGroupedQuant) {
