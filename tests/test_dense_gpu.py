@@ -93,3 +93,11 @@ def test_dense_graph_replay_equals_eager():
     assert torch.equal(out.view(torch.int16), eager1.view(torch.int16))
     assert layer.error_bits() == 0
     layer.close()
+
+
+def test_more_tokens_than_one_pass():
+    """150 tokens: three passes of the dense path through one workspace."""
+    case = cases.make_case(2048, 256, 32, 4, BF, BF, 150, seed=250)
+    figs = _check_case(case, tokens=[0, 63, 64, 127, 128, 149], check_stages=False)
+    assert figs["launches"] == 3 * DENSE_LAUNCHES
+    assert figs["err_bits"] == 0

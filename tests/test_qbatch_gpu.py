@@ -108,3 +108,12 @@ def test_batched_graph_replay_equals_eager():
     assert torch.equal(out.view(torch.int16), eager1.view(torch.int16))
     assert layer.error_bits() == 0
     layer.close()
+
+
+def test_more_tokens_than_one_pass():
+    """150 tokens: three passes of the batched path through one workspace
+    (the tile counters and sorted planes are rebuilt every pass)."""
+    case = cases.make_case(2048, 512, 32, 4, Q4K, Q4K, 150, seed=360)
+    figs = _check_case(case, tokens=[0, 63, 64, 127, 128, 149], check_stages=False)
+    assert figs["launches"] == 3 * BATCHED_LAUNCHES
+    assert figs["err_bits"] == 0
