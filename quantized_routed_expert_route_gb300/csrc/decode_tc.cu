@@ -23,7 +23,7 @@
 //                 accumulation) into a gate and an up accumulator in tensor
 //                 memory; four warps apply s_gate / s_up and SiLU-GLU in fp32
 //                 and store the intermediate a, split as bf16 hi + lo.
-//   k_dt_gemm<1>  down.  A tile is (expert, 128 output rows, tokens); per K
+//   k_dt_gemm<1>  down.  A tile is (expert, 128 output rows, <= 32 tokens); per K
 //                 chunk the 128 down rows and the tokens' hi and lo rows; two
 //                 MMAs per K step (hi, then lo, into one accumulator) carry a
 //                 to ~2^-16; the epilogue scales by s_down * routing weight
@@ -32,9 +32,9 @@
 //                 route order, no atomics.
 //
 // Roles in a GEMM CTA (one CTA per SM, persistent over tiles): warp 0 lane 0
-// issues the TMA loads into a 4-deep ring of stages, warp 1 owns the tensor
-// memory and its lane 0 issues the MMAs, warps 2..5 run the epilogue from two
-// alternating accumulator buffers.  Every wait is bounded in device time; on
+// issues the TMA loads into a ring of stages (4 for gate_up, 8 for down),
+// warp 1 owns the tensor memory and its lane 0 issues the MMAs, warps 2..5
+// run the epilogue from two alternating accumulator buffers.  Every wait is bounded in device time; on
 // a timeout the CTA raises the error word, stops issuing, lets what it
 // issued finish (bounded) and frees its tensor memory.
 #include <cuda_bf16.h>
@@ -48,9 +48,22 @@ namespace {
 
 constexpr int kDtThreads = 192;                  // warp 0 TMA, warp 1 TMEM + MMA, warps 2..5 epilogue
 constexpr int kDtRows = 128;                     // weight rows per tile (the MMA's M)
-constexpr int kDtMaxN = 128;                     // tokens per tile (the MMA's N, a multiple of 16)
-constexpr int kDtStages = 4;
-constexpr int kDtStageBytes = 48 * 1024;         // gate_up: 16 KB gate + 16 KB up + <= 16 KB tokens
+// Per-phase tile shape.  gate_up: <= 128 tokens (the MMA's N), 4 stages of
+// 48 KB (16 KB gate + 16 KB up + <= 16 KB tokens).  down: a stage carries
+// only 16 KB of weights (128 rows x 64 bf16), so tiles take <= 32 tokens and
+// the ring has 8 stages of 24 KB (weights, then the hi and lo token rows):
+// 128 KB of weights in flight per SM, enough to cover DRAM latency at this
+// SM's share of the bandwidth.
+template <int PHASE>
+struct DtShape {
+  static constexpr int kMaxN = PHASE == 0 ? 128 : 32;
+  static constexpr int kStages = PHASE == 0 ? 4 : 8;
+  static constexpr int kStageBytes = PHASE == 0 ? 48 * 1024 : 24 * 1024;
+  static constexpr int kBOff = PHASE == 0 ? 32768 : 16384;     // token rows (down: the hi rows)
+  static constexpr int kLoOff = 20480;                          // down: the lo rows
+  static constexpr uint32_t kCols = PHASE == 0 ? 512 : 64;      // two accumulator buffers
+};
+constexpr int kDtMaxStages = 8;
 constexpr int kDtEpiThreads = 128;
 constexpr uint64_t kDtWaitNs = 2000000000ull;    // one wait gives up after 2 s of device time
 constexpr int kRouteThreads = 512;
@@ -141,6 +154,7 @@ struct DtTile {
   int e, rb, srow0, nv, n;   // expert, row block, first sorted row, valid tokens, MMA N (nv rounded up to 16)
 };
 
+template <int MAXN>
 __device__ __forceinline__ DtTile dt_tile(const int* tile_pre, const int* offs, int E, int NB, int t) {
   int lo = 0, hi = E;
   while (hi - lo > 1) {
@@ -152,8 +166,8 @@ __device__ __forceinline__ DtTile dt_tile(const int* tile_pre, const int* offs, 
   d.e = lo;
   const int tl = t - tile_pre[lo];
   d.rb = tl % NB;
-  d.srow0 = offs[lo] + (tl / NB) * kDtMaxN;
-  d.nv = min(kDtMaxN, offs[lo + 1] - d.srow0);
+  d.srow0 = offs[lo] + (tl / NB) * MAXN;
+  d.nv = min(MAXN, offs[lo + 1] - d.srow0);
   d.n = (d.nv + 15) & ~15;
   return d;
 }
@@ -164,13 +178,15 @@ __device__ __forceinline__ DtTile dt_tile(const int* tile_pre, const int* offs, 
 template <int PHASE>
 __global__ void __launch_bounds__(kDtThreads, 1) k_dt_gemm(const __grid_constant__ DtParams p) {
   extern __shared__ uint8_t smem_raw[];
-  __shared__ uint64_t full_bar[kDtStages], empty_bar[kDtStages], accf_bar[2], acce_bar[2], drain_bar;
+  using Sh = DtShape<PHASE>;
+  constexpr int kStages = Sh::kStages;
+  __shared__ uint64_t full_bar[kDtMaxStages], empty_bar[kDtMaxStages], accf_bar[2], acce_bar[2], drain_bar;
   __shared__ uint32_t tmem_base;
   __shared__ int tile_pre[kMaxE + 1];
   __shared__ int offs[kMaxE + 1];
   __shared__ int wsum[33];
   __shared__ volatile int abort_flag;
-  constexpr uint32_t kCols = PHASE == 0 ? 512 : 256;   // two accumulator buffers
+  constexpr uint32_t kCols = Sh::kCols;
   constexpr uint32_t kBufCols = kCols / 2;
   uint8_t* base = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -184,7 +200,7 @@ __global__ void __launch_bounds__(kDtThreads, 1) k_dt_gemm(const __grid_constant
   }
   if (tid == 0) {
     abort_flag = 0;
-    for (int s = 0; s < kDtStages; ++s) {
+    for (int s = 0; s < kStages; ++s) {
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], 1);
     }
@@ -202,7 +218,7 @@ __global__ void __launch_bounds__(kDtThreads, 1) k_dt_gemm(const __grid_constant
   __syncthreads();
   for (int e = tid; e < E; e += kDtThreads) {
     const int M = offs[e + 1] - offs[e];
-    tile_pre[e] = ((M + kDtMaxN - 1) / kDtMaxN) * NB;
+    tile_pre[e] = ((M + Sh::kMaxN - 1) / Sh::kMaxN) * NB;
   }
   __syncthreads();
   const int total = block_exclusive_scan(tile_pre, E, wsum);
@@ -220,15 +236,15 @@ __global__ void __launch_bounds__(kDtThreads, 1) k_dt_gemm(const __grid_constant
       uint32_t g = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-        const DtTile ti = dt_tile(tile_pre, offs, E, NB, t);
+        const DtTile ti = dt_tile<Sh::kMaxN>(tile_pre, offs, E, NB, t);
         const int nb16 = ti.n >> 4;
         for (int kc = 0; kc < nK; ++kc, ++g) {
-          const uint32_t s = g % kDtStages, u = g / kDtStages;
+          const uint32_t s = g % kStages, u = g / kStages;
           if (u >= 1 && !dt_wait(&empty_bar[s], (u - 1) & 1u, abort)) {
             ok = false;
             break;
           }
-          uint8_t* st = base + s * kDtStageBytes;
+          uint8_t* st = base + s * Sh::kStageBytes;
           const int x = kc * 64;
           if (PHASE == 0) {
             mbar_arrive_expect_tx(&full_bar[s], 32768u + 2048u * (uint32_t)nb16);
@@ -241,8 +257,8 @@ __global__ void __launch_bounds__(kDtThreads, 1) k_dt_gemm(const __grid_constant
             mbar_arrive_expect_tx(&full_bar[s], 16384u + 4096u * (uint32_t)nb16);
             tma_load_2d_hint(st, &p.map_dn, x, ti.e * p.H + ti.rb * kDtRows, &full_bar[s], pol);
             for (int j = 0; j < nb16; ++j) {
-              tma_load_2d(st + 16384 + 2048 * j, &p.map_ih, x, ti.srow0 + 16 * j, &full_bar[s]);
-              tma_load_2d(st + 32768 + 2048 * j, &p.map_ih, x, p.RTp + ti.srow0 + 16 * j, &full_bar[s]);
+              tma_load_2d(st + Sh::kBOff + 2048 * j, &p.map_ih, x, ti.srow0 + 16 * j, &full_bar[s]);
+              tma_load_2d(st + Sh::kLoOff + 2048 * j, &p.map_ih, x, p.RTp + ti.srow0 + 16 * j, &full_bar[s]);
             }
           }
         }
@@ -250,8 +266,8 @@ __global__ void __launch_bounds__(kDtThreads, 1) k_dt_gemm(const __grid_constant
       if (!ok) {
         atomicOr(p.err, kErrTimeout);
         // the copies already issued land before the CTA may exit (bounded)
-        for (uint32_t j = (g > (uint32_t)kDtStages ? g - kDtStages : 0u); j < g; ++j)
-          mbar_wait_spin(&full_bar[j % kDtStages], (j / kDtStages) & 1u, kDtWaitNs);
+        for (uint32_t j = (g > (uint32_t)kStages ? g - kStages : 0u); j < g; ++j)
+          mbar_wait_spin(&full_bar[j % kStages], (j / kStages) & 1u, kDtWaitNs);
       }
     }
   } else if (warp == 1) {
@@ -260,7 +276,7 @@ __global__ void __launch_bounds__(kDtThreads, 1) k_dt_gemm(const __grid_constant
       uint32_t g = 0, tcount = 0;
       bool ok = true, issued = false;
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++tcount) {
-        const DtTile ti = dt_tile(tile_pre, offs, E, NB, t);
+        const DtTile ti = dt_tile<Sh::kMaxN>(tile_pre, offs, E, NB, t);
         const uint32_t bb = tcount & 1u, v = tcount >> 1;
         if (v >= 1 && !dt_wait(&acce_bar[bb], (v - 1) & 1u, abort)) {
           ok = false;
@@ -270,13 +286,13 @@ __global__ void __launch_bounds__(kDtThreads, 1) k_dt_gemm(const __grid_constant
         const uint32_t idesc = tc::idesc_f16(kDtRows, (uint32_t)ti.n, true);
         const uint32_t d = tmem + bb * kBufCols;
         for (int kc = 0; kc < nK; ++kc, ++g) {
-          const uint32_t s = g % kDtStages, u = g / kDtStages;
+          const uint32_t s = g % kStages, u = g / kStages;
           if (!dt_wait(&full_bar[s], u & 1u, abort)) {
             ok = false;
             break;
           }
           tc::fence_after_sync();
-          const uint32_t a0 = smem_addr(base + s * kDtStageBytes);
+          const uint32_t a0 = smem_addr(base + s * Sh::kStageBytes);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             const uint32_t acc = (kc > 0 || kk > 0) ? 1u : 0u;
@@ -286,8 +302,8 @@ __global__ void __launch_bounds__(kDtThreads, 1) k_dt_gemm(const __grid_constant
               tc::mma_f16(d + 128, tc::desc_sw128(a0 + 16384 + 32 * kk), bd, idesc, acc);
             } else {
               const uint64_t ad = tc::desc_sw128(a0 + 32 * kk);
-              tc::mma_f16(d, ad, tc::desc_sw128(a0 + 16384 + 32 * kk), idesc, acc);
-              tc::mma_f16(d, ad, tc::desc_sw128(a0 + 32768 + 32 * kk), idesc, 1u);
+              tc::mma_f16(d, ad, tc::desc_sw128(a0 + Sh::kBOff + 32 * kk), idesc, acc);
+              tc::mma_f16(d, ad, tc::desc_sw128(a0 + Sh::kLoOff + 32 * kk), idesc, 1u);
             }
           }
           issued = true;
@@ -311,7 +327,7 @@ __global__ void __launch_bounds__(kDtThreads, 1) k_dt_gemm(const __grid_constant
     uint32_t tcount = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < total; t += gridDim.x, ++tcount) {
-      const DtTile ti = dt_tile(tile_pre, offs, E, NB, t);
+      const DtTile ti = dt_tile<Sh::kMaxN>(tile_pre, offs, E, NB, t);
       const uint32_t bb = tcount & 1u, v = tcount >> 1;
       if (!dt_wait(&accf_bar[bb], v & 1u, abort)) {
         ok = false;
@@ -376,7 +392,8 @@ __global__ void __launch_bounds__(kDtThreads, 1) k_dt_gemm(const __grid_constant
   if (warp == 1) tc::tmem_dealloc(tmem, kCols);
 }
 
-size_t dt_gemm_smem() { return 1024 + (size_t)kDtStages * kDtStageBytes; }
+template <int PHASE>
+size_t dt_gemm_smem() { return 1024 + (size_t)DtShape<PHASE>::kStages * DtShape<PHASE>::kStageBytes; }
 
 template <typename Kern>
 cudaError_t launch_dt(Kern kernel, int grid, int threads, size_t smem, cudaStream_t stream, const DtParams& p) {
@@ -401,8 +418,8 @@ cudaError_t launch_dense(const DtParams& p, cudaStream_t stream) {
   const int G = sm_count();
   cudaError_t e;
   if ((e = launch_dt(k_dt_route, G, kRouteThreads, dt_route_smem(p.E, p.RT), stream, p)) != cudaSuccess) return e;
-  if ((e = launch_dt(k_dt_gemm<0>, G, kDtThreads, dt_gemm_smem(), stream, p)) != cudaSuccess) return e;
-  if ((e = launch_dt(k_dt_gemm<1>, G, kDtThreads, dt_gemm_smem(), stream, p)) != cudaSuccess) return e;
+  if ((e = launch_dt(k_dt_gemm<0>, G, kDtThreads, dt_gemm_smem<0>(), stream, p)) != cudaSuccess) return e;
+  if ((e = launch_dt(k_dt_gemm<1>, G, kDtThreads, dt_gemm_smem<1>(), stream, p)) != cudaSuccess) return e;
   const long long n = (long long)p.T * (p.H / 4);
   return launch_dt(k_dt_combine, (int)((n + 255) / 256), 256, 0, stream, p);
 }
