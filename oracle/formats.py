@@ -25,11 +25,20 @@ Formats and where they come from:
     K/16 scale bytes.
   * BF16 rows -- raw little-endian bf16 (FreeToken issue #194, "Proposed
     design": BF16 rows go to a dense kernel, not MMVQ).
+  * Q6_K super-block -- 256 values in 210 bytes: ql[128] (low 4 bits of each
+    code), qh[64] (high 2 bits), scales[16] (int8, one per 16 values), fp16
+    d; value d*scale_g*(q - 32) with q the 6-bit code.  Q4_0 block -- fp16 d
+    then 16 bytes of 4-bit codes, value d*(q - 8).  Both are among the GGUF
+    types of FreeToken PR #704 ("Tests": the Q4_0 rows of the real Gemma
+    checkpoint, and Q6_K in the synthetic type list); the bit layouts are the
+    public GGUF ones, stated in prose at q6k_codes and q4_0_codes (the pages
+    give neither), so GGUF byte compatibility is unpinned.
 
 Pins (tests/test_oracle_formats.py): UE4M3 against torch's float8_e4m3fn
 decoder over all 127 finite codes; E2M1 against the same decoder through the
 E2M1-in-E4M3 embedding; fp16/bf16 via numpy bit views; Q4_K unpack by an
-exhaustive single-bit invariant plus a hand-worked golden super-block; q8_1 by
+exhaustive single-bit invariant plus a hand-worked golden super-block; Q6_K and
+Q4_0 codes by the same single-bit invariant and hand-worked values; q8_1 by
 crafted vectors with hand-computed results and the round-trip bound; integer
 block dots by brute force over Python ints.
 """
@@ -41,8 +50,9 @@ QK8 = 32          # q8_1 / Q8_0 block length
 QK_K = 256        # Q4_K super-block length
 NVFP4_GROUP = 16  # values per UE4M3 scale
 
-TYPE_BF16, TYPE_Q8_0, TYPE_Q4_K, TYPE_NVFP4 = 0, 1, 2, 3
-TYPE_NAMES = {TYPE_BF16: "bf16", TYPE_Q8_0: "q8_0", TYPE_Q4_K: "q4_k", TYPE_NVFP4: "nvfp4"}
+TYPE_BF16, TYPE_Q8_0, TYPE_Q4_K, TYPE_NVFP4, TYPE_Q6_K, TYPE_Q4_0 = 0, 1, 2, 3, 4, 5
+TYPE_NAMES = {TYPE_BF16: "bf16", TYPE_Q8_0: "q8_0", TYPE_Q4_K: "q4_k", TYPE_NVFP4: "nvfp4", TYPE_Q6_K: "q6_k",
+              TYPE_Q4_0: "q4_0"}
 
 Q8_1_BLOCK_BYTES = 36   # fp16 d, fp16 s, 32 int8
 
@@ -59,6 +69,10 @@ def row_bytes(wtype: int, k: int) -> int:
         return (k // 256) * 144 if k % 256 == 0 else 0
     if wtype == TYPE_NVFP4:
         return k // 2 + k // 16 if k % 32 == 0 else 0
+    if wtype == TYPE_Q6_K:
+        return (k // 256) * 210 if k % 256 == 0 else 0
+    if wtype == TYPE_Q4_0:
+        return (k // 32) * 18 if k % 32 == 0 else 0
     return 0
 
 
@@ -227,6 +241,37 @@ def q4k_codes(qs128) -> np.ndarray:
     return out.reshape(out.shape[:-3] + (256,))
 
 
+def q6k_codes(sb210) -> np.ndarray:
+    """The 256 signed codes q - 32 (in [-32, 31]) of Q6_K super-blocks
+    (uint8 [..., 210]) in value order.  Value v = 128*n + 32*c + l (half n,
+    quarter c, lane l < 32): its low 4 bits are nibble c // 2 (low nibble
+    first) of ql byte 64*n + 32*(c % 2) + l, its high 2 bits are bits 2c and
+    2c+1 of qh byte 32*n + l."""
+    b = np.asarray(sb210, dtype=np.int64)
+    ql, qh = b[..., 0:128], b[..., 128:192]
+    out = np.zeros(b.shape[:-1] + (256,), dtype=np.int64)
+    for n in range(2):
+        for c in range(4):
+            lo = (ql[..., 64 * n + 32 * (c % 2): 64 * n + 32 * (c % 2) + 32] >> (4 * (c // 2))) & 0x0F
+            hi = (qh[..., 32 * n: 32 * n + 32] >> (2 * c)) & 3
+            out[..., 128 * n + 32 * c: 128 * n + 32 * c + 32] = (lo | (hi << 4)) - 32
+    return out
+
+
+def q6k_scales(sb210) -> np.ndarray:
+    """The 16 signed 8-bit scales of Q6_K super-blocks; scale g covers values
+    16g .. 16g+15."""
+    return np.asarray(sb210, dtype=np.uint8)[..., 192:208].view(np.int8).astype(np.int64)
+
+
+def q4_0_codes(blk18) -> np.ndarray:
+    """The 32 signed codes q - 8 (in [-8, 7]) of Q4_0 blocks (uint8 [..., 18])
+    in value order: value j < 16 is the low nibble of code byte j, value j+16
+    its high nibble."""
+    b = np.asarray(blk18, dtype=np.int64)[..., 2:18]
+    return np.concatenate([b & 0x0F, b >> 4], axis=-1) - 8
+
+
 def dequantize_rows(wtype: int, rows, k: int) -> np.ndarray:
     """Decode bank rows (uint8 [R, row_bytes(wtype, k)]) to fp64 [R, k].
 
@@ -257,6 +302,16 @@ def dequantize_rows(wtype: int, rows, k: int) -> np.ndarray:
         nib = np.stack([codes & 0x0F, codes >> 4], axis=-1).reshape(r, k)
         v = e2m1_value(nib) * np.repeat(ue4m3_value(scl), NVFP4_GROUP, axis=-1)
         return v
+    if wtype == TYPE_Q6_K:
+        sb = rows.reshape(r, k // 256, 210)
+        d = fp16_bits_to_f64(sb[..., 208:210].copy().view(np.uint16)[..., 0])
+        q = q6k_codes(sb).reshape(r, k // 256, 16, 16).astype(np.float64)
+        v = d[..., None, None] * q6k_scales(sb)[..., None] * q
+        return v.reshape(r, k)
+    if wtype == TYPE_Q4_0:
+        blk = rows.reshape(r, k // 32, 18)
+        d = fp16_bits_to_f64(blk[..., 0:2].copy().view(np.uint16)[..., 0])
+        return (q4_0_codes(blk) * d[..., None]).reshape(r, k)
     raise ValueError(wtype)
 
 
@@ -270,6 +325,8 @@ def block_dots(wtype: int, rows, k: int, act_qs) -> np.ndarray:
     NVFP4: one int per 16-block, sum((2*E2M1(code)) * a_q); doubling makes
            every E2M1 magnitude an integer {0,1,2,3,4,6,8,12}.
     Q4_K:  one int per 32-sub-block, sum(q4 * a_q).
+    Q6_K:  one int per 16-value scale group, sum((q6 - 32) * a_q).
+    Q4_0:  one int per 32-block, sum((q4 - 8) * a_q).
     Returns int64 [R, nblocks]."""
     rows = np.asarray(rows, dtype=np.uint8)
     a = np.asarray(act_qs, dtype=np.int64).reshape(k)
@@ -284,5 +341,11 @@ def block_dots(wtype: int, rows, k: int, act_qs) -> np.ndarray:
         return (w2 * a).reshape(r, k // 16, 16).sum(axis=-1)
     if wtype == TYPE_Q4_K:
         q = q4k_codes(rows.reshape(r, k // 256, 144)[..., 16:144]).reshape(r, k)
+        return (q * a).reshape(r, k // 32, 32).sum(axis=-1)
+    if wtype == TYPE_Q6_K:
+        q = q6k_codes(rows.reshape(r, k // 256, 210)).reshape(r, k)
+        return (q * a).reshape(r, k // 16, 16).sum(axis=-1)
+    if wtype == TYPE_Q4_0:
+        q = q4_0_codes(rows.reshape(r, k // 32, 18)).reshape(r, k)
         return (q * a).reshape(r, k // 32, 32).sum(axis=-1)
     raise ValueError(wtype)

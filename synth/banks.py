@@ -19,7 +19,7 @@ from __future__ import annotations
 
 import numpy as np
 
-BF16, Q8_0, Q4_K, NVFP4 = 0, 1, 2, 3
+BF16, Q8_0, Q4_K, NVFP4, Q6_K, Q4_0 = 0, 1, 2, 3, 4, 5
 
 
 def rng(seed: int) -> np.random.Generator:
@@ -27,7 +27,8 @@ def rng(seed: int) -> np.random.Generator:
 
 
 def row_bytes(wtype: int, k: int) -> int:
-    return {BF16: 2 * k, Q8_0: k // 32 * 34, Q4_K: k // 256 * 144, NVFP4: k // 2 + k // 16}[wtype]
+    return {BF16: 2 * k, Q8_0: k // 32 * 34, Q4_K: k // 256 * 144, NVFP4: k // 2 + k // 16,
+            Q6_K: k // 256 * 210, Q4_0: k // 32 * 18}[wtype]
 
 
 # ------------------------------------------------------------------ activations / routing
@@ -147,6 +148,55 @@ def convert_q4k(w: np.ndarray) -> np.ndarray:
     return out.reshape(R, nsb * 144)
 
 
+def convert_q6k(w: np.ndarray) -> np.ndarray:
+    """Q6_K rows from fp32 [R, K] by a plain absmax encoder: per 16 values
+    step = amax / 31; per super-block d = max(step) / 127 (fp16); int8 scale
+    round(step / d); codes round(w / (d * scale)) + 32 clipped to 0..63, packed
+    into ql (low 4 bits) and qh (high 2 bits) in the GGUF order (value
+    128n + 32c + l: nibble c // 2 of ql[64n + 32(c % 2) + l], bits 2c..2c+1 of
+    qh[32n + l])."""
+    R, K = w.shape
+    nsb = K // 256
+    x = w.astype(np.float64).reshape(R, nsb, 16, 16)
+    step = np.abs(x).max(axis=-1) / 31.0
+    d = (step.max(axis=-1) / 127.0).astype(np.float16)
+    d64 = d.astype(np.float64)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        sc = np.where(d64[..., None] > 0, np.rint(step / d64[..., None]), 0).clip(-128, 127).astype(np.int64)
+        eff = d64[..., None] * sc
+        q = np.where(eff[..., None] != 0, np.rint(x / np.where(eff != 0, eff, 1)[..., None]), 0)
+    q = (q + 32).clip(0, 63).astype(np.int64).reshape(R, nsb, 256)
+    out = np.zeros((R, nsb, 210), dtype=np.uint8)
+    for n in range(2):
+        for c in range(4):
+            v = q[..., 128 * n + 32 * c: 128 * n + 32 * c + 32]
+            lo, hi = v & 0x0F, v >> 4
+            o = 64 * n + 32 * (c % 2)
+            out[..., o: o + 32] |= (lo << (4 * (c // 2))).astype(np.uint8)
+            out[..., 128 + 32 * n: 128 + 32 * n + 32] |= (hi << (2 * c)).astype(np.uint8)
+    out[..., 192:208] = sc.astype(np.int8).view(np.uint8)
+    out[..., 208:210] = d.view(np.uint16)[..., None].view(np.uint8).reshape(R, nsb, 2)
+    return out.reshape(R, nsb * 210)
+
+
+def convert_q4_0(w: np.ndarray) -> np.ndarray:
+    """Q4_0 rows from fp32 [R, K]: per 32 values d = amax / 7 (fp16), codes
+    round(w / d) + 8 clipped to 0..15; value j < 16 in the low nibble of code
+    byte j, value j + 16 in its high nibble."""
+    R, K = w.shape
+    nb = K // 32
+    x = w.astype(np.float64).reshape(R, nb, 32)
+    d = (np.abs(x).max(axis=-1) / 7.0).astype(np.float16)
+    d64 = d.astype(np.float64)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        q = np.where(d64[..., None] > 0, np.rint(x / np.where(d64 > 0, d64, 1)[..., None]), 0)
+    q = (q + 8).clip(0, 15).astype(np.uint8)
+    out = np.zeros((R, nb, 18), dtype=np.uint8)
+    out[..., 0:2] = d.view(np.uint16)[..., None].view(np.uint8).reshape(R, nb, 2)
+    out[..., 2:18] = q[..., :16] | (q[..., 16:] << 4)
+    return out.reshape(R, nb * 18)
+
+
 def q8_0_codes_bank(seed: int, rows: int, k: int) -> np.ndarray:
     """Q8_0 rows with int8 codes uniform in [-127, 127] and fp16 scales
     uniform in (1e-4, 5e-4) (the tiny single-layer configuration)."""
@@ -179,6 +229,10 @@ def converted_expert(seed: int, e: int, H: int, I: int, gate_up_type: int, down_
             gu = np.concatenate(parts, axis=0)
         elif gate_up_type == Q4_K:
             gu = convert_q4k(wg)
+        elif gate_up_type == Q6_K:
+            gu = convert_q6k(wg)
+        elif gate_up_type == Q4_0:
+            gu = convert_q4_0(wg)
         else:
             gu = convert_bf16(wg)
     if down_type == Q8_0:
@@ -191,6 +245,10 @@ def converted_expert(seed: int, e: int, H: int, I: int, gate_up_type: int, down_
             dn = convert_nvfp4(wd, s2)
         elif down_type == Q4_K:
             dn = convert_q4k(wd)
+        elif down_type == Q6_K:
+            dn = convert_q6k(wd)
+        elif down_type == Q4_0:
+            dn = convert_q4_0(wd)
         else:
             dn = convert_bf16(wd)
     return gu, dn, sc

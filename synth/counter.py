@@ -16,6 +16,9 @@ row only, keeps scale fields finite and of a realistic size:
         dmin fp16 -> exponent field 4 (2^-11 .. 2^-10); the rest unchanged.
   Q8_0 (34-byte blocks): d fp16 -> exponent field 3 (2^-12 .. 2^-11);
         code byte 0x80 (-128) -> 0x81 (-127).
+  Q6_K (210-byte super-blocks): the 16 int8 sub-block scales keep their low 5
+        bits (0 .. 31); d fp16 -> exponent field 1 (2^-14 .. 2^-13).
+  Q4_0 (18-byte blocks): d fp16 -> exponent field 3 (2^-12 .. 2^-11).
   BF16: each value keeps its sign and 7 mantissa bits; its exponent becomes
         119 + (bits 7..8 of the raw value): magnitudes 2^-8 .. 2^-4.
 
@@ -30,11 +33,12 @@ C1 = 0xBF58476D1CE4E5B9
 C2 = 0x94D049BB133111EB
 M64 = (1 << 64) - 1
 
-BF16, Q8_0, Q4_K, NVFP4 = 0, 1, 2, 3
+BF16, Q8_0, Q4_K, NVFP4, Q6_K, Q4_0 = 0, 1, 2, 3, 4, 5
 
 
 def _row_bytes(wtype: int, k: int) -> int:
-    return {BF16: 2 * k, Q8_0: k // 32 * 34, Q4_K: k // 256 * 144, NVFP4: k // 2 + k // 16}[wtype]
+    return {BF16: 2 * k, Q8_0: k // 32 * 34, Q4_K: k // 256 * 144, NVFP4: k // 2 + k // 16,
+            Q6_K: k // 256 * 210, Q4_0: k // 32 * 18}[wtype]
 
 
 # ------------------------------------------------------------------ host (numpy)
@@ -73,6 +77,13 @@ def _mask_np(rows: np.ndarray, wtype: int, k: int) -> np.ndarray:
         blk[..., 1] = 0x0C | (blk[..., 1] & 0x03)
         q = blk[..., 2:]
         q[q == 0x80] = 0x81
+    elif wtype == Q6_K:
+        sb = rows.reshape(rows.shape[0], -1, 210)
+        sb[..., 192:208] &= 0x1F
+        sb[..., 209] = 0x04 | (sb[..., 209] & 0x03)
+    elif wtype == Q4_0:
+        blk = rows.reshape(rows.shape[0], -1, 18)
+        blk[..., 1] = 0x0C | (blk[..., 1] & 0x03)
     elif wtype == BF16:
         v = rows.view(np.uint16).astype(np.uint32)
         exp = 119 + ((v >> 7) & 3)
@@ -137,6 +148,13 @@ def _mask_torch(rows, wtype: int, k: int) -> None:
         blk[..., 1] = torch.bitwise_or(torch.bitwise_and(blk[..., 1], 0x03), 0x0C)
         q = blk[..., 2:]
         q.masked_fill_(q == 0x80, 0x81)
+    elif wtype == Q6_K:
+        sb = rows.view(rows.shape[0], -1, 210)
+        sb[..., 192:208] = torch.bitwise_and(sb[..., 192:208], 0x1F)
+        sb[..., 209] = torch.bitwise_or(torch.bitwise_and(sb[..., 209], 0x03), 0x04)
+    elif wtype == Q4_0:
+        blk = rows.view(rows.shape[0], -1, 18)
+        blk[..., 1] = torch.bitwise_or(torch.bitwise_and(blk[..., 1], 0x03), 0x0C)
     elif wtype == BF16:
         v = rows.view(torch.int16).to(torch.int32) & 0xFFFF
         exp = 119 + torch.bitwise_and(torch.bitwise_right_shift(v, 7), 3)

@@ -124,6 +124,62 @@ def test_q4k_superblock_golden_values(golden_dir):
         assert v[int(idx)] == val, idx
 
 
+def test_q6k_codes_single_bit_bijection():
+    """With every code byte zero each code is -32; setting one bit of ql or qh
+    raises exactly one code by a single power of two, and the 192*8 bits cover
+    all 256*6 (value, bit) slots once."""
+    hits = set()
+    for byte in range(192):
+        for bit in range(8):
+            sb = np.zeros(210, dtype=np.uint8)
+            sb[byte] = 1 << bit
+            q = F.q6k_codes(sb) + 32
+            nz = np.nonzero(q)[0]
+            assert len(nz) == 1
+            v = int(q[nz[0]])
+            assert v & (v - 1) == 0
+            hits.add((int(nz[0]), v.bit_length() - 1))
+    assert len(hits) == 256 * 6
+
+
+def test_q6k_superblock_hand_values():
+    """Values worked by hand from the GGUF Q6_K layout (ql low 4 bits, qh high
+    2 bits, int8 scale per 16 values, fp16 d; value d*scale*(q-32))."""
+    sb = np.zeros(210, dtype=np.uint8)
+    sb[208:210] = np.array([0x3800], dtype=np.uint16).view(np.uint8)   # d = 0.5
+    sc = np.zeros(16, dtype=np.int8)
+    sc[0], sc[2], sc[4], sc[6], sc[14] = 2, -1, 7, 1, -4
+    sb[192:208] = sc.view(np.uint8)
+    sb[0] = 0x21          # ql[0]: value 0 low bits 1, value 64 low bits 2
+    sb[128] = 0x27        # qh[0]: value 0 high 3, value 32 high 1, value 64 high 2, value 96 high 0
+    sb[64 + 32 + 5] = 0xF0  # ql[101]: value 229 low bits 15 (high nibble), value 165 low bits 0
+    sb[128 + 32 + 5] = 0xC0  # qh[37]: value 229 high bits 3
+    v = F.dequantize_rows(F.TYPE_Q6_K, sb[None, :], 256)[0]
+    want = {0: 0.5 * 2 * (49 - 32), 32: 0.5 * -1 * (16 - 32), 64: 0.5 * 7 * (34 - 32), 96: 0.5 * 1 * -32,
+            1: 0.5 * 2 * -32, 128: 0.0, 229: 0.5 * -4 * (63 - 32), 165: 0.0}
+    for idx, val in want.items():
+        assert v[idx] == val, (idx, v[idx], val)
+    assert (17.0, 8.0, 7.0, -16.0, -32.0, -62.0) == (v[0], v[32], v[64], v[96], v[1], v[229])
+
+
+def test_q4_0_codes_single_bit_and_hand_values():
+    hits = set()
+    for byte in range(2, 18):
+        for bit in range(8):
+            blk = np.zeros(18, dtype=np.uint8)
+            blk[byte] = 1 << bit
+            q = F.q4_0_codes(blk) + 8
+            nz = np.nonzero(q)[0]
+            assert len(nz) == 1 and (int(q[nz[0]]) & (int(q[nz[0]]) - 1)) == 0
+            hits.add((int(nz[0]), int(q[nz[0]]).bit_length() - 1))
+    assert len(hits) == 32 * 4
+    blk = np.zeros(18, dtype=np.uint8)
+    blk[0:2] = np.array([0x3400], dtype=np.uint16).view(np.uint8)   # d = 0.25
+    blk[2] = 0x9F         # value 0: 15 - 8 = 7, value 16: 9 - 8 = 1
+    v = F.dequantize_rows(F.TYPE_Q4_0, blk[None, :], 32)[0]
+    assert (v[0], v[16], v[3], v[19]) == (1.75, 0.25, -2.0, -2.0)
+
+
 # ---------------------------------------------------------------- q8_1
 
 def _fp32_round(fr: Fraction) -> Fraction:
@@ -198,7 +254,8 @@ def test_q8_1_round_trip_bound():
 _E2M1_X2 = {0: 0, 1: 1, 2: 2, 3: 3, 4: 4, 5: 6, 6: 8, 7: 12}
 
 
-@pytest.mark.parametrize("wtype,k", [(F.TYPE_Q8_0, 96), (F.TYPE_NVFP4, 128), (F.TYPE_Q4_K, 512)])
+@pytest.mark.parametrize("wtype,k", [(F.TYPE_Q8_0, 96), (F.TYPE_NVFP4, 128), (F.TYPE_Q4_K, 512),
+                                     (F.TYPE_Q6_K, 512), (F.TYPE_Q4_0, 96)])
 def test_block_dots_brute_force(wtype, k):
     r = np.random.default_rng(5 + wtype)
     rb = F.row_bytes(wtype, k)
@@ -220,6 +277,22 @@ def test_block_dots_brute_force(wtype, k):
                     mag = _E2M1_X2[nib & 7]
                     vals.append(-mag if nib & 8 else mag)
             want = [sum(vals[b * 16 + i] * af[b * 16 + i] for i in range(16)) for b in range(k // 16)]
+        elif wtype == F.TYPE_Q6_K:
+            vals = []
+            for sbi in range(k // 256):
+                b = row[sbi * 210: sbi * 210 + 210]
+                for v in range(256):
+                    n, c, l = v // 128, (v % 128) // 32, v % 32
+                    lo = (b[64 * n + 32 * (c % 2) + l] >> (4 * (c // 2))) & 15
+                    hi = (b[128 + 32 * n + l] >> (2 * c)) & 3
+                    vals.append(lo + 16 * hi - 32)
+            want = [sum(vals[g * 16 + i] * af[g * 16 + i] for i in range(16)) for g in range(k // 16)]
+        elif wtype == F.TYPE_Q4_0:
+            want = []
+            for b in range(k // 32):
+                qs = row[b * 18 + 2: b * 18 + 18]
+                vals = [(x & 15) - 8 for x in qs] + [(x >> 4) - 8 for x in qs]
+                want.append(sum(vals[i] * af[b * 32 + i] for i in range(32)))
         else:
             want = []
             for sbi in range(k // 256):

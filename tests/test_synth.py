@@ -16,7 +16,7 @@ def test_splitmix64_known_first_outputs():
 
 
 def test_counter_bank_host_equals_torch_cpu():
-    for wtype, k in [(C.NVFP4, 256), (C.Q4_K, 512), (C.Q8_0, 256), (C.BF16, 64)]:
+    for wtype, k in [(C.NVFP4, 256), (C.Q4_K, 512), (C.Q8_0, 256), (C.BF16, 64), (C.Q6_K, 512), (C.Q4_0, 256)]:
         rb = C._row_bytes(wtype, k)
         rows = 40
         t = torch.empty(rows * rb, dtype=torch.uint8)
@@ -28,7 +28,7 @@ def test_counter_bank_host_equals_torch_cpu():
 
 
 def test_counter_banks_decode_finite():
-    for wtype, k in [(C.NVFP4, 256), (C.Q4_K, 512), (C.Q8_0, 256), (C.BF16, 64)]:
+    for wtype, k in [(C.NVFP4, 256), (C.Q4_K, 512), (C.Q8_0, 256), (C.BF16, 64), (C.Q6_K, 512), (C.Q4_0, 256)]:
         rows = C.bank_bytes_np(99, wtype, k, 0, 64)
         v = F.dequantize_rows(wtype, rows, k)
         # NVFP4 rows exclude weight_scale_2 (applied to the projection output)
@@ -54,6 +54,14 @@ def test_converted_q4k_reconstructs():
     back = F.dequantize_rows(F.TYPE_Q4_K, S.convert_q4k(w), 512)
     rel = np.linalg.norm(back - w) / np.linalg.norm(w)
     assert rel < 0.12
+
+
+def test_converted_q6k_and_q4_0_reconstruct():
+    r = np.random.default_rng(2)
+    w = (r.standard_normal((4, 512)) * 0.02).astype(np.float32)
+    for wtype, conv, tol in ((F.TYPE_Q6_K, S.convert_q6k, 0.03), (F.TYPE_Q4_0, S.convert_q4_0, 0.12)):
+        back = F.dequantize_rows(wtype, conv(w), 512)
+        assert np.linalg.norm(back - w) / np.linalg.norm(w) < tol
 
 
 def test_routings():
