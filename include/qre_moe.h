@@ -50,8 +50,23 @@ extern "C" {
  *   MOE_NVFP4: K/2 code bytes (E2M1; element 2i in the low nibble of byte i)
  *              then K/16 UE4M3 scale bytes, one per 16 values (Strata PR #292,
  *              "NVFP4 routed experts ...", Summary/Pipeline: group 16).  The
- *              per-expert weight_scale_2 lives in the scale bank, not the row. */
-typedef enum { MOE_BF16 = 0, MOE_Q8_0 = 1, MOE_Q4_K = 2, MOE_NVFP4 = 3 } moe_type;
+ *              per-expert weight_scale_2 lives in the scale bank, not the row.
+ *   MOE_Q6_K : K/256 super-blocks of 210 bytes {uint8 ql[128]; uint8 qh[64];
+ *              int8 scales[16]; fp16 d}; value v = 128n + 32c + l of a
+ *              super-block has the low nibble c/2 of ql[64n + 32(c mod 2) + l]
+ *              and bits 2c, 2c+1 of qh[32n + l] as its 6-bit code q, and the
+ *              value d*scales[v/16]*(q - 32) (GGUF Q6_K bit layout; one of the
+ *              ggml weight types FreeToken PR #704 lists, "How it plugs into
+ *              the CPU executor").
+ *   MOE_Q4_0 : K/32 blocks of {fp16 d; uint8 qs[16]} (18 bytes); value j < 16
+ *              is the low nibble of qs[j], value j+16 its high nibble, value
+ *              d*(q - 8) (GGUF Q4_0 bit layout; the CPU format of FreeToken
+ *              PR #704, "Tests").
+ * Gate_up and down may be of different types (e.g. Q4_K gate_up with Q6_K
+ * down, the pairing of a Q4_K_M checkpoint). */
+typedef enum {
+  MOE_BF16 = 0, MOE_Q8_0 = 1, MOE_Q4_K = 2, MOE_NVFP4 = 3, MOE_Q6_K = 4, MOE_Q4_0 = 5
+} moe_type;
 
 typedef enum {
   MOE_OK = 0,
@@ -251,8 +266,9 @@ int moe_quantize_q8_1(const float* x, int64_t n, void* out_blocks, void* stream)
  * row_bytes(type, k)) against q8_1 activation blocks (device, k/32 blocks of
  * 36 bytes).  out: device int32 [nrows, nb] with nb = k/16 for MOE_NVFP4 (one
  * per 16-value block, sum of (2*E2M1 code value) * q), k/32 for MOE_Q8_0 and
- * MOE_Q4_K (sum of code * q; Q4_K per 32-value sub-block).  MOE_BF16 is
- * MOE_EINVAL. */
+ * MOE_Q4_K (sum of code * q; Q4_K per 32-value sub-block), k/16 for MOE_Q6_K
+ * (sum of (code - 32) * q per 16-value scale group), k/32 for MOE_Q4_0 (sum of
+ * (code - 8) * q).  MOE_BF16 is MOE_EINVAL. */
 int moe_debug_block_dots(int32_t type, const void* rows, int32_t nrows, int32_t k,
                          const void* act_blocks, int32_t* out, void* stream);
 

@@ -661,6 +661,8 @@ cudaError_t launch_gate_up(const DecodeParams& p, cudaStream_t stream) {
       return launch_gu_w<W_NVFP4>(p, smem, stream);
     case W_Q4_K: return launch_gu_w<W_Q4_K>(p, smem, stream);
     case W_Q8_0: return launch_gu_w<W_Q8_0>(p, smem, stream);
+    case W_Q6_K: return launch_gu_w<W_Q6_K>(p, smem, stream);
+    case W_Q4_0: return launch_gu_w<W_Q4_0>(p, smem, stream);
     default: return launch_gu_w<W_BF16>(p, smem, stream);
   }
 }
@@ -685,6 +687,8 @@ cudaError_t launch_down(const DecodeParams& p, cudaStream_t stream) {
       return launch_dn_w<W_NVFP4, 8>(p, smem, stream);
     case W_Q4_K: return launch_dn_w<W_Q4_K, 8>(p, smem, stream);
     case W_Q8_0: return launch_dn_w<W_Q8_0, 8>(p, smem, stream);
+    case W_Q6_K: return launch_dn_w<W_Q6_K, 8>(p, smem, stream);
+    case W_Q4_0: return launch_dn_w<W_Q4_0, 8>(p, smem, stream);
     default: return launch_dn_w<W_BF16, 16>(p, smem, stream);
   }
 }
@@ -722,6 +726,8 @@ __device__ __forceinline__ ActQ8 act_from_block(const uint8_t* blk) {
   for (int i = 0; i < 8; ++i) a.q[i] = (int)qw[i];
   a.d = f16_bits_to_f32((uint32_t)blk[0] | ((uint32_t)blk[1] << 8));
   a.sum = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) a.sum = __dp4a(a.q[i], 0x01010101, a.sum);
   return a;
 }
 
@@ -747,6 +753,19 @@ __global__ void k_block_dots(int type, const uint8_t* rows, int nrows, int k, co
     float dsc, dmm;
     q4k_decode(row, b, nib, dsc, dmm);
     out[(size_t)r * nb + b] = int_dot8(nib, a.q);
+  } else if (type == W_Q6_K) {
+    int wq[8];
+    float d, s0, s1;
+    q6k_decode(row, b, wq, d, s0, s1);
+    int d0, d1;
+    int_dots_halves(wq, a.q, d0, d1);
+    out[(size_t)r * (k / 16) + 2 * b] = d0;
+    out[(size_t)r * (k / 16) + 2 * b + 1] = d1;
+  } else if (type == W_Q4_0) {
+    int wq[8];
+    float d;
+    q4_0_decode(row, b, wq, d);
+    out[(size_t)r * nb + b] = int_dot8(wq, a.q) - 8 * a.sum;
   } else {
     int wq[8];
     float d;

@@ -579,7 +579,28 @@ __device__ __forceinline__ void accum_q_block(const uint8_t* row, int k, int b, 
         acc[t] += a[t].d * (dsc * (float)dd - dmm * (float)a[t].sum);
       }
     }
+  } else if constexpr (WT == W_Q6_K) {
+    int wq[8];
+    float d, s0, s1;
+    q6k_decode(row, b, wq, d, s0, s1);
+#pragma unroll
+    for (int t = 0; t < NTT; ++t) {
+      if (NTT == 1 || t < nt) {
+        int d0, d1;
+        int_dots_halves(wq, a[t].q, d0, d1);
+        acc[t] += (d * a[t].d) * (s0 * (float)d0 + s1 * (float)d1);
+      }
+    }
+  } else if constexpr (WT == W_Q4_0) {
+    int wq[8];
+    float d;
+    q4_0_decode(row, b, wq, d);
+#pragma unroll
+    for (int t = 0; t < NTT; ++t) {
+      if (NTT == 1 || t < nt) acc[t] += (d * a[t].d) * (float)(int_dot8(wq, a[t].q) - 8 * a[t].sum);
+    }
   } else {  // W_Q8_0
+    static_assert(WT == W_Q8_0 || WT == W_BF16, "unhandled weight type");  // BF16: unreachable instantiations
     int wq[8];
     float d;
     q8_0_decode(row, b, wq, d);

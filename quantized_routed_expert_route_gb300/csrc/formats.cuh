@@ -16,6 +16,12 @@
 //           (sc, m) bytes, 128 code bytes; value d*sc_j*q - dmin*m_j.
 //   NVFP4 : row = K/2 E2M1 code bytes (element 2i low nibble of byte i) then
 //           K/16 UE4M3 scale bytes; value E2M1(code)*UE4M3(scale).
+//   Q6_K  : 210-byte super-block of 256: ql[128] (low 4 bits), qh[64] (high
+//           2 bits), 16 int8 scales (one per 16 values), fp16 d;
+//           value d*sc_g*(q - 32).
+//   Q4_0  : fp16 d then 16 code bytes (18 bytes per 32 values); value j < 16
+//           is the low nibble of code byte j, value j+16 its high nibble;
+//           value d*(q - 8).
 #pragma once
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -24,9 +30,9 @@
 
 namespace qre {
 
-enum WType : int { W_BF16 = 0, W_Q8_0 = 1, W_Q4_K = 2, W_NVFP4 = 3 };
+enum WType : int { W_BF16 = 0, W_Q8_0 = 1, W_Q4_K = 2, W_NVFP4 = 3, W_Q6_K = 4, W_Q4_0 = 5 };
 // Kernel-side variant of W_NVFP4 whose rows (9k/16 bytes) are not 16-byte aligned.
-constexpr int W_NVFP4_U = 4;
+constexpr int W_NVFP4_U = 16;
 
 __host__ __device__ inline int row_bytes_of(int t, int k) {
   switch (t) {
@@ -34,6 +40,8 @@ __host__ __device__ inline int row_bytes_of(int t, int k) {
     case W_Q8_0: return (k % 32 == 0) ? (k / 32) * 34 : 0;
     case W_Q4_K: return (k % 256 == 0) ? (k / 256) * 144 : 0;
     case W_NVFP4: return (k % 32 == 0) ? k / 2 + k / 16 : 0;
+    case W_Q6_K: return (k % 256 == 0) ? (k / 256) * 210 : 0;
+    case W_Q4_0: return (k % 32 == 0) ? (k / 32) * 18 : 0;
   }
   return 0;
 }
@@ -42,7 +50,7 @@ __host__ __device__ inline int row_bytes_of(int t, int k) {
 
 // A q8_1 activation block as the dot loops hold it: the 32 codes as eight
 // int8x4 words in value order, d decoded from its fp16 copy, and the exact
-// integer sum of the codes (for the Q4_K min term).
+// integer sum of the codes (for the Q4_K min and the Q4_0 offset terms).
 struct ActQ8 {
   int q[8];
   float d;
@@ -263,6 +271,79 @@ __device__ __forceinline__ void q8_0_decode(const uint8_t* row, int b, int (&w)[
   for (int i = 0; i < 8; ++i) {
     const uint32_t lo = lds16(blk + 2 + 4 * i), hi = lds16(blk + 4 + 4 * i);
     w[i] = (int)(lo | (hi << 16));
+  }
+}
+
+// ------------------------------------------------------------------ Q6_K
+
+// 32 bytes from a 2-byte aligned address inside a super-block as eight
+// words: aligned 32-bit loads, realigned with a funnel shift when the address
+// is 2 mod 4.  The extra word read then ends 2 bytes past the 32, which every
+// caller keeps inside the same super-block.
+__device__ __forceinline__ void lds_words8_a2(const uint8_t* p, uint32_t (&w)[8]) {
+  const uint32_t mis = (uint32_t)(reinterpret_cast<uintptr_t>(p) & 3u);  // 0 or 2
+  const uint8_t* a = p - mis;
+  uint32_t r[9];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) r[i] = lds32(a + 4 * i);
+  r[8] = mis ? lds32(a + 32) : 0u;
+  const uint32_t sh = 8u * mis;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) w[i] = __funnelshift_r(r[i], r[i + 1], sh);
+}
+
+// Decode sub-block b (32 values) of a Q6_K row (super-blocks 2-byte aligned):
+// the signed codes q - 32 as int8x4 words in value order, d, and the two
+// int8 scales of its 16-value halves.  Sub-block j = b mod 8 of a super-block
+// covers values 32j .. 32j+31, i.e. half n = j/4 and quarter c = j mod 4: its
+// low nibbles are nibble c/2 of ql[64n + 32(c mod 2) + l] and its high bits
+// are bits 2c, 2c+1 of qh[32n + l], l = 0..31.
+__device__ __forceinline__ void q6k_decode(const uint8_t* row, int b, int (&w)[8], float& d, float& s0, float& s1) {
+  const uint8_t* sb = row + (b >> 3) * 210;
+  const int j = b & 7, n = j >> 2, c = j & 3;
+  uint32_t lo[8], hi[8];
+  lds_words8_a2(sb + 64 * n + 32 * (c & 1), lo);
+  lds_words8_a2(sb + 128 + 32 * n, hi);
+  const int sl = 4 * (c >> 1), sh = 2 * c;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    // 6-bit code u in 0..63 per byte; u ^ 32 with bit 5 copied into bits 6, 7
+    // is u - 32 as a two's-complement byte
+    const uint32_t u = ((lo[i] >> sl) & 0x0F0F0F0Fu) | (((hi[i] >> sh) & 0x03030303u) << 4);
+    const uint32_t x = u ^ 0x20202020u, sg = x & 0x20202020u;
+    w[i] = (int)(x | (sg << 1) | (sg << 2));
+  }
+  const uint32_t scw = lds16(sb + 192 + 2 * j);
+  s0 = (float)(int8_t)(scw & 0xFFu);
+  s1 = (float)(int8_t)(scw >> 8);
+  d = f16_bits_to_f32(lds16(sb + 208));
+}
+
+// Integer dots of the two 16-value halves of a decoded Q6_K sub-block.
+__device__ __forceinline__ void int_dots_halves(const int (&w)[8], const int (&q)[8], int& d0, int& d1) {
+  int a0 = 0, a1 = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    a0 = __dp4a(w[i], q[i], a0);
+    a1 = __dp4a(w[i + 4], q[i + 4], a1);
+  }
+  d0 = a0;
+  d1 = a1;
+}
+
+// ------------------------------------------------------------------ Q4_0
+
+// Block b of a Q4_0 row (18-byte blocks, 2-byte aligned): the unsigned codes
+// q (0..15) as int8x4 words in value order, and d.  The offset -8 is applied
+// by the caller through the activation block's exact code sum.
+__device__ __forceinline__ void q4_0_decode(const uint8_t* row, int b, int (&w)[8], float& d) {
+  const uint8_t* blk = row + 18 * b;
+  d = f16_bits_to_f32(lds16(blk));
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t c = lds16(blk + 2 + 4 * i) | ((uint32_t)lds16(blk + 4 + 4 * i) << 16);
+    w[i] = (int)(c & 0x0F0F0F0Fu);
+    w[i + 4] = (int)((c >> 4) & 0x0F0F0F0Fu);
   }
 }
 

@@ -479,9 +479,10 @@ static cudaError_t launch_ls_t(const DecodeParams& p, cudaStream_t stream, bool 
   return cudaLaunchKernelEx(&cfg, k_layer_small<WG, WD, LPR>, p);
 }
 
-// Same-type layers of the four formats (aligned NVFP4 rows); other pairs use
-// the two-kernel path.
+// Same-type layers of every format (aligned NVFP4 rows) and the Q4_K gate_up
+// + Q6_K down pair of Q4_K_M checkpoints; other pairs use the two-kernel path.
 static cudaError_t dispatch_ls(const DecodeParams& p, cudaStream_t stream, bool probe_only, bool* fits) {
+  if (p.gu_type == W_Q4_K && p.dn_type == W_Q6_K) return launch_ls_t<W_Q4_K, W_Q6_K, 4>(p, stream, probe_only, fits);
   if (p.gu_type != p.dn_type) {
     if (fits) *fits = false;
     return cudaSuccess;
@@ -495,6 +496,8 @@ static cudaError_t dispatch_ls(const DecodeParams& p, cudaStream_t stream, bool 
       return launch_ls_t<W_NVFP4, W_NVFP4, 8>(p, stream, probe_only, fits);
     case W_Q4_K: return launch_ls_t<W_Q4_K, W_Q4_K, 4>(p, stream, probe_only, fits);
     case W_Q8_0: return launch_ls_t<W_Q8_0, W_Q8_0, 8>(p, stream, probe_only, fits);
+    case W_Q6_K: return launch_ls_t<W_Q6_K, W_Q6_K, 4>(p, stream, probe_only, fits);
+    case W_Q4_0: return launch_ls_t<W_Q4_0, W_Q4_0, 8>(p, stream, probe_only, fits);
     default: return launch_ls_t<W_BF16, W_BF16, 16>(p, stream, probe_only, fits);
   }
 }

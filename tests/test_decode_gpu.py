@@ -56,7 +56,9 @@ def test_q8_1_quantizer_bit_exact():
 
 
 @pytest.mark.parametrize("wtype,k", [(F.TYPE_Q8_0, 256), (F.TYPE_Q8_0, 768), (F.TYPE_NVFP4, 2048),
-                                     (F.TYPE_NVFP4, 768), (F.TYPE_Q4_K, 4096), (F.TYPE_Q4_K, 768)])
+                                     (F.TYPE_NVFP4, 768), (F.TYPE_Q4_K, 4096), (F.TYPE_Q4_K, 768),
+                                     (F.TYPE_Q6_K, 2048), (F.TYPE_Q6_K, 768), (F.TYPE_Q4_0, 2048),
+                                     (F.TYPE_Q4_0, 96)])
 def test_block_dots_bit_exact(wtype, k):
     rows = C.bank_bytes_np(11 + wtype, wtype, k, 0, 64)
     # every byte pattern: raw random codes, including all E2M1 signs and -0
@@ -66,7 +68,9 @@ def test_block_dots_bit_exact(wtype, k):
     act = F.q8_1_pack_blocks(qs, d, s).reshape(-1)
     rows_d = torch.from_numpy(rows.reshape(-1).copy()).to(DEV)
     act_d = torch.from_numpy(act).to(DEV)
-    nb = k // 16 if wtype == F.TYPE_NVFP4 else k // 32
+    # Q6_K at k=768 (630-byte rows) and Q4_0 (18-byte blocks) put blocks at
+    # every 2-byte alignment
+    nb = k // 16 if wtype in (F.TYPE_NVFP4, F.TYPE_Q6_K) else k // 32
     out = torch.empty((64, nb), dtype=torch.int32, device=DEV)
     capi.moe_debug_block_dots(wtype, rows_d.data_ptr(), 64, k, act_d.data_ptr(), out.data_ptr(), _stream())
     torch.cuda.synchronize()
@@ -150,13 +154,75 @@ def test_laguna_zipf_batches_sampled(T):
 
 @pytest.mark.parametrize("gu_t,dn_t", [(F.TYPE_Q4_K, F.TYPE_BF16), (F.TYPE_BF16, F.TYPE_Q4_K),
                                        (F.TYPE_NVFP4, F.TYPE_Q8_0), (F.TYPE_Q8_0, F.TYPE_NVFP4),
-                                       (F.TYPE_BF16, F.TYPE_NVFP4)])
+                                       (F.TYPE_BF16, F.TYPE_NVFP4), (F.TYPE_Q6_K, F.TYPE_Q4_0),
+                                       (F.TYPE_Q4_0, F.TYPE_Q6_K), (F.TYPE_BF16, F.TYPE_Q6_K),
+                                       (F.TYPE_Q6_K, F.TYPE_NVFP4), (F.TYPE_Q4_0, F.TYPE_Q8_0)])
 def test_mixed_type_pairs(gu_t, dn_t):
-    case = cases.make_case(512, 256, 16, 4, gu_t, dn_t, 5, seed=40 + 4 * gu_t + dn_t)
+    """Gate_up and down of different types: the two-kernel path."""
+    case = cases.make_case(512, 256, 16, 4, gu_t, dn_t, 5, seed=40 + 8 * gu_t + dn_t)
+    _negate_q6k_scales(case)
     _check_case(case)
 
 
-@pytest.mark.parametrize("wtype", [F.TYPE_Q8_0, F.TYPE_NVFP4, F.TYPE_BF16])
+def _negate_q6k_scales(case):
+    """Flip the sign of every other int8 scale of the routed Q6_K rows, in the
+    oracle's copy and in the device bank (the synthetic encoder writes
+    non-negative scales only)."""
+    g = case.geom
+    for rows_of, dev, wt, k, nrows in ((case.gu_rows, case.gu_dev, g.gate_up_type, g.H, 2 * g.I),
+                                       (case.dn_rows, case.dn_dev, g.down_type, g.I, g.H)):
+        if wt != F.TYPE_Q6_K:
+            continue
+        rb = F.row_bytes(wt, k)
+        for e, rows in rows_of.items():
+            sb = rows.reshape(nrows, k // 256, 210)
+            assert np.shares_memory(sb, rows)
+            sc = sb[..., 192:208].view(np.int8)
+            sc[..., 1::2] = -sc[..., 1::2]
+            dev[e * nrows * rb:(e + 1) * nrows * rb].copy_(torch.from_numpy(rows.reshape(-1).copy()))
+
+
+@pytest.mark.parametrize("T", [1, 4])
+def test_laguna_shaped_q4_k_gate_up_q6_k_down(T):
+    """H=4096 I=768 E=256 top-10: Q4_K gate_up with Q6_K down (the pairing of
+    a Q4_K_M checkpoint), with negative Q6_K scales; T=1 is one fused launch."""
+    case = cases.make_case(4096, 768, 256, 10, F.TYPE_Q4_K, F.TYPE_Q6_K, T, seed=80 + T)
+    _negate_q6k_scales(case)
+    figs = _check_case(case)
+    if T == 1:
+        assert figs["launches"] == 1
+    assert figs["err_bits"] == 0
+
+
+@pytest.mark.parametrize("T", [1, 8])
+def test_qwen3_30b_a3b_shaped_q6_k_layer(T):
+    """H=2048 I=768 E=128 top-8, Q6_K gate_up and down with negative scales."""
+    case = cases.make_case(2048, 768, 128, 8, F.TYPE_Q6_K, F.TYPE_Q6_K, T, seed=90 + T)
+    _negate_q6k_scales(case)
+    figs = _check_case(case)
+    if T == 1:
+        assert figs["launches"] == 1
+    assert figs["err_bits"] == 0
+
+
+@pytest.mark.parametrize("T", [1, 8])
+def test_q4_0_layer_32_experts_top8(T):
+    """Q4_0 gate_up and down, 32 experts, top-8, H=2048 I=768."""
+    case = cases.make_case(2048, 768, 32, 8, F.TYPE_Q4_0, F.TYPE_Q4_0, T, seed=100 + T)
+    figs = _check_case(case)
+    if T == 1:
+        assert figs["launches"] == 1
+    assert figs["err_bits"] == 0
+
+
+def test_q6_k_more_tokens_than_one_pass():
+    """Q4_K gate_up + Q6_K down over three passes (150 tokens)."""
+    case = cases.make_case(512, 256, 16, 4, F.TYPE_Q4_K, F.TYPE_Q6_K, 150, seed=110)
+    _negate_q6k_scales(case)
+    _check_case(case, tokens=[0, 63, 64, 149], check_stages=False)
+
+
+@pytest.mark.parametrize("wtype", [F.TYPE_Q8_0, F.TYPE_NVFP4, F.TYPE_BF16, F.TYPE_Q4_0])
 def test_ragged_geometry(wtype):
     """H and I not multiples of the 32-lane tiling, odd E, K and T."""
     case = cases.make_case(160, 96, 5, 3, wtype, wtype, 7, seed=50 + wtype)
