@@ -38,13 +38,17 @@ import numpy as np
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-NVFP4, Q4_K, BF16 = 3, 2, 0
+NVFP4, Q4_K, BF16, Q8_0, Q6_K, Q4_0 = 3, 2, 0, 1, 4, 5
+TYPE_NAMES = {BF16: "bf16", Q8_0: "q8_0", Q4_K: "q4_k", NVFP4: "nvfp4", Q6_K: "q6_k", Q4_0: "q4_0"}
 CFG1 = dict(H=2048, I=768, E=128, K=8, gu=NVFP4, dn=NVFP4)
 LAGUNA = dict(H=4096, I=768, E=256, K=10)
+# the other GGUF row types at the same layer shape as the headline (gate_up, down)
+TYPE_PAIRS = ((Q4_K, Q6_K), (Q6_K, Q6_K), (Q4_0, Q4_0), (Q8_0, Q8_0), (Q4_K, Q4_K))
 
 
 def row_bytes(t, k):
-    return {0: 2 * k, 1: k // 32 * 34, 2: k // 256 * 144, 3: k // 2 + k // 16}[t]
+    return {0: 2 * k, 1: k // 32 * 34, 2: k // 256 * 144, 3: k // 2 + k // 16, 4: k // 256 * 210,
+            5: k // 32 * 18}[t]
 
 
 def peaks():
@@ -385,13 +389,16 @@ def run_cpu_baseline(seconds: float) -> dict:
 
 def profile_layer(a):
     """Eager decode passes of one layer for a profiler: the NVFP4 layer
-    (H=2048, I=768, E=128, top-8) or a Laguna-shaped Q4_K / BF16 layer
+    (H=2048, I=768, E=128, top-8) or the same shape with Q4_K+Q6_K, Q6_K or
+    Q4_0 rows, or a Laguna-shaped Q4_K / BF16 layer
     (H=4096, I=768, E=256, top-10, Zipf routing), a stack of --layers banks."""
     import torch
     dev = "cuda:0"
-    if a.profile_layer == "nvfp4":
+    other = {"q4_k_m": (Q4_K, Q6_K), "q6_k": (Q6_K, Q6_K), "q4_0": (Q4_0, Q4_0)}
+    if a.profile_layer == "nvfp4" or a.profile_layer in other:
         c = CFG1
-        st = Stack([(c["gu"], c["dn"])] * a.layers, c["H"], c["I"], c["E"], c["K"], 1, dev)
+        pair = other.get(a.profile_layer, (c["gu"], c["dn"]))
+        st = Stack([pair] * a.layers, c["H"], c["I"], c["E"], c["K"], 1, dev)
         st.prepare(a.T, "softmax", 1)
     else:
         t = Q4_K if a.profile_layer == "q4_k" else BF16
@@ -442,9 +449,10 @@ def main():
     ap.add_argument("--layers", type=int, default=48)
     ap.add_argument("--no-stack", action="store_true", help="skip the 47-layer Laguna sweep")
     ap.add_argument("--no-prefill", action="store_true", help="skip the prompt-path chunk")
+    ap.add_argument("--no-types", action="store_true", help="skip the per-GGUF-type layer stacks")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--cpu-oracle-worker", type=float, default=None, help=argparse.SUPPRESS)
-    ap.add_argument("--profile-layer", choices=["nvfp4", "q4_k", "bf16"], default=None,
+    ap.add_argument("--profile-layer", choices=["nvfp4", "q4_k", "bf16", "q4_k_m", "q6_k", "q4_0"], default=None,
                     help="run --steps eager decode passes of one layer type (for ncu), print nothing else")
     ap.add_argument("--T", type=int, default=1)
     ap.add_argument("--experts", type=int, default=0,
@@ -537,6 +545,26 @@ def main():
         del st
         torch.cuda.empty_cache()
         extra["laguna_47_layer_stack"] = sweep
+
+    if not a.no_types:
+        c = CFG1
+        types = {}
+        for gu_t, dn_t in TYPE_PAIRS:
+            st = Stack([(gu_t, dn_t)] * 24, c["H"], c["I"], c["E"], c["K"], 5, dev)
+            row = {}
+            for T in (1, 8):
+                st.prepare(T, "softmax", 11 + T)
+                msT = st.time_replays(max(10, min(100, a.steps // 4)), a.warmup)
+                gbs = st.bytes_per_step / (msT / 1e3) / 1e9
+                row[f"T={T}"] = {"per_layer_us": msT / 24 * 1e3, "layer_tok_per_s": 24 * T / (msT / 1e3),
+                                 "hbm_gbs": gbs, "frac": gbs / hbm_peak,
+                                 "launches_per_layer": st.launches_per_step / 24}
+            st.close()
+            del st
+            torch.cuda.empty_cache()
+            types[f"{TYPE_NAMES[gu_t]}+{TYPE_NAMES[dn_t]}"] = row
+        extra["gguf_types_24_layer_stack"] = {
+            "workload": "H=2048 I=768 E=128 top-8, softmax routing, 24 resident layer banks per step", **types}
 
     if not a.no_prefill:
         pk, pk_kind = bf16_peak()
