@@ -90,6 +90,14 @@ enum {
   MOE_DECODE_T_CHUNK = 64  /* tokens per internal decode pass (larger T is split) */
 };
 
+/* The GLU of the layer, glu(g, u) = act(g) * u (FreeToken PR #732, "Design":
+ * y = (glu(g, u) @ W_down^T) * s_down * routing_weight; its "Other checks"
+ * run experts with gelu_tanh and silu):
+ *   MOE_GLU_SILU      : act(g) = g / (1 + exp(-g))
+ *   MOE_GLU_GELU_TANH : act(g) = g/2 * (1 + tanh(sqrt(2/pi) * (g + 0.044715 g^3)))
+ * Both are evaluated in fp32. */
+typedef enum { MOE_GLU_SILU = 0, MOE_GLU_GELU_TANH = 1 } moe_glu;
+
 typedef struct {
   int32_t H;             /* hidden size; multiple of 256 for Q4_K gate_up, else of 32 */
   int32_t I;             /* intermediate size; multiple of 32 (256 for Q4_K down) */
@@ -97,6 +105,7 @@ typedef struct {
   int32_t top_k;         /* routes per token, 1..min(E, MOE_MAX_TOPK) */
   int32_t gate_up_type;  /* moe_type of the merged gate_up rows [E, 2I, H]: rows [0,I) gate, [I,2I) up */
   int32_t down_type;     /* moe_type of the down rows [E, H, I] */
+  int32_t glu;           /* moe_glu: the activation of the gate half (0 = SiLU) */
 } moe_layer_geom;
 
 /* Where moe_bank_create reads the rows from. */
@@ -135,6 +144,16 @@ int moe_bank_destroy(moe_bank* bank);
 
 /* Copy the bank's geometry to *out. */
 int moe_bank_geometry(const moe_bank* bank, moe_layer_geom* out);
+
+/* Fold a router's per-expert output scale into the bank's s_down column:
+ * s_down[e] = fp32(s_down[e] * per_expert_scale[e]) for e < E (IEEE fp32
+ * multiply), after which the router's weights are used without that scale
+ * (FreeToken PR #732, "Design": the converter folds Gemma-4's per_expert_scale
+ * into the down experts' scale).  per_expert_scale: E fp32 values in host
+ * (src_kind MOE_SRC_HOST) or device (MOE_SRC_DEVICE) memory, 4-byte aligned.
+ * Synchronizes `stream`; must not run concurrently with a decode on the bank.
+ * Errors: MOE_EINVAL (null, src_kind, alignment), MOE_ENOMEM, MOE_ECUDA. */
+int moe_bank_fold_down_scale(moe_bank* bank, const float* per_expert_scale, int32_t src_kind, void* stream);
 
 /* Workspace bytes moe_decode needs for batches of up to max_tokens tokens
  * (0 on bad arguments).  The workspace holds the quantized activations, the

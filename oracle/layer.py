@@ -16,7 +16,10 @@ input), down (a dot over every output row, per route), and the executor's sum
 over routes.  Strata PR #292, "Summary/Pipeline" fixes that each global scale
 multiplies its own projection's fp32 output and is never folded.
 
-The GLU is SiLU-GLU, silu(g) * u, with silu(g) = g / (1 + exp(-g)).
+The GLU is act(g) * u with act = SiLU, silu(g) = g / (1 + exp(-g)), or the
+tanh form of GELU, gelu_tanh(g) = g/2 * (1 + tanh(sqrt(2/pi) (g + 0.044715 g^3)))
+(Hendrycks and Gimpel, "Gaussian Error Linear Units", 2016); FreeToken PR
+#732, "Other checks", runs experts with both.
 
 Readings where the pages are silent (each listed in the design doc):
   * gate rows are rows [0, I) of an expert's gate_up bank, up rows [I, 2I);
@@ -52,11 +55,28 @@ class Geometry:
     top_k: int
     gate_up_type: int
     down_type: int
+    glu: int = 0          # GLU_SILU or GLU_GELU_TANH
 
 
-def _silu_glu(g: np.ndarray, u: np.ndarray) -> np.ndarray:
+GLU_SILU, GLU_GELU_TANH = 0, 1
+
+
+def silu(g: np.ndarray) -> np.ndarray:
     with np.errstate(over="ignore"):
-        return g / (1.0 + np.exp(-g)) * u
+        return g / (1.0 + np.exp(-g))
+
+
+def gelu_tanh(g: np.ndarray) -> np.ndarray:
+    with np.errstate(over="ignore", invalid="ignore"):
+        return 0.5 * g * (1.0 + np.tanh(np.sqrt(2.0 / np.pi) * (g + 0.044715 * g ** 3)))
+
+
+def _glu(g: np.ndarray, u: np.ndarray, kind: int) -> np.ndarray:
+    if kind == GLU_SILU:
+        return silu(g) * u
+    if kind == GLU_GELU_TANH:
+        return gelu_tanh(g) * u
+    raise ValueError(kind)
 
 
 class _ExpertCache:
@@ -163,7 +183,7 @@ def moe_layer(geom: Geometry, gate_up, down, scale_bank, x_bf16_bits, topk_ids, 
             h = wgu @ xa
             gg = h[: g.I] * sb[e, 0]
             uu = h[g.I:] * sb[e, 1]
-            a = _silu_glu(gg, uu)
+            a = _glu(gg, uu, g.glu)
             aq, ainfo = _act_in(act_kind, g.down_type, a.astype(np.float32)
                                 if g.down_type != F.TYPE_BF16 else a)
             if g.down_type == F.TYPE_BF16:

@@ -18,11 +18,12 @@ MOE_DEVERR_BAD_ID, MOE_DEVERR_TIMEOUT = 1, 2
 MOE_SRC_HOST, MOE_SRC_DEVICE, MOE_SRC_DEVICE_BORROW = 0, 1, 2
 MOE_MAX_E, MOE_MAX_TOPK, MOE_DECODE_T_CHUNK = 1024, 32, 64
 MOE_PREFILL_W4A4, MOE_PREFILL_W4A8 = 0, 1
+MOE_GLU_SILU, MOE_GLU_GELU_TANH = 0, 1
 MOE_NOALLOC_WS_BYTES = 4 << 20
 
 # every symbol include/qre_moe.h declares
 EXPORTS = (
-    "moe_row_bytes", "moe_bank_create", "moe_bank_destroy", "moe_bank_geometry",
+    "moe_row_bytes", "moe_bank_create", "moe_bank_destroy", "moe_bank_geometry", "moe_bank_fold_down_scale",
     "moe_workspace_bytes", "moe_workspace_init", "moe_decode", "moe_get_error",
     "moe_status_string", "moe_last_cuda_error", "moe_quantize_q8_1",
     "moe_debug_block_dots", "moe_debug_decode_stages", "moe_decode_noalloc", "moe_debug_tc_gemm",
@@ -33,7 +34,8 @@ EXPORTS = (
 
 class moe_layer_geom(ctypes.Structure):
     _fields_ = [("H", ctypes.c_int32), ("I", ctypes.c_int32), ("E", ctypes.c_int32),
-                ("top_k", ctypes.c_int32), ("gate_up_type", ctypes.c_int32), ("down_type", ctypes.c_int32)]
+                ("top_k", ctypes.c_int32), ("gate_up_type", ctypes.c_int32), ("down_type", ctypes.c_int32),
+                ("glu", ctypes.c_int32)]
 
 
 class MoeError(RuntimeError):
@@ -58,6 +60,7 @@ def _load() -> ctypes.CDLL:
                                            ctypes.POINTER(vp)]),
         "moe_bank_destroy": (ctypes.c_int, [vp]),
         "moe_bank_geometry": (ctypes.c_int, [vp, ctypes.POINTER(moe_layer_geom)]),
+        "moe_bank_fold_down_scale": (ctypes.c_int, [vp, vp, i32, vp]),
         "moe_workspace_bytes": (sz, [vp, i32]),
         "moe_workspace_init": (ctypes.c_int, [vp, sz, vp]),
         "moe_decode": (ctypes.c_int, [vp, vp, i32, vp, vp, vp, vp, sz, vp]),
@@ -122,6 +125,12 @@ def moe_bank_geometry(bank: int) -> moe_layer_geom:
     g = moe_layer_geom()
     _check(_lib.moe_bank_geometry(bank, ctypes.byref(g)), "moe_bank_geometry")
     return g
+
+
+def moe_bank_fold_down_scale(bank: int, per_expert_scale: int, src_kind: int, stream: int = 0) -> None:
+    """s_down[e] *= per_expert_scale[e] (fp32) in the bank's scale bank."""
+    _check(_lib.moe_bank_fold_down_scale(bank, per_expert_scale, src_kind, stream or None),
+           "moe_bank_fold_down_scale")
 
 
 def moe_workspace_bytes(bank: int, max_tokens: int) -> int:

@@ -118,6 +118,7 @@ int geom_check(const moe_layer_geom* g) {
   if (g->down_type < MOE_BF16 || g->down_type > MOE_Q4_0) return MOE_EINVAL;
   if (row_bytes_of(g->gate_up_type, g->H) == 0 || row_bytes_of(g->down_type, g->I) == 0) return MOE_EINVAL;
   if (g->H % 32 != 0 || g->I % 32 != 0) return MOE_EINVAL;
+  if (g->glu != MOE_GLU_SILU && g->glu != MOE_GLU_GELU_TANH) return MOE_EINVAL;
   return MOE_OK;
 }
 
@@ -242,6 +243,7 @@ DecodeParams make_params(const moe_bank* b, const WsLayout& L, uint8_t* ws, cons
   std::memset(&p, 0, sizeof(p));
   p.H = g.H; p.I = g.I; p.E = g.E; p.K = g.top_k; p.T = T;
   p.gu_type = g.gate_up_type; p.dn_type = g.down_type;
+  p.glu = g.glu;
   p.rb_gu = b->rb_gu; p.rb_dn = b->rb_dn;
   p.gu_bank = b->gu; p.dn_bank = b->dn; p.scales = b->scales;
   p.err = reinterpret_cast<uint32_t*>(ws + L.err);
@@ -442,6 +444,33 @@ int moe_bank_geometry(const moe_bank* b, moe_layer_geom* out) {
   return MOE_OK;
 }
 
+namespace {
+__global__ void k_fold_down_scale(float* scales, const float* pes, int E) {
+  const int e = blockIdx.x * blockDim.x + threadIdx.x;
+  if (e < E) scales[4 * e + 2] = __fmul_rn(scales[4 * e + 2], pes[e]);
+}
+}  // namespace
+
+int moe_bank_fold_down_scale(moe_bank* b, const float* per_expert_scale, int32_t src_kind, void* stream) {
+  if (!b || !per_expert_scale) return MOE_EINVAL;
+  if (src_kind != MOE_SRC_HOST && src_kind != MOE_SRC_DEVICE) return MOE_EINVAL;
+  if (!aligned(per_expert_scale, 4)) return MOE_EINVAL;
+  const int E = b->geom.E;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  float* tmp = nullptr;
+  cudaError_t e = cudaMalloc(&tmp, sizeof(float) * (size_t)E);
+  if (e != cudaSuccess) { cudaGetLastError(); return MOE_ENOMEM; }
+  const cudaMemcpyKind kind = (src_kind == MOE_SRC_HOST) ? cudaMemcpyHostToDevice : cudaMemcpyDeviceToDevice;
+  e = cudaMemcpyAsync(tmp, per_expert_scale, sizeof(float) * (size_t)E, kind, s);
+  if (e == cudaSuccess) {
+    k_fold_down_scale<<<(E + 255) / 256, 256, 0, s>>>(b->scales, tmp, E);
+    e = cudaGetLastError();
+  }
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  cudaFree(tmp);
+  return e == cudaSuccess ? MOE_OK : cuda_fail(e, "fold_down_scale");
+}
+
 size_t moe_workspace_bytes(const moe_bank* b, int32_t max_tokens) {
   if (!b || max_tokens < 1) return 0;
   const Shape sh = decode_shape(b->geom);
@@ -465,6 +494,7 @@ static bool dense_params(const moe_bank* b, const WsLayout& L, uint8_t* ws, cons
   d.H = g.H; d.I = g.I; d.E = g.E; d.K = g.top_k; d.T = p.T;
   d.RT = p.T * g.top_k;
   d.RTp = L.RTp;
+  d.glu = g.glu;
   d.scales = b->scales;
   d.x = p.x; d.ids = p.ids; d.w = p.w; d.out = p.out;
   d.err = p.err;
@@ -494,6 +524,7 @@ static bool qbatch_params(const moe_bank* b, const WsLayout& L, uint8_t* ws, con
   q.H = g.H; q.I = g.I; q.E = g.E; q.K = g.top_k; q.T = p.T;
   q.RT = p.T * g.top_k;
   q.RTp = L.RTp;
+  q.glu = g.glu;
   q.scales = b->scales;
   q.x = p.x; q.ids = p.ids; q.w = p.w; q.out = p.out;
   q.err = p.err;
@@ -784,6 +815,7 @@ int moe_prefill_grouped(const moe_bank* b, const void* x, int32_t T, const int32
   std::memset(&p, 0, sizeof(p));
   p.H = g.H; p.I = g.I; p.E = g.E; p.K = g.top_k; p.T = T; p.RT = T * g.top_k;
   p.mode = mode;
+  p.glu = g.glu;
   p.rb_gu = b->rb_gu; p.rb_dn = b->rb_dn;
   p.gu_bank = b->gu; p.dn_bank = b->dn; p.scales = b->scales;
   p.x = static_cast<const uint16_t*>(x);

@@ -234,7 +234,7 @@ __global__ void __launch_bounds__(kDecodeThreads, MAXNT == 1 ? 2 : 1) k_gate_up(
                                           ass + t * (p.H >> 5));
           if (lane == 0) {
             const int r = g.routes[roff + ri];
-            p.inter[(size_t)r * p.I + si + pi] = silu_glu(h.x * sg, h.y * su_);
+            p.inter[(size_t)r * p.I + si + pi] = glu_act(h.x * sg, h.y * su_, p.glu);
           }
         }
       }
@@ -259,7 +259,7 @@ __global__ void __launch_bounds__(kDecodeThreads, MAXNT == 1 ? 2 : 1) k_gate_up(
             for (int t = 1; t < NT; ++t)
               if (lane == t) { gv = ag[t]; uv = au[t]; }
             const int r = g.routes[roff + c0 + lane];
-            p.inter[(size_t)r * p.I + si + pi] = silu_glu(gv * sg, uv * su_);
+            p.inter[(size_t)r * p.I + si + pi] = glu_act(gv * sg, uv * su_, p.glu);
           }
         }
       }
@@ -310,7 +310,7 @@ __global__ void __launch_bounds__(kDecodeThreads, MAXNT == 1 ? 2 : 1) k_gate_up(
             hu += pbuf[(it2 * NT + t) * 2 + 1];
           }
           const int r = g.routes[roff + ri];
-          p.inter[(size_t)r * p.I + si + pi] = silu_glu(hg * sg, hu * su_);
+          p.inter[(size_t)r * p.I + si + pi] = glu_act(hg * sg, hu * su_, p.glu);
         }
         __syncwarp();
         if (lane == 0) pcnt[buf] = 0;

@@ -764,7 +764,19 @@ __device__ __forceinline__ float dn_row_q8(const uint8_t* rowp, bool vrow, int I
   return v;
 }
 
-__device__ __forceinline__ float silu_glu(float g, float u) { return __fdividef(g, 1.0f + expf(-g)) * u; }
+// The GLU of the layer: act(g) * u, act = SiLU (kind 0) or the tanh form of
+// GELU (kind 1): silu(g) = g / (1 + exp(-g)); gelu_tanh(g) =
+// g/2 * (1 + tanh(sqrt(2/pi) * (g + 0.044715 g^3))) (Hendrycks and Gimpel,
+// "Gaussian Error Linear Units", 2016).  FreeToken PR #732, "Other checks",
+// runs its experts with both.
+constexpr int kGluSilu = 0, kGluGeluTanh = 1;
+__device__ __forceinline__ float glu_act(float g, float u, int kind) {
+  if (kind == kGluGeluTanh) {
+    const float z = 0.7978845608028654f * fmaf(0.044715f * g, g * g, g);
+    return 0.5f * g * (1.0f + tanhf(z)) * u;
+  }
+  return __fdividef(g, 1.0f + expf(-g)) * u;
+}
 
 // Quantize `nblk` 32-value blocks (row-major values from `src`) into q8_1
 // planes in shared memory -- codes q[32*b + i], scales d[b] (fp16 values as

@@ -505,7 +505,7 @@ __global__ void __launch_bounds__(kQbThreads, 1) k_qb_gemm(const __grid_constant
         if (k >= nv) break;
         const int srow = m.srow0 + k;
         const int r = perm_s[srow];
-        const float a = silu_glu(acca[k] * sg, accb[k] * su);
+        const float a = glu_act(acca[k] * sg, accb[k] * su, p.glu);
         float d;
         int sum;
         const int q = q8_1_quantize_lane(a, d, sum);

@@ -351,7 +351,7 @@ __global__ void __launch_bounds__(kDtThreads, 1) k_dt_gemm(const __grid_constant
               const int c = c0 + j;
               if (c < ti.nv) {
                 const int s = ti.srow0 + c;
-                const float a = silu_glu(__uint_as_float(g16[j]) * sg, __uint_as_float(u16[j]) * su);
+                const float a = glu_act(__uint_as_float(g16[j]) * sg, __uint_as_float(u16[j]) * su, p.glu);
                 const uint32_t hb = f32_to_bf16_bits_rn(a);
                 const uint32_t lb = f32_to_bf16_bits_rn(a - __uint_as_float(hb << 16));
                 p.ih[(size_t)s * p.I + i] = (uint16_t)hb;

@@ -17,6 +17,7 @@ constexpr int kMaxGridCtas = 256;   // CTAs of the fused kernel's grid barrier
 // kernel parameter space.
 struct DecodeParams {
   int H, I, E, K, T;
+  int glu;                 // kGluSilu or kGluGeluTanh
   int gu_type, dn_type;
   int rb_gu, rb_dn;
   const uint8_t* gu_bank;  // [E][2I][rb_gu]
@@ -59,6 +60,7 @@ struct DecodeParams {
 enum PfMode : int { PF_W4A4 = 0, PF_W4A8 = 1 };
 struct PfParams {
   int H, I, E, K, T, RT;
+  int glu;
   int mode;
   int rb_gu, rb_dn;
   const uint8_t* gu_bank;   // NVFP4 rows [E][2I][rb_gu]
@@ -90,6 +92,7 @@ struct DtParams {
   CUtensorMap map_xs;       // xs: bf16 [RTp][H], box 64 x 16 rows
   CUtensorMap map_ih;       // ih: bf16 [2*RTp][I] (hi rows, then lo rows), box 64 x 16 rows
   int H, I, E, K, T, RT, RTp;
+  int glu;
   const float* scales;      // [E][4]
   const uint16_t* x;        // bf16 [T][H]
   const int32_t* ids;       // [T][K]
@@ -125,6 +128,7 @@ struct QbParams {
   CUtensorMap map_is;       // iss [RTp][I/4], box 64 x kQbTileTokens rows
   int wt;                   // W_Q4_K or W_NVFP4 (both projections)
   int H, I, E, K, T, RT, RTp;
+  int glu;
   const float* scales;      // [E][4]
   const uint16_t* x;        // bf16 [T][H]
   const int32_t* ids;       // [T][K]

@@ -331,7 +331,7 @@ __global__ void __launch_bounds__(kLsThreads, 1) k_layer_small(const __grid_cons
         }
         if (lane == 0) {
           const int r = g.routes[roff + ri];
-          p.inter[(size_t)r * p.I + si + pi] = silu_glu(h.x * sg, h.y * su_);
+          p.inter[(size_t)r * p.I + si + pi] = glu_act(h.x * sg, h.y * su_, p.glu);
         }
       }
     }

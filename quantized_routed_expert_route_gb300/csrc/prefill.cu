@@ -454,7 +454,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(const __grid_constant
           tc::tmem_ld_wait();
 #pragma unroll
           for (int j = 0; j < 16; ++j)
-            a[16 * half + j] = silu_glu(__uint_as_float(g16[j]) * sg, __uint_as_float(u16[j]) * su);
+            a[16 * half + j] = glu_act(__uint_as_float(g16[j]) * sg, __uint_as_float(u16[j]) * su, p.glu);
         }
         if (valid) {
           uint4* dst = reinterpret_cast<uint4*>(p.i16 + (size_t)(srow0 + m) * p.I + nt * 128 + 32 * cg);

@@ -16,11 +16,13 @@ from . import capi
 
 class MoeLayer:
     def __init__(self, H: int, I: int, E: int, top_k: int, gate_up_type: int, down_type: int,
-                 gate_up, down, scale_bank=None, borrow: bool = False, max_tokens: int = capi.MOE_DECODE_T_CHUNK):
+                 gate_up, down, scale_bank=None, borrow: bool = False, max_tokens: int = capi.MOE_DECODE_T_CHUNK,
+                 glu: int = capi.MOE_GLU_SILU):
         """gate_up / down: uint8 tensors (host or CUDA) holding the compact rows;
         scale_bank: fp32 [E, 4] tensor on the same device, or None (ones).
-        borrow=True keeps the CUDA tensors as the bank (no copy)."""
-        self.geom = capi.moe_layer_geom(H, I, E, top_k, gate_up_type, down_type)
+        borrow=True keeps the CUDA tensors as the bank (no copy).  glu:
+        MOE_GLU_SILU or MOE_GLU_GELU_TANH."""
+        self.geom = capi.moe_layer_geom(H, I, E, top_k, gate_up_type, down_type, glu)
         self.H, self.I, self.E, self.top_k = H, I, E, top_k
         on_dev = gate_up.is_cuda
         if borrow and not on_dev:

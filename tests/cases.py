@@ -26,7 +26,7 @@ class Case:
     dn_dev: object = None
 
 
-def make_case(H, I, E, K, gu_t, dn_t, T, seed, routing="softmax", ids=None, device="cuda") -> Case:
+def make_case(H, I, E, K, gu_t, dn_t, T, seed, routing="softmax", ids=None, device="cuda", glu=0) -> Case:
     import torch
     if ids is None:
         if routing == "zipf":
@@ -55,7 +55,7 @@ def make_case(H, I, E, K, gu_t, dn_t, T, seed, routing="softmax", ids=None, devi
     for e in routed:
         gu_dev[e * 2 * I * rb_gu:(e + 1) * 2 * I * rb_gu].copy_(torch.from_numpy(gu_rows[e].reshape(-1)))
         dn_dev[e * H * rb_dn:(e + 1) * H * rb_dn].copy_(torch.from_numpy(dn_rows[e].reshape(-1)))
-    return Case(OL.Geometry(H, I, E, K, gu_t, dn_t), x, ids, w, sb, gu_rows, dn_rows,
+    return Case(OL.Geometry(H, I, E, K, gu_t, dn_t, glu), x, ids, w, sb, gu_rows, dn_rows,
                 gu_dev[:n_gu], dn_dev[:n_dn])
 
 
@@ -76,7 +76,7 @@ def run_gpu(case: Case, stages=True):
     T = case.x.shape[0]
     dev = "cuda"
     layer = MoeLayer(g.H, g.I, g.E, g.top_k, g.gate_up_type, g.down_type, case.gu_dev, case.dn_dev,
-                     torch.from_numpy(case.sb).to(dev), borrow=True, max_tokens=max(T, 1))
+                     torch.from_numpy(case.sb).to(dev), borrow=True, max_tokens=max(T, 1), glu=g.glu)
     x = torch.from_numpy(case.x.view(np.int16)).to(dev)
     ids = torch.from_numpy(case.ids).to(dev)
     w = torch.from_numpy(case.w).to(dev)
@@ -120,7 +120,7 @@ class PrefillCase:
     dn_dev: object = None
 
 
-def make_prefill_case(H, I, E, K, T, seed, routing="softmax", ids=None, device="cuda") -> PrefillCase:
+def make_prefill_case(H, I, E, K, T, seed, routing="softmax", ids=None, device="cuda", glu=0) -> PrefillCase:
     """NVFP4 banks filled on the device by the counter-based generator (every
     expert is routed to in a prompt chunk); the oracle regenerates the rows of
     the experts it checks on the host."""
@@ -142,7 +142,7 @@ def make_prefill_case(H, I, E, K, T, seed, routing="softmax", ids=None, device="
     dn_dev = torch.empty(n_dn + 16, dtype=torch.uint8, device=device)
     C.fill_bank_torch(gu_dev[:n_gu], seed * 31 + 5, t, H)
     C.fill_bank_torch(dn_dev[:n_dn], seed * 31 + 6, t, I)
-    return PrefillCase(OL.Geometry(H, I, E, K, t, t), x, ids, w, sb, seed, gu_dev[:n_gu], dn_dev[:n_dn])
+    return PrefillCase(OL.Geometry(H, I, E, K, t, t, glu), x, ids, w, sb, seed, gu_dev[:n_gu], dn_dev[:n_dn])
 
 
 def prefill_oracle(case: PrefillCase, mode: int, tokens=None):
@@ -168,7 +168,7 @@ def run_prefill_gpu(case: PrefillCase, mode: int, stages=True):
     dev = "cuda"
     stream = torch.cuda.current_stream().cuda_stream
     sb = torch.from_numpy(case.sb).to(dev)
-    geom = capi.moe_layer_geom(g.H, g.I, g.E, g.top_k, g.gate_up_type, g.down_type)
+    geom = capi.moe_layer_geom(g.H, g.I, g.E, g.top_k, g.gate_up_type, g.down_type, g.glu)
     bank = capi.moe_bank_create(geom, case.gu_dev.data_ptr(), case.gu_dev.numel(), case.dn_dev.data_ptr(),
                                 case.dn_dev.numel(), sb.data_ptr(), capi.MOE_SRC_DEVICE_BORROW, stream)
     wsb = capi.moe_prefill_workspace_bytes(bank, T, mode)

@@ -222,6 +222,52 @@ def test_q6_k_more_tokens_than_one_pass():
     _check_case(case, tokens=[0, 63, 64, 149], check_stages=False)
 
 
+@pytest.mark.parametrize("shape,gu_t,dn_t,T,launches", [
+    ((2048, 768, 128, 8), F.TYPE_NVFP4, F.TYPE_NVFP4, 1, 1),   # fused
+    ((512, 256, 16, 4), F.TYPE_NVFP4, F.TYPE_Q8_0, 5, None),   # two-kernel
+    ((256, 256, 8, 4), F.TYPE_BF16, F.TYPE_BF16, 4, 4),        # dense, tensor cores
+    ((512, 512, 16, 4), F.TYPE_Q4_K, F.TYPE_Q4_K, 8, 4),       # batched
+    ((512, 512, 16, 4), F.TYPE_NVFP4, F.TYPE_NVFP4, 8, 4),     # batched
+])
+def test_gelu_tanh_glu_on_every_decode_path(shape, gu_t, dn_t, T, launches):
+    """The gelu_tanh GLU in each path's gate_up epilogue."""
+    H, I, E, K = shape
+    case = cases.make_case(H, I, E, K, gu_t, dn_t, T, seed=120 + T + 3 * gu_t, glu=1)
+    figs = _check_case(case)
+    if launches is not None:
+        assert figs["launches"] == launches
+    assert figs["err_bits"] == 0
+
+
+@pytest.mark.parametrize("src", ["host", "device"])
+def test_fold_down_scale_equals_prefolded_bank(src):
+    """moe_bank_fold_down_scale(per_expert_scale) gives the outputs, bit for
+    bit, of a bank created with s_down * per_expert_scale (fp32), and those
+    match the oracle on the folded scale bank."""
+    from quantized_routed_expert_route_gb300.layer import MoeLayer
+    from synth import banks as S
+    case = cases.make_case(512, 256, 16, 4, F.TYPE_Q4_K, F.TYPE_Q6_K, 3, seed=130)
+    g = case.geom
+    pes = S.rng(131).uniform(0.25, 4.0, size=g.E).astype(np.float32)
+    layer = MoeLayer(g.H, g.I, g.E, g.top_k, g.gate_up_type, g.down_type, case.gu_dev, case.dn_dev,
+                     torch.from_numpy(case.sb).to(DEV), borrow=True, max_tokens=3)
+    if src == "host":
+        capi.moe_bank_fold_down_scale(layer.bank, pes.ctypes.data, capi.MOE_SRC_HOST, _stream())
+    else:
+        pes_d = torch.from_numpy(pes).to(DEV)
+        capi.moe_bank_fold_down_scale(layer.bank, pes_d.data_ptr(), capi.MOE_SRC_DEVICE, _stream())
+    x = torch.from_numpy(case.x.view(np.int16)).to(DEV).view(torch.bfloat16)
+    out = layer.decode(x, torch.from_numpy(case.ids).to(DEV), torch.from_numpy(case.w).to(DEV))
+    torch.cuda.synchronize()
+    folded = out.view(torch.int16).cpu().numpy().view(np.uint16)
+    layer.close()
+    case.sb[:, 2] = case.sb[:, 2] * pes          # fp32 products
+    figs = _check_case(case)
+    res = cases.run_gpu(case, stages=False)
+    assert np.array_equal(res["out"], folded)
+    assert figs["err_bits"] == 0
+
+
 @pytest.mark.parametrize("wtype", [F.TYPE_Q8_0, F.TYPE_NVFP4, F.TYPE_BF16, F.TYPE_Q4_0])
 def test_ragged_geometry(wtype):
     """H and I not multiples of the 32-lane tiling, odd E, K and T."""

@@ -76,6 +76,55 @@ def test_unit_scale_bf16_layer_equals_matmul_formula():
         assert np.allclose(out[t], ref, rtol=1e-13, atol=1e-15)
 
 
+def _gelu_erf(v):
+    # the exact GELU, v * Phi(v), from the error function
+    return 0.5 * v * (1.0 + np.vectorize(math.erf)(v / math.sqrt(2.0)))
+
+
+def test_gelu_tanh_pins():
+    """The tanh form approximates v * Phi(v) to within 4.8e-4 everywhere (the
+    largest gap, 4.73e-4, sits near v = +-2.70); its odd part is exactly v/2,
+    so gelu(v) - gelu(-v) = v; gelu(0) = 0 and gelu(v) -> v, 0 in the tails."""
+    v = np.linspace(-12.0, 12.0, 240001)
+    gt = L.gelu_tanh(v)
+    gap = np.abs(gt - _gelu_erf(v))
+    assert gap.max() <= 4.8e-4
+    assert 4.6e-4 <= gap.max()                     # the tanh form, not the exact one
+    assert abs(abs(v[np.argmax(gap)]) - 2.70) < 0.05   # the gap is even in v
+    assert np.allclose(gt - L.gelu_tanh(-v), v, rtol=0, atol=1e-14)
+    assert L.gelu_tanh(np.array([0.0]))[0] == 0.0
+    assert abs(L.gelu_tanh(np.array([12.0]))[0] - 12.0) < 1e-12
+    assert abs(L.gelu_tanh(np.array([-12.0]))[0]) < 1e-12
+
+
+def test_unit_scale_bf16_gelu_layer_against_exact_gelu():
+    """One route, unit scales, BF16 rows: the gelu_tanh layer is
+    (gelu(x Wg^T) * (x Wu^T)) Wd^T up to the tanh form's 4.8e-4 gap, which
+    reaches the output at most through |Wd| @ (4.8e-4 * |x Wu^T|)."""
+    H, I, E = 64, 32, 2
+    r = np.random.default_rng(9)
+    wgu = (r.standard_normal((E, 2 * I, H)) * 0.3).astype(np.float32)
+    wd = (r.standard_normal((E, H, I)) * 0.3).astype(np.float32)
+    gu = np.stack([S.convert_bf16(wgu[e]) for e in range(E)])
+    dn = np.stack([S.convert_bf16(wd[e]) for e in range(E)])
+    x = S.hidden_bf16(10, 2, H)
+    geom = L.Geometry(H, I, E, 1, F.TYPE_BF16, F.TYPE_BF16, glu=L.GLU_GELU_TANH)
+    ids = np.array([[1], [0]], np.int32)
+    out, _, _ = L.moe_layer(geom, gu, dn, None, x, ids, np.ones((2, 1), np.float32))
+    silu_out, _, _ = L.moe_layer(L.Geometry(H, I, E, 1, F.TYPE_BF16, F.TYPE_BF16), gu, dn, None, x, ids,
+                                 np.ones((2, 1), np.float32))
+    xt = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).double().numpy()
+    for t, e in enumerate([1, 0]):
+        Wg = torch.from_numpy(wgu[e][:I]).bfloat16().double().numpy()
+        Wu = torch.from_numpy(wgu[e][I:]).bfloat16().double().numpy()
+        Wd = torch.from_numpy(wd[e]).bfloat16().double().numpy()
+        hg, hu = Wg @ xt[t], Wu @ xt[t]
+        ref = (_gelu_erf(hg) * hu) @ Wd.T
+        bound = np.abs(Wd) @ (4.8e-4 * np.abs(hu)) + 1e-12
+        assert (np.abs(out[t] - ref) <= bound).all()
+        assert np.abs(silu_out[t] - ref).max() > 10 * bound.max()   # the kind is honoured
+
+
 def test_layer_invariants():
     geom, gu, dn, sb, x, ids, w = _tiny(seed=3, T=3)
     base, _, _ = L.moe_layer(geom, gu, dn, sb, x, ids, w)

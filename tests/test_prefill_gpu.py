@@ -129,6 +129,14 @@ def test_prefill_ragged_small(mode):
 
 
 @pytest.mark.parametrize("mode", [0, 1])
+def test_prefill_ragged_small_gelu_tanh(mode):
+    """The ragged small layer with the gelu_tanh GLU."""
+    T, E, K = 300, 8, 3
+    case = cases.make_prefill_case(256, 256, E, K, T, seed=210 + mode, ids=_ragged_ids(T, E, K, 8), glu=1)
+    _check_prefill(case, mode)
+
+
+@pytest.mark.parametrize("mode", [0, 1])
 def test_prefill_qwen3_30b_a3b_shaped_chunk(mode):
     """H=2048 I=768 E=128 top-8, a 4096-token chunk (32768 routed rows); the
     oracle checks a sample of tokens, the sort and the quantized x in full."""

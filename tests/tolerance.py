@@ -1,7 +1,7 @@
 """Which GPU results count as correct, derived from the arithmetic.
 
-The GPU computes in fp32 (block contributions accumulated in fp32, SiLU in
-fp32, one bf16 rounding at the end); the oracle computes the same method in
+The GPU computes in fp32 (block contributions accumulated in fp32, the GLU
+activation in fp32, one bf16 rounding at the end); the oracle computes the same method in
 fp64.  So a GPU output differs from the oracle's fp64 value by at most
 
   * the fp32 accumulation error of the down dot and the route sum,
@@ -44,8 +44,32 @@ def ulp_fp16(v):
     return np.exp2(np.maximum(ex.astype(np.float64) - 11.0, -24.0))
 
 
+def _act_slope_eval(g, kind):
+    """The GLU activation at g, |its derivative|, and a bound on the error of
+    its fp32 evaluation beyond a few relative roundings (which the caller
+    adds).  SiLU: g*sigmoid(g), derivative sig*(1 + g*(1 - sig)).  gelu_tanh:
+    0.5*g*(1 + tanh z), z = c0*(g + c1*g^3), derivative
+    0.5*(1 + tanh z) + 0.5*g*(1 - tanh^2 z)*c0*(1 + 3*c1*g^2); z carries about
+    6 roundings, tanhf 2 ulp, so the evaluation error is at most
+    0.5*|g|*(6u*|z|*(1 - tanh^2 z) + 4u) plus a few roundings of the value
+    (doubled below)."""
+    if kind == 1:
+        c0, c1 = np.sqrt(2.0 / np.pi), 0.044715
+        with np.errstate(over="ignore", invalid="ignore"):
+            z = c0 * (g + c1 * g ** 3)
+            th = np.tanh(z)
+            sech2 = 1.0 - th * th
+            act = 0.5 * g * (1.0 + th)
+            slope = np.abs(0.5 * (1.0 + th) + 0.5 * g * sech2 * c0 * (1.0 + 3.0 * c1 * g * g))
+            ev = U32 * (np.abs(g) * (6.0 * np.abs(z) * sech2 + 4.0) + 6.0 * np.abs(act))
+        return act, slope, np.nan_to_num(ev)
+    with np.errstate(over="ignore"):
+        sig = 1.0 / (1.0 + np.exp(-g))
+    return g * sig, np.abs(sig * (1.0 + g * (1.0 - sig))), np.zeros_like(g)
+
+
 def _inter_error(geom, st, t, k, xh, wgu):
-    """fp32 error bound of the intermediate silu(g)*u of route (t, k)."""
+    """fp32 error bound of the intermediate act(g)*u of route (t, k)."""
     I = geom.I
     e = int(st["ids"][t, k])
     sg, su = abs(st["scales"][e, 0]), abs(st["scales"][e, 1])
@@ -55,12 +79,10 @@ def _inter_error(geom, st, t, k, xh, wgu):
     Su = su * (np.abs(wgu[I:]) @ np.abs(xh))
     nblk = geom.H // 32
     eps_h = 2.0 * (nblk + 40) * U32             # per-lane sequential sums, warp tree, scale products
-    with np.errstate(over="ignore"):
-        sig = 1.0 / (1.0 + np.exp(-g))
-    silu = g * sig
-    dsilu = np.abs(sig * (1.0 + g * (1.0 - sig)))
-    a = silu * u
-    return dsilu * np.abs(u) * eps_h * Sg + np.abs(silu) * eps_h * Su + 16 * U32 * np.abs(a) + 1e-30
+    act, dact, ev = _act_slope_eval(g, getattr(geom, "glu", 0))
+    a = act * u
+    return (dact * np.abs(u) * eps_h * Sg + np.abs(act) * eps_h * Su + ev * np.abs(u) + 16 * U32 * np.abs(a)
+            + 1e-30)
 
 
 def output_bounds(geom, st):
