@@ -343,6 +343,69 @@ def bench_prefill(dev, steps, warmup, mode, bf16_peak):
             "launches_per_chunk": 5}
 
 
+def bench_linear(dev, steps, warmup, hbm_peak):
+    """moe_linear on NVFP4 rows with per-row scales: 48 fused qkv projections
+    of the headline layer shape (H=2048; q 4096 + k 512 + v 512 rows each,
+    5.9 MB of rows per layer, 283 MB in all, beyond L2) as 48 launches
+    replayed from one CUDA graph, and the same rows as one launch of
+    245,760 rows.  T = 1 and 8; algorithmic bytes = rows + scales + x + out."""
+    import torch
+
+    from quantized_routed_expert_route_gb300 import capi
+    from synth import banks as S
+    from synth import counter as C
+    NL, N, K = 48, 5120, 2048
+    rb = row_bytes(NVFP4, K)
+    rows = torch.empty(NL * N * rb + 16, dtype=torch.uint8, device=dev)
+    C.fill_bank_torch(rows[: NL * N * rb], 5001, NVFP4, K)
+    rs = torch.from_numpy(S.rng(5002).uniform(0.1, 2.0, size=NL * N).astype(np.float32)).to(dev)
+    res = {"workload": "NVFP4 fused qkv rows, H=2048, N=5120 per layer, 48 layers (283 MB), per-row scales"}
+    for T in (1, 8):
+        x = torch.from_numpy(S.hidden_bf16(5003 + T, T, K).view(np.int16)).to(dev)
+        out = torch.empty((NL, T, N), dtype=torch.int16, device=dev)
+        big = torch.empty((T, NL * N), dtype=torch.int16, device=dev)
+        err = torch.zeros(1, dtype=torch.int32, device=dev)
+        st = torch.cuda.Stream(device=dev)
+
+        def layers(sp):
+            for l in range(NL):
+                capi.moe_linear(NVFP4, rows.data_ptr() + l * N * rb, N, K, rs.data_ptr() + 4 * l * N, x.data_ptr(),
+                                T, out[l].data_ptr(), err.data_ptr(), sp)
+
+        def one(sp):
+            capi.moe_linear(NVFP4, rows.data_ptr(), NL * N, K, rs.data_ptr(), x.data_ptr(), T, big.data_ptr(),
+                            err.data_ptr(), sp)
+
+        with torch.cuda.stream(st):
+            layers(st.cuda_stream)
+            one(st.cuda_stream)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=st):
+                layers(st.cuda_stream)
+        torch.cuda.synchronize()
+        row = {}
+        for name, fn, nlaunch in (("48_layer_graph", lambda: g.replay(), NL),
+                                  ("one_launch", lambda: one(st.cuda_stream), 1)):
+            with torch.cuda.stream(st):
+                for _ in range(warmup):
+                    fn()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(st)
+                for _ in range(steps):
+                    fn()
+                e1.record(st)
+            e1.synchronize()
+            ms = e0.elapsed_time(e1) / steps
+            nbytes = NL * N * (rb + 4) + nlaunch * T * K * 2 + NL * N * T * 2   # rows + scales, x per launch, out
+            gbs = nbytes / (ms / 1e3) / 1e9
+            row[name] = {"us_per_step": ms * 1e3, "us_per_launch": ms * 1e3 / nlaunch, "hbm_gbs": gbs,
+                         "frac": gbs / hbm_peak, "launches": nlaunch}
+        row["device_error_bits"] = int(err.item())
+        res[f"T={T}"] = row
+        del g
+    return res
+
+
 # ------------------------------------------------------------------ CPU oracle timing
 
 def cpu_oracle_worker(seconds: float, seed: int = 0) -> dict:
@@ -450,6 +513,7 @@ def main():
     ap.add_argument("--no-stack", action="store_true", help="skip the 47-layer Laguna sweep")
     ap.add_argument("--no-prefill", action="store_true", help="skip the prompt-path chunk")
     ap.add_argument("--no-types", action="store_true", help="skip the per-GGUF-type layer stacks")
+    ap.add_argument("--no-linear", action="store_true", help="skip the dense NVFP4 linear")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--cpu-oracle-worker", type=float, default=None, help=argparse.SUPPRESS)
     ap.add_argument("--profile-layer", choices=["nvfp4", "q4_k", "bf16", "q4_k_m", "q6_k", "q4_0"], default=None,
@@ -565,6 +629,10 @@ def main():
             types[f"{TYPE_NAMES[gu_t]}+{TYPE_NAMES[dn_t]}"] = row
         extra["gguf_types_24_layer_stack"] = {
             "workload": "H=2048 I=768 E=128 top-8, softmax routing, 24 resident layer banks per step", **types}
+
+    if not a.no_linear:
+        extra["dense_linear_nvfp4"] = bench_linear(dev, max(10, min(100, a.steps // 4)), a.warmup, hbm_peak)
+        torch.cuda.empty_cache()
 
     if not a.no_prefill:
         pk, pk_kind = bf16_peak()

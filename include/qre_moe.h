@@ -87,7 +87,8 @@ enum {
 enum {
   MOE_MAX_E = 1024,        /* experts per layer */
   MOE_MAX_TOPK = 32,       /* routes per token */
-  MOE_DECODE_T_CHUNK = 64  /* tokens per internal decode pass (larger T is split) */
+  MOE_DECODE_T_CHUNK = 64, /* tokens per internal decode pass (larger T is split) */
+  MOE_LINEAR_MAX_T = 8     /* tokens per moe_linear call */
 };
 
 /* The GLU of the layer, glu(g, u) = act(g) * u (FreeToken PR #732, "Design":
@@ -314,6 +315,32 @@ int moe_debug_prefill_stages(const moe_bank* bank, const void* x, int32_t T,
                              const int32_t* topk_ids, const float* topk_w, int32_t mode,
                              void* out, void* ws, size_t ws_bytes, void* stream,
                              void* xq, int32_t* off, int32_t* perm, void* i16);
+
+/* Dense quantized linear with a per-output-row scale in its epilogue:
+ *   out[t, n] = bf16(row_scale[n] * sum_k W[n, k] * q8_1(x[t])[k])
+ * for t < T, n < N (FreeToken PR #732, "Design": a dense linear multiplies
+ * its matmul result by its scale; a fused module of several tensors, e.g.
+ * qkv or gate_up, carries ggml_scale, one fp32 value per output row, each
+ * part's scale or 1).  x is quantized to q8_1 per 32 values inside the call
+ * (the decode path's prep_input), each 32-value block's integer dot is exact,
+ * the block scales and row_scale are applied in fp32, and the output is
+ * rounded once to bf16 (ties to even).
+ *   type:      MOE_NVFP4, MOE_Q4_K, MOE_Q8_0, MOE_Q6_K or MOE_Q4_0 (MOE_BF16 is
+ *              MOE_EUNSUPPORTED); an NVFP4 tensor's weight_scale_2 goes into
+ *              row_scale
+ *   rows:      device, N rows of moe_row_bytes(type, K) bytes back to back,
+ *              16-byte aligned and readable up to the next 16-byte boundary
+ *              past the last row
+ *   row_scale: device fp32 [N], or NULL for ones
+ *   x:         device bf16 [T][K], 16-byte aligned; out: device bf16 [T][N]
+ *   T:         1..MOE_LINEAR_MAX_T; T = 0 is a no-op
+ *   dev_err:   device uint32 or NULL; OR-ed with MOE_DEVERR_TIMEOUT if a
+ *              bounded wait ran out
+ * Asynchronous on `stream`; allocates nothing.  Errors: MOE_EINVAL (null
+ * pointer, alignment, sizes), MOE_EUNSUPPORTED (type, or T*K too large for
+ * the activations to stay in shared memory: about 150 K values), MOE_ECUDA. */
+int moe_linear(int32_t type, const void* rows, int32_t N, int32_t K, const float* row_scale,
+               const void* x, int32_t T, void* out, uint32_t* dev_err, void* stream);
 
 /* Tensor-core check: D[128, N] = A[128, K] * B[N, K]^T with fp16 A and B
  * (device, row-major), fp32 D (device, row-major), computed with the tcgen05

@@ -16,7 +16,7 @@ MOE_BF16, MOE_Q8_0, MOE_Q4_K, MOE_NVFP4, MOE_Q6_K, MOE_Q4_0 = 0, 1, 2, 3, 4, 5
 MOE_OK, MOE_EINVAL, MOE_EUNSUPPORTED, MOE_ENOMEM, MOE_ECUDA, MOE_EDEVICE = 0, -1, -2, -3, -4, -5
 MOE_DEVERR_BAD_ID, MOE_DEVERR_TIMEOUT = 1, 2
 MOE_SRC_HOST, MOE_SRC_DEVICE, MOE_SRC_DEVICE_BORROW = 0, 1, 2
-MOE_MAX_E, MOE_MAX_TOPK, MOE_DECODE_T_CHUNK = 1024, 32, 64
+MOE_MAX_E, MOE_MAX_TOPK, MOE_DECODE_T_CHUNK, MOE_LINEAR_MAX_T = 1024, 32, 64, 8
 MOE_PREFILL_W4A4, MOE_PREFILL_W4A8 = 0, 1
 MOE_GLU_SILU, MOE_GLU_GELU_TANH = 0, 1
 MOE_NOALLOC_WS_BYTES = 4 << 20
@@ -29,6 +29,7 @@ EXPORTS = (
     "moe_debug_block_dots", "moe_debug_decode_stages", "moe_decode_noalloc", "moe_debug_tc_gemm",
     "moe_prefill_workspace_bytes", "moe_prefill_grouped", "moe_debug_prefill_stages",
     "moe_decode_kernel_count", "moe_decode_io_bytes", "moe_decode_io_offsets", "moe_decode_host",
+    "moe_linear",
 )
 
 
@@ -72,6 +73,7 @@ def _load() -> ctypes.CDLL:
         "moe_debug_decode_stages": (ctypes.c_int, [vp, vp, i32, vp, vp, vp, vp, sz, vp, vp, vp, vp]),
         "moe_decode_noalloc": (ctypes.c_int, [vp, vp, i32, vp, vp, vp, vp]),
         "moe_debug_tc_gemm": (ctypes.c_int, [vp, vp, i32, i32, vp, vp, vp]),
+        "moe_linear": (ctypes.c_int, [i32, vp, i32, i32, vp, vp, i32, vp, vp, vp]),
         "moe_prefill_workspace_bytes": (sz, [vp, i32, i32]),
         "moe_decode_kernel_count": (ctypes.c_int, [vp, i32]),
         "moe_decode_io_bytes": (sz, [vp, i32]),
@@ -176,6 +178,13 @@ def moe_debug_decode_stages(bank: int, x: int, T: int, topk_ids: int, topk_w: in
     _check(_lib.moe_debug_decode_stages(bank, x, T, topk_ids, topk_w, out, ws, ws_bytes, stream or None,
                                         x_blocks or None, inter or None, inter_blocks or None),
            "moe_debug_decode_stages")
+
+
+def moe_linear(wtype: int, rows: int, N: int, K: int, row_scale: int | None, x: int, T: int, out: int,
+               dev_err: int | None = None, stream: int = 0) -> None:
+    """out[T, N] (bf16) = row_scale * (q8_1(x[T, K]) @ W[N, K]^T) for quantized rows W."""
+    _check(_lib.moe_linear(wtype, rows, N, K, row_scale or None, x, T, out, dev_err or None, stream or None),
+           "moe_linear")
 
 
 def moe_debug_tc_gemm(A: int, B: int, K: int, N: int, D: int, dev_err: int, stream: int = 0) -> None:

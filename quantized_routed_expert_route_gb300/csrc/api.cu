@@ -853,6 +853,31 @@ int moe_debug_prefill_stages(const moe_bank* b, const void* x, int32_t T, const 
   return e == cudaSuccess ? MOE_OK : cuda_fail(e, "prefill debug export");
 }
 
+int moe_linear(int32_t type, const void* rows, int32_t N, int32_t K, const float* row_scale, const void* x,
+               int32_t T, void* out, uint32_t* dev_err, void* stream) {
+  if (T == 0) return MOE_OK;
+  if (!rows || !x || !out || N < 1 || K < 32 || T < 0) return MOE_EINVAL;
+  if (type < MOE_BF16 || type > MOE_Q4_0) return MOE_EINVAL;
+  if (type == MOE_BF16) return MOE_EUNSUPPORTED;
+  if (T > MOE_LINEAR_MAX_T) return MOE_EUNSUPPORTED;
+  const int rb = row_bytes_of(type, K);
+  if (rb == 0) return MOE_EINVAL;
+  if (!aligned(rows, 16) || !aligned(x, 16) || !aligned(out, 2) || (row_scale && !aligned(row_scale, 4)) ||
+      (dev_err && !aligned(dev_err, 4)))
+    return MOE_EINVAL;
+  LinParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.type = type; p.N = N; p.K = K; p.T = T; p.rb = rb;
+  p.rows = static_cast<const uint8_t*>(rows);
+  p.row_scale = row_scale;
+  p.x = static_cast<const uint16_t*>(x);
+  p.out = static_cast<uint16_t*>(out);
+  p.err = dev_err;
+  if (!plan_linear(p)) return MOE_EUNSUPPORTED;
+  cudaError_t e = launch_linear(p, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MOE_OK : cuda_fail(e, "linear");
+}
+
 int moe_debug_tc_gemm(const void* A, const void* B, int32_t K, int32_t N, float* D, int32_t* dev_err,
                       void* stream) {
   if (!A || !B || !D || !dev_err || K <= 0 || K % 64 != 0 || N < 16 || N > 256 || N % 16 != 0) return MOE_EINVAL;

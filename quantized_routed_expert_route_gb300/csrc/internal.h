@@ -179,6 +179,22 @@ cudaError_t launch_tc_gemm_check(const uint16_t* A, const uint16_t* B, int K, in
 cudaError_t launch_export_q8(const int8_t* q, const float* d, const uint16_t* s, int64_t nblocks,
                              uint8_t* out, cudaStream_t stream);
 
+// Dense quantized linear with per-output-row scales (linear.cu).
+constexpr int kLinearMaxT = 8;
+struct LinParams {
+  int type;                 // WType of the rows (a quantized type)
+  int N, K, T, rb;          // rows, values per row, tokens, bytes per row
+  const uint8_t* rows;      // [N][rb]
+  const float* row_scale;   // [N] or null (ones)
+  const uint16_t* x;        // bf16 [T][K]
+  uint16_t* out;            // bf16 [T][N]
+  uint32_t* err;            // error word (kErrTimeout) or null
+  int rps, stage_bytes, nstage, act_bytes, grid;   // launch plan (plan_linear)
+};
+bool plan_linear(LinParams& p);
+size_t linear_smem_bytes(const LinParams& p);
+cudaError_t launch_linear(const LinParams& p, cudaStream_t stream);
+
 int sm_count();
 
 }  // namespace qre
