@@ -139,6 +139,12 @@ def _act_in(kind: str, wtype: int, v32: np.ndarray) -> tuple[np.ndarray, dict]:
     if kind == "nvfp4":
         codes, scl = quantize_nvfp4_act(v32)
         return dequantize_nvfp4_act(codes, scl), {"codes": codes, "scales": scl}
+    if kind == "fp16":
+        # the FP16 prompt mode: no quantization, one IEEE rounding to fp16
+        # (nearest even; beyond 65504 the value overflows to infinity)
+        with np.errstate(over="ignore"):
+            h = np.asarray(v32, dtype=np.float32).astype(np.float16)
+        return h.astype(np.float64), {"f16": h}
     raise ValueError(kind)
 
 
@@ -150,7 +156,10 @@ def moe_layer(geom: Geometry, gate_up, down, scale_bank, x_bf16_bits, topk_ids, 
     scale_bank: fp32 [E, 4] or None (all ones); gate_up / down: the compact
     banks as uint8 arrays ([E, 2I, row_bytes] and [E, H, row_bytes]), or
     mappings from expert id to that expert's rows.
-    act_kind: "q8_1" (decode and the W4A8 prompt path) or "nvfp4" (W4A4).
+    act_kind: "q8_1" (decode and the W4A8 prompt path), "nvfp4" (W4A4) or
+    "fp16" (the FP16 prompt mode: x and the fp32 intermediate rounded to fp16,
+    not quantized; Strata PR #292, "Summary/Pipeline", lists W4A8, W4A4 and
+    FP16 prompt modes).
 
     Returns (out_f64 [T, H], out_bf16_bits [T, H], stages dict or None)."""
     g = geom

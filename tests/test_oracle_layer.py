@@ -125,6 +125,37 @@ def test_unit_scale_bf16_gelu_layer_against_exact_gelu():
         assert np.abs(silu_out[t] - ref).max() > 10 * bound.max()   # the kind is honoured
 
 
+def test_fp16_prompt_mode_is_the_unquantized_layer_up_to_fp16_rounding():
+    """In the FP16 mode x (bf16) is exact in fp16 and only the intermediate
+    is rounded (relative error <= 2^-11 in the normal range), so the output
+    differs from the unquantized layer by at most
+    s_down * w * |Wd| @ ((2^-11 + 2^-23) |a| + 2^-25) (the fp32 cast of the
+    intermediate comes first), and does differ."""
+    H, I, E, K, T = 256, 256, 6, 2, 3
+    gu, dn, sb = S.converted_layer(21, H, I, E, S.NVFP4, S.NVFP4)
+    x = S.hidden_bf16(22, T, H)
+    ids, w = S.softmax_topk_routing(23, T, E, K)
+    geom = L.Geometry(H, I, E, K, F.TYPE_NVFP4, F.TYPE_NVFP4)
+    out, _, st = L.moe_layer(geom, gu, dn, sb, x, ids, w, act_kind="fp16", stages=True)
+    xt = F.bf16_bits_to_f64(x).reshape(T, H)
+    assert np.array_equal(st["x_hat"], xt)
+    for t in range(T):
+        want = np.zeros(H)
+        bound = np.zeros(H)
+        for k in range(K):
+            e = int(ids[t, k])
+            Wgu = F.dequantize_rows(F.TYPE_NVFP4, gu[e], H)
+            Wd = F.dequantize_rows(F.TYPE_NVFP4, dn[e], I)
+            h = Wgu @ xt[t]
+            g, u = h[:I] * float(sb[e, 0]), h[I:] * float(sb[e, 1])
+            a = g / (1.0 + np.exp(-g)) * u
+            f = float(sb[e, 2]) * float(w[t, k])
+            want += (Wd @ a) * f
+            bound += abs(f) * (np.abs(Wd) @ ((2.0 ** -11 + 2.0 ** -23) * np.abs(a) + 2.0 ** -25))
+        assert (np.abs(out[t] - want) <= bound * (1 + 1e-9) + 1e-300).all()
+        assert np.abs(out[t] - want).max() > 0
+
+
 def test_layer_invariants():
     geom, gu, dn, sb, x, ids, w = _tiny(seed=3, T=3)
     base, _, _ = L.moe_layer(geom, gu, dn, sb, x, ids, w)
