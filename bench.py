@@ -336,7 +336,7 @@ def bench_prefill(dev, steps, warmup, mode, bf16_peak):
     err = capi.moe_get_error(ws.data_ptr(), wsb, stream)
     capi.moe_bank_destroy(bank)
     tflops = prefill_flops(c) / (ms / 1e3) / 1e12
-    return {"mode": "W4A4" if mode == 0 else "W4A8", "ms_per_chunk": ms, "tok_per_s": T / (ms / 1e3),
+    return {"mode": {0: "W4A4", 1: "W4A8", 2: "FP16"}[mode], "ms_per_chunk": ms, "tok_per_s": T / (ms / 1e3),
             "tflops": tflops, "mma": "tcgen05 kind::f16 (exact fp16 operands, fp32 accumulation)",
             "frac_of_measured_bf16_peak": tflops / bf16_peak,
             "frac_of_nominal_fp4_peak": tflops / 13500.0, "device_error_bits": err,
@@ -477,6 +477,27 @@ def profile_layer(a):
     print(json.dumps({"profile_layer": a.profile_layer, "T": a.T, "layers": a.layers, "steps": a.steps}))
 
 
+def profile_linear(a):
+    """Eager one-launch dense NVFP4 linears (the bench's 283 MB of rows) for a profiler."""
+    import torch
+
+    from quantized_routed_expert_route_gb300 import capi
+    from synth import counter as C
+    dev = "cuda:0"
+    N, K = 48 * 5120, 2048
+    rb = row_bytes(NVFP4, K)
+    rows = torch.empty(N * rb + 16, dtype=torch.uint8, device=dev)
+    C.fill_bank_torch(rows[: N * rb], 5001, NVFP4, K)
+    rs = torch.ones(N, dtype=torch.float32, device=dev)
+    x = torch.zeros((a.T, K), dtype=torch.int16, device=dev)
+    out = torch.empty((a.T, N), dtype=torch.int16, device=dev)
+    s = torch.cuda.current_stream().cuda_stream
+    for _ in range(a.steps):
+        capi.moe_linear(NVFP4, rows.data_ptr(), N, K, rs.data_ptr(), x.data_ptr(), a.T, out.data_ptr(), None, s)
+    torch.cuda.synchronize()
+    print(json.dumps({"profile_linear": True, "T": a.T, "steps": a.steps}))
+
+
 # ------------------------------------------------------------------ main
 
 def job_throughput(ms_local, units_per_rank, world, device):
@@ -514,6 +535,8 @@ def main():
     ap.add_argument("--no-prefill", action="store_true", help="skip the prompt-path chunk")
     ap.add_argument("--no-types", action="store_true", help="skip the per-GGUF-type layer stacks")
     ap.add_argument("--no-linear", action="store_true", help="skip the dense NVFP4 linear")
+    ap.add_argument("--profile-linear", action="store_true",
+                    help="run --steps one-launch dense NVFP4 linears (245,760 x 2048, T=--T) for ncu")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--cpu-oracle-worker", type=float, default=None, help=argparse.SUPPRESS)
     ap.add_argument("--profile-layer", choices=["nvfp4", "q4_k", "bf16", "q4_k_m", "q6_k", "q4_0"], default=None,
@@ -521,7 +544,7 @@ def main():
     ap.add_argument("--T", type=int, default=1)
     ap.add_argument("--experts", type=int, default=0,
                     help="with --profile-layer q4_k/bf16: experts per layer (default 256), to shrink a capture")
-    ap.add_argument("--profile-prefill", choices=["w4a4", "w4a8"], default=None,
+    ap.add_argument("--profile-prefill", choices=["w4a4", "w4a8", "fp16"], default=None,
                     help="run --steps prompt-path chunks (for ncu), print nothing else")
     a = ap.parse_args()
 
@@ -530,10 +553,13 @@ def main():
         return
     if a.profile_prefill:
         import torch
-        r = bench_prefill("cuda:0", a.steps, 1, 0 if a.profile_prefill == "w4a4" else 1, bf16_peak()[0])
+        r = bench_prefill("cuda:0", a.steps, 1, {"w4a4": 0, "w4a8": 1, "fp16": 2}[a.profile_prefill], bf16_peak()[0])
         print(json.dumps(r))
         return
 
+    if a.profile_linear:
+        profile_linear(a)
+        return
     if a.cpu_oracle_worker is not None:
         print(json.dumps(cpu_oracle_worker(a.cpu_oracle_worker)))
         return
@@ -640,7 +666,8 @@ def main():
             "workload": "nvfp4 layer H=2048 I=768 E=128 top-8, 4096 tokens (32768 routed rows)",
             "peak_tflops": pk, "peak_kind": pk_kind, "gflop_per_chunk": prefill_flops(PREFILL) / 1e9,
             "w4a4": bench_prefill(dev, max(3, min(20, a.steps // 20)), a.warmup, 0, pk),
-            "w4a8": bench_prefill(dev, max(3, min(20, a.steps // 20)), a.warmup, 1, pk)}
+            "w4a8": bench_prefill(dev, max(3, min(20, a.steps // 20)), a.warmup, 1, pk),
+            "fp16": bench_prefill(dev, max(3, min(20, a.steps // 20)), a.warmup, 2, pk)}
         torch.cuda.empty_cache()
 
     cpu = run_cpu_baseline(a.cpu_seconds) if (rank == 0 and a.cpu_seconds > 0) else None

@@ -206,10 +206,11 @@ int moe_decode_noalloc(const moe_bank* bank, const void* x, int32_t T,
 
 /* ---------------------------------------------------------------- prompt path
  * Grouped expert GEMMs for a prompt chunk (Strata PR #292, "Summary/Pipeline":
- * the prompt path, W4A4 with activations quantized to NVFP4 on the fly, or
- * W4A8 with q8_1 activations).  NVFP4 gate_up and down banks only, H and I
- * multiples of 256; other banks return MOE_EUNSUPPORTED. */
-enum { MOE_PREFILL_W4A4 = 0, MOE_PREFILL_W4A8 = 1 };
+ * the prompt path, W4A8 with q8_1 activations, W4A4 with activations
+ * quantized to NVFP4 on the fly, or FP16 with activations kept in fp16).
+ * NVFP4 gate_up and down banks only, H and I multiples of 256; other banks
+ * return MOE_EUNSUPPORTED. */
+enum { MOE_PREFILL_W4A4 = 0, MOE_PREFILL_W4A8 = 1, MOE_PREFILL_FP16 = 2 };
 
 /* Workspace bytes moe_prefill_grouped needs for T tokens in `mode`; 0 if the
  * bank or mode is unsupported or T < 1. */
@@ -220,10 +221,11 @@ size_t moe_prefill_workspace_bytes(const moe_bank* bank, int32_t T, int32_t mode
  * path's activation quantization.  Steps: routes sorted by expert (stable);
  * x quantized per token (W4A4: per 16 values a UE4M3 scale = amax/6 and E2M1
  * codes, both rounded to nearest even with saturation, global scale 1; W4A8:
- * the q8_1 rule of the decode path); a grouped gate_up GEMM on the tensor
- * cores over the exactly dequantized operands (fp16 values, fp32
- * accumulation) with s_gate, s_up and SiLU-GLU in an fp32 epilogue that
- * requantizes the intermediate the same way as x; a grouped down GEMM whose
+ * the q8_1 rule of the decode path; FP16: x rounded to fp16, nearest even);
+ * a grouped gate_up GEMM on the tensor cores over the exactly dequantized
+ * operands (fp16 values, fp32 accumulation) with s_gate, s_up and the GLU in
+ * an fp32 epilogue that requantizes the intermediate the same way as x (FP16:
+ * rounds it to fp16); a grouped down GEMM whose
  * epilogue scales by s_down * routing weight; a sum over k = 0..K-1 in order.
  * x: bf16 [T, H] (device, 16-byte aligned); topk_ids int32 and topk_w fp32
  * [T, K] (device); out bf16 [T, H] (device, 8-byte aligned); ws: device,

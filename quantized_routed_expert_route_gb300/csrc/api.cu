@@ -772,7 +772,8 @@ PfLayout pf_layout(const moe_layer_geom& g, int64_t T, int mode) {
   L.off = o; o = align_up(o + 4 * ((size_t)g.E + 1), A);
   L.perm = o; o = align_up(o + 4 * RT, A);
   L.xq = o;
-  o = align_up(o + (mode == PF_W4A4 ? (size_t)T * (g.H / 2 + g.H / 16) : (size_t)T * (g.H / 32) * 36), A);
+  o = align_up(o + (mode == PF_W4A4 ? (size_t)T * (g.H / 2 + g.H / 16)
+                    : mode == PF_W4A8 ? (size_t)T * (g.H / 32) * 36 : 0), A);
   L.x16 = o; o = align_up(o + 2 * (size_t)T * g.H, A);
   L.x16lo = o; o = align_up(o + (mode == PF_W4A8 ? 2 * (size_t)T * g.H : 0), A);
   L.i16 = o; o = align_up(o + 2 * RT * g.I, A);
@@ -782,7 +783,7 @@ PfLayout pf_layout(const moe_layer_geom& g, int64_t T, int mode) {
 }
 
 int pf_check(const moe_bank* b, int32_t mode) {
-  if (!b || (mode != PF_W4A4 && mode != PF_W4A8)) return MOE_EINVAL;
+  if (!b || (mode != PF_W4A4 && mode != PF_W4A8 && mode != PF_FP16)) return MOE_EINVAL;
   const moe_layer_geom& g = b->geom;
   if (g.gate_up_type != MOE_NVFP4 || g.down_type != MOE_NVFP4) return MOE_EUNSUPPORTED;
   if (g.H % 256 != 0 || g.I % 256 != 0) return MOE_EUNSUPPORTED;
@@ -845,8 +846,9 @@ int moe_debug_prefill_stages(const moe_bank* b, const void* x, int32_t T, const 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const size_t RT = (size_t)T * g.top_k;
   cudaError_t e = cudaSuccess;
-  const size_t xq_bytes = (mode == PF_W4A4) ? (size_t)T * (g.H / 2 + g.H / 16) : (size_t)T * (g.H / 32) * 36;
-  if (xq) e = cudaMemcpyAsync(xq, base + L.xq, xq_bytes, cudaMemcpyDeviceToDevice, s);
+  const size_t xq_bytes = (mode == PF_W4A4) ? (size_t)T * (g.H / 2 + g.H / 16)
+                          : (mode == PF_W4A8) ? (size_t)T * (g.H / 32) * 36 : 2 * (size_t)T * g.H;
+  if (xq) e = cudaMemcpyAsync(xq, base + (mode == PF_FP16 ? L.x16 : L.xq), xq_bytes, cudaMemcpyDeviceToDevice, s);
   if (e == cudaSuccess && off) e = cudaMemcpyAsync(off, base + L.off, 4 * ((size_t)g.E + 1), cudaMemcpyDeviceToDevice, s);
   if (e == cudaSuccess && perm) e = cudaMemcpyAsync(perm, base + L.perm, 4 * RT, cudaMemcpyDeviceToDevice, s);
   if (e == cudaSuccess && i16) e = cudaMemcpyAsync(i16, base + L.i16, 2 * RT * g.I, cudaMemcpyDeviceToDevice, s);

@@ -57,7 +57,7 @@ struct DecodeParams {
 
 // The prompt path (prefill.cu): routes sorted by expert, then two grouped
 // GEMMs on the tensor cores (gate_up, down) and a fixed-order combine.
-enum PfMode : int { PF_W4A4 = 0, PF_W4A8 = 1 };
+enum PfMode : int { PF_W4A4 = 0, PF_W4A8 = 1, PF_FP16 = 2 };
 struct PfParams {
   int H, I, E, K, T, RT;
   int glu;

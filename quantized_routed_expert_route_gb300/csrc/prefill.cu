@@ -12,7 +12,8 @@
 //                 16 values: UE4M3 scale = amax/6 nearest-even, E2M1 codes
 //                 nearest-even, global scale 1) or q8_1 -- and stored both as
 //                 codes and as fp16 operands: the exact dequantized NVFP4
-//                 values, or each q8_1 value q*d as an fp16 pair hi + lo.
+//                 values, or each q8_1 value q*d as an fp16 pair hi + lo.  The
+//                 FP16 mode quantizes nothing: x rounded to fp16 is the operand.
 //   k_pf_gemm<0>  P3: grouped gate_up GEMM.  A tile is (expert, 256 sorted
 //                 rows, 128 intermediate columns): 128 gate rows and 128 up
 //                 rows of the expert's NVFP4 bank are expanded to fp16
@@ -20,9 +21,10 @@
 //                 tiles, the rows' activations are gathered beside them, and
 //                 one thread issues tcgen05 kind::f16 MMAs into two 128x256
 //                 fp32 accumulators in tensor memory.  The epilogue applies
-//                 s_gate / s_up and SiLU-GLU in fp32, requantizes each 16 (or
+//                 s_gate / s_up and the GLU in fp32, requantizes each 16 (or
 //                 32) intermediate values to NVFP4 (or q8_1), and stores the
-//                 exact fp16 dequantized values.
+//                 exact fp16 dequantized values (the FP16 mode stores the
+//                 intermediate rounded to fp16).
 //   k_pf_gemm<1>  P4: grouped down GEMM, (expert, 256 rows, 256 outputs)
 //                 tiles over the requantized intermediate; the epilogue scales
 //                 by s_down * routing weight and stores fp32 per route.
@@ -183,9 +185,26 @@ __device__ __forceinline__ void q8_1_quant32_f16(const float (&v)[32], uint32_t 
   }
 }
 
-// One thread per 16 (W4A4) or 32 (W4A8) values of x.
+// One thread per 16 (W4A4) or 32 (W4A8, FP16) values of x.
 __global__ void k_pf_quant(const __grid_constant__ PfParams p) {
   const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (p.mode == PF_FP16) {
+    const int nb = p.H / 32;
+    if (idx >= (long long)p.T * nb) return;
+    const int t = (int)(idx / nb), b = (int)(idx - (long long)t * nb);
+    const uint4* src = reinterpret_cast<const uint4*>(p.x + (size_t)t * p.H + 32 * b);
+    uint4* dst = reinterpret_cast<uint4*>(p.x16 + (size_t)t * p.H + 32 * b);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float f[8];
+      bf16x8_to_f32(__ldg(src + i), f);
+      uint32_t h[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) h[j] = f32_to_f16_bits_rn(f[2 * j]) | (f32_to_f16_bits_rn(f[2 * j + 1]) << 16);
+      dst[i] = make_uint4(h[0], h[1], h[2], h[3]);
+    }
+    return;
+  }
   if (p.mode == PF_W4A4) {
     const int nb = p.H / 16;
     if (idx >= (long long)p.T * nb) return;
@@ -458,7 +477,16 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(const __grid_constant
         }
         if (valid) {
           uint4* dst = reinterpret_cast<uint4*>(p.i16 + (size_t)(srow0 + m) * p.I + nt * 128 + 32 * cg);
-          if (p.mode == PF_W4A4) {
+          if (p.mode == PF_FP16) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              uint32_t hw[4];
+#pragma unroll
+              for (int j = 0; j < 4; ++j)
+                hw[j] = f32_to_f16_bits_rn(a[8 * i + 2 * j]) | (f32_to_f16_bits_rn(a[8 * i + 2 * j + 1]) << 16);
+              dst[i] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+            }
+          } else if (p.mode == PF_W4A4) {
 #pragma unroll
             for (int b = 0; b < 2; ++b) {
               uint32_t sbyte, c0, c1, hw[8];

@@ -46,8 +46,8 @@ from oracle import layer as OL  # noqa: E402
 from tests import cases  # noqa: E402
 
 # The prompt configuration's tolerances (relative L2 of the bf16 output against
-# the oracle's bf16 output): 1e-2 for W4A4, 2e-3 for W4A8.
-TOL_L2 = {0: 1e-2, 1: 2e-3}
+# the oracle's bf16 output): 1e-2 for W4A4, 2e-3 for W4A8 and FP16.
+TOL_L2 = {0: 1e-2, 1: 2e-3, 2: 2e-3}
 
 
 def _stable_sort(ids, E):
@@ -62,6 +62,8 @@ def _stable_sort(ids, E):
 
 def _x_quantized(case, mode):
     x32 = F.bf16_bits_to_f64(case.x).astype(np.float32)
+    if mode == 2:   # the FP16 mode exports x rounded to fp16
+        return x32.astype(np.float16).view(np.uint8).reshape(-1)
     if mode == 0:
         codes, sc = OL.quantize_nvfp4_act(x32)
         packed = (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
@@ -118,7 +120,7 @@ def _ragged_ids(T, E, K, seed):
     return ids
 
 
-@pytest.mark.parametrize("mode", [0, 1])
+@pytest.mark.parametrize("mode", [0, 1, 2])
 def test_prefill_ragged_small(mode):
     """H=256 I=256 E=8 top-3, T=300: one expert with 300 rows (two tiles, the
     second partly filled), uneven others, an empty expert, a bad id."""
@@ -128,7 +130,7 @@ def test_prefill_ragged_small(mode):
     assert res["err"] & capi.MOE_DEVERR_BAD_ID
 
 
-@pytest.mark.parametrize("mode", [0, 1])
+@pytest.mark.parametrize("mode", [0, 1, 2])
 def test_prefill_ragged_small_gelu_tanh(mode):
     """The ragged small layer with the gelu_tanh GLU."""
     T, E, K = 300, 8, 3
@@ -136,7 +138,7 @@ def test_prefill_ragged_small_gelu_tanh(mode):
     _check_prefill(case, mode)
 
 
-@pytest.mark.parametrize("mode", [0, 1])
+@pytest.mark.parametrize("mode", [0, 1, 2])
 def test_prefill_qwen3_30b_a3b_shaped_chunk(mode):
     """H=2048 I=768 E=128 top-8, a 4096-token chunk (32768 routed rows); the
     oracle checks a sample of tokens, the sort and the quantized x in full."""
