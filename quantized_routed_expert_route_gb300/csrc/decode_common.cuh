@@ -560,12 +560,25 @@ __device__ __forceinline__ void accum_q_block(const uint8_t* row, int k, int b, 
     uint32_t pos[8], neg[8];
     float2 s;
     nvfp4_decode<WT == W_NVFP4>(row, k, b, pos, neg, s);
+    if constexpr (NTT >= 3) {
+      int w[8];
+      nvfp4_signed(pos, neg, w);
 #pragma unroll
-    for (int t = 0; t < NTT; ++t) {
-      if (NTT == 1 || t < nt) {
-        int d0, d1;
-        nvfp4_int_dots(pos, neg, a[t].q, d0, d1);
-        acc[t] += a[t].d * 0.5f * (s.x * (float)d0 + s.y * (float)d1);
+      for (int t = 0; t < NTT; ++t) {
+        if (t < nt) {
+          int d0, d1;
+          int_dots_halves(w, a[t].q, d0, d1);
+          acc[t] += a[t].d * 0.5f * (s.x * (float)d0 + s.y * (float)d1);
+        }
+      }
+    } else {
+#pragma unroll
+      for (int t = 0; t < NTT; ++t) {
+        if (NTT == 1 || t < nt) {
+          int d0, d1;
+          nvfp4_int_dots(pos, neg, a[t].q, d0, d1);
+          acc[t] += a[t].d * 0.5f * (s.x * (float)d0 + s.y * (float)d1);
+        }
       }
     }
   } else if constexpr (WT == W_Q4_K) {

@@ -209,6 +209,16 @@ __device__ __forceinline__ void nvfp4_decode(const uint8_t* row, int k, int b, u
   scales = ue4m3x2_to_float2(lds16(row + (k >> 1) + 2 * b));
 }
 
+// The same codes as signed bytes (2*value in -12..12): a negative code's
+// magnitude n becomes (0x80 - n) ^ 0x80 = 256 - n, computed on whole words
+// without borrows (n <= 12 < 0x80), and the positive and negative halves
+// are disjoint.  One dp4a per word and token instead of two: the cheaper
+// form once a decoded block is dotted with three or more tokens.
+__device__ __forceinline__ void nvfp4_signed(const uint32_t (&pos)[8], const uint32_t (&neg)[8], int (&w)[8]) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) w[i] = (int)(pos[i] | ((0x80808080u - neg[i]) ^ 0x80808080u));
+}
+
 // Integer dots of the two 16-value halves: sum((2*E2M1) * q).
 __device__ __forceinline__ void nvfp4_int_dots(const uint32_t (&pos)[8], const uint32_t (&neg)[8], const int (&q)[8],
                                                int& d0, int& d1) {
@@ -319,7 +329,8 @@ __device__ __forceinline__ void q6k_decode(const uint8_t* row, int b, int (&w)[8
   d = f16_bits_to_f32(lds16(sb + 208));
 }
 
-// Integer dots of the two 16-value halves of a decoded Q6_K sub-block.
+// Integer dots of the two 16-value halves of a decoded sub-block of signed
+// bytes (Q6_K, or NVFP4 through nvfp4_signed).
 __device__ __forceinline__ void int_dots_halves(const int (&w)[8], const int (&q)[8], int& d0, int& d1) {
   int a0 = 0, a1 = 0;
 #pragma unroll

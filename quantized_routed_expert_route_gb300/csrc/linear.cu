@@ -13,11 +13,11 @@
 // its producer warp streams the range through a ring of shared-memory slots
 // with 1-D TMA bulk copies (a slot holds whole rows, copied from the 16-byte
 // boundary at or below the first row), while 15 consumer warps quantize x to
-// q8_1 once into shared memory and then take the slot's rows, four per warp
-// and eight lanes per row: the lanes stride the 32-value blocks of the row,
-// each block's exact integer dot with every token's q8_1 block is scaled in
-// fp32 (the same block functions as the routed-expert path), a shuffle
-// reduction sums the eight lanes, and lane t writes token t's output.  Every wait is bounded in device time; on a
+// q8_1 once into shared memory and then take the slot's rows one per warp:
+// lanes stride the 32-value blocks of a row, each block's exact integer dot
+// with every token's q8_1 block is scaled in fp32 (the same block functions
+// as the routed-expert path), a warp reduction sums the lanes, and lane t
+// writes token t's output.  Every wait is bounded in device time; on a
 // timeout the CTA raises the error word and lets its copies in flight land.
 #include "decode_common.cuh"
 
@@ -29,9 +29,6 @@ constexpr int kLinConsumerWarps = 15;   // 16 warps in all: 4 per SM sub-partiti
 constexpr int kLinConsumers = 32 * kLinConsumerWarps;
 constexpr int kLinThreads = kLinConsumers + 32;           // + one TMA producer warp
 constexpr int kLinMaxStages = 8;
-constexpr int kLinLanesPerRow = 8;                          // = kLinearMaxT: lane t of a row writes token t
-constexpr int kLinRowsPerWarp = 32 / kLinLanesPerRow;
-static_assert(kLinLanesPerRow >= kLinearMaxT, "one lane per token writes a row's outputs");
 constexpr uint64_t kLinWaitNs = 2000000000ull;            // one wait gives up after 2 s of device time
 
 __device__ __forceinline__ bool lin_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
@@ -104,7 +101,6 @@ __global__ void __launch_bounds__(kLinThreads, 1) k_linear(const __grid_constant
 
   // ---------------- consumers: q8_1 of x, once, into shared memory
   const int T = p.T, K = p.K, nbk = K / 32;
-  const int grp = lane / kLinLanesPerRow, sl = lane % kLinLanesPerRow;
   int8_t* aq = reinterpret_cast<int8_t*>(lin_smem);
   float* ad = reinterpret_cast<float*>(lin_smem + (size_t)T * K);
   int* as = reinterpret_cast<int*>(ad + (size_t)T * nbk);
@@ -144,35 +140,30 @@ __global__ void __launch_bounds__(kLinThreads, 1) k_linear(const __grid_constant
     const int n = min(p.rps, r_end - r0);
     const uint8_t* src = p.rows + (size_t)r0 * p.rb;
     const uint8_t* base = ring + (size_t)s * p.stage_bytes + (src - align16_down(src));
-    // a warp takes 4 rows at a time, 8 lanes a row (lane group grp, lane sl)
-    for (int j0 = kLinRowsPerWarp * warp; j0 < n; j0 += kLinRowsPerWarp * kLinConsumerWarps) {
-      const int j = j0 + grp;
-      const bool valid = j < n;
-      const uint8_t* row = base + (size_t)(valid ? j : j0) * p.rb;
+    for (int j = warp; j < n; j += kLinConsumerWarps) {
+      const uint8_t* row = base + (size_t)j * p.rb;
       float acc[LT];
 #pragma unroll
       for (int t = 0; t < LT; ++t) acc[t] = 0.f;
-      if (valid) {
-        for (int b = sl; b < nbk; b += kLinLanesPerRow) {
-          ActQ8 a[LT];
+      for (int b = lane; b < nbk; b += 32) {
+        ActQ8 a[LT];
 #pragma unroll
-          for (int t = 0; t < LT; ++t)
-            if (LT == 1 || t < T) a[t] = act_block(act, t, b);
-          accum_q_block<WT, LT>(row, K, b, a, T, acc);
-        }
+        for (int t = 0; t < LT; ++t)
+          if (LT == 1 || t < T) a[t] = act_block(act, t, b);
+        accum_q_block<WT, LT>(row, K, b, a, T, acc);
       }
 #pragma unroll
       for (int t = 0; t < LT; ++t)
 #pragma unroll
-        for (int o = kLinLanesPerRow / 2; o > 0; o >>= 1) acc[t] += __shfl_xor_sync(0xffffffffu, acc[t], o);
+        for (int o = 16; o > 0; o >>= 1) acc[t] += __shfl_xor_sync(0xffffffffu, acc[t], o);
       float v = acc[0];
 #pragma unroll
       for (int t = 1; t < LT; ++t)
-        if (sl == t) v = acc[t];
-      if (valid && sl < T) {
+        if (lane == t) v = acc[t];
+      if (lane < T) {
         const int rn = r0 + j;
         const float rs = p.row_scale ? __ldg(p.row_scale + rn) : 1.0f;
-        p.out[(size_t)sl * p.N + rn] = (uint16_t)f32_to_bf16_bits_rn(v * rs);
+        p.out[(size_t)lane * p.N + rn] = (uint16_t)f32_to_bf16_bits_rn(v * rs);
       }
     }
     mbar_arrive(&empty_bar[s]);
