@@ -245,14 +245,12 @@ __device__ __forceinline__ void qb_chunk_nvfp4(const uint8_t* ca, const uint8_t*
 #pragma unroll
   for (int jj = 0; jj < 2; ++jj) {
     const int j = 2 * q + jj;
-    int wa[8], wb[8];
-    {
-      uint32_t pa[8], na[8], pb[8], nb[8];
-      nvfp4_words(lds128(ca + tc::sw128_chunk(u, j)), pa, na);
-      nvfp4_words(lds128(cb + tc::sw128_chunk(u, j)), pb, nb);
-      nvfp4_signed(pa, na, wa);
-      nvfp4_signed(pb, nb, wb);
-    }
+    // sign-split words (two dp4a per word and token): most tiles of a
+    // decode batch hold one or two tokens, where this beats converting the
+    // words to signed bytes first (measured on the T=8 layer)
+    uint32_t pa[8], na[8], pb[8], nb[8];
+    nvfp4_words(lds128(ca + tc::sw128_chunk(u, j)), pa, na);
+    nvfp4_words(lds128(cb + tc::sw128_chunk(u, j)), pb, nb);
     const float2 fa = ue4m3x2_to_float2((uint16_t)(swa >> (16 * jj)));
     const float2 fb = ue4m3x2_to_float2((uint16_t)(swb >> (16 * jj)));
 #pragma unroll
@@ -263,8 +261,8 @@ __device__ __forceinline__ void qb_chunk_nvfp4(const uint8_t* ca, const uint8_t*
       const int qv[8] = {(int)q0.x, (int)q0.y, (int)q0.z, (int)q0.w, (int)q1.x, (int)q1.y, (int)q1.z, (int)q1.w};
       const float ad = *reinterpret_cast<const float*>(recs + t * REC_PITCH + 8 * j);
       int a0, a1, b0, b1;
-      int_dots_halves(wa, qv, a0, a1);
-      int_dots_halves(wb, qv, b0, b1);
+      nvfp4_int_dots(pa, na, qv, a0, a1);
+      nvfp4_int_dots(pb, nb, qv, b0, b1);
       acca[t] += ad * 0.5f * (fa.x * (float)a0 + fa.y * (float)a1);
       accb[t] += ad * 0.5f * (fb.x * (float)b0 + fb.y * (float)b1);
     }
