@@ -33,6 +33,16 @@ Formats and where they come from:
     checkpoint, and Q6_K in the synthetic type list); the bit layouts are the
     public GGUF ones, stated in prose at q6k_codes and q4_0_codes (the pages
     give neither), so GGUF byte compatibility is unpinned.
+  * Q4_1, Q5_0, Q5_1, Q5_K and MXFP4 -- the remaining types of the synthetic
+    list in FreeToken PR #704 ("Validation": Q4_1, Q5_1, Q4_K, Q5_0, Q6_K,
+    MXFP4, Q5_K rows).  32-value blocks: Q4_1 fp16 d, fp16 m, 16 code bytes,
+    value d*q + m; Q5_0 fp16 d, a 32-bit word of high bits, 16 code bytes,
+    value d*(q - 16); Q5_1 fp16 d, fp16 m, the high-bit word, 16 code
+    bytes, value d*q + m; MXFP4 one E8M0 byte e then 16 code bytes of E2M1,
+    value E2M1(code) * 2^(e - 127).  Q5_K: 256 values in 176 bytes, the Q4_K
+    header (d, dmin, 12 packed scale bytes), 32 bytes of high bits, 128 code
+    bytes; value d*sc_j*q - dmin*m_j with 5-bit q.  Public GGUF layouts,
+    stated in prose at each decoder; GGUF byte compatibility is unpinned.
 
 Pins (tests/test_oracle_formats.py): UE4M3 against torch's float8_e4m3fn
 decoder over all 127 finite codes; E2M1 against the same decoder through the
@@ -51,8 +61,10 @@ QK_K = 256        # Q4_K super-block length
 NVFP4_GROUP = 16  # values per UE4M3 scale
 
 TYPE_BF16, TYPE_Q8_0, TYPE_Q4_K, TYPE_NVFP4, TYPE_Q6_K, TYPE_Q4_0 = 0, 1, 2, 3, 4, 5
+TYPE_Q4_1, TYPE_Q5_0, TYPE_Q5_1, TYPE_Q5_K, TYPE_MXFP4 = 6, 7, 8, 9, 10
 TYPE_NAMES = {TYPE_BF16: "bf16", TYPE_Q8_0: "q8_0", TYPE_Q4_K: "q4_k", TYPE_NVFP4: "nvfp4", TYPE_Q6_K: "q6_k",
-              TYPE_Q4_0: "q4_0"}
+              TYPE_Q4_0: "q4_0", TYPE_Q4_1: "q4_1", TYPE_Q5_0: "q5_0", TYPE_Q5_1: "q5_1", TYPE_Q5_K: "q5_k",
+              TYPE_MXFP4: "mxfp4"}
 
 Q8_1_BLOCK_BYTES = 36   # fp16 d, fp16 s, 32 int8
 
@@ -73,6 +85,11 @@ def row_bytes(wtype: int, k: int) -> int:
         return (k // 256) * 210 if k % 256 == 0 else 0
     if wtype == TYPE_Q4_0:
         return (k // 32) * 18 if k % 32 == 0 else 0
+    per32 = {TYPE_Q4_1: 20, TYPE_Q5_0: 22, TYPE_Q5_1: 24, TYPE_MXFP4: 17}
+    if wtype in per32:
+        return (k // 32) * per32[wtype] if k % 32 == 0 else 0
+    if wtype == TYPE_Q5_K:
+        return (k // 256) * 176 if k % 256 == 0 else 0
     return 0
 
 
@@ -272,6 +289,42 @@ def q4_0_codes(blk18) -> np.ndarray:
     return np.concatenate([b & 0x0F, b >> 4], axis=-1) - 8
 
 
+def nibble_split_codes(qs16) -> np.ndarray:
+    """The 32 4-bit codes of a block's 16 code bytes in value order: value j
+    < 16 is the low nibble of byte j, value j + 16 its high nibble (Q4_0,
+    Q4_1, Q5_0, Q5_1, MXFP4)."""
+    b = np.asarray(qs16, dtype=np.int64)
+    return np.concatenate([b & 0x0F, b >> 4], axis=-1)
+
+
+def q5_high_bits(qh4) -> np.ndarray:
+    """The 32 high bits of a Q5_0 / Q5_1 block: bit j of the little-endian
+    32-bit word qh is the fifth bit (value 16) of value j's code."""
+    b = np.asarray(qh4, dtype=np.int64)
+    word = b[..., 0] | (b[..., 1] << 8) | (b[..., 2] << 16) | (b[..., 3] << 24)
+    return (word[..., None] >> np.arange(32)) & 1
+
+
+def q5k_codes(sb176) -> np.ndarray:
+    """The 256 5-bit codes of Q5_K super-blocks in value order: the low 4
+    bits as in Q4_K (code byte l of chunk c: sub-block 2c in the low nibble,
+    2c+1 in the high nibble), the fifth bit of value l of sub-block j is bit
+    j of high-bit byte l."""
+    b = np.asarray(sb176, dtype=np.int64)
+    lo = q4k_codes(b[..., 48:176]).reshape(b.shape[:-1] + (8, 32))
+    qh = b[..., 16:48]                                        # [..., 32]
+    hi = (qh[..., None, :] >> np.arange(8)[:, None]) & 1      # [..., 8 sub-blocks, 32]
+    return (lo | (hi << 4)).reshape(b.shape[:-1] + (256,))
+
+
+def e8m0_value(e) -> np.ndarray:
+    """E8M0 (the MXFP4 block scale): 2^(e - 127) for e = 0..254; 255 is not a
+    finite scale (NaN in the microscaling formats) and is kept out of banks."""
+    e = np.asarray(e, dtype=np.int64)
+    assert (e < 255).all()
+    return np.ldexp(1.0, e - 127)
+
+
 def dequantize_rows(wtype: int, rows, k: int) -> np.ndarray:
     """Decode bank rows (uint8 [R, row_bytes(wtype, k)]) to fp64 [R, k].
 
@@ -312,6 +365,33 @@ def dequantize_rows(wtype: int, rows, k: int) -> np.ndarray:
         blk = rows.reshape(r, k // 32, 18)
         d = fp16_bits_to_f64(blk[..., 0:2].copy().view(np.uint16)[..., 0])
         return (q4_0_codes(blk) * d[..., None]).reshape(r, k)
+    if wtype in (TYPE_Q4_1, TYPE_Q5_0, TYPE_Q5_1):
+        nbytes = {TYPE_Q4_1: 20, TYPE_Q5_0: 22, TYPE_Q5_1: 24}[wtype]
+        blk = rows.reshape(r, k // 32, nbytes)
+        d = fp16_bits_to_f64(blk[..., 0:2].copy().view(np.uint16)[..., 0])
+        if wtype == TYPE_Q4_1:
+            m = fp16_bits_to_f64(blk[..., 2:4].copy().view(np.uint16)[..., 0])
+            v = d[..., None] * nibble_split_codes(blk[..., 4:20]) + m[..., None]
+        elif wtype == TYPE_Q5_0:
+            q = nibble_split_codes(blk[..., 6:22]) | (q5_high_bits(blk[..., 2:6]) << 4)
+            v = d[..., None] * (q - 16)
+        else:
+            m = fp16_bits_to_f64(blk[..., 2:4].copy().view(np.uint16)[..., 0])
+            q = nibble_split_codes(blk[..., 8:24]) | (q5_high_bits(blk[..., 4:8]) << 4)
+            v = d[..., None] * q + m[..., None]
+        return v.reshape(r, k)
+    if wtype == TYPE_Q5_K:
+        sb = rows.reshape(r, k // 256, 176)
+        d = fp16_bits_to_f64(sb[..., 0:2].copy().view(np.uint16)[..., 0])
+        dmin = fp16_bits_to_f64(sb[..., 2:4].copy().view(np.uint16)[..., 0])
+        sc, mn = q4k_scale_min(sb[..., 4:16])
+        q = q5k_codes(sb).reshape(r, k // 256, 8, 32).astype(np.float64)
+        v = d[..., None, None] * sc[..., None] * q - dmin[..., None, None] * mn[..., None]
+        return v.reshape(r, k)
+    if wtype == TYPE_MXFP4:
+        blk = rows.reshape(r, k // 32, 17)
+        v = e2m1_value(nibble_split_codes(blk[..., 1:17])) * e8m0_value(blk[..., 0])[..., None]
+        return v.reshape(r, k)
     raise ValueError(wtype)
 
 
@@ -327,6 +407,10 @@ def block_dots(wtype: int, rows, k: int, act_qs) -> np.ndarray:
     Q4_K:  one int per 32-sub-block, sum(q4 * a_q).
     Q6_K:  one int per 16-value scale group, sum((q6 - 32) * a_q).
     Q4_0:  one int per 32-block, sum((q4 - 8) * a_q).
+    Q4_1, Q5_1, Q5_K: one int per 32 values, sum(q * a_q) (q unsigned; the
+           min term goes through the activation block's code sum).
+    Q5_0:  one int per 32-block, sum((q5 - 16) * a_q).
+    MXFP4: one int per 32-block, sum((2*E2M1(code)) * a_q).
     Returns int64 [R, nblocks]."""
     rows = np.asarray(rows, dtype=np.uint8)
     a = np.asarray(act_qs, dtype=np.int64).reshape(k)
@@ -348,4 +432,19 @@ def block_dots(wtype: int, rows, k: int, act_qs) -> np.ndarray:
     if wtype == TYPE_Q4_0:
         q = q4_0_codes(rows.reshape(r, k // 32, 18)).reshape(r, k)
         return (q * a).reshape(r, k // 32, 32).sum(axis=-1)
-    raise ValueError(wtype)
+    if wtype == TYPE_Q4_1:
+        q = nibble_split_codes(rows.reshape(r, k // 32, 20)[..., 4:20]).reshape(r, k)
+    elif wtype == TYPE_Q5_0:
+        blk = rows.reshape(r, k // 32, 22)
+        q = (nibble_split_codes(blk[..., 6:22]) | (q5_high_bits(blk[..., 2:6]) << 4)).reshape(r, k) - 16
+    elif wtype == TYPE_Q5_1:
+        blk = rows.reshape(r, k // 32, 24)
+        q = (nibble_split_codes(blk[..., 8:24]) | (q5_high_bits(blk[..., 4:8]) << 4)).reshape(r, k)
+    elif wtype == TYPE_Q5_K:
+        q = q5k_codes(rows.reshape(r, k // 256, 176)).reshape(r, k)
+    elif wtype == TYPE_MXFP4:
+        codes = nibble_split_codes(rows.reshape(r, k // 32, 17)[..., 1:17]).reshape(r, k)
+        q = np.rint(2.0 * e2m1_value(codes)).astype(np.int64)
+    else:
+        raise ValueError(wtype)
+    return (q * a).reshape(r, k // 32, 32).sum(axis=-1)

@@ -20,6 +20,9 @@ from __future__ import annotations
 import numpy as np
 
 BF16, Q8_0, Q4_K, NVFP4, Q6_K, Q4_0 = 0, 1, 2, 3, 4, 5
+Q4_1, Q5_0, Q5_1, Q5_K, MXFP4 = 6, 7, 8, 9, 10
+# types with no converter here: their "converted" rows are counter-based rows
+COUNTER_ONLY = (Q4_1, Q5_0, Q5_1, Q5_K, MXFP4)
 
 
 def rng(seed: int) -> np.random.Generator:
@@ -28,7 +31,8 @@ def rng(seed: int) -> np.random.Generator:
 
 def row_bytes(wtype: int, k: int) -> int:
     return {BF16: 2 * k, Q8_0: k // 32 * 34, Q4_K: k // 256 * 144, NVFP4: k // 2 + k // 16,
-            Q6_K: k // 256 * 210, Q4_0: k // 32 * 18}[wtype]
+            Q6_K: k // 256 * 210, Q4_0: k // 32 * 18, Q4_1: k // 32 * 20, Q5_0: k // 32 * 22,
+            Q5_1: k // 32 * 24, Q5_K: k // 256 * 176, MXFP4: k // 32 * 17}[wtype]
 
 
 # ------------------------------------------------------------------ activations / routing
@@ -213,10 +217,16 @@ def q8_0_codes_bank(seed: int, rows: int, k: int) -> np.ndarray:
 def converted_expert(seed: int, e: int, H: int, I: int, gate_up_type: int, down_type: int):
     """One converted expert: (gate_up uint8 [2I, rb_gu], down uint8 [H, rb_d],
     scales fp32 [4]).  Weights ~ N(0, 0.02) (Q8_0: the direct code recipe);
-    NVFP4 projections get s2 = amax / (6 * 448) each (gate, up, down)."""
+    NVFP4 projections get s2 = amax / (6 * 448) each (gate, up, down).  The
+    COUNTER_ONLY types take counter-based rows (every code pattern, scales
+    masked to a realistic range) instead of converted weights."""
     r = rng(seed * 100003 + e)
     sc = np.ones(4, dtype=np.float32)
-    if gate_up_type == Q8_0:
+    if gate_up_type in COUNTER_ONLY or down_type in COUNTER_ONLY:
+        from . import counter
+    if gate_up_type in COUNTER_ONLY:
+        gu = counter.bank_bytes_np(seed * 100003 + e, gate_up_type, H, 0, 2 * I)
+    elif gate_up_type == Q8_0:
         gu = q8_0_codes_bank(seed * 100003 + e, 2 * I, H)
     else:
         wg = (r.standard_normal((2 * I, H)) * 0.02).astype(np.float32)
@@ -235,7 +245,9 @@ def converted_expert(seed: int, e: int, H: int, I: int, gate_up_type: int, down_
             gu = convert_q4_0(wg)
         else:
             gu = convert_bf16(wg)
-    if down_type == Q8_0:
+    if down_type in COUNTER_ONLY:
+        dn = counter.bank_bytes_np(seed * 100003 + e + 50000, down_type, I, 0, H)
+    elif down_type == Q8_0:
         dn = q8_0_codes_bank(seed * 100003 + e + 50000, H, I)
     else:
         wd = (r.standard_normal((H, I)) * 0.02).astype(np.float32)

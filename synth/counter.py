@@ -19,6 +19,10 @@ row only, keeps scale fields finite and of a realistic size:
   Q6_K (210-byte super-blocks): the 16 int8 sub-block scales keep their low 5
         bits (0 .. 31); d fp16 -> exponent field 1 (2^-14 .. 2^-13).
   Q4_0 (18-byte blocks): d fp16 -> exponent field 3 (2^-12 .. 2^-11).
+  Q4_1 / Q5_1 (20 / 24-byte blocks): d as Q4_0; m fp16 keeps its sign,
+        exponent field 3.  Q5_0 (22-byte blocks): d as Q4_0.
+  Q5_K (176-byte super-blocks): d and dmin as Q4_K.
+  MXFP4 (17-byte blocks): E8M0 byte -> 118 + (b & 3) (scales 2^-9 .. 2^-6).
   BF16: each value keeps its sign and 7 mantissa bits; its exponent becomes
         119 + (bits 7..8 of the raw value): magnitudes 2^-8 .. 2^-4.
 
@@ -34,11 +38,13 @@ C2 = 0x94D049BB133111EB
 M64 = (1 << 64) - 1
 
 BF16, Q8_0, Q4_K, NVFP4, Q6_K, Q4_0 = 0, 1, 2, 3, 4, 5
+Q4_1, Q5_0, Q5_1, Q5_K, MXFP4 = 6, 7, 8, 9, 10
 
 
 def _row_bytes(wtype: int, k: int) -> int:
     return {BF16: 2 * k, Q8_0: k // 32 * 34, Q4_K: k // 256 * 144, NVFP4: k // 2 + k // 16,
-            Q6_K: k // 256 * 210, Q4_0: k // 32 * 18}[wtype]
+            Q6_K: k // 256 * 210, Q4_0: k // 32 * 18, Q4_1: k // 32 * 20, Q5_0: k // 32 * 22,
+            Q5_1: k // 32 * 24, Q5_K: k // 256 * 176, MXFP4: k // 32 * 17}[wtype]
 
 
 # ------------------------------------------------------------------ host (numpy)
@@ -84,6 +90,18 @@ def _mask_np(rows: np.ndarray, wtype: int, k: int) -> np.ndarray:
     elif wtype == Q4_0:
         blk = rows.reshape(rows.shape[0], -1, 18)
         blk[..., 1] = 0x0C | (blk[..., 1] & 0x03)
+    elif wtype in (Q4_1, Q5_0, Q5_1):
+        blk = rows.reshape(rows.shape[0], -1, {Q4_1: 20, Q5_0: 22, Q5_1: 24}[wtype])
+        blk[..., 1] = 0x0C | (blk[..., 1] & 0x03)
+        if wtype != Q5_0:
+            blk[..., 3] = (blk[..., 3] & 0x80) | 0x0C | (blk[..., 3] & 0x03)
+    elif wtype == Q5_K:
+        sb = rows.reshape(rows.shape[0], -1, 176)
+        sb[..., 1] = 0x04 | (sb[..., 1] & 0x03)
+        sb[..., 3] = 0x10 | (sb[..., 3] & 0x03)
+    elif wtype == MXFP4:
+        blk = rows.reshape(rows.shape[0], -1, 17)
+        blk[..., 0] = 118 + (blk[..., 0] & 0x03)
     elif wtype == BF16:
         v = rows.view(np.uint16).astype(np.uint32)
         exp = 119 + ((v >> 7) & 3)
@@ -155,6 +173,18 @@ def _mask_torch(rows, wtype: int, k: int) -> None:
     elif wtype == Q4_0:
         blk = rows.view(rows.shape[0], -1, 18)
         blk[..., 1] = torch.bitwise_or(torch.bitwise_and(blk[..., 1], 0x03), 0x0C)
+    elif wtype in (Q4_1, Q5_0, Q5_1):
+        blk = rows.view(rows.shape[0], -1, {Q4_1: 20, Q5_0: 22, Q5_1: 24}[wtype])
+        blk[..., 1] = torch.bitwise_or(torch.bitwise_and(blk[..., 1], 0x03), 0x0C)
+        if wtype != Q5_0:
+            blk[..., 3] = torch.bitwise_or(torch.bitwise_and(blk[..., 3], 0x83), 0x0C)
+    elif wtype == Q5_K:
+        sb = rows.view(rows.shape[0], -1, 176)
+        sb[..., 1] = torch.bitwise_or(torch.bitwise_and(sb[..., 1], 0x03), 0x04)
+        sb[..., 3] = torch.bitwise_or(torch.bitwise_and(sb[..., 3], 0x03), 0x10)
+    elif wtype == MXFP4:
+        blk = rows.view(rows.shape[0], -1, 17)
+        blk[..., 0] = torch.bitwise_and(blk[..., 0], 0x03) + 118
     elif wtype == BF16:
         v = rows.view(torch.int16).to(torch.int32) & 0xFFFF
         exp = 119 + torch.bitwise_and(torch.bitwise_right_shift(v, 7), 3)

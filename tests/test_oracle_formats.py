@@ -180,6 +180,97 @@ def test_q4_0_codes_single_bit_and_hand_values():
     assert (v[0], v[16], v[3], v[19]) == (1.75, 0.25, -2.0, -2.0)
 
 
+def _f16(v):
+    return np.array([v], dtype=np.float16).view(np.uint8)
+
+
+@pytest.mark.parametrize("wtype,code_bytes,offset", [(F.TYPE_Q4_1, range(4, 20), 0),
+                                                     (F.TYPE_Q5_0, range(2, 22), 16),
+                                                     (F.TYPE_Q5_1, range(4, 24), 0)])
+def test_q4_1_q5_codes_single_bit_bijection(wtype, code_bytes, offset):
+    """d = 1, m = 0: each single set bit of the code and high-bit bytes gives
+    exactly one value a single power-of-two code, and the bits cover every
+    (value, code bit) pair once: 32 x 4 for Q4_1, 32 x 5 for Q5_x."""
+    nb = F.row_bytes(wtype, 32)
+    hits = set()
+    for byte in code_bytes:
+        for bit in range(8):
+            blk = np.zeros(nb, dtype=np.uint8)
+            blk[0:2] = _f16(1.0)
+            blk[byte] = 1 << bit
+            q = np.rint(F.dequantize_rows(wtype, blk[None, :], 32)[0]).astype(np.int64) + offset
+            nz = np.nonzero(q)[0]
+            assert len(nz) == 1 and (int(q[nz[0]]) & (int(q[nz[0]]) - 1)) == 0
+            hits.add((int(nz[0]), int(q[nz[0]]).bit_length() - 1))
+    assert len(hits) == 32 * (4 if wtype == F.TYPE_Q4_1 else 5)
+
+
+def test_q4_1_q5_0_q5_1_hand_values():
+    blk = np.zeros(20, dtype=np.uint8)                       # Q4_1: d = 0.5, m = -1
+    blk[0:2], blk[2:4] = _f16(0.5), _f16(-1.0)
+    blk[4] = 0x3A                                            # value 0: code 10, value 16: code 3
+    v = F.dequantize_rows(F.TYPE_Q4_1, blk[None, :], 32)[0]
+    assert (v[0], v[16], v[5]) == (4.0, 0.5, -1.0)
+    blk = np.zeros(22, dtype=np.uint8)                       # Q5_0: d = 0.25, high bits of values 0 and 16
+    blk[0:2] = _f16(0.25)
+    blk[2:6] = np.array([0x00010001], dtype="<u4").view(np.uint8)
+    blk[6] = 0x2F                                            # value 0: 15 + 16, value 16: 2 + 16
+    v = F.dequantize_rows(F.TYPE_Q5_0, blk[None, :], 32)[0]
+    assert (v[0], v[16], v[1]) == (3.75, 0.5, -4.0)
+    blk = np.zeros(24, dtype=np.uint8)                       # Q5_1: d = 0.5, m = 0.25, high bit of value 31
+    blk[0:2], blk[2:4] = _f16(0.5), _f16(0.25)
+    blk[7] = 0x80
+    blk[8 + 15] = 0x70                                       # value 15: code 0, value 31: 7 + 16
+    v = F.dequantize_rows(F.TYPE_Q5_1, blk[None, :], 32)[0]
+    assert (v[15], v[31]) == (0.25, 11.75)
+
+
+def test_q5k_superblock_hand_values():
+    """d = 1, dmin = 0.5; sub-block 0: sc 3, m 2; sub-block 5: sc 1 + 16
+    (top bits from byte 1), m 2.  Value 0: nibble 5 + fifth bit (bit 0 of
+    high-bit byte 0) = 21 -> 3*21 - 1 = 62.  Value 167 (sub-block 5, lane 7):
+    high nibble 9 of code byte 64 + 7, fifth bit = bit 5 of high-bit byte 7
+    -> 25 -> 17*25 - 1 = 424."""
+    sb = np.zeros(176, dtype=np.uint8)
+    sb[0:2], sb[2:4] = _f16(1.0), _f16(0.5)
+    sb[4 + 0], sb[4 + 4] = 3, 2            # sc0, m0
+    sb[4 + 1] = 0x40                       # top bits of sc5 = 1 (sc1 stays 0)
+    sb[4 + 9] = 0x21                       # sc5 low nibble 1, m5 low nibble 2
+    sb[48 + 0] = 0x05
+    sb[16 + 0] = 0x01
+    sb[48 + 64 + 7] = 0x90
+    sb[16 + 7] = 0x20
+    v = F.dequantize_rows(F.TYPE_Q5_K, sb[None, :], 256)[0]
+    assert v[0] == 62.0 and v[167] == 424.0
+    assert v[1] == -1.0                    # code 0 of sub-block 0: -dmin*m0
+    assert v[160] == -1.0 and v[32] == 0.0  # sub-block 5 lane 0; sub-block 1 has sc = m = 0
+
+
+def test_q5k_codes_single_bit_bijection():
+    hits = set()
+    for byte in range(16, 176):
+        for bit in range(8):
+            sb = np.zeros(176, dtype=np.uint8)
+            sb[byte] = 1 << bit
+            q = F.q5k_codes(sb)
+            nz = np.nonzero(q)[0]
+            assert len(nz) == 1 and (int(q[nz[0]]) & (int(q[nz[0]]) - 1)) == 0
+            hits.add((int(nz[0]), int(q[nz[0]]).bit_length() - 1))
+    assert len(hits) == 256 * 5
+
+
+def test_mxfp4_hand_values_and_e8m0():
+    assert F.e8m0_value(127) == 1.0 and F.e8m0_value(0) == 2.0 ** -127 and F.e8m0_value(254) == 2.0 ** 127
+    blk = np.zeros(2 * 17, dtype=np.uint8)
+    blk[0] = 126                            # 0.5
+    blk[1] = 0x9B                           # value 0: code 11 = -1.5, value 16: code 9 = -0.5
+    blk[17] = 130                           # 8
+    blk[18 + 15] = 0x07                     # block 1 value 15: code 7 = 6
+    v = F.dequantize_rows(F.TYPE_MXFP4, blk[None, :], 64)[0]
+    assert (v[0], v[16], v[1]) == (-0.75, -0.25, 0.0)
+    assert v[32 + 15] == 48.0 and v[32 + 31] == 0.0
+
+
 # ---------------------------------------------------------------- q8_1
 
 def _fp32_round(fr: Fraction) -> Fraction:
@@ -255,7 +346,9 @@ _E2M1_X2 = {0: 0, 1: 1, 2: 2, 3: 3, 4: 4, 5: 6, 6: 8, 7: 12}
 
 
 @pytest.mark.parametrize("wtype,k", [(F.TYPE_Q8_0, 96), (F.TYPE_NVFP4, 128), (F.TYPE_Q4_K, 512),
-                                     (F.TYPE_Q6_K, 512), (F.TYPE_Q4_0, 96)])
+                                     (F.TYPE_Q6_K, 512), (F.TYPE_Q4_0, 96), (F.TYPE_Q4_1, 96),
+                                     (F.TYPE_Q5_0, 96), (F.TYPE_Q5_1, 96), (F.TYPE_Q5_K, 512),
+                                     (F.TYPE_MXFP4, 96)])
 def test_block_dots_brute_force(wtype, k):
     r = np.random.default_rng(5 + wtype)
     rb = F.row_bytes(wtype, k)
@@ -293,6 +386,31 @@ def test_block_dots_brute_force(wtype, k):
                 qs = row[b * 18 + 2: b * 18 + 18]
                 vals = [(x & 15) - 8 for x in qs] + [(x >> 4) - 8 for x in qs]
                 want.append(sum(vals[i] * af[b * 32 + i] for i in range(32)))
+        elif wtype in (F.TYPE_Q4_1, F.TYPE_Q5_0, F.TYPE_Q5_1, F.TYPE_MXFP4):
+            nbytes, qoff, hoff = {F.TYPE_Q4_1: (20, 4, None), F.TYPE_Q5_0: (22, 6, 2), F.TYPE_Q5_1: (24, 8, 4),
+                                  F.TYPE_MXFP4: (17, 1, None)}[wtype]
+            want = []
+            for b in range(k // 32):
+                blk = row[b * nbytes: (b + 1) * nbytes]
+                qs = blk[qoff: qoff + 16]
+                vals = [x & 15 for x in qs] + [x >> 4 for x in qs]
+                if hoff is not None:
+                    word = blk[hoff] | (blk[hoff + 1] << 8) | (blk[hoff + 2] << 16) | (blk[hoff + 3] << 24)
+                    vals = [v + 16 * ((word >> i) & 1) for i, v in enumerate(vals)]
+                if wtype == F.TYPE_Q5_0:
+                    vals = [v - 16 for v in vals]
+                if wtype == F.TYPE_MXFP4:
+                    vals = [(-_E2M1_X2[v & 7] if v & 8 else _E2M1_X2[v & 7]) for v in vals]
+                want.append(sum(vals[i] * af[b * 32 + i] for i in range(32)))
+        elif wtype == F.TYPE_Q5_K:
+            want = []
+            for sbi in range(k // 256):
+                b = row[sbi * 176: sbi * 176 + 176]
+                for j in range(8):
+                    c = j // 2
+                    codes = [((b[48 + c * 32 + l] >> (4 * (j % 2))) & 15) + 16 * ((b[16 + l] >> j) & 1)
+                             for l in range(32)]
+                    want.append(sum(codes[l] * af[sbi * 256 + j * 32 + l] for l in range(32)))
         else:
             want = []
             for sbi in range(k // 256):
