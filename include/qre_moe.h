@@ -62,10 +62,28 @@ extern "C" {
  *              is the low nibble of qs[j], value j+16 its high nibble, value
  *              d*(q - 8) (GGUF Q4_0 bit layout; the CPU format of FreeToken
  *              PR #704, "Tests").
+ *   MOE_Q4_1 : K/32 blocks of {fp16 d; fp16 m; uint8 qs[16]} (20 bytes), codes
+ *              as MOE_Q4_0, value d*q + m.
+ *   MOE_Q5_0 : K/32 blocks of {fp16 d; uint8 qh[4]; uint8 qs[16]} (22 bytes):
+ *              the low 4 code bits as MOE_Q4_0, bit j of the little-endian
+ *              word qh is the fifth bit of value j; value d*(q - 16).
+ *   MOE_Q5_1 : K/32 blocks of {fp16 d; fp16 m; uint8 qh[4]; uint8 qs[16]}
+ *              (24 bytes), codes as MOE_Q5_0, value d*q + m.
+ *   MOE_Q5_K : K/256 super-blocks of 176 bytes {fp16 d; fp16 dmin; uint8
+ *              scales[12]; uint8 qh[32]; uint8 qs[128]}: scales and the low 4
+ *              code bits as MOE_Q4_K, bit j of qh[l] the fifth bit of value l
+ *              of sub-block j; value d*sc_j*q - dmin*m_j.
+ *   MOE_MXFP4: K/32 blocks of {uint8 e; uint8 qs[16]} (17 bytes), E2M1 codes
+ *              laid out as MOE_Q4_0, value E2M1(code) * 2^(e - 127); e = 255
+ *              (not a finite E8M0 scale) must not occur.
+ * (Q4_1 through MXFP4 are the remaining types of FreeToken PR #704's
+ * synthetic list, "Validation"; GGUF bit layouts.)  Banks must be readable
+ * up to the next 16-byte boundary past their last row.
  * Gate_up and down may be of different types (e.g. Q4_K gate_up with Q6_K
  * down, the pairing of a Q4_K_M checkpoint). */
 typedef enum {
-  MOE_BF16 = 0, MOE_Q8_0 = 1, MOE_Q4_K = 2, MOE_NVFP4 = 3, MOE_Q6_K = 4, MOE_Q4_0 = 5
+  MOE_BF16 = 0, MOE_Q8_0 = 1, MOE_Q4_K = 2, MOE_NVFP4 = 3, MOE_Q6_K = 4, MOE_Q4_0 = 5,
+  MOE_Q4_1 = 6, MOE_Q5_0 = 7, MOE_Q5_1 = 8, MOE_Q5_K = 9, MOE_MXFP4 = 10
 } moe_type;
 
 typedef enum {
@@ -290,7 +308,9 @@ int moe_quantize_q8_1(const float* x, int64_t n, void* out_blocks, void* stream)
  * per 16-value block, sum of (2*E2M1 code value) * q), k/32 for MOE_Q8_0 and
  * MOE_Q4_K (sum of code * q; Q4_K per 32-value sub-block), k/16 for MOE_Q6_K
  * (sum of (code - 32) * q per 16-value scale group), k/32 for MOE_Q4_0 (sum of
- * (code - 8) * q).  MOE_BF16 is MOE_EINVAL. */
+ * (code - 8) * q), MOE_Q5_0 (sum of (code - 16) * q), MOE_Q4_1, MOE_Q5_1 and
+ * MOE_Q5_K (sum of code * q) and MOE_MXFP4 (sum of (2*E2M1 code value) * q).
+ * MOE_BF16 is MOE_EINVAL. */
 int moe_debug_block_dots(int32_t type, const void* rows, int32_t nrows, int32_t k,
                          const void* act_blocks, int32_t* out, void* stream);
 
@@ -327,9 +347,8 @@ int moe_debug_prefill_stages(const moe_bank* bank, const void* x, int32_t T,
  * (the decode path's prep_input), each 32-value block's integer dot is exact,
  * the block scales and row_scale are applied in fp32, and the output is
  * rounded once to bf16 (ties to even).
- *   type:      MOE_NVFP4, MOE_Q4_K, MOE_Q8_0, MOE_Q6_K or MOE_Q4_0 (MOE_BF16 is
- *              MOE_EUNSUPPORTED); an NVFP4 tensor's weight_scale_2 goes into
- *              row_scale
+ *   type:      any quantized moe_type (MOE_BF16 is MOE_EUNSUPPORTED); an
+ *              NVFP4 tensor's weight_scale_2 goes into row_scale
  *   rows:      device, N rows of moe_row_bytes(type, K) bytes back to back,
  *              16-byte aligned and readable up to the next 16-byte boundary
  *              past the last row

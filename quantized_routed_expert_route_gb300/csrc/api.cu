@@ -114,8 +114,8 @@ int geom_check(const moe_layer_geom* g) {
   if (!g) return MOE_EINVAL;
   if (g->E < 1 || g->E > kMaxE || g->top_k < 1 || g->top_k > kMaxTopK || g->top_k > g->E) return MOE_EINVAL;
   if (g->H < 32 || g->I < 32 || g->H > (1 << 16) || g->I > (1 << 16)) return MOE_EINVAL;
-  if (g->gate_up_type < MOE_BF16 || g->gate_up_type > MOE_Q4_0) return MOE_EINVAL;
-  if (g->down_type < MOE_BF16 || g->down_type > MOE_Q4_0) return MOE_EINVAL;
+  if (g->gate_up_type < MOE_BF16 || g->gate_up_type > MOE_MXFP4) return MOE_EINVAL;
+  if (g->down_type < MOE_BF16 || g->down_type > MOE_MXFP4) return MOE_EINVAL;
   if (row_bytes_of(g->gate_up_type, g->H) == 0 || row_bytes_of(g->down_type, g->I) == 0) return MOE_EINVAL;
   if (g->H % 32 != 0 || g->I % 32 != 0) return MOE_EINVAL;
   if (g->glu != MOE_GLU_SILU && g->glu != MOE_GLU_GELU_TANH) return MOE_EINVAL;
@@ -324,7 +324,8 @@ DecodeParams make_params(const moe_bank* b, const WsLayout& L, uint8_t* ws, cons
     case W_Q4_K: p.w0 = 3; break;
     case W_Q8_0: p.w0 = 2; break;
     case W_Q6_K: p.w0 = 3; break;
-    case W_Q4_0: p.w0 = 2; break;
+    case W_Q5_K: p.w0 = 3; break;
+    case W_Q4_0: case W_Q4_1: case W_Q5_0: case W_Q5_1: case W_MXFP4: p.w0 = 2; break;
     default: p.w0 = 4; break;
   }
   return p;
@@ -747,8 +748,7 @@ int moe_quantize_q8_1(const float* x, int64_t n, void* out_blocks, void* stream)
 int moe_debug_block_dots(int32_t type, const void* rows, int32_t nrows, int32_t k, const void* act, int32_t* out,
                          void* stream) {
   if (!rows || !act || !out || nrows < 0 || k <= 0) return MOE_EINVAL;
-  if (type != MOE_Q8_0 && type != MOE_Q4_K && type != MOE_NVFP4 && type != MOE_Q6_K && type != MOE_Q4_0)
-    return MOE_EINVAL;
+  if (type <= MOE_BF16 || type > MOE_MXFP4) return MOE_EINVAL;
   if (row_bytes_of(type, k) == 0 || !aligned(rows, 16) || !aligned(act, 4) || !aligned(out, 4)) return MOE_EINVAL;
   cudaError_t e = launch_block_dots(type, static_cast<const uint8_t*>(rows), nrows, k,
                                     static_cast<const uint8_t*>(act), out, static_cast<cudaStream_t>(stream));
@@ -859,7 +859,7 @@ int moe_linear(int32_t type, const void* rows, int32_t N, int32_t K, const float
                int32_t T, void* out, uint32_t* dev_err, void* stream) {
   if (T == 0) return MOE_OK;
   if (!rows || !x || !out || N < 1 || K < 32 || T < 0) return MOE_EINVAL;
-  if (type < MOE_BF16 || type > MOE_Q4_0) return MOE_EINVAL;
+  if (type < MOE_BF16 || type > MOE_MXFP4) return MOE_EINVAL;
   if (type == MOE_BF16) return MOE_EUNSUPPORTED;
   if (T > MOE_LINEAR_MAX_T) return MOE_EUNSUPPORTED;
   const int rb = row_bytes_of(type, K);

@@ -612,6 +612,39 @@ __device__ __forceinline__ void accum_q_block(const uint8_t* row, int k, int b, 
     for (int t = 0; t < NTT; ++t) {
       if (NTT == 1 || t < nt) acc[t] += (d * a[t].d) * (float)(int_dot8(wq, a[t].q) - 8 * a[t].sum);
     }
+  } else if constexpr (WT == W_Q4_1 || WT == W_Q5_1) {
+    int wq[8];
+    float d, m;
+    if constexpr (WT == W_Q4_1) q4_1_decode(row, b, wq, d, m);
+    else q5_1_decode(row, b, wq, d, m);
+#pragma unroll
+    for (int t = 0; t < NTT; ++t) {
+      if (NTT == 1 || t < nt) acc[t] += a[t].d * (d * (float)int_dot8(wq, a[t].q) + m * (float)a[t].sum);
+    }
+  } else if constexpr (WT == W_Q5_0) {
+    int wq[8];
+    float d;
+    q5_0_decode(row, b, wq, d);
+#pragma unroll
+    for (int t = 0; t < NTT; ++t) {
+      if (NTT == 1 || t < nt) acc[t] += (d * a[t].d) * (float)(int_dot8(wq, a[t].q) - 16 * a[t].sum);
+    }
+  } else if constexpr (WT == W_Q5_K) {
+    int wq[8];
+    float dsc, dmm;
+    q5k_decode(row, b, wq, dsc, dmm);
+#pragma unroll
+    for (int t = 0; t < NTT; ++t) {
+      if (NTT == 1 || t < nt) acc[t] += a[t].d * (dsc * (float)int_dot8(wq, a[t].q) - dmm * (float)a[t].sum);
+    }
+  } else if constexpr (WT == W_MXFP4) {
+    int wq[8];
+    float sc;
+    mxfp4_decode(row, b, wq, sc);
+#pragma unroll
+    for (int t = 0; t < NTT; ++t) {
+      if (NTT == 1 || t < nt) acc[t] += (a[t].d * sc * 0.5f) * (float)int_dot8(wq, a[t].q);
+    }
   } else {  // W_Q8_0
     static_assert(WT == W_Q8_0 || WT == W_BF16, "unhandled weight type");  // BF16: unreachable instantiations
     int wq[8];

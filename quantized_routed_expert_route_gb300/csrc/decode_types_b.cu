@@ -1,0 +1,25 @@
+// Two-kernel decode path: gate_up and down instantiated for Q6_K, Q4_0, Q4_1
+// rows (the kernels are in decode_twok.cuh).
+#include "decode_twok.cuh"
+
+namespace qre {
+
+cudaError_t launch_gate_up_types_b(const DecodeParams& p, size_t smem, cudaStream_t stream) {
+  switch (p.gu_type) {
+    case W_Q6_K: return launch_gu_w<W_Q6_K>(p, smem, stream);
+    case W_Q4_0: return launch_gu_w<W_Q4_0>(p, smem, stream);
+    case W_Q4_1: return launch_gu_w<W_Q4_1>(p, smem, stream);
+  }
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_down_types_b(const DecodeParams& p, size_t smem, cudaStream_t stream) {
+  switch (p.dn_type) {
+    case W_Q6_K: return launch_dn_w<W_Q6_K, 8>(p, smem, stream);
+    case W_Q4_0: return launch_dn_w<W_Q4_0, 8>(p, smem, stream);
+    case W_Q4_1: return launch_dn_w<W_Q4_1, 8>(p, smem, stream);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace qre

@@ -22,6 +22,16 @@
 //   Q4_0  : fp16 d then 16 code bytes (18 bytes per 32 values); value j < 16
 //           is the low nibble of code byte j, value j+16 its high nibble;
 //           value d*(q - 8).
+//   Q4_1  : fp16 d, fp16 m, 16 code bytes as Q4_0 (20 bytes); value d*q + m.
+//   Q5_0  : fp16 d, a 32-bit word whose bit j is the fifth code bit of value
+//           j, 16 code bytes as Q4_0 (22 bytes); value d*(q - 16).
+//   Q5_1  : fp16 d, fp16 m, the high-bit word, 16 code bytes (24 bytes);
+//           value d*q + m.
+//   Q5_K  : 176-byte super-block of 256: the Q4_K header (d, dmin, 12 packed
+//           scale bytes), 32 high-bit bytes (bit j of byte l: value l of
+//           sub-block j), 128 code bytes as Q4_K; value d*sc_j*q - dmin*m_j.
+//   MXFP4 : one E8M0 byte e, 16 code bytes of E2M1 as Q4_0 (17 bytes);
+//           value E2M1(code) * 2^(e - 127).
 #pragma once
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -30,7 +40,10 @@
 
 namespace qre {
 
-enum WType : int { W_BF16 = 0, W_Q8_0 = 1, W_Q4_K = 2, W_NVFP4 = 3, W_Q6_K = 4, W_Q4_0 = 5 };
+enum WType : int {
+  W_BF16 = 0, W_Q8_0 = 1, W_Q4_K = 2, W_NVFP4 = 3, W_Q6_K = 4, W_Q4_0 = 5,
+  W_Q4_1 = 6, W_Q5_0 = 7, W_Q5_1 = 8, W_Q5_K = 9, W_MXFP4 = 10
+};
 // Kernel-side variant of W_NVFP4 whose rows (9k/16 bytes) are not 16-byte aligned.
 constexpr int W_NVFP4_U = 16;
 
@@ -42,6 +55,11 @@ __host__ __device__ inline int row_bytes_of(int t, int k) {
     case W_NVFP4: return (k % 32 == 0) ? k / 2 + k / 16 : 0;
     case W_Q6_K: return (k % 256 == 0) ? (k / 256) * 210 : 0;
     case W_Q4_0: return (k % 32 == 0) ? (k / 32) * 18 : 0;
+    case W_Q4_1: return (k % 32 == 0) ? (k / 32) * 20 : 0;
+    case W_Q5_0: return (k % 32 == 0) ? (k / 32) * 22 : 0;
+    case W_Q5_1: return (k % 32 == 0) ? (k / 32) * 24 : 0;
+    case W_Q5_K: return (k % 256 == 0) ? (k / 256) * 176 : 0;
+    case W_MXFP4: return (k % 32 == 0) ? (k / 32) * 17 : 0;
   }
   return 0;
 }
@@ -236,12 +254,10 @@ __device__ __forceinline__ void nvfp4_int_dots(const uint32_t (&pos)[8], const u
 
 // ------------------------------------------------------------------ Q4_K
 
-// Decode sub-block b (32 values) of a Q4_K row: the codes as int8x4 words in
-// value order, and the fp32 factors d*sc_j and dmin*m_j (both exact).
-__device__ __forceinline__ void q4k_decode(const uint8_t* row, int b, int (&nib)[8], float& dsc, float& dmm) {
-  const uint8_t* sb = row + (b >> 3) * 144;
-  const int j = b & 7;
-  const uint4 hdr = lds128(sb);  // x: d | dmin << 16, y: scales[0..3], z: scales[4..7], w: scales[8..11]
+// d*sc_j and dmin*m_j of sub-block j from the 16-byte header of a Q4_K or
+// Q5_K super-block (x: d | dmin << 16, y: scales[0..3], z: scales[4..7],
+// w: scales[8..11]); both products are exact in fp32.
+__device__ __forceinline__ void k_quant_scales(const uint4 hdr, int j, float& dsc, float& dmm) {
   const float d = f16_bits_to_f32(hdr.x & 0xFFFFu);
   const float dmin = f16_bits_to_f32(hdr.x >> 16);
   uint32_t sc, m;
@@ -254,14 +270,40 @@ __device__ __forceinline__ void q4k_decode(const uint8_t* row, int b, int (&nib)
     sc = (s8 & 15u) | (((hdr.y >> (8 * jj + 6)) & 3u) << 4);
     m = (s8 >> 4) | (((hdr.z >> (8 * jj + 6)) & 3u) << 4);
   }
+  dsc = d * (float)sc;
+  dmm = dmin * (float)m;
+}
+
+// Decode sub-block b (32 values) of a Q4_K row: the codes as int8x4 words in
+// value order, and the fp32 factors d*sc_j and dmin*m_j (both exact).
+__device__ __forceinline__ void q4k_decode(const uint8_t* row, int b, int (&nib)[8], float& dsc, float& dmm) {
+  const uint8_t* sb = row + (b >> 3) * 144;
+  const int j = b & 7;
+  k_quant_scales(lds128(sb), j, dsc, dmm);
   const uint8_t* qs = sb + 16 + (j >> 1) * 32;
   const uint4 q0 = lds128(qs), q1 = lds128(qs + 16);
   const int sh = (j & 1) * 4;
   const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
 #pragma unroll
   for (int i = 0; i < 8; ++i) nib[i] = (int)((w[i] >> sh) & 0x0F0F0F0Fu);
-  dsc = d * (float)sc;
-  dmm = dmin * (float)m;
+}
+
+// Sub-block b of a Q5_K row (16-byte aligned super-blocks): the 5-bit codes
+// as int8x4 words in value order and d*sc_j, dmin*m_j.  The low 4 bits are
+// laid out as in Q4_K (code bytes at offset 48); the fifth bit of value l is
+// bit j of high-bit byte l (offset 16).
+__device__ __forceinline__ void q5k_decode(const uint8_t* row, int b, int (&q)[8], float& dsc, float& dmm) {
+  const uint8_t* sb = row + (b >> 3) * 176;
+  const int j = b & 7;
+  k_quant_scales(lds128(sb), j, dsc, dmm);
+  const uint8_t* qs = sb + 48 + (j >> 1) * 32;
+  const uint4 q0 = lds128(qs), q1 = lds128(qs + 16);
+  const uint4 h0 = lds128(sb + 16), h1 = lds128(sb + 32);
+  const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+  const uint32_t h[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+  const int sh = (j & 1) * 4;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) q[i] = (int)(((w[i] >> sh) & 0x0F0F0F0Fu) | (((h[i] >> j) & 0x01010101u) << 4));
 }
 
 __device__ __forceinline__ int int_dot8(const int (&w)[8], const int (&q)[8]) {
@@ -355,6 +397,97 @@ __device__ __forceinline__ void q4_0_decode(const uint8_t* row, int b, int (&w)[
     const uint32_t c = lds16(blk + 2 + 4 * i) | ((uint32_t)lds16(blk + 4 + 4 * i) << 16);
     w[i] = (int)(c & 0x0F0F0F0Fu);
     w[i + 4] = (int)((c >> 4) & 0x0F0F0F0Fu);
+  }
+}
+
+// ------------------------------------------------------------------ Q4_1, Q5_0, Q5_1, MXFP4
+
+// Bits 0..3 of x to bit 4 of bytes 0..3 (the fifth code bit of four values):
+// the multiply places copies of x at bits 0, 7, 14 and 21, which do not
+// overlap, so bit k lands at bit 8k with no carries.
+__device__ __forceinline__ uint32_t q5_spread(uint32_t x) {
+  return (((x & 15u) * 0x00204081u) & 0x01010101u) << 4;
+}
+
+// Block b of a Q4_1 row (20-byte blocks, 4-byte aligned): unsigned codes,
+// d and m.
+__device__ __forceinline__ void q4_1_decode(const uint8_t* row, int b, int (&w)[8], float& d, float& m) {
+  const uint8_t* blk = row + 20 * b;
+  const uint32_t dm = lds32(blk);
+  d = f16_bits_to_f32(dm & 0xFFFFu);
+  m = f16_bits_to_f32(dm >> 16);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t c = lds32(blk + 4 + 4 * i);
+    w[i] = (int)(c & 0x0F0F0F0Fu);
+    w[i + 4] = (int)((c >> 4) & 0x0F0F0F0Fu);
+  }
+}
+
+// Block b of a Q5_0 row (22-byte blocks, 2-byte aligned): unsigned 5-bit
+// codes (the offset -16 goes through the activation's code sum) and d.
+__device__ __forceinline__ void q5_0_decode(const uint8_t* row, int b, int (&w)[8], float& d) {
+  const uint8_t* blk = row + 22 * b;
+  d = f16_bits_to_f32(lds16(blk));
+  const uint32_t qh = lds16(blk + 2) | ((uint32_t)lds16(blk + 4) << 16);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t c = lds16(blk + 6 + 4 * i) | ((uint32_t)lds16(blk + 8 + 4 * i) << 16);
+    w[i] = (int)((c & 0x0F0F0F0Fu) | q5_spread(qh >> (4 * i)));
+    w[i + 4] = (int)(((c >> 4) & 0x0F0F0F0Fu) | q5_spread(qh >> (16 + 4 * i)));
+  }
+}
+
+// Block b of a Q5_1 row (24-byte blocks, 8-byte aligned): unsigned 5-bit
+// codes, d and m.
+__device__ __forceinline__ void q5_1_decode(const uint8_t* row, int b, int (&w)[8], float& d, float& m) {
+  const uint8_t* blk = row + 24 * b;
+  const uint32_t dm = lds32(blk), qh = lds32(blk + 4);
+  d = f16_bits_to_f32(dm & 0xFFFFu);
+  m = f16_bits_to_f32(dm >> 16);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t c = lds32(blk + 8 + 4 * i);
+    w[i] = (int)((c & 0x0F0F0F0Fu) | q5_spread(qh >> (4 * i)));
+    w[i + 4] = (int)(((c >> 4) & 0x0F0F0F0Fu) | q5_spread(qh >> (16 + 4 * i)));
+  }
+}
+
+// Four 4-bit codes (one per byte, 0..15) as signed bytes 2*E2M1(code): the
+// codes packed as a 16-bit prmt selector, then the sign-split lookup of
+// nvfp4_words made signed as in nvfp4_signed.
+__device__ __forceinline__ uint32_t e2m1x4_signed(uint32_t codes) {
+  const uint32_t t = codes | (codes >> 4);
+  const uint32_t sel = (t & 0xFFu) | ((t >> 8) & 0xFF00u);
+  const uint32_t pos = prmt(kE2M1x2Lo, kE2M1x2Hi, sel);
+  const uint32_t neg = prmt(kE2M1x2Lo, kE2M1x2Hi, sel ^ 0x8888u);
+  return pos | ((0x80808080u - neg) ^ 0x80808080u);
+}
+
+// Block b of an MXFP4 row (17-byte blocks, any alignment): the 32 values
+// 2*E2M1(code) as signed int8x4 words in value order, and 2^(e - 127).  The
+// block is read as five aligned words starting at or below it (up to 3
+// bytes before and 3 bytes past its 17 bytes, inside the row's 4-byte
+// rounded span) and realigned with funnel shifts.
+__device__ __forceinline__ void mxfp4_decode(const uint8_t* row, int b, int (&w)[8], float& scale) {
+  const uint8_t* blk = row + 17 * b;
+  const uint32_t mis = (uint32_t)(reinterpret_cast<uintptr_t>(blk) & 3u);
+  const uint8_t* a = blk - mis;
+  uint32_t r[5];
+#pragma unroll
+  for (int i = 0; i < 5; ++i) r[i] = lds32(a + 4 * i);
+  const uint32_t sh = 8u * mis;
+  uint32_t v[5];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) v[i] = __funnelshift_r(r[i], r[i + 1], sh);
+  v[4] = r[4] >> sh;
+  const uint32_t e = v[0] & 0xFFu;
+  scale = e ? __uint_as_float(e << 23) : __uint_as_float(0x00400000u);   // 2^(e - 127)
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t c = __funnelshift_r(v[i], v[i + 1], 8);   // code bytes 4i .. 4i+3
+    w[i] = (int)e2m1x4_signed(c & 0x0F0F0F0Fu);
+    w[i + 4] = (int)e2m1x4_signed((c >> 4) & 0x0F0F0F0Fu);
   }
 }
 

@@ -498,6 +498,11 @@ static cudaError_t dispatch_ls(const DecodeParams& p, cudaStream_t stream, bool 
     case W_Q8_0: return launch_ls_t<W_Q8_0, W_Q8_0, 8>(p, stream, probe_only, fits);
     case W_Q6_K: return launch_ls_t<W_Q6_K, W_Q6_K, 4>(p, stream, probe_only, fits);
     case W_Q4_0: return launch_ls_t<W_Q4_0, W_Q4_0, 8>(p, stream, probe_only, fits);
+    case W_Q4_1: return launch_ls_t<W_Q4_1, W_Q4_1, 8>(p, stream, probe_only, fits);
+    case W_Q5_0: return launch_ls_t<W_Q5_0, W_Q5_0, 8>(p, stream, probe_only, fits);
+    case W_Q5_1: return launch_ls_t<W_Q5_1, W_Q5_1, 8>(p, stream, probe_only, fits);
+    case W_Q5_K: return launch_ls_t<W_Q5_K, W_Q5_K, 4>(p, stream, probe_only, fits);
+    case W_MXFP4: return launch_ls_t<W_MXFP4, W_MXFP4, 8>(p, stream, probe_only, fits);
     default: return launch_ls_t<W_BF16, W_BF16, 16>(p, stream, probe_only, fits);
   }
 }

@@ -223,6 +223,11 @@ cudaError_t launch_linear(const LinParams& p, cudaStream_t stream) {
     case W_Q8_0: return launch_lin_w<W_Q8_0>(p, p.grid, smem, stream);
     case W_Q6_K: return launch_lin_w<W_Q6_K>(p, p.grid, smem, stream);
     case W_Q4_0: return launch_lin_w<W_Q4_0>(p, p.grid, smem, stream);
+    case W_Q4_1: return launch_lin_w<W_Q4_1>(p, p.grid, smem, stream);
+    case W_Q5_0: return launch_lin_w<W_Q5_0>(p, p.grid, smem, stream);
+    case W_Q5_1: return launch_lin_w<W_Q5_1>(p, p.grid, smem, stream);
+    case W_Q5_K: return launch_lin_w<W_Q5_K>(p, p.grid, smem, stream);
+    case W_MXFP4: return launch_lin_w<W_MXFP4>(p, p.grid, smem, stream);
   }
   return cudaErrorInvalidValue;
 }

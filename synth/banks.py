@@ -21,8 +21,6 @@ import numpy as np
 
 BF16, Q8_0, Q4_K, NVFP4, Q6_K, Q4_0 = 0, 1, 2, 3, 4, 5
 Q4_1, Q5_0, Q5_1, Q5_K, MXFP4 = 6, 7, 8, 9, 10
-# types with no converter here: their "converted" rows are counter-based rows
-COUNTER_ONLY = (Q4_1, Q5_0, Q5_1, Q5_K, MXFP4)
 
 
 def rng(seed: int) -> np.random.Generator:
@@ -201,6 +199,99 @@ def convert_q4_0(w: np.ndarray) -> np.ndarray:
     return out.reshape(R, nb * 18)
 
 
+def _f16_bytes(v: np.ndarray) -> np.ndarray:
+    """fp16 values [...] -> their two little-endian bytes [..., 2]."""
+    return v.astype(np.float16).view(np.uint16)[..., None].view(np.uint8).reshape(v.shape + (2,))
+
+
+def _nibble_split(q: np.ndarray) -> np.ndarray:
+    """32 codes (0..15) per block -> 16 bytes: value j low nibble, j+16 high."""
+    return (q[..., :16] | (q[..., 16:] << 4)).astype(np.uint8)
+
+
+def _q5_high_word(q: np.ndarray) -> np.ndarray:
+    """The fifth bits of 32 5-bit codes as 4 little-endian bytes (bit j: value j)."""
+    bits = ((q >> 4) & 1).astype(np.uint64)
+    word = (bits << np.arange(32, dtype=np.uint64)).sum(axis=-1).astype(np.uint32)
+    return word[..., None].view(np.uint8).reshape(q.shape[:-1] + (4,))
+
+
+def convert_q4_1_q5(w: np.ndarray, wtype: int) -> np.ndarray:
+    """Q4_1 / Q5_0 / Q5_1 rows from fp32 [R, K], per 32 values.  Q4_1 and
+    Q5_1 (value d*q + m): m = fp16(min), d = fp16((max - min) / (2^bits - 1)),
+    q = round((w - m) / d) clipped.  Q5_0 (value d*(q - 16)): d = fp16(amax /
+    15), q = round(w / d) + 16 clipped to 0..31."""
+    R, K = w.shape
+    x = w.astype(np.float64).reshape(R, K // 32, 32)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        if wtype == Q5_0:
+            d = (np.abs(x).max(axis=-1) / 15.0).astype(np.float16)
+            d64 = d.astype(np.float64)
+            q = (np.where(d64[..., None] > 0, np.rint(x / np.where(d64 > 0, d64, 1)[..., None]), 0) + 16).clip(0, 31)
+            m = None
+        else:
+            top = 15.0 if wtype == Q4_1 else 31.0
+            m = x.min(axis=-1).astype(np.float16)
+            d = ((x.max(axis=-1) - m.astype(np.float64)) / top).astype(np.float16)
+            d64 = d.astype(np.float64)
+            q = np.where(d64[..., None] > 0,
+                         np.rint((x - m.astype(np.float64)[..., None]) / np.where(d64 > 0, d64, 1)[..., None]),
+                         0).clip(0, top)
+    q = q.astype(np.int64)
+    parts = [_f16_bytes(d)]
+    if m is not None:
+        parts.append(_f16_bytes(m))
+    if wtype != Q4_1:
+        parts.append(_q5_high_word(q))
+    parts.append(_nibble_split(q & 15))
+    return np.concatenate(parts, axis=-1).reshape(R, -1)
+
+
+def convert_q5k(w: np.ndarray) -> np.ndarray:
+    """Q5_K rows from fp32 [R, K]: the Q4_K min/max encoder with 5-bit codes
+    (step = (max - lo) / 31), the low 4 bits laid out as Q4_K, the fifth bit
+    of value l of sub-block j in bit j of high-bit byte l."""
+    R, K = w.shape
+    nsb = K // 256
+    x = w.astype(np.float64).reshape(R, nsb, 8, 32)
+    lo = np.minimum(0.0, x.min(axis=-1))
+    step = (x.max(axis=-1) - lo) / 31.0
+    d = (step.max(axis=-1) / 63.0).astype(np.float16)
+    dmin = ((-lo).max(axis=-1) / 63.0).astype(np.float16)
+    d64, dmin64 = d.astype(np.float64), dmin.astype(np.float64)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        sc = np.where(d64[..., None] > 0, np.rint(step / d64[..., None]), 0).clip(0, 63).astype(np.int64)
+        mn = np.where(dmin64[..., None] > 0, np.rint(-lo / dmin64[..., None]), 0).clip(0, 63).astype(np.int64)
+        eff = d64[..., None] * sc
+        q = np.where(eff[..., None] > 0,
+                     np.rint((x + (dmin64[..., None] * mn)[..., None]) / np.where(eff > 0, eff, 1)[..., None]),
+                     0).clip(0, 31).astype(np.int64)
+    out = np.zeros((R, nsb, 176), dtype=np.uint8)
+    out[..., 0:2] = _f16_bytes(d)
+    out[..., 2:4] = _f16_bytes(dmin)
+    out[..., 4:16] = _pack_q4k_scales(sc, mn)
+    hb = ((q >> 4) & 1).astype(np.uint8)                  # [R, nsb, 8, 32]
+    out[..., 16:48] = (hb << np.arange(8, dtype=np.uint8)[:, None]).sum(axis=-2).astype(np.uint8)
+    qq = (q & 15).astype(np.uint8).reshape(R, nsb, 4, 2, 32)
+    out[..., 48:176] = (qq[..., 0, :] | (qq[..., 1, :] << 4)).reshape(R, nsb, 128)
+    return out.reshape(R, nsb * 176)
+
+
+def convert_mxfp4(w: np.ndarray) -> np.ndarray:
+    """MXFP4 rows from fp32 [R, K]: per 32 values the E8M0 exponent e =
+    127 + ceil(log2(amax / 6)) (so amax / 2^(e-127) <= 6), codes the nearest
+    E2M1 of w / 2^(e-127)."""
+    R, K = w.shape
+    x = w.astype(np.float64).reshape(R, K // 32, 32)
+    amax = np.abs(x).max(axis=-1)
+    with np.errstate(divide="ignore"):
+        ex = np.where(amax > 0, np.ceil(np.log2(np.where(amax > 0, amax, 1) / 6.0)), -127)
+    e = np.clip(ex + 127, 0, 254).astype(np.int64)
+    codes = _e2m1_code(x / np.ldexp(1.0, e - 127)[..., None]).astype(np.int64)
+    out = np.concatenate([e.astype(np.uint8)[..., None], _nibble_split(codes)], axis=-1)
+    return out.reshape(R, -1)
+
+
 def q8_0_codes_bank(seed: int, rows: int, k: int) -> np.ndarray:
     """Q8_0 rows with int8 codes uniform in [-127, 127] and fp16 scales
     uniform in (1e-4, 5e-4) (the tiny single-layer configuration)."""
@@ -217,16 +308,10 @@ def q8_0_codes_bank(seed: int, rows: int, k: int) -> np.ndarray:
 def converted_expert(seed: int, e: int, H: int, I: int, gate_up_type: int, down_type: int):
     """One converted expert: (gate_up uint8 [2I, rb_gu], down uint8 [H, rb_d],
     scales fp32 [4]).  Weights ~ N(0, 0.02) (Q8_0: the direct code recipe);
-    NVFP4 projections get s2 = amax / (6 * 448) each (gate, up, down).  The
-    COUNTER_ONLY types take counter-based rows (every code pattern, scales
-    masked to a realistic range) instead of converted weights."""
+    NVFP4 projections get s2 = amax / (6 * 448) each (gate, up, down)."""
     r = rng(seed * 100003 + e)
     sc = np.ones(4, dtype=np.float32)
-    if gate_up_type in COUNTER_ONLY or down_type in COUNTER_ONLY:
-        from . import counter
-    if gate_up_type in COUNTER_ONLY:
-        gu = counter.bank_bytes_np(seed * 100003 + e, gate_up_type, H, 0, 2 * I)
-    elif gate_up_type == Q8_0:
+    if gate_up_type == Q8_0:
         gu = q8_0_codes_bank(seed * 100003 + e, 2 * I, H)
     else:
         wg = (r.standard_normal((2 * I, H)) * 0.02).astype(np.float32)
@@ -243,11 +328,15 @@ def converted_expert(seed: int, e: int, H: int, I: int, gate_up_type: int, down_
             gu = convert_q6k(wg)
         elif gate_up_type == Q4_0:
             gu = convert_q4_0(wg)
+        elif gate_up_type in (Q4_1, Q5_0, Q5_1):
+            gu = convert_q4_1_q5(wg, gate_up_type)
+        elif gate_up_type == Q5_K:
+            gu = convert_q5k(wg)
+        elif gate_up_type == MXFP4:
+            gu = convert_mxfp4(wg)
         else:
             gu = convert_bf16(wg)
-    if down_type in COUNTER_ONLY:
-        dn = counter.bank_bytes_np(seed * 100003 + e + 50000, down_type, I, 0, H)
-    elif down_type == Q8_0:
+    if down_type == Q8_0:
         dn = q8_0_codes_bank(seed * 100003 + e + 50000, H, I)
     else:
         wd = (r.standard_normal((H, I)) * 0.02).astype(np.float32)
@@ -261,6 +350,12 @@ def converted_expert(seed: int, e: int, H: int, I: int, gate_up_type: int, down_
             dn = convert_q6k(wd)
         elif down_type == Q4_0:
             dn = convert_q4_0(wd)
+        elif down_type in (Q4_1, Q5_0, Q5_1):
+            dn = convert_q4_1_q5(wd, down_type)
+        elif down_type == Q5_K:
+            dn = convert_q5k(wd)
+        elif down_type == MXFP4:
+            dn = convert_mxfp4(wd)
         else:
             dn = convert_bf16(wd)
     return gu, dn, sc

@@ -58,7 +58,9 @@ def test_q8_1_quantizer_bit_exact():
 @pytest.mark.parametrize("wtype,k", [(F.TYPE_Q8_0, 256), (F.TYPE_Q8_0, 768), (F.TYPE_NVFP4, 2048),
                                      (F.TYPE_NVFP4, 768), (F.TYPE_Q4_K, 4096), (F.TYPE_Q4_K, 768),
                                      (F.TYPE_Q6_K, 2048), (F.TYPE_Q6_K, 768), (F.TYPE_Q4_0, 2048),
-                                     (F.TYPE_Q4_0, 96)])
+                                     (F.TYPE_Q4_0, 96), (F.TYPE_Q4_1, 256), (F.TYPE_Q5_0, 96),
+                                     (F.TYPE_Q5_1, 256), (F.TYPE_Q5_K, 768), (F.TYPE_MXFP4, 96),
+                                     (F.TYPE_MXFP4, 2048)])
 def test_block_dots_bit_exact(wtype, k):
     rows = C.bank_bytes_np(11 + wtype, wtype, k, 0, 64)
     # every byte pattern: raw random codes, including all E2M1 signs and -0
@@ -66,11 +68,15 @@ def test_block_dots_bit_exact(wtype, k):
     a = r.standard_normal(k).astype(np.float32)
     qs, d, s, _ = F.quantize_q8_1(a)
     act = F.q8_1_pack_blocks(qs, d, s).reshape(-1)
-    rows_d = torch.from_numpy(rows.reshape(-1).copy()).to(DEV)
+    # banks are readable to the next 16-byte boundary past their end (MXFP4
+    # blocks are read as aligned words)
+    rows_d = torch.zeros(rows.size + 16, dtype=torch.uint8, device=DEV)
+    rows_d[: rows.size].copy_(torch.from_numpy(rows.reshape(-1).copy()))
     act_d = torch.from_numpy(act).to(DEV)
     # Q6_K at k=768 (630-byte rows) and Q4_0 (18-byte blocks) put blocks at
     # every 2-byte alignment
     nb = k // 16 if wtype in (F.TYPE_NVFP4, F.TYPE_Q6_K) else k // 32
+    assert nb == F.block_dots(wtype, rows[:1], k, np.zeros((k // 32, 32), np.int8)).shape[1]
     out = torch.empty((64, nb), dtype=torch.int32, device=DEV)
     capi.moe_debug_block_dots(wtype, rows_d.data_ptr(), 64, k, act_d.data_ptr(), out.data_ptr(), _stream())
     torch.cuda.synchronize()
@@ -156,7 +162,9 @@ def test_laguna_zipf_batches_sampled(T):
                                        (F.TYPE_NVFP4, F.TYPE_Q8_0), (F.TYPE_Q8_0, F.TYPE_NVFP4),
                                        (F.TYPE_BF16, F.TYPE_NVFP4), (F.TYPE_Q6_K, F.TYPE_Q4_0),
                                        (F.TYPE_Q4_0, F.TYPE_Q6_K), (F.TYPE_BF16, F.TYPE_Q6_K),
-                                       (F.TYPE_Q6_K, F.TYPE_NVFP4), (F.TYPE_Q4_0, F.TYPE_Q8_0)])
+                                       (F.TYPE_Q6_K, F.TYPE_NVFP4), (F.TYPE_Q4_0, F.TYPE_Q8_0),
+                                       (F.TYPE_Q5_K, F.TYPE_Q4_1), (F.TYPE_Q5_0, F.TYPE_MXFP4),
+                                       (F.TYPE_MXFP4, F.TYPE_Q5_1), (F.TYPE_Q4_1, F.TYPE_Q5_K)])
 def test_mixed_type_pairs(gu_t, dn_t):
     """Gate_up and down of different types: the two-kernel path."""
     case = cases.make_case(512, 256, 16, 4, gu_t, dn_t, 5, seed=40 + 8 * gu_t + dn_t)
@@ -202,6 +210,16 @@ def test_qwen3_30b_a3b_shaped_q6_k_layer(T):
     figs = _check_case(case)
     if T == 1:
         assert figs["launches"] == 1
+    assert figs["err_bits"] == 0
+
+
+@pytest.mark.parametrize("wtype", [F.TYPE_Q4_1, F.TYPE_Q5_0, F.TYPE_Q5_1, F.TYPE_Q5_K, F.TYPE_MXFP4])
+def test_more_gguf_types_fused_layer(wtype):
+    """H=2048 I=768 E=128 top-8, T=1, one fused launch, counter-based rows
+    (every code pattern) for Q4_1, Q5_0, Q5_1, Q5_K and MXFP4 banks."""
+    case = cases.make_case(2048, 768, 128, 8, wtype, wtype, 1, seed=140 + wtype)
+    figs = _check_case(case)
+    assert figs["launches"] == 1
     assert figs["err_bits"] == 0
 
 

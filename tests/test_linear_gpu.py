@@ -55,9 +55,12 @@ def _rows(seed, wtype, K, N):
     return rows, dev
 
 
-@pytest.mark.parametrize("wtype,K", [(F.TYPE_NVFP4, 2048), (F.TYPE_NVFP4, 160), (F.TYPE_Q4_K, 2048),
-                                     (F.TYPE_Q8_0, 768), (F.TYPE_Q6_K, 768), (F.TYPE_Q4_0, 2048)])
-@pytest.mark.parametrize("T", [1, 3, 8])
+@pytest.mark.parametrize("wtype,K,T", [(w, k, t) for w, k in [(F.TYPE_NVFP4, 2048), (F.TYPE_NVFP4, 160),
+                                                             (F.TYPE_Q4_K, 2048), (F.TYPE_Q8_0, 768),
+                                                             (F.TYPE_Q6_K, 768), (F.TYPE_Q4_0, 2048)]
+                                       for t in (1, 3, 8)] +
+                         [(F.TYPE_Q4_1, 768, 3), (F.TYPE_Q5_0, 2048, 1), (F.TYPE_Q5_1, 160, 8),
+                          (F.TYPE_Q5_K, 768, 3), (F.TYPE_MXFP4, 2048, 1), (F.TYPE_MXFP4, 160, 3)])
 def test_linear_matches_oracle(wtype, K, T):
     """N = 1000 rows (a ragged share per CTA and per ring slot), per-row
     scales of three parts (a fused qkv-like module); NVFP4 at K = 160 has

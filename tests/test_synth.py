@@ -75,3 +75,20 @@ def test_routings():
     assert all(len(set(row)) == 10 for row in ids) and np.allclose(w.sum(1), 1, atol=1e-6)
     # Zipf popularity: far fewer distinct experts than uniform routing would give
     assert len(np.unique(ids)) < 200
+
+
+def test_converted_q4_1_q5_q5k_mxfp4_reconstruct():
+    """The encoders of the other GGUF types round-trip N(0, 0.02) weights
+    through the oracle's decoders within their code steps."""
+    r = np.random.default_rng(3)
+    w = (r.standard_normal((4, 512)) * 0.02).astype(np.float32)
+    for wtype, enc, tol in [(F.TYPE_Q4_1, lambda v: S.convert_q4_1_q5(v, S.Q4_1), 0.08),
+                            (F.TYPE_Q5_0, lambda v: S.convert_q4_1_q5(v, S.Q5_0), 0.06),
+                            (F.TYPE_Q5_1, lambda v: S.convert_q4_1_q5(v, S.Q5_1), 0.04),
+                            (F.TYPE_Q5_K, S.convert_q5k, 0.06),
+                            (F.TYPE_MXFP4, S.convert_mxfp4, 0.15)]:
+        rows = enc(w)
+        assert rows.shape == (4, F.row_bytes(wtype, 512))
+        back = F.dequantize_rows(wtype, rows, 512)
+        rel = np.linalg.norm(back - w) / np.linalg.norm(w)
+        assert rel < tol, (wtype, rel)
