@@ -270,16 +270,24 @@ class Stack:
 # DRAM bytes of one k_layer_small launch (NVFP4 layer, T=1) from an ncu capture
 # (dram__bytes_read.sum + dram__bytes_write.sum); valid only for the kernel
 # source it was taken on.
-TRAFFIC = {"file": "quantized_routed_expert_route_gb300/csrc/layer_small.cu",
-           "sha1": "178bc0a816245293ca5905a693df15852c714cc8", "bytes": 21380096}
+# ncu DRAM bytes (read + write) of one headline k_layer_small launch, valid
+# while the sources its code comes from are unchanged (one SHA-1 over them)
+TRAFFIC = {"files": ["quantized_routed_expert_route_gb300/csrc/layer_small.cu",
+                     "quantized_routed_expert_route_gb300/csrc/decode_common.cuh",
+                     "quantized_routed_expert_route_gb300/csrc/formats.cuh",
+                     "quantized_routed_expert_route_gb300/csrc/ptx.cuh"],
+           "sha1": "f05564b4d6c0abcdf6e94cd329709ca92932fc31", "bytes": None}
 
 
 def traffic_bytes():
     import hashlib
-    p = os.path.join(ROOT, TRAFFIC["file"])
-    if not os.path.exists(p):
-        return None
-    return TRAFFIC["bytes"] if hashlib.sha1(open(p, "rb").read()).hexdigest() == TRAFFIC["sha1"] else None
+    h = hashlib.sha1()
+    for f in TRAFFIC["files"]:
+        p = os.path.join(ROOT, f)
+        if not os.path.exists(p):
+            return None
+        h.update(open(p, "rb").read())
+    return TRAFFIC["bytes"] if h.hexdigest() == TRAFFIC["sha1"] else None
 
 
 PREFILL = dict(H=2048, I=768, E=128, K=8, T=4096)
