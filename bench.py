@@ -276,7 +276,7 @@ TRAFFIC = {"files": ["quantized_routed_expert_route_gb300/csrc/layer_small.cu",
                      "quantized_routed_expert_route_gb300/csrc/decode_common.cuh",
                      "quantized_routed_expert_route_gb300/csrc/formats.cuh",
                      "quantized_routed_expert_route_gb300/csrc/ptx.cuh"],
-           "sha1": "f05564b4d6c0abcdf6e94cd329709ca92932fc31", "bytes": None}
+           "sha1": "f05564b4d6c0abcdf6e94cd329709ca92932fc31", "bytes": 21380096}
 
 
 def traffic_bytes():
