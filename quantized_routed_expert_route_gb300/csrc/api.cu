@@ -104,7 +104,8 @@ enum { kGroupedNone = 0, kGroupedDense = 1, kGroupedQuant = 2 };
 
 int grouped_kind(const moe_layer_geom& g) {
   if (g.gate_up_type == MOE_BF16 && g.down_type == MOE_BF16 && g.H % 64 == 0 && g.I % 64 == 0) return kGroupedDense;
-  if ((g.gate_up_type == MOE_Q4_K || g.gate_up_type == MOE_NVFP4) && g.down_type == g.gate_up_type &&
+  if ((g.gate_up_type == MOE_Q4_K || g.gate_up_type == MOE_Q4_0 || g.gate_up_type == MOE_NVFP4) &&
+      g.down_type == g.gate_up_type &&
       g.H % 256 == 0 && g.I % 256 == 0)
     return kGroupedQuant;
   return kGroupedNone;
@@ -316,7 +317,8 @@ DecodeParams make_params(const moe_bank* b, const WsLayout& L, uint8_t* ws, cons
   // The grouped paths take over from the fused kernel once they are faster
   // (measured: BF16 from 2 tokens; Q4_K from 20 routes per pass, the
   // Laguna-shaped layer at T=2; NVFP4 between 16 and 32 routes, the
-  // Qwen3-30B-A3B-shaped layer at T=2 and T=4).
+  // Qwen3-30B-A3B-shaped layer at T=2 and T=4; Q4_0 takes the Q4_K
+  // threshold: the same bytes per 256 values and the same kernel).
   const int RTn = T * g.top_k;
   if ((b->grouped == kGroupedDense && T >= 2) || (b->grouped == kGroupedQuant && RTn >= 20)) p.use_ls = 0;
   switch (p.gu_type) {
@@ -416,7 +418,7 @@ int moe_bank_create(const moe_layer_geom* geom, const void* gate_up, size_t gate
       map_bf16_rows(&b->map_gu, b->gu, (uint64_t)g.E * 2 * g.I, (uint64_t)g.H, 128) &&
       map_bf16_rows(&b->map_dn, b->dn, (uint64_t)g.E * g.H, (uint64_t)g.I, 128))
     b->grouped = kGroupedDense;
-  if (gk == kGroupedQuant && g.gate_up_type == MOE_Q4_K &&
+  if (gk == kGroupedQuant && (g.gate_up_type == MOE_Q4_K || g.gate_up_type == MOE_Q4_0) &&
       map_byte_rows(&b->map_gu, b->gu, (uint64_t)g.E * 2 * g.I, (uint64_t)rb_gu, 144, 128) &&
       map_byte_rows(&b->map_dn, b->dn, (uint64_t)g.E * g.H, (uint64_t)rb_dn, 144, 128))
     b->grouped = kGroupedQuant;

@@ -1,4 +1,4 @@
-// Batched decode path for Q4_K banks.
+// Batched decode path for Q4_K, Q4_0 and NVFP4 banks.
 //
 // At batches the fused small-batch kernel cannot hold, a Q4_K layer has
 // several tokens routed to many of its selected experts.  The pass still
@@ -231,6 +231,68 @@ __device__ __forceinline__ void qb_chunk(const uint8_t* rowa, const uint8_t* row
   }
 }
 
+// The 36 bytes of quarter Q (blocks 2Q and 2Q+1) of a row's Q4_0 K chunk
+// (eight 18-byte blocks, 144 bytes, rows 144 bytes apart) as nine words:
+// three conflict-free 16-byte loads from the 16-byte boundary 32Q at or below
+// byte 36Q, of which words Q .. Q+8 are the quarter's (32Q + 48 >= 36Q + 36
+// for Q <= 3, and 32Q + 48 <= 144).
+template <int Q>
+__device__ __forceinline__ void q4_0_quarter(const uint8_t* row, uint32_t (&w)[9]) {
+  const uint4 a = lds128(row + 32 * Q), b = lds128(row + 32 * Q + 16), c = lds128(row + 32 * Q + 32);
+  const uint32_t all[12] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w, c.x, c.y, c.z, c.w};
+#pragma unroll
+  for (int i = 0; i < 9; ++i) w[i] = all[Q + i];
+}
+
+// Unsigned codes (low nibbles: values 0..15, high: 16..31) and d of the two
+// blocks of a quarter: block 2Q is bytes 0..17 (d, then codes from byte 2),
+// block 2Q+1 bytes 18..35 (d in the high half of word 4, codes in words 5..8).
+__device__ __forceinline__ void q4_0_quarter_codes(const uint32_t (&w)[9], int (&c0)[8], int (&c1)[8], float& d0,
+                                                   float& d1) {
+  d0 = f16_bits_to_f32(w[0] & 0xFFFFu);
+  d1 = f16_bits_to_f32(w[4] >> 16);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t x = __funnelshift_r(w[i], w[i + 1], 16), y = w[5 + i];
+    c0[i] = (int)(x & 0x0F0F0F0Fu);
+    c0[i + 4] = (int)((x >> 4) & 0x0F0F0F0Fu);
+    c1[i] = (int)(y & 0x0F0F0F0Fu);
+    c1[i + 4] = (int)((y >> 4) & 0x0F0F0F0Fu);
+  }
+}
+
+// Q4_0 blocks 2Q and 2Q+1 of one K chunk of rows a and b against the tile's
+// tokens: each block's dot is d_a * d * (sum(q * a_q) - 8 * sum(a_q)).
+template <int REC_PITCH, int Q>
+__device__ __forceinline__ void qb_chunk_q4_0(const uint8_t* rowa, const uint8_t* rowb, const uint8_t* codes,
+                                              const uint8_t* recs, int nv, float (&acca)[kQbTok],
+                                              float (&accb)[kQbTok]) {
+  int a0[8], a1[8], b0[8], b1[8];
+  float da0, da1, db0, db1;
+  {
+    uint32_t w[9];
+    q4_0_quarter<Q>(rowa, w);
+    q4_0_quarter_codes(w, a0, a1, da0, da1);
+    q4_0_quarter<Q>(rowb, w);
+    q4_0_quarter_codes(w, b0, b1, db0, db1);
+  }
+#pragma unroll
+  for (int t = 0; t < kQbTok; ++t) {
+    if (t >= nv) break;
+    const uint8_t* cp = codes + t * 256 + 64 * Q;
+    const uint4 q0 = lds128(cp), q1 = lds128(cp + 16), q2 = lds128(cp + 32), q3 = lds128(cp + 48);
+    const uint4 rc = lds128(recs + t * REC_PITCH + 16 * Q);   // (d, sum) of blocks 2Q and 2Q+1
+    const int ql[8] = {(int)q0.x, (int)q0.y, (int)q0.z, (int)q0.w, (int)q1.x, (int)q1.y, (int)q1.z, (int)q1.w};
+    const int qh[8] = {(int)q2.x, (int)q2.y, (int)q2.z, (int)q2.w, (int)q3.x, (int)q3.y, (int)q3.z, (int)q3.w};
+    const float e0 = __uint_as_float(rc.x), e1 = __uint_as_float(rc.z);
+    const int s0 = 8 * (int)rc.y, s1 = 8 * (int)rc.w;
+    acca[t] += e0 * (da0 * (float)(int_dot8(a0, ql) - s0));
+    accb[t] += e0 * (db0 * (float)(int_dot8(b0, ql) - s0));
+    acca[t] += e1 * (da1 * (float)(int_dot8(a1, qh) - s1));
+    accb[t] += e1 * (db1 * (float)(int_dot8(b1, qh) - s1));
+  }
+}
+
 // NVFP4 blocks 2q and 2q+1 of one K chunk for rows a and b (unit u of the
 // tile): each row's 128 code bytes sit in a 128-byte-swizzled tile (16-byte
 // chunk j of row u at position j ^ (u % 8)), its 16 UE4M3 bytes at scl + 16u
@@ -404,7 +466,7 @@ __global__ void __launch_bounds__(kQbThreads, 1) k_qb_gemm(const __grid_constant
           const CUtensorMap* mw = PHASE == 0 ? &p.map_wgu : &p.map_wdn;
           mbar_arrive_expect_tx(&full_bar[s], PHASE == 0 ? (uint32_t)(kQbCodesOff + nv * 320)
                                                          : (uint32_t)(kQbRecOff + kQbTok * 64));
-          if (WT == W_Q4_K) {
+          if (WT == W_Q4_K || WT == W_Q4_0) {   // both 144 bytes per 256-value chunk of a row
             tma_load_2d_hint(st, mw, kc * kQbSb, ya, &full_bar[s], pol);
             tma_load_2d_hint(st + 128 * kQbSb, mw, kc * kQbSb, yb, &full_bar[s], pol);
           } else {
@@ -457,10 +519,19 @@ __global__ void __launch_bounds__(kQbThreads, 1) k_qb_gemm(const __grid_constant
       for (int i = 0; i < kQbTok; ++i) acca[i] = accb[i] = 0.f;
     }
     const uint8_t* st = base + s * kQbStageBytes;
-    if (WT == W_Q4_K)
+    if (WT == W_Q4_K) {
       qb_chunk<PHASE == 0 ? 128 : 64>(st + u * kQbSb, st + (128 + u) * kQbSb, st + kQbCodesOff, st + kQbRecOff, q,
                                       nv, acca, accb);
-    else
+    } else if (WT == W_Q4_0) {
+      constexpr int RP = PHASE == 0 ? 128 : 64;
+      const uint8_t *ra = st + u * kQbSb, *rb = st + (128 + u) * kQbSb;
+      switch (q) {   // warp-uniform: the quarter's word offset is a compile-time constant
+        case 0: qb_chunk_q4_0<RP, 0>(ra, rb, st + kQbCodesOff, st + kQbRecOff, nv, acca, accb); break;
+        case 1: qb_chunk_q4_0<RP, 1>(ra, rb, st + kQbCodesOff, st + kQbRecOff, nv, acca, accb); break;
+        case 2: qb_chunk_q4_0<RP, 2>(ra, rb, st + kQbCodesOff, st + kQbRecOff, nv, acca, accb); break;
+        default: qb_chunk_q4_0<RP, 3>(ra, rb, st + kQbCodesOff, st + kQbRecOff, nv, acca, accb); break;
+      }
+    } else
       qb_chunk_nvfp4<PHASE == 0 ? 128 : 64>(st, st + 16384, st + 32768, st + 34816, u, st + kQbCodesOff,
                                             st + kQbRecOff, q, nv, acca, accb);
     mbar_arrive(&empty_bar[s]);
@@ -568,6 +639,9 @@ cudaError_t launch_qbatch(const QbParams& p, cudaStream_t stream) {
   if (p.wt == W_NVFP4) {
     if ((e = launch_qb(k_qb_gemm<0, W_NVFP4>, G, kQbThreads, qb_gemm_smem(), stream, p)) != cudaSuccess) return e;
     if ((e = launch_qb(k_qb_gemm<1, W_NVFP4>, G, kQbThreads, qb_gemm_smem(), stream, p)) != cudaSuccess) return e;
+  } else if (p.wt == W_Q4_0) {
+    if ((e = launch_qb(k_qb_gemm<0, W_Q4_0>, G, kQbThreads, qb_gemm_smem(), stream, p)) != cudaSuccess) return e;
+    if ((e = launch_qb(k_qb_gemm<1, W_Q4_0>, G, kQbThreads, qb_gemm_smem(), stream, p)) != cudaSuccess) return e;
   } else {
     if ((e = launch_qb(k_qb_gemm<0, W_Q4_K>, G, kQbThreads, qb_gemm_smem(), stream, p)) != cudaSuccess) return e;
     if ((e = launch_qb(k_qb_gemm<1, W_Q4_K>, G, kQbThreads, qb_gemm_smem(), stream, p)) != cudaSuccess) return e;

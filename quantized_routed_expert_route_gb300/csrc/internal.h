@@ -119,14 +119,14 @@ struct DtParams {
 constexpr int kQbTileTokens = 8;    // routed tokens per tile of the batched kernels
 struct QbParams {
   // banks as byte matrices [E*2I][rb_gu] and [E*H][rb_dn], boxes of 128 rows:
-  // Q4_K: map_w* boxes 144 bytes wide (one super-block); NVFP4: map_w* boxes
+  // Q4_K, Q4_0: map_w* boxes 144 bytes wide (256 values); NVFP4: map_w* boxes
   // the 128 code bytes of a chunk (128-byte swizzle), map_w*s its 16 scale bytes
   CUtensorMap map_wgu, map_wdn, map_wgus, map_wdns;
   CUtensorMap map_xq;       // xq [T][H], box 256 x 1 row
   CUtensorMap map_xr;       // xrec [T][H/4], box 64 x 1 row
   CUtensorMap map_iq;       // iqs [RTp][I], box 256 x kQbTileTokens rows
   CUtensorMap map_is;       // iss [RTp][I/4], box 64 x kQbTileTokens rows
-  int wt;                   // W_Q4_K or W_NVFP4 (both projections)
+  int wt;                   // W_Q4_K, W_Q4_0 or W_NVFP4 (both projections)
   int H, I, E, K, T, RT, RTp;
   int glu;
   const float* scales;      // [E][4]

@@ -1,4 +1,4 @@
-"""GPU parity of the batched path for Q4_K and NVFP4 banks: batches the fused
+"""GPU parity of the batched path for Q4_K, Q4_0 and NVFP4 banks: batches the fused
 small-batch kernel cannot hold, decoded by the grouped CUDA-core kernels
 (route + quantize, gate_up + requantize, down, route sum: four launches per
 pass).  Same bounds as the other decode tests (tests/tolerance.py),
@@ -22,6 +22,7 @@ from tests.test_decode_gpu import _check_case  # noqa: E402
 BATCHED_LAUNCHES = 4
 Q4K = F.TYPE_Q4_K
 NV4 = F.TYPE_NVFP4
+Q40 = F.TYPE_Q4_0
 
 
 @pytest.mark.parametrize("T", [16, 64])
@@ -44,7 +45,17 @@ def test_qwen3_30b_a3b_shaped_nvfp4_batches(T):
     assert figs["err_bits"] == 0
 
 
-@pytest.mark.parametrize("wtype", [Q4K, NV4])
+@pytest.mark.parametrize("T", [8, 24])
+def test_q4_0_32_experts_top8_batches(T):
+    """H=2048 I=768 E=32 top-8 Q4_0, softmax routing, every token checked
+    with the stage exports."""
+    case = cases.make_case(2048, 768, 32, 8, Q40, Q40, T, seed=360 + T)
+    figs = _check_case(case)
+    assert figs["launches"] == BATCHED_LAUNCHES
+    assert figs["err_bits"] == 0
+
+
+@pytest.mark.parametrize("wtype", [Q4K, NV4, Q40])
 def test_every_token_with_stages(wtype):
     """40 tokens over 24 experts (tiles of 1..8 tokens), every token checked
     with the stage exports."""
@@ -54,7 +65,7 @@ def test_every_token_with_stages(wtype):
     assert figs["err_bits"] == 0
 
 
-@pytest.mark.parametrize("wtype", [Q4K, NV4])
+@pytest.mark.parametrize("wtype", [Q4K, NV4, Q40])
 def test_one_expert_over_many_token_blocks(wtype):
     """Every route on one expert (duplicates inside each token): 256 routed
     rows, thirty-two 8-token blocks per weight tile."""
@@ -66,7 +77,7 @@ def test_one_expert_over_many_token_blocks(wtype):
     assert figs["err_bits"] == 0
 
 
-@pytest.mark.parametrize("wtype", [Q4K, NV4])
+@pytest.mark.parametrize("wtype", [Q4K, NV4, Q40])
 def test_bad_ids_flag_and_contribute_zero(wtype):
     T, K = 48, 3
     r = np.random.default_rng(7)
