@@ -363,6 +363,70 @@ int moe_debug_prefill_stages(const moe_bank* bank, const void* x, int32_t T,
 int moe_linear(int32_t type, const void* rows, int32_t N, int32_t K, const float* row_scale,
                const void* x, int32_t T, void* out, uint32_t* dev_err, void* stream);
 
+/* ---------------------------------------------------------------- expert cache
+ * For expert banks larger than the GPU's memory (FreeToken issue #194,
+ * "avoid max-stride padding for heterogeneous GGUF expert banks", Proposed
+ * design): a byte budget is split into exact-geometry slot pools, one per
+ * tuple of row sizes, each with its own LRU state keyed by (layer, expert);
+ * missed experts are copied from the layer's compact rows straight into
+ * their slots.  A pool is a bank whose experts are its slots, so a request
+ * decodes with moe_decode on moe_cache_bank() after its routing ids are
+ * replaced by the slot ids moe_cache_acquire returns. */
+
+/* Slots per geometry for a byte budget: with w_g = selections[g] (routed
+ * expert selections per token of the layers of geometry g, e.g. layers x
+ * top_k), n_g = floor(budget * w_g / sum_h w_h * expert_bytes[h]); the bytes
+ * left over then go one slot at a time to the smallest expert size that still
+ * fits.  (For 39 Q4_K layers of 5.0625 MiB experts and 8 BF16 layers of
+ * 18 MiB experts at top-10, the budget of 480 x 18 MiB gives 988 + 202 slots,
+ * the pages' Controlled A/B.)  slots: int64 [ngeom] out.  Host only. */
+int moe_cache_plan(int64_t budget_bytes, int32_t ngeom, const int64_t* expert_bytes,
+                   const int64_t* selections, int64_t* slots);
+
+/* The LRU state of one pool, on the host (no device memory). */
+typedef struct moe_slot_table moe_slot_table;
+int moe_slot_table_create(int32_t nslots, moe_slot_table** out);
+int moe_slot_table_destroy(moe_slot_table* table);
+
+/* Slots for one request of layer `layer`: ids int32 [n] (host) are expert ids
+ * of that layer; ids outside [0, E) get slot -1.  The request's distinct
+ * valid experts that are resident (hits) become the most recent first; each
+ * missing one then takes the least recently used slot (never-used slots are
+ * the least recent, lowest index first) and becomes the most recent, so a
+ * request never evicts its own experts.  Writes slot_ids [n], and for each
+ * miss, in first-occurrence order, fill_slots[i] / fill_experts[i] (capacity:
+ * the number of slots) with *nfill the count.  MOE_EUNSUPPORTED if the request
+ * names more distinct experts than there are slots (nothing changes). */
+int moe_slot_table_acquire(moe_slot_table* table, int32_t layer, const int32_t* ids, int32_t n, int32_t E,
+                           int32_t* slot_ids, int32_t* fill_slots, int32_t* fill_experts, int32_t* nfill);
+int moe_slot_table_stats(const moe_slot_table* table, int64_t* hits, int64_t* misses);
+
+/* One exact-geometry pool of nslots slots on the device (1..MOE_MAX_E; the
+ * geometry's E is ignored, its top_k must not exceed nslots).  Allocates
+ * nslots expert rows of each projection (+256 bytes) and zeroes them on
+ * `stream`. */
+typedef struct moe_cache moe_cache;
+int moe_cache_create(const moe_layer_geom* geom, int32_t nslots, void* stream, moe_cache** out);
+int moe_cache_destroy(moe_cache* cache);
+
+/* The pool as a bank (owned by the cache): decode with slot ids. */
+moe_bank* moe_cache_bank(moe_cache* cache);
+
+/* Make one request's experts resident: moe_slot_table_acquire on the pool's
+ * LRU state, then for each miss three copies on `stream` (cudaMemcpyAsync,
+ * any memory the device can address; pinned host memory keeps them
+ * asynchronous): the expert's 2I gate_up rows and H down rows from the
+ * layer's compact banks (gate_up [E][2I][row bytes], down [E][H][row bytes],
+ * the same layout moe_bank_create takes) and its scale row from scales [E][4]
+ * (NULL: ones).  Decode on the same stream after this call; the sources must
+ * stay valid until the copies complete.  *nfill (may be NULL) = misses. */
+int moe_cache_acquire(moe_cache* cache, int32_t layer, const void* gate_up, const void* down,
+                      const float* scales, int32_t E, const int32_t* ids, int32_t n, int32_t* slot_ids,
+                      int32_t* nfill, void* stream);
+
+/* Cumulative hits and misses (distinct experts per request) and bytes copied. */
+int moe_cache_stats(const moe_cache* cache, int64_t* hits, int64_t* misses, int64_t* copied_bytes);
+
 /* Tensor-core check: D[128, N] = A[128, K] * B[N, K]^T with fp16 A and B
  * (device, row-major), fp32 D (device, row-major), computed with the tcgen05
  * kind::f16 MMA on swizzled shared-memory tiles that the prompt-path GEMMs

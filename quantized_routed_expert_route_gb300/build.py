@@ -15,7 +15,7 @@ CSRC = os.path.join(PKG, "csrc")
 LIBDIR = os.path.join(PKG, "lib")
 LIBNAME = "libqre_moe.so"
 SOURCES = ["decode.cu", "decode_types_b.cu", "decode_types_c.cu", "layer_small.cu", "prefill.cu", "decode_tc.cu",
-           "decode_qb.cu", "linear.cu", "api.cu"]
+           "decode_qb.cu", "linear.cu", "cache.cu", "api.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ARCH + ["-lineinfo", "-O3", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall"]
 

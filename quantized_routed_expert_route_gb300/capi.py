@@ -30,7 +30,9 @@ EXPORTS = (
     "moe_debug_block_dots", "moe_debug_decode_stages", "moe_decode_noalloc", "moe_debug_tc_gemm",
     "moe_prefill_workspace_bytes", "moe_prefill_grouped", "moe_debug_prefill_stages",
     "moe_decode_kernel_count", "moe_decode_io_bytes", "moe_decode_io_offsets", "moe_decode_host",
-    "moe_linear",
+    "moe_linear", "moe_cache_plan", "moe_slot_table_create", "moe_slot_table_destroy", "moe_slot_table_acquire",
+    "moe_slot_table_stats", "moe_cache_create", "moe_cache_destroy", "moe_cache_bank", "moe_cache_acquire",
+    "moe_cache_stats",
 )
 
 
@@ -75,6 +77,16 @@ def _load() -> ctypes.CDLL:
         "moe_decode_noalloc": (ctypes.c_int, [vp, vp, i32, vp, vp, vp, vp]),
         "moe_debug_tc_gemm": (ctypes.c_int, [vp, vp, i32, i32, vp, vp, vp]),
         "moe_linear": (ctypes.c_int, [i32, vp, i32, i32, vp, vp, i32, vp, vp, vp]),
+        "moe_cache_plan": (ctypes.c_int, [i64, i32, vp, vp, vp]),
+        "moe_slot_table_create": (ctypes.c_int, [i32, ctypes.POINTER(vp)]),
+        "moe_slot_table_destroy": (ctypes.c_int, [vp]),
+        "moe_slot_table_acquire": (ctypes.c_int, [vp, i32, vp, i32, i32, vp, vp, vp, vp]),
+        "moe_slot_table_stats": (ctypes.c_int, [vp, vp, vp]),
+        "moe_cache_create": (ctypes.c_int, [ctypes.POINTER(moe_layer_geom), i32, vp, ctypes.POINTER(vp)]),
+        "moe_cache_destroy": (ctypes.c_int, [vp]),
+        "moe_cache_bank": (vp, [vp]),
+        "moe_cache_acquire": (ctypes.c_int, [vp, i32, vp, vp, vp, i32, vp, i32, vp, vp, vp]),
+        "moe_cache_stats": (ctypes.c_int, [vp, vp, vp, vp]),
         "moe_prefill_workspace_bytes": (sz, [vp, i32, i32]),
         "moe_decode_kernel_count": (ctypes.c_int, [vp, i32]),
         "moe_decode_io_bytes": (sz, [vp, i32]),
@@ -186,6 +198,79 @@ def moe_linear(wtype: int, rows: int, N: int, K: int, row_scale: int | None, x: 
     """out[T, N] (bf16) = row_scale * (q8_1(x[T, K]) @ W[N, K]^T) for quantized rows W."""
     _check(_lib.moe_linear(wtype, rows, N, K, row_scale or None, x, T, out, dev_err or None, stream or None),
            "moe_linear")
+
+
+def moe_cache_plan(budget_bytes: int, expert_bytes, selections) -> list:
+    """Slots per geometry for a byte budget (see include/qre_moe.h)."""
+    n = len(expert_bytes)
+    eb = (ctypes.c_int64 * n)(*expert_bytes)
+    sel = (ctypes.c_int64 * n)(*selections)
+    out = (ctypes.c_int64 * n)()
+    _check(_lib.moe_cache_plan(budget_bytes, n, eb, sel, out), "moe_cache_plan")
+    return [int(v) for v in out]
+
+
+class SlotTable:
+    """The host LRU state of one slot pool (moe_slot_table)."""
+
+    def __init__(self, nslots: int):
+        h = ctypes.c_void_p()
+        _check(_lib.moe_slot_table_create(nslots, ctypes.byref(h)), "moe_slot_table_create")
+        self.h, self.nslots = h.value, nslots
+
+    def acquire(self, layer: int, ids, E: int):
+        """(slot per id, [(slot, expert) to fill]) for one request."""
+        n = len(ids)
+        a = (ctypes.c_int32 * max(n, 1))(*ids)
+        slots = (ctypes.c_int32 * max(n, 1))()
+        fs = (ctypes.c_int32 * self.nslots)()
+        fe = (ctypes.c_int32 * self.nslots)()
+        nf = ctypes.c_int32(0)
+        _check(_lib.moe_slot_table_acquire(self.h, layer, a, n, E, slots, fs, fe, ctypes.byref(nf)),
+               "moe_slot_table_acquire")
+        return [int(slots[i]) for i in range(n)], [(int(fs[i]), int(fe[i])) for i in range(nf.value)]
+
+    def stats(self):
+        h, m = ctypes.c_int64(0), ctypes.c_int64(0)
+        _check(_lib.moe_slot_table_stats(self.h, ctypes.byref(h), ctypes.byref(m)), "moe_slot_table_stats")
+        return int(h.value), int(m.value)
+
+    def close(self):
+        if self.h:
+            _lib.moe_slot_table_destroy(self.h)
+            self.h = None
+
+
+def moe_cache_create(geom: moe_layer_geom, nslots: int, stream: int = 0) -> int:
+    out = ctypes.c_void_p()
+    _check(_lib.moe_cache_create(ctypes.byref(geom), nslots, stream or None, ctypes.byref(out)), "moe_cache_create")
+    return out.value
+
+
+def moe_cache_destroy(cache: int) -> None:
+    _check(_lib.moe_cache_destroy(cache), "moe_cache_destroy")
+
+
+def moe_cache_bank(cache: int) -> int:
+    return _lib.moe_cache_bank(cache)
+
+
+def moe_cache_acquire(cache: int, layer: int, gate_up: int, down: int, scales: int | None, E: int, ids,
+                      stream: int = 0):
+    """Slot ids for one request's expert ids (host list) and the number of misses."""
+    n = len(ids)
+    a = (ctypes.c_int32 * max(n, 1))(*ids)
+    slots = (ctypes.c_int32 * max(n, 1))()
+    nf = ctypes.c_int32(0)
+    _check(_lib.moe_cache_acquire(cache, layer, gate_up, down, scales or None, E, a, n, slots, ctypes.byref(nf),
+                                  stream or None), "moe_cache_acquire")
+    return [int(slots[i]) for i in range(n)], int(nf.value)
+
+
+def moe_cache_stats(cache: int):
+    h, m, b = ctypes.c_int64(0), ctypes.c_int64(0), ctypes.c_int64(0)
+    _check(_lib.moe_cache_stats(cache, ctypes.byref(h), ctypes.byref(m), ctypes.byref(b)), "moe_cache_stats")
+    return int(h.value), int(m.value), int(b.value)
 
 
 def moe_debug_tc_gemm(A: int, B: int, K: int, N: int, D: int, dev_err: int, stream: int = 0) -> None:

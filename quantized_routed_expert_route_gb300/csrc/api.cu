@@ -335,6 +335,11 @@ DecodeParams make_params(const moe_bank* b, const WsLayout& L, uint8_t* ws, cons
 
 }  // namespace
 
+namespace qre {   // internals the expert cache (cache.cu) uses
+float* bank_scales(moe_bank* b) { return b ? b->scales : nullptr; }
+int report_cuda_error(cudaError_t e, const char* what) { return cuda_fail(e, what); }
+}  // namespace qre
+
 extern "C" {
 
 size_t moe_row_bytes(int32_t type, int64_t k) {

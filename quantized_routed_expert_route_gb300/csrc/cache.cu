@@ -1,0 +1,258 @@
+// Exact-geometry expert cache for expert banks larger than the GPU's memory.
+//
+// FreeToken issue #194, "avoid max-stride padding for heterogeneous GGUF
+// expert banks", Proposed design: the byte-denominated bank arena is carved
+// into disjoint exact-width pools, one per geometry (the tuple of row sizes),
+// each with its own tags and LRU state; decode views and LRU updates are
+// routed by layer; compact pinned-host rows are copied straight into the
+// slots with no payload-sized device temporary.
+//
+// Here a pool is an ordinary bank over device memory whose "experts" are the
+// slots (E = slots), so every decode path runs on it unchanged once a
+// request's routing ids are remapped to slots.  moe_cache_acquire keeps the
+// LRU state on the host: it maps each routed (layer, expert) to a slot,
+// evicting the least recently used slot for each miss, and enqueues one copy
+// per projection and miss from the layer's compact rows (any memory the
+// device can read; pinned host memory for asynchronous copies) into the
+// slot, plus the expert's scale row.  With exact-width slots the rows keep
+// their compact layout, so each copy is a single contiguous transfer.
+#include <cuda_runtime.h>
+
+#include <cstring>
+#include <new>
+#include <unordered_map>
+#include <vector>
+
+#include "../../include/qre_moe.h"
+#include "formats.cuh"
+#include "internal.h"
+
+// LRU state of one pool: a doubly linked list over the slots, least recent at
+// the head; never-used slots start in index order (slot 0 least recent).
+struct moe_slot_table {
+  int nslots;
+  std::vector<int> prev, next;
+  int head, tail;
+  std::vector<long long> key_of;                 // slot -> (layer, expert) key, -1 when never used
+  std::unordered_map<long long, int> slot_of;    // key -> slot
+  long long hits, misses;
+};
+
+struct moe_cache {
+  moe_layer_geom geom;       // E = slots
+  moe_slot_table* table;
+  moe_bank* bank;            // the pool as a bank (borrows gu / dn)
+  uint8_t* gu;               // [slots][2I][rb_gu] + slack
+  uint8_t* dn;               // [slots][H][rb_dn] + slack
+  size_t gu_expert, dn_expert;
+  long long h2d_bytes;
+  std::vector<int32_t> fill_slots, fill_experts;
+};
+
+namespace {
+
+const float kOnes[4] = {1.0f, 1.0f, 1.0f, 1.0f};   // scale row of an expert whose layer has no scale bank
+
+long long slot_key(int layer, int e) { return ((long long)(uint32_t)layer << 32) | (uint32_t)e; }
+
+void lru_unlink(moe_slot_table* t, int s) {
+  const int p = t->prev[s], n = t->next[s];
+  if (p >= 0) t->next[p] = n; else t->head = n;
+  if (n >= 0) t->prev[n] = p; else t->tail = p;
+  t->prev[s] = t->next[s] = -1;
+}
+
+void lru_push_recent(moe_slot_table* t, int s) {
+  t->prev[s] = t->tail;
+  t->next[s] = -1;
+  if (t->tail >= 0) t->next[t->tail] = s; else t->head = s;
+  t->tail = s;
+}
+
+}  // namespace
+
+int moe_slot_table_create(int32_t nslots, moe_slot_table** out) {
+  if (!out || nslots < 1) return MOE_EINVAL;
+  moe_slot_table* t = new (std::nothrow) moe_slot_table;
+  if (!t) return MOE_ENOMEM;
+  t->nslots = nslots;
+  t->prev.assign(nslots, -1);
+  t->next.assign(nslots, -1);
+  t->key_of.assign(nslots, -1);
+  t->head = t->tail = -1;
+  for (int s = 0; s < nslots; ++s) lru_push_recent(t, s);
+  t->hits = t->misses = 0;
+  *out = t;
+  return MOE_OK;
+}
+
+int moe_slot_table_destroy(moe_slot_table* t) {
+  delete t;
+  return MOE_OK;
+}
+
+int moe_slot_table_acquire(moe_slot_table* t, int32_t layer, const int32_t* ids, int32_t n, int32_t E,
+                           int32_t* slot_ids, int32_t* fill_slots, int32_t* fill_experts, int32_t* nfill) {
+  if (!t || (n > 0 && (!ids || !slot_ids)) || n < 0 || E < 1 || layer < 0 || !nfill) return MOE_EINVAL;
+  // the request's distinct valid keys, in first-occurrence order
+  std::vector<long long> keys;
+  std::unordered_map<long long, int> seen;
+  for (int i = 0; i < n; ++i) {
+    const int e = ids[i];
+    if (e < 0 || e >= E) continue;
+    const long long k = slot_key(layer, e);
+    if (seen.emplace(k, 1).second) keys.push_back(k);
+  }
+  if ((long long)keys.size() > t->nslots) return MOE_EUNSUPPORTED;
+  if (!keys.empty() && (!fill_slots || !fill_experts)) return MOE_EINVAL;
+  // hits become the most recent first, so no miss of this request evicts them
+  for (const long long k : keys) {
+    const auto it = t->slot_of.find(k);
+    if (it == t->slot_of.end()) continue;
+    lru_unlink(t, it->second);
+    lru_push_recent(t, it->second);
+    ++t->hits;
+  }
+  int nf = 0;
+  for (const long long k : keys) {
+    if (t->slot_of.count(k)) continue;
+    const int s = t->head;   // least recent: neither a hit nor an earlier miss of this request
+    lru_unlink(t, s);
+    if (t->key_of[s] >= 0) t->slot_of.erase(t->key_of[s]);
+    t->key_of[s] = k;
+    t->slot_of[k] = s;
+    lru_push_recent(t, s);
+    ++t->misses;
+    fill_slots[nf] = s;
+    fill_experts[nf] = (int32_t)(k & 0xFFFFFFFFll);
+    ++nf;
+  }
+  for (int i = 0; i < n; ++i) {
+    const int e = ids[i];
+    slot_ids[i] = (e < 0 || e >= E) ? -1 : t->slot_of[slot_key(layer, e)];
+  }
+  *nfill = nf;
+  return MOE_OK;
+}
+
+int moe_slot_table_stats(const moe_slot_table* t, int64_t* hits, int64_t* misses) {
+  if (!t) return MOE_EINVAL;
+  if (hits) *hits = t->hits;
+  if (misses) *misses = t->misses;
+  return MOE_OK;
+}
+
+int moe_cache_plan(int64_t budget_bytes, int32_t ngeom, const int64_t* expert_bytes, const int64_t* selections,
+                   int64_t* slots) {
+  if (budget_bytes < 0 || ngeom < 1 || !expert_bytes || !selections || !slots) return MOE_EINVAL;
+  __int128 unit = 0;
+  for (int g = 0; g < ngeom; ++g) {
+    if (expert_bytes[g] < 1 || selections[g] < 0) return MOE_EINVAL;
+    unit += (__int128)selections[g] * expert_bytes[g];
+  }
+  __int128 left = budget_bytes;
+  for (int g = 0; g < ngeom; ++g) {
+    slots[g] = unit > 0 ? (int64_t)((__int128)budget_bytes * selections[g] / unit) : 0;
+    left -= (__int128)slots[g] * expert_bytes[g];
+  }
+  // the bytes left over: one slot at a time of the smallest size that fits
+  for (;;) {
+    int best = -1;
+    for (int g = 0; g < ngeom; ++g)
+      if (expert_bytes[g] <= left && (best < 0 || expert_bytes[g] < expert_bytes[best])) best = g;
+    if (best < 0) break;
+    ++slots[best];
+    left -= expert_bytes[best];
+  }
+  return MOE_OK;
+}
+
+int moe_cache_create(const moe_layer_geom* geom, int32_t nslots, void* stream, moe_cache** out) {
+  if (!geom || !out || nslots < 1 || nslots > MOE_MAX_E) return MOE_EINVAL;
+  moe_layer_geom g = *geom;
+  g.E = nslots;
+  const int rb_gu = qre::row_bytes_of(g.gate_up_type, g.H), rb_dn = qre::row_bytes_of(g.down_type, g.I);
+  if (rb_gu == 0 || rb_dn == 0) return MOE_EINVAL;
+  moe_cache* c = new (std::nothrow) moe_cache;
+  if (!c) return MOE_ENOMEM;
+  c->geom = g;
+  c->gu_expert = (size_t)2 * g.I * rb_gu;
+  c->dn_expert = (size_t)g.H * rb_dn;
+  c->h2d_bytes = 0;
+  c->gu = c->dn = nullptr;
+  c->bank = nullptr;
+  c->table = nullptr;
+  int st = moe_slot_table_create(nslots, &c->table);
+  if (st) { delete c; return st; }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t gu_bytes = c->gu_expert * nslots, dn_bytes = c->dn_expert * nslots;
+  if (cudaMalloc(&c->gu, gu_bytes + 256) != cudaSuccess || cudaMalloc(&c->dn, dn_bytes + 256) != cudaSuccess) {
+    cudaGetLastError();
+    cudaFree(c->gu); cudaFree(c->dn);
+    moe_slot_table_destroy(c->table);
+    delete c;
+    return MOE_ENOMEM;
+  }
+  // defined contents for slots that were never filled (a decode may only
+  // route to filled slots, but the tensor-map tiles of a slot read a whole box)
+  cudaError_t e = cudaMemsetAsync(c->gu, 0, gu_bytes + 256, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(c->dn, 0, dn_bytes + 256, s);
+  if (e == cudaSuccess) st = moe_bank_create(&g, c->gu, gu_bytes, c->dn, dn_bytes, nullptr, MOE_SRC_DEVICE_BORROW,
+                                             stream, &c->bank);
+  if (e != cudaSuccess || st != MOE_OK) {
+    cudaFree(c->gu); cudaFree(c->dn);
+    moe_slot_table_destroy(c->table);
+    delete c;
+    return e != cudaSuccess ? qre::report_cuda_error(e, "cache create") : st;
+  }
+  c->fill_slots.resize(nslots);
+  c->fill_experts.resize(nslots);
+  *out = c;
+  return MOE_OK;
+}
+
+int moe_cache_destroy(moe_cache* c) {
+  if (!c) return MOE_OK;
+  moe_bank_destroy(c->bank);   // synchronizes the device
+  cudaFree(c->gu);
+  cudaFree(c->dn);
+  moe_slot_table_destroy(c->table);
+  delete c;
+  return MOE_OK;
+}
+
+moe_bank* moe_cache_bank(moe_cache* c) { return c ? c->bank : nullptr; }
+
+int moe_cache_acquire(moe_cache* c, int32_t layer, const void* gate_up, const void* down, const float* scales,
+                      int32_t E, const int32_t* ids, int32_t n, int32_t* slot_ids, int32_t* nfill, void* stream) {
+  if (!c || !gate_up || !down || E < 1) return MOE_EINVAL;
+  int32_t nf = 0;
+  const int st = moe_slot_table_acquire(c->table, layer, ids, n, E, slot_ids, c->fill_slots.data(),
+                                        c->fill_experts.data(), &nf);
+  if (st) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  float* sdev = qre::bank_scales(c->bank);
+  const uint8_t* gsrc = static_cast<const uint8_t*>(gate_up);
+  const uint8_t* dsrc = static_cast<const uint8_t*>(down);
+  for (int i = 0; i < nf; ++i) {
+    const size_t slot = (size_t)c->fill_slots[i], e = (size_t)c->fill_experts[i];
+    cudaError_t err = cudaMemcpyAsync(c->gu + slot * c->gu_expert, gsrc + e * c->gu_expert, c->gu_expert,
+                                      cudaMemcpyDefault, s);
+    if (err == cudaSuccess)
+      err = cudaMemcpyAsync(c->dn + slot * c->dn_expert, dsrc + e * c->dn_expert, c->dn_expert, cudaMemcpyDefault,
+                            s);
+    if (err == cudaSuccess)
+      err = cudaMemcpyAsync(sdev + 4 * slot, scales ? scales + 4 * e : kOnes, 16, cudaMemcpyDefault, s);
+    if (err != cudaSuccess) return qre::report_cuda_error(err, "cache fill");
+    c->h2d_bytes += (long long)(c->gu_expert + c->dn_expert + 16);
+  }
+  if (nfill) *nfill = nf;
+  return MOE_OK;
+}
+
+int moe_cache_stats(const moe_cache* c, int64_t* hits, int64_t* misses, int64_t* copied_bytes) {
+  if (!c) return MOE_EINVAL;
+  moe_slot_table_stats(c->table, hits, misses);
+  if (copied_bytes) *copied_bytes = c->h2d_bytes;
+  return MOE_OK;
+}

@@ -6,6 +6,8 @@
 #include <cstddef>
 #include <cstdint>
 
+struct moe_bank;   // the C ABI's opaque bank (api.cu)
+
 namespace qre {
 
 constexpr int kMaxE = 1024;
@@ -194,6 +196,11 @@ struct LinParams {
 bool plan_linear(LinParams& p);
 size_t linear_smem_bytes(const LinParams& p);
 cudaError_t launch_linear(const LinParams& p, cudaStream_t stream);
+
+// Bank internals the expert cache (cache.cu) writes: the device scale rows
+// [E][4]; and the library's CUDA error report (sets moe_last_cuda_error).
+float* bank_scales(moe_bank* b);
+int report_cuda_error(cudaError_t e, const char* what);
 
 int sm_count();
 
