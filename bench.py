@@ -414,6 +414,77 @@ def bench_linear(dev, steps, warmup, hbm_peak):
     return res
 
 
+def bench_cache(dev, tokens, hbm_peak):
+    """Decode through the expert cache: four Laguna-shaped Q4_K layers
+    (H=4096, I=768, E=256, top-10; 1.36 GB of compact rows each) live in
+    pinned host memory; one pool of 160 slots (0.85 GB, 16 % of the 1,024
+    experts) serves them.  A token runs the four layers in turn with Zipf
+    routing: moe_cache_acquire (host LRU, copies of the missed experts) then
+    moe_decode on the pool, all on one stream; timed with CUDA events over
+    `tokens` tokens after a warm-up of 50."""
+    import torch
+
+    from quantized_routed_expert_route_gb300 import capi
+    from synth import banks as S
+    from synth import counter as C
+    L, NL, NSLOTS = LAGUNA, 4, 160
+    H, I, E, K = L["H"], L["I"], L["E"], L["K"]
+    rb_gu, rb_dn = row_bytes(Q4_K, H), row_bytes(Q4_K, I)
+    stream = torch.cuda.current_stream().cuda_stream
+    host = []
+    for l in range(NL):
+        gu = torch.empty(E * 2 * I * rb_gu, dtype=torch.uint8, device=dev)
+        dn = torch.empty(E * H * rb_dn, dtype=torch.uint8, device=dev)
+        C.fill_bank_torch(gu, 7000 + 2 * l, Q4_K, H)
+        C.fill_bank_torch(dn, 7001 + 2 * l, Q4_K, I)
+        host.append((gu.cpu().pin_memory(), dn.cpu().pin_memory()))
+        del gu, dn
+    torch.cuda.empty_cache()
+    cache = capi.moe_cache_create(capi.moe_layer_geom(H, I, NSLOTS, K, Q4_K, Q4_K), NSLOTS, stream)
+    pool = capi.moe_cache_bank(cache)
+    wsb = capi.moe_workspace_bytes(pool, 1)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
+    capi.moe_workspace_init(ws.data_ptr(), wsb, stream)
+    n_all = 50 + tokens
+    routes = [S.zipf_routing(7100 + l, n_all, E, K) for l in range(NL)]
+    x = torch.from_numpy(S.hidden_bf16(7200, 1, H).view(np.int16)).to(dev)
+    out = torch.empty((1, H), dtype=torch.int16, device=dev)
+    sid = torch.empty((n_all, NL, K), dtype=torch.int32).pin_memory()
+    sid_d = torch.empty((NL, K), dtype=torch.int32, device=dev)
+    wts = [torch.from_numpy(w).to(dev) for _, w in routes]
+
+    def token(t):
+        for l in range(NL):
+            ids = [int(v) for v in routes[l][0][t]]
+            slots, _ = capi.moe_cache_acquire(cache, l, host[l][0].data_ptr(), host[l][1].data_ptr(), None, E, ids,
+                                              stream)
+            sid[t, l] = torch.tensor(slots, dtype=torch.int32)
+            sid_d[l].copy_(sid[t, l], non_blocking=True)
+            capi.moe_decode(pool, x.data_ptr(), 1, sid_d[l].data_ptr(), wts[l][t].data_ptr(), out.data_ptr(),
+                            ws.data_ptr(), wsb, stream)
+
+    for t in range(50):
+        token(t)
+    torch.cuda.synchronize()
+    h0, m0, b0 = capi.moe_cache_stats(cache)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for t in range(50, n_all):
+        token(t)
+    e1.record()
+    e1.synchronize()
+    ms = e0.elapsed_time(e1)
+    h1, m1, b1 = capi.moe_cache_stats(cache)
+    err = capi.moe_get_error(ws.data_ptr(), wsb, stream)
+    capi.moe_cache_destroy(cache)
+    del host
+    return {"workload": "4 Laguna-shaped Q4_K layers in pinned host memory (5.4 GB), 160-slot pool (0.85 GB), "
+                        "T=1, Zipf(1.1) routing", "tokens": tokens,
+            "tok_per_s": tokens / (ms / 1e3), "us_per_layer": ms * 1e3 / (tokens * NL),
+            "hit_rate": (h1 - h0) / max(1, (h1 - h0) + (m1 - m0)), "misses_per_layer": (m1 - m0) / (tokens * NL),
+            "h2d_gbs": (b1 - b0) / (ms / 1e3) / 1e9, "device_error_bits": err}
+
+
 # ------------------------------------------------------------------ CPU oracle timing
 
 def cpu_oracle_worker(seconds: float, seed: int = 0) -> dict:
@@ -543,6 +614,7 @@ def main():
     ap.add_argument("--no-prefill", action="store_true", help="skip the prompt-path chunk")
     ap.add_argument("--no-types", action="store_true", help="skip the per-GGUF-type layer stacks")
     ap.add_argument("--no-linear", action="store_true", help="skip the dense NVFP4 linear")
+    ap.add_argument("--no-cache", action="store_true", help="skip the expert-cache leg")
     ap.add_argument("--profile-linear", action="store_true",
                     help="run --steps one-launch dense NVFP4 linears (245,760 x 2048, T=--T) for ncu")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
@@ -666,6 +738,10 @@ def main():
 
     if not a.no_linear:
         extra["dense_linear_nvfp4"] = bench_linear(dev, max(10, min(100, a.steps // 4)), a.warmup, hbm_peak)
+        torch.cuda.empty_cache()
+
+    if not a.no_cache:
+        extra["expert_cache"] = bench_cache(dev, max(50, min(400, a.steps)), hbm_peak)
         torch.cuda.empty_cache()
 
     if not a.no_prefill:
