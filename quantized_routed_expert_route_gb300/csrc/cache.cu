@@ -15,7 +15,11 @@
 // per projection and miss from the layer's compact rows (any memory the
 // device can read; pinned host memory for asynchronous copies) into the
 // slot, plus the expert's scale row.  With exact-width slots the rows keep
-// their compact layout, so each copy is a single contiguous transfer.
+// their compact layout, so each copy is a single contiguous transfer.  When
+// the layer's rows live in memory the GPU addresses directly (pinned host
+// memory, reached over the host link, or device memory), all of a request's
+// copies run as one kernel in which every SM loads and stores 16-byte
+// vectors; other sources go through the copy engine (cudaMemcpyAsync).
 #include <cuda_runtime.h>
 
 #include <cstring>
@@ -52,6 +56,71 @@ struct moe_cache {
 namespace {
 
 const float kOnes[4] = {1.0f, 1.0f, 1.0f, 1.0f};   // scale row of an expert whose layer has no scale bank
+
+// One launch copies up to kFillMaxJobs contiguous byte ranges, cut into
+// 16 KB chunks that the CTAs take in turn (kernel parameters stay < 4 KB).
+constexpr int kFillMaxJobs = 120;
+constexpr unsigned long long kFillChunk = 16384;
+struct FillParams {
+  int njobs;
+  unsigned long long chunk0[kFillMaxJobs + 1];   // first chunk of each job; chunk0[njobs] = total
+  const uint8_t* src[kFillMaxJobs];
+  uint8_t* dst[kFillMaxJobs];
+  unsigned long long bytes[kFillMaxJobs];
+};
+
+__global__ void __launch_bounds__(256) k_cache_fill(const __grid_constant__ FillParams p) {
+  const unsigned long long total = p.chunk0[p.njobs];
+  int j = 0;
+  for (unsigned long long c = blockIdx.x; c < total; c += gridDim.x) {
+    while (p.chunk0[j + 1] <= c) ++j;            // chunks are visited in increasing order
+    const unsigned long long off = (c - p.chunk0[j]) * kFillChunk;
+    const unsigned long long rest = p.bytes[j] - off;
+    const unsigned long long n = rest < kFillChunk ? rest : kFillChunk;
+    const uint8_t* s = p.src[j] + off;
+    uint8_t* d = p.dst[j] + off;
+    if (((reinterpret_cast<uintptr_t>(s) | reinterpret_cast<uintptr_t>(d) | n) & 15u) == 0) {
+      const uint4* s4 = reinterpret_cast<const uint4*>(s);
+      uint4* d4 = reinterpret_cast<uint4*>(d);
+      for (unsigned long long i = threadIdx.x; i < n / 16; i += blockDim.x) d4[i] = s4[i];
+    } else {
+      for (unsigned long long i = threadIdx.x; i < n; i += blockDim.x) d[i] = s[i];
+    }
+  }
+}
+
+// The address the device uses for `p` when it may load from it directly
+// (device or managed memory, or pinned host memory mapped into the device's
+// address space), else nullptr.
+const uint8_t* device_view(const void* p) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged || a.type == cudaMemoryTypeHost)
+    return static_cast<const uint8_t*>(a.devicePointer);
+  return nullptr;
+}
+
+cudaError_t launch_fill(FillParams& fp, cudaStream_t s) {
+  if (fp.njobs == 0) return cudaSuccess;
+  const unsigned long long total = fp.chunk0[fp.njobs];
+  const unsigned long long cap = 4ull * (unsigned long long)qre::sm_count();
+  const int grid = (int)(total < cap ? total : cap);
+  k_cache_fill<<<grid, 256, 0, s>>>(fp);
+  fp.njobs = 0;
+  fp.chunk0[0] = 0;
+  return cudaGetLastError();
+}
+
+void add_fill(FillParams& fp, const uint8_t* src, uint8_t* dst, unsigned long long bytes) {
+  const int j = fp.njobs++;
+  fp.src[j] = src;
+  fp.dst[j] = dst;
+  fp.bytes[j] = bytes;
+  fp.chunk0[j + 1] = fp.chunk0[j] + (bytes + kFillChunk - 1) / kFillChunk;
+}
 
 long long slot_key(int layer, int e) { return ((long long)(uint32_t)layer << 32) | (uint32_t)e; }
 
@@ -234,17 +303,35 @@ int moe_cache_acquire(moe_cache* c, int32_t layer, const void* gate_up, const vo
   float* sdev = qre::bank_scales(c->bank);
   const uint8_t* gsrc = static_cast<const uint8_t*>(gate_up);
   const uint8_t* dsrc = static_cast<const uint8_t*>(down);
+  // rows the device can load directly are copied by one kernel per request
+  const uint8_t* gview = nf > 0 ? device_view(gate_up) : nullptr;
+  const uint8_t* dview = nf > 0 ? device_view(down) : nullptr;
+  const bool by_kernel = gview && dview;
+  FillParams fp;
+  fp.njobs = 0;
+  fp.chunk0[0] = 0;
   for (int i = 0; i < nf; ++i) {
     const size_t slot = (size_t)c->fill_slots[i], e = (size_t)c->fill_experts[i];
-    cudaError_t err = cudaMemcpyAsync(c->gu + slot * c->gu_expert, gsrc + e * c->gu_expert, c->gu_expert,
-                                      cudaMemcpyDefault, s);
-    if (err == cudaSuccess)
-      err = cudaMemcpyAsync(c->dn + slot * c->dn_expert, dsrc + e * c->dn_expert, c->dn_expert, cudaMemcpyDefault,
+    cudaError_t err = cudaSuccess;
+    if (by_kernel) {
+      if (fp.njobs + 2 > kFillMaxJobs) err = launch_fill(fp, s);
+      add_fill(fp, gview + e * c->gu_expert, c->gu + slot * c->gu_expert, c->gu_expert);
+      add_fill(fp, dview + e * c->dn_expert, c->dn + slot * c->dn_expert, c->dn_expert);
+    } else {
+      err = cudaMemcpyAsync(c->gu + slot * c->gu_expert, gsrc + e * c->gu_expert, c->gu_expert, cudaMemcpyDefault,
                             s);
+      if (err == cudaSuccess)
+        err = cudaMemcpyAsync(c->dn + slot * c->dn_expert, dsrc + e * c->dn_expert, c->dn_expert,
+                              cudaMemcpyDefault, s);
+    }
     if (err == cudaSuccess)
       err = cudaMemcpyAsync(sdev + 4 * slot, scales ? scales + 4 * e : kOnes, 16, cudaMemcpyDefault, s);
     if (err != cudaSuccess) return qre::report_cuda_error(err, "cache fill");
     c->h2d_bytes += (long long)(c->gu_expert + c->dn_expert + 16);
+  }
+  if (by_kernel) {
+    const cudaError_t err = launch_fill(fp, s);
+    if (err != cudaSuccess) return qre::report_cuda_error(err, "cache fill");
   }
   if (nfill) *nfill = nf;
   return MOE_OK;

@@ -23,7 +23,10 @@ from tests import tolerance as tol  # noqa: E402
 DEV = "cuda"
 
 
-def test_cache_decode_equals_resident_decode_and_follows_the_lru():
+@pytest.mark.parametrize("pinned", [True, False])
+def test_cache_decode_equals_resident_decode_and_follows_the_lru(pinned):
+    """pinned: the layers' rows in pinned host memory (copied by the fill
+    kernel over the host link) or in pageable memory (the copy engine)."""
     H, I, E, K, NSLOTS = 512, 256, 32, 4, 12
     wt = F.TYPE_Q4_K
     stream = torch.cuda.current_stream().cuda_stream
@@ -33,8 +36,8 @@ def test_cache_decode_equals_resident_decode_and_follows_the_lru():
     for l in range(3):
         reqs = [cases.make_case(H, I, E, K, wt, wt, T, seed=500 + 10 * l + T) for T in (2, 3)]
         src = reqs[0]
-        host = dict(gu=src.gu_dev.cpu().pin_memory(), dn=src.dn_dev.cpu().pin_memory(),
-                    sb=torch.from_numpy(src.sb).pin_memory())
+        pin = (lambda t: t.pin_memory()) if pinned else (lambda t: t)
+        host = dict(gu=pin(src.gu_dev.cpu()), dn=pin(src.dn_dev.cpu()), sb=pin(torch.from_numpy(src.sb.copy())))
         for rq in reqs[1:]:   # every request of a layer uses the first case's banks and scales
             rq.gu_dev, rq.dn_dev, rq.sb = src.gu_dev, src.dn_dev, src.sb
             rq.gu_rows, rq.dn_rows = src.gu_rows, src.dn_rows
