@@ -419,7 +419,9 @@ moe_bank* moe_cache_bank(moe_cache* cache);
  * layer's compact banks (gate_up [E][2I][row bytes], down [E][H][row bytes],
  * the same layout moe_bank_create takes) and its scale row from scales [E][4]
  * (NULL: ones).  Decode on the same stream after this call; the sources must
- * stay valid until the copies complete.  *nfill (may be NULL) = misses. */
+ * stay valid until the copies complete.  *nfill (may be NULL) = misses.  If
+ * enqueueing a copy fails (MOE_ECUDA), the slots this request assigned are
+ * untagged, so a later request copies those experts again. */
 int moe_cache_acquire(moe_cache* cache, int32_t layer, const void* gate_up, const void* down,
                       const float* scales, int32_t E, const int32_t* ids, int32_t n, int32_t* slot_ids,
                       int32_t* nfill, void* stream);

@@ -131,6 +131,13 @@ void lru_unlink(moe_slot_table* t, int s) {
   t->prev[s] = t->next[s] = -1;
 }
 
+// Forget a slot's tag (its rows are not what the tag says): it stays where it
+// is in the LRU order and holds no expert until filled again.
+void slot_untag(moe_slot_table* t, int s) {
+  if (t->key_of[s] >= 0) t->slot_of.erase(t->key_of[s]);
+  t->key_of[s] = -1;
+}
+
 void lru_push_recent(moe_slot_table* t, int s) {
   t->prev[s] = t->tail;
   t->next[s] = -1;
@@ -326,12 +333,18 @@ int moe_cache_acquire(moe_cache* c, int32_t layer, const void* gate_up, const vo
     }
     if (err == cudaSuccess)
       err = cudaMemcpyAsync(sdev + 4 * slot, scales ? scales + 4 * e : kOnes, 16, cudaMemcpyDefault, s);
-    if (err != cudaSuccess) return qre::report_cuda_error(err, "cache fill");
+    if (err != cudaSuccess) {
+      for (int k = 0; k < nf; ++k) slot_untag(c->table, c->fill_slots[k]);   // none of this request's fills counts
+      return qre::report_cuda_error(err, "cache fill");
+    }
     c->h2d_bytes += (long long)(c->gu_expert + c->dn_expert + 16);
   }
   if (by_kernel) {
     const cudaError_t err = launch_fill(fp, s);
-    if (err != cudaSuccess) return qre::report_cuda_error(err, "cache fill");
+    if (err != cudaSuccess) {
+      for (int k = 0; k < nf; ++k) slot_untag(c->table, c->fill_slots[k]);
+      return qre::report_cuda_error(err, "cache fill");
+    }
   }
   if (nfill) *nfill = nf;
   return MOE_OK;

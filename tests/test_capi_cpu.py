@@ -62,3 +62,41 @@ def test_host_argument_checks(capi):
     assert lib.moe_workspace_bytes(None, 4) == 0
     assert lib.moe_bank_destroy(None) == capi.MOE_OK
     assert capi.status_string(capi.MOE_EDEVICE) == "device-side error flag set"
+
+
+def test_host_argument_checks_of_the_newer_entry_points(capi):
+    """moe_linear, the GLU field, the s_down fold, the prompt modes and the
+    expert cache refuse bad arguments before any CUDA call."""
+    lib = capi.library()
+    buf = (ctypes.c_uint8 * 64)()
+    out = ctypes.c_void_p()
+    # moe_linear: T = 0 is a no-op; nulls, sizes, types and alignment are refused
+    assert lib.moe_linear(capi.MOE_NVFP4, buf, 4, 256, None, buf, 0, buf, None, None) == capi.MOE_OK
+    assert lib.moe_linear(capi.MOE_NVFP4, None, 4, 256, None, buf, 1, buf, None, None) == capi.MOE_EINVAL
+    assert lib.moe_linear(capi.MOE_BF16, buf, 4, 256, None, buf, 1, buf, None, None) == capi.MOE_EUNSUPPORTED
+    assert lib.moe_linear(capi.MOE_NVFP4, buf, 4, 256, None, buf, capi.MOE_LINEAR_MAX_T + 1, buf, None,
+                          None) == capi.MOE_EUNSUPPORTED
+    assert lib.moe_linear(capi.MOE_Q4_K, buf, 4, 96, None, buf, 1, buf, None, None) == capi.MOE_EINVAL
+    assert lib.moe_linear(11, buf, 4, 256, None, buf, 1, buf, None, None) == capi.MOE_EINVAL
+    assert lib.moe_linear(capi.MOE_NVFP4, ctypes.addressof(buf) + 1, 4, 256, None, buf, 1, buf, None,
+                          None) == capi.MOE_EINVAL
+    # geometry: an unknown GLU or type is refused
+    g = capi.moe_layer_geom(256, 128, 8, 2, capi.MOE_Q8_0, capi.MOE_Q8_0, 2)
+    assert lib.moe_bank_create(ctypes.byref(g), buf, 64, buf, 64, None, 0, None, ctypes.byref(out)) == capi.MOE_EINVAL
+    g = capi.moe_layer_geom(256, 128, 8, 2, capi.MOE_MXFP4 + 1, capi.MOE_Q8_0)
+    assert lib.moe_bank_create(ctypes.byref(g), buf, 64, buf, 64, None, 0, None, ctypes.byref(out)) == capi.MOE_EINVAL
+    # fold, prompt modes, cache
+    assert lib.moe_bank_fold_down_scale(None, buf, capi.MOE_SRC_HOST, None) == capi.MOE_EINVAL
+    assert lib.moe_prefill_workspace_bytes(None, 16, capi.MOE_PREFILL_FP16) == 0
+    assert lib.moe_prefill_grouped(None, buf, 1, buf, buf, 3, buf, buf, 64, None) == capi.MOE_EINVAL
+    g = capi.moe_layer_geom(256, 256, 8, 2, capi.MOE_Q4_K, capi.MOE_Q4_K)
+    assert lib.moe_cache_create(ctypes.byref(g), 0, None, ctypes.byref(out)) == capi.MOE_EINVAL
+    assert lib.moe_cache_create(None, 4, None, ctypes.byref(out)) == capi.MOE_EINVAL
+    assert lib.moe_cache_bank(None) is None
+    assert lib.moe_cache_acquire(None, 0, buf, buf, None, 8, None, 0, None, None, None) == capi.MOE_EINVAL
+    assert lib.moe_cache_destroy(None) == capi.MOE_OK
+    assert lib.moe_slot_table_create(0, ctypes.byref(out)) == capi.MOE_EINVAL
+    assert out.value is None
+    slots = (ctypes.c_int64 * 1)()
+    assert lib.moe_cache_plan(-1, 1, (ctypes.c_int64 * 1)(5), (ctypes.c_int64 * 1)(1), slots) == capi.MOE_EINVAL
+    assert lib.moe_cache_plan(100, 1, (ctypes.c_int64 * 1)(0), (ctypes.c_int64 * 1)(1), slots) == capi.MOE_EINVAL
