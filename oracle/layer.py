@@ -21,7 +21,7 @@ tanh form of GELU, gelu_tanh(g) = g/2 * (1 + tanh(sqrt(2/pi) (g + 0.044715 g^3))
 (Hendrycks and Gimpel, "Gaussian Error Linear Units", 2016); FreeToken PR
 #732, "Other checks", runs experts with both.
 
-Readings where the pages are silent (each listed in the design doc):
+Readings where the pages are silent:
   * gate rows are rows [0, I) of an expert's gate_up bank, up rows [I, 2I);
   * a route whose expert id is outside [0, E) contributes nothing;
   * the intermediate is cast to fp32 and quantized to q8_1 when the down
