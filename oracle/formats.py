@@ -24,7 +24,10 @@ Formats and where they come from:
     2i in the low nibble of byte i, 2i+1 in the high nibble) followed by the
     K/16 scale bytes.
   * BF16 rows -- raw little-endian bf16 (FreeToken issue #194, "Proposed
-    design": BF16 rows go to a dense kernel, not MMVQ).
+    design": BF16 rows go to a dense kernel, not MMVQ).  F16 and F32 rows
+    (raw little-endian fp16 / fp32) are the other float rows of FreeToken PR
+    #704's synthetic list ("Validation": F16, F32, BF16 with quantized
+    partners); like BF16 they keep the activations float.
   * Q6_K super-block -- 256 values in 210 bytes: ql[128] (low 4 bits of each
     code), qh[64] (high 2 bits), scales[16] (int8, one per 16 values), fp16
     d; value d*scale_g*(q - 32) with q the 6-bit code.  Q4_0 block -- fp16 d
@@ -62,9 +65,12 @@ NVFP4_GROUP = 16  # values per UE4M3 scale
 
 TYPE_BF16, TYPE_Q8_0, TYPE_Q4_K, TYPE_NVFP4, TYPE_Q6_K, TYPE_Q4_0 = 0, 1, 2, 3, 4, 5
 TYPE_Q4_1, TYPE_Q5_0, TYPE_Q5_1, TYPE_Q5_K, TYPE_MXFP4 = 6, 7, 8, 9, 10
+TYPE_F16, TYPE_F32 = 11, 12
 TYPE_NAMES = {TYPE_BF16: "bf16", TYPE_Q8_0: "q8_0", TYPE_Q4_K: "q4_k", TYPE_NVFP4: "nvfp4", TYPE_Q6_K: "q6_k",
               TYPE_Q4_0: "q4_0", TYPE_Q4_1: "q4_1", TYPE_Q5_0: "q5_0", TYPE_Q5_1: "q5_1", TYPE_Q5_K: "q5_k",
-              TYPE_MXFP4: "mxfp4"}
+              TYPE_MXFP4: "mxfp4", TYPE_F16: "f16", TYPE_F32: "f32"}
+# float rows: the activations stay float (no q8_1), the intermediate stays fp32
+FLOAT_TYPES = (TYPE_BF16, TYPE_F16, TYPE_F32)
 
 Q8_1_BLOCK_BYTES = 36   # fp16 d, fp16 s, 32 int8
 
@@ -73,8 +79,10 @@ def row_bytes(wtype: int, k: int) -> int:
     """Bytes of one bank row of ``k`` values; 0 when ``k`` is not a whole
     number of blocks.  FreeToken PR #704, "How it plugs into the CPU executor"
     (each bank holds rows of row_bytes(type, K))."""
-    if wtype == TYPE_BF16:
+    if wtype in (TYPE_BF16, TYPE_F16):
         return 2 * k if k % 32 == 0 else 0
+    if wtype == TYPE_F32:
+        return 4 * k if k % 32 == 0 else 0
     if wtype == TYPE_Q8_0:
         return (k // 32) * 34 if k % 32 == 0 else 0
     if wtype == TYPE_Q4_K:
@@ -336,6 +344,10 @@ def dequantize_rows(wtype: int, rows, k: int) -> np.ndarray:
     r = rows.shape[0]
     if wtype == TYPE_BF16:
         return bf16_bits_to_f64(rows.view(np.uint16)).reshape(r, k)
+    if wtype == TYPE_F16:
+        return fp16_bits_to_f64(rows.view(np.uint16)).reshape(r, k)
+    if wtype == TYPE_F32:
+        return rows.view("<f4").astype(np.float64).reshape(r, k)
     if wtype == TYPE_Q8_0:
         blk = rows.reshape(r, k // 32, 34)
         d = fp16_bits_to_f64(blk[..., 0:2].copy().view(np.uint16)[..., 0])

@@ -131,7 +131,7 @@ def dequantize_nvfp4_act(codes, scales) -> np.ndarray:
 
 def _act_in(kind: str, wtype: int, v32: np.ndarray) -> tuple[np.ndarray, dict]:
     """prep_input / prep_inter: fp32 values -> what the next dot consumes."""
-    if wtype == F.TYPE_BF16:
+    if wtype in F.FLOAT_TYPES:
         return v32.astype(np.float64), {}
     if kind == "q8_1":
         qs, d, s, sumq = F.quantize_q8_1(v32)
@@ -194,8 +194,8 @@ def moe_layer(geom: Geometry, gate_up, down, scale_bank, x_bf16_bits, topk_ids, 
             uu = h[g.I:] * sb[e, 1]
             a = _glu(gg, uu, g.glu)
             aq, ainfo = _act_in(act_kind, g.down_type, a.astype(np.float32)
-                                if g.down_type != F.TYPE_BF16 else a)
-            if g.down_type == F.TYPE_BF16:
+                                if g.down_type not in F.FLOAT_TYPES else a)
+            if g.down_type in F.FLOAT_TYPES:
                 aq = a
             y = (wd @ aq) * sb[e, 2] * w[t, k]
             out[t] += y

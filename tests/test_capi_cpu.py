@@ -37,10 +37,13 @@ def test_every_declared_symbol_is_exported(capi):
 
 
 def test_row_bytes_agree_with_the_oracle(capi):
-    for t in sorted(F.TYPE_NAMES):
+    built = [t for t in sorted(F.TYPE_NAMES) if t not in (F.TYPE_F16, F.TYPE_F32)]
+    for t in built:
         for k in (32, 96, 256, 768, 2048, 4096, 100):
             assert capi.moe_row_bytes(t, k) == F.row_bytes(t, k), (t, k)
-    assert capi.moe_row_bytes(11, 256) == 0 and capi.moe_row_bytes(16, 256) == 0
+    # F16 / F32 rows exist in the oracle only so far; 16 is a kernel-side variant, not a type
+    for t in (F.TYPE_F16, F.TYPE_F32, 16):
+        assert capi.moe_row_bytes(t, 256) == 0
 
 
 def test_host_argument_checks(capi):

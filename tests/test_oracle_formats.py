@@ -423,6 +423,19 @@ def test_block_dots_brute_force(wtype, k):
         assert list(got[ri]) == want
 
 
+def test_f16_f32_rows_hand_values():
+    """Little-endian fp16 / fp32 rows decode to their IEEE values: 1, -2,
+    the smallest fp16 subnormal 2^-24, the largest fp16 65504; fp32 1.5,
+    -0.25, 2^-149."""
+    h = np.array([0x3C00, 0xC000, 0x0001, 0x7BFF] * 8, dtype="<u2").view(np.uint8)
+    v = F.dequantize_rows(F.TYPE_F16, h[None, :], 32)[0]
+    assert list(v[:4]) == [1.0, -2.0, 2.0 ** -24, 65504.0]
+    f = np.array([0x3FC00000, 0xBE800000, 0x00000001, 0] * 8, dtype="<u4").view(np.uint8)
+    v = F.dequantize_rows(F.TYPE_F32, f[None, :], 32)[0]
+    assert list(v[:4]) == [1.5, -0.25, 2.0 ** -149, 0.0]
+    assert F.row_bytes(F.TYPE_F16, 64) == 128 and F.row_bytes(F.TYPE_F32, 64) == 256
+
+
 def test_row_bytes_match_the_pages_geometry():
     # FreeToken issue #194, Reproduction geometry: Q4_K 3,538,944 B gate/up and
     # 1,769,472 B down per expert; BF16 12,582,912 B and 6,291,456 B (H=4096, I=768)

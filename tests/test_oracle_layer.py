@@ -156,6 +156,29 @@ def test_fp16_prompt_mode_is_the_unquantized_layer_up_to_fp16_rounding():
         assert np.abs(out[t] - want).max() > 0
 
 
+def test_f16_gate_up_f32_down_layer_keeps_activations_float():
+    """F16 gate_up and F32 down rows (float rows): x is not quantized and the
+    intermediate stays unquantized, so with unit scales and one route the
+    layer is silu(x Wg^T) * (x Wu^T) Wd^T on the rows' exact values."""
+    H, I, E = 64, 32, 2
+    r = np.random.default_rng(11)
+    wgu = (r.standard_normal((E, 2 * I, H)) * 0.1).astype(np.float16)
+    wd = (r.standard_normal((E, H, I)) * 0.1).astype(np.float32)
+    gu = wgu.view(np.uint8).reshape(E, 2 * I, 2 * H)
+    dn = wd.view(np.uint8).reshape(E, H, 4 * I)
+    x = S.hidden_bf16(12, 2, H)
+    geom = L.Geometry(H, I, E, 1, F.TYPE_F16, F.TYPE_F32)
+    ids = np.array([[1], [0]], np.int32)
+    out, _, st = L.moe_layer(geom, gu, dn, None, x, ids, np.ones((2, 1), np.float32), stages=True)
+    xt = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).double().numpy()
+    assert np.array_equal(st["x_hat"], xt)
+    for t, e in enumerate([1, 0]):
+        Wg, Wu = wgu[e][:I].astype(np.float64), wgu[e][I:].astype(np.float64)
+        hg, hu = Wg @ xt[t], Wu @ xt[t]
+        ref = ((hg / (1 + np.exp(-hg))) * hu) @ wd[e].astype(np.float64).T
+        assert np.allclose(out[t], ref, rtol=1e-13, atol=1e-15)
+
+
 def test_layer_invariants():
     geom, gu, dn, sb, x, ids, w = _tiny(seed=3, T=3)
     base, _, _ = L.moe_layer(geom, gu, dn, sb, x, ids, w)

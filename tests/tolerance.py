@@ -89,7 +89,7 @@ def output_bounds(geom, st):
     """beta [T, H]: bound on |gpu_fp32_out - oracle_fp64_out| before bf16 rounding,
     plus per-route data for the intermediate checks."""
     T, K, H, I = st["ids"].shape[0], geom.top_k, geom.H, geom.I
-    quant_down = geom.down_type != F.TYPE_BF16
+    quant_down = geom.down_type not in F.FLOAT_TYPES
     beta = np.zeros((T, H))
     inter_err = np.zeros((T, K, I))
     amb = np.zeros((T, K, I), dtype=bool)
