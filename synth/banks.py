@@ -21,6 +21,7 @@ import numpy as np
 
 BF16, Q8_0, Q4_K, NVFP4, Q6_K, Q4_0 = 0, 1, 2, 3, 4, 5
 Q4_1, Q5_0, Q5_1, Q5_K, MXFP4 = 6, 7, 8, 9, 10
+F16, F32 = 11, 12
 
 
 def rng(seed: int) -> np.random.Generator:
@@ -30,7 +31,7 @@ def rng(seed: int) -> np.random.Generator:
 def row_bytes(wtype: int, k: int) -> int:
     return {BF16: 2 * k, Q8_0: k // 32 * 34, Q4_K: k // 256 * 144, NVFP4: k // 2 + k // 16,
             Q6_K: k // 256 * 210, Q4_0: k // 32 * 18, Q4_1: k // 32 * 20, Q5_0: k // 32 * 22,
-            Q5_1: k // 32 * 24, Q5_K: k // 256 * 176, MXFP4: k // 32 * 17}[wtype]
+            Q5_1: k // 32 * 24, Q5_K: k // 256 * 176, MXFP4: k // 32 * 17, F16: 2 * k, F32: 4 * k}[wtype]
 
 
 # ------------------------------------------------------------------ activations / routing
@@ -292,6 +293,12 @@ def convert_mxfp4(w: np.ndarray) -> np.ndarray:
     return out.reshape(R, -1)
 
 
+def convert_float(w: np.ndarray, wtype: int) -> np.ndarray:
+    """F16 rows (round to nearest even) or F32 rows from fp32 [R, K]."""
+    v = w.astype(np.float16) if wtype == F16 else w.astype(np.float32)
+    return np.ascontiguousarray(v).view(np.uint8).reshape(w.shape[0], -1)
+
+
 def q8_0_codes_bank(seed: int, rows: int, k: int) -> np.ndarray:
     """Q8_0 rows with int8 codes uniform in [-127, 127] and fp16 scales
     uniform in (1e-4, 5e-4) (the tiny single-layer configuration)."""
@@ -334,6 +341,8 @@ def converted_expert(seed: int, e: int, H: int, I: int, gate_up_type: int, down_
             gu = convert_q5k(wg)
         elif gate_up_type == MXFP4:
             gu = convert_mxfp4(wg)
+        elif gate_up_type in (F16, F32):
+            gu = convert_float(wg, gate_up_type)
         else:
             gu = convert_bf16(wg)
     if down_type == Q8_0:
@@ -356,6 +365,8 @@ def converted_expert(seed: int, e: int, H: int, I: int, gate_up_type: int, down_
             dn = convert_q5k(wd)
         elif down_type == MXFP4:
             dn = convert_mxfp4(wd)
+        elif down_type in (F16, F32):
+            dn = convert_float(wd, down_type)
         else:
             dn = convert_bf16(wd)
     return gu, dn, sc

@@ -25,6 +25,10 @@ row only, keeps scale fields finite and of a realistic size:
   MXFP4 (17-byte blocks): E8M0 byte -> 118 + (b & 3) (scales 2^-9 .. 2^-6).
   BF16: each value keeps its sign and 7 mantissa bits; its exponent becomes
         119 + (bits 7..8 of the raw value): magnitudes 2^-8 .. 2^-4.
+  F16: each value keeps its sign and 10 mantissa bits; its exponent field
+        becomes 7 + (bits 10..11): magnitudes 2^-8 .. 2^-4.
+  F32: each value keeps its sign and 23 mantissa bits; its exponent field
+        becomes 119 + (bits 23..24): magnitudes 2^-8 .. 2^-4.
 
 Both implementations below follow this definition independently.
 """
@@ -39,12 +43,13 @@ M64 = (1 << 64) - 1
 
 BF16, Q8_0, Q4_K, NVFP4, Q6_K, Q4_0 = 0, 1, 2, 3, 4, 5
 Q4_1, Q5_0, Q5_1, Q5_K, MXFP4 = 6, 7, 8, 9, 10
+F16, F32 = 11, 12
 
 
 def _row_bytes(wtype: int, k: int) -> int:
     return {BF16: 2 * k, Q8_0: k // 32 * 34, Q4_K: k // 256 * 144, NVFP4: k // 2 + k // 16,
             Q6_K: k // 256 * 210, Q4_0: k // 32 * 18, Q4_1: k // 32 * 20, Q5_0: k // 32 * 22,
-            Q5_1: k // 32 * 24, Q5_K: k // 256 * 176, MXFP4: k // 32 * 17}[wtype]
+            Q5_1: k // 32 * 24, Q5_K: k // 256 * 176, MXFP4: k // 32 * 17, F16: 2 * k, F32: 4 * k}[wtype]
 
 
 # ------------------------------------------------------------------ host (numpy)
@@ -107,6 +112,16 @@ def _mask_np(rows: np.ndarray, wtype: int, k: int) -> np.ndarray:
         exp = 119 + ((v >> 7) & 3)
         v = (v & 0x807F) | (exp << 7)
         rows[:] = v.astype(np.uint16).view(np.uint8).reshape(rows.shape)
+    elif wtype == F16:
+        v = rows.view(np.uint16).astype(np.uint32)
+        exp = 7 + ((v >> 10) & 3)
+        v = (v & 0x83FF) | (exp << 10)
+        rows[:] = v.astype(np.uint16).view(np.uint8).reshape(rows.shape)
+    elif wtype == F32:
+        v = rows.view(np.uint32).astype(np.uint64)
+        exp = 119 + ((v >> 23) & 3)
+        v = (v & 0x807FFFFF) | (exp << 23)
+        rows[:] = v.astype(np.uint32).view(np.uint8).reshape(rows.shape)
     return rows
 
 
@@ -191,3 +206,15 @@ def _mask_torch(rows, wtype: int, k: int) -> None:
         v = torch.bitwise_or(torch.bitwise_and(v, 0x807F), torch.bitwise_left_shift(exp, 7))
         v = torch.where(v >= 0x8000, v - 0x10000, v)
         rows.view(torch.int16).copy_(v.to(torch.int16))
+    elif wtype == F16:
+        v = rows.view(torch.int16).to(torch.int32) & 0xFFFF
+        exp = 7 + torch.bitwise_and(torch.bitwise_right_shift(v, 10), 3)
+        v = torch.bitwise_or(torch.bitwise_and(v, 0x83FF), torch.bitwise_left_shift(exp, 10))
+        v = torch.where(v >= 0x8000, v - 0x10000, v)
+        rows.view(torch.int16).copy_(v.to(torch.int16))
+    elif wtype == F32:
+        v = rows.view(torch.int32).to(torch.int64) & 0xFFFFFFFF
+        exp = 119 + torch.bitwise_and(torch.bitwise_right_shift(v, 23), 3)
+        v = torch.bitwise_or(torch.bitwise_and(v, 0x807FFFFF), torch.bitwise_left_shift(exp, 23))
+        v = torch.where(v >= 0x80000000, v - 0x100000000, v)
+        rows.view(torch.int32).copy_(v.to(torch.int32))

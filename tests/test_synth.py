@@ -17,7 +17,8 @@ def test_splitmix64_known_first_outputs():
 
 def test_counter_bank_host_equals_torch_cpu():
     for wtype, k in [(C.NVFP4, 256), (C.Q4_K, 512), (C.Q8_0, 256), (C.BF16, 64), (C.Q6_K, 512), (C.Q4_0, 256),
-                     (C.Q4_1, 256), (C.Q5_0, 256), (C.Q5_1, 256), (C.Q5_K, 512), (C.MXFP4, 256)]:
+                     (C.Q4_1, 256), (C.Q5_0, 256), (C.Q5_1, 256), (C.Q5_K, 512), (C.MXFP4, 256),
+                     (C.F16, 64), (C.F32, 64)]:
         rb = C._row_bytes(wtype, k)
         rows = 40
         t = torch.empty(rows * rb, dtype=torch.uint8)
@@ -30,7 +31,8 @@ def test_counter_bank_host_equals_torch_cpu():
 
 def test_counter_banks_decode_finite():
     for wtype, k in [(C.NVFP4, 256), (C.Q4_K, 512), (C.Q8_0, 256), (C.BF16, 64), (C.Q6_K, 512), (C.Q4_0, 256),
-                     (C.Q4_1, 256), (C.Q5_0, 256), (C.Q5_1, 256), (C.Q5_K, 512), (C.MXFP4, 256)]:
+                     (C.Q4_1, 256), (C.Q5_0, 256), (C.Q5_1, 256), (C.Q5_K, 512), (C.MXFP4, 256),
+                     (C.F16, 64), (C.F32, 64)]:
         rows = C.bank_bytes_np(99, wtype, k, 0, 64)
         v = F.dequantize_rows(wtype, rows, k)
         # NVFP4 rows exclude weight_scale_2 (applied to the projection output)
