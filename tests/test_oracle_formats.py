@@ -259,6 +259,29 @@ def test_q5k_codes_single_bit_bijection():
     assert len(hits) == 256 * 5
 
 
+def test_mxfp4_codes_single_bit_bijection():
+    """e = 127 (scale 1): each single set bit of the 16 code bytes changes
+    exactly one value, to E2M1 of a one-bit code (0.5, 1, 2 or -0 for the
+    sign bit alone), and the bits cover every (value, code bit) pair once."""
+    hits = set()
+    mags = {1: 0.5, 2: 1.0, 4: 2.0}
+    for byte in range(1, 17):
+        for bit in range(8):
+            blk = np.zeros(17, dtype=np.uint8)
+            blk[0] = 127
+            blk[byte] = 1 << bit
+            v = F.dequantize_rows(F.TYPE_MXFP4, blk[None, :], 32)[0]
+            code_bit = bit % 4
+            value = (byte - 1) + (16 if bit >= 4 else 0)
+            if code_bit == 3:            # the sign bit of a zero code: -0
+                assert (v == 0).all() and np.signbit(v[value]) and np.signbit(v).sum() == 1
+            else:
+                nz = np.nonzero(v)[0]
+                assert list(nz) == [value] and v[value] == mags[1 << code_bit]
+            hits.add((value, code_bit))
+    assert len(hits) == 32 * 4
+
+
 def test_mxfp4_hand_values_and_e8m0():
     assert F.e8m0_value(127) == 1.0 and F.e8m0_value(0) == 2.0 ** -127 and F.e8m0_value(254) == 2.0 ** 127
     blk = np.zeros(2 * 17, dtype=np.uint8)
