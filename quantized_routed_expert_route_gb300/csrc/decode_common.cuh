@@ -268,6 +268,46 @@ __device__ inline void group_routes_warp(const int32_t* ids, int RT, int E, int 
   if (lane == 0) g.misc[1] = bad ? 1 : 0;
 }
 
+// Group up to 32 routes with one warp (lane r holds route r): match/shuffle
+// give each distinct valid expert its slot (ascending id) and each route its
+// place after the earlier routes of the same expert.
+__device__ inline void group_routes_small_warp(const int32_t* ids, int RT, int E, int K, const GroupSmem& g,
+                                               int lane) {
+  int e = (lane < RT) ? ids[lane] : -1;
+  const bool valid = (lane < RT) && e >= 0 && e < E;
+  const bool bad = (lane < RT) && !valid;
+  const int key = valid ? e : -1 - lane;
+  const unsigned peers = __match_any_sync(0xffffffffu, key);
+  const bool first = valid && (lane == __ffs(peers) - 1);
+  int slot = 0, off = 0;
+  for (int j = 0; j < 32; ++j) {
+    const int ej = __shfl_sync(0xffffffffu, key, j);
+    const int fj = __shfl_sync(0xffffffffu, first ? 1 : 0, j);
+    const unsigned pj = __shfl_sync(0xffffffffu, peers, j);
+    if (valid && fj && ej < key) {
+      ++slot;
+      off += __popc(pj);
+    }
+  }
+  const int rank = __popc(peers & ((1u << lane) - 1u));
+  if (valid) {
+    g.routes[off + rank] = (int16_t)lane;
+    g.rtok[off + rank] = (int16_t)(lane / K);
+  }
+  if (first) {
+    g.slot_e[slot] = e;
+    g.slot_off[slot] = off;
+  }
+  const unsigned firsts = __ballot_sync(0xffffffffu, first);
+  const unsigned valids = __ballot_sync(0xffffffffu, valid);
+  const unsigned bads = __ballot_sync(0xffffffffu, bad);
+  if (lane == 0) {
+    g.slot_off[__popc(firsts)] = __popc(valids);
+    g.misc[0] = __popc(firsts);
+    g.misc[1] = bads ? 1 : 0;
+  }
+}
+
 // Group the T*K routes by expert: the distinct valid experts in ascending id
 // order become slots; each slot lists its routes in route order.  Reads only
 // `ids`.  Every CTA of a kernel computes the same grouping.  Up to 32 routes
@@ -277,41 +317,7 @@ __device__ inline void group_routes(const int32_t* ids, int RT, int E, int K, co
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nthr = blockDim.x;
   if (RT <= 32) {
-    if (warp == 0) {
-      int e = (lane < RT) ? ids[lane] : -1;
-      const bool valid = (lane < RT) && e >= 0 && e < E;
-      const bool bad = (lane < RT) && !valid;
-      const int key = valid ? e : -1 - lane;
-      const unsigned peers = __match_any_sync(0xffffffffu, key);
-      const bool first = valid && (lane == __ffs(peers) - 1);
-      int slot = 0, off = 0;
-      for (int j = 0; j < 32; ++j) {
-        const int ej = __shfl_sync(0xffffffffu, key, j);
-        const int fj = __shfl_sync(0xffffffffu, first ? 1 : 0, j);
-        const unsigned pj = __shfl_sync(0xffffffffu, peers, j);
-        if (valid && fj && ej < key) {
-          ++slot;
-          off += __popc(pj);
-        }
-      }
-      const int rank = __popc(peers & ((1u << lane) - 1u));
-      if (valid) {
-        g.routes[off + rank] = (int16_t)lane;
-        g.rtok[off + rank] = (int16_t)(lane / K);
-      }
-      if (first) {
-        g.slot_e[slot] = e;
-        g.slot_off[slot] = off;
-      }
-      const unsigned firsts = __ballot_sync(0xffffffffu, first);
-      const unsigned valids = __ballot_sync(0xffffffffu, valid);
-      const unsigned bads = __ballot_sync(0xffffffffu, bad);
-      if (lane == 0) {
-        g.slot_off[__popc(firsts)] = __popc(valids);
-        g.misc[0] = __popc(firsts);
-        g.misc[1] = bads ? 1 : 0;
-      }
-    }
+    if (warp == 0) group_routes_small_warp(ids, RT, E, K, g, lane);
     __syncthreads();
     return;
   }
@@ -816,11 +822,14 @@ __device__ __forceinline__ float dn_row_q8(const uint8_t* rowp, bool vrow, int I
 // "Gaussian Error Linear Units", 2016).  FreeToken PR #732, "Other checks",
 // runs its experts with both.
 constexpr int kGluSilu = 0, kGluGeluTanh = 1;
+// gelu_tanh(g) * u, out of line: it keeps tanhf's code out of every kernel's
+// hot path when the layer uses SiLU
+static __device__ __noinline__ float gelu_tanh_glu(float g, float u) {
+  const float z = 0.7978845608028654f * fmaf(0.044715f * g, g * g, g);
+  return 0.5f * g * (1.0f + tanhf(z)) * u;
+}
 __device__ __forceinline__ float glu_act(float g, float u, int kind) {
-  if (kind == kGluGeluTanh) {
-    const float z = 0.7978845608028654f * fmaf(0.044715f * g, g * g, g);
-    return 0.5f * g * (1.0f + tanhf(z)) * u;
-  }
+  if (kind == kGluGeluTanh) return gelu_tanh_glu(g, u);
   return __fdividef(g, 1.0f + expf(-g)) * u;
 }
 

@@ -75,6 +75,14 @@ struct ActQ8 {
   int sum;
 };
 
+// The exact path of the q8_1 rule for one element: rint(x / d) with the IEEE
+// division, 0 when d == 0.  It is taken rarely (x*r within 2^-12 of a
+// half-integer, or d not a normal number), so it stays out of line: inlined
+// at every element it would multiply the code size of each quantizing kernel.
+static __device__ __noinline__ int q8_1_code_exact(float x, float d) {
+  return (d == 0.0f) ? 0 : __float2int_rn(__fdiv_rn(x, d));
+}
+
 // Quantize one 32-value block held by one thread: d = amax/127 (IEEE fp32
 // division), q_i = round-half-even(v_i/d) (IEEE fp32 division), 0 when d = 0;
 // returns the 32 codes packed as eight int8x4 words, d, and the exact code
@@ -104,7 +112,7 @@ __device__ __forceinline__ void q8_1_quantize_block(const float (&v)[32], uint32
       const float near = fabsf(t - floorf(t) - 0.5f);
       int q;
       if (fast && near > 0.000244140625f) q = __float2int_rn(t);
-      else q = (d == 0.0f) ? 0 : __float2int_rn(__fdiv_rn(x, d));
+      else q = q8_1_code_exact(x, d);
       sum += q;
       word |= ((uint32_t)(q & 0xFF)) << (8 * j);
     }
@@ -134,7 +142,7 @@ __device__ __forceinline__ void q8_1_quantize_quad(const float (&v)[8], uint32_t
     const float near = fabsf(t - floorf(t) - 0.5f);
     int q;
     if (fast && near > 0.000244140625f) q = __float2int_rn(t);
-    else q = (d == 0.0f) ? 0 : __float2int_rn(__fdiv_rn(v[i], d));
+    else q = q8_1_code_exact(v[i], d);
     s += q;
     w[i >> 2] |= ((uint32_t)(q & 0xFF)) << (8 * (i & 3));
   }
@@ -159,7 +167,7 @@ __device__ __forceinline__ int q8_1_quantize_lane(float v, float& d, int& sum) {
   const float near = fabsf(t - floorf(t) - 0.5f);
   int q;
   if (fast && near > 0.000244140625f) q = __float2int_rn(t);
-  else q = (d == 0.0f) ? 0 : __float2int_rn(__fdiv_rn(v, d));
+  else q = q8_1_code_exact(v, d);
   int s = q;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);

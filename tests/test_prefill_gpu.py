@@ -44,6 +44,7 @@ def test_tc_gemm_matches_f64(K, N):
 from oracle import formats as F  # noqa: E402
 from oracle import layer as OL  # noqa: E402
 from tests import cases  # noqa: E402
+from tests import tolerance as tol  # noqa: E402
 
 # The prompt configuration's tolerances (relative L2 of the bf16 output against
 # the oracle's bf16 output): 1e-2 for W4A4, 2e-3 for W4A8 and FP16.
@@ -73,6 +74,12 @@ def _x_quantized(case, mode):
 
 
 def _check_prefill(case, mode, tokens=None):
+    """The sort and the quantized x bit for bit; then, from the oracle's own
+    stages (tests/tolerance.py, prefill_bounds), every bf16 output within its
+    derived bound, equal to the oracle's bf16 output wherever that rounding is
+    unambiguous, and the requantized intermediate equal to the oracle's
+    except where an fp32 intermediate may round the other way; the prompt
+    configuration's relative-L2 tolerance is kept as an aggregate line."""
     res = cases.run_prefill_gpu(case, mode)
     g = case.geom
     T = case.x.shape[0]
@@ -82,30 +89,31 @@ def _check_prefill(case, mode, tokens=None):
     assert np.array_equal(res["xq"], _x_quantized(case, mode)), "quantized activations differ"
     ref, ref_bits, st = cases.prefill_oracle(case, mode, tokens)
     sel = np.arange(T) if tokens is None else np.asarray(tokens)
-    got = F.bf16_bits_to_f64(res["out"][sel])
-    refb = F.bf16_bits_to_f64(ref_bits)
-    assert np.isfinite(got).all()
-    rel_l2 = np.linalg.norm(got - refb) / max(np.linalg.norm(refb), 1e-30)
-    rel_l2_f64 = np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-30)
-    assert rel_l2 <= TOL_L2[mode], (rel_l2, rel_l2_f64)
-    # the requantized intermediate of the checked routes: most values equal
-    # the oracle's exactly (a value may differ where the fp32 and fp64
-    # intermediates round to different codes; W4A4 values are exact in fp16)
+    beta, flips, amb = tol.prefill_bounds(g, st, mode)
+    figs = tol.check_output(res["out"][sel], ref, beta, l2_tol=TOL_L2[mode])
+    # the requantized intermediate of the checked routes (the GPU exports it
+    # as fp16 in sorted-row order; the W4A8 operand is q*d rounded once to fp16)
     pos = np.full(case.ids.size, -1, dtype=np.int64)
     pos[order] = np.arange(order.size)
-    eq = tot = 0
+    n_amb = n_tot = 0
     for i, t in enumerate(sel):
         for k in range(g.top_k):
             if not st["valid"][i, k]:
                 continue
             row = res["i16"][pos[t * g.top_k + k]].astype(np.float64)
             want = st["inter_hat"][i, k]
-            if mode == 1:   # the exported W4A8 operand is q*d rounded once to fp16
+            allowed = flips[i, k]
+            if mode == 1:
                 want = want.astype(np.float16).astype(np.float64)
-            eq += int(np.sum(row == want))
-            tot += row.size
-    assert eq >= 0.99 * tot, (eq, tot)
-    return res, rel_l2
+                allowed = allowed + tol.ulp_fp16(np.abs(want) + allowed)
+            diff = np.abs(row - want)
+            a = amb[i, k]
+            assert np.all(diff[~a] == 0), f"route ({t},{k}): {int(np.sum(diff[~a] != 0))} unambiguous codes differ"
+            assert np.all(diff <= allowed * (1 + 1e-9) + 1e-300), f"route ({t},{k}): a code beyond its rounding"
+            n_amb += int(a.sum())
+            n_tot += a.size
+    figs["inter_ambiguous_frac"] = n_amb / max(n_tot, 1)
+    return res, figs
 
 
 def _ragged_ids(T, E, K, seed):
@@ -143,5 +151,5 @@ def test_prefill_qwen3_30b_a3b_shaped_chunk(mode):
     """H=2048 I=768 E=128 top-8, a 4096-token chunk (32768 routed rows); the
     oracle checks a sample of tokens, the sort and the quantized x in full."""
     case = cases.make_prefill_case(2048, 768, 128, 8, 4096, seed=300 + mode)
-    res, rel = _check_prefill(case, mode, tokens=[0, 1, 2047, 4095])
+    res, _ = _check_prefill(case, mode, tokens=[0, 1, 2047, 4095])
     assert res["err"] == 0
