@@ -202,18 +202,21 @@ int moe_decode(const moe_bank* bank, const void* x, int32_t T,
 /* moe_decode without a caller-provided workspace, for callers that cannot
  * allocate device memory: plugins whose host framework owns every device
  * allocation and hands the library only its own tensors, and latency-critical
- * serving paths where a cudaMalloc may synchronize the device.  The paper has
+ * serving paths where a cudaMalloc may synchronize the device.  The pages have
  * no counterpart to this entry point; it exists for those callers.
  *
  * The workspace is a fixed MOE_NOALLOC_WS_BYTES array in device memory that
  * every GPU loading this library holds until the process exits.  The first
- * call on a device looks up that array's device address (with that device
- * current); make that first call before any stream capture.  Every call
+ * call on a device (and the first after that device's context was torn down
+ * and created again) looks up that array's device address with that device
+ * current; make that first call before any stream capture.  Every call
  * shares the array and starts by clearing its error word; the array keeps the
  * last call's contents otherwise.  Calls that overlap on the GPU (on different
- * streams, or from different threads) race on it, so order them.  Device-side
- * error bits of these calls are not reported (a bad id still contributes
- * zero).  Arguments as for moe_decode.  Returns MOE_EINVAL, without launching
+ * streams, or from different threads) race on it, so order them.  This call
+ * itself reports no device-side error bits: a bad id contributes zero, and a
+ * bounded wait that ran out leaves the outputs invalid; read the bits with
+ * moe_get_error(NULL, 0, stream, &bits), which reads this array's error word.
+ * Arguments as for moe_decode.  Returns MOE_EINVAL, without launching
  * anything, when one pass of this call would need more workspace than
  * MOE_NOALLOC_WS_BYTES (moe_workspace_bytes(bank, T) tells), and never calls
  * cudaMalloc or cudaFree. */
@@ -283,7 +286,9 @@ int moe_decode_host(const moe_bank* bank, const void* x, int32_t T,
 
 /* Read and clear the workspace's sticky device error bits (synchronizes
  * `stream`).  *dev_err receives the MOE_DEVERR_* bits; returns MOE_EDEVICE if
- * any was set, MOE_OK otherwise. */
+ * any was set, MOE_OK otherwise.  ws = NULL (ws_bytes ignored) reads the
+ * fixed workspace of moe_decode_noalloc on the current device; this too
+ * allocates nothing. */
 int moe_get_error(void* ws, size_t ws_bytes, void* stream, int32_t* dev_err);
 
 /* Text for a moe_status value (static storage). */
@@ -437,6 +442,21 @@ int moe_cache_stats(const moe_cache* cache, int64_t* hits, int64_t* misses, int6
  * bounded wait for the MMA ran out. */
 int moe_debug_tc_gemm(const void* A, const void* B, int32_t K, int32_t N, float* D,
                       int32_t* dev_err, void* stream);
+
+/* Failure-detection check (the auxiliary failure detection of the build, not
+ * an operation of the pages): one thread runs one of the kernels' bounded
+ * waits on an mbarrier whose phase nothing completes, so the wait runs out
+ * and the kernel sets MOE_DEVERR_TIMEOUT in *dev_err and returns; the
+ * context stays usable.
+ *   mode 0: the sleeping-poll wait of the decode kernels, `limit` polls of at
+ *           most about 0.5 ms each;
+ *   mode 1: the spinning wait of the grouped and prompt-path kernels, `limit`
+ *           microseconds of device time.
+ *   limit:  1 .. MOE_DEBUG_WAIT_MAX.
+ *   dev_err: device uint32 (caller-zeroed); OR-ed with MOE_DEVERR_TIMEOUT.
+ * Asynchronous on `stream`; allocates nothing.  Errors: MOE_EINVAL. */
+enum { MOE_DEBUG_WAIT_MAX = 64 };
+int moe_debug_wait_timeout(int32_t mode, int32_t limit, uint32_t* dev_err, void* stream);
 
 #ifdef __cplusplus
 }

@@ -21,6 +21,7 @@ MOE_MAX_E, MOE_MAX_TOPK, MOE_DECODE_T_CHUNK, MOE_LINEAR_MAX_T = 1024, 32, 64, 8
 MOE_PREFILL_W4A4, MOE_PREFILL_W4A8, MOE_PREFILL_FP16 = 0, 1, 2
 MOE_GLU_SILU, MOE_GLU_GELU_TANH = 0, 1
 MOE_NOALLOC_WS_BYTES = 4 << 20
+MOE_DEBUG_WAIT_MAX = 64
 
 # every symbol include/qre_moe.h declares
 EXPORTS = (
@@ -28,6 +29,7 @@ EXPORTS = (
     "moe_workspace_bytes", "moe_workspace_init", "moe_decode", "moe_get_error",
     "moe_status_string", "moe_last_cuda_error", "moe_quantize_q8_1",
     "moe_debug_block_dots", "moe_debug_decode_stages", "moe_decode_noalloc", "moe_debug_tc_gemm",
+    "moe_debug_wait_timeout",
     "moe_prefill_workspace_bytes", "moe_prefill_grouped", "moe_debug_prefill_stages",
     "moe_decode_kernel_count", "moe_decode_io_bytes", "moe_decode_io_offsets", "moe_decode_host",
     "moe_linear", "moe_cache_plan", "moe_slot_table_create", "moe_slot_table_destroy", "moe_slot_table_acquire",
@@ -76,6 +78,7 @@ def _load() -> ctypes.CDLL:
         "moe_debug_decode_stages": (ctypes.c_int, [vp, vp, i32, vp, vp, vp, vp, sz, vp, vp, vp, vp]),
         "moe_decode_noalloc": (ctypes.c_int, [vp, vp, i32, vp, vp, vp, vp]),
         "moe_debug_tc_gemm": (ctypes.c_int, [vp, vp, i32, i32, vp, vp, vp]),
+        "moe_debug_wait_timeout": (ctypes.c_int, [i32, i32, vp, vp]),
         "moe_linear": (ctypes.c_int, [i32, vp, i32, i32, vp, vp, i32, vp, vp, vp]),
         "moe_cache_plan": (ctypes.c_int, [i64, i32, vp, vp, vp]),
         "moe_slot_table_create": (ctypes.c_int, [i32, ctypes.POINTER(vp)]),
@@ -271,6 +274,11 @@ def moe_cache_stats(cache: int):
     h, m, b = ctypes.c_int64(0), ctypes.c_int64(0), ctypes.c_int64(0)
     _check(_lib.moe_cache_stats(cache, ctypes.byref(h), ctypes.byref(m), ctypes.byref(b)), "moe_cache_stats")
     return int(h.value), int(m.value), int(b.value)
+
+
+def moe_debug_wait_timeout(mode: int, limit: int, dev_err: int, stream: int = 0) -> None:
+    """A bounded wait that runs out (failure-detection check); see include/qre_moe.h."""
+    _check(_lib.moe_debug_wait_timeout(mode, limit, dev_err, stream or None), "moe_debug_wait_timeout")
 
 
 def moe_debug_tc_gemm(A: int, B: int, K: int, N: int, D: int, dev_err: int, stream: int = 0) -> None:

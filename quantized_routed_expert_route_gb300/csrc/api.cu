@@ -692,21 +692,52 @@ static __device__ __align__(256) uint8_t g_noalloc_ws[MOE_NOALLOC_WS_BYTES];
 namespace {
 constexpr int kMaxDevices = 64;
 std::mutex g_noalloc_mu;
+// Per device: the context the address was looked up in, and the address.
+// Keyed on the context, so a device reset (a new context, the module loaded
+// again) looks the address up again instead of using a stale one.
+void* g_noalloc_ctx[kMaxDevices] = {};
 void* g_noalloc_ptr[kMaxDevices] = {};
+
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+
+CtxGetCurrentFn ctx_get_current() {
+  static std::once_flag once;
+  static CtxGetCurrentFn fn = nullptr;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess && f)
+      fn = reinterpret_cast<CtxGetCurrentFn>(f);
+    else
+      cudaGetLastError();
+  });
+  return fn;
+}
 
 int noalloc_workspace(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "noalloc: cudaGetDevice");
   if (dev < 0 || dev >= kMaxDevices) return MOE_EUNSUPPORTED;
+  const CtxGetCurrentFn get = ctx_get_current();
+  CUcontext ctx = nullptr;
+  if (!get || get(&ctx) != CUDA_SUCCESS) ctx = nullptr;
   std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  if (!g_noalloc_ptr[dev]) {
-    void* ptr = nullptr;
-    e = cudaGetSymbolAddress(&ptr, g_noalloc_ws);
-    if (e != cudaSuccess || !ptr) return cuda_fail(e, "noalloc: cudaGetSymbolAddress");
-    g_noalloc_ptr[dev] = ptr;
+  if (g_noalloc_ptr[dev] && ctx && g_noalloc_ctx[dev] == (void*)ctx) {
+    *out = g_noalloc_ptr[dev];
+    return MOE_OK;
   }
-  *out = g_noalloc_ptr[dev];
+  // first call in this context: the lookup (which also makes the device's
+  // context current if it was not yet)
+  void* ptr = nullptr;
+  e = cudaGetSymbolAddress(&ptr, g_noalloc_ws);
+  if (e != cudaSuccess || !ptr) return cuda_fail(e, "noalloc: cudaGetSymbolAddress");
+  ctx = nullptr;
+  if (!get || get(&ctx) != CUDA_SUCCESS) ctx = nullptr;   // unknown: looked up again next call
+  g_noalloc_ptr[dev] = ptr;
+  g_noalloc_ctx[dev] = (void*)ctx;
+  *out = ptr;
   return MOE_OK;
 }
 }  // namespace
@@ -733,7 +764,13 @@ int moe_decode_noalloc(const moe_bank* b, const void* x, int32_t T, const int32_
 }
 
 int moe_get_error(void* ws, size_t ws_bytes, void* stream, int32_t* dev_err) {
-  if (!ws || ws_bytes < 4 || !dev_err) return MOE_EINVAL;
+  if (!dev_err) return MOE_EINVAL;
+  if (!ws) {   // the fixed workspace of moe_decode_noalloc
+    const int st = noalloc_workspace(&ws);
+    if (st) return st;
+    ws_bytes = MOE_NOALLOC_WS_BYTES;
+  }
+  if (ws_bytes < 4) return MOE_EINVAL;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint32_t v = 0;
   cudaError_t e = cudaMemcpyAsync(&v, ws, 4, cudaMemcpyDeviceToHost, s);
@@ -894,6 +931,13 @@ int moe_debug_tc_gemm(const void* A, const void* B, int32_t K, int32_t N, float*
   cudaError_t e = launch_tc_gemm_check(static_cast<const uint16_t*>(A), static_cast<const uint16_t*>(B), K, N, D,
                                        dev_err, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? MOE_OK : cuda_fail(e, "tc_gemm");
+}
+
+int moe_debug_wait_timeout(int32_t mode, int32_t limit, uint32_t* dev_err, void* stream) {
+  if (!dev_err || !aligned(dev_err, 4) || (mode != 0 && mode != 1)) return MOE_EINVAL;
+  if (limit < 1 || limit > MOE_DEBUG_WAIT_MAX) return MOE_EINVAL;
+  cudaError_t e = launch_wait_timeout(mode, (uint32_t)limit, dev_err, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MOE_OK : cuda_fail(e, "wait_timeout");
 }
 
 int moe_debug_decode_stages(const moe_bank* b, const void* x, int32_t T, const int32_t* ids, const float* w,

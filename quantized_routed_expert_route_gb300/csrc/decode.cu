@@ -275,4 +275,29 @@ cudaError_t launch_export_q8(const int8_t* q, const float* d, const uint16_t* s,
   return cudaGetLastError();
 }
 
+// Test hook: one of the kernels' bounded waits on an mbarrier whose phase
+// nothing ever completes (it expects one arrival that never comes), with a
+// short limit.  mode 0: mbar_wait_bounded, `limit` sleeping polls (the form
+// the decode kernels use); mode 1: mbar_wait_spin, `limit` microseconds of
+// device time (the grouped and prompt-path kernels).  When the wait runs out
+// the kernel ORs kErrTimeout into *err and returns, as those kernels do.
+__global__ void k_wait_timeout(int mode, uint32_t limit, uint32_t* err) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const bool ok = (mode == 0) ? mbar_wait_bounded(&bar, 0u, limit)
+                                : mbar_wait_spin(&bar, 0u, 1000ull * (unsigned long long)limit);
+    if (!ok) atomicOr(err, kErrTimeout);
+  }
+}
+
+cudaError_t launch_wait_timeout(int mode, uint32_t limit, uint32_t* err, cudaStream_t stream) {
+  k_wait_timeout<<<1, 32, 0, stream>>>(mode, limit, err);
+  return cudaGetLastError();
+}
+
 }  // namespace qre

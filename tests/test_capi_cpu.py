@@ -103,3 +103,16 @@ def test_host_argument_checks_of_the_newer_entry_points(capi):
     slots = (ctypes.c_int64 * 1)()
     assert lib.moe_cache_plan(-1, 1, (ctypes.c_int64 * 1)(5), (ctypes.c_int64 * 1)(1), slots) == capi.MOE_EINVAL
     assert lib.moe_cache_plan(100, 1, (ctypes.c_int64 * 1)(0), (ctypes.c_int64 * 1)(1), slots) == capi.MOE_EINVAL
+
+
+def test_wait_timeout_hook_argument_checks(capi):
+    """The failure-detection hook rejects bad modes, limits and pointers on
+    the host, before any device work."""
+    lib = capi.library()
+    buf = ctypes.create_string_buffer(64)
+    addr = ctypes.addressof(buf)
+    assert lib.moe_debug_wait_timeout(2, 4, addr, None) == capi.MOE_EINVAL
+    assert lib.moe_debug_wait_timeout(0, 0, addr, None) == capi.MOE_EINVAL
+    assert lib.moe_debug_wait_timeout(1, capi.MOE_DEBUG_WAIT_MAX + 1, addr, None) == capi.MOE_EINVAL
+    assert lib.moe_debug_wait_timeout(0, 4, None, None) == capi.MOE_EINVAL
+    assert lib.moe_debug_wait_timeout(0, 4, addr + 1, None) == capi.MOE_EINVAL

@@ -1,10 +1,13 @@
 """moe_decode_noalloc: the decode entry point for callers that cannot allocate
 device memory (plugins whose host framework owns every device allocation,
-serving paths where a cudaMalloc may synchronize the device).  It runs on the library's
-fixed device workspace; this checks, through the C ABI, that two calls in a
-row give the same outputs as moe_decode with a caller workspace, within the
-layer tolerance the other tests use.  This file is collected last so that a
-failure here comes after every other test has run."""
+serving paths where a cudaMalloc may synchronize the device).  It runs on the
+library's fixed device workspace.  Through the C ABI this checks, on calls in
+a row, that its outputs equal those of moe_decode with a caller workspace bit
+for bit (the same kernels on the same inputs), including the grouped Q4_K
+path whose tensor maps point into the fixed workspace; that one call is
+within the oracle's derived bounds; and that moe_get_error with no workspace
+reads the fixed workspace's error word.  This file is collected last so that
+a failure here comes after every other test has run."""
 import numpy as np
 import pytest
 
@@ -19,35 +22,65 @@ from quantized_routed_expert_route_gb300 import capi  # noqa: E402
 from quantized_routed_expert_route_gb300.layer import MoeLayer  # noqa: E402
 from synth import banks as S  # noqa: E402
 from tests import cases  # noqa: E402
+from tests import tolerance as tol  # noqa: E402
 
 
-def _close(a_bits, b_bits):
-    a = F.bf16_bits_to_f64(a_bits)
-    b = F.bf16_bits_to_f64(b_bits)
-    scale = max(np.abs(b).max(), 1e-30)
-    max_rel = np.abs(a - b).max() / scale
-    rel_l2 = np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-30)
-    assert max_rel <= 2e-3 and rel_l2 <= 5e-4, (max_rel, rel_l2)
-
-
-def test_noalloc_matches_moe_decode_on_two_calls():
-    case = cases.make_case(2048, 768, 128, 8, F.TYPE_NVFP4, F.TYPE_NVFP4, 8, seed=200)
+def _layer(case):
     g = case.geom
-    layer = MoeLayer(g.H, g.I, g.E, g.top_k, g.gate_up_type, g.down_type, case.gu_dev, case.dn_dev,
-                     torch.from_numpy(case.sb).cuda(), borrow=True)
+    return MoeLayer(g.H, g.I, g.E, g.top_k, g.gate_up_type, g.down_type, case.gu_dev, case.dn_dev,
+                    torch.from_numpy(case.sb).cuda(), borrow=True)
+
+
+def _both(layer, x, ids, w, T, H, stream):
+    ref = torch.empty((T, H), dtype=torch.int16, device="cuda")
+    got = torch.full((T, H), -1, dtype=torch.int16, device="cuda")
+    capi.moe_decode(layer.bank, x.data_ptr(), T, ids.data_ptr(), w.data_ptr(), ref.data_ptr(),
+                    layer.ws.data_ptr(), layer.ws_bytes, stream)
+    capi.moe_decode_noalloc(layer.bank, x.data_ptr(), T, ids.data_ptr(), w.data_ptr(), got.data_ptr(), stream)
+    torch.cuda.synchronize()
+    return got.cpu().numpy().view(np.uint16), ref.cpu().numpy().view(np.uint16)
+
+
+def _no_device_error(stream):
+    bits = capi.ctypes.c_int32(-1)
+    st = capi.library().moe_get_error(None, 0, stream, capi.ctypes.byref(bits))
+    assert st == capi.MOE_OK and bits.value == 0, (st, bits.value)
+
+
+def test_noalloc_matches_moe_decode_on_calls_in_a_row():
     stream = torch.cuda.current_stream().cuda_stream
+    # the Qwen3-30B-A3B-shaped NVFP4 layer: the fused kernel at T=1, the batched path at T=8
+    case = cases.make_case(2048, 768, 128, 8, F.TYPE_NVFP4, F.TYPE_NVFP4, 1, seed=200)
+    g = case.geom
+    layer = _layer(case)
     for call, T in enumerate((1, 8)):
+        assert capi.moe_workspace_bytes(layer.bank, T) <= capi.MOE_NOALLOC_WS_BYTES
         x = torch.from_numpy(S.hidden_bf16(300 + call, T, g.H).view(np.int16)).cuda()
         ids_np, w_np = S.softmax_topk_routing(400 + call, T, g.E, g.top_k)
-        ids = torch.from_numpy(ids_np).cuda()
-        w = torch.from_numpy(w_np).cuda()
-        ref = torch.empty((T, g.H), dtype=torch.int16, device="cuda")
-        got = torch.full((T, g.H), -1, dtype=torch.int16, device="cuda")
-        capi.moe_decode(layer.bank, x.data_ptr(), T, ids.data_ptr(), w.data_ptr(), ref.data_ptr(),
-                        layer.ws.data_ptr(), layer.ws_bytes, stream)
-        capi.moe_decode_noalloc(layer.bank, x.data_ptr(), T, ids.data_ptr(), w.data_ptr(), got.data_ptr(), stream)
-        torch.cuda.synchronize()
-        _close(got.cpu().numpy().view(np.uint16), ref.cpu().numpy().view(np.uint16))
+        got, ref = _both(layer, x, torch.from_numpy(ids_np).cuda(), torch.from_numpy(w_np).cuda(), T, g.H, stream)
+        assert np.array_equal(got, ref), f"call {call} (T={T}): outputs differ from moe_decode"
+        _no_device_error(stream)
+    # one call against the oracle: the case's own inputs (its routed experts hold converted rows)
+    x = torch.from_numpy(case.x.view(np.int16)).cuda()
+    got, ref = _both(layer, x, torch.from_numpy(case.ids).cuda(), torch.from_numpy(case.w).cuda(), 1, g.H, stream)
+    assert np.array_equal(got, ref)
+    want, _, st = cases.oracle(case)
+    beta, _, _ = tol.output_bounds(g, st)
+    tol.check_output(got, want, beta)
+    layer.close()
+    # the Laguna-shaped Q4_K layer at T=16: the grouped path, whose tensor maps
+    # are encoded over the fixed workspace's device address
+    case = cases.make_case(4096, 768, 256, 10, F.TYPE_Q4_K, F.TYPE_Q4_K, 16, seed=210, routing="zipf")
+    g = case.geom
+    layer = _layer(case)
+    assert capi.moe_decode_kernel_count(layer.bank, 16) == 4
+    assert capi.moe_workspace_bytes(layer.bank, 16) <= capi.MOE_NOALLOC_WS_BYTES
+    x = torch.from_numpy(case.x.view(np.int16)).cuda()
+    ids, w = torch.from_numpy(case.ids).cuda(), torch.from_numpy(case.w).cuda()
+    for call in range(2):
+        got, ref = _both(layer, x, ids, w, 16, g.H, stream)
+        assert np.array_equal(got, ref), f"Laguna Q4_K call {call}: outputs differ from moe_decode"
+    _no_device_error(stream)
     layer.close()
 
 
