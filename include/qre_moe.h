@@ -76,14 +76,19 @@ extern "C" {
  *   MOE_MXFP4: K/32 blocks of {uint8 e; uint8 qs[16]} (17 bytes), E2M1 codes
  *              laid out as MOE_Q4_0, value E2M1(code) * 2^(e - 127); e = 255
  *              (not a finite E8M0 scale) must not occur.
- * (Q4_1 through MXFP4 are the remaining types of FreeToken PR #704's
- * synthetic list, "Validation"; GGUF bit layouts.)  Banks must be readable
+ *   MOE_F16  : K little-endian IEEE fp16 (2K bytes).
+ *   MOE_F32  : K little-endian IEEE fp32 (4K bytes).
+ * (Q4_1 through MXFP4, F16 and F32 are the remaining types of FreeToken PR
+ * #704's synthetic list, "Validation"; GGUF bit layouts.)  Float rows (BF16,
+ * F16, F32) take the activations unquantized, as BF16 does: x as its bf16
+ * values, the intermediate as fp32; a float gate_up or down may sit beside a
+ * quantized one of the other projection.  Banks must be readable
  * up to the next 16-byte boundary past their last row.
  * Gate_up and down may be of different types (e.g. Q4_K gate_up with Q6_K
  * down, the pairing of a Q4_K_M checkpoint). */
 typedef enum {
   MOE_BF16 = 0, MOE_Q8_0 = 1, MOE_Q4_K = 2, MOE_NVFP4 = 3, MOE_Q6_K = 4, MOE_Q4_0 = 5,
-  MOE_Q4_1 = 6, MOE_Q5_0 = 7, MOE_Q5_1 = 8, MOE_Q5_K = 9, MOE_MXFP4 = 10
+  MOE_Q4_1 = 6, MOE_Q5_0 = 7, MOE_Q5_1 = 8, MOE_Q5_K = 9, MOE_MXFP4 = 10, MOE_F16 = 11, MOE_F32 = 12
 } moe_type;
 
 typedef enum {
@@ -315,7 +320,7 @@ int moe_quantize_q8_1(const float* x, int64_t n, void* out_blocks, void* stream)
  * (sum of (code - 32) * q per 16-value scale group), k/32 for MOE_Q4_0 (sum of
  * (code - 8) * q), MOE_Q5_0 (sum of (code - 16) * q), MOE_Q4_1, MOE_Q5_1 and
  * MOE_Q5_K (sum of code * q) and MOE_MXFP4 (sum of (2*E2M1 code value) * q).
- * MOE_BF16 is MOE_EINVAL. */
+ * Float types (MOE_BF16, MOE_F16, MOE_F32) are MOE_EINVAL. */
 int moe_debug_block_dots(int32_t type, const void* rows, int32_t nrows, int32_t k,
                          const void* act_blocks, int32_t* out, void* stream);
 
@@ -352,7 +357,7 @@ int moe_debug_prefill_stages(const moe_bank* bank, const void* x, int32_t T,
  * (the decode path's prep_input), each 32-value block's integer dot is exact,
  * the block scales and row_scale are applied in fp32, and the output is
  * rounded once to bf16 (ties to even).
- *   type:      any quantized moe_type (MOE_BF16 is MOE_EUNSUPPORTED); an
+ *   type:      any quantized moe_type (float types are MOE_EUNSUPPORTED); an
  *              NVFP4 tensor's weight_scale_2 goes into row_scale
  *   rows:      device, N rows of moe_row_bytes(type, K) bytes back to back,
  *              16-byte aligned and readable up to the next 16-byte boundary

@@ -13,7 +13,7 @@ import os
 from .build import lib_path
 
 MOE_BF16, MOE_Q8_0, MOE_Q4_K, MOE_NVFP4, MOE_Q6_K, MOE_Q4_0 = 0, 1, 2, 3, 4, 5
-MOE_Q4_1, MOE_Q5_0, MOE_Q5_1, MOE_Q5_K, MOE_MXFP4 = 6, 7, 8, 9, 10
+MOE_Q4_1, MOE_Q5_0, MOE_Q5_1, MOE_Q5_K, MOE_MXFP4, MOE_F16, MOE_F32 = 6, 7, 8, 9, 10, 11, 12
 MOE_OK, MOE_EINVAL, MOE_EUNSUPPORTED, MOE_ENOMEM, MOE_ECUDA, MOE_EDEVICE = 0, -1, -2, -3, -4, -5
 MOE_DEVERR_BAD_ID, MOE_DEVERR_TIMEOUT = 1, 2
 MOE_SRC_HOST, MOE_SRC_DEVICE, MOE_SRC_DEVICE_BORROW = 0, 1, 2

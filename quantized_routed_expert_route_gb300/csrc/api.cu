@@ -115,8 +115,8 @@ int geom_check(const moe_layer_geom* g) {
   if (!g) return MOE_EINVAL;
   if (g->E < 1 || g->E > kMaxE || g->top_k < 1 || g->top_k > kMaxTopK || g->top_k > g->E) return MOE_EINVAL;
   if (g->H < 32 || g->I < 32 || g->H > (1 << 16) || g->I > (1 << 16)) return MOE_EINVAL;
-  if (g->gate_up_type < MOE_BF16 || g->gate_up_type > MOE_MXFP4) return MOE_EINVAL;
-  if (g->down_type < MOE_BF16 || g->down_type > MOE_MXFP4) return MOE_EINVAL;
+  if (g->gate_up_type < MOE_BF16 || g->gate_up_type > MOE_F32) return MOE_EINVAL;
+  if (g->down_type < MOE_BF16 || g->down_type > MOE_F32) return MOE_EINVAL;
   if (row_bytes_of(g->gate_up_type, g->H) == 0 || row_bytes_of(g->down_type, g->I) == 0) return MOE_EINVAL;
   if (g->H % 32 != 0 || g->I % 32 != 0) return MOE_EINVAL;
   if (g->glu != MOE_GLU_SILU && g->glu != MOE_GLU_GELU_TANH) return MOE_EINVAL;
@@ -216,10 +216,10 @@ void plan_layer_small(const moe_layer_geom& g, int T, DecodeParams& p) {
   const int gu_stage = 2 * q.gu_up_off, dn_stage = q.dn_slots_per_stage * q.dn_piece_bytes;
   q.ls_sb = gu_stage > dn_stage ? gu_stage : dn_stage;
   const size_t RT = (size_t)T * g.top_k;
-  const size_t xa = (g.gate_up_type == MOE_BF16) ? 2 * (size_t)T * g.H : (size_t)T * g.H + 8 * (size_t)T * (g.H / 32);
+  const size_t xa = is_float_w(g.gate_up_type) ? 2 * (size_t)T * g.H : (size_t)T * g.H + 8 * (size_t)T * (g.H / 32);
   q.gu_act_smem = 1;
   q.gu_act_bytes = (int)align_up(xa, 16);
-  if (g.down_type == MOE_BF16) {
+  if (is_float_w(g.down_type)) {
     const size_t ia = 4 * RT * g.I;
     q.dn_act_smem = ia <= 48 * 1024 ? 1 : 0;
     q.dn_act_bytes = q.dn_act_smem ? (int)align_up(ia, 16) : 0;
@@ -266,8 +266,8 @@ DecodeParams make_params(const moe_bank* b, const WsLayout& L, uint8_t* ws, cons
   // + k_down.
   {
     const size_t RT0 = (size_t)T * g.top_k;
-    const size_t gu_need = (g.gate_up_type == MOE_BF16) ? 2 * (size_t)T * g.H : (size_t)T * g.H * 5 / 4;
-    const size_t dn_need = (g.down_type == MOE_BF16) ? 0 : RT0 * g.I * 5 / 4;
+    const size_t gu_need = is_float_w(g.gate_up_type) ? 2 * (size_t)T * g.H : (size_t)T * g.H * 5 / 4;
+    const size_t dn_need = is_float_w(g.down_type) ? 0 : RT0 * g.I * 5 / 4;
     p.maxnt = (T <= 2 && gu_need <= 48 * 1024 && dn_need <= 64 * 1024) ? 1 : 4;
   }
   p.g_gu = sh.g_gu;
@@ -297,12 +297,12 @@ DecodeParams make_params(const moe_bank* b, const WsLayout& L, uint8_t* ws, cons
   p.dn_nstage = dns < 2 ? 2 : (dns > 8 ? 8 : dns);
   // activations staged in shared memory when they fit (always on the two-kernel path)
   const size_t RT = (size_t)T * g.top_k;
-  const size_t gu_act = (g.gate_up_type == MOE_BF16) ? 2 * (size_t)T * g.H
+  const size_t gu_act = is_float_w(g.gate_up_type) ? 2 * (size_t)T * g.H
                                                      : (size_t)T * g.H + 8 * (size_t)T * (g.H / 32);
   p.gu_act_smem = (p.maxnt == 1 || gu_act <= 24 * 1024) ? 1 : 0;
   p.gu_act_bytes = p.gu_act_smem ? (int)align_up(gu_act, 16) : 0;
-  const size_t dn_act = (g.down_type == MOE_BF16) ? 4 * RT * g.I : RT * g.I + 8 * RT * (g.I / 32);
-  p.dn_act_smem = ((p.maxnt == 1 && g.down_type != MOE_BF16) || dn_act <= 24 * 1024) ? 1 : 0;
+  const size_t dn_act = is_float_w(g.down_type) ? 4 * RT * g.I : RT * g.I + 8 * RT * (g.I / 32);
+  p.dn_act_smem = ((p.maxnt == 1 && !is_float_w(g.down_type)) || dn_act <= 24 * 1024) ? 1 : 0;
   p.dn_act_bytes = p.dn_act_smem ? (int)align_up(dn_act, 16) : 0;
   // ring depths: no deeper than the stages a CTA is expected to have, and
   // small enough at low token counts for a down CTA to sit beside a gate_up CTA
@@ -792,7 +792,7 @@ int moe_quantize_q8_1(const float* x, int64_t n, void* out_blocks, void* stream)
 int moe_debug_block_dots(int32_t type, const void* rows, int32_t nrows, int32_t k, const void* act, int32_t* out,
                          void* stream) {
   if (!rows || !act || !out || nrows < 0 || k <= 0) return MOE_EINVAL;
-  if (type <= MOE_BF16 || type > MOE_MXFP4) return MOE_EINVAL;
+  if (type <= MOE_BF16 || type > MOE_MXFP4) return MOE_EINVAL;   // quantized types only
   if (row_bytes_of(type, k) == 0 || !aligned(rows, 16) || !aligned(act, 4) || !aligned(out, 4)) return MOE_EINVAL;
   cudaError_t e = launch_block_dots(type, static_cast<const uint8_t*>(rows), nrows, k,
                                     static_cast<const uint8_t*>(act), out, static_cast<cudaStream_t>(stream));
@@ -903,8 +903,8 @@ int moe_linear(int32_t type, const void* rows, int32_t N, int32_t K, const float
                int32_t T, void* out, uint32_t* dev_err, void* stream) {
   if (T == 0) return MOE_OK;
   if (!rows || !x || !out || N < 1 || K < 32 || T < 0) return MOE_EINVAL;
-  if (type < MOE_BF16 || type > MOE_MXFP4) return MOE_EINVAL;
-  if (type == MOE_BF16) return MOE_EUNSUPPORTED;
+  if (type < MOE_BF16 || type > MOE_F32) return MOE_EINVAL;
+  if (is_float_w(type)) return MOE_EUNSUPPORTED;
   if (T > MOE_LINEAR_MAX_T) return MOE_EUNSUPPORTED;
   const int rb = row_bytes_of(type, K);
   if (rb == 0) return MOE_EINVAL;
@@ -954,13 +954,13 @@ int moe_debug_decode_stages(const moe_bank* b, const void* x, int32_t T, const i
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaSuccess;
   const int64_t RT = (int64_t)T * g.top_k;
-  if (x_blocks && g.gate_up_type != MOE_BF16)
+  if (x_blocks && !is_float_w(g.gate_up_type))
     e = launch_export_q8(reinterpret_cast<int8_t*>(base + L.xq), reinterpret_cast<float*>(base + L.xd),
                          reinterpret_cast<uint16_t*>(base + L.xsh), (int64_t)T * (g.H / 32),
                          static_cast<uint8_t*>(x_blocks), s);
   if (e == cudaSuccess && inter)
     e = cudaMemcpyAsync(inter, base + L.inter, 4 * (size_t)RT * g.I, cudaMemcpyDeviceToDevice, s);
-  if (e == cudaSuccess && inter_blocks && g.down_type != MOE_BF16)
+  if (e == cudaSuccess && inter_blocks && !is_float_w(g.down_type))
     e = launch_export_q8(reinterpret_cast<int8_t*>(base + L.iq), reinterpret_cast<float*>(base + L.id),
                          reinterpret_cast<uint16_t*>(base + L.ish), RT * (g.I / 32),
                          static_cast<uint8_t*>(inter_blocks), s);

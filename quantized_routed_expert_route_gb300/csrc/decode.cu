@@ -94,7 +94,7 @@ size_t down_smem_bytes(const DecodeParams& p) {
 }
 
 cudaError_t launch_prep(const DecodeParams& p, cudaStream_t stream) {
-  const int quantize_x = (p.gu_type != W_BF16) ? 1 : 0;
+  const int quantize_x = is_float_w(p.gu_type) ? 0 : 1;
   const int work = quantize_x ? (p.T * (p.H / 32) + kThreads - 1) / kThreads : 1;
   const int cntb = (p.cnt_len + kThreads - 1) / kThreads;
   int grid = work > cntb ? work : cntb;
@@ -121,7 +121,8 @@ cudaError_t launch_gate_up(const DecodeParams& p, cudaStream_t stream) {
     case W_Q4_K: return launch_gu_w<W_Q4_K>(p, smem, stream);
     case W_Q8_0: return launch_gu_w<W_Q8_0>(p, smem, stream);
     case W_Q6_K: case W_Q4_0: case W_Q4_1: return launch_gate_up_types_b(p, smem, stream);
-    case W_Q5_0: case W_Q5_1: case W_Q5_K: case W_MXFP4: return launch_gate_up_types_c(p, smem, stream);
+    case W_Q5_0: case W_Q5_1: case W_Q5_K: case W_MXFP4: case W_F16: case W_F32:
+      return launch_gate_up_types_c(p, smem, stream);
     default: return launch_gu_w<W_BF16>(p, smem, stream);
   }
 }
@@ -135,7 +136,8 @@ cudaError_t launch_down(const DecodeParams& p, cudaStream_t stream) {
     case W_Q4_K: return launch_dn_w<W_Q4_K, 8>(p, smem, stream);
     case W_Q8_0: return launch_dn_w<W_Q8_0, 8>(p, smem, stream);
     case W_Q6_K: case W_Q4_0: case W_Q4_1: return launch_down_types_b(p, smem, stream);
-    case W_Q5_0: case W_Q5_1: case W_Q5_K: case W_MXFP4: return launch_down_types_c(p, smem, stream);
+    case W_Q5_0: case W_Q5_1: case W_Q5_K: case W_MXFP4: case W_F16: case W_F32:
+      return launch_down_types_c(p, smem, stream);
     default: return launch_dn_w<W_BF16, 16>(p, smem, stream);
   }
 }

@@ -652,7 +652,7 @@ __device__ __forceinline__ void accum_q_block(const uint8_t* row, int k, int b, 
       if (NTT == 1 || t < nt) acc[t] += (a[t].d * sc * 0.5f) * (float)int_dot8(wq, a[t].q);
     }
   } else {  // W_Q8_0
-    static_assert(WT == W_Q8_0 || WT == W_BF16, "unhandled weight type");  // BF16: unreachable instantiations
+    static_assert(WT == W_Q8_0 || is_float_w(WT), "unhandled weight type");  // float rows: unreachable instantiations
     int wq[8];
     float d;
     q8_0_decode(row, b, wq, d);
@@ -673,11 +673,11 @@ __device__ __forceinline__ void gu_item(const uint8_t* grow, const uint8_t* urow
   float accg[NTT], accu[NTT];
 #pragma unroll
   for (int t = 0; t < NTT; ++t) accg[t] = accu[t] = 0.f;
-  if constexpr (WT == W_BF16) {
+  if constexpr (is_float_w(WT)) {
     for (int c = b0 + lane; c < b1; c += 32) {
       float wg[8], wu[8];
-      bf16x8_to_f32(lds128(grow + 16 * c), wg);
-      bf16x8_to_f32(lds128(urow + 16 * c), wu);
+      float_row_chunk8<WT>(grow, c, wg);
+      float_row_chunk8<WT>(urow, c, wu);
 #pragma unroll
       for (int t = 0; t < NTT; ++t) {
         if (NTT == 1 || t < nt) {
@@ -912,10 +912,10 @@ __device__ __forceinline__ void dn_item(const uint8_t* rowp, bool vrow, int I, i
 #pragma unroll
   for (int t = 0; t < NTT; ++t) acc[t] = 0.f;
   if (vrow) {
-    if constexpr (WT == W_BF16) {
+    if constexpr (is_float_w(WT)) {
       for (int c = sl; c < I / 8; c += LPR) {
         float wv[8];
-        bf16x8_to_f32(lds128(rowp + 16 * c), wv);
+        float_row_chunk8<WT>(rowp, c, wv);
 #pragma unroll
         for (int t = 0; t < NTT; ++t) {
           if (NTT == 1 || t < nt) {

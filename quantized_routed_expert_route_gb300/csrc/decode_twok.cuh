@@ -108,7 +108,7 @@ __global__ void __launch_bounds__(kDecodeThreads, MAXNT == 1 ? 2 : 1) k_gate_up(
   ActSrc act;
   act.n = p.H;
   act.xb = p.x;
-  if (WT == W_BF16) {
+  if (is_float_w(WT)) {
     if (p.gu_act_smem) {
       copy_to_smem(actm, p.x, 2 * (size_t)p.T * p.H);
       act.xb = reinterpret_cast<const uint16_t*>(actm);
@@ -132,8 +132,8 @@ __global__ void __launch_bounds__(kDecodeThreads, MAXNT == 1 ? 2 : 1) k_gate_up(
   }
   consumer_sync();
 
-  const bool requant = !kFused && (p.dn_type != W_BF16);
-  const int nb = (WT == W_BF16) ? p.H / 8 : p.H / 32;   // blocks (8 values for BF16, 32 otherwise)
+  const bool requant = !kFused && (!is_float_w(p.dn_type));
+  const int nb = (is_float_w(WT)) ? p.H / 8 : p.H / 32;   // blocks (8 values for BF16, 32 otherwise)
   const int max_ks = max(1, nb / 32);
   const int cw = warp;                                  // consumer warp 0..7
   const size_t rbg = (size_t)p.rb_gu;
@@ -164,7 +164,7 @@ __global__ void __launch_bounds__(kDecodeThreads, MAXNT == 1 ? 2 : 1) k_gate_up(
       g.misc[6] = 1;
       break;
     }
-    if (kFused && WT != W_BF16 && ks_n == 1) {
+    if (kFused && !is_float_w(WT) && ks_n == 1) {
       // one or two tokens: activations are shared-memory q8_1 planes; each
       // warp takes whole pairs, routes of the expert one after another
       const int8_t* aqs = reinterpret_cast<const int8_t*>(actm);
@@ -399,7 +399,7 @@ __global__ void __launch_bounds__(kDecodeThreads, MAXNT == 1 ? 2 : 1) k_down(con
   ActSrc act;
   act.n = p.I;
   act.xf = p.inter;
-  if (WT == W_BF16) {
+  if (is_float_w(WT)) {
     if (p.dn_act_smem) {
       copy_to_smem(actm, p.inter, 4 * (size_t)RT * p.I);
       act.xf = reinterpret_cast<const float*>(actm);
@@ -447,7 +447,7 @@ __global__ void __launch_bounds__(kDecodeThreads, MAXNT == 1 ? 2 : 1) k_down(con
       const int e = g.slot_e[u];
       const uint8_t* src = p.dn_bank + ((size_t)e * p.H + j0 + st.js) * rbd;
       const uint8_t* piece = sbuf + (size_t)i * p.dn_piece_bytes + (src - align16_down(src));
-      if (kFused && WT != W_BF16) {
+      if (kFused && !is_float_w(WT)) {
         // one or two tokens: the requantized intermediate is in shared memory
         const int8_t* aqs = reinterpret_cast<const int8_t*>(actm);
         const float* ads = reinterpret_cast<const float*>(actm + (size_t)RT * p.I);

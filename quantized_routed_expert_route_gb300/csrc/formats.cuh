@@ -42,8 +42,10 @@ namespace qre {
 
 enum WType : int {
   W_BF16 = 0, W_Q8_0 = 1, W_Q4_K = 2, W_NVFP4 = 3, W_Q6_K = 4, W_Q4_0 = 5,
-  W_Q4_1 = 6, W_Q5_0 = 7, W_Q5_1 = 8, W_Q5_K = 9, W_MXFP4 = 10
+  W_Q4_1 = 6, W_Q5_0 = 7, W_Q5_1 = 8, W_Q5_K = 9, W_MXFP4 = 10, W_F16 = 11, W_F32 = 12
 };
+// Float rows (BF16, F16, F32): the activations reach them unquantized.
+__host__ __device__ constexpr bool is_float_w(int t) { return t == W_BF16 || t == W_F16 || t == W_F32; }
 // Kernel-side variant of W_NVFP4 whose rows (9k/16 bytes) are not 16-byte aligned.
 constexpr int W_NVFP4_U = 16;
 
@@ -60,6 +62,8 @@ __host__ __device__ inline int row_bytes_of(int t, int k) {
     case W_Q5_1: return (k % 32 == 0) ? (k / 32) * 24 : 0;
     case W_Q5_K: return (k % 256 == 0) ? (k / 256) * 176 : 0;
     case W_MXFP4: return (k % 32 == 0) ? (k / 32) * 17 : 0;
+    case W_F16: return (k % 32 == 0) ? 2 * k : 0;
+    case W_F32: return (k % 32 == 0) ? 4 * k : 0;
   }
   return 0;
 }
@@ -507,6 +511,28 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4 v, float (&f)[8]) {
   f[2] = __uint_as_float(v.y << 16); f[3] = __uint_as_float(v.y & 0xFFFF0000u);
   f[4] = __uint_as_float(v.z << 16); f[5] = __uint_as_float(v.z & 0xFFFF0000u);
   f[6] = __uint_as_float(v.w << 16); f[7] = __uint_as_float(v.w & 0xFFFF0000u);
+}
+
+// Values 8c .. 8c+7 of a float row in shared memory as fp32 (exact): BF16 and
+// F16 rows hold 8 values in 16 bytes, F32 rows in 32.
+template <int WT>
+__device__ __forceinline__ void float_row_chunk8(const uint8_t* row, int c, float (&f)[8]) {
+  if constexpr (WT == W_F32) {
+    const float4 a = *reinterpret_cast<const float4*>(row + 32 * c);
+    const float4 b = *reinterpret_cast<const float4*>(row + 32 * c + 16);
+    f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+    f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+  } else if constexpr (WT == W_F16) {
+    const uint4 v = *reinterpret_cast<const uint4*>(row + 16 * c);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      f[2 * i] = f16_bits_to_f32(w[i] & 0xFFFFu);
+      f[2 * i + 1] = f16_bits_to_f32(w[i] >> 16);
+    }
+  } else {
+    bf16x8_to_f32(*reinterpret_cast<const uint4*>(row + 16 * c), f);
+  }
 }
 
 }  // namespace qre

@@ -284,7 +284,7 @@ __global__ void __launch_bounds__(kLsThreads, 1) k_layer_small(const __grid_cons
   int8_t* xq = reinterpret_cast<int8_t*>(xact);
   float* xd = reinterpret_cast<float*>(xact + (size_t)p.T * p.H);
   int* xs = reinterpret_cast<int*>(xd + (size_t)p.T * nbh);
-  if constexpr (WG == W_BF16) {
+  if constexpr (is_float_w(WG)) {
     copy_to_smem<kLsConsumers>(xact, p.x, 2 * (size_t)p.T * p.H);
   } else {
     ls_quantize<true>(p.x, p.T * nbh, nullptr, nbh, xq, xd, xs, blockIdx.x == 0, p.xq, p.xd, p.xsum, p.xsh);
@@ -318,13 +318,13 @@ __global__ void __launch_bounds__(kLsThreads, 1) k_layer_small(const __grid_cons
       for (int ri = 0; ri < Tu; ++ri) {
         const int t = g.rtok[roff + ri];
         float2 h;
-        if constexpr (WG == W_BF16) {
+        if constexpr (is_float_w(WG)) {
           ActSrc act;
           act.xb = reinterpret_cast<const uint16_t*>(xact);
           act.n = p.H;
           int tok[NT] = {t, 0, 0, 0};
           float ag[NT], au[NT];
-          gu_item<W_BF16, 1>(grow, urow, p.H, 0, p.H / 8, lane, act, tok, 1, ag, au);
+          gu_item<WG, 1>(grow, urow, p.H, 0, p.H / 8, lane, act, tok, 1, ag, au);
           h = make_float2(ag[0], au[0]);
         } else {
           h = gu_pair_q8<WG>(grow, urow, p.H, lane, xq + (size_t)t * p.H, xd + t * nbh, xs + t * nbh);
@@ -355,7 +355,7 @@ __global__ void __launch_bounds__(kLsThreads, 1) k_layer_small(const __grid_cons
   ActSrc dact;
   dact.n = p.I;
   dact.xf = p.inter;
-  if constexpr (WD == W_BF16) {
+  if constexpr (is_float_w(WD)) {
     if (p.dn_act_smem) {
       copy_to_smem<kLsConsumers>(iact, p.inter, 4 * (size_t)RT * p.I);
       dact.xf = reinterpret_cast<const float*>(iact);
@@ -392,10 +392,10 @@ __global__ void __launch_bounds__(kLsThreads, 1) k_layer_small(const __grid_cons
         for (int ri = 0; ri < Tu; ++ri) {
           const int r = g.routes[roff + ri];
           float v;
-          if constexpr (WD == W_BF16) {
+          if constexpr (is_float_w(WD)) {
             int rt[NT] = {r, 0, 0, 0};
             float res[NT];
-            dn_item<W_BF16, LPR, 1>(rowp, vrow, p.I, sl, dact, rt, 1, res);
+            dn_item<WD, LPR, 1>(rowp, vrow, p.I, sl, dact, rt, 1, res);
             v = res[0];
           } else {
             v = dn_row_q8<WD, LPR>(rowp, vrow, p.I, sl, iq + (size_t)r * p.I, idd + r * nbi, is + r * nbi);
@@ -503,6 +503,8 @@ static cudaError_t dispatch_ls(const DecodeParams& p, cudaStream_t stream, bool 
     case W_Q5_1: return launch_ls_t<W_Q5_1, W_Q5_1, 8>(p, stream, probe_only, fits);
     case W_Q5_K: return launch_ls_t<W_Q5_K, W_Q5_K, 4>(p, stream, probe_only, fits);
     case W_MXFP4: return launch_ls_t<W_MXFP4, W_MXFP4, 8>(p, stream, probe_only, fits);
+    case W_F16: return launch_ls_t<W_F16, W_F16, 16>(p, stream, probe_only, fits);
+    case W_F32: return launch_ls_t<W_F32, W_F32, 16>(p, stream, probe_only, fits);
     default: return launch_ls_t<W_BF16, W_BF16, 16>(p, stream, probe_only, fits);
   }
 }

@@ -37,13 +37,11 @@ def test_every_declared_symbol_is_exported(capi):
 
 
 def test_row_bytes_agree_with_the_oracle(capi):
-    built = [t for t in sorted(F.TYPE_NAMES) if t not in (F.TYPE_F16, F.TYPE_F32)]
-    for t in built:
+    for t in sorted(F.TYPE_NAMES):
         for k in (32, 96, 256, 768, 2048, 4096, 100):
             assert capi.moe_row_bytes(t, k) == F.row_bytes(t, k), (t, k)
-    # F16 / F32 rows exist in the oracle only so far; 16 is a kernel-side variant, not a type
-    for t in (F.TYPE_F16, F.TYPE_F32, 16):
-        assert capi.moe_row_bytes(t, 256) == 0
+    # 16 is a kernel-side variant of NVFP4, not a type
+    assert capi.moe_row_bytes(16, 256) == 0
 
 
 def test_host_argument_checks(capi):
@@ -80,7 +78,8 @@ def test_host_argument_checks_of_the_newer_entry_points(capi):
     assert lib.moe_linear(capi.MOE_NVFP4, buf, 4, 256, None, buf, capi.MOE_LINEAR_MAX_T + 1, buf, None,
                           None) == capi.MOE_EUNSUPPORTED
     assert lib.moe_linear(capi.MOE_Q4_K, buf, 4, 96, None, buf, 1, buf, None, None) == capi.MOE_EINVAL
-    assert lib.moe_linear(11, buf, 4, 256, None, buf, 1, buf, None, None) == capi.MOE_EINVAL
+    assert lib.moe_linear(capi.MOE_F16, buf, 4, 256, None, buf, 1, buf, None, None) == capi.MOE_EUNSUPPORTED
+    assert lib.moe_linear(13, buf, 4, 256, None, buf, 1, buf, None, None) == capi.MOE_EINVAL
     assert lib.moe_linear(capi.MOE_NVFP4, ctypes.addressof(buf) + 1, 4, 256, None, buf, 1, buf, None,
                           None) == capi.MOE_EINVAL
     # geometry: an unknown GLU or type is refused

@@ -94,7 +94,7 @@ def _check_case(case, tokens=None, check_stages=True):
     figs = tol.check_output(res["out"][sel], ref, beta)
     g = case.geom
     if check_stages and "inter" in res:
-        if g.gate_up_type != F.TYPE_BF16:
+        if g.gate_up_type not in F.FLOAT_TYPES:
             for i, t in enumerate(sel):
                 xi = st["x_act"][i]
                 want = F.q8_1_pack_blocks(xi["qs"], xi["d"], xi["s"]).reshape(-1)
@@ -105,7 +105,7 @@ def _check_case(case, tokens=None, check_stages=True):
                     continue
                 ginter = res["inter"][t, k].astype(np.float64)
                 assert (np.abs(ginter - st["inter"][i, k]) <= inter_err[i, k]).all(), (t, k)
-                if g.down_type != F.TYPE_BF16:
+                if g.down_type not in F.FLOAT_TYPES:
                     blk = res["inter_blocks"][t, k]
                     gq = blk[:, 4:].view(np.int8).astype(np.int64).reshape(-1)
                     oq = st["inter_act"][i][k]["qs"].astype(np.int64).reshape(-1)
@@ -164,7 +164,10 @@ def test_laguna_zipf_batches_sampled(T):
                                        (F.TYPE_Q4_0, F.TYPE_Q6_K), (F.TYPE_BF16, F.TYPE_Q6_K),
                                        (F.TYPE_Q6_K, F.TYPE_NVFP4), (F.TYPE_Q4_0, F.TYPE_Q8_0),
                                        (F.TYPE_Q5_K, F.TYPE_Q4_1), (F.TYPE_Q5_0, F.TYPE_MXFP4),
-                                       (F.TYPE_MXFP4, F.TYPE_Q5_1), (F.TYPE_Q4_1, F.TYPE_Q5_K)])
+                                       (F.TYPE_MXFP4, F.TYPE_Q5_1), (F.TYPE_Q4_1, F.TYPE_Q5_K),
+                                       (F.TYPE_F16, F.TYPE_Q4_K), (F.TYPE_Q8_0, F.TYPE_F32),
+                                       (F.TYPE_F32, F.TYPE_NVFP4), (F.TYPE_Q6_K, F.TYPE_F16),
+                                       (F.TYPE_BF16, F.TYPE_F32), (F.TYPE_F16, F.TYPE_F32)])
 def test_mixed_type_pairs(gu_t, dn_t):
     """Gate_up and down of different types: the two-kernel path."""
     case = cases.make_case(512, 256, 16, 4, gu_t, dn_t, 5, seed=40 + 8 * gu_t + dn_t)
@@ -220,6 +223,20 @@ def test_more_gguf_types_fused_layer(wtype):
     case = cases.make_case(2048, 768, 128, 8, wtype, wtype, 1, seed=140 + wtype)
     figs = _check_case(case)
     assert figs["launches"] == 1
+    assert figs["err_bits"] == 0
+
+
+@pytest.mark.parametrize("T", [1, 3])
+@pytest.mark.parametrize("wtype", [F.TYPE_F16, F.TYPE_F32])
+def test_float_row_layer(wtype, T):
+    """H=2048 I=768 E=32 top-8 with F16 or F32 gate_up and down rows (float
+    types of FreeToken PR #704's synthetic list, "Validation"): x reaches the
+    rows as its bf16 values, the intermediate as fp32; T=1 is one fused
+    launch."""
+    case = cases.make_case(2048, 768, 32, 8, wtype, wtype, T, seed=150 + wtype + T)
+    figs = _check_case(case)
+    if T == 1:
+        assert figs["launches"] == 1
     assert figs["err_bits"] == 0
 
 
