@@ -28,6 +28,7 @@ from __future__ import annotations
 import argparse
 import json
 import os
+import platform
 import subprocess
 import sys
 import threading
@@ -69,54 +70,104 @@ def bf16_peak():
 # ------------------------------------------------------------------ clocks
 
 class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+    """SM clock and throttle reasons sampled during the timed region: NVML read
+    through ctypes about every millisecond (the GPU found by its UUID, so the
+    right one of a shared machine's GPUs), else nvidia-smi every 20 ms.  Read
+    only; no setting is changed."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    # NVML clock-event reason bits
+    REASONS = {"sw_power_cap": 0x4, "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20, "hw_thermal_slowdown": 0x40}
 
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
-        self.rows = []
+        self.rows = []          # (sm_mhz, max_mhz, reason names)
         self.proc = None
+        self.stop = threading.Event()
+        self.thread = None
+        self.source = None
+
+    def _nvml_handle(self):
+        import ctypes
+        nv = ctypes.CDLL("libnvidia-ml.so.1")
+        if nv.nvmlInit_v2() != 0:
+            return None, None
+        h = ctypes.c_void_p()
+        try:
+            import torch
+            uuid = str(torch.cuda.get_device_properties(self.gpu).uuid)
+            key = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+            if nv.nvmlDeviceGetHandleByUUID(key.encode(), ctypes.byref(h)) == 0:
+                return nv, h
+        except Exception:
+            pass
+        return None, None
+
+    def _nvml_loop(self, nv, h):
+        import ctypes
+        sm, mx, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx))
+        try:
+            get_reasons = nv.nvmlDeviceGetCurrentClocksEventReasons
+        except AttributeError:
+            get_reasons = nv.nvmlDeviceGetCurrentClocksThrottleReasons
+        while not self.stop.is_set():
+            if nv.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(sm)) == 0:
+                names = []
+                if get_reasons(h, ctypes.byref(rs)) == 0:
+                    names = [n for n, b in self.REASONS.items() if rs.value & b]
+                self.rows.append((float(sm.value), float(mx.value), names))
+            time.sleep(0.001)
 
     def __enter__(self):
+        try:
+            nv, h = self._nvml_handle()
+        except OSError:
+            nv, h = None, None
+        if nv is not None:
+            self.source = "nvml, ~1 ms"
+            self.thread = threading.Thread(target=self._nvml_loop, args=(nv, h), daemon=True)
+            self.thread.start()
+            return self
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
                  "-lms", "20"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.source = "nvidia-smi, 20 ms"
+            self.thread = threading.Thread(target=self._read_smi, daemon=True)
             self.thread.start()
         except FileNotFoundError:
             self.proc = None
         return self
 
-    def _read(self):
+    def _read_smi(self):
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in self.proc.stdout:
-            self.rows.append([c.strip() for c in line.split(",")])
+            r = [c.strip() for c in line.split(",")]
+            if len(r) > 8 and r[1].replace(".", "").isdigit() and r[2].replace(".", "").isdigit():
+                self.rows.append((float(r[1]), float(r[2]),
+                                  [n for n, v in zip(names, r[5:9]) if v.lower() == "active"]))
 
     def __exit__(self, *a):
+        self.stop.set()
         if self.proc:
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=5)
 
     def summary(self):
         if not self.rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
-        sm = [float(r[1]) for r in self.rows if len(r) > 8 and r[1].replace(".", "").isdigit()]
-        mx = [float(r[2]) for r in self.rows if len(r) > 8 and r[2].replace(".", "").isdigit()]
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = set()
-        for r in self.rows:
-            if len(r) > 8:
-                for n, v in zip(names, r[5:9]):
-                    if v.strip().lower() == "active":
-                        reasons.add(n)
-        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": sorted(reasons), "samples": len(self.rows)}
+        sm = [r[0] for r in self.rows]
+        reasons = sorted({n for r in self.rows for n in r[2]})
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": max(r[1] for r in self.rows),
+                "reasons": reasons, "samples": len(self.rows), "source": self.source}
 
 
 # ------------------------------------------------------------------ stacks of layers on the device
@@ -487,47 +538,134 @@ def bench_cache(dev, tokens, hbm_peak):
 
 # ------------------------------------------------------------------ CPU oracle timing
 
-def cpu_oracle_worker(seconds: float, seed: int = 0) -> dict:
-    """Time the oracle on tokens of the headline workload (one NVFP4 layer,
-    T=1, top-8, the same counter-based bank bytes the GPU bench uses) until
-    `seconds` have elapsed; only the routed experts' rows are generated, and
-    generating them is outside the timed part."""
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo)."""
+    try:
+        out = subprocess.run(["lscpu"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return platform.processor() or platform.machine()
+
+
+_ORACLE_ROWS = {}
+
+
+def _oracle_task(arg):
+    """One pool task: `ntok` tokens of the headline layer through the oracle,
+    in a process of its own (one BLAS thread); the routed experts' rows of the
+    process's fixed routing are generated once per process, outside the
+    timing.  Returns (tokens, oracle seconds)."""
+    seed, ntok = arg
     from oracle import layer as OL
     from synth import banks as S
     from synth import counter as C
     c = CFG1
     geom = OL.Geometry(c["H"], c["I"], c["E"], c["K"], c["gu"], c["dn"])
-    sb = S.counter_scale_bank(seed * 1000, c["E"], c["gu"], c["dn"])
-    done, spent, t = 0, 0.0, 0
-    while spent < seconds and done < 64:
-        ids, w = S.softmax_topk_routing(seed * 7 + t, 1, c["E"], c["K"])
-        x = S.hidden_bf16(seed + t, 1, c["H"])
+    if seed not in _ORACLE_ROWS:
+        ids, w = S.softmax_topk_routing(seed * 7, 1, c["E"], c["K"])
         gu, dn = {}, {}
         for e in (int(v) for v in ids.reshape(-1)):
             gu[e] = C.bank_bytes_np(seed * 1000, c["gu"], c["H"], e * 2 * c["I"], 2 * c["I"])
             dn[e] = C.bank_bytes_np(seed * 1000 + 1, c["dn"], c["I"], e * c["H"], c["H"])
+        _ORACLE_ROWS[seed] = (ids, w, gu, dn, S.counter_scale_bank(seed * 1000, c["E"], c["gu"], c["dn"]), 0)
+    ids, w, gu, dn, sb, n = _ORACLE_ROWS[seed]
+    spent = 0.0
+    for i in range(ntok):
+        x = S.hidden_bf16(seed * 131 + n + i, 1, c["H"])
         t0 = time.perf_counter()
         OL.moe_layer(geom, gu, dn, sb, x, ids, w)
         spent += time.perf_counter() - t0
-        done += 1
-        t += 1
-    return {"value": done / spent, "unit": "layer-tok/s", "cores": 1, "kind": "oracle",
-            "sample": f"{done} tokens x 1 NVFP4 layer (H=2048, I=768, E=128, top-8), numpy fp64, "
-                      f"1 BLAS thread, {spent:.1f} s of oracle time"}
+    _ORACLE_ROWS[seed] = (ids, w, gu, dn, sb, n + ntok)
+    return ntok, spent
 
 
-def run_cpu_baseline(seconds: float) -> dict:
-    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
-               CUDA_VISIBLE_DEVICES="")
-    res = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-oracle-worker", str(seconds)],
-                         stdout=subprocess.PIPE, stderr=subprocess.PIPE, text=True, env=env, cwd=ROOT)
-    if res.returncode != 0:
-        return {"value": None, "unit": "layer-tok/s", "cores": 1, "kind": "oracle",
-                "sample": "failed: " + res.stderr.strip()[-300:]}
-    return json.loads(res.stdout.strip().splitlines()[-1])
+class OraclePool:
+    """A spawn pool of oracle processes, one per host core, each with one BLAS
+    thread and no GPU (started before any CUDA call of this process)."""
+
+    def __init__(self, n: int):
+        import multiprocessing as mp
+        for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+            os.environ[k] = "1"
+        saved = os.environ.get("CUDA_VISIBLE_DEVICES")
+        os.environ["CUDA_VISIBLE_DEVICES"] = ""
+        self.n = n
+        self.pool = mp.get_context("spawn").Pool(n)
+        if saved is None:
+            del os.environ["CUDA_VISIBLE_DEVICES"]
+        else:
+            os.environ["CUDA_VISIBLE_DEVICES"] = saved
+
+    def rate(self, ntok: int, seed0: int, procs: int | None = None) -> tuple[float, int]:
+        """Summed throughput (tokens / oracle second, over the processes) of
+        `ntok` tokens in each of `procs` processes at once."""
+        k = self.n if procs is None else procs
+        res = self.pool.map(_oracle_task, [(seed0 + i, ntok) for i in range(k)], chunksize=1)
+        return sum(t / s for t, s in res), sum(t for t, _ in res)
+
+    def close(self):
+        self.pool.terminate()
+        self.pool.join()
+
+
+def run_cpu_baseline(pool: "OraclePool", seconds: float) -> dict:
+    """The oracle on the host cores: one process alone, then every process at
+    once (one per core, tokens split across them, throughput summed), each
+    for about `seconds` of oracle time."""
+    try:
+        pool.rate(1, 0, procs=pool.n)                        # rows generated, imports warm
+        one, t1 = pool.rate(max(1, int(seconds * 1.5)), 0, procs=1)
+        many, tn = pool.rate(max(1, int(seconds * 1.5)), 0)
+    except Exception as e:   # noqa: BLE001 (reported in the line, the bench goes on)
+        return {"value": None, "unit": "layer-tok/s", "cores": 1, "kind": "oracle", "sample": f"failed: {e}"}
+    return {"value": many, "unit": "layer-tok/s", "cores": pool.n, "kind": "oracle", "cpu_model": cpu_model(),
+            "sample": f"{pool.n} oracle processes at once (one per core, one BLAS thread each), {tn} tokens of one "
+                      f"NVFP4 layer (H=2048, I=768, E=128, top-8) in all, numpy fp64; throughput summed over the "
+                      f"processes",
+            "single_core": {"value": one, "cores": 1, "sample": f"{t1} tokens in one process"}}
 
 
 # ------------------------------------------------------------------ profiling driver
+
+def summary_of(line: dict) -> dict:
+    """A compact digest of the line (rounded): the headline, the Laguna stack
+    sweep, the other-type layers, the prompt chunk, the dense linear, the
+    expert cache and the CPU baseline."""
+    ex = line.get("extra", {})
+    r3 = lambda v: None if v is None else float(f"{v:.3g}")   # noqa: E731
+    s = {"layer_us_T1": r3(ex.get("per_layer_us")), "hbm_frac_T1": r3(line["roofline"]["frac"]),
+         "layer_us_T8": r3(ex.get("t8", {}).get("per_layer_us"))}
+    if "laguna_47_layer_stack" in ex:
+        s["laguna_stack"] = {k: {"tok_s": r3(v["stack_tok_per_s"]), "hbm_frac": r3(v["frac"])}
+                             for k, v in ex["laguna_47_layer_stack"].items()}
+    if "gguf_types_24_layer_stack" in ex:
+        s["types_layer_us_T1_T8"] = {k: [r3(v["T=1"]["per_layer_us"]), r3(v["T=8"]["per_layer_us"])]
+                                     for k, v in ex["gguf_types_24_layer_stack"].items() if k != "workload"}
+    if "prefill_4096_token_chunk" in ex:
+        pf = ex["prefill_4096_token_chunk"]
+        s["prefill_chunk_ms"] = {m: r3(pf[m]["ms_per_chunk"]) for m in ("w4a4", "w4a8", "fp16") if m in pf}
+        s["prefill_tflops"] = {m: r3(pf[m]["tflops"]) for m in ("w4a4", "w4a8", "fp16") if m in pf}
+        if "w4a4" in pf:
+            s["prefill_w4a4_frac_nominal_fp4"] = r3(pf["w4a4"].get("frac_of_nominal_fp4_peak"))
+    if "dense_linear_nvfp4" in ex:
+        dl = ex["dense_linear_nvfp4"]
+        s["linear_one_launch_hbm_frac"] = {k: r3(dl[k]["one_launch"]["frac"]) for k in ("T=1", "T=8") if k in dl}
+    if "expert_cache" in ex:
+        s["cache_tok_s"] = r3(ex["expert_cache"].get("tok_per_s"))
+    cpu = line.get("cpu_baseline") or {}
+    s["cpu_oracle"] = {"value": r3(cpu.get("value")), "cores": cpu.get("cores"),
+                       "single_core": r3((cpu.get("single_core") or {}).get("value"))}
+    return s
+
 
 def profile_layer(a):
     """Eager decode passes of one layer for a profiler: the NVFP4 layer
@@ -618,7 +756,6 @@ def main():
     ap.add_argument("--profile-linear", action="store_true",
                     help="run --steps one-launch dense NVFP4 linears (245,760 x 2048, T=--T) for ncu")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
-    ap.add_argument("--cpu-oracle-worker", type=float, default=None, help=argparse.SUPPRESS)
     ap.add_argument("--profile-layer", choices=["nvfp4", "q4_k", "bf16", "q4_k_m", "q6_k", "q4_0"], default=None,
                     help="run --steps eager decode passes of one layer type (for ncu), print nothing else")
     ap.add_argument("--T", type=int, default=1)
@@ -640,9 +777,6 @@ def main():
     if a.profile_linear:
         profile_linear(a)
         return
-    if a.cpu_oracle_worker is not None:
-        print(json.dumps(cpu_oracle_worker(a.cpu_oracle_worker)))
-        return
 
     workload = (f"qwen3-30b-a3b-shaped nvfp4 routed-expert decode layer (H=2048, I=768, E=128, top-8, T=1), "
                 f"{a.layers} distinct resident layer banks per step")
@@ -658,20 +792,28 @@ def main():
         rank = int(os.environ.get("RANK", "0"))
         if rank != 0:
             return
+        pool = OraclePool(os.cpu_count() or 1)
+        pool.rate(1, 1000, procs=pool.n)   # rows generated, imports warm (outside the steps)
         vals = []
         for i in range(a.warmup + a.steps):
-            r = cpu_oracle_worker(max(1.0, a.cpu_seconds / max(1, a.steps)), seed=i)
+            v, _ = pool.rate(1, 1000)
             if i >= a.warmup:
-                vals.append(r["value"])
+                vals.append(v)
+        pool.close()
         v = float(np.mean(vals))
         print(json.dumps({
             "impl": "reference", "metric": metric, "value": v, "unit": "layer-tok/s",
             "n_gpus": a.gpus, "steps": a.steps, "warmup": a.warmup, "higher_is_better": True,
             "dtype": "f64", "data": "synthetic", "config": config(a.gpus),
-            "cpu_baseline": {"kind": "oracle", "cores": 1, "value": v,
-                             "sample": "per step: tokens of one NVFP4 layer through the numpy oracle"},
+            "cpu_baseline": {"kind": "oracle", "cores": pool.n, "value": v, "cpu_model": cpu_model(),
+                             "sample": f"per step: one token of one NVFP4 layer in each of {pool.n} oracle "
+                                       f"processes at once (one per core); throughput summed"},
             "e2e": {"value": v, "unit": "layer-tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}))
         return
+
+    # the oracle's process pool starts before any CUDA call of this process
+    rank0 = int(os.environ.get("RANK", "0")) == 0
+    pool = OraclePool(os.cpu_count() or 1) if (rank0 and a.cpu_seconds > 0) else None
 
     import torch
     rank, world, local = dist_setup(a.gpus)
@@ -762,7 +904,9 @@ def main():
             "fp16": bench_prefill(dev, max(3, min(20, a.steps // 20)), a.warmup, 2, pk)}
         torch.cuda.empty_cache()
 
-    cpu = run_cpu_baseline(a.cpu_seconds) if (rank == 0 and a.cpu_seconds > 0) else None
+    cpu = run_cpu_baseline(pool, a.cpu_seconds / 2) if pool is not None else None
+    if pool is not None:
+        pool.close()
     if rank == 0:
         line = {
             "metric": metric,
@@ -780,6 +924,7 @@ def main():
             "cpu_baseline": cpu,
             "extra": extra,
         }
+        line["summary"] = summary_of(line)   # last, so a tail of the output keeps it
         print(json.dumps(line))
     if world > 1:
         torch.distributed.barrier()
