@@ -448,6 +448,19 @@ int moe_cache_stats(const moe_cache* cache, int64_t* hits, int64_t* misses, int6
 int moe_debug_tc_gemm(const void* A, const void* B, int32_t K, int32_t N, float* D,
                       int32_t* dev_err, void* stream);
 
+/* Block-scaled FP4 tensor-core check: D[128, N] = sum over k of
+ * (E2M1(A[m][k]) * UE4M3(sA[m][k/16])) * (E2M1(B[n][k]) * UE4M3(sB[n][k/16]))
+ * on the tcgen05 kind::mxf4nvf4 MMA (per-16 UE4M3 scales in tensor memory)
+ * that the W4A4 prompt path runs on (Strata PR #292, "Summary/Pipeline":
+ * W4A4 on FP4 MMA).  A: device, 128 rows of K/2 bytes of E2M1 codes (value
+ * 2i in the low nibble of byte i); B: N rows likewise; sA, sB: 128 / N rows
+ * of K/16 UE4M3 bytes; D: device fp32 [128][N].  K a positive multiple of
+ * 256, N a multiple of 16 in [16, 128], A, B, sA, sB 16-byte aligned.
+ * *dev_err (device int32, caller-zeroed) gets bit 0 if a bounded wait for
+ * the MMA ran out. */
+int moe_debug_fp4_gemm(const void* A, const void* scale_A, const void* B, const void* scale_B, int32_t K,
+                       int32_t N, float* D, int32_t* dev_err, void* stream);
+
 /* Failure-detection check (the auxiliary failure detection of the build, not
  * an operation of the pages): one thread runs one of the kernels' bounded
  * waits on an mbarrier whose phase nothing completes, so the wait runs out

@@ -29,7 +29,7 @@ EXPORTS = (
     "moe_workspace_bytes", "moe_workspace_init", "moe_decode", "moe_get_error",
     "moe_status_string", "moe_last_cuda_error", "moe_quantize_q8_1",
     "moe_debug_block_dots", "moe_debug_decode_stages", "moe_decode_noalloc", "moe_debug_tc_gemm",
-    "moe_debug_wait_timeout",
+    "moe_debug_wait_timeout", "moe_debug_fp4_gemm",
     "moe_prefill_workspace_bytes", "moe_prefill_grouped", "moe_debug_prefill_stages",
     "moe_decode_kernel_count", "moe_decode_io_bytes", "moe_decode_io_offsets", "moe_decode_host",
     "moe_linear", "moe_cache_plan", "moe_slot_table_create", "moe_slot_table_destroy", "moe_slot_table_acquire",
@@ -79,6 +79,7 @@ def _load() -> ctypes.CDLL:
         "moe_decode_noalloc": (ctypes.c_int, [vp, vp, i32, vp, vp, vp, vp]),
         "moe_debug_tc_gemm": (ctypes.c_int, [vp, vp, i32, i32, vp, vp, vp]),
         "moe_debug_wait_timeout": (ctypes.c_int, [i32, i32, vp, vp]),
+        "moe_debug_fp4_gemm": (ctypes.c_int, [vp, vp, vp, vp, i32, i32, vp, vp, vp]),
         "moe_linear": (ctypes.c_int, [i32, vp, i32, i32, vp, vp, i32, vp, vp, vp]),
         "moe_cache_plan": (ctypes.c_int, [i64, i32, vp, vp, vp]),
         "moe_slot_table_create": (ctypes.c_int, [i32, ctypes.POINTER(vp)]),
@@ -279,6 +280,12 @@ def moe_cache_stats(cache: int):
 def moe_debug_wait_timeout(mode: int, limit: int, dev_err: int, stream: int = 0) -> None:
     """A bounded wait that runs out (failure-detection check); see include/qre_moe.h."""
     _check(_lib.moe_debug_wait_timeout(mode, limit, dev_err, stream or None), "moe_debug_wait_timeout")
+
+
+def moe_debug_fp4_gemm(A: int, sA: int, B: int, sB: int, K: int, N: int, D: int, dev_err: int,
+                       stream: int = 0) -> None:
+    """One block-scaled FP4 tensor-core tile (see include/qre_moe.h)."""
+    _check(_lib.moe_debug_fp4_gemm(A, sA, B, sB, K, N, D, dev_err, stream or None), "moe_debug_fp4_gemm")
 
 
 def moe_debug_tc_gemm(A: int, B: int, K: int, N: int, D: int, dev_err: int, stream: int = 0) -> None:

@@ -940,6 +940,19 @@ int moe_debug_wait_timeout(int32_t mode, int32_t limit, uint32_t* dev_err, void*
   return e == cudaSuccess ? MOE_OK : cuda_fail(e, "wait_timeout");
 }
 
+int moe_debug_fp4_gemm(const void* A, const void* scale_A, const void* B, const void* scale_B, int32_t K,
+                       int32_t N, float* D, int32_t* dev_err, void* stream) {
+  if (!A || !scale_A || !B || !scale_B || !D || !dev_err) return MOE_EINVAL;
+  if (K < 256 || K % 256 != 0 || N < 16 || N > 128 || N % 16 != 0) return MOE_EINVAL;
+  if (!aligned(A, 16) || !aligned(B, 16) || !aligned(scale_A, 16) || !aligned(scale_B, 16) || !aligned(D, 4) ||
+      !aligned(dev_err, 4))
+    return MOE_EINVAL;
+  cudaError_t e = launch_fp4_gemm_check(static_cast<const uint8_t*>(A), static_cast<const uint8_t*>(scale_A),
+                                        static_cast<const uint8_t*>(B), static_cast<const uint8_t*>(scale_B), K, N, D,
+                                        dev_err, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MOE_OK : cuda_fail(e, "fp4_gemm");
+}
+
 int moe_debug_decode_stages(const moe_bank* b, const void* x, int32_t T, const int32_t* ids, const float* w,
                             void* out, void* ws, size_t ws_bytes, void* stream, void* x_blocks, float* inter,
                             void* inter_blocks) {

@@ -179,6 +179,8 @@ cudaError_t launch_prefill(const PfParams& p, cudaStream_t stream);
 cudaError_t launch_tc_gemm_check(const uint16_t* A, const uint16_t* B, int K, int N, float* D, int* err,
                                  cudaStream_t stream);
 cudaError_t launch_wait_timeout(int mode, uint32_t limit, uint32_t* err, cudaStream_t stream);
+cudaError_t launch_fp4_gemm_check(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const uint8_t* sB, int K,
+                                  int N, float* D, int* err, cudaStream_t stream);
 cudaError_t launch_export_q8(const int8_t* q, const float* d, const uint16_t* s, int64_t nblocks,
                              uint8_t* out, cudaStream_t stream);
 

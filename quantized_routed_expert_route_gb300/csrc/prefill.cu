@@ -118,6 +118,117 @@ cudaError_t launch_tc_gemm_check(const uint16_t* A, const uint16_t* B, int K, in
   return cudaGetLastError();
 }
 
+// Block-scaled FP4 check: D[128, N] = sum over K of (A * sA) * (B * sB)^T
+// with A [128][K/2] and B [N][K/2] packed E2M1 codes (value 2i in the low
+// nibble of byte i) and sA [128][K/16], sB [N][K/16] UE4M3 scales, on the
+// tcgen05 kind::mxf4nvf4 MMA: each 256-value K chunk's codes go to 128-byte
+// swizzled tiles; for each of its four MMAs (64 values) the scales of the
+// 128 rows go to a 512-byte atom (line r: the four scales of rows r, r+32,
+// r+64, r+96) that tcgen05.cp copies to four tensor-memory columns.  N <= 128,
+// a multiple of 16; rows of B (and their scales) beyond N read as zero.
+// Global loads check their alignment (a misaligned one is skipped and flags
+// bit 1 of *err).
+__global__ void __launch_bounds__(128, 1) k_fp4_gemm_check(const uint8_t* A, const uint8_t* sA, const uint8_t* B,
+                                                           const uint8_t* sB, int K, int N, float* D, int* err) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint64_t bar;
+  __shared__ uint32_t tmem_base;
+  uint8_t* base = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+  uint8_t* sa = base;                 // 128 rows x 128 bytes, swizzled
+  uint8_t* sb = base + 16384;         // 128 rows x 128 bytes, swizzled
+  uint8_t* ssa = base + 32768;        // four 512-byte scale atoms (one per MMA)
+  uint8_t* ssb = base + 32768 + 2048;
+  const int tid = threadIdx.x, warp = tid >> 5;
+  if (warp == 0) {
+    tc::tmem_alloc(&tmem_base, 256);
+    tc::tmem_relinquish();
+  }
+  if (tid == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = tmem_base;
+  const uint32_t t_sfa = tmem + 128, t_sfb = tmem + 144;   // 4 MMAs x 4 columns each
+  const uint32_t idesc = tc::idesc_mxf4nvf4(128, (uint32_t)N);
+  const size_t rb = (size_t)K / 2, sb_row = (size_t)K / 16;
+  uint32_t phase = 0;
+  bool ok = true, misaligned = false;
+  for (int k0 = 0; k0 < K; k0 += 256) {
+    for (int i = tid; i < 128 * 8; i += 128) {
+      const int r = i >> 3, c = i & 7;
+      const uint8_t* pa = A + (size_t)r * rb + k0 / 2 + 16 * c;
+      const uint8_t* pb = B + (size_t)r * rb + k0 / 2 + 16 * c;
+      uint4 va = make_uint4(0, 0, 0, 0), vb = make_uint4(0, 0, 0, 0);
+      if ((reinterpret_cast<uintptr_t>(pa) & 15) == 0) va = *reinterpret_cast<const uint4*>(pa);
+      else misaligned = true;
+      if (r < N) {
+        if ((reinterpret_cast<uintptr_t>(pb) & 15) == 0) vb = *reinterpret_cast<const uint4*>(pb);
+        else misaligned = true;
+      }
+      *reinterpret_cast<uint4*>(sa + tc::sw128_chunk(r, c)) = va;
+      *reinterpret_cast<uint4*>(sb + tc::sw128_chunk(r, c)) = vb;
+    }
+    // scale atoms: atom kk, line r (32), word c (4): rows r + 32 c, blocks 4 kk .. 4 kk + 3
+    for (int i = tid; i < 4 * 32 * 4; i += 128) {
+      const int kk = i >> 7, r = (i >> 2) & 31, c = i & 3;
+      const int row = r + 32 * c;
+      const uint8_t* qa = sA + (size_t)row * sb_row + k0 / 16 + 4 * kk;
+      const uint8_t* qb = sB + (size_t)row * sb_row + k0 / 16 + 4 * kk;
+      uint32_t wa = 0, wb = 0;
+      if ((reinterpret_cast<uintptr_t>(qa) & 3) == 0) wa = *reinterpret_cast<const uint32_t*>(qa);
+      else misaligned = true;
+      if (row < N) {
+        if ((reinterpret_cast<uintptr_t>(qb) & 3) == 0) wb = *reinterpret_cast<const uint32_t*>(qb);
+        else misaligned = true;
+      }
+      *reinterpret_cast<uint32_t*>(ssa + 512 * kk + 16 * r + 4 * c) = wa;
+      *reinterpret_cast<uint32_t*>(ssb + 512 * kk + 16 * r + 4 * c) = wb;
+    }
+    fence_proxy_async_smem();
+    __syncthreads();
+    if (tid == 0) {
+      tc::fence_after_sync();
+      for (int kk = 0; kk < 4; ++kk) {
+        tc::tmem_cp_32x128b_x4(t_sfa + 4 * kk, tc::desc_plain(smem_addr(ssa + 512 * kk), 128));
+        tc::tmem_cp_32x128b_x4(t_sfb + 4 * kk, tc::desc_plain(smem_addr(ssb + 512 * kk), 128));
+      }
+      for (int kk = 0; kk < 4; ++kk)
+        tc::mma_mxf4nvf4(tmem, tc::desc_sw128(smem_addr(sa) + 32 * kk), tc::desc_sw128(smem_addr(sb) + 32 * kk),
+                         idesc, t_sfa + 4 * kk, t_sfb + 4 * kk, (k0 > 0 || kk > 0) ? 1u : 0u);
+      tc::mma_commit(&bar);
+    }
+    if (!mbar_wait_bounded(&bar, phase, kWaitLimit)) ok = false;
+    phase ^= 1u;
+    tc::fence_after_sync();
+  }
+  for (int j0 = 0; j0 < N; j0 += 32) {
+    uint32_t r[32];
+    tc::tmem_ld32(tmem + ((uint32_t)(32 * warp) << 16) + (uint32_t)j0, r);
+    tc::tmem_ld_wait();
+    const int m = 32 * warp + (tid & 31);
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (j0 + j < N) D[(size_t)m * N + j0 + j] = __uint_as_float(r[j]);
+  }
+  if (!ok) atomicOr(err, 1);
+  if (misaligned) atomicOr(err, 2);
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 0) tc::tmem_dealloc(tmem, 256);
+}
+
+cudaError_t launch_fp4_gemm_check(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const uint8_t* sB, int K,
+                                  int N, float* D, int* err, cudaStream_t stream) {
+  const size_t smem = 1024 + 32768 + 4096;
+  cudaError_t e = cudaFuncSetAttribute(k_fp4_gemm_check, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  k_fp4_gemm_check<<<1, 128, smem, stream>>>(A, sA, B, sB, K, N, D, err);
+  return cudaGetLastError();
+}
+
 // ------------------------------------------------------------------ P1: routes sorted by expert
 
 constexpr int kSortThreads = 1024;

@@ -52,6 +52,57 @@ __host__ __device__ __forceinline__ uint32_t idesc_f16(uint32_t M, uint32_t N, b
   return d;
 }
 
+// Instruction descriptor of kind::mxf4nvf4 with block scaling (NVFP4: E2M1
+// A and B, packed two values a byte, UE4M3 scales per 16 values along K),
+// both K-major, fp32 accumulator, M x N.  Fields (the PTX ISA's descriptor
+// for the block-scaled kinds): bits 4-5 the scale-B data id, 7-9 A format
+// (E2M1 = 1 for the mxf4 kinds), 10-12 B format, 15/16 A/B major (0 =
+// K-major), 17-22 N >> 3, 23 scale type (0 = UE4M3), 24-28 M >> 4, 29-30
+// the scale-A data id.  With 16-value blocks an MMA (K = 64) uses four
+// scales of a row, one 32-bit tensor-memory column: both data ids are 0.
+__host__ __device__ __forceinline__ uint32_t idesc_mxf4nvf4(uint32_t M, uint32_t N) {
+  uint32_t d = 0;
+  d |= 1u << 7;                       // A: E2M1
+  d |= 1u << 10;                      // B: E2M1
+  d |= (N >> 3) << 17;
+  d |= (M >> 4) << 24;                // scale type bit 23 = 0: UE4M3
+  return d;
+}
+
+// Shared-memory descriptor of a plain (unswizzled) K-major tile whose 8-row
+// groups of 16-byte rows are `sbo` bytes apart: the source of tcgen05.cp.
+__device__ __forceinline__ uint64_t desc_plain(uint32_t saddr, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)1u << 16;                     // leading byte offset (one 16-byte column)
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32; // stride byte offset
+  d |= (uint64_t)1u << 46;                     // version
+  return d;                                    // swizzle 0: none
+}
+
+// 32 rows x 16 bytes of shared memory -> four consecutive 32-bit columns
+// from `taddr` of tensor-memory lanes r, r+32, r+64, r+96 (row r to each of
+// the four lane quarters).
+__device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
+// D[tmem] (+)= (A * scale_A) * (B * scale_B)^T with NVFP4 operands in shared
+// memory and their per-16 UE4M3 scales in tensor memory (one column each for
+// the 64 values of this MMA), issued by one thread.  Scale layout for M (or
+// N) = 128 rows: four tensor-memory columns from sfa/sfb; column c of lane l
+// holds the four scales (bytes, K order) of row (l % 32) + 32 c, the same in
+// every lane quarter -- one 512-byte shared-memory atom (line r: rows r,
+// r+32, r+64, r+96, four bytes each) copied by tmem_cp_32x128b_x4.
+__device__ __forceinline__ void mma_mxf4nvf4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%5], [%6], p;\n\t}"
+      ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
+      : "memory");
+}
+
 // Tensor memory: allocate `ncols` columns (a power of two >= 32) for the CTA;
 // the whole warp executes it and the address lands in *dst (shared memory).
 __device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {

@@ -39,6 +39,55 @@ def test_tc_gemm_matches_f64(K, N):
     assert (np.abs(got - want) <= bound).all(), float(np.max(np.abs(got - want) / bound))
 
 
+def _nvfp4_dequant(codes, scales, rows, K):
+    c = np.empty((rows, K), dtype=np.int64)
+    c[:, 0::2] = codes & 15
+    c[:, 1::2] = codes >> 4
+    v = F.e2m1_value(c).reshape(rows, K // 16, 16) * F.ue4m3_value(scales)[:, :, None]
+    return v.reshape(rows, K)
+
+
+@pytest.mark.parametrize("K,N,case", [(256, 128, "random"), (2048, 128, "random"), (512, 64, "random"),
+                                      (256, 128, "row_scales"), (256, 128, "k_scales")])
+def test_fp4_block_scaled_gemm_matches_f64(K, N, case):
+    """The tcgen05 kind::mxf4nvf4 MMA with per-16 UE4M3 scales in tensor
+    memory, against float64 of the decoded operands: every product of two
+    scaled E2M1 values is exact in fp32, so the only error is the fp32
+    accumulation, K * 2^-24 * sum|a*b| per element.  Structured scales (a
+    distinct scale per row of A and of B, a distinct scale per 16-value block
+    of K) check that every scale reaches its own rows and blocks."""
+    r = np.random.default_rng(K + N + len(case))
+    if case == "random":
+        a = r.integers(0, 256, size=(128, K // 2), dtype=np.uint8)
+        b = r.integers(0, 256, size=(N, K // 2), dtype=np.uint8)
+        sa = r.integers(0x28, 0x48, size=(128, K // 16), dtype=np.uint8)
+        sb = r.integers(0x28, 0x48, size=(N, K // 16), dtype=np.uint8)
+    else:
+        a = np.full((128, K // 2), 0x22, np.uint8)     # every value 1.0
+        b = np.full((N, K // 2), 0x22, np.uint8)
+        sa = np.full((128, K // 16), 0x38, np.uint8)   # 1.0
+        sb = np.full((N, K // 16), 0x38, np.uint8)
+        if case == "row_scales":
+            sa[:] = (((np.arange(128) % 8) + 3) << 3).astype(np.uint8)[:, None]
+            sb[:] = (((np.arange(N) % 7) + 4) << 3).astype(np.uint8)[:, None]
+        else:
+            sa[:] = ((np.arange(K // 16) % 12 + 2) << 3).astype(np.uint8)[None, :]
+    dev = [torch.from_numpy(v).to(DEV) for v in (a, sa, b, sb)]
+    d = torch.full((128, N), float("nan"), dtype=torch.float32, device=DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    capi.moe_debug_fp4_gemm(dev[0].data_ptr(), dev[1].data_ptr(), dev[2].data_ptr(), dev[3].data_ptr(), K, N,
+                            d.data_ptr(), err.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    A = _nvfp4_dequant(a, sa, 128, K)
+    B = _nvfp4_dequant(b, sb, N, K)
+    got = d.cpu().numpy().astype(np.float64)
+    want = A @ B.T
+    bound = K * 2.0 ** -24 * (np.abs(A) @ np.abs(B).T) + 1e-30
+    assert np.isfinite(got).all()
+    assert (np.abs(got - want) <= bound).all(), float(np.max(np.abs(got - want) / bound))
+
+
 # ------------------------------------------------------------------ prompt path (grouped GEMMs)
 
 from oracle import formats as F  # noqa: E402
