@@ -395,11 +395,24 @@ def bench_prefill(dev, steps, warmup, mode, bf16_peak):
     err = capi.moe_get_error(ws.data_ptr(), wsb, stream)
     capi.moe_bank_destroy(bank)
     tflops = prefill_flops(c) / (ms / 1e3) / 1e12
-    return {"mode": {0: "W4A4", 1: "W4A8", 2: "FP16"}[mode], "ms_per_chunk": ms, "tok_per_s": T / (ms / 1e3),
-            "tflops": tflops, "mma": "tcgen05 kind::f16 (exact fp16 operands, fp32 accumulation)",
-            "frac_of_measured_bf16_peak": tflops / bf16_peak,
-            "frac_of_nominal_fp4_peak": tflops / 13500.0, "device_error_bits": err,
-            "launches_per_chunk": 5}
+    # algorithmic bytes: both banks once, x in and the bf16 output, ids and weights
+    alg = E * 2 * I * rb_gu + E * H * rb_dn + 2 * T * H * 2 + 8 * T * K
+    hbm_peak, _ = peaks()
+    res = {"mode": {0: "W4A4", 1: "W4A8", 2: "FP16"}[mode], "ms_per_chunk": ms, "tok_per_s": T / (ms / 1e3),
+           "tflops": tflops, "alg_bytes": alg, "hbm_gbs": alg / (ms / 1e3) / 1e9,
+           "hbm_frac": alg / (ms / 1e3) / 1e9 / hbm_peak, "device_error_bits": err}
+    if mode == 0:
+        # the FP4 peak: the measured bf16 peak times the nominal FP4 / BF16 ratio (13.5 / 2.25)
+        res.update({"mma": "tcgen05 kind::mxf4nvf4 block-scaled FP4 (E2M1 x E2M1, UE4M3 per 16, fp32 accumulation), "
+                           "operands by 2-D TMA",
+                    "peak_tflops": bf16_peak * 6.0, "peak_kind": "measured bf16 x 6 (nominal FP4/BF16 ratio)",
+                    "frac_of_fp4_peak": tflops / (bf16_peak * 6.0), "frac_of_nominal_fp4_peak": tflops / 13500.0,
+                    "launches_per_chunk": 6})
+    else:
+        res.update({"mma": "tcgen05 kind::f16 (exact fp16 operands, fp32 accumulation)",
+                    "frac_of_measured_bf16_peak": tflops / bf16_peak, "frac_of_nominal_fp4_peak": tflops / 13500.0,
+                    "launches_per_chunk": 5})
+    return res
 
 
 def bench_linear(dev, steps, warmup, hbm_peak):

@@ -804,7 +804,7 @@ int moe_debug_block_dots(int32_t type, const void* rows, int32_t nrows, int32_t 
 namespace {
 
 struct PfLayout {
-  size_t err, off, perm, xq, x16, x16lo, i16, y, total;
+  size_t err, off, perm, xq, x16, x16lo, i16, y, xs, in4, total;
 };
 
 PfLayout pf_layout(const moe_layer_geom& g, int64_t T, int mode) {
@@ -822,6 +822,12 @@ PfLayout pf_layout(const moe_layer_geom& g, int64_t T, int mode) {
   L.x16lo = o; o = align_up(o + (mode == PF_W4A8 ? 2 * (size_t)T * g.H : 0), A);
   L.i16 = o; o = align_up(o + 2 * RT * g.I, A);
   L.y = o; o = align_up(o + 4 * RT * g.H, A);
+  // W4A4 on the FP4 tensor cores: NVFP4 rows of x and of the intermediate in sorted route order
+  L.xs = L.in4 = 0;
+  if (mode == PF_W4A4) {
+    L.xs = o; o = align_up(o + RT * (size_t)(g.H / 2 + g.H / 16), A);
+    L.in4 = o; o = align_up(o + RT * (size_t)(g.I / 2 + g.I / 16), A);
+  }
   L.total = o;
   return L;
 }
@@ -842,8 +848,8 @@ size_t moe_prefill_workspace_bytes(const moe_bank* b, int32_t T, int32_t mode) {
   return pf_layout(b->geom, T, mode).total;
 }
 
-int moe_prefill_grouped(const moe_bank* b, const void* x, int32_t T, const int32_t* ids, const float* w,
-                        int32_t mode, void* out, void* ws, size_t ws_bytes, void* stream) {
+static int prefill_impl(const moe_bank* b, const void* x, int32_t T, const int32_t* ids, const float* w, int32_t mode,
+                        void* out, void* ws, size_t ws_bytes, void* stream, bool export_i16) {
   int st = pf_check(b, mode);
   if (st) return st;
   if (T < 0) return MOE_EINVAL;
@@ -875,14 +881,47 @@ int moe_prefill_grouped(const moe_bank* b, const void* x, int32_t T, const int32
   p.x16lo = reinterpret_cast<uint16_t*>(base + L.x16lo);
   p.i16 = reinterpret_cast<uint16_t*>(base + L.i16);
   p.y = reinterpret_cast<float*>(base + L.y);
+  // W4A4 runs on the block-scaled FP4 tensor cores when the bank has its TMA maps
+  if (mode == PF_W4A4 && b->grouped == kGroupedQuant) {
+    Pf4Params q;
+    std::memset(&q, 0, sizeof(q));
+    q.map_wgu = b->map_gu; q.map_wgus = b->map_gus;
+    q.map_wdn = b->map_dn; q.map_wdns = b->map_dns;
+    q.H = g.H; q.I = g.I; q.E = g.E; q.K = g.top_k; q.T = T; q.RT = T * g.top_k;
+    q.glu = g.glu;
+    q.export_i16 = export_i16 ? 1 : 0;
+    q.scales = b->scales; q.ids = ids; q.w = w;
+    q.err = p.err; q.off = p.off; q.perm = p.perm;
+    q.xq = p.xq;
+    q.xs = base + L.xs;
+    q.in4 = base + L.in4;
+    q.i16 = p.i16;
+    q.y = p.y;
+    const uint64_t rbx = (uint64_t)(g.H / 2 + g.H / 16), rbi = (uint64_t)(g.I / 2 + g.I / 16);
+    if (!map_byte_rows(&q.map_xs, q.xs, (uint64_t)q.RT, rbx, 128, 128, true) ||
+        !map_byte_rows(&q.map_xss, q.xs, (uint64_t)q.RT, rbx, 16, 128) ||
+        !map_byte_rows(&q.map_in, q.in4, (uint64_t)q.RT, rbi, 128, 128, true) ||
+        !map_byte_rows(&q.map_ins, q.in4, (uint64_t)q.RT, rbi, 16, 128)) {
+      std::snprintf(g_cuda_err, sizeof(g_cuda_err), "prompt path: tensor map encode failed");
+      return MOE_ECUDA;
+    }
+    p.x16 = nullptr;   // the fp16 operand of the kind::f16 GEMMs is not needed
+    cudaError_t e = launch_prefill(p, static_cast<cudaStream_t>(stream), &q);
+    return e == cudaSuccess ? MOE_OK : cuda_fail(e, "prefill launch");
+  }
   cudaError_t e = launch_prefill(p, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? MOE_OK : cuda_fail(e, "prefill launch");
+}
+
+int moe_prefill_grouped(const moe_bank* b, const void* x, int32_t T, const int32_t* ids, const float* w,
+                        int32_t mode, void* out, void* ws, size_t ws_bytes, void* stream) {
+  return prefill_impl(b, x, T, ids, w, mode, out, ws, ws_bytes, stream, false);
 }
 
 int moe_debug_prefill_stages(const moe_bank* b, const void* x, int32_t T, const int32_t* ids, const float* w,
                              int32_t mode, void* out, void* ws, size_t ws_bytes, void* stream, void* xq,
                              int32_t* off, int32_t* perm, void* i16) {
-  int st = moe_prefill_grouped(b, x, T, ids, w, mode, out, ws, ws_bytes, stream);
+  int st = prefill_impl(b, x, T, ids, w, mode, out, ws, ws_bytes, stream, true);
   if (st || T == 0) return st;
   const moe_layer_geom& g = b->geom;
   const PfLayout L = pf_layout(g, T, mode);

@@ -83,6 +83,32 @@ struct PfParams {
   float* y;                 // fp32 [RT][H]: down output of each route times s_down * w, by route index
 };
 
+// The W4A4 prompt path on the block-scaled FP4 tensor cores (prefill_fp4.cu):
+// x quantized to NVFP4 per token (k_pf_quant), its rows gathered in sorted
+// route order, then two grouped GEMMs (tcgen05 kind::mxf4nvf4, both operands
+// fed by 2-D TMA, per-16 UE4M3 scales in tensor memory) and the fixed-order
+// combine.  NVFP4 rows are codes (K/2 bytes) then scales (K/16 bytes).
+struct Pf4Params {
+  CUtensorMap map_xs, map_xss;    // xs [RT][H/2 + H/16]: code boxes 128 B x 128 rows (swizzled), scale boxes 16 x 128
+  CUtensorMap map_wgu, map_wgus;  // gate_up bank [E*2I][H/2 + H/16], the same boxes
+  CUtensorMap map_in, map_ins;    // in4 [RT][I/2 + I/16]
+  CUtensorMap map_wdn, map_wdns;  // down bank [E*H][I/2 + I/16]
+  int H, I, E, K, T, RT;
+  int glu;
+  int export_i16;                 // also write the dequantized intermediate as fp16 (inspection)
+  const float* scales;            // [E][4]
+  const int32_t* ids;             // [T][K]
+  const float* w;                 // [T][K]
+  uint32_t* err;
+  const int* off;                 // [E+1]
+  const int* perm;                // [RT]
+  const uint8_t* xq;              // NVFP4 x by token [T][H/2 + H/16]
+  uint8_t* xs;                    // NVFP4 x by sorted row [RT][H/2 + H/16]
+  uint8_t* in4;                   // NVFP4 intermediate by sorted row [RT][I/2 + I/16]
+  uint16_t* i16;                  // fp16 [RT][I] (export_i16 only)
+  float* y;                       // fp32 [RT][H] by route index
+};
+
 // The dense path (decode_tc.cu): BF16 gate_up and down banks at batches the
 // fused kernel cannot hold.  Routes sorted by expert, the routed tokens'
 // hidden states gathered in that order, then two grouped GEMMs on the tensor
@@ -175,7 +201,10 @@ cudaError_t launch_qbatch(const QbParams& p, cudaStream_t stream);
 cudaError_t launch_quantize_q8_1_blocks(const float* x, int64_t n, uint8_t* out, cudaStream_t stream);
 cudaError_t launch_block_dots(int type, const uint8_t* rows, int nrows, int k, const uint8_t* act,
                               int32_t* out, cudaStream_t stream);
-cudaError_t launch_prefill(const PfParams& p, cudaStream_t stream);
+struct Pf4Params;
+cudaError_t launch_prefill(const PfParams& p, cudaStream_t stream, const Pf4Params* fp4 = nullptr);
+// The W4A4 GEMMs on FP4 (after k_pf_sort and k_pf_quant of launch_prefill).
+cudaError_t launch_prefill_fp4(const Pf4Params& q, const PfParams& p, cudaStream_t stream);
 cudaError_t launch_tc_gemm_check(const uint16_t* A, const uint16_t* B, int K, int N, float* D, int* err,
                                  cudaStream_t stream);
 cudaError_t launch_wait_timeout(int mode, uint32_t limit, uint32_t* err, cudaStream_t stream);

@@ -336,9 +336,11 @@ __global__ void k_pf_quant(const __grid_constant__ PfParams p) {
     const size_t rbx = (size_t)p.H / 2 + p.H / 16;
     *reinterpret_cast<uint2*>(p.xq + (size_t)t * rbx + 8 * b) = make_uint2(c0, c1);
     p.xq[(size_t)t * rbx + p.H / 2 + b] = (uint8_t)sbyte;
-    uint4* dst = reinterpret_cast<uint4*>(p.x16 + (size_t)t * p.H + 16 * b);
-    dst[0] = make_uint4(h[0], h[1], h[2], h[3]);
-    dst[1] = make_uint4(h[4], h[5], h[6], h[7]);
+    if (p.x16) {   // the fp16 operand of the kind::f16 GEMMs (not used on the FP4 tensor cores)
+      uint4* dst = reinterpret_cast<uint4*>(p.x16 + (size_t)t * p.H + 16 * b);
+      dst[0] = make_uint4(h[0], h[1], h[2], h[3]);
+      dst[1] = make_uint4(h[4], h[5], h[6], h[7]);
+    }
   } else {
     const int nb = p.H / 32;
     if (idx >= (long long)p.T * nb) return;
@@ -653,9 +655,328 @@ __global__ void k_pf_combine(const __grid_constant__ PfParams p) {
   route_sum4(p.ids, p.y, p.out, p.T, p.K, p.E, p.H, (long long)blockIdx.x * blockDim.x + threadIdx.x);
 }
 
+// ------------------------------------------------------------------ W4A4 on the FP4 tensor cores
+
+namespace {
+
+constexpr int kF4Threads = 256;    // warp 0 TMA, warp 1 scale atoms + MMA, warps 4..7 epilogue
+constexpr int kF4Code = 16384;     // one operand's codes per stage: 128 rows x 128 bytes (256 values)
+constexpr int kF4Scale = 2048;     // its scales: 128 rows x 16 bytes
+constexpr int kF4Op = kF4Code + kF4Scale;
+
+__device__ __forceinline__ void f4_tma(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+      ::"r"(smem_addr(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
+      : "memory");
+}
+
+// Bounded wait (2 s of device time) that also gives up once another role of
+// the CTA has.
+__device__ __forceinline__ bool f4_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 255u) == 0u) {
+      if (*abort) return false;
+      if (globaltimer_ns() - t0 > kSpinLimit) {
+        *abort = 1;
+        return false;
+      }
+    }
+  }
+}
+
+// The four 512-byte MMA scale atoms of one operand's 128 x 16-byte scale tile
+// (row R: the sixteen UE4M3 scales of row R in this 256-value chunk): atom
+// kk, line R % 32, word R / 32 holds the four scales of MMA kk.  One warp.
+__device__ __forceinline__ void f4_scale_atoms(const uint8_t* tile, uint8_t* atoms, int lane) {
+  const uint32_t* src = reinterpret_cast<const uint32_t*>(tile);
+  uint32_t* dst = reinterpret_cast<uint32_t*>(atoms);
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const int wsrc = lane + 32 * i;
+    const int R = wsrc >> 2, kk = wsrc & 3;
+    dst[kk * 128 + (R & 31) * 4 + (R >> 5)] = src[wsrc];
+  }
+}
+
+// Tile t of the sequence every role walks: row blocks of 128 sorted rows,
+// expert by expert (rbpre: the prefix of each expert's row blocks), each
+// with ncb column blocks of 128.  The expert cursor only moves forward.
+struct F4Tile {
+  int e, row0, rows, cb;
+};
+__device__ __forceinline__ bool f4_tile(int t, int ncb, const int* rbpre, const int* soff, int E, int& ecur,
+                                        F4Tile& tl) {
+  const int rbg = t / ncb;
+  if (rbg >= rbpre[E]) return false;
+  while (rbpre[ecur + 1] <= rbg) ++ecur;
+  tl.e = ecur;
+  tl.row0 = soff[ecur] + 128 * (rbg - rbpre[ecur]);
+  tl.rows = min(128, soff[ecur + 1] - tl.row0);
+  tl.cb = t - rbg * ncb;
+  return true;
+}
+
+}  // namespace
+
+// NVFP4 rows of x in sorted route order: sorted row i is token perm[i] / K's
+// row of k_pf_quant, 16 bytes a thread.  Rows past the valid routes stay
+// unwritten (the GEMMs never use them as valid rows).
+__global__ void k_pf4_gather(const __grid_constant__ Pf4Params p) {
+  const int rb = p.H / 2 + p.H / 16, nch = rb / 16;
+  const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= (long long)p.RT * nch) return;
+  const int i = (int)(idx / nch), c = (int)(idx - (long long)i * nch);
+  if (i >= p.off[p.E]) return;
+  const int t = p.perm[i] / p.K;
+  *reinterpret_cast<uint4*>(p.xs + (size_t)i * rb + 16 * c) =
+      __ldg(reinterpret_cast<const uint4*>(p.xq + (size_t)t * rb + 16 * c));
+}
+
+// Grouped GEMM of the W4A4 prompt path on tcgen05 kind::mxf4nvf4.
+// PHASE 0 (gate_up): tile = (expert, 128 sorted rows, 128 intermediate
+// columns); per 256-value chunk of H one stage holds the rows' NVFP4 x codes
+// and scales and the tile's 128 gate and 128 up weight rows (codes and
+// scales), all by 2-D TMA; the gate and up accumulators (128 columns each)
+// stay in tensor memory over the chunks; the epilogue applies s_gate, s_up
+// and the GLU in fp32 and requantizes each 16 values to NVFP4 (the prompt
+// path's activation rule), writing the sorted NVFP4 intermediate.
+// PHASE 1 (down): tile = (expert, 128 sorted rows, 128 output rows); the
+// epilogue writes y[route] = acc * s_down * w.  One CTA per SM walks the
+// tiles (blockIdx.x, + gridDim.x, ...); every product of two scaled E2M1
+// values is exact in fp32 and the MMA accumulates in fp32.
+template <int PHASE>
+__global__ void __launch_bounds__(kF4Threads, 1) k_pf4_gemm(const __grid_constant__ Pf4Params p) {
+  constexpr int NB = PHASE == 0 ? 2 : 1;   // weight operands per stage: gate and up, or down
+  constexpr int NS = PHASE == 0 ? 3 : 4;   // stages
+  constexpr int kStage = (1 + NB) * kF4Op;
+  constexpr int kAtoms = (1 + NB) * 2048;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint64_t full[NS], empty[NS], acc_full, acc_empty, drain;
+  __shared__ uint32_t tmem_base;
+  __shared__ int abort_flag, consumed;
+  uint8_t* base = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+  uint8_t* stages = base;
+  uint8_t* atoms = base + NS * kStage;
+  int* soff = reinterpret_cast<int*>(atoms + NS * kAtoms);   // [E+1] first sorted row of each expert
+  int* rbpre = soff + (p.E + 1);                             // [E+1] row blocks before each expert
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int E = p.E;
+  const int Kd = PHASE == 0 ? p.H : p.I;   // reduction length
+  const int nchunk = Kd / 256;
+  const int ncb = (PHASE == 0 ? p.I : p.H) / 128;
+  volatile int* abort = &abort_flag;
+
+  if (warp == 0) {
+    tc::tmem_alloc(&tmem_base, 512);
+    tc::tmem_relinquish();
+  }
+  if (tid == 0) {
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    mbar_init(&acc_full, 1);
+    mbar_init(&acc_empty, 128);
+    mbar_init(&drain, 1);
+    fence_mbar_init();
+    abort_flag = 0;
+    consumed = 0;
+  }
+  for (int e = tid; e <= E; e += kF4Threads) soff[e] = p.off[e];
+  __syncthreads();
+  if (warp == 0) {
+    const int per = (E + 31) / 32, e0 = lane * per;
+    int local = 0;
+    for (int i = 0; i < per; ++i)
+      if (e0 + i < E) local += (soff[e0 + i + 1] - soff[e0 + i] + 127) / 128;
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    int run = incl - local;
+    for (int i = 0; i < per; ++i)
+      if (e0 + i < E) {
+        rbpre[e0 + i] = run;
+        run += (soff[e0 + i + 1] - soff[e0 + i] + 127) / 128;
+      }
+    if (lane == 31) rbpre[E] = incl;
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = tmem_base;
+
+  if (warp == 0) {
+    // ---- TMA producer
+    if (lane == 0) {
+      const CUtensorMap* ma = PHASE == 0 ? &p.map_xs : &p.map_in;
+      const CUtensorMap* mas = PHASE == 0 ? &p.map_xss : &p.map_ins;
+      const CUtensorMap* mb = PHASE == 0 ? &p.map_wgu : &p.map_wdn;
+      const CUtensorMap* mbs = PHASE == 0 ? &p.map_wgus : &p.map_wdns;
+      int ecur = 0, q = 0;
+      F4Tile tl;
+      for (int t = blockIdx.x; !*abort && f4_tile(t, ncb, rbpre, soff, E, ecur, tl); t += gridDim.x) {
+        const int yb = PHASE == 0 ? tl.e * 2 * p.I + 128 * tl.cb : tl.e * p.H + 128 * tl.cb;
+        for (int kc = 0; kc < nchunk; ++kc, ++q) {
+          const int s = q % NS;
+          if (q >= NS && !f4_wait(&empty[s], (uint32_t)(((q / NS) & 1) ^ 1), abort)) break;
+          uint8_t* st = stages + (size_t)s * kStage;
+          mbar_arrive_expect_tx(&full[s], (uint32_t)kStage);
+          f4_tma(st, ma, 128 * kc, tl.row0, &full[s]);
+          f4_tma(st + kF4Code, mas, Kd / 2 + 16 * kc, tl.row0, &full[s]);
+          f4_tma(st + kF4Op, mb, 128 * kc, yb, &full[s]);
+          f4_tma(st + kF4Op + kF4Code, mbs, Kd / 2 + 16 * kc, yb, &full[s]);
+          if (PHASE == 0) {
+            f4_tma(st + 2 * kF4Op, mb, 128 * kc, yb + p.I, &full[s]);
+            f4_tma(st + 2 * kF4Op + kF4Code, mbs, Kd / 2 + 16 * kc, yb + p.I, &full[s]);
+          }
+        }
+      }
+      // wait (bounded) for copies that no MMA consumed (only after an abort)
+      __threadfence_block();
+      for (int qn = 0; qn < q; ++qn) {
+        if (qn < q - NS) continue;
+        mbar_wait_spin(&full[qn % NS], (uint32_t)((qn / NS) & 1), kSpinLimit);
+      }
+    }
+  } else if (warp == 1) {
+    // ---- scale atoms and MMA issue
+    const uint32_t idesc = tc::idesc_mxf4nvf4(128, 128);
+    int ecur = 0, q = 0, ntile = 0;
+    F4Tile tl;
+    for (int t = blockIdx.x; !*abort && f4_tile(t, ncb, rbpre, soff, E, ecur, tl); t += gridDim.x) {
+      if (ntile > 0 && !f4_wait(&acc_empty, (uint32_t)((ntile - 1) & 1), abort)) break;
+      tc::fence_after_sync();
+      bool ok = true;
+      for (int kc = 0; kc < nchunk; ++kc, ++q) {
+        const int s = q % NS;
+        if (!f4_wait(&full[s], (uint32_t)((q / NS) & 1), abort)) {
+          ok = false;
+          break;
+        }
+        uint8_t* st = stages + (size_t)s * kStage;
+        uint8_t* at = atoms + (size_t)s * kAtoms;
+#pragma unroll
+        for (int op = 0; op < 1 + NB; ++op) f4_scale_atoms(st + op * kF4Op + kF4Code, at + op * 2048, lane);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tc::fence_after_sync();
+          const uint32_t sf = tmem + 256 + (uint32_t)(s * (1 + NB) * 16);
+#pragma unroll
+          for (int op = 0; op < 1 + NB; ++op)
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              tc::tmem_cp_32x128b_x4(sf + op * 16 + 4 * kk, tc::desc_plain(smem_addr(at + op * 2048 + kk * 512), 128));
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t ad = tc::desc_sw128(smem_addr(st) + 32 * kk);
+#pragma unroll
+            for (int nb = 0; nb < NB; ++nb)
+              tc::mma_mxf4nvf4(tmem + 128 * nb, ad, tc::desc_sw128(smem_addr(st + (1 + nb) * kF4Op) + 32 * kk), idesc,
+                               sf + 4 * kk, sf + (1 + nb) * 16 + 4 * kk, (kc > 0 || kk > 0) ? 1u : 0u);
+          }
+          tc::mma_commit(&empty[s]);   // the stage's smem and scale columns are free once these MMAs are done
+        }
+        __syncwarp();
+      }
+      if (!ok) break;
+      if (lane == 0) tc::mma_commit(&acc_full);
+      __syncwarp();
+      ++ntile;
+    }
+    if (lane == 0) {
+      consumed = q;
+      tc::mma_commit(&drain);   // everything this thread issued is complete before the dealloc
+      mbar_wait_spin(&drain, 0u, kSpinLimit);
+    }
+  } else if (warp >= 4) {
+    // ---- epilogue: warp w reads tensor-memory lanes 32 * (w % 4) .. + 31, one tile row a thread
+    const int qd = warp & 3;
+    const uint32_t tq = tmem + ((uint32_t)(32 * qd) << 16);
+    const int rbi = p.I / 2 + p.I / 16;
+    int ecur = 0, ntile = 0;
+    F4Tile tl;
+    for (int t = blockIdx.x; !*abort && f4_tile(t, ncb, rbpre, soff, E, ecur, tl); t += gridDim.x, ++ntile) {
+      if (!f4_wait(&acc_full, (uint32_t)(ntile & 1), abort)) break;
+      tc::fence_after_sync();
+      const int m = 32 * qd + lane;
+      const bool valid = m < tl.rows;
+      const int row = tl.row0 + m;
+      if (PHASE == 0) {
+        const float sg = __ldg(p.scales + 4 * tl.e + 0), su = __ldg(p.scales + 4 * tl.e + 1);
+        uint32_t codes[16], sc[2] = {0u, 0u};
+#pragma unroll
+        for (int blk = 0; blk < 8; ++blk) {
+          uint32_t g16[16], u16[16];
+          tc::tmem_ld16(tq + 16 * blk, g16);
+          tc::tmem_ld16(tq + 128 + 16 * blk, u16);
+          tc::tmem_ld_wait();
+          float a[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) a[j] = glu_act(__uint_as_float(g16[j]) * sg, __uint_as_float(u16[j]) * su, p.glu);
+          uint32_t sbyte, c0, c1, hw[8];
+          nvfp4_quant16(a, sbyte, c0, c1, hw);
+          codes[2 * blk] = c0;
+          codes[2 * blk + 1] = c1;
+          sc[blk >> 2] |= sbyte << (8 * (blk & 3));
+          if (p.export_i16 && valid) {
+            uint4* dst = reinterpret_cast<uint4*>(p.i16 + (size_t)row * p.I + 128 * tl.cb + 16 * blk);
+            dst[0] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+            dst[1] = make_uint4(hw[4], hw[5], hw[6], hw[7]);
+          }
+        }
+        if (valid) {
+          uint8_t* dst = p.in4 + (size_t)row * rbi;
+          uint4* dc = reinterpret_cast<uint4*>(dst + 64 * tl.cb);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) dc[i] = make_uint4(codes[4 * i], codes[4 * i + 1], codes[4 * i + 2], codes[4 * i + 3]);
+          *reinterpret_cast<uint2*>(dst + p.I / 2 + 8 * tl.cb) = make_uint2(sc[0], sc[1]);
+        }
+      } else {
+        const float sd = __ldg(p.scales + 4 * tl.e + 2);
+        const int r = valid ? p.perm[row] : 0;
+        const float f = valid ? sd * __ldg(p.w + r) : 0.f;
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          uint32_t v[32];
+          tc::tmem_ld32(tq + 32 * cc, v);
+          tc::tmem_ld_wait();
+          if (valid) {
+            float4* dst = reinterpret_cast<float4*>(p.y + (size_t)r * p.H + 128 * tl.cb + 32 * cc);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              dst[i] = make_float4(__uint_as_float(v[4 * i]) * f, __uint_as_float(v[4 * i + 1]) * f,
+                                   __uint_as_float(v[4 * i + 2]) * f, __uint_as_float(v[4 * i + 3]) * f);
+          }
+        }
+      }
+      tc::fence_before_sync();
+      mbar_arrive(&acc_empty);
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  if (tid == 0 && abort_flag) atomicOr(p.err, kErrTimeout);
+  if (warp == 0) tc::tmem_dealloc(tmem, 512);
+}
+
+template <int PHASE>
+size_t pf4_smem(int E) {
+  constexpr int NB = PHASE == 0 ? 2 : 1, NS = PHASE == 0 ? 3 : 4;
+  return 1024 + (size_t)NS * ((1 + NB) * kF4Op + (1 + NB) * 2048) + 8 * ((size_t)E + 1);
+}
+
 // ------------------------------------------------------------------ launch
 
-cudaError_t launch_prefill(const PfParams& p, cudaStream_t stream) {
+cudaError_t launch_prefill(const PfParams& p, cudaStream_t stream, const Pf4Params* fp4) {
   cudaError_t e;
   const size_t ssort = pf_sort_smem(p.E);
   if ((e = cudaFuncSetAttribute(k_pf_sort, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ssort)) != cudaSuccess)
@@ -667,6 +988,7 @@ cudaError_t launch_prefill(const PfParams& p, cudaStream_t stream) {
     k_pf_quant<<<(unsigned)((n + 255) / 256), 256, 0, stream>>>(p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
+  if (fp4) return launch_prefill_fp4(*fp4, p, stream);
   const size_t sg = pf_gemm_smem();
   if (p.mode == PF_W4A8) {
     if ((e = cudaFuncSetAttribute(k_pf_gemm<0, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sg)) !=
@@ -689,6 +1011,27 @@ cudaError_t launch_prefill(const PfParams& p, cudaStream_t stream) {
     const long long n = (long long)p.T * (p.H / 4);
     k_pf_combine<<<(unsigned)((n + 255) / 256), 256, 0, stream>>>(p);
   }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prefill_fp4(const Pf4Params& q, const PfParams& p, cudaStream_t stream) {
+  cudaError_t e;
+  {
+    const long long n = (long long)q.RT * ((q.H / 2 + q.H / 16) / 16);
+    k_pf4_gather<<<(unsigned)((n + 255) / 256), 256, 0, stream>>>(q);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  const size_t s0 = pf4_smem<0>(q.E), s1 = pf4_smem<1>(q.E);
+  if ((e = cudaFuncSetAttribute(k_pf4_gemm<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s0)) != cudaSuccess)
+    return e;
+  if ((e = cudaFuncSetAttribute(k_pf4_gemm<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s1)) != cudaSuccess)
+    return e;
+  k_pf4_gemm<0><<<sm_count(), kF4Threads, s0, stream>>>(q);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  k_pf4_gemm<1><<<sm_count(), kF4Threads, s1, stream>>>(q);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  const long long n = (long long)p.T * (p.H / 4);
+  k_pf_combine<<<(unsigned)((n + 255) / 256), 256, 0, stream>>>(p);
   return cudaGetLastError();
 }
 
