@@ -737,27 +737,36 @@ __global__ void k_pf4_gather(const __grid_constant__ Pf4Params p) {
 }
 
 // Grouped GEMM of the W4A4 prompt path on tcgen05 kind::mxf4nvf4.
-// PHASE 0 (gate_up): tile = (expert, 128 sorted rows, 128 intermediate
+// PHASE 0 (gate_up): tile = (expert, 128 sorted rows, 64 intermediate
 // columns); per 256-value chunk of H one stage holds the rows' NVFP4 x codes
-// and scales and the tile's 128 gate and 128 up weight rows (codes and
-// scales), all by 2-D TMA; the gate and up accumulators (128 columns each)
+// and scales and the tile's 64 gate and 64 up weight rows (codes and
+// scales), all by 2-D TMA; the gate and up accumulators (64 columns each)
 // stay in tensor memory over the chunks; the epilogue applies s_gate, s_up
 // and the GLU in fp32 and requantizes each 16 values to NVFP4 (the prompt
 // path's activation rule), writing the sorted NVFP4 intermediate.
 // PHASE 1 (down): tile = (expert, 128 sorted rows, 128 output rows); the
-// epilogue writes y[route] = acc * s_down * w.  One CTA per SM walks the
-// tiles (blockIdx.x, + gridDim.x, ...); every product of two scaled E2M1
-// values is exact in fp32 and the MMA accumulates in fp32.
+// epilogue writes y[route] = acc * s_down * w.
+// Roles: warp 0 issues the TMA copies; warps 2 and 3 turn each stage's
+// 128 x 16-byte scale tiles into the MMA's scale atoms; warp 1 copies the
+// atoms to tensor memory and issues the MMAs; warps 4..7 run the epilogue.
+// The accumulators are double-buffered, so a tile's epilogue overlaps the
+// next tile's MMAs.  One CTA per SM walks the tiles (blockIdx.x, +
+// gridDim.x, ...).  Every product of two scaled E2M1 values is exact in
+// fp32 and the MMA accumulates in fp32.
 template <int PHASE>
 __global__ void __launch_bounds__(kF4Threads, 1) k_pf4_gemm(const __grid_constant__ Pf4Params p) {
-  constexpr int NB = PHASE == 0 ? 2 : 1;   // weight operands per stage: gate and up, or down
-  constexpr int NS = PHASE == 0 ? 3 : 4;   // stages
-  constexpr int kStage = (1 + NB) * kF4Op;
+  constexpr int NB = PHASE == 0 ? 2 : 1;      // weight operands per stage: gate and up, or down
+  constexpr int BR = PHASE == 0 ? 64 : 128;   // weight rows per operand (MMA N)
+  constexpr int NS = 4;                       // stages
+  constexpr int kB = BR * 144;                // one weight operand per stage: codes then scales
+  constexpr int kStage = kF4Op + NB * kB;     // 36,864 bytes in both phases
   constexpr int kAtoms = (1 + NB) * 2048;
+  constexpr int kAcc = NB * BR;               // accumulator columns of one buffer (128)
+  static_assert(kStage % 1024 == 0 && kF4Op % 1024 == 0 && kB % 1024 == 0, "1024-byte aligned code tiles");
   extern __shared__ uint8_t smem_raw[];
-  __shared__ uint64_t full[NS], empty[NS], acc_full, acc_empty, drain;
+  __shared__ uint64_t full[NS], ready[NS], empty[NS], acc_full[2], acc_empty[2], drain;
   __shared__ uint32_t tmem_base;
-  __shared__ int abort_flag, consumed;
+  __shared__ int abort_flag;
   uint8_t* base = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   uint8_t* stages = base;
   uint8_t* atoms = base + NS * kStage;
@@ -767,7 +776,7 @@ __global__ void __launch_bounds__(kF4Threads, 1) k_pf4_gemm(const __grid_constan
   const int E = p.E;
   const int Kd = PHASE == 0 ? p.H : p.I;   // reduction length
   const int nchunk = Kd / 256;
-  const int ncb = (PHASE == 0 ? p.I : p.H) / 128;
+  const int ncb = (PHASE == 0 ? p.I : p.H) / BR;
   volatile int* abort = &abort_flag;
 
   if (warp == 0) {
@@ -777,14 +786,16 @@ __global__ void __launch_bounds__(kF4Threads, 1) k_pf4_gemm(const __grid_constan
   if (tid == 0) {
     for (int i = 0; i < NS; ++i) {
       mbar_init(&full[i], 1);
+      mbar_init(&ready[i], 2);
       mbar_init(&empty[i], 1);
     }
-    mbar_init(&acc_full, 1);
-    mbar_init(&acc_empty, 128);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&acc_full[i], 1);
+      mbar_init(&acc_empty[i], 128);
+    }
     mbar_init(&drain, 1);
     fence_mbar_init();
     abort_flag = 0;
-    consumed = 0;
   }
   for (int e = tid; e <= E; e += kF4Threads) soff[e] = p.off[e];
   __syncthreads();
@@ -822,37 +833,35 @@ __global__ void __launch_bounds__(kF4Threads, 1) k_pf4_gemm(const __grid_constan
       int ecur = 0, q = 0;
       F4Tile tl;
       for (int t = blockIdx.x; !*abort && f4_tile(t, ncb, rbpre, soff, E, ecur, tl); t += gridDim.x) {
-        const int yb = PHASE == 0 ? tl.e * 2 * p.I + 128 * tl.cb : tl.e * p.H + 128 * tl.cb;
+        const int yb = PHASE == 0 ? tl.e * 2 * p.I + BR * tl.cb : tl.e * p.H + BR * tl.cb;
+        bool ok = true;
         for (int kc = 0; kc < nchunk; ++kc, ++q) {
           const int s = q % NS;
-          if (q >= NS && !f4_wait(&empty[s], (uint32_t)(((q / NS) & 1) ^ 1), abort)) break;
+          if (q >= NS && !f4_wait(&empty[s], (uint32_t)(((q / NS) & 1) ^ 1), abort)) {
+            ok = false;
+            break;
+          }
           uint8_t* st = stages + (size_t)s * kStage;
           mbar_arrive_expect_tx(&full[s], (uint32_t)kStage);
           f4_tma(st, ma, 128 * kc, tl.row0, &full[s]);
           f4_tma(st + kF4Code, mas, Kd / 2 + 16 * kc, tl.row0, &full[s]);
-          f4_tma(st + kF4Op, mb, 128 * kc, yb, &full[s]);
-          f4_tma(st + kF4Op + kF4Code, mbs, Kd / 2 + 16 * kc, yb, &full[s]);
-          if (PHASE == 0) {
-            f4_tma(st + 2 * kF4Op, mb, 128 * kc, yb + p.I, &full[s]);
-            f4_tma(st + 2 * kF4Op + kF4Code, mbs, Kd / 2 + 16 * kc, yb + p.I, &full[s]);
+#pragma unroll
+          for (int nb = 0; nb < NB; ++nb) {
+            f4_tma(st + kF4Op + nb * kB, mb, 128 * kc, yb + nb * p.I, &full[s]);
+            f4_tma(st + kF4Op + nb * kB + BR * 128, mbs, Kd / 2 + 16 * kc, yb + nb * p.I, &full[s]);
           }
         }
+        if (!ok) break;
       }
-      // wait (bounded) for copies that no MMA consumed (only after an abort)
-      __threadfence_block();
-      for (int qn = 0; qn < q; ++qn) {
-        if (qn < q - NS) continue;
+      // wait (bounded) for the last copies issued (complete already unless a role gave up)
+      for (int qn = q - NS < 0 ? 0 : q - NS; qn < q; ++qn)
         mbar_wait_spin(&full[qn % NS], (uint32_t)((qn / NS) & 1), kSpinLimit);
-      }
     }
-  } else if (warp == 1) {
-    // ---- scale atoms and MMA issue
-    const uint32_t idesc = tc::idesc_mxf4nvf4(128, 128);
-    int ecur = 0, q = 0, ntile = 0;
+  } else if (warp == 2 || warp == 3) {
+    // ---- scale atoms: warp 2 those of the x / intermediate rows, warp 3 those of the weight rows
+    int ecur = 0, q = 0;
     F4Tile tl;
     for (int t = blockIdx.x; !*abort && f4_tile(t, ncb, rbpre, soff, E, ecur, tl); t += gridDim.x) {
-      if (ntile > 0 && !f4_wait(&acc_empty, (uint32_t)((ntile - 1) & 1), abort)) break;
-      tc::fence_after_sync();
       bool ok = true;
       for (int kc = 0; kc < nchunk; ++kc, ++q) {
         const int s = q % NS;
@@ -860,14 +869,52 @@ __global__ void __launch_bounds__(kF4Threads, 1) k_pf4_gemm(const __grid_constan
           ok = false;
           break;
         }
-        uint8_t* st = stages + (size_t)s * kStage;
+        const uint8_t* st = stages + (size_t)s * kStage;
         uint8_t* at = atoms + (size_t)s * kAtoms;
+        if (warp == 2) {
+          f4_scale_atoms(st + kF4Code, at, lane);
+        } else {
 #pragma unroll
-        for (int op = 0; op < 1 + NB; ++op) f4_scale_atoms(st + op * kF4Op + kF4Code, at + op * 2048, lane);
+          for (int nb = 0; nb < NB; ++nb) {
+            const uint32_t* src = reinterpret_cast<const uint32_t*>(st + kF4Op + nb * kB + BR * 128);
+            uint32_t* dst = reinterpret_cast<uint32_t*>(at + (1 + nb) * 2048);
+#pragma unroll
+            for (int i = 0; i < BR / 8; ++i) {
+              const int wsrc = lane + 32 * i;
+              const int R = wsrc >> 2, kk = wsrc & 3;
+              dst[kk * 128 + (R & 31) * 4 + (R >> 5)] = src[wsrc];
+            }
+          }
+        }
         fence_proxy_async_smem();
         __syncwarp();
+        if (lane == 0) mbar_arrive(&ready[s]);
+      }
+      if (!ok) break;
+    }
+  } else if (warp == 1) {
+    // ---- tensor-memory scale copies and MMA issue
+    const uint32_t idesc = tc::idesc_mxf4nvf4(128, BR);
+    int ecur = 0, q = 0, ntile = 0;
+    F4Tile tl;
+    for (int t = blockIdx.x; !*abort && f4_tile(t, ncb, rbpre, soff, E, ecur, tl); t += gridDim.x, ++ntile) {
+      const int buf = ntile & 1;
+      if (ntile >= 2 && !f4_wait(&acc_empty[buf], (uint32_t)(((ntile >> 1) - 1) & 1), abort)) break;
+      tc::fence_after_sync();
+      bool ok = true;
+      for (int kc = 0; kc < nchunk; ++kc, ++q) {
+        const int s = q % NS;
+        if (!f4_wait(&ready[s], (uint32_t)((q / NS) & 1), abort)) {
+          ok = false;
+          break;
+        }
         if (lane == 0) {
+          // the copies are complete (the atom warps saw it); this acquire
+          // orders them for this thread's MMAs as well
+          mbar_try_wait(&full[s], (uint32_t)((q / NS) & 1));
           tc::fence_after_sync();
+          const uint8_t* st = stages + (size_t)s * kStage;
+          const uint8_t* at = atoms + (size_t)s * kAtoms;
           const uint32_t sf = tmem + 256 + (uint32_t)(s * (1 + NB) * 16);
 #pragma unroll
           for (int op = 0; op < 1 + NB; ++op)
@@ -879,44 +926,44 @@ __global__ void __launch_bounds__(kF4Threads, 1) k_pf4_gemm(const __grid_constan
             const uint64_t ad = tc::desc_sw128(smem_addr(st) + 32 * kk);
 #pragma unroll
             for (int nb = 0; nb < NB; ++nb)
-              tc::mma_mxf4nvf4(tmem + 128 * nb, ad, tc::desc_sw128(smem_addr(st + (1 + nb) * kF4Op) + 32 * kk), idesc,
-                               sf + 4 * kk, sf + (1 + nb) * 16 + 4 * kk, (kc > 0 || kk > 0) ? 1u : 0u);
+              tc::mma_mxf4nvf4(tmem + kAcc * buf + BR * nb, ad,
+                               tc::desc_sw128(smem_addr(st + kF4Op + nb * kB) + 32 * kk), idesc, sf + 4 * kk,
+                               sf + (1 + nb) * 16 + 4 * kk, (kc > 0 || kk > 0) ? 1u : 0u);
           }
-          tc::mma_commit(&empty[s]);   // the stage's smem and scale columns are free once these MMAs are done
+          tc::mma_commit(&empty[s]);   // the stage's smem, atoms and scale columns are free once these MMAs are done
         }
         __syncwarp();
       }
       if (!ok) break;
-      if (lane == 0) tc::mma_commit(&acc_full);
+      if (lane == 0) tc::mma_commit(&acc_full[buf]);
       __syncwarp();
-      ++ntile;
     }
     if (lane == 0) {
-      consumed = q;
       tc::mma_commit(&drain);   // everything this thread issued is complete before the dealloc
       mbar_wait_spin(&drain, 0u, kSpinLimit);
     }
   } else if (warp >= 4) {
     // ---- epilogue: warp w reads tensor-memory lanes 32 * (w % 4) .. + 31, one tile row a thread
     const int qd = warp & 3;
-    const uint32_t tq = tmem + ((uint32_t)(32 * qd) << 16);
     const int rbi = p.I / 2 + p.I / 16;
     int ecur = 0, ntile = 0;
     F4Tile tl;
     for (int t = blockIdx.x; !*abort && f4_tile(t, ncb, rbpre, soff, E, ecur, tl); t += gridDim.x, ++ntile) {
-      if (!f4_wait(&acc_full, (uint32_t)(ntile & 1), abort)) break;
+      const int buf = ntile & 1;
+      if (!f4_wait(&acc_full[buf], (uint32_t)((ntile >> 1) & 1), abort)) break;
       tc::fence_after_sync();
+      const uint32_t tq = tmem + ((uint32_t)(32 * qd) << 16) + (uint32_t)(kAcc * buf);
       const int m = 32 * qd + lane;
       const bool valid = m < tl.rows;
       const int row = tl.row0 + m;
       if (PHASE == 0) {
         const float sg = __ldg(p.scales + 4 * tl.e + 0), su = __ldg(p.scales + 4 * tl.e + 1);
-        uint32_t codes[16], sc[2] = {0u, 0u};
+        uint32_t codes[8], sc = 0u;
 #pragma unroll
-        for (int blk = 0; blk < 8; ++blk) {
+        for (int blk = 0; blk < BR / 16; ++blk) {
           uint32_t g16[16], u16[16];
           tc::tmem_ld16(tq + 16 * blk, g16);
-          tc::tmem_ld16(tq + 128 + 16 * blk, u16);
+          tc::tmem_ld16(tq + BR + 16 * blk, u16);
           tc::tmem_ld_wait();
           float a[16];
 #pragma unroll
@@ -925,19 +972,21 @@ __global__ void __launch_bounds__(kF4Threads, 1) k_pf4_gemm(const __grid_constan
           nvfp4_quant16(a, sbyte, c0, c1, hw);
           codes[2 * blk] = c0;
           codes[2 * blk + 1] = c1;
-          sc[blk >> 2] |= sbyte << (8 * (blk & 3));
+          sc |= sbyte << (8 * blk);
           if (p.export_i16 && valid) {
-            uint4* dst = reinterpret_cast<uint4*>(p.i16 + (size_t)row * p.I + 128 * tl.cb + 16 * blk);
+            uint4* dst = reinterpret_cast<uint4*>(p.i16 + (size_t)row * p.I + BR * tl.cb + 16 * blk);
             dst[0] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
             dst[1] = make_uint4(hw[4], hw[5], hw[6], hw[7]);
           }
         }
+        tc::fence_before_sync();
+        mbar_arrive(&acc_empty[buf]);   // the accumulator is read: the MMAs of the tile after next may start
         if (valid) {
           uint8_t* dst = p.in4 + (size_t)row * rbi;
-          uint4* dc = reinterpret_cast<uint4*>(dst + 64 * tl.cb);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) dc[i] = make_uint4(codes[4 * i], codes[4 * i + 1], codes[4 * i + 2], codes[4 * i + 3]);
-          *reinterpret_cast<uint2*>(dst + p.I / 2 + 8 * tl.cb) = make_uint2(sc[0], sc[1]);
+          uint4* dc = reinterpret_cast<uint4*>(dst + (BR / 2) * tl.cb);
+          dc[0] = make_uint4(codes[0], codes[1], codes[2], codes[3]);
+          dc[1] = make_uint4(codes[4], codes[5], codes[6], codes[7]);
+          *reinterpret_cast<uint32_t*>(dst + p.I / 2 + (BR / 16) * tl.cb) = sc;
         }
       } else {
         const float sd = __ldg(p.scales + 4 * tl.e + 2);
@@ -948,8 +997,12 @@ __global__ void __launch_bounds__(kF4Threads, 1) k_pf4_gemm(const __grid_constan
           uint32_t v[32];
           tc::tmem_ld32(tq + 32 * cc, v);
           tc::tmem_ld_wait();
+          if (cc == 3) {
+            tc::fence_before_sync();
+            mbar_arrive(&acc_empty[buf]);
+          }
           if (valid) {
-            float4* dst = reinterpret_cast<float4*>(p.y + (size_t)r * p.H + 128 * tl.cb + 32 * cc);
+            float4* dst = reinterpret_cast<float4*>(p.y + (size_t)r * p.H + BR * tl.cb + 32 * cc);
 #pragma unroll
             for (int i = 0; i < 8; ++i)
               dst[i] = make_float4(__uint_as_float(v[4 * i]) * f, __uint_as_float(v[4 * i + 1]) * f,
@@ -957,8 +1010,6 @@ __global__ void __launch_bounds__(kF4Threads, 1) k_pf4_gemm(const __grid_constan
           }
         }
       }
-      tc::fence_before_sync();
-      mbar_arrive(&acc_empty);
     }
   }
   tc::fence_before_sync();
@@ -970,8 +1021,8 @@ __global__ void __launch_bounds__(kF4Threads, 1) k_pf4_gemm(const __grid_constan
 
 template <int PHASE>
 size_t pf4_smem(int E) {
-  constexpr int NB = PHASE == 0 ? 2 : 1, NS = PHASE == 0 ? 3 : 4;
-  return 1024 + (size_t)NS * ((1 + NB) * kF4Op + (1 + NB) * 2048) + 8 * ((size_t)E + 1);
+  constexpr int NB = PHASE == 0 ? 2 : 1, BR = PHASE == 0 ? 64 : 128, NS = 4;
+  return 1024 + (size_t)NS * (kF4Op + NB * BR * 144 + (1 + NB) * 2048) + 8 * ((size_t)E + 1);
 }
 
 // ------------------------------------------------------------------ launch
