@@ -250,6 +250,28 @@ size_t pf_sort_smem(int E) { return sizeof(int) * ((size_t)(kSortThreads / 32) *
 
 // ------------------------------------------------------------------ P2: activation quantizers
 
+// E2M1 codes (nearest even, saturating) of v[i] / sv for eight values, as
+// the IEEE fp32 division gives them: the codes of v * r (r = 1/sv rounded)
+// are taken unless v * r lies within 2^-20 (relative) of an E2M1 rounding
+// boundary -- the quotients differ by a few units in the last place, and
+// the rounding is monotone, so equal codes at t(1 - 2^-20), t and
+// t(1 + 2^-20) are the codes of the division -- else the division is done.
+__device__ __forceinline__ uint32_t e2m1x8_div(const float* v, float sv, float r) {
+  float t[8], tl[8], th[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    t[i] = v[i] * r;
+    tl[i] = t[i] * 0.99999904632568359375f;   // 1 - 2^-20
+    th[i] = t[i] * 1.00000095367431640625f;   // 1 + 2^-20
+  }
+  const uint32_t c = tc::e2m1x8_rne_sat(t);
+  if (c == tc::e2m1x8_rne_sat(tl) && c == tc::e2m1x8_rne_sat(th)) return c;
+  float q[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) q[i] = __fdiv_rn(v[i], sv);
+  return tc::e2m1x8_rne_sat(q);
+}
+
 // NVFP4 quantization of 16 values (W4A4 activations and intermediate): the
 // UE4M3 scale byte, the eight code bytes as two words, and the exact fp16
 // dequantized values (code * scale) as eight f16x2 words.
@@ -262,11 +284,9 @@ __device__ __forceinline__ void nvfp4_quant16(const float* v, uint32_t& sbyte, u
   const uint32_t s2 = tc::ue4m3x2_to_f16x2((uint16_t)(sbyte | (sbyte << 8)));   // (scale, scale)
   const float sv = f16_bits_to_f32(s2 & 0xFFFFu);
   if (sv > 0.f) {
-    float q[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) q[i] = __fdiv_rn(v[i], sv);
-    c0 = tc::e2m1x8_rne_sat(q);
-    c1 = tc::e2m1x8_rne_sat(q + 8);
+    const float r = __frcp_rn(sv);
+    c0 = e2m1x8_div(v, sv, r);
+    c1 = e2m1x8_div(v + 8, sv, r);
   } else {
     c0 = c1 = 0u;
   }
@@ -659,7 +679,7 @@ __global__ void k_pf_combine(const __grid_constant__ PfParams p) {
 
 namespace {
 
-constexpr int kF4Threads = 256;    // warp 0 TMA, warp 1 scale atoms + MMA, warps 4..7 epilogue
+constexpr int kF4Threads = 384;    // warp 0 TMA, warp 1 MMA, warps 2-3 scale atoms, warps 4..11 epilogue
 constexpr int kF4Code = 16384;     // one operand's codes per stage: 128 rows x 128 bytes (256 values)
 constexpr int kF4Scale = 2048;     // its scales: 128 rows x 16 bytes
 constexpr int kF4Op = kF4Code + kF4Scale;
@@ -673,10 +693,13 @@ __device__ __forceinline__ void f4_tma(void* dst, const CUtensorMap* map, int x,
 
 // Bounded wait (2 s of device time) that also gives up once another role of
 // the CTA has.
-__device__ __forceinline__ bool f4_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+// With `sleepy`, the waiting warp pauses between polls (roles off the
+// critical path, so that they leave issue slots to the others).
+__device__ __forceinline__ bool f4_wait(uint64_t* bar, uint32_t parity, volatile int* abort, bool sleepy = false) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t i = 1;; ++i) {
+    if (sleepy) __nanosleep(128);
     if (mbar_try_wait(bar, parity)) return true;
     if ((i & 255u) == 0u) {
       if (*abort) return false;
@@ -748,7 +771,8 @@ __global__ void k_pf4_gather(const __grid_constant__ Pf4Params p) {
 // epilogue writes y[route] = acc * s_down * w.
 // Roles: warp 0 issues the TMA copies; warps 2 and 3 turn each stage's
 // 128 x 16-byte scale tiles into the MMA's scale atoms; warp 1 copies the
-// atoms to tensor memory and issues the MMAs; warps 4..7 run the epilogue.
+// atoms to tensor memory and issues the MMAs; warps 4..11 run the epilogue
+// (two per tensor-memory lane quarter, each half of the tile's columns).
 // The accumulators are double-buffered, so a tile's epilogue overlaps the
 // next tile's MMAs.  One CTA per SM walks the tiles (blockIdx.x, +
 // gridDim.x, ...).  Every product of two scaled E2M1 values is exact in
@@ -757,7 +781,7 @@ template <int PHASE>
 __global__ void __launch_bounds__(kF4Threads, 1) k_pf4_gemm(const __grid_constant__ Pf4Params p) {
   constexpr int NB = PHASE == 0 ? 2 : 1;      // weight operands per stage: gate and up, or down
   constexpr int BR = PHASE == 0 ? 64 : 128;   // weight rows per operand (MMA N)
-  constexpr int NS = 4;                       // stages
+  constexpr int NS = PHASE == 0 ? 5 : 4;       // stages (TMEM: 256 accumulator + NS * 48 or 32 scale columns)
   constexpr int kB = BR * 144;                // one weight operand per stage: codes then scales
   constexpr int kStage = kF4Op + NB * kB;     // 36,864 bytes in both phases
   constexpr int kAtoms = (1 + NB) * 2048;
@@ -791,7 +815,7 @@ __global__ void __launch_bounds__(kF4Threads, 1) k_pf4_gemm(const __grid_constan
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&acc_full[i], 1);
-      mbar_init(&acc_empty[i], 128);
+      mbar_init(&acc_empty[i], 256);
     }
     mbar_init(&drain, 1);
     fence_mbar_init();
@@ -837,7 +861,7 @@ __global__ void __launch_bounds__(kF4Threads, 1) k_pf4_gemm(const __grid_constan
         bool ok = true;
         for (int kc = 0; kc < nchunk; ++kc, ++q) {
           const int s = q % NS;
-          if (q >= NS && !f4_wait(&empty[s], (uint32_t)(((q / NS) & 1) ^ 1), abort)) {
+          if (q >= NS && !f4_wait(&empty[s], (uint32_t)(((q / NS) & 1) ^ 1), abort, true)) {
             ok = false;
             break;
           }
@@ -943,14 +967,16 @@ __global__ void __launch_bounds__(kF4Threads, 1) k_pf4_gemm(const __grid_constan
       mbar_wait_spin(&drain, 0u, kSpinLimit);
     }
   } else if (warp >= 4) {
-    // ---- epilogue: warp w reads tensor-memory lanes 32 * (w % 4) .. + 31, one tile row a thread
-    const int qd = warp & 3;
+    // ---- epilogue: warp w reads tensor-memory lanes 32 * (w % 4) .. + 31 (one tile row a
+    // thread) and half hh of the tile's columns
+    const int qd = warp & 3, hh = (warp - 4) >> 2;
     const int rbi = p.I / 2 + p.I / 16;
+    float* tr = reinterpret_cast<float*>(rbpre + (p.E + 1)) + (warp - 4) * (32 * 33);   // down: a 32 x 32 transpose
     int ecur = 0, ntile = 0;
     F4Tile tl;
     for (int t = blockIdx.x; !*abort && f4_tile(t, ncb, rbpre, soff, E, ecur, tl); t += gridDim.x, ++ntile) {
       const int buf = ntile & 1;
-      if (!f4_wait(&acc_full[buf], (uint32_t)((ntile >> 1) & 1), abort)) break;
+      if (!f4_wait(&acc_full[buf], (uint32_t)((ntile >> 1) & 1), abort, true)) break;
       tc::fence_after_sync();
       const uint32_t tq = tmem + ((uint32_t)(32 * qd) << 16) + (uint32_t)(kAcc * buf);
       const int m = 32 * qd + lane;
@@ -958,56 +984,61 @@ __global__ void __launch_bounds__(kF4Threads, 1) k_pf4_gemm(const __grid_constan
       const int row = tl.row0 + m;
       if (PHASE == 0) {
         const float sg = __ldg(p.scales + 4 * tl.e + 0), su = __ldg(p.scales + 4 * tl.e + 1);
-        uint32_t codes[8], sc = 0u;
+        uint32_t codes[4], sc = 0u;
 #pragma unroll
-        for (int blk = 0; blk < BR / 16; ++blk) {
+        for (int j2 = 0; j2 < 2; ++j2) {
+          const int blk = 2 * hh + j2;
           uint32_t g16[16], u16[16];
           tc::tmem_ld16(tq + 16 * blk, g16);
           tc::tmem_ld16(tq + BR + 16 * blk, u16);
           tc::tmem_ld_wait();
+          if (j2 == 1) {
+            tc::fence_before_sync();
+            mbar_arrive(&acc_empty[buf]);   // this warp's part of the accumulator is read
+          }
           float a[16];
 #pragma unroll
           for (int j = 0; j < 16; ++j) a[j] = glu_act(__uint_as_float(g16[j]) * sg, __uint_as_float(u16[j]) * su, p.glu);
           uint32_t sbyte, c0, c1, hw[8];
           nvfp4_quant16(a, sbyte, c0, c1, hw);
-          codes[2 * blk] = c0;
-          codes[2 * blk + 1] = c1;
-          sc |= sbyte << (8 * blk);
+          codes[2 * j2] = c0;
+          codes[2 * j2 + 1] = c1;
+          sc |= sbyte << (8 * j2);
           if (p.export_i16 && valid) {
             uint4* dst = reinterpret_cast<uint4*>(p.i16 + (size_t)row * p.I + BR * tl.cb + 16 * blk);
             dst[0] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
             dst[1] = make_uint4(hw[4], hw[5], hw[6], hw[7]);
           }
         }
-        tc::fence_before_sync();
-        mbar_arrive(&acc_empty[buf]);   // the accumulator is read: the MMAs of the tile after next may start
         if (valid) {
           uint8_t* dst = p.in4 + (size_t)row * rbi;
-          uint4* dc = reinterpret_cast<uint4*>(dst + (BR / 2) * tl.cb);
-          dc[0] = make_uint4(codes[0], codes[1], codes[2], codes[3]);
-          dc[1] = make_uint4(codes[4], codes[5], codes[6], codes[7]);
-          *reinterpret_cast<uint32_t*>(dst + p.I / 2 + (BR / 16) * tl.cb) = sc;
+          *reinterpret_cast<uint4*>(dst + (BR / 2) * tl.cb + 16 * hh) = make_uint4(codes[0], codes[1], codes[2], codes[3]);
+          *reinterpret_cast<uint16_t*>(dst + p.I / 2 + (BR / 16) * tl.cb + 2 * hh) = (uint16_t)sc;
         }
       } else {
         const float sd = __ldg(p.scales + 4 * tl.e + 2);
         const int r = valid ? p.perm[row] : 0;
         const float f = valid ? sd * __ldg(p.w + r) : 0.f;
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
+        for (int j2 = 0; j2 < 2; ++j2) {
+          const int cc = 2 * hh + j2;
           uint32_t v[32];
           tc::tmem_ld32(tq + 32 * cc, v);
           tc::tmem_ld_wait();
-          if (cc == 3) {
+          if (j2 == 1) {
             tc::fence_before_sync();
             mbar_arrive(&acc_empty[buf]);
           }
-          if (valid) {
-            float4* dst = reinterpret_cast<float4*>(p.y + (size_t)r * p.H + BR * tl.cb + 32 * cc);
+          // through shared memory, so that each store writes 128 contiguous bytes of one route's row
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-              dst[i] = make_float4(__uint_as_float(v[4 * i]) * f, __uint_as_float(v[4 * i + 1]) * f,
-                                   __uint_as_float(v[4 * i + 2]) * f, __uint_as_float(v[4 * i + 3]) * f);
+          for (int i = 0; i < 32; ++i) tr[lane * 33 + i] = __uint_as_float(v[i]) * f;
+          __syncwarp();
+          for (int rr = 0; rr < 32; ++rr) {
+            const int rr_route = __shfl_sync(0xffffffffu, r, rr);
+            const bool rr_valid = __shfl_sync(0xffffffffu, valid ? 1 : 0, rr) != 0;
+            if (rr_valid) p.y[(size_t)rr_route * p.H + BR * tl.cb + 32 * cc + lane] = tr[rr * 33 + lane];
           }
+          __syncwarp();
         }
       }
     }
@@ -1021,8 +1052,9 @@ __global__ void __launch_bounds__(kF4Threads, 1) k_pf4_gemm(const __grid_constan
 
 template <int PHASE>
 size_t pf4_smem(int E) {
-  constexpr int NB = PHASE == 0 ? 2 : 1, BR = PHASE == 0 ? 64 : 128, NS = 4;
-  return 1024 + (size_t)NS * (kF4Op + NB * BR * 144 + (1 + NB) * 2048) + 8 * ((size_t)E + 1);
+  constexpr int NB = PHASE == 0 ? 2 : 1, BR = PHASE == 0 ? 64 : 128, NS = PHASE == 0 ? 5 : 4;
+  return 1024 + (size_t)NS * (kF4Op + NB * BR * 144 + (1 + NB) * 2048) + 8 * ((size_t)E + 1) +
+         (PHASE == 1 ? 8 * 32 * 33 * 4 : 0);
 }
 
 // ------------------------------------------------------------------ launch
