@@ -249,10 +249,16 @@ size_t moe_prefill_workspace_bytes(const moe_bank* bank, int32_t T, int32_t mode
  * codes, both rounded to nearest even with saturation, global scale 1; W4A8:
  * the q8_1 rule of the decode path; FP16: x rounded to fp16, nearest even);
  * a grouped gate_up GEMM on the tensor cores over the exactly dequantized
- * operands (fp16 values, fp32 accumulation) with s_gate, s_up and the GLU in
- * an fp32 epilogue that requantizes the intermediate the same way as x (FP16:
- * rounds it to fp16); a grouped down GEMM whose
- * epilogue scales by s_down * routing weight; a sum over k = 0..K-1 in order.
+ * operands (fp32 accumulation of exact products) with s_gate, s_up and the
+ * GLU in an fp32 epilogue that requantizes the intermediate the same way as x
+ * (FP16: rounds it to fp16); a grouped down GEMM whose epilogue scales by
+ * s_down * routing weight; the route sum in fp32, rounded once to bf16.
+ * W4A8 and FP16 (and W4A4 on a bank without the FP4 tensor-core layout) add
+ * k = 0..K-1 in order, so repeated calls give identical bits; W4A4 on the
+ * block-scaled FP4 tensor cores adds each route into its token's fp32 sum as
+ * the down tiles finish (bulk reductions at L2), so the order of those K
+ * additions, and with it the last fp32 bits of a sum, can differ between
+ * calls (the error bound is the same for every order).
  * x: bf16 [T, H] (device, 16-byte aligned); topk_ids int32 and topk_w fp32
  * [T, K] (device); out bf16 [T, H] (device, 8-byte aligned); ws: device,
  * 256-byte aligned, >= moe_prefill_workspace_bytes(bank, T, mode) bytes (no

@@ -807,7 +807,9 @@ struct PfLayout {
   size_t err, off, perm, xq, x16, x16lo, i16, y, xs, in4, total;
 };
 
-PfLayout pf_layout(const moe_layer_geom& g, int64_t T, int mode) {
+// fp4: W4A4 on the FP4 tensor cores (the bank has its TMA maps): no fp16
+// operands, and y holds one fp32 sum per token instead of one row per route.
+PfLayout pf_layout(const moe_layer_geom& g, int64_t T, int mode, bool fp4) {
   PfLayout L;
   const size_t A = 256;
   const size_t RT = (size_t)T * g.top_k;
@@ -818,19 +820,21 @@ PfLayout pf_layout(const moe_layer_geom& g, int64_t T, int mode) {
   L.xq = o;
   o = align_up(o + (mode == PF_W4A4 ? (size_t)T * (g.H / 2 + g.H / 16)
                     : mode == PF_W4A8 ? (size_t)T * (g.H / 32) * 36 : 0), A);
-  L.x16 = o; o = align_up(o + 2 * (size_t)T * g.H, A);
+  L.x16 = o; o = align_up(o + (fp4 ? 0 : 2 * (size_t)T * g.H), A);
   L.x16lo = o; o = align_up(o + (mode == PF_W4A8 ? 2 * (size_t)T * g.H : 0), A);
   L.i16 = o; o = align_up(o + 2 * RT * g.I, A);
-  L.y = o; o = align_up(o + 4 * RT * g.H, A);
+  L.y = o; o = align_up(o + 4 * (fp4 ? (size_t)T : RT) * g.H, A);
   // W4A4 on the FP4 tensor cores: NVFP4 rows of x and of the intermediate in sorted route order
   L.xs = L.in4 = 0;
-  if (mode == PF_W4A4) {
+  if (fp4) {
     L.xs = o; o = align_up(o + RT * (size_t)(g.H / 2 + g.H / 16), A);
     L.in4 = o; o = align_up(o + RT * (size_t)(g.I / 2 + g.I / 16), A);
   }
   L.total = o;
   return L;
 }
+
+bool pf_fp4(const moe_bank* b, int32_t mode) { return mode == PF_W4A4 && b->grouped == kGroupedQuant; }
 
 int pf_check(const moe_bank* b, int32_t mode) {
   if (!b || (mode != PF_W4A4 && mode != PF_W4A8 && mode != PF_FP16)) return MOE_EINVAL;
@@ -845,7 +849,7 @@ int pf_check(const moe_bank* b, int32_t mode) {
 size_t moe_prefill_workspace_bytes(const moe_bank* b, int32_t T, int32_t mode) {
   if (pf_check(b, mode) != MOE_OK || T < 1) return 0;
   if ((int64_t)T * b->geom.top_k > (int64_t)(1 << 30)) return 0;
-  return pf_layout(b->geom, T, mode).total;
+  return pf_layout(b->geom, T, mode, pf_fp4(b, mode)).total;
 }
 
 static int prefill_impl(const moe_bank* b, const void* x, int32_t T, const int32_t* ids, const float* w, int32_t mode,
@@ -859,7 +863,7 @@ static int prefill_impl(const moe_bank* b, const void* x, int32_t T, const int32
     return MOE_EINVAL;
   const moe_layer_geom& g = b->geom;
   if ((int64_t)T * g.top_k > (int64_t)(1 << 30)) return MOE_EINVAL;
-  const PfLayout L = pf_layout(g, T, mode);
+  const PfLayout L = pf_layout(g, T, mode, pf_fp4(b, mode));
   if (ws_bytes < L.total) return MOE_EINVAL;
   uint8_t* base = static_cast<uint8_t*>(ws);
   PfParams p;
@@ -882,7 +886,7 @@ static int prefill_impl(const moe_bank* b, const void* x, int32_t T, const int32
   p.i16 = reinterpret_cast<uint16_t*>(base + L.i16);
   p.y = reinterpret_cast<float*>(base + L.y);
   // W4A4 runs on the block-scaled FP4 tensor cores when the bank has its TMA maps
-  if (mode == PF_W4A4 && b->grouped == kGroupedQuant) {
+  if (pf_fp4(b, mode)) {
     Pf4Params q;
     std::memset(&q, 0, sizeof(q));
     // gate_up weight boxes of 64 rows (the tile's gate and up halves), down of 128
@@ -897,6 +901,7 @@ static int prefill_impl(const moe_bank* b, const void* x, int32_t T, const int32
     q.in4 = base + L.in4;
     q.i16 = p.i16;
     q.y = p.y;
+    q.out = p.out;
     const uint64_t rbx = (uint64_t)(g.H / 2 + g.H / 16), rbi = (uint64_t)(g.I / 2 + g.I / 16);
     if (!map_byte_rows(&q.map_wgu, b->gu, (uint64_t)g.E * 2 * g.I, rbx, 128, 64, true) ||
         !map_byte_rows(&q.map_wgus, b->gu, (uint64_t)g.E * 2 * g.I, rbx, 16, 64) ||
@@ -926,7 +931,7 @@ int moe_debug_prefill_stages(const moe_bank* b, const void* x, int32_t T, const 
   int st = prefill_impl(b, x, T, ids, w, mode, out, ws, ws_bytes, stream, true);
   if (st || T == 0) return st;
   const moe_layer_geom& g = b->geom;
-  const PfLayout L = pf_layout(g, T, mode);
+  const PfLayout L = pf_layout(g, T, mode, pf_fp4(b, mode));
   const uint8_t* base = static_cast<const uint8_t*>(ws);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const size_t RT = (size_t)T * g.top_k;

@@ -83,11 +83,13 @@ struct PfParams {
   float* y;                 // fp32 [RT][H]: down output of each route times s_down * w, by route index
 };
 
-// The W4A4 prompt path on the block-scaled FP4 tensor cores (prefill_fp4.cu):
+// The W4A4 prompt path on the block-scaled FP4 tensor cores (prefill.cu):
 // x quantized to NVFP4 per token (k_pf_quant), its rows gathered in sorted
 // route order, then two grouped GEMMs (tcgen05 kind::mxf4nvf4, both operands
-// fed by 2-D TMA, per-16 UE4M3 scales in tensor memory) and the fixed-order
-// combine.  NVFP4 rows are codes (K/2 bytes) then scales (K/16 bytes).
+// fed by 2-D TMA, per-16 UE4M3 scales in tensor memory); the down GEMM adds
+// each route's scaled row into its token's fp32 sum by bulk reductions at L2,
+// and one pass rounds the sums to bf16.  NVFP4 rows are codes (K/2 bytes)
+// then scales (K/16 bytes).
 struct Pf4Params {
   CUtensorMap map_xs, map_xss;    // xs [RT][H/2 + H/16]: code boxes 128 B x 128 rows (swizzled), scale boxes 16 x 128
   CUtensorMap map_wgu, map_wgus;  // gate_up bank [E*2I][H/2 + H/16], the same boxes
@@ -106,7 +108,8 @@ struct Pf4Params {
   uint8_t* xs;                    // NVFP4 x by sorted row [RT][H/2 + H/16]
   uint8_t* in4;                   // NVFP4 intermediate by sorted row [RT][I/2 + I/16]
   uint16_t* i16;                  // fp16 [RT][I] (export_i16 only)
-  float* y;                       // fp32 [RT][H] by route index
+  float* y;                       // fp32 [T][H]: each token's sum of its routes' scaled down outputs
+  uint16_t* out;                  // bf16 [T][H]
 };
 
 // The dense path (decode_tc.cu): BF16 gate_up and down banks at batches the
@@ -204,7 +207,7 @@ cudaError_t launch_block_dots(int type, const uint8_t* rows, int nrows, int k, c
 struct Pf4Params;
 cudaError_t launch_prefill(const PfParams& p, cudaStream_t stream, const Pf4Params* fp4 = nullptr);
 // The W4A4 GEMMs on FP4 (after k_pf_sort and k_pf_quant of launch_prefill).
-cudaError_t launch_prefill_fp4(const Pf4Params& q, const PfParams& p, cudaStream_t stream);
+cudaError_t launch_prefill_fp4(const Pf4Params& q, cudaStream_t stream);
 cudaError_t launch_tc_gemm_check(const uint16_t* A, const uint16_t* B, int K, int N, float* D, int* err,
                                  cudaStream_t stream);
 cudaError_t launch_wait_timeout(int mode, uint32_t limit, uint32_t* err, cudaStream_t stream);

@@ -31,6 +31,13 @@
 //   k_pf_combine  P6: out[t] = bf16(sum over k = 0..K-1 of the route rows),
 //                 in route order, no atomics.
 //
+// W4A4 on a bank with the grouped TMA maps runs on the block-scaled FP4
+// tensor cores instead (no fp16 operands): k_pf4_gather lays x's NVFP4 rows
+// out in sorted order and zeroes the fp32 token sums; k_pf4_gemm<0> (P3) and
+// k_pf4_gemm<1> (P4) are tcgen05 kind::mxf4nvf4 GEMMs, the second adding each
+// route's scaled row into its token's sum by bulk reductions at L2 (P6 in
+// completion order); k_pf4_finish rounds the sums to bf16.
+//
 // Every product in the MMAs is of two exact fp16 values (NVFP4 code * scale,
 // or a q8_1 value rounded to fp16 once), accumulated in fp32.
 #include <cuda_fp16.h>
@@ -683,6 +690,15 @@ constexpr int kF4Threads = 384;    // warp 0 TMA, warp 1 MMA, warps 2-3 scale at
 constexpr int kF4Code = 16384;     // one operand's codes per stage: 128 rows x 128 bytes (256 values)
 constexpr int kF4Scale = 2048;     // its scales: 128 rows x 16 bytes
 constexpr int kF4Op = kF4Code + kF4Scale;
+constexpr int kF4Stage = 2 * kF4Op;     // the activation rows' operand, then the weight rows'
+constexpr int kF4Atoms = 2 * kF4Scale;  // both operands' MMA scale atoms
+constexpr int kF4GuCols = 64;           // intermediate columns of one gate_up tile (64 gate + 64 up rows)
+constexpr int kF4EpRow = 272;           // down epilogue: one row's 64 fp32 outputs, padded to spread banks
+
+template <int PHASE>
+struct F4Cfg {
+  static constexpr int NS = PHASE == 0 ? 5 : 3;   // stages; tensor memory: 256 accumulator + NS * 32 scale columns
+};
 
 __device__ __forceinline__ void f4_tma(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
   asm volatile(
@@ -690,6 +706,18 @@ __device__ __forceinline__ void f4_tma(void* dst, const CUtensorMap* map, int x,
       ::"r"(smem_addr(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
       : "memory");
 }
+
+// out[0 .. bytes/4) += the fp32 values at src, as one asynchronous bulk
+// reduction performed at L2 (16-byte aligned addresses, bytes a multiple of 16).
+__device__ __forceinline__ void bulk_reduce_add_f32(float* out, const void* src, uint32_t bytes) {
+  asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;"
+               ::"l"(out), "r"(smem_addr(src)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// this thread's bulk operations have read their shared-memory sources
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// ... and are complete
+__device__ __forceinline__ void bulk_wait_done() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // Bounded wait (2 s of device time) that also gives up once another role of
 // the CTA has.
@@ -727,7 +755,7 @@ __device__ __forceinline__ void f4_scale_atoms(const uint8_t* tile, uint8_t* ato
 
 // Tile t of the sequence every role walks: row blocks of 128 sorted rows,
 // expert by expert (rbpre: the prefix of each expert's row blocks), each
-// with ncb column blocks of 128.  The expert cursor only moves forward.
+// with ncb column blocks.  The expert cursor only moves forward.
 struct F4Tile {
   int e, row0, rows, cb;
 };
@@ -747,10 +775,12 @@ __device__ __forceinline__ bool f4_tile(int t, int ncb, const int* rbpre, const 
 
 // NVFP4 rows of x in sorted route order: sorted row i is token perm[i] / K's
 // row of k_pf_quant, 16 bytes a thread.  Rows past the valid routes stay
-// unwritten (the GEMMs never use them as valid rows).
+// unwritten (the GEMMs never use them as valid rows).  The same launch zeroes
+// the fp32 token sums the down GEMM adds into.
 __global__ void k_pf4_gather(const __grid_constant__ Pf4Params p) {
   const int rb = p.H / 2 + p.H / 16, nch = rb / 16;
   const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx < (long long)p.T * (p.H / 4)) reinterpret_cast<float4*>(p.y)[idx] = make_float4(0.f, 0.f, 0.f, 0.f);
   if (idx >= (long long)p.RT * nch) return;
   const int i = (int)(idx / nch), c = (int)(idx - (long long)i * nch);
   if (i >= p.off[p.E]) return;
@@ -759,16 +789,30 @@ __global__ void k_pf4_gather(const __grid_constant__ Pf4Params p) {
       __ldg(reinterpret_cast<const uint4*>(p.xq + (size_t)t * rb + 16 * c));
 }
 
-// Grouped GEMM of the W4A4 prompt path on tcgen05 kind::mxf4nvf4.
+// out[t] = bf16 of the fp32 token sum (round to nearest even), four values a thread.
+__global__ void k_pf4_finish(const __grid_constant__ Pf4Params p) {
+  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= (long long)p.T * (p.H / 4)) return;
+  const float4 v = __ldcg(reinterpret_cast<const float4*>(p.y) + i);
+  uint2 o;
+  o.x = f32_to_bf16_bits_rn(v.x) | (f32_to_bf16_bits_rn(v.y) << 16);
+  o.y = f32_to_bf16_bits_rn(v.z) | (f32_to_bf16_bits_rn(v.w) << 16);
+  reinterpret_cast<uint2*>(p.out)[i] = o;
+}
+
+// Grouped GEMM of the W4A4 prompt path on tcgen05 kind::mxf4nvf4 (MMA
+// M = N = 128, K = 64 per instruction).
 // PHASE 0 (gate_up): tile = (expert, 128 sorted rows, 64 intermediate
 // columns); per 256-value chunk of H one stage holds the rows' NVFP4 x codes
-// and scales and the tile's 64 gate and 64 up weight rows (codes and
-// scales), all by 2-D TMA; the gate and up accumulators (64 columns each)
-// stay in tensor memory over the chunks; the epilogue applies s_gate, s_up
-// and the GLU in fp32 and requantizes each 16 values to NVFP4 (the prompt
-// path's activation rule), writing the sorted NVFP4 intermediate.
+// and scales and the tile's 64 gate rows followed by its 64 up rows (codes
+// and scales), all by 2-D TMA, so that one MMA covers both projections: the
+// accumulator's columns 0..63 are gate, 64..127 up, and stay in tensor memory
+// over the chunks.  The epilogue applies s_gate, s_up and the GLU in fp32 and
+// requantizes each 16 values to NVFP4 (the prompt path's activation rule),
+// writing the sorted NVFP4 intermediate.
 // PHASE 1 (down): tile = (expert, 128 sorted rows, 128 output rows); the
-// epilogue writes y[route] = acc * s_down * w.
+// epilogue scales each route's row by s_down * w and adds it into its token's
+// fp32 sum with bulk reductions at L2 (the route sum; see k_pf4_finish).
 // Roles: warp 0 issues the TMA copies; warps 2 and 3 turn each stage's
 // 128 x 16-byte scale tiles into the MMA's scale atoms; warp 1 copies the
 // atoms to tensor memory and issues the MMAs; warps 4..11 run the epilogue
@@ -779,28 +823,23 @@ __global__ void k_pf4_gather(const __grid_constant__ Pf4Params p) {
 // fp32 and the MMA accumulates in fp32.
 template <int PHASE>
 __global__ void __launch_bounds__(kF4Threads, 1) k_pf4_gemm(const __grid_constant__ Pf4Params p) {
-  constexpr int NB = PHASE == 0 ? 2 : 1;      // weight operands per stage: gate and up, or down
-  constexpr int BR = PHASE == 0 ? 64 : 128;   // weight rows per operand (MMA N)
-  constexpr int NS = PHASE == 0 ? 5 : 4;       // stages (TMEM: 256 accumulator + NS * 48 or 32 scale columns)
-  constexpr int kB = BR * 144;                // one weight operand per stage: codes then scales
-  constexpr int kStage = kF4Op + NB * kB;     // 36,864 bytes in both phases
-  constexpr int kAtoms = (1 + NB) * 2048;
-  constexpr int kAcc = NB * BR;               // accumulator columns of one buffer (128)
-  static_assert(kStage % 1024 == 0 && kF4Op % 1024 == 0 && kB % 1024 == 0, "1024-byte aligned code tiles");
+  constexpr int NS = F4Cfg<PHASE>::NS;
+  static_assert(256 + NS * 32 <= 512, "tensor memory: two 128-column accumulators and the stages' scales");
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t full[NS], ready[NS], empty[NS], acc_full[2], acc_empty[2], drain;
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
   uint8_t* base = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   uint8_t* stages = base;
-  uint8_t* atoms = base + NS * kStage;
-  int* soff = reinterpret_cast<int*>(atoms + NS * kAtoms);   // [E+1] first sorted row of each expert
+  uint8_t* atoms = base + NS * kF4Stage;
+  uint8_t* ep = atoms + NS * kF4Atoms;                       // down: the epilogue rows
+  int* soff = reinterpret_cast<int*>(ep + (PHASE == 1 ? 8 * 32 * kF4EpRow : 0));   // [E+1] first sorted row of each expert
   int* rbpre = soff + (p.E + 1);                             // [E+1] row blocks before each expert
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int E = p.E;
   const int Kd = PHASE == 0 ? p.H : p.I;   // reduction length
   const int nchunk = Kd / 256;
-  const int ncb = (PHASE == 0 ? p.I : p.H) / BR;
+  const int ncb = PHASE == 0 ? p.I / kF4GuCols : p.H / 128;
   volatile int* abort = &abort_flag;
 
   if (warp == 0) {
@@ -857,7 +896,8 @@ __global__ void __launch_bounds__(kF4Threads, 1) k_pf4_gemm(const __grid_constan
       int ecur = 0, q = 0;
       F4Tile tl;
       for (int t = blockIdx.x; !*abort && f4_tile(t, ncb, rbpre, soff, E, ecur, tl); t += gridDim.x) {
-        const int yb = PHASE == 0 ? tl.e * 2 * p.I + BR * tl.cb : tl.e * p.H + BR * tl.cb;
+        // first weight row of the tile: its gate rows (the up rows are I further), or its down rows
+        const int yb = PHASE == 0 ? tl.e * 2 * p.I + kF4GuCols * tl.cb : tl.e * p.H + 128 * tl.cb;
         bool ok = true;
         for (int kc = 0; kc < nchunk; ++kc, ++q) {
           const int s = q % NS;
@@ -865,14 +905,19 @@ __global__ void __launch_bounds__(kF4Threads, 1) k_pf4_gemm(const __grid_constan
             ok = false;
             break;
           }
-          uint8_t* st = stages + (size_t)s * kStage;
-          mbar_arrive_expect_tx(&full[s], (uint32_t)kStage);
+          uint8_t* st = stages + (size_t)s * kF4Stage;
+          uint8_t* sb = st + kF4Op;
+          mbar_arrive_expect_tx(&full[s], (uint32_t)kF4Stage);
           f4_tma(st, ma, 128 * kc, tl.row0, &full[s]);
           f4_tma(st + kF4Code, mas, Kd / 2 + 16 * kc, tl.row0, &full[s]);
-#pragma unroll
-          for (int nb = 0; nb < NB; ++nb) {
-            f4_tma(st + kF4Op + nb * kB, mb, 128 * kc, yb + nb * p.I, &full[s]);
-            f4_tma(st + kF4Op + nb * kB + BR * 128, mbs, Kd / 2 + 16 * kc, yb + nb * p.I, &full[s]);
+          if (PHASE == 0) {
+            f4_tma(sb, mb, 128 * kc, yb, &full[s]);
+            f4_tma(sb + kF4Code / 2, mb, 128 * kc, yb + p.I, &full[s]);
+            f4_tma(sb + kF4Code, mbs, Kd / 2 + 16 * kc, yb, &full[s]);
+            f4_tma(sb + kF4Code + kF4Scale / 2, mbs, Kd / 2 + 16 * kc, yb + p.I, &full[s]);
+          } else {
+            f4_tma(sb, mb, 128 * kc, yb, &full[s]);
+            f4_tma(sb + kF4Code, mbs, Kd / 2 + 16 * kc, yb, &full[s]);
           }
         }
         if (!ok) break;
@@ -893,23 +938,9 @@ __global__ void __launch_bounds__(kF4Threads, 1) k_pf4_gemm(const __grid_constan
           ok = false;
           break;
         }
-        const uint8_t* st = stages + (size_t)s * kStage;
-        uint8_t* at = atoms + (size_t)s * kAtoms;
-        if (warp == 2) {
-          f4_scale_atoms(st + kF4Code, at, lane);
-        } else {
-#pragma unroll
-          for (int nb = 0; nb < NB; ++nb) {
-            const uint32_t* src = reinterpret_cast<const uint32_t*>(st + kF4Op + nb * kB + BR * 128);
-            uint32_t* dst = reinterpret_cast<uint32_t*>(at + (1 + nb) * 2048);
-#pragma unroll
-            for (int i = 0; i < BR / 8; ++i) {
-              const int wsrc = lane + 32 * i;
-              const int R = wsrc >> 2, kk = wsrc & 3;
-              dst[kk * 128 + (R & 31) * 4 + (R >> 5)] = src[wsrc];
-            }
-          }
-        }
+        const int op = warp - 2;
+        f4_scale_atoms(stages + (size_t)s * kF4Stage + op * kF4Op + kF4Code, atoms + (size_t)s * kF4Atoms + op * kF4Scale,
+                       lane);
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&ready[s]);
@@ -918,7 +949,7 @@ __global__ void __launch_bounds__(kF4Threads, 1) k_pf4_gemm(const __grid_constan
     }
   } else if (warp == 1) {
     // ---- tensor-memory scale copies and MMA issue
-    const uint32_t idesc = tc::idesc_mxf4nvf4(128, BR);
+    const uint32_t idesc = tc::idesc_mxf4nvf4(128, 128);
     int ecur = 0, q = 0, ntile = 0;
     F4Tile tl;
     for (int t = blockIdx.x; !*abort && f4_tile(t, ncb, rbpre, soff, E, ecur, tl); t += gridDim.x, ++ntile) {
@@ -937,23 +968,18 @@ __global__ void __launch_bounds__(kF4Threads, 1) k_pf4_gemm(const __grid_constan
           // orders them for this thread's MMAs as well
           mbar_try_wait(&full[s], (uint32_t)((q / NS) & 1));
           tc::fence_after_sync();
-          const uint8_t* st = stages + (size_t)s * kStage;
-          const uint8_t* at = atoms + (size_t)s * kAtoms;
-          const uint32_t sf = tmem + 256 + (uint32_t)(s * (1 + NB) * 16);
+          const uint32_t st = smem_addr(stages + (size_t)s * kF4Stage);
+          const uint32_t at = smem_addr(atoms + (size_t)s * kF4Atoms);
+          const uint32_t sf = tmem + 256 + (uint32_t)(s * 32);
 #pragma unroll
-          for (int op = 0; op < 1 + NB; ++op)
+          for (int op = 0; op < 2; ++op)
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-              tc::tmem_cp_32x128b_x4(sf + op * 16 + 4 * kk, tc::desc_plain(smem_addr(at + op * 2048 + kk * 512), 128));
+              tc::tmem_cp_32x128b_x4(sf + op * 16 + 4 * kk, tc::desc_plain(at + op * kF4Scale + kk * 512, 128));
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t ad = tc::desc_sw128(smem_addr(st) + 32 * kk);
-#pragma unroll
-            for (int nb = 0; nb < NB; ++nb)
-              tc::mma_mxf4nvf4(tmem + kAcc * buf + BR * nb, ad,
-                               tc::desc_sw128(smem_addr(st + kF4Op + nb * kB) + 32 * kk), idesc, sf + 4 * kk,
-                               sf + (1 + nb) * 16 + 4 * kk, (kc > 0 || kk > 0) ? 1u : 0u);
-          }
+          for (int kk = 0; kk < 4; ++kk)
+            tc::mma_mxf4nvf4(tmem + 128 * buf, tc::desc_sw128(st + 32 * kk), tc::desc_sw128(st + kF4Op + 32 * kk), idesc,
+                             sf + 4 * kk, sf + 16 + 4 * kk, (kc > 0 || kk > 0) ? 1u : 0u);
           tc::mma_commit(&empty[s]);   // the stage's smem, atoms and scale columns are free once these MMAs are done
         }
         __syncwarp();
@@ -971,14 +997,14 @@ __global__ void __launch_bounds__(kF4Threads, 1) k_pf4_gemm(const __grid_constan
     // thread) and half hh of the tile's columns
     const int qd = warp & 3, hh = (warp - 4) >> 2;
     const int rbi = p.I / 2 + p.I / 16;
-    float* tr = reinterpret_cast<float*>(rbpre + (p.E + 1)) + (warp - 4) * (32 * 33);   // down: a 32 x 32 transpose
+    float* mine = reinterpret_cast<float*>(ep + (size_t)((warp - 4) * 32 + lane) * kF4EpRow);   // down: this row's 64 outputs
     int ecur = 0, ntile = 0;
     F4Tile tl;
     for (int t = blockIdx.x; !*abort && f4_tile(t, ncb, rbpre, soff, E, ecur, tl); t += gridDim.x, ++ntile) {
       const int buf = ntile & 1;
       if (!f4_wait(&acc_full[buf], (uint32_t)((ntile >> 1) & 1), abort, true)) break;
       tc::fence_after_sync();
-      const uint32_t tq = tmem + ((uint32_t)(32 * qd) << 16) + (uint32_t)(kAcc * buf);
+      const uint32_t tq = tmem + ((uint32_t)(32 * qd) << 16) + (uint32_t)(128 * buf);
       const int m = 32 * qd + lane;
       const bool valid = m < tl.rows;
       const int row = tl.row0 + m;
@@ -990,7 +1016,7 @@ __global__ void __launch_bounds__(kF4Threads, 1) k_pf4_gemm(const __grid_constan
           const int blk = 2 * hh + j2;
           uint32_t g16[16], u16[16];
           tc::tmem_ld16(tq + 16 * blk, g16);
-          tc::tmem_ld16(tq + BR + 16 * blk, u16);
+          tc::tmem_ld16(tq + kF4GuCols + 16 * blk, u16);
           tc::tmem_ld_wait();
           if (j2 == 1) {
             tc::fence_before_sync();
@@ -1005,43 +1031,45 @@ __global__ void __launch_bounds__(kF4Threads, 1) k_pf4_gemm(const __grid_constan
           codes[2 * j2 + 1] = c1;
           sc |= sbyte << (8 * j2);
           if (p.export_i16 && valid) {
-            uint4* dst = reinterpret_cast<uint4*>(p.i16 + (size_t)row * p.I + BR * tl.cb + 16 * blk);
+            uint4* dst = reinterpret_cast<uint4*>(p.i16 + (size_t)row * p.I + kF4GuCols * tl.cb + 16 * blk);
             dst[0] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
             dst[1] = make_uint4(hw[4], hw[5], hw[6], hw[7]);
           }
         }
         if (valid) {
           uint8_t* dst = p.in4 + (size_t)row * rbi;
-          *reinterpret_cast<uint4*>(dst + (BR / 2) * tl.cb + 16 * hh) = make_uint4(codes[0], codes[1], codes[2], codes[3]);
-          *reinterpret_cast<uint16_t*>(dst + p.I / 2 + (BR / 16) * tl.cb + 2 * hh) = (uint16_t)sc;
+          *reinterpret_cast<uint4*>(dst + (kF4GuCols / 2) * tl.cb + 16 * hh) =
+              make_uint4(codes[0], codes[1], codes[2], codes[3]);
+          *reinterpret_cast<uint16_t*>(dst + p.I / 2 + (kF4GuCols / 16) * tl.cb + 2 * hh) = (uint16_t)sc;
         }
       } else {
         const float sd = __ldg(p.scales + 4 * tl.e + 2);
         const int r = valid ? p.perm[row] : 0;
         const float f = valid ? sd * __ldg(p.w + r) : 0.f;
+        bulk_wait_read();   // the previous tile's reduction has read this row
 #pragma unroll
         for (int j2 = 0; j2 < 2; ++j2) {
-          const int cc = 2 * hh + j2;
           uint32_t v[32];
-          tc::tmem_ld32(tq + 32 * cc, v);
+          tc::tmem_ld32(tq + 64 * hh + 32 * j2, v);
           tc::tmem_ld_wait();
           if (j2 == 1) {
             tc::fence_before_sync();
             mbar_arrive(&acc_empty[buf]);
           }
-          // through shared memory, so that each store writes 128 contiguous bytes of one route's row
 #pragma unroll
-          for (int i = 0; i < 32; ++i) tr[lane * 33 + i] = __uint_as_float(v[i]) * f;
-          __syncwarp();
-          for (int rr = 0; rr < 32; ++rr) {
-            const int rr_route = __shfl_sync(0xffffffffu, r, rr);
-            const bool rr_valid = __shfl_sync(0xffffffffu, valid ? 1 : 0, rr) != 0;
-            if (rr_valid) p.y[(size_t)rr_route * p.H + BR * tl.cb + 32 * cc + lane] = tr[rr * 33 + lane];
-          }
-          __syncwarp();
+          for (int i = 0; i < 32; i += 4)
+            *reinterpret_cast<float4*>(mine + 32 * j2 + i) =
+                make_float4(__uint_as_float(v[i]) * f, __uint_as_float(v[i + 1]) * f, __uint_as_float(v[i + 2]) * f,
+                            __uint_as_float(v[i + 3]) * f);
+        }
+        if (valid) {
+          fence_proxy_async_smem();
+          bulk_reduce_add_f32(p.y + (size_t)(r / p.K) * p.H + 128 * tl.cb + 64 * hh, mine, 256);
+          bulk_commit();
         }
       }
     }
+    if (PHASE == 1) bulk_wait_done();
   }
   tc::fence_before_sync();
   __syncthreads();
@@ -1052,9 +1080,8 @@ __global__ void __launch_bounds__(kF4Threads, 1) k_pf4_gemm(const __grid_constan
 
 template <int PHASE>
 size_t pf4_smem(int E) {
-  constexpr int NB = PHASE == 0 ? 2 : 1, BR = PHASE == 0 ? 64 : 128, NS = PHASE == 0 ? 5 : 4;
-  return 1024 + (size_t)NS * (kF4Op + NB * BR * 144 + (1 + NB) * 2048) + 8 * ((size_t)E + 1) +
-         (PHASE == 1 ? 8 * 32 * 33 * 4 : 0);
+  return 1024 + (size_t)F4Cfg<PHASE>::NS * (kF4Stage + kF4Atoms) + (PHASE == 1 ? 8 * 32 * kF4EpRow : 0) +
+         8 * ((size_t)E + 1);
 }
 
 // ------------------------------------------------------------------ launch
@@ -1071,7 +1098,7 @@ cudaError_t launch_prefill(const PfParams& p, cudaStream_t stream, const Pf4Para
     k_pf_quant<<<(unsigned)((n + 255) / 256), 256, 0, stream>>>(p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  if (fp4) return launch_prefill_fp4(*fp4, p, stream);
+  if (fp4) return launch_prefill_fp4(*fp4, stream);
   const size_t sg = pf_gemm_smem();
   if (p.mode == PF_W4A8) {
     if ((e = cudaFuncSetAttribute(k_pf_gemm<0, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sg)) !=
@@ -1097,10 +1124,12 @@ cudaError_t launch_prefill(const PfParams& p, cudaStream_t stream, const Pf4Para
   return cudaGetLastError();
 }
 
-cudaError_t launch_prefill_fp4(const Pf4Params& q, const PfParams& p, cudaStream_t stream) {
+cudaError_t launch_prefill_fp4(const Pf4Params& q, cudaStream_t stream) {
   cudaError_t e;
+  const long long nsum = (long long)q.T * (q.H / 4);   // float4s of the fp32 token sums
   {
-    const long long n = (long long)q.RT * ((q.H / 2 + q.H / 16) / 16);
+    long long n = (long long)q.RT * ((q.H / 2 + q.H / 16) / 16);
+    if (n < nsum) n = nsum;
     k_pf4_gather<<<(unsigned)((n + 255) / 256), 256, 0, stream>>>(q);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
@@ -1113,8 +1142,7 @@ cudaError_t launch_prefill_fp4(const Pf4Params& q, const PfParams& p, cudaStream
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   k_pf4_gemm<1><<<sm_count(), kF4Threads, s1, stream>>>(q);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  const long long n = (long long)p.T * (p.H / 4);
-  k_pf_combine<<<(unsigned)((n + 255) / 256), 256, 0, stream>>>(p);
+  k_pf4_finish<<<(unsigned)((nsum + 255) / 256), 256, 0, stream>>>(q);
   return cudaGetLastError();
 }
 
