@@ -804,7 +804,7 @@ int moe_debug_block_dots(int32_t type, const void* rows, int32_t nrows, int32_t 
 namespace {
 
 struct PfLayout {
-  size_t err, off, perm, xq, x16, x16lo, i16, y, xs, in4, total;
+  size_t err, off, perm, bcnt, xq, x16, x16lo, i16, y, xs, in4, total;
 };
 
 // fp4: W4A4 on the FP4 tensor cores (the bank has its TMA maps): no fp16
@@ -817,6 +817,7 @@ PfLayout pf_layout(const moe_layer_geom& g, int64_t T, int mode, bool fp4) {
   L.err = o; o = align_up(o + 4, A);
   L.off = o; o = align_up(o + 4 * ((size_t)g.E + 1), A);
   L.perm = o; o = align_up(o + 4 * RT, A);
+  L.bcnt = o; o = align_up(o + 4 * (size_t)kSortBlocks * g.E, A);
   L.xq = o;
   o = align_up(o + (mode == PF_W4A4 ? (size_t)T * (g.H / 2 + g.H / 16)
                     : mode == PF_W4A8 ? (size_t)T * (g.H / 32) * 36 : 0), A);
@@ -880,6 +881,7 @@ static int prefill_impl(const moe_bank* b, const void* x, int32_t T, const int32
   p.err = reinterpret_cast<uint32_t*>(base + L.err);
   p.off = reinterpret_cast<int*>(base + L.off);
   p.perm = reinterpret_cast<int*>(base + L.perm);
+  p.bcnt = reinterpret_cast<int*>(base + L.bcnt);
   p.xq = base + L.xq;
   p.x16 = reinterpret_cast<uint16_t*>(base + L.x16);
   p.x16lo = reinterpret_cast<uint16_t*>(base + L.x16lo);

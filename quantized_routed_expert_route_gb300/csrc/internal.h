@@ -11,6 +11,7 @@ struct moe_bank;   // the C ABI's opaque bank (api.cu)
 namespace qre {
 
 constexpr int kMaxE = 1024;
+constexpr int kSortBlocks = 32;   // blocks of the prompt path's two-pass route sort
 constexpr int kMaxTopK = 32;
 constexpr int kTChunk = 64;
 constexpr int kMaxGridCtas = 256;   // CTAs of the fused kernel's grid barrier
@@ -76,6 +77,7 @@ struct PfParams {
   uint32_t* err;
   int* off;                 // [E+1] first sorted row of each expert; off[E] = valid routes
   int* perm;                // [RT]  route index of each sorted row
+  int* bcnt;                // [kSortBlocks][E] the sort's per-block expert counts
   uint8_t* xq;              // quantized x: NVFP4 rows [T][H/2 + H/16] (W4A4) or q8_1 blocks [T][H/32][36] (W4A8)
   uint16_t* x16;            // fp16 [T][H]: the dequantized quantized x (the gate_up A operand)
   uint16_t* x16lo;          // fp16 [T][H], W4A8 only: q*d - x16 (x16 + x16lo carries q*d to ~2^-22)

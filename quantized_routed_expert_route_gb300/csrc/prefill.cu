@@ -6,8 +6,10 @@
 // with q8_1 activations; FreeToken PR #732, "Design", for the layer formula
 // and the per-expert weight_scale_2 applied to each projection's fp32 output):
 //
-//   k_pf_sort     P1: the T*K routes sorted by expert (stable: route order
-//                 t*K+k inside an expert), per-expert row offsets.
+//   k_pf_count,   P1: the T*K routes sorted by expert (stable: route order
+//   k_pf_scatter  t*K+k inside an expert), per-expert row offsets: per-block
+//                 expert counts over slices of the routes, then every block
+//                 places its slice after the earlier blocks' routes.
 //   k_pf_quant    P2: every token's hidden state quantized once -- NVFP4 (per
 //                 16 values: UE4M3 scale = amax/6 nearest-even, E2M1 codes
 //                 nearest-even, global scale 1) or q8_1 -- and stored both as
@@ -239,21 +241,103 @@ cudaError_t launch_fp4_gemm_check(const uint8_t* A, const uint8_t* sA, const uin
 // ------------------------------------------------------------------ P1: routes sorted by expert
 
 constexpr int kSortThreads = 1024;
+constexpr int kSortRoutes = 1024;   // routes per block (the grid has at most kSortBlocks blocks)
 
-// One CTA sorts the routes by expert (stable: route order inside an expert);
-// routes whose id is outside [0, E) are left out and flag the error word.
-__global__ void __launch_bounds__(kSortThreads) k_pf_sort(const __grid_constant__ PfParams p) {
-  extern __shared__ int ssm[];
-  constexpr int NW = kSortThreads / 32;
-  int* cnt = ssm;               // [NW][E]
-  int* base = cnt + NW * p.E;   // [E]
-  int* wsum = base + p.E;       // [33]
-  if (threadIdx.x == 0) *p.err = 0u;  // each prompt-path call starts with a clear error word
-  const bool bad = sort_routes_block(p.ids, p.RT, p.E, cnt, base, wsum, p.off, p.perm);
-  if (bad && (threadIdx.x & 31) == 0) atomicOr(p.err, kErrBadId);
+// Blocks of the two sort passes for RT routes: block b takes the routes
+// [b * per, (b + 1) * per), per = ceil(RT / blocks).
+int pf_sort_blocks(long long RT) {
+  const long long nb = (RT + kSortRoutes - 1) / kSortRoutes;
+  return nb < 1 ? 1 : nb > kSortBlocks ? kSortBlocks : (int)nb;
 }
 
-size_t pf_sort_smem(int E) { return sizeof(int) * ((size_t)(kSortThreads / 32) * E + E + 33); }
+// First pass: block b counts the valid routes of each expert in its slice
+// (bcnt[b][e]).  Block 0 clears the error word (each prompt-path call starts
+// clean; the second pass, a later launch, is the first to set it).
+__global__ void __launch_bounds__(kSortThreads) k_pf_count(const __grid_constant__ PfParams p) {
+  extern __shared__ int ssm[];
+  int* cnt = ssm;   // [E]
+  const int tid = threadIdx.x, b = blockIdx.x, E = p.E;
+  if (b == 0 && tid == 0) *p.err = 0u;
+  for (int e = tid; e < E; e += kSortThreads) cnt[e] = 0;
+  __syncthreads();
+  const int per = (p.RT + gridDim.x - 1) / gridDim.x;
+  const int r0 = min(p.RT, b * per), r1 = min(p.RT, r0 + per);
+  for (int r = r0 + tid; r < r1; r += kSortThreads) {
+    const int e = __ldg(p.ids + r);
+    if (e >= 0 && e < E) atomicAdd(&cnt[e], 1);
+  }
+  __syncthreads();
+  for (int e = tid; e < E; e += kSortThreads) p.bcnt[(size_t)b * E + e] = cnt[e];
+}
+
+// Second pass: every block derives the experts' offsets (an exclusive scan of
+// the per-expert totals; block 0 stores them) and its own first row of each
+// expert (the offset plus the earlier blocks' counts), then places its slice
+// warp by warp (each warp a consecutive sub-slice, its lanes ranked by
+// __match_any_sync), so the order inside an expert is the route order: the
+// stable sort.  Routes whose id is outside [0, E) are left out and flag the
+// error word.
+__global__ void __launch_bounds__(kSortThreads) k_pf_scatter(const __grid_constant__ PfParams p) {
+  extern __shared__ int ssm[];
+  constexpr int NW = kSortThreads / 32;
+  const int E = p.E, tid = threadIdx.x, lane = tid & 31, w = tid >> 5, b = blockIdx.x;
+  int* cnt = ssm;              // [NW][E]: per-warp counts, then each warp's first row of each expert
+  int* base = cnt + NW * E;    // [E]
+  int* pre = base + E;         // [E]
+  int* wsum = pre + E;         // [33]
+  for (int e = tid; e < E; e += kSortThreads) {
+    int tot = 0, before = 0;
+    for (int bb = 0; bb < (int)gridDim.x; ++bb) {
+      const int c = p.bcnt[(size_t)bb * E + e];
+      tot += c;
+      if (bb < b) before += c;
+    }
+    base[e] = tot;
+    pre[e] = before;
+  }
+  for (int i = tid; i < NW * E; i += kSortThreads) cnt[i] = 0;
+  __syncthreads();
+  const int total = block_exclusive_scan(base, E, wsum);
+  if (b == 0) {
+    for (int e = tid; e < E; e += kSortThreads) p.off[e] = base[e];
+    if (tid == 0) p.off[E] = total;
+  }
+  const int per = (p.RT + gridDim.x - 1) / gridDim.x;
+  const int s0 = min(p.RT, b * per), s1 = min(p.RT, s0 + per);
+  const int wper = (s1 - s0 + NW - 1) / NW;
+  const int r0 = min(s1, s0 + w * wper), r1 = min(s1, r0 + wper);
+  bool bad = false;
+  for (int r = r0 + lane; r < r1; r += 32) {
+    const int e = __ldg(p.ids + r);
+    if (e >= 0 && e < E) atomicAdd(&cnt[w * E + e], 1);
+    else bad = true;
+  }
+  __syncthreads();
+  for (int e = tid; e < E; e += kSortThreads) {
+    int acc = base[e] + pre[e];
+    for (int ww = 0; ww < NW; ++ww) {
+      const int c = cnt[ww * E + e];
+      cnt[ww * E + e] = acc;
+      acc += c;
+    }
+  }
+  __syncthreads();
+  for (int rb = r0; rb < r1; rb += 32) {
+    const int r = rb + lane;
+    const int e = (r < r1) ? __ldg(p.ids + r) : -1;
+    const bool v = r < r1 && e >= 0 && e < E;
+    const unsigned peers = __match_any_sync(0xffffffffu, v ? e : -1 - lane);
+    const int rank = __popc(peers & ((1u << lane) - 1u));
+    if (v) p.perm[cnt[w * E + e] + rank] = r;
+    __syncwarp();
+    if (v && rank == 0) cnt[w * E + e] += __popc(peers);
+    __syncwarp();
+  }
+  if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(p.err, kErrBadId);
+}
+
+size_t pf_count_smem(int E) { return sizeof(int) * (size_t)E; }
+size_t pf_scatter_smem(int E) { return sizeof(int) * ((size_t)(kSortThreads / 32) * E + 2 * (size_t)E + 33); }
 
 // ------------------------------------------------------------------ P2: activation quantizers
 
@@ -1088,10 +1172,14 @@ size_t pf4_smem(int E) {
 
 cudaError_t launch_prefill(const PfParams& p, cudaStream_t stream, const Pf4Params* fp4) {
   cudaError_t e;
-  const size_t ssort = pf_sort_smem(p.E);
-  if ((e = cudaFuncSetAttribute(k_pf_sort, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ssort)) != cudaSuccess)
+  const int nsb = pf_sort_blocks(p.RT);
+  const size_t sc = pf_count_smem(p.E), ss = pf_scatter_smem(p.E);
+  if ((e = cudaFuncSetAttribute(k_pf_count, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sc)) != cudaSuccess ||
+      (e = cudaFuncSetAttribute(k_pf_scatter, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ss)) != cudaSuccess)
     return e;
-  k_pf_sort<<<1, kSortThreads, ssort, stream>>>(p);
+  k_pf_count<<<nsb, kSortThreads, sc, stream>>>(p);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  k_pf_scatter<<<nsb, kSortThreads, ss, stream>>>(p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   {
     const long long n = (long long)p.T * (p.mode == PF_W4A4 ? p.H / 16 : p.H / 32);
