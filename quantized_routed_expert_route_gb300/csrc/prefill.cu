@@ -770,18 +770,17 @@ __global__ void k_pf_combine(const __grid_constant__ PfParams p) {
 
 namespace {
 
-constexpr int kF4Threads = 384;    // warp 0 TMA, warp 1 MMA, warps 2-3 scale atoms, warps 4..11 epilogue
+constexpr int kF4Threads = 448;    // warp 0 TMA, warp 1 MMA, warps 2-5 scales, warps 6..13 epilogue
 constexpr int kF4Code = 16384;     // one operand's codes per stage: 128 rows x 128 bytes (256 values)
 constexpr int kF4Scale = 2048;     // its scales: 128 rows x 16 bytes
 constexpr int kF4Op = kF4Code + kF4Scale;
 constexpr int kF4Stage = 2 * kF4Op;     // the activation rows' operand, then the weight rows'
-constexpr int kF4Atoms = 2 * kF4Scale;  // both operands' MMA scale atoms
 constexpr int kF4GuCols = 64;           // intermediate columns of one gate_up tile (64 gate + 64 up rows)
 constexpr int kF4EpRow = 272;           // down epilogue: one row's 64 fp32 outputs, padded to spread banks
 
 template <int PHASE>
 struct F4Cfg {
-  static constexpr int NS = PHASE == 0 ? 5 : 3;   // stages; tensor memory: 256 accumulator + NS * 32 scale columns
+  static constexpr int NS = PHASE == 0 ? 6 : 4;   // stages; tensor memory: 256 accumulator + NS * 32 scale columns
 };
 
 __device__ __forceinline__ void f4_tma(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
@@ -823,18 +822,23 @@ __device__ __forceinline__ bool f4_wait(uint64_t* bar, uint32_t parity, volatile
   }
 }
 
-// The four 512-byte MMA scale atoms of one operand's 128 x 16-byte scale tile
-// (row R: the sixteen UE4M3 scales of row R in this 256-value chunk): atom
-// kk, line R % 32, word R / 32 holds the four scales of MMA kk.  One warp.
-__device__ __forceinline__ void f4_scale_atoms(const uint8_t* tile, uint8_t* atoms, int lane) {
-  const uint32_t* src = reinterpret_cast<const uint32_t*>(tile);
-  uint32_t* dst = reinterpret_cast<uint32_t*>(atoms);
+// One lane quarter of a stage's MMA scales in tensor memory (the warp with
+// that quarter, q = warp % 4): the scale tile of one operand holds, for each
+// of 128 rows R, 16 UE4M3 scales (four per MMA kk, K order); column 4 kk + c
+// of every lane l of every quarter holds the four scales of row (l % 32) +
+// 32 c for MMA kk -- the block-scaled MMA's layout for 128 rows, replicated in
+// each quarter.  Lane l reads rows l, l + 32, l + 64, l + 96 (16 bytes each).
+__device__ __forceinline__ void f4_scales_to_tmem(const uint8_t* tile, uint32_t taddr, int lane) {
+  uint32_t col[16];
 #pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    const int wsrc = lane + 32 * i;
-    const int R = wsrc >> 2, kk = wsrc & 3;
-    dst[kk * 128 + (R & 31) * 4 + (R >> 5)] = src[wsrc];
+  for (int c = 0; c < 4; ++c) {
+    const uint4 v = *reinterpret_cast<const uint4*>(tile + 16 * (lane + 32 * c));
+    col[c] = v.x;
+    col[4 + c] = v.y;
+    col[8 + c] = v.z;
+    col[12 + c] = v.w;
   }
+  tc::tmem_st16(taddr, col);
 }
 
 // Tile t of the sequence every role walks: row blocks of 128 sorted rows,
@@ -897,9 +901,9 @@ __global__ void k_pf4_finish(const __grid_constant__ Pf4Params p) {
 // PHASE 1 (down): tile = (expert, 128 sorted rows, 128 output rows); the
 // epilogue scales each route's row by s_down * w and adds it into its token's
 // fp32 sum with bulk reductions at L2 (the route sum; see k_pf4_finish).
-// Roles: warp 0 issues the TMA copies; warps 2 and 3 turn each stage's
-// 128 x 16-byte scale tiles into the MMA's scale atoms; warp 1 copies the
-// atoms to tensor memory and issues the MMAs; warps 4..11 run the epilogue
+// Roles: warp 0 issues the TMA copies; warps 2..5 (one per tensor-memory
+// lane quarter) store each stage's scales from its 128 x 16-byte scale tiles
+// into tensor memory; warp 1 issues the MMAs; warps 6..13 run the epilogue
 // (two per tensor-memory lane quarter, each half of the tile's columns).
 // The accumulators are double-buffered, so a tile's epilogue overlaps the
 // next tile's MMAs.  One CTA per SM walks the tiles (blockIdx.x, +
@@ -915,8 +919,7 @@ __global__ void __launch_bounds__(kF4Threads, 1) k_pf4_gemm(const __grid_constan
   __shared__ int abort_flag;
   uint8_t* base = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   uint8_t* stages = base;
-  uint8_t* atoms = base + NS * kF4Stage;
-  uint8_t* ep = atoms + NS * kF4Atoms;                       // down: the epilogue rows
+  uint8_t* ep = base + NS * kF4Stage;                        // down: the epilogue rows
   int* soff = reinterpret_cast<int*>(ep + (PHASE == 1 ? 8 * 32 * kF4EpRow : 0));   // [E+1] first sorted row of each expert
   int* rbpre = soff + (p.E + 1);                             // [E+1] row blocks before each expert
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -933,7 +936,7 @@ __global__ void __launch_bounds__(kF4Threads, 1) k_pf4_gemm(const __grid_constan
   if (tid == 0) {
     for (int i = 0; i < NS; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&ready[i], 2);
+      mbar_init(&ready[i], 4);
       mbar_init(&empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -1010,8 +1013,9 @@ __global__ void __launch_bounds__(kF4Threads, 1) k_pf4_gemm(const __grid_constan
       for (int qn = q - NS < 0 ? 0 : q - NS; qn < q; ++qn)
         mbar_wait_spin(&full[qn % NS], (uint32_t)((qn / NS) & 1), kSpinLimit);
     }
-  } else if (warp == 2 || warp == 3) {
-    // ---- scale atoms: warp 2 those of the x / intermediate rows, warp 3 those of the weight rows
+  } else if (warp >= 2 && warp <= 5) {
+    // ---- scales: this warp's lane quarter of both operands' scale columns
+    const uint32_t tq = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + 256u;
     int ecur = 0, q = 0;
     F4Tile tl;
     for (int t = blockIdx.x; !*abort && f4_tile(t, ncb, rbpre, soff, E, ecur, tl); t += gridDim.x) {
@@ -1022,10 +1026,11 @@ __global__ void __launch_bounds__(kF4Threads, 1) k_pf4_gemm(const __grid_constan
           ok = false;
           break;
         }
-        const int op = warp - 2;
-        f4_scale_atoms(stages + (size_t)s * kF4Stage + op * kF4Op + kF4Code, atoms + (size_t)s * kF4Atoms + op * kF4Scale,
-                       lane);
-        fence_proxy_async_smem();
+        const uint8_t* st = stages + (size_t)s * kF4Stage;
+        f4_scales_to_tmem(st + kF4Code, tq + (uint32_t)(s * 32), lane);
+        f4_scales_to_tmem(st + kF4Op + kF4Code, tq + (uint32_t)(s * 32 + 16), lane);
+        tc::tmem_st_wait();
+        tc::fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(&ready[s]);
       }
@@ -1048,23 +1053,17 @@ __global__ void __launch_bounds__(kF4Threads, 1) k_pf4_gemm(const __grid_constan
           break;
         }
         if (lane == 0) {
-          // the copies are complete (the atom warps saw it); this acquire
+          // the copies are complete (the scale warps saw it); this acquire
           // orders them for this thread's MMAs as well
           mbar_try_wait(&full[s], (uint32_t)((q / NS) & 1));
           tc::fence_after_sync();
           const uint32_t st = smem_addr(stages + (size_t)s * kF4Stage);
-          const uint32_t at = smem_addr(atoms + (size_t)s * kF4Atoms);
-          const uint32_t sf = tmem + 256 + (uint32_t)(s * 32);
-#pragma unroll
-          for (int op = 0; op < 2; ++op)
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              tc::tmem_cp_32x128b_x4(sf + op * 16 + 4 * kk, tc::desc_plain(at + op * kF4Scale + kk * 512, 128));
+          const uint32_t sf = tmem + 256 + (uint32_t)(s * 32);   // the scale warps' columns of this stage
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
             tc::mma_mxf4nvf4(tmem + 128 * buf, tc::desc_sw128(st + 32 * kk), tc::desc_sw128(st + kF4Op + 32 * kk), idesc,
                              sf + 4 * kk, sf + 16 + 4 * kk, (kc > 0 || kk > 0) ? 1u : 0u);
-          tc::mma_commit(&empty[s]);   // the stage's smem, atoms and scale columns are free once these MMAs are done
+          tc::mma_commit(&empty[s]);   // the stage's smem and scale columns are free once these MMAs are done
         }
         __syncwarp();
       }
@@ -1076,12 +1075,12 @@ __global__ void __launch_bounds__(kF4Threads, 1) k_pf4_gemm(const __grid_constan
       tc::mma_commit(&drain);   // everything this thread issued is complete before the dealloc
       mbar_wait_spin(&drain, 0u, kSpinLimit);
     }
-  } else if (warp >= 4) {
+  } else if (warp >= 6) {
     // ---- epilogue: warp w reads tensor-memory lanes 32 * (w % 4) .. + 31 (one tile row a
     // thread) and half hh of the tile's columns
-    const int qd = warp & 3, hh = (warp - 4) >> 2;
+    const int qd = warp & 3, hh = (warp - 6) >> 2;
     const int rbi = p.I / 2 + p.I / 16;
-    float* mine = reinterpret_cast<float*>(ep + (size_t)((warp - 4) * 32 + lane) * kF4EpRow);   // down: this row's 64 outputs
+    float* mine = reinterpret_cast<float*>(ep + (size_t)((warp - 6) * 32 + lane) * kF4EpRow);   // down: this row's 64 outputs
     int ecur = 0, ntile = 0;
     F4Tile tl;
     for (int t = blockIdx.x; !*abort && f4_tile(t, ncb, rbpre, soff, E, ecur, tl); t += gridDim.x, ++ntile) {
@@ -1164,7 +1163,7 @@ __global__ void __launch_bounds__(kF4Threads, 1) k_pf4_gemm(const __grid_constan
 
 template <int PHASE>
 size_t pf4_smem(int E) {
-  return 1024 + (size_t)F4Cfg<PHASE>::NS * (kF4Stage + kF4Atoms) + (PHASE == 1 ? 8 * 32 * kF4EpRow : 0) +
+  return 1024 + (size_t)F4Cfg<PHASE>::NS * kF4Stage + (PHASE == 1 ? 8 * 32 * kF4EpRow : 0) +
          8 * ((size_t)E + 1);
 }
 

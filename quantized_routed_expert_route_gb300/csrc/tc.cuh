@@ -93,7 +93,8 @@ __device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t sdes
 // N) = 128 rows: four tensor-memory columns from sfa/sfb; column c of lane l
 // holds the four scales (bytes, K order) of row (l % 32) + 32 c, the same in
 // every lane quarter -- one 512-byte shared-memory atom (line r: rows r,
-// r+32, r+64, r+96, four bytes each) copied by tmem_cp_32x128b_x4.
+// r+32, r+64, r+96, four bytes each) copied by tmem_cp_32x128b_x4, or the
+// same words stored by each lane quarter's warp with tmem_st16.
 __device__ __forceinline__ void mma_mxf4nvf4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                             uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
   asm volatile(
@@ -161,6 +162,18 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
       : "r"(taddr));
 }
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Sixteen consecutive 32-bit columns of this thread's tensor-memory lane <- r
+// (warp w writes lanes 32 * (w % 4) .. + 31; taddr carries that lane base).
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+      ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+// This thread's tensor-memory stores are complete.
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // Eight E2M1 codes (one 32-bit word, element 2i in the low nibble of byte i)
 // -> eight fp16 values as four f16x2 words (exact).
