@@ -776,7 +776,7 @@ constexpr int kF4Scale = 2048;     // its scales: 128 rows x 16 bytes
 constexpr int kF4Op = kF4Code + kF4Scale;
 constexpr int kF4Stage = 2 * kF4Op;     // the activation rows' operand, then the weight rows'
 constexpr int kF4GuCols = 64;           // intermediate columns of one gate_up tile (64 gate + 64 up rows)
-constexpr int kF4EpRow = 272;           // down epilogue: one row's 64 fp32 outputs, padded to spread banks
+constexpr int kF4EpRow = 528;           // down epilogue: one row's 128 fp32 outputs, padded to spread banks
 
 template <int PHASE>
 struct F4Cfg {
@@ -903,8 +903,10 @@ __global__ void k_pf4_finish(const __grid_constant__ Pf4Params p) {
 // fp32 sum with bulk reductions at L2 (the route sum; see k_pf4_finish).
 // Roles: warp 0 issues the TMA copies; warps 2..5 (one per tensor-memory
 // lane quarter) store each stage's scales from its 128 x 16-byte scale tiles
-// into tensor memory; warp 1 issues the MMAs; warps 6..13 run the epilogue
-// (two per tensor-memory lane quarter, each half of the tile's columns).
+// into tensor memory; warp 1 issues the MMAs; the epilogue runs on warps
+// 6..13 for gate_up (two per tensor-memory lane quarter, each half of the
+// tile's columns) and on warps 6..9 for down (one per quarter, whole rows, so
+// that each route row is one 512-byte reduction).
 // The accumulators are double-buffered, so a tile's epilogue overlaps the
 // next tile's MMAs.  One CTA per SM walks the tiles (blockIdx.x, +
 // gridDim.x, ...).  Every product of two scaled E2M1 values is exact in
@@ -920,7 +922,7 @@ __global__ void __launch_bounds__(kF4Threads, 1) k_pf4_gemm(const __grid_constan
   uint8_t* base = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   uint8_t* stages = base;
   uint8_t* ep = base + NS * kF4Stage;                        // down: the epilogue rows
-  int* soff = reinterpret_cast<int*>(ep + (PHASE == 1 ? 8 * 32 * kF4EpRow : 0));   // [E+1] first sorted row of each expert
+  int* soff = reinterpret_cast<int*>(ep + (PHASE == 1 ? 128 * kF4EpRow : 0));   // [E+1] first sorted row of each expert
   int* rbpre = soff + (p.E + 1);                             // [E+1] row blocks before each expert
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int E = p.E;
@@ -941,7 +943,7 @@ __global__ void __launch_bounds__(kF4Threads, 1) k_pf4_gemm(const __grid_constan
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&acc_full[i], 1);
-      mbar_init(&acc_empty[i], 256);
+      mbar_init(&acc_empty[i], PHASE == 0 ? 256 : 128);   // the epilogue threads that read a buffer
     }
     mbar_init(&drain, 1);
     fence_mbar_init();
@@ -1075,12 +1077,12 @@ __global__ void __launch_bounds__(kF4Threads, 1) k_pf4_gemm(const __grid_constan
       tc::mma_commit(&drain);   // everything this thread issued is complete before the dealloc
       mbar_wait_spin(&drain, 0u, kSpinLimit);
     }
-  } else if (warp >= 6) {
+  } else if (warp >= 6 && (PHASE == 0 || warp < 10)) {
     // ---- epilogue: warp w reads tensor-memory lanes 32 * (w % 4) .. + 31 (one tile row a
     // thread) and half hh of the tile's columns
     const int qd = warp & 3, hh = (warp - 6) >> 2;
     const int rbi = p.I / 2 + p.I / 16;
-    float* mine = reinterpret_cast<float*>(ep + (size_t)((warp - 6) * 32 + lane) * kF4EpRow);   // down: this row's 64 outputs
+    float* mine = reinterpret_cast<float*>(ep + (size_t)(32 * qd + lane) * kF4EpRow);   // down: this row's 128 outputs
     int ecur = 0, ntile = 0;
     F4Tile tl;
     for (int t = blockIdx.x; !*abort && f4_tile(t, ncb, rbpre, soff, E, ecur, tl); t += gridDim.x, ++ntile) {
@@ -1131,23 +1133,23 @@ __global__ void __launch_bounds__(kF4Threads, 1) k_pf4_gemm(const __grid_constan
         const float f = valid ? sd * __ldg(p.w + r) : 0.f;
         bulk_wait_read();   // the previous tile's reduction has read this row
 #pragma unroll
-        for (int j2 = 0; j2 < 2; ++j2) {
+        for (int j4 = 0; j4 < 4; ++j4) {
           uint32_t v[32];
-          tc::tmem_ld32(tq + 64 * hh + 32 * j2, v);
+          tc::tmem_ld32(tq + 32 * j4, v);
           tc::tmem_ld_wait();
-          if (j2 == 1) {
+          if (j4 == 3) {
             tc::fence_before_sync();
             mbar_arrive(&acc_empty[buf]);
           }
 #pragma unroll
           for (int i = 0; i < 32; i += 4)
-            *reinterpret_cast<float4*>(mine + 32 * j2 + i) =
+            *reinterpret_cast<float4*>(mine + 32 * j4 + i) =
                 make_float4(__uint_as_float(v[i]) * f, __uint_as_float(v[i + 1]) * f, __uint_as_float(v[i + 2]) * f,
                             __uint_as_float(v[i + 3]) * f);
         }
         if (valid) {
           fence_proxy_async_smem();
-          bulk_reduce_add_f32(p.y + (size_t)(r / p.K) * p.H + 128 * tl.cb + 64 * hh, mine, 256);
+          bulk_reduce_add_f32(p.y + (size_t)(r / p.K) * p.H + 128 * tl.cb, mine, 512);
           bulk_commit();
         }
       }
@@ -1163,7 +1165,7 @@ __global__ void __launch_bounds__(kF4Threads, 1) k_pf4_gemm(const __grid_constan
 
 template <int PHASE>
 size_t pf4_smem(int E) {
-  return 1024 + (size_t)F4Cfg<PHASE>::NS * kF4Stage + (PHASE == 1 ? 8 * 32 * kF4EpRow : 0) +
+  return 1024 + (size_t)F4Cfg<PHASE>::NS * kF4Stage + (PHASE == 1 ? 128 * kF4EpRow : 0) +
          8 * ((size_t)E + 1);
 }
 
