@@ -804,7 +804,7 @@ int moe_debug_block_dots(int32_t type, const void* rows, int32_t nrows, int32_t 
 namespace {
 
 struct PfLayout {
-  size_t err, off, perm, bcnt, xq, x16, x16lo, i16, y, xs, in4, total;
+  size_t err, off, perm, bcnt, inv, xq, x16, x16lo, i16, y, xs, in4, total;
 };
 
 // fp4: W4A4 on the FP4 tensor cores (the bank has its TMA maps): no fp16
@@ -818,6 +818,7 @@ PfLayout pf_layout(const moe_layer_geom& g, int64_t T, int mode, bool fp4) {
   L.off = o; o = align_up(o + 4 * ((size_t)g.E + 1), A);
   L.perm = o; o = align_up(o + 4 * RT, A);
   L.bcnt = o; o = align_up(o + 4 * (size_t)kSortBlocks * g.E, A);
+  L.inv = o; o = align_up(o + (fp4 ? 4 * RT : 0), A);
   L.xq = o;
   o = align_up(o + (mode == PF_W4A4 ? (size_t)T * (g.H / 2 + g.H / 16)
                     : mode == PF_W4A8 ? (size_t)T * (g.H / 32) * 36 : 0), A);
@@ -889,6 +890,12 @@ static int prefill_impl(const moe_bank* b, const void* x, int32_t T, const int32
   p.y = reinterpret_cast<float*>(base + L.y);
   // W4A4 runs on the block-scaled FP4 tensor cores when the bank has its TMA maps
   if (pf_fp4(b, mode)) {
+    // the FP4 GEMMs number their tiles in int: (row blocks) x (column blocks) stays below 2^31
+    const long long rbmax = (long long)T * g.top_k / 128 + g.E;
+    const long long cbmax = g.I / 64 > g.H / 128 ? g.I / 64 : g.H / 128;
+    if (rbmax * cbmax >= (1LL << 31)) return MOE_EUNSUPPORTED;
+    p.inv = reinterpret_cast<int*>(base + L.inv);
+    p.xs = base + L.xs;
     Pf4Params q;
     std::memset(&q, 0, sizeof(q));
     // gate_up weight boxes of 64 rows (the tile's gate and up halves), down of 128

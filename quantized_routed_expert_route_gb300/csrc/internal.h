@@ -78,16 +78,19 @@ struct PfParams {
   int* off;                 // [E+1] first sorted row of each expert; off[E] = valid routes
   int* perm;                // [RT]  route index of each sorted row
   int* bcnt;                // [kSortBlocks][E] the sort's per-block expert counts
+  int* inv;                 // [RT]  W4A4 on the FP4 tensor cores: sorted row of each route (-1: invalid id), else null
+  uint8_t* xs;              // [RT][H/2 + H/16] W4A4 on the FP4 tensor cores: NVFP4 x by sorted row, else null
   uint8_t* xq;              // quantized x: NVFP4 rows [T][H/2 + H/16] (W4A4) or q8_1 blocks [T][H/32][36] (W4A8)
   uint16_t* x16;            // fp16 [T][H]: the dequantized quantized x (the gate_up A operand)
   uint16_t* x16lo;          // fp16 [T][H], W4A8 only: q*d - x16 (x16 + x16lo carries q*d to ~2^-22)
   uint16_t* i16;            // fp16 [RT][I]: the dequantized requantized intermediate, sorted rows
   float* y;                 // fp32 [RT][H]: down output of each route times s_down * w, by route index
+                            // (W4A4 on the FP4 tensor cores: fp32 [T][H] token sums, zeroed by k_pf_quant)
 };
 
 // The W4A4 prompt path on the block-scaled FP4 tensor cores (prefill.cu):
-// x quantized to NVFP4 per token (k_pf_quant), its rows gathered in sorted
-// route order, then two grouped GEMMs (tcgen05 kind::mxf4nvf4, both operands
+// x quantized to NVFP4 per token and written to every sorted row of its
+// routes (k_pf_quant), then two grouped GEMMs (tcgen05 kind::mxf4nvf4, both operands
 // fed by 2-D TMA, per-16 UE4M3 scales in tensor memory); the down GEMM adds
 // each route's scaled row into its token's fp32 sum by bulk reductions at L2,
 // and one pass rounds the sums to bf16.  NVFP4 rows are codes (K/2 bytes)

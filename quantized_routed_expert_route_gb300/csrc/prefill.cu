@@ -34,8 +34,8 @@
 //                 in route order, no atomics.
 //
 // W4A4 on a bank with the grouped TMA maps runs on the block-scaled FP4
-// tensor cores instead (no fp16 operands): k_pf4_gather lays x's NVFP4 rows
-// out in sorted order and zeroes the fp32 token sums; k_pf4_gemm<0> (P3) and
+// tensor cores instead (no fp16 operands): k_pf_quant also writes x's NVFP4
+// rows in sorted order and zeroes the fp32 token sums; k_pf4_gemm<0> (P3) and
 // k_pf4_gemm<1> (P4) are tcgen05 kind::mxf4nvf4 GEMMs, the second adding each
 // route's scaled row into its token's sum by bulk reductions at L2 (P6 in
 // completion order); k_pf4_finish rounds the sums to bf16.
@@ -309,8 +309,12 @@ __global__ void __launch_bounds__(kSortThreads) k_pf_scatter(const __grid_consta
   bool bad = false;
   for (int r = r0 + lane; r < r1; r += 32) {
     const int e = __ldg(p.ids + r);
-    if (e >= 0 && e < E) atomicAdd(&cnt[w * E + e], 1);
-    else bad = true;
+    if (e >= 0 && e < E) {
+      atomicAdd(&cnt[w * E + e], 1);
+    } else {
+      bad = true;
+      if (p.inv) p.inv[r] = -1;
+    }
   }
   __syncthreads();
   for (int e = tid; e < E; e += kSortThreads) {
@@ -328,7 +332,10 @@ __global__ void __launch_bounds__(kSortThreads) k_pf_scatter(const __grid_consta
     const bool v = r < r1 && e >= 0 && e < E;
     const unsigned peers = __match_any_sync(0xffffffffu, v ? e : -1 - lane);
     const int rank = __popc(peers & ((1u << lane) - 1u));
-    if (v) p.perm[cnt[w * E + e] + rank] = r;
+    if (v) {
+      p.perm[cnt[w * E + e] + rank] = r;
+      if (p.inv) p.inv[r] = cnt[w * E + e] + rank;
+    }
     __syncwarp();
     if (v && rank == 0) cnt[w * E + e] += __popc(peers);
     __syncwarp();
@@ -447,6 +454,19 @@ __global__ void k_pf_quant(const __grid_constant__ PfParams p) {
     const size_t rbx = (size_t)p.H / 2 + p.H / 16;
     *reinterpret_cast<uint2*>(p.xq + (size_t)t * rbx + 8 * b) = make_uint2(c0, c1);
     p.xq[(size_t)t * rbx + p.H / 2 + b] = (uint8_t)sbyte;
+    if (p.xs) {
+      // the FP4 tensor-core GEMMs: this token's row at every sorted row of
+      // its valid routes, and its fp32 token sums zeroed for the down GEMM
+      for (int k = 0; k < p.K; ++k) {
+        const int row = __ldg(p.inv + (size_t)t * p.K + k);
+        if (row < 0) continue;
+        *reinterpret_cast<uint2*>(p.xs + (size_t)row * rbx + 8 * b) = make_uint2(c0, c1);
+        p.xs[(size_t)row * rbx + p.H / 2 + b] = (uint8_t)sbyte;
+      }
+      float4* ys = reinterpret_cast<float4*>(p.y + (size_t)t * p.H + 16 * b);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) ys[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
     if (p.x16) {   // the fp16 operand of the kind::f16 GEMMs (not used on the FP4 tensor cores)
       uint4* dst = reinterpret_cast<uint4*>(p.x16 + (size_t)t * p.H + 16 * b);
       dst[0] = make_uint4(h[0], h[1], h[2], h[3]);
@@ -783,18 +803,27 @@ struct F4Cfg {
   static constexpr int NS = PHASE == 0 ? 6 : 4;   // stages; tensor memory: 256 accumulator + NS * 32 scale columns
 };
 
-__device__ __forceinline__ void f4_tma(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+// 2-D TMA load of one box at (x, y) with an L2 cache policy (weights: evict
+// first, so that the activations and the token sums stay in L2).
+__device__ __forceinline__ void f4_tma(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar, uint64_t pol) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
-      ::"r"(smem_addr(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;"
+      ::"r"(smem_addr(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar)), "l"(pol)
       : "memory");
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
 }
 
 // out[0 .. bytes/4) += the fp32 values at src, as one asynchronous bulk
-// reduction performed at L2 (16-byte aligned addresses, bytes a multiple of 16).
-__device__ __forceinline__ void bulk_reduce_add_f32(float* out, const void* src, uint32_t bytes) {
-  asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;"
-               ::"l"(out), "r"(smem_addr(src)), "r"(bytes) : "memory");
+// reduction performed at L2 (16-byte aligned addresses, bytes a multiple of
+// 16), with an L2 cache policy for the destination lines.
+__device__ __forceinline__ void bulk_reduce_add_f32(float* out, const void* src, uint32_t bytes, uint64_t pol) {
+  asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.L2::cache_hint.add.f32 [%0], [%1], %2, %3;"
+               ::"l"(out), "r"(smem_addr(src)), "r"(bytes), "l"(pol) : "memory");
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // this thread's bulk operations have read their shared-memory sources
@@ -860,22 +889,6 @@ __device__ __forceinline__ bool f4_tile(int t, int ncb, const int* rbpre, const 
 }
 
 }  // namespace
-
-// NVFP4 rows of x in sorted route order: sorted row i is token perm[i] / K's
-// row of k_pf_quant, 16 bytes a thread.  Rows past the valid routes stay
-// unwritten (the GEMMs never use them as valid rows).  The same launch zeroes
-// the fp32 token sums the down GEMM adds into.
-__global__ void k_pf4_gather(const __grid_constant__ Pf4Params p) {
-  const int rb = p.H / 2 + p.H / 16, nch = rb / 16;
-  const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  if (idx < (long long)p.T * (p.H / 4)) reinterpret_cast<float4*>(p.y)[idx] = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (idx >= (long long)p.RT * nch) return;
-  const int i = (int)(idx / nch), c = (int)(idx - (long long)i * nch);
-  if (i >= p.off[p.E]) return;
-  const int t = p.perm[i] / p.K;
-  *reinterpret_cast<uint4*>(p.xs + (size_t)i * rb + 16 * c) =
-      __ldg(reinterpret_cast<const uint4*>(p.xq + (size_t)t * rb + 16 * c));
-}
 
 // out[t] = bf16 of the fp32 token sum (round to nearest even), four values a thread.
 __global__ void k_pf4_finish(const __grid_constant__ Pf4Params p) {
@@ -982,6 +995,7 @@ __global__ void __launch_bounds__(kF4Threads, 1) k_pf4_gemm(const __grid_constan
       const CUtensorMap* mas = PHASE == 0 ? &p.map_xss : &p.map_ins;
       const CUtensorMap* mb = PHASE == 0 ? &p.map_wgu : &p.map_wdn;
       const CUtensorMap* mbs = PHASE == 0 ? &p.map_wgus : &p.map_wdns;
+      const uint64_t pw = l2_policy_evict_first(), pa = l2_policy_evict_last();
       int ecur = 0, q = 0;
       F4Tile tl;
       for (int t = blockIdx.x; !*abort && f4_tile(t, ncb, rbpre, soff, E, ecur, tl); t += gridDim.x) {
@@ -997,16 +1011,16 @@ __global__ void __launch_bounds__(kF4Threads, 1) k_pf4_gemm(const __grid_constan
           uint8_t* st = stages + (size_t)s * kF4Stage;
           uint8_t* sb = st + kF4Op;
           mbar_arrive_expect_tx(&full[s], (uint32_t)kF4Stage);
-          f4_tma(st, ma, 128 * kc, tl.row0, &full[s]);
-          f4_tma(st + kF4Code, mas, Kd / 2 + 16 * kc, tl.row0, &full[s]);
+          f4_tma(st, ma, 128 * kc, tl.row0, &full[s], pa);
+          f4_tma(st + kF4Code, mas, Kd / 2 + 16 * kc, tl.row0, &full[s], pa);
           if (PHASE == 0) {
-            f4_tma(sb, mb, 128 * kc, yb, &full[s]);
-            f4_tma(sb + kF4Code / 2, mb, 128 * kc, yb + p.I, &full[s]);
-            f4_tma(sb + kF4Code, mbs, Kd / 2 + 16 * kc, yb, &full[s]);
-            f4_tma(sb + kF4Code + kF4Scale / 2, mbs, Kd / 2 + 16 * kc, yb + p.I, &full[s]);
+            f4_tma(sb, mb, 128 * kc, yb, &full[s], pw);
+            f4_tma(sb + kF4Code / 2, mb, 128 * kc, yb + p.I, &full[s], pw);
+            f4_tma(sb + kF4Code, mbs, Kd / 2 + 16 * kc, yb, &full[s], pw);
+            f4_tma(sb + kF4Code + kF4Scale / 2, mbs, Kd / 2 + 16 * kc, yb + p.I, &full[s], pw);
           } else {
-            f4_tma(sb, mb, 128 * kc, yb, &full[s]);
-            f4_tma(sb + kF4Code, mbs, Kd / 2 + 16 * kc, yb, &full[s]);
+            f4_tma(sb, mb, 128 * kc, yb, &full[s], pw);
+            f4_tma(sb + kF4Code, mbs, Kd / 2 + 16 * kc, yb, &full[s], pw);
           }
         }
         if (!ok) break;
@@ -1083,6 +1097,7 @@ __global__ void __launch_bounds__(kF4Threads, 1) k_pf4_gemm(const __grid_constan
     const int qd = warp & 3, hh = (warp - 6) >> 2;
     const int rbi = p.I / 2 + p.I / 16;
     float* mine = reinterpret_cast<float*>(ep + (size_t)(32 * qd + lane) * kF4EpRow);   // down: this row's 128 outputs
+    const uint64_t pkeep = l2_policy_evict_last();   // the token sums stay in L2 for k_pf4_finish
     int ecur = 0, ntile = 0;
     F4Tile tl;
     for (int t = blockIdx.x; !*abort && f4_tile(t, ncb, rbpre, soff, E, ecur, tl); t += gridDim.x, ++ntile) {
@@ -1149,7 +1164,7 @@ __global__ void __launch_bounds__(kF4Threads, 1) k_pf4_gemm(const __grid_constan
         }
         if (valid) {
           fence_proxy_async_smem();
-          bulk_reduce_add_f32(p.y + (size_t)(r / p.K) * p.H + 128 * tl.cb, mine, 512);
+          bulk_reduce_add_f32(p.y + (size_t)(r / p.K) * p.H + 128 * tl.cb, mine, 512, pkeep);
           bulk_commit();
         }
       }
@@ -1216,12 +1231,6 @@ cudaError_t launch_prefill(const PfParams& p, cudaStream_t stream, const Pf4Para
 cudaError_t launch_prefill_fp4(const Pf4Params& q, cudaStream_t stream) {
   cudaError_t e;
   const long long nsum = (long long)q.T * (q.H / 4);   // float4s of the fp32 token sums
-  {
-    long long n = (long long)q.RT * ((q.H / 2 + q.H / 16) / 16);
-    if (n < nsum) n = nsum;
-    k_pf4_gather<<<(unsigned)((n + 255) / 256), 256, 0, stream>>>(q);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  }
   const size_t s0 = pf4_smem<0>(q.E), s1 = pf4_smem<1>(q.E);
   if ((e = cudaFuncSetAttribute(k_pf4_gemm<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s0)) != cudaSuccess)
     return e;
