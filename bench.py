@@ -407,7 +407,7 @@ def bench_prefill(dev, steps, warmup, mode, bf16_peak):
                            "operands by 2-D TMA",
                     "peak_tflops": bf16_peak * 6.0, "peak_kind": "measured bf16 x 6 (nominal FP4/BF16 ratio)",
                     "frac_of_fp4_peak": tflops / (bf16_peak * 6.0), "frac_of_nominal_fp4_peak": tflops / 13500.0,
-                    "launches_per_chunk": 7})
+                    "launches_per_chunk": 6})
     else:
         res.update({"mma": "tcgen05 kind::f16 (exact fp16 operands, fp32 accumulation)",
                     "frac_of_measured_bf16_peak": tflops / bf16_peak, "frac_of_nominal_fp4_peak": tflops / 13500.0,

@@ -803,8 +803,9 @@ struct F4Cfg {
   static constexpr int NS = PHASE == 0 ? 6 : 4;   // stages; tensor memory: 256 accumulator + NS * 32 scale columns
 };
 
-// 2-D TMA load of one box at (x, y) with an L2 cache policy (weights: evict
-// first, so that the activations and the token sums stay in L2).
+// 2-D TMA load of one box at (x, y) with an L2 cache policy (the activation
+// rows and the token sums evict last, the weights normally: a weight tile is
+// read again by the expert's other row blocks soon after).
 __device__ __forceinline__ void f4_tma(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar, uint64_t pol) {
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
@@ -815,6 +816,11 @@ __device__ __forceinline__ void f4_tma(void* dst, const CUtensorMap* map, int x,
 __device__ __forceinline__ uint64_t l2_policy_evict_last() {
   uint64_t pol;
   asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_normal() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
   return pol;
 }
 
@@ -995,7 +1001,7 @@ __global__ void __launch_bounds__(kF4Threads, 1) k_pf4_gemm(const __grid_constan
       const CUtensorMap* mas = PHASE == 0 ? &p.map_xss : &p.map_ins;
       const CUtensorMap* mb = PHASE == 0 ? &p.map_wgu : &p.map_wdn;
       const CUtensorMap* mbs = PHASE == 0 ? &p.map_wgus : &p.map_wdns;
-      const uint64_t pw = l2_policy_evict_first(), pa = l2_policy_evict_last();
+      const uint64_t pw = l2_policy_evict_normal(), pa = l2_policy_evict_last();
       int ecur = 0, q = 0;
       F4Tile tl;
       for (int t = blockIdx.x; !*abort && f4_tile(t, ncb, rbpre, soff, E, ecur, tl); t += gridDim.x) {
