@@ -398,10 +398,11 @@ def bench_prefill(dev, steps, warmup, mode, bf16_peak):
     # algorithmic bytes: both banks once, x in and the bf16 output, ids and weights
     alg = E * 2 * I * rb_gu + E * H * rb_dn + 2 * T * H * 2 + 8 * T * K
     hbm_peak, _ = peaks()
-    res = {"mode": {0: "W4A4", 1: "W4A8", 2: "FP16"}[mode], "ms_per_chunk": ms, "tok_per_s": T / (ms / 1e3),
+    res = {"mode": {0: "W4A4", 1: "W4A8", 2: "FP16", 3: "W4A4 (fixed-order route sum)"}[mode], "ms_per_chunk": ms,
+           "tok_per_s": T / (ms / 1e3),
            "tflops": tflops, "alg_bytes": alg, "hbm_gbs": alg / (ms / 1e3) / 1e9,
            "hbm_frac": alg / (ms / 1e3) / 1e9 / hbm_peak, "device_error_bits": err}
-    if mode == 0:
+    if mode in (0, 3):
         # the FP4 peak: the measured bf16 peak times the nominal FP4 / BF16 ratio (13.5 / 2.25)
         res.update({"mma": "tcgen05 kind::mxf4nvf4 block-scaled FP4 (E2M1 x E2M1, UE4M3 per 16, fp32 accumulation), "
                            "operands by 2-D TMA",
@@ -665,8 +666,8 @@ def summary_of(line: dict) -> dict:
                                      for k, v in ex["gguf_types_24_layer_stack"].items() if k != "workload"}
     if "prefill_4096_token_chunk" in ex:
         pf = ex["prefill_4096_token_chunk"]
-        s["prefill_chunk_ms"] = {m: r3(pf[m]["ms_per_chunk"]) for m in ("w4a4", "w4a8", "fp16") if m in pf}
-        s["prefill_tflops"] = {m: r3(pf[m]["tflops"]) for m in ("w4a4", "w4a8", "fp16") if m in pf}
+        s["prefill_chunk_ms"] = {m: r3(pf[m]["ms_per_chunk"]) for m in ("w4a4", "w4a4_fixed", "w4a8", "fp16") if m in pf}
+        s["prefill_tflops"] = {m: r3(pf[m]["tflops"]) for m in ("w4a4", "w4a4_fixed", "w4a8", "fp16") if m in pf}
         if "w4a4" in pf:
             s["prefill_w4a4_frac_nominal_fp4"] = r3(pf["w4a4"].get("frac_of_nominal_fp4_peak"))
     if "dense_linear_nvfp4" in ex:
@@ -774,7 +775,7 @@ def main():
     ap.add_argument("--T", type=int, default=1)
     ap.add_argument("--experts", type=int, default=0,
                     help="with --profile-layer q4_k/bf16: experts per layer (default 256), to shrink a capture")
-    ap.add_argument("--profile-prefill", choices=["w4a4", "w4a8", "fp16"], default=None,
+    ap.add_argument("--profile-prefill", choices=["w4a4", "w4a4_fixed", "w4a8", "fp16"], default=None,
                     help="run --steps prompt-path chunks (for ncu), print nothing else")
     a = ap.parse_args()
 
@@ -783,7 +784,8 @@ def main():
         return
     if a.profile_prefill:
         import torch
-        r = bench_prefill("cuda:0", a.steps, 1, {"w4a4": 0, "w4a8": 1, "fp16": 2}[a.profile_prefill], bf16_peak()[0])
+        r = bench_prefill("cuda:0", a.steps, 1, {"w4a4": 0, "w4a8": 1, "fp16": 2, "w4a4_fixed": 3}[a.profile_prefill],
+                          bf16_peak()[0])
         print(json.dumps(r))
         return
 
@@ -913,6 +915,7 @@ def main():
             "workload": "nvfp4 layer H=2048 I=768 E=128 top-8, 4096 tokens (32768 routed rows)",
             "peak_tflops": pk, "peak_kind": pk_kind, "gflop_per_chunk": prefill_flops(PREFILL) / 1e9,
             "w4a4": bench_prefill(dev, max(3, min(20, a.steps // 20)), a.warmup, 0, pk),
+            "w4a4_fixed": bench_prefill(dev, max(3, min(20, a.steps // 20)), a.warmup, 3, pk),
             "w4a8": bench_prefill(dev, max(3, min(20, a.steps // 20)), a.warmup, 1, pk),
             "fp16": bench_prefill(dev, max(3, min(20, a.steps // 20)), a.warmup, 2, pk)}
         torch.cuda.empty_cache()

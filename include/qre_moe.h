@@ -236,7 +236,7 @@ int moe_decode_noalloc(const moe_bank* bank, const void* x, int32_t T,
  * quantized to NVFP4 on the fly, or FP16 with activations kept in fp16).
  * NVFP4 gate_up and down banks only, H and I multiples of 256; other banks
  * return MOE_EUNSUPPORTED. */
-enum { MOE_PREFILL_W4A4 = 0, MOE_PREFILL_W4A8 = 1, MOE_PREFILL_FP16 = 2 };
+enum { MOE_PREFILL_W4A4 = 0, MOE_PREFILL_W4A8 = 1, MOE_PREFILL_FP16 = 2, MOE_PREFILL_W4A4_FIXED = 3 };
 
 /* Workspace bytes moe_prefill_grouped needs for T tokens in `mode`; 0 if the
  * bank or mode is unsupported or T < 1. */
@@ -253,12 +253,14 @@ size_t moe_prefill_workspace_bytes(const moe_bank* bank, int32_t T, int32_t mode
  * GLU in an fp32 epilogue that requantizes the intermediate the same way as x
  * (FP16: rounds it to fp16); a grouped down GEMM whose epilogue scales by
  * s_down * routing weight; the route sum in fp32, rounded once to bf16.
- * W4A8 and FP16 (and W4A4 on a bank without the FP4 tensor-core layout) add
- * k = 0..K-1 in order, so repeated calls give identical bits; W4A4 on the
- * block-scaled FP4 tensor cores adds each route into its token's fp32 sum as
- * the down tiles finish (bulk reductions at L2), so the order of those K
- * additions, and with it the last fp32 bits of a sum, can differ between
- * calls (the error bound is the same for every order).
+ * W4A8, FP16 and MOE_PREFILL_W4A4_FIXED (W4A4 arithmetic, the same
+ * kernels up to the down epilogue) add k = 0..K-1 in order, so repeated
+ * calls give identical bits.  MOE_PREFILL_W4A4 on the block-scaled FP4
+ * tensor cores adds each route into its token's fp32 sum as the down tiles
+ * finish (bulk reductions at L2, no per-route fp32 rows in HBM), so the order
+ * of those K additions, and with it the last fp32 bits of a sum, can differ
+ * between calls (the error bound is the same for every order).  On a bank
+ * without the FP4 tensor-core layout both W4A4 modes take the fixed order.
  * x: bf16 [T, H] (device, 16-byte aligned); topk_ids int32 and topk_w fp32
  * [T, K] (device); out bf16 [T, H] (device, 8-byte aligned); ws: device,
  * 256-byte aligned, >= moe_prefill_workspace_bytes(bank, T, mode) bytes (no

@@ -18,7 +18,7 @@ MOE_OK, MOE_EINVAL, MOE_EUNSUPPORTED, MOE_ENOMEM, MOE_ECUDA, MOE_EDEVICE = 0, -1
 MOE_DEVERR_BAD_ID, MOE_DEVERR_TIMEOUT = 1, 2
 MOE_SRC_HOST, MOE_SRC_DEVICE, MOE_SRC_DEVICE_BORROW = 0, 1, 2
 MOE_MAX_E, MOE_MAX_TOPK, MOE_DECODE_T_CHUNK, MOE_LINEAR_MAX_T = 1024, 32, 64, 8
-MOE_PREFILL_W4A4, MOE_PREFILL_W4A8, MOE_PREFILL_FP16 = 0, 1, 2
+MOE_PREFILL_W4A4, MOE_PREFILL_W4A8, MOE_PREFILL_FP16, MOE_PREFILL_W4A4_FIXED = 0, 1, 2, 3
 MOE_GLU_SILU, MOE_GLU_GELU_TANH = 0, 1
 MOE_NOALLOC_WS_BYTES = 4 << 20
 MOE_DEBUG_WAIT_MAX = 64

@@ -808,8 +808,9 @@ struct PfLayout {
 };
 
 // fp4: W4A4 on the FP4 tensor cores (the bank has its TMA maps): no fp16
-// operands, and y holds one fp32 sum per token instead of one row per route.
-PfLayout pf_layout(const moe_layer_geom& g, int64_t T, int mode, bool fp4) {
+// operands, and y holds one fp32 sum per token instead of one row per route
+// unless the route sum takes the fixed order.
+PfLayout pf_layout(const moe_layer_geom& g, int64_t T, int mode, bool fp4, bool fixed) {
   PfLayout L;
   const size_t A = 256;
   const size_t RT = (size_t)T * g.top_k;
@@ -825,7 +826,7 @@ PfLayout pf_layout(const moe_layer_geom& g, int64_t T, int mode, bool fp4) {
   L.x16 = o; o = align_up(o + (fp4 ? 0 : 2 * (size_t)T * g.H), A);
   L.x16lo = o; o = align_up(o + (mode == PF_W4A8 ? 2 * (size_t)T * g.H : 0), A);
   L.i16 = o; o = align_up(o + 2 * RT * g.I, A);
-  L.y = o; o = align_up(o + 4 * (fp4 ? (size_t)T : RT) * g.H, A);
+  L.y = o; o = align_up(o + 4 * (fp4 && !fixed ? (size_t)T : RT) * g.H, A);
   // W4A4 on the FP4 tensor cores: NVFP4 rows of x and of the intermediate in sorted route order
   L.xs = L.in4 = 0;
   if (fp4) {
@@ -838,8 +839,18 @@ PfLayout pf_layout(const moe_layer_geom& g, int64_t T, int mode, bool fp4) {
 
 bool pf_fp4(const moe_bank* b, int32_t mode) { return mode == PF_W4A4 && b->grouped == kGroupedQuant; }
 
-int pf_check(const moe_bank* b, int32_t mode) {
-  if (!b || (mode != PF_W4A4 && mode != PF_W4A8 && mode != PF_FP16)) return MOE_EINVAL;
+// The public mode as the kernels' arithmetic mode and the route-sum order.
+bool pf_mode(int32_t pub, int& mode, bool& fixed) {
+  fixed = pub != MOE_PREFILL_W4A4;
+  mode = pub == MOE_PREFILL_W4A4_FIXED ? PF_W4A4 : pub;
+  return pub == MOE_PREFILL_W4A4 || pub == MOE_PREFILL_W4A8 || pub == MOE_PREFILL_FP16 ||
+         pub == MOE_PREFILL_W4A4_FIXED;
+}
+
+int pf_check(const moe_bank* b, int32_t pub) {
+  int mode;
+  bool fixed;
+  if (!b || !pf_mode(pub, mode, fixed)) return MOE_EINVAL;
   const moe_layer_geom& g = b->geom;
   if (g.gate_up_type != MOE_NVFP4 || g.down_type != MOE_NVFP4) return MOE_EUNSUPPORTED;
   if (g.H % 256 != 0 || g.I % 256 != 0) return MOE_EUNSUPPORTED;
@@ -851,13 +862,19 @@ int pf_check(const moe_bank* b, int32_t mode) {
 size_t moe_prefill_workspace_bytes(const moe_bank* b, int32_t T, int32_t mode) {
   if (pf_check(b, mode) != MOE_OK || T < 1) return 0;
   if ((int64_t)T * b->geom.top_k > (int64_t)(1 << 30)) return 0;
-  return pf_layout(b->geom, T, mode, pf_fp4(b, mode)).total;
+  int m;
+  bool fixed;
+  pf_mode(mode, m, fixed);
+  return pf_layout(b->geom, T, m, pf_fp4(b, m), fixed).total;
 }
 
-static int prefill_impl(const moe_bank* b, const void* x, int32_t T, const int32_t* ids, const float* w, int32_t mode,
+static int prefill_impl(const moe_bank* b, const void* x, int32_t T, const int32_t* ids, const float* w, int32_t pub,
                         void* out, void* ws, size_t ws_bytes, void* stream, bool export_i16) {
-  int st = pf_check(b, mode);
+  int st = pf_check(b, pub);
   if (st) return st;
+  int mode;
+  bool fixed;
+  pf_mode(pub, mode, fixed);
   if (T < 0) return MOE_EINVAL;
   if (T == 0) return MOE_OK;
   if (!x || !ids || !w || !out || !ws) return MOE_EINVAL;
@@ -865,7 +882,7 @@ static int prefill_impl(const moe_bank* b, const void* x, int32_t T, const int32
     return MOE_EINVAL;
   const moe_layer_geom& g = b->geom;
   if ((int64_t)T * g.top_k > (int64_t)(1 << 30)) return MOE_EINVAL;
-  const PfLayout L = pf_layout(g, T, mode, pf_fp4(b, mode));
+  const PfLayout L = pf_layout(g, T, mode, pf_fp4(b, mode), fixed);
   if (ws_bytes < L.total) return MOE_EINVAL;
   uint8_t* base = static_cast<uint8_t*>(ws);
   PfParams p;
@@ -896,6 +913,7 @@ static int prefill_impl(const moe_bank* b, const void* x, int32_t T, const int32
     if (rbmax * cbmax >= (1LL << 31)) return MOE_EUNSUPPORTED;
     p.inv = reinterpret_cast<int*>(base + L.inv);
     p.xs = base + L.xs;
+    p.ysum = fixed ? nullptr : p.y;
     Pf4Params q;
     std::memset(&q, 0, sizeof(q));
     // gate_up weight boxes of 64 rows (the tile's gate and up halves), down of 128
@@ -911,6 +929,7 @@ static int prefill_impl(const moe_bank* b, const void* x, int32_t T, const int32
     q.i16 = p.i16;
     q.y = p.y;
     q.out = p.out;
+    q.fixed = fixed ? 1 : 0;
     const uint64_t rbx = (uint64_t)(g.H / 2 + g.H / 16), rbi = (uint64_t)(g.I / 2 + g.I / 16);
     if (!map_byte_rows(&q.map_wgu, b->gu, (uint64_t)g.E * 2 * g.I, rbx, 128, 64, true) ||
         !map_byte_rows(&q.map_wgus, b->gu, (uint64_t)g.E * 2 * g.I, rbx, 16, 64) ||
@@ -940,7 +959,9 @@ int moe_debug_prefill_stages(const moe_bank* b, const void* x, int32_t T, const 
   int st = prefill_impl(b, x, T, ids, w, mode, out, ws, ws_bytes, stream, true);
   if (st || T == 0) return st;
   const moe_layer_geom& g = b->geom;
-  const PfLayout L = pf_layout(g, T, mode, pf_fp4(b, mode));
+  bool fixed;
+  pf_mode(mode, mode, fixed);
+  const PfLayout L = pf_layout(g, T, mode, pf_fp4(b, mode), fixed);
   const uint8_t* base = static_cast<const uint8_t*>(ws);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const size_t RT = (size_t)T * g.top_k;

@@ -80,6 +80,7 @@ struct PfParams {
   int* bcnt;                // [kSortBlocks][E] the sort's per-block expert counts
   int* inv;                 // [RT]  W4A4 on the FP4 tensor cores: sorted row of each route (-1: invalid id), else null
   uint8_t* xs;              // [RT][H/2 + H/16] W4A4 on the FP4 tensor cores: NVFP4 x by sorted row, else null
+  float* ysum;              // [T][H] fp32 token sums that k_pf_quant zeroes (FP4 tensor cores, completion-order sum), else null
   uint8_t* xq;              // quantized x: NVFP4 rows [T][H/2 + H/16] (W4A4) or q8_1 blocks [T][H/32][36] (W4A8)
   uint16_t* x16;            // fp16 [T][H]: the dequantized quantized x (the gate_up A operand)
   uint16_t* x16lo;          // fp16 [T][H], W4A8 only: q*d - x16 (x16 + x16lo carries q*d to ~2^-22)
@@ -114,7 +115,9 @@ struct Pf4Params {
   uint8_t* in4;                   // NVFP4 intermediate by sorted row [RT][I/2 + I/16]
   uint16_t* i16;                  // fp16 [RT][I] (export_i16 only)
   float* y;                       // fp32 [T][H]: each token's sum of its routes' scaled down outputs
+                                  // (fixed: fp32 [RT][H], each route's scaled down output by route index)
   uint16_t* out;                  // bf16 [T][H]
+  int fixed;                      // route sum in the order k = 0..K-1 (k_pf4_combine) instead of L2 reductions
 };
 
 // The dense path (decode_tc.cu): BF16 gate_up and down banks at batches the

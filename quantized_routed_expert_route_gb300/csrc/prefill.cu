@@ -38,7 +38,8 @@
 // rows in sorted order and zeroes the fp32 token sums; k_pf4_gemm<0> (P3) and
 // k_pf4_gemm<1> (P4) are tcgen05 kind::mxf4nvf4 GEMMs, the second adding each
 // route's scaled row into its token's sum by bulk reductions at L2 (P6 in
-// completion order); k_pf4_finish rounds the sums to bf16.
+// completion order); k_pf4_finish rounds the sums to bf16.  The fixed-order
+// mode stores each route's row instead and k_pf4_combine sums k = 0..K-1.
 //
 // Every product in the MMAs is of two exact fp16 values (NVFP4 code * scale,
 // or a q8_1 value rounded to fp16 once), accumulated in fp32.
@@ -456,16 +457,19 @@ __global__ void k_pf_quant(const __grid_constant__ PfParams p) {
     p.xq[(size_t)t * rbx + p.H / 2 + b] = (uint8_t)sbyte;
     if (p.xs) {
       // the FP4 tensor-core GEMMs: this token's row at every sorted row of
-      // its valid routes, and its fp32 token sums zeroed for the down GEMM
+      // its valid routes, and (completion-order route sum) its fp32 token
+      // sums zeroed for the down GEMM
       for (int k = 0; k < p.K; ++k) {
         const int row = __ldg(p.inv + (size_t)t * p.K + k);
         if (row < 0) continue;
         *reinterpret_cast<uint2*>(p.xs + (size_t)row * rbx + 8 * b) = make_uint2(c0, c1);
         p.xs[(size_t)row * rbx + p.H / 2 + b] = (uint8_t)sbyte;
       }
-      float4* ys = reinterpret_cast<float4*>(p.y + (size_t)t * p.H + 16 * b);
+      if (p.ysum) {
+        float4* ys = reinterpret_cast<float4*>(p.ysum + (size_t)t * p.H + 16 * b);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) ys[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int i = 0; i < 4; ++i) ys[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
     }
     if (p.x16) {   // the fp16 operand of the kind::f16 GEMMs (not used on the FP4 tensor cores)
       uint4* dst = reinterpret_cast<uint4*>(p.x16 + (size_t)t * p.H + 16 * b);
@@ -831,6 +835,12 @@ __device__ __forceinline__ void bulk_reduce_add_f32(float* out, const void* src,
   asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.L2::cache_hint.add.f32 [%0], [%1], %2, %3;"
                ::"l"(out), "r"(smem_addr(src)), "r"(bytes), "l"(pol) : "memory");
 }
+// out[0 .. bytes) = the bytes at src, as one asynchronous bulk copy (the same alignment rules).
+__device__ __forceinline__ void bulk_store(void* out, const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(out), "r"(smem_addr(src)),
+               "r"(bytes)
+               : "memory");
+}
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // this thread's bulk operations have read their shared-memory sources
 __device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
@@ -896,6 +906,11 @@ __device__ __forceinline__ bool f4_tile(int t, int ncb, const int* rbpre, const 
 
 }  // namespace
 
+// Fixed-order route sum: out[t] = bf16(sum over k = 0..K-1 of the route rows), four values a thread.
+__global__ void k_pf4_combine(const __grid_constant__ Pf4Params p) {
+  route_sum4(p.ids, p.y, p.out, p.T, p.K, p.E, p.H, (long long)blockIdx.x * blockDim.x + threadIdx.x);
+}
+
 // out[t] = bf16 of the fp32 token sum (round to nearest even), four values a thread.
 __global__ void k_pf4_finish(const __grid_constant__ Pf4Params p) {
   const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
@@ -919,7 +934,8 @@ __global__ void k_pf4_finish(const __grid_constant__ Pf4Params p) {
 // writing the sorted NVFP4 intermediate.
 // PHASE 1 (down): tile = (expert, 128 sorted rows, 128 output rows); the
 // epilogue scales each route's row by s_down * w and adds it into its token's
-// fp32 sum with bulk reductions at L2 (the route sum; see k_pf4_finish).
+// fp32 sum with bulk reductions at L2 (the route sum; see k_pf4_finish), or,
+// with p.fixed, stores it as the route's own fp32 row for k_pf4_combine.
 // Roles: warp 0 issues the TMA copies; warps 2..5 (one per tensor-memory
 // lane quarter) store each stage's scales from its 128 x 16-byte scale tiles
 // into tensor memory; warp 1 issues the MMAs; the epilogue runs on warps
@@ -1170,7 +1186,8 @@ __global__ void __launch_bounds__(kF4Threads, 1) k_pf4_gemm(const __grid_constan
         }
         if (valid) {
           fence_proxy_async_smem();
-          bulk_reduce_add_f32(p.y + (size_t)(r / p.K) * p.H + 128 * tl.cb, mine, 512, pkeep);
+          if (p.fixed) bulk_store(p.y + (size_t)r * p.H + 128 * tl.cb, mine, 512);   // the route's own row
+          else bulk_reduce_add_f32(p.y + (size_t)(r / p.K) * p.H + 128 * tl.cb, mine, 512, pkeep);
           bulk_commit();
         }
       }
@@ -1246,7 +1263,8 @@ cudaError_t launch_prefill_fp4(const Pf4Params& q, cudaStream_t stream) {
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   k_pf4_gemm<1><<<sm_count(), kF4Threads, s1, stream>>>(q);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  k_pf4_finish<<<(unsigned)((nsum + 255) / 256), 256, 0, stream>>>(q);
+  if (q.fixed) k_pf4_combine<<<(unsigned)((nsum + 255) / 256), 256, 0, stream>>>(q);
+  else k_pf4_finish<<<(unsigned)((nsum + 255) / 256), 256, 0, stream>>>(q);
   return cudaGetLastError();
 }
 

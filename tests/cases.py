@@ -155,7 +155,7 @@ def prefill_oracle(case: PrefillCase, mode: int, tokens=None):
     for e in routed:
         gu[e] = C.bank_bytes_np(case.seed * 31 + 5, g.gate_up_type, g.H, e * 2 * g.I, 2 * g.I)
         dn[e] = C.bank_bytes_np(case.seed * 31 + 6, g.down_type, g.I, e * g.H, g.H)
-    kind = {0: "nvfp4", 1: "q8_1", 2: "fp16"}[mode]
+    kind = {0: "nvfp4", 1: "q8_1", 2: "fp16", 3: "nvfp4"}[mode]   # 3: W4A4 arithmetic, fixed-order route sum
     return OL.moe_layer(g, gu, dn, case.sb, case.x[sel], case.ids[sel], case.w[sel], act_kind=kind, stages=True)
 
 
@@ -180,7 +180,8 @@ def run_prefill_gpu(case: PrefillCase, mode: int, stages=True):
     RT = T * g.top_k
     res = {}
     if stages:
-        xq_bytes = {0: T * (g.H // 2 + g.H // 16), 1: T * (g.H // 32) * 36, 2: 2 * T * g.H}[mode]
+        xq_bytes = {0: T * (g.H // 2 + g.H // 16), 1: T * (g.H // 32) * 36, 2: 2 * T * g.H,
+                    3: T * (g.H // 2 + g.H // 16)}[mode]
         xq = torch.zeros(xq_bytes, dtype=torch.uint8, device=dev)
         off = torch.zeros(g.E + 1, dtype=torch.int32, device=dev)
         perm = torch.zeros(RT, dtype=torch.int32, device=dev)
