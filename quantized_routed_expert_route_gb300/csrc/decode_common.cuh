@@ -280,7 +280,7 @@ __device__ inline void group_routes_small_warp(const int32_t* ids, int RT, int E
   const unsigned peers = __match_any_sync(0xffffffffu, key);
   const bool first = valid && (lane == __ffs(peers) - 1);
   int slot = 0, off = 0;
-  for (int j = 0; j < 32; ++j) {
+  for (int j = 0; j < RT; ++j) {   // lanes >= RT hold no route
     const int ej = __shfl_sync(0xffffffffu, key, j);
     const int fj = __shfl_sync(0xffffffffu, first ? 1 : 0, j);
     const unsigned pj = __shfl_sync(0xffffffffu, peers, j);

@@ -5,7 +5,9 @@
 // route grouping and a second weight-fetch latency cost more than the work.
 // Every CTA (one per SM, 16 consumer warps + 1 TMA producer warp):
 //   1. waits for the previous grid, groups the routes by expert, takes an even
-//      share of the (expert, i) gate/up pairs and H/#CTAs output rows;
+//      share of the (expert, i) gate/up pairs and H/#CTAs output rows (up to
+//      32 routes the producer warp does this alone and starts streaming while
+//      the consumers quantize x);
 //   2. the producer streams that CTA's gate/up rows and then its down rows of
 //      every routed expert through one ring of TMA stages, so the down rows
 //      are prefetched while gate_up computes;
@@ -148,7 +150,8 @@ __global__ void __launch_bounds__(kLsThreads, 1) k_layer_small(const __grid_cons
   uint8_t* ring = smem;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)NS * SB);
   uint64_t* empty = full + NS;
-  uint8_t* xact = reinterpret_cast<uint8_t*>(empty + NS);
+  uint64_t* grouped = empty + NS;   // small batches: the producer warp's grouping and split are published
+  uint8_t* xact = reinterpret_cast<uint8_t*>(grouped + 1);
   xact += (16 - (reinterpret_cast<uintptr_t>(xact) & 15)) & 15;
   uint8_t* iact = xact + p.gu_act_bytes;
   float* ysm = reinterpret_cast<float*>(iact + p.dn_act_bytes);
@@ -158,23 +161,39 @@ __global__ void __launch_bounds__(kLsThreads, 1) k_layer_small(const __grid_cons
   gbase_smem += (16 - (reinterpret_cast<uintptr_t>(gbase_smem) & 15)) & 15;
   GroupSmem g = carve_group(gbase_smem, p.E, RT);
 
+  // Up to 32 routes the producer warp groups the routes and splits the
+  // pairs itself and starts streaming at once, while the consumers quantize
+  // x; they meet at the `grouped` barrier.  More routes: the whole CTA groups.
+  const bool small = RT <= 32;
   if (tid == 0) {
     for (int s = 0; s < NS; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], kLsWarps);
     }
+    mbar_init(grouped, 1);
     fence_mbar_init();
   }
+  if (small && warp == kLsWarps) {
+    // the lines of ids, weights and x into L2 while the previous grid finishes
+    // (prefetches only: every load of them comes after griddepcontrol.wait)
+    if (lane == 0) prefetch_l2(p.ids);
+    if (lane == 1) prefetch_l2(p.w);
+    for (int i = lane; i < (2 * p.T * p.H + 127) / 128; i += 32) prefetch_l2(reinterpret_cast<const uint8_t*>(p.x) + 128 * i);
+  }
+  __syncthreads();   // the mbarriers are initialised
   pdl_wait();   // x and ids may come from the previous grid
   pdl_launch_dependents();
   // the barrier epoch (written by the previous launch); a relaxed load, so
   // it does not hold up this thread's later work
   const unsigned epoch = (tid == 0) ? ld_relaxed_gpu(p.bar) : 0u;
-  group_routes(p.ids, RT, p.E, p.K, g);
-  const int S = g.misc[0];
-  if (RT <= 32 && tid == 0) {
-    // small batch: every expert has about one route, so split the pairs
-    // evenly (32-bit arithmetic when the products fit)
+  if (!small) group_routes(p.ids, RT, p.E, p.K, g);
+  else if (warp == kLsWarps) group_routes_small_warp(p.ids, RT, p.E, p.K, g, lane);
+  if (small && warp == kLsWarps) {
+    __syncwarp();
+    const int S = g.misc[0];
+    // every expert has about one route, so split the pairs evenly (32-bit
+    // arithmetic when the products fit)
+    if (lane == 0) {
     const unsigned P = (unsigned)S * (unsigned)p.I;
     unsigned lo, hi;
     if (P <= 0xFFFFFFFFu / gridDim.x) {
@@ -191,7 +210,11 @@ __global__ void __launch_bounds__(kLsThreads, 1) k_layer_small(const __grid_cons
     g.misc[6] = 0;
     g.misc[7] = 0;
     if (blockIdx.x == 0 && g.misc[1]) atomicOr(p.err, kErrBadId);
-  } else if (RT > 32 && warp == 0) {
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(grouped);   // after the warp's grouping and the split (release)
+  } else if (!small && warp == 0) {
+    const int S = g.misc[0];
     // Split of the S*I (gate, up) pairs, balanced by cost: a pair costs its
     // row bytes plus one decode-and-dot per route of its expert, so cost =
     // 1 + routes of the slot.
@@ -213,27 +236,29 @@ __global__ void __launch_bounds__(kLsThreads, 1) k_layer_small(const __grid_cons
       if (blockIdx.x == 0 && g.misc[1]) atomicOr(p.err, kErrBadId);
     }
   }
-  __syncthreads();
-  const int ub = g.misc[2], ib = g.misc[3], ue = g.misc[4], ie = g.misc[5];
+  if (!small) __syncthreads();
   const int j0 = (int)((unsigned)p.H * blockIdx.x / gridDim.x);
   const int j1 = (int)((unsigned)p.H * (blockIdx.x + 1) / gridDim.x);
   const int nj = j1 - j0;
   const int sps = p.dn_slots_per_stage, rs = p.dn_rs;
-  const int ngrp = (S + sps - 1) / sps;
-  const int nst_dn = (S > 0 && nj > 0) ? ((nj + rs - 1) / rs) * ngrp : 0;
 
   if (warp == kLsWarps) {
     // TMA producer: this CTA's gate/up stages, then its down stages, through one ring.
     if (lane == 0) {
       const uint64_t pol = l2_policy_evict_first();
+      const int ub = g.misc[2], ib = g.misc[3], ue = g.misc[4], ie = g.misc[5];
       PairCursor pc{ub, ib};
       int buf = 0;
       uint32_t eph = 0;
       bool wrapped = false, ok = true;
-      int k = 0;
+      int k = 0, nst_dn = -1;
       for (;;) {
         int su = 0, si = 0, sn = 0;
         const bool gu = next_gu_stage(pc, ue, ie, p.I, p.ps, su, si, sn);
+        if (!gu && nst_dn < 0) {   // the down stage count, once the gate/up stages are out
+          const int S = g.misc[0];
+          nst_dn = (S > 0 && nj > 0) ? ((nj + rs - 1) / rs) * ((S + sps - 1) / sps) : 0;
+        }
         if (!gu && k >= nst_dn) break;
         if (wrapped) {
           if (!mbar_wait_bounded(&empty[buf], eph, kWaitLimit)) {
@@ -244,7 +269,7 @@ __global__ void __launch_bounds__(kLsThreads, 1) k_layer_small(const __grid_cons
         }
         uint8_t* dst = ring + (size_t)buf * SB;
         if (gu) issue_gu_stage(p, dst, &full[buf], g.slot_e[su], si, sn, pol);
-        else issue_dn_stage(p, dst, &full[buf], g, down_stage(k++, S, nj, rs, sps), j0, pol);
+        else issue_dn_stage(p, dst, &full[buf], g, down_stage(k++, g.misc[0], nj, rs, sps), j0, pol);
         atomicAdd(&g.misc[7], 1);
         if (++buf == NS) {
           buf = 0;
@@ -259,6 +284,26 @@ __global__ void __launch_bounds__(kLsThreads, 1) k_layer_small(const __grid_cons
 
   // ---------------- consumers
   const int cw = warp;
+  const int nbh = p.H / 32, nbi = p.I / 32;
+  int8_t* xq = reinterpret_cast<int8_t*>(xact);
+  float* xd = reinterpret_cast<float*>(xact + (size_t)p.T * p.H);
+  int* xs = reinterpret_cast<int*>(xd + (size_t)p.T * nbh);
+  if (small) {
+    // x first (it needs no grouping), then the producer's grouping and split
+    if constexpr (is_float_w(WG)) {
+      copy_to_smem<kLsConsumers>(xact, p.x, 2 * (size_t)p.T * p.H);
+    } else {
+      ls_quantize<true>(p.x, p.T * nbh, nullptr, nbh, xq, xd, xs, blockIdx.x == 0, p.xq, p.xd, p.xsum, p.xsh);
+    }
+    if (!mbar_wait_bounded(grouped, 0u, kWaitLimit)) {
+      if (tid == 0) atomicOr(p.err, kErrTimeout);
+      return;
+    }
+  }
+  const int S = g.misc[0];
+  const int ub = g.misc[2], ib = g.misc[3], ue = g.misc[4], ie = g.misc[5];
+  const int ngrp = (S + sps - 1) / sps;
+  const int nst_dn = (S > 0 && nj > 0) ? ((nj + rs - 1) / rs) * ngrp : 0;
   // route validity and s_down * w of every route, from the grouping (off the
   // producer's path: the producer is already streaming)
   for (int r = tid; r < RT; r += kLsConsumers) {
@@ -280,14 +325,12 @@ __global__ void __launch_bounds__(kLsThreads, 1) k_layer_small(const __grid_cons
     g.sscale[3 * sl + 0] = __ldg(p.scales + 4 * e + 0);
     g.sscale[3 * sl + 1] = __ldg(p.scales + 4 * e + 1);
   }
-  const int nbh = p.H / 32, nbi = p.I / 32;
-  int8_t* xq = reinterpret_cast<int8_t*>(xact);
-  float* xd = reinterpret_cast<float*>(xact + (size_t)p.T * p.H);
-  int* xs = reinterpret_cast<int*>(xd + (size_t)p.T * nbh);
-  if constexpr (is_float_w(WG)) {
-    copy_to_smem<kLsConsumers>(xact, p.x, 2 * (size_t)p.T * p.H);
-  } else {
-    ls_quantize<true>(p.x, p.T * nbh, nullptr, nbh, xq, xd, xs, blockIdx.x == 0, p.xq, p.xd, p.xsum, p.xsh);
+  if (!small) {
+    if constexpr (is_float_w(WG)) {
+      copy_to_smem<kLsConsumers>(xact, p.x, 2 * (size_t)p.T * p.H);
+    } else {
+      ls_quantize<true>(p.x, p.T * nbh, nullptr, nbh, xq, xd, xs, blockIdx.x == 0, p.xq, p.xd, p.xsum, p.xsh);
+    }
   }
   consumer_sync<kLsConsumers>();
 
@@ -440,7 +483,7 @@ __global__ void __launch_bounds__(kLsThreads, 1) k_layer_small(const __grid_cons
 
 size_t layer_small_smem_bytes(const DecodeParams& p) {
   const int RT = p.T * p.K;
-  return (size_t)p.ls_ns * p.ls_sb + 16 * (size_t)p.ls_ns + 16 + (size_t)p.gu_act_bytes + (size_t)p.dn_act_bytes +
+  return (size_t)p.ls_ns * p.ls_sb + 16 * (size_t)p.ls_ns + 32 + (size_t)p.gu_act_bytes + (size_t)p.dn_act_bytes +
          sizeof(float) * (size_t)RT * (p.dn_rows_max + 1) + (size_t)RT + 16 + group_smem_bytes(p.E, RT);
 }
 

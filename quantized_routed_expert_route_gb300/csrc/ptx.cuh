@@ -76,6 +76,11 @@ __device__ __forceinline__ bool mbar_wait_spin(uint64_t* bar, uint32_t parity, u
   }
 }
 
+// Bring the 128-byte line holding p into L2 (no register result, no ordering).
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
   uint64_t pol;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
