@@ -447,6 +447,51 @@ int moe_cache_acquire(moe_cache* cache, int32_t layer, const void* gate_up, cons
 /* Cumulative hits and misses (distinct experts per request) and bytes copied. */
 int moe_cache_stats(const moe_cache* cache, int64_t* hits, int64_t* misses, int64_t* copied_bytes);
 
+/* Forget which expert every slot holds (LRU order and counters unchanged):
+ * the next request for each expert misses and copies it again.  Host only. */
+int moe_slot_table_invalidate(moe_slot_table* table);
+int moe_cache_invalidate(moe_cache* cache);
+
+/* A byte-denominated bank arena (FreeToken issue #194, Proposed design):
+ * pools carved from one caller-owned device buffer at disjoint offsets.
+ * moe_cache_bytes: the device bytes of a pool of nslots slots (gate_up rows,
+ * then down rows, each region 256-byte aligned with 256 bytes of slack); 0
+ * on bad arguments.  moe_cache_create_at: moe_cache_create on
+ * [base, base + moe_cache_bytes) of caller memory (base 256-byte aligned,
+ * bytes >= moe_cache_bytes; MOE_EINVAL otherwise), zeroed on `stream`; the
+ * memory is not freed by moe_cache_destroy. */
+size_t moe_cache_bytes(const moe_layer_geom* geom, int32_t nslots);
+int moe_cache_create_at(const moe_layer_geom* geom, int32_t nslots, void* base, size_t bytes, void* stream,
+                        moe_cache** out);
+
+/* Full-layer prefill overlay (FreeToken issue #194, Proposed design: prefill
+ * of a whole layer runs on one shared overlay of the arena, and the geometry
+ * pools are invalidated before the overlay is written).  An overlay holds one
+ * layer's complete bank -- all E experts' gate_up rows, then its down rows,
+ * at the layer's exact stride -- at `base`, which may overlap pools of the
+ * same arena; size the arena region for the largest layer that will use it.
+ * moe_overlay_bytes: bytes an overlay of this geometry needs (0 on bad
+ * arguments).  moe_overlay_create: base 256-byte aligned, bytes >=
+ * moe_overlay_bytes (MOE_EINVAL otherwise); allocates only the bank's scale
+ * rows.  moe_overlay_bank: the overlay as a bank for moe_prefill_grouped (or
+ * moe_decode), owned by the overlay. */
+typedef struct moe_overlay moe_overlay;
+size_t moe_overlay_bytes(const moe_layer_geom* geom);
+int moe_overlay_create(const moe_layer_geom* geom, void* base, size_t bytes, void* stream, moe_overlay** out);
+int moe_overlay_destroy(moe_overlay* overlay);
+moe_bank* moe_overlay_bank(moe_overlay* overlay);
+
+/* Write one layer into the overlay: first, on the host, every pool of
+ * pools[0..npools) whose rows share any byte with the overlay is invalidated
+ * (moe_cache_invalidate); then the layer's compact rows (gate_up
+ * [E][2I][row bytes], down [E][H][row bytes], any memory the device can
+ * address; device-addressable sources are copied by one kernel) and its
+ * scale rows (scales [E][4], NULL: ones) are copied in on `stream`.  Run the
+ * prefill on the same stream.  A later fill of an overlapping pool
+ * overwrites the overlay: load it again before the next prefill. */
+int moe_overlay_load(moe_overlay* overlay, moe_cache* const* pools, int32_t npools, const void* gate_up,
+                     const void* down, const float* scales, void* stream);
+
 /* Tensor-core check: D[128, N] = A[128, K] * B[N, K]^T with fp16 A and B
  * (device, row-major), fp32 D (device, row-major), computed with the tcgen05
  * kind::f16 MMA on swizzled shared-memory tiles that the prompt-path GEMMs

@@ -23,8 +23,15 @@ Readings (the pages print no rule):
     and becomes the most recent.  A request may not name more distinct
     experts than the pool has slots.  Keys are (layer, expert).
 
+  * overlay: the full-layer prefill overlay is a byte range of the same
+    arena as the pools (the pages: keep full-layer prefill on a shared
+    overlay; invalidate the geometry pools before it is written).  Writing
+    it invalidates every pool with a byte in that range -- each slot forgets
+    its expert, the LRU order and the counters stay -- and no other pool.
+
 Pins (tests/test_oracle_cache.py): the pages' 988 + 202 split; byte-budget
-invariants; hand-worked LRU sequences.
+invariants; hand-worked LRU sequences, with and without invalidation; the
+overlay's overlap rule on touching and overlapping ranges.
 """
 from __future__ import annotations
 
@@ -88,3 +95,28 @@ class SlotLRU:
             fills.append((s, k[1]))
         out = [self.slot_of[(layer, int(e))] if 0 <= int(e) < E else -1 for e in ids]
         return out, fills
+
+    def invalidate(self):
+        """Every slot forgets its expert; the LRU order and counters stay."""
+        self.key_of = [None] * self.nslots
+        self.slot_of = {}
+
+
+class Arena:
+    """Pools carved from one byte range, and the full-layer prefill overlay."""
+
+    def __init__(self):
+        self.pools = []   # (SlotLRU, [(lo, hi), ...]) in creation order
+
+    def add_pool(self, lru: SlotLRU, ranges):
+        self.pools.append((lru, [(int(a), int(b)) for a, b in ranges]))
+
+    def write_overlay(self, lo: int, hi: int):
+        """Invalidate the pools with a byte in [lo, hi), before the overlay
+        is written; returns their indices in creation order."""
+        hit = []
+        for i, (lru, ranges) in enumerate(self.pools):
+            if any(a < hi and lo < b for a, b in ranges):
+                lru.invalidate()
+                hit.append(i)
+        return hit

@@ -34,7 +34,8 @@ EXPORTS = (
     "moe_decode_kernel_count", "moe_decode_io_bytes", "moe_decode_io_offsets", "moe_decode_host",
     "moe_linear", "moe_cache_plan", "moe_slot_table_create", "moe_slot_table_destroy", "moe_slot_table_acquire",
     "moe_slot_table_stats", "moe_cache_create", "moe_cache_destroy", "moe_cache_bank", "moe_cache_acquire",
-    "moe_cache_stats",
+    "moe_cache_stats", "moe_slot_table_invalidate", "moe_cache_invalidate", "moe_cache_bytes", "moe_cache_create_at",
+    "moe_overlay_bytes", "moe_overlay_create", "moe_overlay_destroy", "moe_overlay_bank", "moe_overlay_load",
 )
 
 
@@ -91,6 +92,15 @@ def _load() -> ctypes.CDLL:
         "moe_cache_bank": (vp, [vp]),
         "moe_cache_acquire": (ctypes.c_int, [vp, i32, vp, vp, vp, i32, vp, i32, vp, vp, vp]),
         "moe_cache_stats": (ctypes.c_int, [vp, vp, vp, vp]),
+        "moe_slot_table_invalidate": (ctypes.c_int, [vp]),
+        "moe_cache_invalidate": (ctypes.c_int, [vp]),
+        "moe_cache_bytes": (sz, [ctypes.POINTER(moe_layer_geom), i32]),
+        "moe_cache_create_at": (ctypes.c_int, [ctypes.POINTER(moe_layer_geom), i32, vp, sz, vp, ctypes.POINTER(vp)]),
+        "moe_overlay_bytes": (sz, [ctypes.POINTER(moe_layer_geom)]),
+        "moe_overlay_create": (ctypes.c_int, [ctypes.POINTER(moe_layer_geom), vp, sz, vp, ctypes.POINTER(vp)]),
+        "moe_overlay_destroy": (ctypes.c_int, [vp]),
+        "moe_overlay_bank": (vp, [vp]),
+        "moe_overlay_load": (ctypes.c_int, [vp, vp, i32, vp, vp, vp, vp]),
         "moe_prefill_workspace_bytes": (sz, [vp, i32, i32]),
         "moe_decode_kernel_count": (ctypes.c_int, [vp, i32]),
         "moe_decode_io_bytes": (sz, [vp, i32]),
@@ -239,6 +249,9 @@ class SlotTable:
         _check(_lib.moe_slot_table_stats(self.h, ctypes.byref(h), ctypes.byref(m)), "moe_slot_table_stats")
         return int(h.value), int(m.value)
 
+    def invalidate(self):
+        _check(_lib.moe_slot_table_invalidate(self.h), "moe_slot_table_invalidate")
+
     def close(self):
         if self.h:
             _lib.moe_slot_table_destroy(self.h)
@@ -253,6 +266,48 @@ def moe_cache_create(geom: moe_layer_geom, nslots: int, stream: int = 0) -> int:
 
 def moe_cache_destroy(cache: int) -> None:
     _check(_lib.moe_cache_destroy(cache), "moe_cache_destroy")
+
+
+def moe_cache_bytes(geom: moe_layer_geom, nslots: int) -> int:
+    return int(_lib.moe_cache_bytes(ctypes.byref(geom), nslots))
+
+
+def moe_cache_create_at(geom: moe_layer_geom, nslots: int, base: int, nbytes: int, stream: int = 0) -> int:
+    """A pool carved from caller device memory [base, base + nbytes)."""
+    out = ctypes.c_void_p()
+    _check(_lib.moe_cache_create_at(ctypes.byref(geom), nslots, base, nbytes, stream or None, ctypes.byref(out)),
+           "moe_cache_create_at")
+    return out.value
+
+
+def moe_cache_invalidate(cache: int) -> None:
+    _check(_lib.moe_cache_invalidate(cache), "moe_cache_invalidate")
+
+
+def moe_overlay_bytes(geom: moe_layer_geom) -> int:
+    return int(_lib.moe_overlay_bytes(ctypes.byref(geom)))
+
+
+def moe_overlay_create(geom: moe_layer_geom, base: int, nbytes: int, stream: int = 0) -> int:
+    out = ctypes.c_void_p()
+    _check(_lib.moe_overlay_create(ctypes.byref(geom), base, nbytes, stream or None, ctypes.byref(out)),
+           "moe_overlay_create")
+    return out.value
+
+
+def moe_overlay_destroy(overlay: int) -> None:
+    _check(_lib.moe_overlay_destroy(overlay), "moe_overlay_destroy")
+
+
+def moe_overlay_bank(overlay: int) -> int:
+    return _lib.moe_overlay_bank(overlay)
+
+
+def moe_overlay_load(overlay: int, pools, gate_up: int, down: int, scales: int | None, stream: int = 0) -> None:
+    """Invalidate the overlapping pools, then copy one layer's rows into the overlay."""
+    arr = (ctypes.c_void_p * max(len(pools), 1))(*pools)
+    _check(_lib.moe_overlay_load(overlay, arr, len(pools), gate_up, down, scales or None, stream or None),
+           "moe_overlay_load")
 
 
 def moe_cache_bank(cache: int) -> int:

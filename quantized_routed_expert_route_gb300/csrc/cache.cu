@@ -49,8 +49,20 @@ struct moe_cache {
   uint8_t* gu;               // [slots][2I][rb_gu] + slack
   uint8_t* dn;               // [slots][H][rb_dn] + slack
   size_t gu_expert, dn_expert;
+  size_t gu_span, dn_span;   // bytes of each region, slack included
+  bool owns_rows;            // false: carved from caller memory (moe_cache_create_at)
   long long h2d_bytes;
   std::vector<int32_t> fill_slots, fill_experts;
+};
+
+// One layer's whole bank at the start of an arena that pools also occupy
+// (the full-layer prefill overlay): gate_up rows, then down rows.
+struct moe_overlay {
+  moe_layer_geom geom;
+  uint8_t* base;
+  size_t bytes;              // moe_overlay_bytes(geom)
+  size_t gu_bytes, dn_bytes; // E * 2I * rb_gu, E * H * rb_dn
+  moe_bank* bank;            // borrows [base, base + bytes)
 };
 
 namespace {
@@ -211,6 +223,12 @@ int moe_slot_table_acquire(moe_slot_table* t, int32_t layer, const int32_t* ids,
   return MOE_OK;
 }
 
+int moe_slot_table_invalidate(moe_slot_table* t) {
+  if (!t) return MOE_EINVAL;
+  for (int s = 0; s < t->nslots; ++s) slot_untag(t, s);
+  return MOE_OK;
+}
+
 int moe_slot_table_stats(const moe_slot_table* t, int64_t* hits, int64_t* misses) {
   if (!t) return MOE_EINVAL;
   if (hits) *hits = t->hits;
@@ -243,40 +261,49 @@ int moe_cache_plan(int64_t budget_bytes, int32_t ngeom, const int64_t* expert_by
   return MOE_OK;
 }
 
-int moe_cache_create(const moe_layer_geom* geom, int32_t nslots, void* stream, moe_cache** out) {
-  if (!geom || !out || nslots < 1 || nslots > MOE_MAX_E) return MOE_EINVAL;
+namespace {
+
+size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
+
+// Bytes of a pool's rows: the gate_up region then the down region, each with
+// 256 bytes of slack (a tensor-map tile of the last slot reads a whole box).
+bool pool_spans(const moe_layer_geom& g, int32_t nslots, size_t& gu_expert, size_t& dn_expert, size_t& gu_span,
+                size_t& dn_span) {
+  const int rb_gu = qre::row_bytes_of(g.gate_up_type, g.H), rb_dn = qre::row_bytes_of(g.down_type, g.I);
+  if (rb_gu == 0 || rb_dn == 0) return false;
+  gu_expert = (size_t)2 * g.I * rb_gu;
+  dn_expert = (size_t)g.H * rb_dn;
+  gu_span = align256(gu_expert * nslots + 256);
+  dn_span = align256(dn_expert * nslots + 256);
+  return true;
+}
+
+// The pool over rows at gu / dn (owned or carved), zeroed on `stream`.
+int cache_make(const moe_layer_geom* geom, int32_t nslots, uint8_t* gu, uint8_t* dn, bool owns, void* stream,
+               moe_cache** out) {
   moe_layer_geom g = *geom;
   g.E = nslots;
-  const int rb_gu = qre::row_bytes_of(g.gate_up_type, g.H), rb_dn = qre::row_bytes_of(g.down_type, g.I);
-  if (rb_gu == 0 || rb_dn == 0) return MOE_EINVAL;
   moe_cache* c = new (std::nothrow) moe_cache;
   if (!c) return MOE_ENOMEM;
   c->geom = g;
-  c->gu_expert = (size_t)2 * g.I * rb_gu;
-  c->dn_expert = (size_t)g.H * rb_dn;
+  pool_spans(g, nslots, c->gu_expert, c->dn_expert, c->gu_span, c->dn_span);
   c->h2d_bytes = 0;
-  c->gu = c->dn = nullptr;
+  c->gu = gu;
+  c->dn = dn;
+  c->owns_rows = owns;
   c->bank = nullptr;
   c->table = nullptr;
   int st = moe_slot_table_create(nslots, &c->table);
   if (st) { delete c; return st; }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const size_t gu_bytes = c->gu_expert * nslots, dn_bytes = c->dn_expert * nslots;
-  if (cudaMalloc(&c->gu, gu_bytes + 256) != cudaSuccess || cudaMalloc(&c->dn, dn_bytes + 256) != cudaSuccess) {
-    cudaGetLastError();
-    cudaFree(c->gu); cudaFree(c->dn);
-    moe_slot_table_destroy(c->table);
-    delete c;
-    return MOE_ENOMEM;
-  }
   // defined contents for slots that were never filled (a decode may only
   // route to filled slots, but the tensor-map tiles of a slot read a whole box)
-  cudaError_t e = cudaMemsetAsync(c->gu, 0, gu_bytes + 256, s);
-  if (e == cudaSuccess) e = cudaMemsetAsync(c->dn, 0, dn_bytes + 256, s);
-  if (e == cudaSuccess) st = moe_bank_create(&g, c->gu, gu_bytes, c->dn, dn_bytes, nullptr, MOE_SRC_DEVICE_BORROW,
-                                             stream, &c->bank);
+  cudaError_t e = cudaMemsetAsync(c->gu, 0, c->gu_span, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(c->dn, 0, c->dn_span, s);
+  if (e == cudaSuccess)
+    st = moe_bank_create(&g, c->gu, c->gu_expert * nslots, c->dn, c->dn_expert * nslots, nullptr,
+                         MOE_SRC_DEVICE_BORROW, stream, &c->bank);
   if (e != cudaSuccess || st != MOE_OK) {
-    cudaFree(c->gu); cudaFree(c->dn);
     moe_slot_table_destroy(c->table);
     delete c;
     return e != cudaSuccess ? qre::report_cuda_error(e, "cache create") : st;
@@ -287,11 +314,54 @@ int moe_cache_create(const moe_layer_geom* geom, int32_t nslots, void* stream, m
   return MOE_OK;
 }
 
+}  // namespace
+
+int moe_cache_create(const moe_layer_geom* geom, int32_t nslots, void* stream, moe_cache** out) {
+  if (!geom || !out || nslots < 1 || nslots > MOE_MAX_E) return MOE_EINVAL;
+  size_t ge, de, gs, ds;
+  if (!pool_spans(*geom, nslots, ge, de, gs, ds)) return MOE_EINVAL;
+  uint8_t *gu = nullptr, *dn = nullptr;
+  if (cudaMalloc(&gu, gs) != cudaSuccess || cudaMalloc(&dn, ds) != cudaSuccess) {
+    cudaGetLastError();
+    cudaFree(gu); cudaFree(dn);
+    return MOE_ENOMEM;
+  }
+  const int st = cache_make(geom, nslots, gu, dn, true, stream, out);
+  if (st) { cudaFree(gu); cudaFree(dn); }
+  return st;
+}
+
+size_t moe_cache_bytes(const moe_layer_geom* geom, int32_t nslots) {
+  if (!geom || nslots < 1 || nslots > MOE_MAX_E) return 0;
+  size_t ge, de, gs, ds;
+  if (!pool_spans(*geom, nslots, ge, de, gs, ds)) return 0;
+  return gs + ds;
+}
+
+int moe_cache_create_at(const moe_layer_geom* geom, int32_t nslots, void* base, size_t bytes, void* stream,
+                        moe_cache** out) {
+  if (!geom || !out || !base || nslots < 1 || nslots > MOE_MAX_E) return MOE_EINVAL;
+  if ((reinterpret_cast<uintptr_t>(base) & 255) != 0) return MOE_EINVAL;
+  const size_t need = moe_cache_bytes(geom, nslots);
+  if (need == 0 || bytes < need) return MOE_EINVAL;
+  size_t ge, de, gs, ds;
+  pool_spans(*geom, nslots, ge, de, gs, ds);
+  uint8_t* gu = static_cast<uint8_t*>(base);
+  return cache_make(geom, nslots, gu, gu + gs, false, stream, out);
+}
+
+int moe_cache_invalidate(moe_cache* c) {
+  if (!c) return MOE_EINVAL;
+  return moe_slot_table_invalidate(c->table);
+}
+
 int moe_cache_destroy(moe_cache* c) {
   if (!c) return MOE_OK;
   moe_bank_destroy(c->bank);   // synchronizes the device
-  cudaFree(c->gu);
-  cudaFree(c->dn);
+  if (c->owns_rows) {
+    cudaFree(c->gu);
+    cudaFree(c->dn);
+  }
   moe_slot_table_destroy(c->table);
   delete c;
   return MOE_OK;
@@ -355,4 +425,82 @@ int moe_cache_stats(const moe_cache* c, int64_t* hits, int64_t* misses, int64_t*
   moe_slot_table_stats(c->table, hits, misses);
   if (copied_bytes) *copied_bytes = c->h2d_bytes;
   return MOE_OK;
+}
+
+// ------------------------------------------------------------------ full-layer prefill overlay
+
+size_t moe_overlay_bytes(const moe_layer_geom* geom) {
+  if (!geom || geom->E < 1 || geom->E > MOE_MAX_E) return 0;
+  const int rb_gu = qre::row_bytes_of(geom->gate_up_type, geom->H), rb_dn = qre::row_bytes_of(geom->down_type, geom->I);
+  if (rb_gu == 0 || rb_dn == 0) return 0;
+  return align256((size_t)geom->E * 2 * geom->I * rb_gu + 256) + align256((size_t)geom->E * geom->H * rb_dn + 256);
+}
+
+int moe_overlay_create(const moe_layer_geom* geom, void* base, size_t bytes, void* stream, moe_overlay** out) {
+  if (!geom || !base || !out) return MOE_EINVAL;
+  if ((reinterpret_cast<uintptr_t>(base) & 255) != 0) return MOE_EINVAL;
+  const size_t need = moe_overlay_bytes(geom);
+  if (need == 0 || bytes < need) return MOE_EINVAL;
+  moe_overlay* ov = new (std::nothrow) moe_overlay;
+  if (!ov) return MOE_ENOMEM;
+  ov->geom = *geom;
+  ov->base = static_cast<uint8_t*>(base);
+  ov->bytes = need;
+  ov->gu_bytes = (size_t)geom->E * 2 * geom->I * qre::row_bytes_of(geom->gate_up_type, geom->H);
+  ov->dn_bytes = (size_t)geom->E * geom->H * qre::row_bytes_of(geom->down_type, geom->I);
+  ov->bank = nullptr;
+  const int st = moe_bank_create(geom, ov->base, ov->gu_bytes, ov->base + align256(ov->gu_bytes + 256), ov->dn_bytes,
+                                 nullptr, MOE_SRC_DEVICE_BORROW, stream, &ov->bank);
+  if (st) {
+    delete ov;
+    return st;
+  }
+  *out = ov;
+  return MOE_OK;
+}
+
+int moe_overlay_destroy(moe_overlay* ov) {
+  if (!ov) return MOE_OK;
+  moe_bank_destroy(ov->bank);
+  delete ov;
+  return MOE_OK;
+}
+
+moe_bank* moe_overlay_bank(moe_overlay* ov) { return ov ? ov->bank : nullptr; }
+
+int moe_overlay_load(moe_overlay* ov, moe_cache* const* pools, int32_t npools, const void* gate_up, const void* down,
+                     const float* scales, void* stream) {
+  if (!ov || !gate_up || !down || npools < 0 || (npools > 0 && !pools)) return MOE_EINVAL;
+  // every pool whose rows share bytes with the overlay loses its tags before
+  // anything is copied (the pages' order: invalidate, then write the overlay)
+  const uintptr_t o0 = reinterpret_cast<uintptr_t>(ov->base), o1 = o0 + ov->bytes;
+  for (int i = 0; i < npools; ++i) {
+    moe_cache* c = pools[i];
+    if (!c) return MOE_EINVAL;
+    const uintptr_t g0 = reinterpret_cast<uintptr_t>(c->gu), g1 = g0 + c->gu_span;
+    const uintptr_t d0 = reinterpret_cast<uintptr_t>(c->dn), d1 = d0 + c->dn_span;
+    if ((g0 < o1 && o0 < g1) || (d0 < o1 && o0 < d1)) moe_slot_table_invalidate(c->table);
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* gdst = ov->base;
+  uint8_t* ddst = ov->base + align256(ov->gu_bytes + 256);
+  const uint8_t* gview = device_view(gate_up);
+  const uint8_t* dview = device_view(down);
+  cudaError_t e;
+  if (gview && dview) {
+    FillParams fp;
+    fp.njobs = 0;
+    fp.chunk0[0] = 0;
+    add_fill(fp, gview, gdst, ov->gu_bytes);
+    add_fill(fp, dview, ddst, ov->dn_bytes);
+    e = launch_fill(fp, s);
+  } else {
+    e = cudaMemcpyAsync(gdst, gate_up, ov->gu_bytes, cudaMemcpyDefault, s);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(ddst, down, ov->dn_bytes, cudaMemcpyDefault, s);
+  }
+  float* sdev = qre::bank_scales(ov->bank);
+  for (int ex = 0; e == cudaSuccess && ex < (scales ? 1 : ov->geom.E); ++ex)
+    e = scales ? cudaMemcpyAsync(sdev, scales, 16 * (size_t)ov->geom.E, cudaMemcpyDefault, s)
+               : cudaMemcpyAsync(sdev + 4 * ex, kOnes, 16, cudaMemcpyHostToDevice, s);
+  return e == cudaSuccess ? MOE_OK : qre::report_cuda_error(e, "overlay load");
 }

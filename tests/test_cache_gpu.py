@@ -17,6 +17,7 @@ if not torch.cuda.is_available():
 from oracle import cache as OC  # noqa: E402
 from oracle import formats as F  # noqa: E402
 from quantized_routed_expert_route_gb300 import capi  # noqa: E402
+from synth import banks as S  # noqa: E402
 from tests import cases  # noqa: E402
 from tests import tolerance as tol  # noqa: E402
 
@@ -81,3 +82,98 @@ def test_cache_decode_equals_resident_decode_and_follows_the_lru(pinned):
     rb_gu, rb_dn = F.row_bytes(wt, H), F.row_bytes(wt, I)
     assert copied == misses * (2 * I * rb_gu + H * rb_dn + 16)
     capi.moe_cache_destroy(cache)
+
+
+def test_prefill_overlay_invalidates_the_pools_it_overwrites():
+    """One arena: an NVFP4 pool (4 slots) at its start, inside the region of
+    the full-layer prefill overlay, and a Q8_0 pool (2 slots) after it.
+    Decoding through the NVFP4 pool equals resident decoding; loading the
+    layer into the overlay invalidates that pool (it overwrote its slots) but
+    not the Q8_0 pool; prefill on the overlay bank equals prefill on the
+    resident bank bit for bit (fixed-order W4A4); the same decode request
+    through the NVFP4 pool then misses every expert again and still equals
+    resident decoding, while the Q8_0 pool's request hits."""
+    H, I, E, K, T = 256, 256, 8, 2, 2
+    nv = capi.MOE_NVFP4
+    stream = torch.cuda.current_stream().cuda_stream
+    case = cases.make_prefill_case(H, I, E, K, 64, seed=910)
+    gu_host = case.gu_dev.cpu().pin_memory()
+    dn_host = case.dn_dev.cpu().pin_memory()
+    sb_dev = torch.from_numpy(case.sb).to(DEV)
+    sb_host = torch.from_numpy(case.sb.copy()).pin_memory()
+    geom = capi.moe_layer_geom(H, I, E, K, nv, nv)
+    resident = capi.moe_bank_create(geom, case.gu_dev.data_ptr(), case.gu_dev.numel(), case.dn_dev.data_ptr(),
+                                    case.dn_dev.numel(), sb_dev.data_ptr(), capi.MOE_SRC_DEVICE_BORROW, stream)
+    q8 = cases.make_case(H, I, E, K, F.TYPE_Q8_0, F.TYPE_Q8_0, T, seed=911)
+    q8_gu, q8_dn = q8.gu_dev.cpu().pin_memory(), q8.dn_dev.cpu().pin_memory()
+    # the arena: [overlay region, with the NVFP4 pool at its start][the Q8_0 pool]
+    ov_bytes = capi.moe_overlay_bytes(geom)
+    pa_bytes = capi.moe_cache_bytes(geom, 4)
+    g8 = capi.moe_layer_geom(H, I, E, K, capi.MOE_Q8_0, capi.MOE_Q8_0)
+    pb_bytes = capi.moe_cache_bytes(g8, 2)
+    assert pa_bytes < ov_bytes
+    arena = torch.empty(ov_bytes + pb_bytes, dtype=torch.uint8, device=DEV)
+    base = arena.data_ptr()
+    assert base % 256 == 0
+    pool_a = capi.moe_cache_create_at(geom, 4, base, pa_bytes, stream)
+    pool_b = capi.moe_cache_create_at(g8, 2, base + ov_bytes, pb_bytes, stream)
+    overlay = capi.moe_overlay_create(geom, base, ov_bytes, stream)
+    bank_a = capi.moe_cache_bank(pool_a)
+    wsb = max(capi.moe_workspace_bytes(bank_a, T), capi.moe_workspace_bytes(resident, T))
+    ws = torch.empty(wsb, dtype=torch.uint8, device=DEV)
+    capi.moe_workspace_init(ws.data_ptr(), wsb, stream)
+    x = torch.from_numpy(S.hidden_bf16(912, T, H).view(np.int16)).to(DEV)
+    ids_np = np.array([[1, 5], [5, 6]], dtype=np.int32)
+    w = torch.tensor([[0.6, 0.4], [0.3, 0.7]], dtype=torch.float32, device=DEV)
+
+    def decode(bank, ids):
+        out = torch.empty((T, H), dtype=torch.int16, device=DEV)
+        capi.moe_decode(bank, x.data_ptr(), T, ids.data_ptr(), w.data_ptr(), out.data_ptr(), ws.data_ptr(), wsb,
+                        stream)
+        torch.cuda.synchronize()
+        assert capi.moe_get_error(ws.data_ptr(), wsb, stream) == 0
+        return out.cpu().numpy().view(np.uint16)
+
+    want = decode(resident, torch.from_numpy(ids_np).to(DEV))
+
+    def through_pool():
+        slots, nfill = capi.moe_cache_acquire(pool_a, 0, gu_host.data_ptr(), dn_host.data_ptr(), sb_host.data_ptr(),
+                                              E, [int(v) for v in ids_np.reshape(-1)], stream)
+        got = decode(bank_a, torch.tensor(slots, dtype=torch.int32, device=DEV).reshape(T, K))
+        return got, nfill
+
+    got, nfill = through_pool()
+    assert nfill == 3 and np.array_equal(got, want)
+    got, nfill = through_pool()
+    assert nfill == 0 and np.array_equal(got, want)          # all hits
+    _, nb = capi.moe_cache_acquire(pool_b, 0, q8_gu.data_ptr(), q8_dn.data_ptr(), None, E, [2, 3], stream)
+    assert nb == 2
+    # the overlay: invalidates pool_a (it lies inside), not pool_b, then copies the layer in
+    capi.moe_overlay_load(overlay, [pool_a, pool_b], gu_host.data_ptr(), dn_host.data_ptr(), sb_host.data_ptr(),
+                          stream)
+    Tp = case.x.shape[0]
+    xp = torch.from_numpy(case.x.view(np.int16)).to(DEV)
+    idp, wp = torch.from_numpy(case.ids).to(DEV), torch.from_numpy(case.w).to(DEV)
+    mode = capi.MOE_PREFILL_W4A4_FIXED
+
+    def prefill(bank):
+        pw = capi.moe_prefill_workspace_bytes(bank, Tp, mode)
+        pws = torch.empty(pw, dtype=torch.uint8, device=DEV)
+        out = torch.empty((Tp, H), dtype=torch.int16, device=DEV)
+        capi.moe_prefill_grouped(bank, xp.data_ptr(), Tp, idp.data_ptr(), wp.data_ptr(), mode, out.data_ptr(),
+                                 pws.data_ptr(), pw, stream)
+        torch.cuda.synchronize()
+        assert capi.moe_get_error(pws.data_ptr(), pw, stream) == 0
+        return out.cpu().numpy().view(np.uint16)
+
+    assert np.array_equal(prefill(capi.moe_overlay_bank(overlay)), prefill(resident))
+    # pool_a's slots were overwritten and forgotten: every expert is copied again
+    got, nfill = through_pool()
+    assert nfill == 3 and np.array_equal(got, want)
+    _, nb = capi.moe_cache_acquire(pool_b, 0, q8_gu.data_ptr(), q8_dn.data_ptr(), None, E, [2, 3], stream)
+    assert nb == 0
+    torch.cuda.synchronize()
+    capi.moe_overlay_destroy(overlay)
+    capi.moe_cache_destroy(pool_a)
+    capi.moe_cache_destroy(pool_b)
+    capi.moe_bank_destroy(resident)

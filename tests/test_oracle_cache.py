@@ -46,3 +46,33 @@ def test_lru_request_hits_are_never_evicted_by_its_misses():
     assert out == [1, 0] and fills == [(1, 4)]
     with pytest.raises(ValueError):
         c.acquire(0, [1, 2, 3, 4], 8)
+
+
+def test_lru_after_invalidation_keeps_the_order():
+    """Hand-worked: 3 slots; [5, 6] fills slots 0 and 1 (order 2, 0, 1);
+    after invalidation expert 5 misses and takes slot 2, the least recent --
+    not slot 0, where it was, nor a reset order's slot 0."""
+    lru = OC.SlotLRU(3)
+    s, f = lru.acquire(0, [5, 6], 8)
+    assert s == [0, 1] and f == [(0, 5), (1, 6)]
+    lru.invalidate()
+    s, f = lru.acquire(0, [5], 8)
+    assert s == [2] and f == [(2, 5)]
+    s, f = lru.acquire(0, [6, 5], 8)   # 5 hits; 6 misses and takes slot 0 (order was 0, 1, 2)
+    assert s == [0, 2] and f == [(0, 6)]
+    assert (lru.hits, lru.misses) == (1, 4)
+
+
+def test_overlay_invalidates_exactly_the_overlapping_pools():
+    a, b, c = OC.SlotLRU(2), OC.SlotLRU(2), OC.SlotLRU(2)
+    arena = OC.Arena()
+    arena.add_pool(a, [(0, 100), (100, 150)])
+    arena.add_pool(b, [(150, 300)])
+    arena.add_pool(c, [(300, 400)])
+    for lru in (a, b, c):
+        lru.acquire(0, [1], 4)
+    assert arena.write_overlay(0, 150) == [0]      # ends where b starts: b keeps its tags
+    assert arena.write_overlay(299, 300) == [1]    # one byte of b
+    assert a.acquire(0, [1], 4)[1] == [(1, 1)]     # a forgot expert 1 (slot 1 was least recent)
+    assert b.acquire(0, [1], 4)[1] == [(1, 1)]
+    assert c.acquire(0, [1], 4)[1] == []           # c was never overlapped
