@@ -34,8 +34,9 @@
 //                 in route order, no atomics.
 //
 // W4A4 on a bank with the grouped TMA maps runs on the block-scaled FP4
-// tensor cores instead (no fp16 operands): k_pf_quant also writes x's NVFP4
-// rows in sorted order and zeroes the fp32 token sums; k_pf4_gemm<0> (P3) and
+// tensor cores instead (no fp16 operands): k_pf4_quant (a warp per token) also
+// writes x's NVFP4 rows in sorted order and zeroes the fp32 token sums;
+// k_pf4_gemm<0> (P3) and
 // k_pf4_gemm<1> (P4) are tcgen05 kind::mxf4nvf4 GEMMs, the second adding each
 // route's scaled row into its token's sum by bulk reductions at L2 (P6 in
 // completion order); k_pf4_finish rounds the sums to bf16.  The fixed-order
@@ -415,6 +416,50 @@ __device__ __forceinline__ void q8_1_quant32_f16(const float (&v)[32], uint32_t 
   }
 }
 
+// W4A4 on the FP4 tensor cores: one warp per token.  Lane l quantizes the
+// 16-value blocks l, l + 32, ... of the token (the rule of nvfp4_quant16),
+// writes them to the token's row and to the sorted row of each of its valid
+// routes (consecutive lanes: consecutive 8-byte code groups and scale bytes),
+// and zeroes the token's fp32 sums when the route sum reduces into them.
+__global__ void __launch_bounds__(256) k_pf4_quant(const __grid_constant__ PfParams p) {
+  const int lane = threadIdx.x & 31;
+  const int t = (int)((blockIdx.x * (unsigned)blockDim.x + threadIdx.x) >> 5);
+  if (t >= p.T) return;
+  const int nb = p.H / 16;
+  const size_t rbx = (size_t)p.H / 2 + p.H / 16;
+  const int myrow = lane < p.K ? __ldg(p.inv + (size_t)t * p.K + lane) : -1;
+  for (int b0 = 0; b0 < nb; b0 += 32) {   // warp-uniform: the shuffles below need every lane
+    const int b = b0 + lane;
+    const bool on = b < nb;
+    uint32_t sbyte = 0u, c0 = 0u, c1 = 0u;
+    if (on) {
+      const uint4* src = reinterpret_cast<const uint4*>(p.x + (size_t)t * p.H + 16 * b);
+      float v[16];
+      float f[8];
+      bf16x8_to_f32(__ldg(src), f);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] = f[i];
+      bf16x8_to_f32(__ldg(src + 1), f);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[8 + i] = f[i];
+      uint32_t h[8];
+      nvfp4_quant16(v, sbyte, c0, c1, h);
+      *reinterpret_cast<uint2*>(p.xq + (size_t)t * rbx + 8 * b) = make_uint2(c0, c1);
+      p.xq[(size_t)t * rbx + p.H / 2 + b] = (uint8_t)sbyte;
+    }
+    for (int k = 0; k < p.K; ++k) {
+      const int row = __shfl_sync(0xffffffffu, myrow, k);
+      if (row < 0 || !on) continue;
+      *reinterpret_cast<uint2*>(p.xs + (size_t)row * rbx + 8 * b) = make_uint2(c0, c1);
+      p.xs[(size_t)row * rbx + p.H / 2 + b] = (uint8_t)sbyte;
+    }
+  }
+  if (p.ysum) {
+    float4* ys = reinterpret_cast<float4*>(p.ysum + (size_t)t * p.H);
+    for (int i = lane; i < p.H / 4; i += 32) ys[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+}
+
 // One thread per 16 (W4A4) or 32 (W4A8, FP16) values of x.
 __global__ void k_pf_quant(const __grid_constant__ PfParams p) {
   const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
@@ -455,22 +500,6 @@ __global__ void k_pf_quant(const __grid_constant__ PfParams p) {
     const size_t rbx = (size_t)p.H / 2 + p.H / 16;
     *reinterpret_cast<uint2*>(p.xq + (size_t)t * rbx + 8 * b) = make_uint2(c0, c1);
     p.xq[(size_t)t * rbx + p.H / 2 + b] = (uint8_t)sbyte;
-    if (p.xs) {
-      // the FP4 tensor-core GEMMs: this token's row at every sorted row of
-      // its valid routes, and (completion-order route sum) its fp32 token
-      // sums zeroed for the down GEMM
-      for (int k = 0; k < p.K; ++k) {
-        const int row = __ldg(p.inv + (size_t)t * p.K + k);
-        if (row < 0) continue;
-        *reinterpret_cast<uint2*>(p.xs + (size_t)row * rbx + 8 * b) = make_uint2(c0, c1);
-        p.xs[(size_t)row * rbx + p.H / 2 + b] = (uint8_t)sbyte;
-      }
-      if (p.ysum) {
-        float4* ys = reinterpret_cast<float4*>(p.ysum + (size_t)t * p.H + 16 * b);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) ys[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-    }
     if (p.x16) {   // the fp16 operand of the kind::f16 GEMMs (not used on the FP4 tensor cores)
       uint4* dst = reinterpret_cast<uint4*>(p.x16 + (size_t)t * p.H + 16 * b);
       dst[0] = make_uint4(h[0], h[1], h[2], h[3]);
@@ -1220,7 +1249,10 @@ cudaError_t launch_prefill(const PfParams& p, cudaStream_t stream, const Pf4Para
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   k_pf_scatter<<<nsb, kSortThreads, ss, stream>>>(p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  {
+  if (fp4) {
+    k_pf4_quant<<<(unsigned)((p.T + 7) / 8), 256, 0, stream>>>(p);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  } else {
     const long long n = (long long)p.T * (p.mode == PF_W4A4 ? p.H / 16 : p.H / 32);
     k_pf_quant<<<(unsigned)((n + 255) / 256), 256, 0, stream>>>(p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
