@@ -159,7 +159,7 @@ WsLayout ws_layout(const moe_layer_geom& g, int T) {
   const size_t RT = (size_t)T * g.top_k;
   size_t o = 0;
   L.err = o; o = align_up(o + 4, A);
-  L.bar = o; o = align_up(o + 128 * (1 + (size_t)kMaxGridCtas), A);   // arrival count + one line per CTA
+  L.bar = o; o = align_up(o + 128 * 3, A);   // the fused kernel's barrier: epoch, then two arrival counts
   L.xq = o; o = align_up(o + (size_t)T * g.H, A);
   L.xd = o; o = align_up(o + 4 * (size_t)T * (g.H / 32), A);
   L.xsum = o; o = align_up(o + 4 * (size_t)T * (g.H / 32), A);

@@ -55,7 +55,7 @@ struct DecodeParams {
   int use_ls;              // 1: one k_layer_small launch replaces k_gate_up + k_down
   int g_ls;                // its grid (one CTA per SM)
   int ls_ns, ls_sb;        // ring depth and bytes per ring slot
-  unsigned* bar;           // grid-barrier words in the workspace (count, then one line per CTA)
+  unsigned* bar;           // grid-barrier words in the workspace (epoch, then two arrival counts, 128 B apart)
 };
 
 // The prompt path (prefill.cu): routes sorted by expert, then two grouped

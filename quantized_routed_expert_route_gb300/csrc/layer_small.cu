@@ -15,7 +15,8 @@
 //      gate and up row with it, apply s_gate / s_up and SiLU-GLU in fp32 and
 //      write the fp32 intermediate (FreeToken PR #732, "Design"; Strata PR
 //      #292, "Summary/Pipeline");
-//   4. a grid barrier (bounded spin) makes every CTA's intermediate visible;
+//   4. a grid barrier (one arrival count per launch, release adds and
+//      acquire polls, bounded) makes every CTA's intermediate visible;
 //   5. each CTA requantizes the whole intermediate to q8_1 in shared memory
 //      (prep_inter), dots its down rows with every route, and sums the routes
 //      of a token in route order with w * s_down, writing bf16 with no atomics
@@ -41,38 +42,35 @@ __device__ __forceinline__ void st_relaxed_gpu(unsigned* p, unsigned v) {
 }
 
 // Barrier over all CTAs of the grid.  bar[0] is an epoch that only changes
-// between launches; CTA c owns the word bar[32 * (1 + c)] (its own 128-byte
-// line).  Arriving, a CTA fences (publishing its earlier writes) and stores
-// epoch + 1 into its word; one warp then reads every CTA's word in rounds of
-// independent relaxed loads until all hold epoch + 1, and fences (acquire).
-// After the barrier CTA 0 advances the epoch for the next launch (every CTA
-// read it before publishing its own word, so before CTA 0 could pass).  The
-// wait is bounded: on timeout the error word is flagged and the CTA goes on
-// (its results are then invalid, but nothing hangs).
+// between launches; the launch of epoch n counts its arrivals in the word
+// bar[32 * (1 + n % 2)] (its own 128-byte line), which the previous launch
+// left at zero.  Arriving, thread 0 of a CTA adds 1 with release semantics
+// (publishing the CTA's earlier writes, ordered before it by the consumer
+// barrier) and polls the count with acquire loads until every CTA has
+// arrived.  After the barrier CTA 0 zeroes the other count (the next
+// launch's) and advances the epoch (every CTA read it before arriving, so
+// before CTA 0 could pass).  The wait is bounded: on timeout the error word
+// is flagged and the CTA goes on (its results are then invalid, but nothing
+// hangs; the launch after next starts from a zeroed count again).
 __device__ void ls_grid_barrier(unsigned* bar, unsigned epoch, uint32_t* err) {
   consumer_sync<kLsConsumers>();
-  if (threadIdx.x < 32) {
-    const unsigned lane = threadIdx.x;
-    const unsigned target = __shfl_sync(0xffffffffu, epoch + 1u, 0);   // thread 0 read the epoch
-    if (lane == 0) {
-      asm volatile("fence.acq_rel.gpu;" ::: "memory");
-      st_relaxed_gpu(bar + 32 * (1 + blockIdx.x), target);
-    }
-    // each round reads every CTA's word once (independent relaxed loads,
-    // one L2 round trip), then an acquire fence once all hold the target
+  if (threadIdx.x == 0) {
+    unsigned* cnt = bar + 32 * (1 + (epoch & 1u));
+    asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(cnt) : "memory");
     unsigned spins = 0;
     for (;;) {
-      bool mine = true;
-      for (unsigned c = lane; c < gridDim.x; c += 32) mine &= (ld_relaxed_gpu(bar + 32 * (1 + c)) == target);
-      if (__all_sync(0xffffffffu, mine)) break;
+      unsigned v;
+      asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(cnt) : "memory");
+      if (v >= gridDim.x) break;
       if (++spins > kGridSpinLimit) {
-        if (lane == 0) atomicOr(err, kErrTimeout);
+        atomicOr(err, kErrTimeout);
         break;
       }
     }
-    asm volatile("fence.acq_rel.gpu;" ::: "memory");
-    __syncwarp();
-    if (lane == 0 && blockIdx.x == 0) st_relaxed_gpu(bar, target);
+    if (blockIdx.x == 0) {
+      st_relaxed_gpu(bar + 32 * (1 + ((epoch + 1u) & 1u)), 0u);
+      st_relaxed_gpu(bar, epoch + 1u);
+    }
   }
   consumer_sync<kLsConsumers>();
 }
