@@ -327,7 +327,7 @@ TRAFFIC = {"files": ["quantized_routed_expert_route_gb300/csrc/layer_small.cu",
                      "quantized_routed_expert_route_gb300/csrc/decode_common.cuh",
                      "quantized_routed_expert_route_gb300/csrc/formats.cuh",
                      "quantized_routed_expert_route_gb300/csrc/ptx.cuh"],
-           "sha1": "f05564b4d6c0abcdf6e94cd329709ca92932fc31", "bytes": 21380096}
+           "sha1": "bce5fd23093e4c72389f886d6252dc40d9012df8", "bytes": 21358848}
 
 
 def traffic_bytes():
