@@ -327,7 +327,7 @@ TRAFFIC = {"files": ["quantized_routed_expert_route_gb300/csrc/layer_small.cu",
                      "quantized_routed_expert_route_gb300/csrc/decode_common.cuh",
                      "quantized_routed_expert_route_gb300/csrc/formats.cuh",
                      "quantized_routed_expert_route_gb300/csrc/ptx.cuh"],
-           "sha1": "bce5fd23093e4c72389f886d6252dc40d9012df8", "bytes": 21358848}
+           "sha1": "11b76df2617f2cae93ff9bc5b6c94c141316d35a", "bytes": 21360384}
 
 
 def traffic_bytes():

@@ -534,7 +534,7 @@ static cudaError_t dispatch_ls(const DecodeParams& p, cudaStream_t stream, bool 
         if (fits) *fits = false;
         return cudaSuccess;
       }
-      return launch_ls_t<W_NVFP4, W_NVFP4, 8>(p, stream, probe_only, fits);
+      return launch_ls_t<W_NVFP4, W_NVFP4, 4>(p, stream, probe_only, fits);
     case W_Q4_K: return launch_ls_t<W_Q4_K, W_Q4_K, 4>(p, stream, probe_only, fits);
     case W_Q8_0: return launch_ls_t<W_Q8_0, W_Q8_0, 8>(p, stream, probe_only, fits);
     case W_Q6_K: return launch_ls_t<W_Q6_K, W_Q6_K, 4>(p, stream, probe_only, fits);
