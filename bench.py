@@ -327,7 +327,7 @@ TRAFFIC = {"files": ["quantized_routed_expert_route_gb300/csrc/layer_small.cu",
                      "quantized_routed_expert_route_gb300/csrc/decode_common.cuh",
                      "quantized_routed_expert_route_gb300/csrc/formats.cuh",
                      "quantized_routed_expert_route_gb300/csrc/ptx.cuh"],
-           "sha1": "11b76df2617f2cae93ff9bc5b6c94c141316d35a", "bytes": 21360384}
+           "sha1": "95c2cc75a694dd2d6f465e355757b79704150548", "bytes": 21355264}
 
 
 def traffic_bytes():

@@ -109,7 +109,7 @@ __device__ void ls_quantize(const void* src, int nblk, const uint8_t* rvalid, in
     }
 #pragma unroll
     for (int h = 0; h < kR; ++h) {
-      if (b0 + h * kQuads >= nblk) break;   // the same in every lane
+      if (b0 + h * kQuads + 8 * (int)(threadIdx.x >> 5) >= nblk) break;   // none of this warp's quads has a block
       uint32_t w0, w1;
       float dd;
       int sum;
