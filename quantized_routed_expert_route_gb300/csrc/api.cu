@@ -923,7 +923,6 @@ static int prefill_impl(const moe_bank* b, const void* x, int32_t T, const int32
     q.export_i16 = export_i16 ? 1 : 0;
     q.scales = b->scales; q.ids = ids; q.w = w;
     q.err = p.err; q.off = p.off; q.perm = p.perm;
-    q.xq = p.xq;
     q.xs = base + L.xs;
     q.in4 = base + L.in4;
     q.i16 = p.i16;

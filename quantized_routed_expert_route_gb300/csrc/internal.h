@@ -110,7 +110,6 @@ struct Pf4Params {
   uint32_t* err;
   const int* off;                 // [E+1]
   const int* perm;                // [RT]
-  const uint8_t* xq;              // NVFP4 x by token [T][H/2 + H/16]
   uint8_t* xs;                    // NVFP4 x by sorted row [RT][H/2 + H/16]
   uint8_t* in4;                   // NVFP4 intermediate by sorted row [RT][I/2 + I/16]
   uint16_t* i16;                  // fp16 [RT][I] (export_i16 only)
