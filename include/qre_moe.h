@@ -508,7 +508,8 @@ int moe_debug_tc_gemm(const void* A, const void* B, int32_t K, int32_t N, float*
  * W4A4 on FP4 MMA).  A: device, 128 rows of K/2 bytes of E2M1 codes (value
  * 2i in the low nibble of byte i); B: N rows likewise; sA, sB: 128 / N rows
  * of K/16 UE4M3 bytes; D: device fp32 [128][N].  K a positive multiple of
- * 256, N a multiple of 16 in [16, 128], A, B, sA, sB 16-byte aligned.
+ * 256, N a multiple of 16 in [16, 256] (above 128 the scales of B take eight
+ * tensor-memory columns a MMA), A, B, sA, sB 16-byte aligned.
  * *dev_err (device int32, caller-zeroed) gets bit 0 if a bounded wait for
  * the MMA ran out. */
 int moe_debug_fp4_gemm(const void* A, const void* scale_A, const void* B, const void* scale_B, int32_t K,

@@ -1018,7 +1018,7 @@ int moe_debug_wait_timeout(int32_t mode, int32_t limit, uint32_t* dev_err, void*
 int moe_debug_fp4_gemm(const void* A, const void* scale_A, const void* B, const void* scale_B, int32_t K,
                        int32_t N, float* D, int32_t* dev_err, void* stream) {
   if (!A || !scale_A || !B || !scale_B || !D || !dev_err) return MOE_EINVAL;
-  if (K < 256 || K % 256 != 0 || N < 16 || N > 128 || N % 16 != 0) return MOE_EINVAL;
+  if (K < 256 || K % 256 != 0 || N < 16 || N > 256 || N % 16 != 0) return MOE_EINVAL;
   if (!aligned(A, 16) || !aligned(B, 16) || !aligned(scale_A, 16) || !aligned(scale_B, 16) || !aligned(D, 4) ||
       !aligned(dev_err, 4))
     return MOE_EINVAL;

@@ -133,12 +133,13 @@ cudaError_t launch_tc_gemm_check(const uint16_t* A, const uint16_t* B, int K, in
 // with A [128][K/2] and B [N][K/2] packed E2M1 codes (value 2i in the low
 // nibble of byte i) and sA [128][K/16], sB [N][K/16] UE4M3 scales, on the
 // tcgen05 kind::mxf4nvf4 MMA: each 256-value K chunk's codes go to 128-byte
-// swizzled tiles; for each of its four MMAs (64 values) the scales of the
+// swizzled tiles; for each of its four MMAs (64 values) the scales of each
 // 128 rows go to a 512-byte atom (line r: the four scales of rows r, r+32,
-// r+64, r+96) that tcgen05.cp copies to four tensor-memory columns.  N <= 128,
-// a multiple of 16; rows of B (and their scales) beyond N read as zero.
-// Global loads check their alignment (a misaligned one is skipped and flags
-// bit 1 of *err).
+// r+64, r+96) that tcgen05.cp copies to four tensor-memory columns; for
+// N > 128 the scales of B rows 128..255 take the next four columns (eight a
+// MMA).  N <= 256, a multiple of 16; rows of B (and their scales) beyond N
+// read as zero.  Global loads check their alignment (a misaligned one is
+// skipped and flags bit 1 of *err).
 __global__ void __launch_bounds__(128, 1) k_fp4_gemm_check(const uint8_t* A, const uint8_t* sA, const uint8_t* B,
                                                            const uint8_t* sB, int K, int N, float* D, int* err) {
   extern __shared__ uint8_t smem_raw[];
@@ -146,12 +147,12 @@ __global__ void __launch_bounds__(128, 1) k_fp4_gemm_check(const uint8_t* A, con
   __shared__ uint32_t tmem_base;
   uint8_t* base = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   uint8_t* sa = base;                 // 128 rows x 128 bytes, swizzled
-  uint8_t* sb = base + 16384;         // 128 rows x 128 bytes, swizzled
-  uint8_t* ssa = base + 32768;        // four 512-byte scale atoms (one per MMA)
-  uint8_t* ssb = base + 32768 + 2048;
+  uint8_t* sb = base + 16384;         // 256 rows x 128 bytes, swizzled
+  uint8_t* ssa = base + 49152;        // four 512-byte scale atoms (one per MMA)
+  uint8_t* ssb = base + 49152 + 2048; // eight: B rows 0..127, then 128..255
   const int tid = threadIdx.x, warp = tid >> 5;
   if (warp == 0) {
-    tc::tmem_alloc(&tmem_base, 256);
+    tc::tmem_alloc(&tmem_base, 512);
     tc::tmem_relinquish();
   }
   if (tid == 0) {
@@ -162,24 +163,28 @@ __global__ void __launch_bounds__(128, 1) k_fp4_gemm_check(const uint8_t* A, con
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = tmem_base;
-  const uint32_t t_sfa = tmem + 128, t_sfb = tmem + 144;   // 4 MMAs x 4 columns each
+  const int nbh = N > 128 ? 2 : 1;                          // 128-row halves of B
+  const uint32_t t_sfa = tmem + 256, t_sfb = tmem + 272;    // 4 MMAs x 4 (A) and 4 x 4 * nbh (B) columns
   const uint32_t idesc = tc::idesc_mxf4nvf4(128, (uint32_t)N);
   const size_t rb = (size_t)K / 2, sb_row = (size_t)K / 16;
   uint32_t phase = 0;
   bool ok = true, misaligned = false;
   for (int k0 = 0; k0 < K; k0 += 256) {
-    for (int i = tid; i < 128 * 8; i += 128) {
+    for (int i = tid; i < 256 * 8; i += 128) {
       const int r = i >> 3, c = i & 7;
-      const uint8_t* pa = A + (size_t)r * rb + k0 / 2 + 16 * c;
+      if (r < 128) {
+        const uint8_t* pa = A + (size_t)r * rb + k0 / 2 + 16 * c;
+        uint4 va = make_uint4(0, 0, 0, 0);
+        if ((reinterpret_cast<uintptr_t>(pa) & 15) == 0) va = *reinterpret_cast<const uint4*>(pa);
+        else misaligned = true;
+        *reinterpret_cast<uint4*>(sa + tc::sw128_chunk(r, c)) = va;
+      }
       const uint8_t* pb = B + (size_t)r * rb + k0 / 2 + 16 * c;
-      uint4 va = make_uint4(0, 0, 0, 0), vb = make_uint4(0, 0, 0, 0);
-      if ((reinterpret_cast<uintptr_t>(pa) & 15) == 0) va = *reinterpret_cast<const uint4*>(pa);
-      else misaligned = true;
+      uint4 vb = make_uint4(0, 0, 0, 0);
       if (r < N) {
         if ((reinterpret_cast<uintptr_t>(pb) & 15) == 0) vb = *reinterpret_cast<const uint4*>(pb);
         else misaligned = true;
       }
-      *reinterpret_cast<uint4*>(sa + tc::sw128_chunk(r, c)) = va;
       *reinterpret_cast<uint4*>(sb + tc::sw128_chunk(r, c)) = vb;
     }
     // scale atoms: atom kk, line r (32), word c (4): rows r + 32 c, blocks 4 kk .. 4 kk + 3
@@ -187,16 +192,20 @@ __global__ void __launch_bounds__(128, 1) k_fp4_gemm_check(const uint8_t* A, con
       const int kk = i >> 7, r = (i >> 2) & 31, c = i & 3;
       const int row = r + 32 * c;
       const uint8_t* qa = sA + (size_t)row * sb_row + k0 / 16 + 4 * kk;
-      const uint8_t* qb = sB + (size_t)row * sb_row + k0 / 16 + 4 * kk;
-      uint32_t wa = 0, wb = 0;
+      uint32_t wa = 0;
       if ((reinterpret_cast<uintptr_t>(qa) & 3) == 0) wa = *reinterpret_cast<const uint32_t*>(qa);
       else misaligned = true;
-      if (row < N) {
-        if ((reinterpret_cast<uintptr_t>(qb) & 3) == 0) wb = *reinterpret_cast<const uint32_t*>(qb);
-        else misaligned = true;
-      }
       *reinterpret_cast<uint32_t*>(ssa + 512 * kk + 16 * r + 4 * c) = wa;
-      *reinterpret_cast<uint32_t*>(ssb + 512 * kk + 16 * r + 4 * c) = wb;
+      for (int hb = 0; hb < 2; ++hb) {
+        const int brow = 128 * hb + row;
+        const uint8_t* qb = sB + (size_t)brow * sb_row + k0 / 16 + 4 * kk;
+        uint32_t wb = 0;
+        if (brow < N) {
+          if ((reinterpret_cast<uintptr_t>(qb) & 3) == 0) wb = *reinterpret_cast<const uint32_t*>(qb);
+          else misaligned = true;
+        }
+        *reinterpret_cast<uint32_t*>(ssb + 2048 * hb + 512 * kk + 16 * r + 4 * c) = wb;
+      }
     }
     fence_proxy_async_smem();
     __syncthreads();
@@ -204,11 +213,13 @@ __global__ void __launch_bounds__(128, 1) k_fp4_gemm_check(const uint8_t* A, con
       tc::fence_after_sync();
       for (int kk = 0; kk < 4; ++kk) {
         tc::tmem_cp_32x128b_x4(t_sfa + 4 * kk, tc::desc_plain(smem_addr(ssa + 512 * kk), 128));
-        tc::tmem_cp_32x128b_x4(t_sfb + 4 * kk, tc::desc_plain(smem_addr(ssb + 512 * kk), 128));
+        for (int hb = 0; hb < nbh; ++hb)
+          tc::tmem_cp_32x128b_x4(t_sfb + 4 * nbh * kk + 4 * hb,
+                                 tc::desc_plain(smem_addr(ssb + 2048 * hb + 512 * kk), 128));
       }
       for (int kk = 0; kk < 4; ++kk)
         tc::mma_mxf4nvf4(tmem, tc::desc_sw128(smem_addr(sa) + 32 * kk), tc::desc_sw128(smem_addr(sb) + 32 * kk),
-                         idesc, t_sfa + 4 * kk, t_sfb + 4 * kk, (k0 > 0 || kk > 0) ? 1u : 0u);
+                         idesc, t_sfa + 4 * kk, t_sfb + 4 * nbh * kk, (k0 > 0 || kk > 0) ? 1u : 0u);
       tc::mma_commit(&bar);
     }
     if (!mbar_wait_bounded(&bar, phase, kWaitLimit)) ok = false;
@@ -228,12 +239,12 @@ __global__ void __launch_bounds__(128, 1) k_fp4_gemm_check(const uint8_t* A, con
   if (misaligned) atomicOr(err, 2);
   tc::fence_before_sync();
   __syncthreads();
-  if (warp == 0) tc::tmem_dealloc(tmem, 256);
+  if (warp == 0) tc::tmem_dealloc(tmem, 512);
 }
 
 cudaError_t launch_fp4_gemm_check(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const uint8_t* sB, int K,
                                   int N, float* D, int* err, cudaStream_t stream) {
-  const size_t smem = 1024 + 32768 + 4096;
+  const size_t smem = 1024 + 49152 + 2048 + 4096;
   cudaError_t e = cudaFuncSetAttribute(k_fp4_gemm_check, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   k_fp4_gemm_check<<<1, 128, smem, stream>>>(A, sA, B, sB, K, N, D, err);

@@ -48,7 +48,8 @@ def _nvfp4_dequant(codes, scales, rows, K):
 
 
 @pytest.mark.parametrize("K,N,case", [(256, 128, "random"), (2048, 128, "random"), (512, 64, "random"),
-                                      (256, 128, "row_scales"), (256, 128, "k_scales")])
+                                      (256, 128, "row_scales"), (256, 128, "k_scales"), (512, 256, "random"),
+                                      (256, 256, "row_scales"), (512, 256, "k_scales")])
 def test_fp4_block_scaled_gemm_matches_f64(K, N, case):
     """The tcgen05 kind::mxf4nvf4 MMA with per-16 UE4M3 scales in tensor
     memory, against float64 of the decoded operands: every product of two
