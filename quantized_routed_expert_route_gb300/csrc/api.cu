@@ -916,7 +916,7 @@ static int prefill_impl(const moe_bank* b, const void* x, int32_t T, const int32
     p.ysum = fixed ? nullptr : p.y;
     Pf4Params q;
     std::memset(&q, 0, sizeof(q));
-    // gate_up weight boxes of 64 rows (the tile's gate and up halves), down of 128
+    // weight boxes of 128 rows (a gate_up tile loads its 128 gate and 128 up rows)
     q.map_wdn = b->map_dn; q.map_wdns = b->map_dns;
     q.H = g.H; q.I = g.I; q.E = g.E; q.K = g.top_k; q.T = T; q.RT = T * g.top_k;
     q.glu = g.glu;
@@ -930,8 +930,8 @@ static int prefill_impl(const moe_bank* b, const void* x, int32_t T, const int32
     q.out = p.out;
     q.fixed = fixed ? 1 : 0;
     const uint64_t rbx = (uint64_t)(g.H / 2 + g.H / 16), rbi = (uint64_t)(g.I / 2 + g.I / 16);
-    if (!map_byte_rows(&q.map_wgu, b->gu, (uint64_t)g.E * 2 * g.I, rbx, 128, 64, true) ||
-        !map_byte_rows(&q.map_wgus, b->gu, (uint64_t)g.E * 2 * g.I, rbx, 16, 64) ||
+    if (!map_byte_rows(&q.map_wgu, b->gu, (uint64_t)g.E * 2 * g.I, rbx, 128, 128, true) ||
+        !map_byte_rows(&q.map_wgus, b->gu, (uint64_t)g.E * 2 * g.I, rbx, 16, 128) ||
         !map_byte_rows(&q.map_xs, q.xs, (uint64_t)q.RT, rbx, 128, 128, true) ||
         !map_byte_rows(&q.map_xss, q.xs, (uint64_t)q.RT, rbx, 16, 128) ||
         !map_byte_rows(&q.map_in, q.in4, (uint64_t)q.RT, rbi, 128, 128, true) ||

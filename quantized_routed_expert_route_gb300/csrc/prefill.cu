@@ -1247,6 +1247,258 @@ size_t pf4_smem(int E) {
          8 * ((size_t)E + 1);
 }
 
+// W4A4 gate_up with one N = 256 MMA per 64 values: the tile is (expert, 128
+// sorted rows, 128 intermediate columns) -- the 128 gate rows then the 128
+// up rows of the column block form one 256-row B operand, so each
+// block-scaled MMA (M = 128, N = 256, K = 64) does twice the work of the
+// 128-wide tile for about the same issue cost.  Tensor memory then holds a
+// single 256-column accumulator (gate in columns 0..127, up in 128..255)
+// beside the stages' scales (A: four columns an MMA; B: eight, rows 128..255
+// in the second four), so the next tile's MMAs wait until the epilogue has
+// read the accumulator; sixteen epilogue warps (four per lane quarter, two
+// 16-value blocks each) keep that short.  Roles otherwise as k_pf4_gemm:
+// warp 0 TMA, warp 1 MMA, warps 2..5 scales (one per lane quarter), warps
+// 6..21 epilogue.
+namespace {
+constexpr int kGuThreads = 704;
+constexpr int kGuStages = 4;
+constexpr int kGuA = kF4Op;                       // 18,432: x rows' codes then scales
+constexpr int kGuBCode = 2 * kF4Code;             // 32,768: 256 weight rows x 128 bytes
+constexpr int kGuStage = kGuA + kGuBCode + 2 * kF4Scale;   // 55,296
+constexpr int kGuSf = 48;                         // scale columns of a stage
+static_assert(kGuStage % 1024 == 0 && kGuA % 1024 == 0, "1024-byte aligned code tiles");
+static_assert(256 + kGuStages * kGuSf <= 512, "tensor memory: the accumulator and the stages' scales");
+
+// One lane quarter of a stage's B scales (256 rows: gate rows then up rows,
+// 16 bytes each) into its 32 columns: column 8 kk + 4 h + c of lane l holds
+// the four scales of row 128 h + (l % 32) + 32 c for MMA kk.
+__device__ __forceinline__ void gu_scales_b_to_tmem(const uint8_t* tile, uint32_t taddr, int lane) {
+  uint32_t lo[16], hi[16];
+#pragma unroll
+  for (int h = 0; h < 2; ++h)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const uint4 v = *reinterpret_cast<const uint4*>(tile + 2048 * h + 16 * (lane + 32 * c));
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        const int col = 8 * kk + 4 * h + c;
+        if (col < 16) lo[col] = w[kk];
+        else hi[col - 16] = w[kk];
+      }
+    }
+  tc::tmem_st16(taddr, lo);
+  tc::tmem_st16(taddr + 16, hi);
+}
+}  // namespace
+
+__global__ void __launch_bounds__(kGuThreads, 1) k_pf4_gate_up(const __grid_constant__ Pf4Params p) {
+  constexpr int NS = kGuStages;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint64_t full[NS], ready[NS], empty[NS], acc_full, acc_empty, drain;
+  __shared__ uint32_t tmem_base;
+  __shared__ int abort_flag;
+  uint8_t* base = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+  uint8_t* stages = base;
+  int* soff = reinterpret_cast<int*>(base + NS * kGuStage);   // [E+1] first sorted row of each expert
+  int* rbpre = soff + (p.E + 1);                               // [E+1] row blocks before each expert
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int E = p.E;
+  const int nchunk = p.H / 256;
+  const int ncb = p.I / 128;
+  volatile int* abort = &abort_flag;
+
+  if (warp == 0) {
+    tc::tmem_alloc(&tmem_base, 512);
+    tc::tmem_relinquish();
+  }
+  if (tid == 0) {
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&ready[i], 4);
+      mbar_init(&empty[i], 1);
+    }
+    mbar_init(&acc_full, 1);
+    mbar_init(&acc_empty, 512);
+    mbar_init(&drain, 1);
+    fence_mbar_init();
+    abort_flag = 0;
+  }
+  for (int e = tid; e <= E; e += kGuThreads) soff[e] = p.off[e];
+  __syncthreads();
+  if (warp == 0) {
+    const int per = (E + 31) / 32, e0 = lane * per;
+    int local = 0;
+    for (int i = 0; i < per; ++i)
+      if (e0 + i < E) local += (soff[e0 + i + 1] - soff[e0 + i] + 127) / 128;
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    int run = incl - local;
+    for (int i = 0; i < per; ++i)
+      if (e0 + i < E) {
+        rbpre[e0 + i] = run;
+        run += (soff[e0 + i + 1] - soff[e0 + i] + 127) / 128;
+      }
+    if (lane == 31) rbpre[E] = incl;
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = tmem_base;
+
+  if (warp == 0) {
+    // ---- TMA producer
+    if (lane == 0) {
+      const uint64_t pw = l2_policy_evict_normal(), pa = l2_policy_evict_last();
+      int ecur = 0, q = 0;
+      F4Tile tl;
+      for (int t = blockIdx.x; !*abort && f4_tile(t, ncb, rbpre, soff, E, ecur, tl); t += gridDim.x) {
+        const int yb = tl.e * 2 * p.I + 128 * tl.cb;   // the tile's first gate row (its up rows are I further)
+        bool ok = true;
+        for (int kc = 0; kc < nchunk; ++kc, ++q) {
+          const int s = q % NS;
+          if (q >= NS && !f4_wait(&empty[s], (uint32_t)(((q / NS) & 1) ^ 1), abort, true)) {
+            ok = false;
+            break;
+          }
+          uint8_t* st = stages + (size_t)s * kGuStage;
+          uint8_t* sb = st + kGuA;
+          mbar_arrive_expect_tx(&full[s], (uint32_t)kGuStage);
+          f4_tma(st, &p.map_xs, 128 * kc, tl.row0, &full[s], pa);
+          f4_tma(st + kF4Code, &p.map_xss, p.H / 2 + 16 * kc, tl.row0, &full[s], pa);
+          f4_tma(sb, &p.map_wgu, 128 * kc, yb, &full[s], pw);
+          f4_tma(sb + kF4Code, &p.map_wgu, 128 * kc, yb + p.I, &full[s], pw);
+          f4_tma(sb + kGuBCode, &p.map_wgus, p.H / 2 + 16 * kc, yb, &full[s], pw);
+          f4_tma(sb + kGuBCode + kF4Scale, &p.map_wgus, p.H / 2 + 16 * kc, yb + p.I, &full[s], pw);
+        }
+        if (!ok) break;
+      }
+      for (int qn = q - NS < 0 ? 0 : q - NS; qn < q; ++qn)
+        mbar_wait_spin(&full[qn % NS], (uint32_t)((qn / NS) & 1), kSpinLimit);
+    }
+  } else if (warp >= 2 && warp <= 5) {
+    // ---- scales: this warp's lane quarter of both operands' scale columns
+    const uint32_t tq = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + 256u;
+    int ecur = 0, q = 0;
+    F4Tile tl;
+    for (int t = blockIdx.x; !*abort && f4_tile(t, ncb, rbpre, soff, E, ecur, tl); t += gridDim.x) {
+      bool ok = true;
+      for (int kc = 0; kc < nchunk; ++kc, ++q) {
+        const int s = q % NS;
+        if (!f4_wait(&full[s], (uint32_t)((q / NS) & 1), abort)) {
+          ok = false;
+          break;
+        }
+        const uint8_t* st = stages + (size_t)s * kGuStage;
+        f4_scales_to_tmem(st + kF4Code, tq + (uint32_t)(s * kGuSf), lane);
+        gu_scales_b_to_tmem(st + kGuA + kGuBCode, tq + (uint32_t)(s * kGuSf + 16), lane);
+        tc::tmem_st_wait();
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ready[s]);
+      }
+      if (!ok) break;
+    }
+  } else if (warp == 1) {
+    // ---- MMA issue: one 128 x 256 x 64 block-scaled MMA per 64 values
+    const uint32_t idesc = tc::idesc_mxf4nvf4(128, 256);
+    int ecur = 0, q = 0, ntile = 0;
+    F4Tile tl;
+    for (int t = blockIdx.x; !*abort && f4_tile(t, ncb, rbpre, soff, E, ecur, tl); t += gridDim.x, ++ntile) {
+      // the single accumulator: the previous tile's epilogue has read it
+      if (ntile >= 1 && !f4_wait(&acc_empty, (uint32_t)((ntile - 1) & 1), abort)) break;
+      tc::fence_after_sync();
+      bool ok = true;
+      for (int kc = 0; kc < nchunk; ++kc, ++q) {
+        const int s = q % NS;
+        if (!f4_wait(&ready[s], (uint32_t)((q / NS) & 1), abort)) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          mbar_try_wait(&full[s], (uint32_t)((q / NS) & 1));   // acquire: the copies the scale warps saw complete
+          tc::fence_after_sync();
+          const uint32_t st = smem_addr(stages + (size_t)s * kGuStage);
+          const uint32_t sf = tmem + 256 + (uint32_t)(s * kGuSf);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            tc::mma_mxf4nvf4(tmem, tc::desc_sw128(st + 32 * kk), tc::desc_sw128(st + kGuA + 32 * kk), idesc,
+                             sf + 4 * kk, sf + 16 + 8 * kk, (kc > 0 || kk > 0) ? 1u : 0u);
+          tc::mma_commit(&empty[s]);
+        }
+        __syncwarp();
+      }
+      if (!ok) break;
+      if (lane == 0) tc::mma_commit(&acc_full);
+      __syncwarp();
+    }
+    if (lane == 0) {
+      tc::mma_commit(&drain);
+      mbar_wait_spin(&drain, 0u, kSpinLimit);
+    }
+  } else if (warp >= 6) {
+    // ---- epilogue: warp w reads lanes 32 * (w % 4) .. + 31 and 16-value blocks 2 hh, 2 hh + 1
+    const int qd = warp & 3, hh = (warp - 6) >> 2;
+    const int rbi = p.I / 2 + p.I / 16;
+    int ecur = 0, ntile = 0;
+    F4Tile tl;
+    for (int t = blockIdx.x; !*abort && f4_tile(t, ncb, rbpre, soff, E, ecur, tl); t += gridDim.x, ++ntile) {
+      if (!f4_wait(&acc_full, (uint32_t)(ntile & 1), abort, true)) break;
+      tc::fence_after_sync();
+      const uint32_t tq = tmem + ((uint32_t)(32 * qd) << 16);
+      const int m = 32 * qd + lane;
+      const bool valid = m < tl.rows;
+      const int row = tl.row0 + m;
+      const float sg = __ldg(p.scales + 4 * tl.e + 0), su = __ldg(p.scales + 4 * tl.e + 1);
+      uint32_t g16[2][16], u16[2][16];
+#pragma unroll
+      for (int j2 = 0; j2 < 2; ++j2) {
+        const int blk = 2 * hh + j2;
+        tc::tmem_ld16(tq + 16 * blk, g16[j2]);
+        tc::tmem_ld16(tq + 128 + 16 * blk, u16[j2]);
+      }
+      tc::tmem_ld_wait();
+      tc::fence_before_sync();
+      mbar_arrive(&acc_empty);   // the accumulator is free for the next tile's MMAs
+      uint32_t codes[4], sc = 0u;
+#pragma unroll
+      for (int j2 = 0; j2 < 2; ++j2) {
+        const int blk = 2 * hh + j2;
+        float a[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          a[j] = glu_act(__uint_as_float(g16[j2][j]) * sg, __uint_as_float(u16[j2][j]) * su, p.glu);
+        uint32_t sbyte, c0, c1, hw[8];
+        nvfp4_quant16(a, sbyte, c0, c1, hw);
+        codes[2 * j2] = c0;
+        codes[2 * j2 + 1] = c1;
+        sc |= sbyte << (8 * j2);
+        if (p.export_i16 && valid) {
+          uint4* dst = reinterpret_cast<uint4*>(p.i16 + (size_t)row * p.I + 128 * tl.cb + 16 * blk);
+          dst[0] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+          dst[1] = make_uint4(hw[4], hw[5], hw[6], hw[7]);
+        }
+      }
+      if (valid) {
+        uint8_t* dst = p.in4 + (size_t)row * rbi;
+        *reinterpret_cast<uint4*>(dst + 64 * tl.cb + 16 * hh) = make_uint4(codes[0], codes[1], codes[2], codes[3]);
+        *reinterpret_cast<uint16_t*>(dst + p.I / 2 + 8 * tl.cb + 2 * hh) = (uint16_t)sc;
+      }
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  if (tid == 0 && abort_flag) atomicOr(p.err, kErrTimeout);
+  if (warp == 0) tc::tmem_dealloc(tmem, 512);
+}
+
+size_t pf4_gate_up_smem(int E) { return 1024 + (size_t)kGuStages * kGuStage + 8 * ((size_t)E + 1); }
+
 // ------------------------------------------------------------------ launch
 
 cudaError_t launch_prefill(const PfParams& p, cudaStream_t stream, const Pf4Params* fp4) {
@@ -1297,12 +1549,12 @@ cudaError_t launch_prefill(const PfParams& p, cudaStream_t stream, const Pf4Para
 cudaError_t launch_prefill_fp4(const Pf4Params& q, cudaStream_t stream) {
   cudaError_t e;
   const long long nsum = (long long)q.T * (q.H / 4);   // float4s of the fp32 token sums
-  const size_t s0 = pf4_smem<0>(q.E), s1 = pf4_smem<1>(q.E);
-  if ((e = cudaFuncSetAttribute(k_pf4_gemm<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s0)) != cudaSuccess)
+  const size_t s0 = pf4_gate_up_smem(q.E), s1 = pf4_smem<1>(q.E);
+  if ((e = cudaFuncSetAttribute(k_pf4_gate_up, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s0)) != cudaSuccess)
     return e;
   if ((e = cudaFuncSetAttribute(k_pf4_gemm<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s1)) != cudaSuccess)
     return e;
-  k_pf4_gemm<0><<<sm_count(), kF4Threads, s0, stream>>>(q);
+  k_pf4_gate_up<<<sm_count(), kGuThreads, s0, stream>>>(q);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   k_pf4_gemm<1><<<sm_count(), kF4Threads, s1, stream>>>(q);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
