@@ -36,10 +36,10 @@
 // W4A4 on a bank with the grouped TMA maps runs on the block-scaled FP4
 // tensor cores instead (no fp16 operands): k_pf4_quant (a warp per token) also
 // writes x's NVFP4 rows in sorted order and zeroes the fp32 token sums;
-// k_pf4_gemm<0> (P3) and
-// k_pf4_gemm<1> (P4) are tcgen05 kind::mxf4nvf4 GEMMs, the second adding each
-// route's scaled row into its token's sum by bulk reductions at L2 (P6 in
-// completion order); k_pf4_finish rounds the sums to bf16.  The fixed-order
+// k_pf4_gate_up (P3, 128 x 256 MMAs) and k_pf4_down (P4, 128 x 128 MMAs) are
+// tcgen05 kind::mxf4nvf4 GEMMs, the second adding each route's scaled row
+// into its token's sum by bulk reductions at L2 (P6 in completion order);
+// k_pf4_finish rounds the sums to bf16.  The fixed-order
 // mode stores each route's row instead and k_pf4_combine sums k = 0..K-1.
 //
 // Every product in the MMAs is of two exact fp16 values (NVFP4 code * scale,
@@ -839,13 +839,9 @@ constexpr int kF4Code = 16384;     // one operand's codes per stage: 128 rows x 
 constexpr int kF4Scale = 2048;     // its scales: 128 rows x 16 bytes
 constexpr int kF4Op = kF4Code + kF4Scale;
 constexpr int kF4Stage = 2 * kF4Op;     // the activation rows' operand, then the weight rows'
-constexpr int kF4GuCols = 64;           // intermediate columns of one gate_up tile (64 gate + 64 up rows)
 constexpr int kF4EpRow = 528;           // down epilogue: one row's 128 fp32 outputs, padded to spread banks
 
-template <int PHASE>
-struct F4Cfg {
-  static constexpr int NS = PHASE == 0 ? 6 : 4;   // stages; tensor memory: 256 accumulator + NS * 32 scale columns
-};
+constexpr int kF4DownStages = 4;       // down stages; tensor memory: 256 accumulator + 4 * 32 scale columns
 
 // 2-D TMA load of one box at (x, y) with an L2 cache policy (the activation
 // rows and the token sums evict last, the weights normally: a weight tile is
@@ -962,33 +958,25 @@ __global__ void k_pf4_finish(const __grid_constant__ Pf4Params p) {
   reinterpret_cast<uint2*>(p.out)[i] = o;
 }
 
-// Grouped GEMM of the W4A4 prompt path on tcgen05 kind::mxf4nvf4 (MMA
-// M = N = 128, K = 64 per instruction).
-// PHASE 0 (gate_up): tile = (expert, 128 sorted rows, 64 intermediate
-// columns); per 256-value chunk of H one stage holds the rows' NVFP4 x codes
-// and scales and the tile's 64 gate rows followed by its 64 up rows (codes
-// and scales), all by 2-D TMA, so that one MMA covers both projections: the
-// accumulator's columns 0..63 are gate, 64..127 up, and stay in tensor memory
-// over the chunks.  The epilogue applies s_gate, s_up and the GLU in fp32 and
-// requantizes each 16 values to NVFP4 (the prompt path's activation rule),
-// writing the sorted NVFP4 intermediate.
-// PHASE 1 (down): tile = (expert, 128 sorted rows, 128 output rows); the
-// epilogue scales each route's row by s_down * w and adds it into its token's
-// fp32 sum with bulk reductions at L2 (the route sum; see k_pf4_finish), or,
-// with p.fixed, stores it as the route's own fp32 row for k_pf4_combine.
+// Grouped down GEMM of the W4A4 prompt path on tcgen05 kind::mxf4nvf4 (MMA
+// M = N = 128, K = 64 per instruction): tile = (expert, 128 sorted rows, 128
+// output rows), the rows' NVFP4 intermediate and the expert's NVFP4 down rows
+// (codes and scales) by 2-D TMA, one 256-value chunk of I per stage.  The
+// epilogue scales each route's row by s_down * w and adds it into its
+// token's fp32 sum with bulk reductions at L2 (the route sum; see
+// k_pf4_finish), or, with p.fixed, stores it as the route's own fp32 row for
+// k_pf4_combine.
 // Roles: warp 0 issues the TMA copies; warps 2..5 (one per tensor-memory
 // lane quarter) store each stage's scales from its 128 x 16-byte scale tiles
-// into tensor memory; warp 1 issues the MMAs; the epilogue runs on warps
-// 6..13 for gate_up (two per tensor-memory lane quarter, each half of the
-// tile's columns) and on warps 6..9 for down (one per quarter, whole rows, so
-// that each route row is one 512-byte reduction).
+// into tensor memory; warp 1 issues the MMAs; warps 6..9 (one per lane
+// quarter, whole rows, so that each route row is one 512-byte reduction) run
+// the epilogue; warps 10..13 have no role.
 // The accumulators are double-buffered, so a tile's epilogue overlaps the
 // next tile's MMAs.  One CTA per SM walks the tiles (blockIdx.x, +
 // gridDim.x, ...).  Every product of two scaled E2M1 values is exact in
 // fp32 and the MMA accumulates in fp32.
-template <int PHASE>
-__global__ void __launch_bounds__(kF4Threads, 1) k_pf4_gemm(const __grid_constant__ Pf4Params p) {
-  constexpr int NS = F4Cfg<PHASE>::NS;
+__global__ void __launch_bounds__(kF4Threads, 1) k_pf4_down(const __grid_constant__ Pf4Params p) {
+  constexpr int NS = kF4DownStages;
   static_assert(256 + NS * 32 <= 512, "tensor memory: two 128-column accumulators and the stages' scales");
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t full[NS], ready[NS], empty[NS], acc_full[2], acc_empty[2], drain;
@@ -997,13 +985,12 @@ __global__ void __launch_bounds__(kF4Threads, 1) k_pf4_gemm(const __grid_constan
   uint8_t* base = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   uint8_t* stages = base;
   uint8_t* ep = base + NS * kF4Stage;                        // down: the epilogue rows
-  int* soff = reinterpret_cast<int*>(ep + (PHASE == 1 ? 128 * kF4EpRow : 0));   // [E+1] first sorted row of each expert
+  int* soff = reinterpret_cast<int*>(ep + 128 * kF4EpRow);   // [E+1] first sorted row of each expert
   int* rbpre = soff + (p.E + 1);                             // [E+1] row blocks before each expert
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int E = p.E;
-  const int Kd = PHASE == 0 ? p.H : p.I;   // reduction length
-  const int nchunk = Kd / 256;
-  const int ncb = PHASE == 0 ? p.I / kF4GuCols : p.H / 128;
+  const int nchunk = p.I / 256;
+  const int ncb = p.H / 128;
   volatile int* abort = &abort_flag;
 
   if (warp == 0) {
@@ -1018,7 +1005,7 @@ __global__ void __launch_bounds__(kF4Threads, 1) k_pf4_gemm(const __grid_constan
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&acc_full[i], 1);
-      mbar_init(&acc_empty[i], PHASE == 0 ? 256 : 128);   // the epilogue threads that read a buffer
+      mbar_init(&acc_empty[i], 128);   // the epilogue threads that read a buffer
     }
     mbar_init(&drain, 1);
     fence_mbar_init();
@@ -1053,16 +1040,11 @@ __global__ void __launch_bounds__(kF4Threads, 1) k_pf4_gemm(const __grid_constan
   if (warp == 0) {
     // ---- TMA producer
     if (lane == 0) {
-      const CUtensorMap* ma = PHASE == 0 ? &p.map_xs : &p.map_in;
-      const CUtensorMap* mas = PHASE == 0 ? &p.map_xss : &p.map_ins;
-      const CUtensorMap* mb = PHASE == 0 ? &p.map_wgu : &p.map_wdn;
-      const CUtensorMap* mbs = PHASE == 0 ? &p.map_wgus : &p.map_wdns;
       const uint64_t pw = l2_policy_evict_normal(), pa = l2_policy_evict_last();
       int ecur = 0, q = 0;
       F4Tile tl;
       for (int t = blockIdx.x; !*abort && f4_tile(t, ncb, rbpre, soff, E, ecur, tl); t += gridDim.x) {
-        // first weight row of the tile: its gate rows (the up rows are I further), or its down rows
-        const int yb = PHASE == 0 ? tl.e * 2 * p.I + kF4GuCols * tl.cb : tl.e * p.H + 128 * tl.cb;
+        const int yb = tl.e * p.H + 128 * tl.cb;   // the tile's first down row
         bool ok = true;
         for (int kc = 0; kc < nchunk; ++kc, ++q) {
           const int s = q % NS;
@@ -1073,17 +1055,10 @@ __global__ void __launch_bounds__(kF4Threads, 1) k_pf4_gemm(const __grid_constan
           uint8_t* st = stages + (size_t)s * kF4Stage;
           uint8_t* sb = st + kF4Op;
           mbar_arrive_expect_tx(&full[s], (uint32_t)kF4Stage);
-          f4_tma(st, ma, 128 * kc, tl.row0, &full[s], pa);
-          f4_tma(st + kF4Code, mas, Kd / 2 + 16 * kc, tl.row0, &full[s], pa);
-          if (PHASE == 0) {
-            f4_tma(sb, mb, 128 * kc, yb, &full[s], pw);
-            f4_tma(sb + kF4Code / 2, mb, 128 * kc, yb + p.I, &full[s], pw);
-            f4_tma(sb + kF4Code, mbs, Kd / 2 + 16 * kc, yb, &full[s], pw);
-            f4_tma(sb + kF4Code + kF4Scale / 2, mbs, Kd / 2 + 16 * kc, yb + p.I, &full[s], pw);
-          } else {
-            f4_tma(sb, mb, 128 * kc, yb, &full[s], pw);
-            f4_tma(sb + kF4Code, mbs, Kd / 2 + 16 * kc, yb, &full[s], pw);
-          }
+          f4_tma(st, &p.map_in, 128 * kc, tl.row0, &full[s], pa);
+          f4_tma(st + kF4Code, &p.map_ins, p.I / 2 + 16 * kc, tl.row0, &full[s], pa);
+          f4_tma(sb, &p.map_wdn, 128 * kc, yb, &full[s], pw);
+          f4_tma(sb + kF4Code, &p.map_wdns, p.I / 2 + 16 * kc, yb, &full[s], pw);
         }
         if (!ok) break;
       }
@@ -1153,11 +1128,9 @@ __global__ void __launch_bounds__(kF4Threads, 1) k_pf4_gemm(const __grid_constan
       tc::mma_commit(&drain);   // everything this thread issued is complete before the dealloc
       mbar_wait_spin(&drain, 0u, kSpinLimit);
     }
-  } else if (warp >= 6 && (PHASE == 0 || warp < 10)) {
-    // ---- epilogue: warp w reads tensor-memory lanes 32 * (w % 4) .. + 31 (one tile row a
-    // thread) and half hh of the tile's columns
-    const int qd = warp & 3, hh = (warp - 6) >> 2;
-    const int rbi = p.I / 2 + p.I / 16;
+  } else if (warp >= 6 && warp < 10) {
+    // ---- epilogue: warp w reads tensor-memory lanes 32 * (w % 4) .. + 31, one tile row a thread
+    const int qd = warp & 3;
     float* mine = reinterpret_cast<float*>(ep + (size_t)(32 * qd + lane) * kF4EpRow);   // down: this row's 128 outputs
     const uint64_t pkeep = l2_policy_evict_last();   // the token sums stay in L2 for k_pf4_finish
     int ecur = 0, ntile = 0;
@@ -1170,41 +1143,7 @@ __global__ void __launch_bounds__(kF4Threads, 1) k_pf4_gemm(const __grid_constan
       const int m = 32 * qd + lane;
       const bool valid = m < tl.rows;
       const int row = tl.row0 + m;
-      if (PHASE == 0) {
-        const float sg = __ldg(p.scales + 4 * tl.e + 0), su = __ldg(p.scales + 4 * tl.e + 1);
-        uint32_t codes[4], sc = 0u;
-#pragma unroll
-        for (int j2 = 0; j2 < 2; ++j2) {
-          const int blk = 2 * hh + j2;
-          uint32_t g16[16], u16[16];
-          tc::tmem_ld16(tq + 16 * blk, g16);
-          tc::tmem_ld16(tq + kF4GuCols + 16 * blk, u16);
-          tc::tmem_ld_wait();
-          if (j2 == 1) {
-            tc::fence_before_sync();
-            mbar_arrive(&acc_empty[buf]);   // this warp's part of the accumulator is read
-          }
-          float a[16];
-#pragma unroll
-          for (int j = 0; j < 16; ++j) a[j] = glu_act(__uint_as_float(g16[j]) * sg, __uint_as_float(u16[j]) * su, p.glu);
-          uint32_t sbyte, c0, c1, hw[8];
-          nvfp4_quant16(a, sbyte, c0, c1, hw);
-          codes[2 * j2] = c0;
-          codes[2 * j2 + 1] = c1;
-          sc |= sbyte << (8 * j2);
-          if (p.export_i16 && valid) {
-            uint4* dst = reinterpret_cast<uint4*>(p.i16 + (size_t)row * p.I + kF4GuCols * tl.cb + 16 * blk);
-            dst[0] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-            dst[1] = make_uint4(hw[4], hw[5], hw[6], hw[7]);
-          }
-        }
-        if (valid) {
-          uint8_t* dst = p.in4 + (size_t)row * rbi;
-          *reinterpret_cast<uint4*>(dst + (kF4GuCols / 2) * tl.cb + 16 * hh) =
-              make_uint4(codes[0], codes[1], codes[2], codes[3]);
-          *reinterpret_cast<uint16_t*>(dst + p.I / 2 + (kF4GuCols / 16) * tl.cb + 2 * hh) = (uint16_t)sc;
-        }
-      } else {
+      {
         const float sd = __ldg(p.scales + 4 * tl.e + 2);
         const int r = valid ? p.perm[row] : 0;
         const float f = valid ? sd * __ldg(p.w + r) : 0.f;
@@ -1232,7 +1171,7 @@ __global__ void __launch_bounds__(kF4Threads, 1) k_pf4_gemm(const __grid_constan
         }
       }
     }
-    if (PHASE == 1) bulk_wait_done();
+    bulk_wait_done();
   }
   tc::fence_before_sync();
   __syncthreads();
@@ -1241,10 +1180,8 @@ __global__ void __launch_bounds__(kF4Threads, 1) k_pf4_gemm(const __grid_constan
   if (warp == 0) tc::tmem_dealloc(tmem, 512);
 }
 
-template <int PHASE>
-size_t pf4_smem(int E) {
-  return 1024 + (size_t)F4Cfg<PHASE>::NS * kF4Stage + (PHASE == 1 ? 128 * kF4EpRow : 0) +
-         8 * ((size_t)E + 1);
+size_t pf4_down_smem(int E) {
+  return 1024 + (size_t)kF4DownStages * kF4Stage + 128 * kF4EpRow + 8 * ((size_t)E + 1);
 }
 
 // W4A4 gate_up with one N = 256 MMA per 64 values: the tile is (expert, 128
@@ -1549,14 +1486,14 @@ cudaError_t launch_prefill(const PfParams& p, cudaStream_t stream, const Pf4Para
 cudaError_t launch_prefill_fp4(const Pf4Params& q, cudaStream_t stream) {
   cudaError_t e;
   const long long nsum = (long long)q.T * (q.H / 4);   // float4s of the fp32 token sums
-  const size_t s0 = pf4_gate_up_smem(q.E), s1 = pf4_smem<1>(q.E);
+  const size_t s0 = pf4_gate_up_smem(q.E), s1 = pf4_down_smem(q.E);
   if ((e = cudaFuncSetAttribute(k_pf4_gate_up, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s0)) != cudaSuccess)
     return e;
-  if ((e = cudaFuncSetAttribute(k_pf4_gemm<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s1)) != cudaSuccess)
+  if ((e = cudaFuncSetAttribute(k_pf4_down, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s1)) != cudaSuccess)
     return e;
   k_pf4_gate_up<<<sm_count(), kGuThreads, s0, stream>>>(q);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  k_pf4_gemm<1><<<sm_count(), kF4Threads, s1, stream>>>(q);
+  k_pf4_down<<<sm_count(), kF4Threads, s1, stream>>>(q);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (q.fixed) k_pf4_combine<<<(unsigned)((nsum + 255) / 256), 256, 0, stream>>>(q);
   else k_pf4_finish<<<(unsigned)((nsum + 255) / 256), 256, 0, stream>>>(q);
