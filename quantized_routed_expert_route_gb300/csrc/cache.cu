@@ -344,8 +344,8 @@ int moe_cache_create_at(const moe_layer_geom* geom, int32_t nslots, void* base, 
   if ((reinterpret_cast<uintptr_t>(base) & 255) != 0) return MOE_EINVAL;
   const size_t need = moe_cache_bytes(geom, nslots);
   if (need == 0 || bytes < need) return MOE_EINVAL;
-  size_t ge, de, gs, ds;
-  pool_spans(*geom, nslots, ge, de, gs, ds);
+  size_t ge = 0, de = 0, gs = 0, ds = 0;
+  if (!pool_spans(*geom, nslots, ge, de, gs, ds)) return MOE_EINVAL;
   uint8_t* gu = static_cast<uint8_t*>(base);
   return cache_make(geom, nslots, gu, gu + gs, false, stream, out);
 }

@@ -447,7 +447,7 @@ __global__ void __launch_bounds__(kDecodeThreads, MAXNT == 1 ? 2 : 1) k_down(con
       const int e = g.slot_e[u];
       const uint8_t* src = p.dn_bank + ((size_t)e * p.H + j0 + st.js) * rbd;
       const uint8_t* piece = sbuf + (size_t)i * p.dn_piece_bytes + (src - align16_down(src));
-      if (kFused && !is_float_w(WT)) {
+      if constexpr (kFused && !is_float_w(WT)) {
         // one or two tokens: the requantized intermediate is in shared memory
         const int8_t* aqs = reinterpret_cast<const int8_t*>(actm);
         const float* ads = reinterpret_cast<const float*>(actm + (size_t)RT * p.I);
@@ -463,29 +463,28 @@ __global__ void __launch_bounds__(kDecodeThreads, MAXNT == 1 ? 2 : 1) k_down(con
             if (vrow && sl == 0) ysm[(size_t)r * p.dn_rows_max + st.js + row] = v;
           }
         }
-        rot = (rot + nq) & (kConsumerWarps - 1);
-        continue;
-      }
-      for (int q = (cw - rot) & (kConsumerWarps - 1); q < nq; q += kConsumerWarps) {
-        const int row = q * RPI + grp;
-        const bool vrow = row < st.nr;
-        const uint8_t* rowp = piece + (size_t)(vrow ? row : 0) * rbd;
-        for (int c0 = 0; c0 < Tu; c0 += MAXNT) {
-          const int nt = min(MAXNT, Tu - c0);
-          int rt[NT];
+      } else {
+        for (int q = (cw - rot) & (kConsumerWarps - 1); q < nq; q += kConsumerWarps) {
+          const int row = q * RPI + grp;
+          const bool vrow = row < st.nr;
+          const uint8_t* rowp = piece + (size_t)(vrow ? row : 0) * rbd;
+          for (int c0 = 0; c0 < Tu; c0 += MAXNT) {
+            const int nt = min(MAXNT, Tu - c0);
+            int rt[NT];
 #pragma unroll
-          for (int t = 0; t < NT; ++t) rt[t] = (t < nt) ? (int)g.routes[roff + c0 + t] : 0;
-          float res[NT];
-          if (MAXNT == 1 || nt == 1) dn_item<WT, LPR, 1>(rowp, vrow, p.I, sl, act, rt, nt, res);
-          else if (nt == 2) dn_item<WT, LPR, 2>(rowp, vrow, p.I, sl, act, rt, nt, res);
-          else dn_item<WT, LPR, (MAXNT > 1 ? 4 : 1)>(rowp, vrow, p.I, sl, act, rt, nt, res);
-          if (vrow && sl < nt) {
-            float v = res[0];
-            int r = rt[0];
+            for (int t = 0; t < NT; ++t) rt[t] = (t < nt) ? (int)g.routes[roff + c0 + t] : 0;
+            float res[NT];
+            if (MAXNT == 1 || nt == 1) dn_item<WT, LPR, 1>(rowp, vrow, p.I, sl, act, rt, nt, res);
+            else if (nt == 2) dn_item<WT, LPR, 2>(rowp, vrow, p.I, sl, act, rt, nt, res);
+            else dn_item<WT, LPR, (MAXNT > 1 ? 4 : 1)>(rowp, vrow, p.I, sl, act, rt, nt, res);
+            if (vrow && sl < nt) {
+              float v = res[0];
+              int r = rt[0];
 #pragma unroll
-            for (int t = 1; t < NT; ++t)
-              if (sl == t) { v = res[t]; r = rt[t]; }
-            ysm[(size_t)r * p.dn_rows_max + st.js + row] = v;
+              for (int t = 1; t < NT; ++t)
+                if (sl == t) { v = res[t]; r = rt[t]; }
+              ysm[(size_t)r * p.dn_rows_max + st.js + row] = v;
+            }
           }
         }
       }
